@@ -1,0 +1,116 @@
+// Host-side plumbing shared by every entry point: thread-local error text,
+// the device status word, and tensor-map encoding through the driver entry
+// point (so the library loads on machines without a driver).
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+__device__ int32_t g_bi_device_status = 0;
+
+static thread_local char t_last_error[512] = "";
+
+bi_status bi_fail(bi_status code, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_last_error, sizeof t_last_error, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+bi_status bi_cuda_check(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return BI_OK;
+    return bi_fail(BI_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+extern "C" const char *bi_last_error(void) { return t_last_error; }
+
+int32_t *bi_status_ptr() {
+    // One address per device; looked up once per device.
+    static std::mutex mu;
+    static int32_t *ptrs[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_bi_device_status) != cudaSuccess)
+            return nullptr;
+        ptrs[dev] = static_cast<int32_t *>(p);
+    }
+    return ptrs[dev];
+}
+
+extern "C" bi_status bi_device_status(int32_t *h_status, void *stream) {
+    BI_REQUIRE(h_status, "bi_device_status: null output");
+    int32_t *d = bi_status_ptr();
+    if (!d) return bi_fail(BI_ERR_CUDA, "bi_device_status: no status word");
+    cudaStream_t s = bi_stream(stream);
+    int32_t zero = 0;
+    bi_status st = bi_cuda_check(
+        cudaMemcpyAsync(h_status, d, sizeof(int32_t), cudaMemcpyDeviceToHost, s),
+        "read status");
+    if (st != BI_OK) return st;
+    st = bi_cuda_check(cudaStreamSynchronize(s), "sync status");
+    if (st != BI_OK) return st;
+    return bi_cuda_check(
+        cudaMemcpy(d, &zero, sizeof zero, cudaMemcpyHostToDevice),
+        "clear status");
+}
+
+// ------------------------------------------------------------ tensor maps --
+
+typedef CUresult (*encode_tiled_fn)(CUtensorMap *, CUtensorMapDataType,
+                                    cuuint32_t, void *, const cuuint64_t *,
+                                    const cuuint64_t *, const cuuint32_t *,
+                                    const cuuint32_t *, CUtensorMapInterleave,
+                                    CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                    CUtensorMapFloatOOBfill);
+
+static encode_tiled_fn get_encode() {
+    static encode_tiled_fn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p,
+                                             12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<encode_tiled_fn>(p);
+    });
+    return fn;
+}
+
+bi_status bi_make_tmap_2d_bf16(CUtensorMap *map, const void *base,
+                               uint64_t inner, uint64_t outer,
+                               uint64_t row_stride_bytes, uint32_t box_inner,
+                               uint32_t box_outer, bool swizzle128) {
+    encode_tiled_fn enc = get_encode();
+    if (!enc)
+        return bi_fail(BI_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                     const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return bi_fail(BI_ERR_INVALID_ARG,
+                       "cuTensorMapEncodeTiled failed (%d): base %p inner %llu "
+                       "outer %llu stride %llu",
+                       (int)r, base, (unsigned long long)inner,
+                       (unsigned long long)outer,
+                       (unsigned long long)row_stride_bytes);
+    return BI_OK;
+}

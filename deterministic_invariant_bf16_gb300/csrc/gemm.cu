@@ -1,0 +1,465 @@
+// bi_gemm: y = x W^T on the tcgen05 tensor cores, batch-invariant.
+//
+// ybb.press, "LLM 推理确定性工程深度实战", section 2.2: library GEMMs pick tile
+// shape, stage count and split-K from (M, N, K), and split-K with atomicAdd
+// is not even run-to-run deterministic.  Section 4 gives the remedy this
+// kernel follows: one tile shape for every M, a split count fixed per weight
+// shape, a fixed-order second stage, no float atomics.
+//
+// Reduction order of one output y[m][n] (independent of M, of the row's
+// place in its tile, and of which CTA does the work):
+//   - K is cut into S = bi_gemm_splits(N, K) slices of whole 64-column
+//     blocks, slice s covering blocks [s*KB/S, (s+1)*KB/S).
+//   - Inside a slice: one tcgen05.mma chain (M=128, N=128, K=16 per
+//     instruction) in ascending k, accumulating in fp32 in tensor memory,
+//     starting from zero.
+//   - Slices are summed in fp32 in slice order: ((p0 + p1) + p2) + ...
+//
+// Two schedules give the same bits:
+//   split: one CTA per (m-tile, n-tile, slice); slices go to memory as fp32
+//          partials and a consumer (bi_rmsnorm, bi_rope, or the reduce
+//          kernel here) sums them in order.  Fills the GPU at small M.
+//   fused: one CTA per (m-tile, n-tile) runs the slices one after another
+//          into two alternating TMEM accumulators; the epilogue warps add
+//          each finished slice to a register running sum in slice order.
+//          No partial traffic; used when there are enough tiles.
+//
+// CTA layout (192 threads): warp 0 lane 0 issues TMA loads into a ring of
+// shared-memory stages; warp 1 owns the TMEM allocation and lane 0 issues
+// the MMAs; warps 2-5 are the epilogue (warp w reads TMEM lanes
+// 32*(w%4) .. 32*(w%4)+31, i.e. tile rows).  Every wait is bounded.
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace {
+
+constexpr int BM = 128, BN = 128, BK = 64;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr uint32_t IDESC = make_idesc_bf16(BM, BN);
+
+constexpr int STAGES_SPLIT = 3;  // ~97 KB: two CTAs per SM
+constexpr int STAGES_FUSED = 6;  // ~193 KB: one CTA per SM
+
+constexpr size_t smem_bytes(int stages) {
+    return 1024 /* alignment slack */ + (size_t)stages * STAGE_BYTES + 256;
+}
+
+struct GemmArgs {
+    int M, N, K, KB, S;
+    int out_kind;
+    void *out;
+    int32_t *status;
+};
+
+__device__ __forceinline__ void store_f32_32(float *dst, int n, int N,
+                                             const float *v) {
+    if (n + 32 <= N && (N & 3) == 0) {
+        float4 *d4 = reinterpret_cast<float4 *>(dst + n);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2],
+                                v[4 * i + 3]);
+    } else {
+        for (int i = 0; i < 32; ++i)
+            if (n + i < N) dst[n + i] = v[i];
+    }
+}
+
+__device__ __forceinline__ void store_bf16_32(uint16_t *dst, int n, int N,
+                                              const float *v) {
+    if (n + 32 <= N && (N & 7) == 0) {
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst + n);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            d4[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]),
+                               pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                               pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
+                               pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+    } else {
+        for (int i = 0; i < 32; ++i)
+            if (n + i < N) dst[n + i] = f32_to_bf16(v[i]);
+    }
+}
+
+// silu(g) * u = (g / (1 + e^-g)) * u, each operation rounded separately.
+__device__ __forceinline__ float swiglu1(float g, float u) {
+    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
+
+template <bool FUSED, int STAGES>
+__global__ void __launch_bounds__(THREADS, FUSED ? 1 : 2)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                const __grid_constant__ CUtensorMap tmB, GemmArgs p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * A_BYTES;
+    uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
+    uint64_t *empty = full + STAGES;
+    uint64_t *acc_full = empty + STAGES;   // [2]
+    uint64_t *acc_empty = acc_full + 2;    // [2]
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(acc_empty + 2);
+
+    constexpr uint32_t TMEM_COLS = FUSED ? 2 * BN : BN;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
+    const int s_lo = FUSED ? 0 : blockIdx.z;
+    const int s_hi = FUSED ? p.S : blockIdx.z + 1;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 4);
+        }
+        mbar_fence_init();
+    }
+    if (warp == 1) tmem_alloc(tslot, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------------------------------------------- producer --
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        int it = 0;
+        bool ok = true;
+        for (int s = s_lo; s < s_hi && ok; ++s) {
+            const int kb0 = (int)((int64_t)s * p.KB / p.S);
+            const int kb1 = (int)((int64_t)(s + 1) * p.KB / p.S);
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const int st = it % STAGES;
+                const uint32_t round = it / STAGES;
+                if (round > 0 && !mbar_wait(&empty[st], (round - 1) & 1,
+                                            p.status)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&full[st], STAGE_BYTES);
+                tma_load_2d(sA + st * A_BYTES, &tmA, kb * BK, m0, &full[st]);
+                tma_load_2d(sB + st * B_BYTES, &tmB, kb * BK, n0, &full[st]);
+            }
+        }
+        if (!ok) {
+            // Let the copies already issued land before the CTA exits.
+            for (int j = std::max(0, it - STAGES); j < it; ++j)
+                mbar_wait(&full[j % STAGES], (j / STAGES) & 1, p.status);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // --------------------------------------------------------- MMA --
+        int it = 0;
+        bool ok = true;
+        for (int s = s_lo, j = 0; s < s_hi; ++s, ++j) {
+            const int buf = FUSED ? (j & 1) : 0;
+            if (FUSED && j >= 2 &&
+                !mbar_wait(&acc_empty[buf], ((j >> 1) - 1) & 1, p.status))
+                ok = false;
+            tc_fence_after();
+            const uint32_t d_tmem = tmem + buf * BN;
+            const int kb0 = (int)((int64_t)s * p.KB / p.S);
+            const int kb1 = (int)((int64_t)(s + 1) * p.KB / p.S);
+            for (int kb = kb0; kb < kb1 && ok; ++kb, ++it) {
+                const int st = it % STAGES;
+                if (!mbar_wait(&full[st], (it / STAGES) & 1, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a = smem_u32(sA + st * A_BYTES);
+                const uint32_t b = smem_u32(sB + st * B_BYTES);
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k)
+                    tc_mma_bf16(d_tmem, make_sw128_desc(a + 32 * k),
+                                make_sw128_desc(b + 32 * k), IDESC,
+                                (kb > kb0 || k > 0) ? 1u : 0u);
+                tc_commit(&empty[st]);
+            }
+            tc_commit(&acc_full[buf]);
+        }
+    } else if (warp >= 2) {
+        // ---------------------------------------------------- epilogue --
+        const int q = warp & 3;
+        const int row = m0 + q * 32 + lane;
+        const bool live = row < p.M;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        float run[FUSED ? BN : 1];
+        bool ok = true;
+        for (int s = s_lo, j = 0; s < s_hi; ++s, ++j) {
+            const int buf = FUSED ? (j & 1) : 0;
+            if (!mbar_wait(&acc_full[buf], FUSED ? ((j >> 1) & 1) : 0,
+                           p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t base = lane_addr + buf * BN;
+            if (FUSED) {
+#pragma unroll
+                for (int c = 0; c < BN; c += 32) {
+                    float v[32];
+                    tmem_ld_32cols(base + c, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        run[c + i] = (j == 0) ? v[i] : __fadd_rn(run[c + i], v[i]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            } else if (p.out_kind == BI_OUT_SWIGLU) {
+                const int f0 = blockIdx.y * (BN / 2);
+                const int NO = p.N / 2;
+#pragma unroll
+                for (int c = 0; c < BN / 2; c += 32) {
+                    float g[32], u[32];
+                    tmem_ld_32cols(base + c, g);
+                    tmem_ld_32cols(base + BN / 2 + c, u);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) g[i] = swiglu1(g[i], u[i]);
+                    if (live)
+                        store_bf16_32(reinterpret_cast<uint16_t *>(p.out) +
+                                          (size_t)row * NO,
+                                      f0 + c, NO, g);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < BN; c += 32) {
+                    float v[32];
+                    tmem_ld_32cols(base + c, v);
+                    if (!live) continue;
+                    if (p.out_kind == BI_OUT_BF16)
+                        store_bf16_32(reinterpret_cast<uint16_t *>(p.out) +
+                                          (size_t)row * p.N,
+                                      n0 + c, p.N, v);
+                    else  // partial slice s (or the only slice)
+                        store_f32_32(reinterpret_cast<float *>(p.out) +
+                                         ((size_t)s * p.M + row) * p.N,
+                                     n0 + c, p.N, v);
+                }
+            }
+        }
+        if (FUSED && ok && live) {
+            if (p.out_kind == BI_OUT_SWIGLU) {
+                const int f0 = blockIdx.y * (BN / 2);
+                const int NO = p.N / 2;
+#pragma unroll
+                for (int c = 0; c < BN / 2; c += 32) {
+                    float g[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        g[i] = swiglu1(run[c + i], run[BN / 2 + c + i]);
+                    store_bf16_32(reinterpret_cast<uint16_t *>(p.out) +
+                                      (size_t)row * NO,
+                                  f0 + c, NO, g);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < BN; c += 32) {
+                    if (p.out_kind == BI_OUT_BF16)
+                        store_bf16_32(reinterpret_cast<uint16_t *>(p.out) +
+                                          (size_t)row * p.N,
+                                      n0 + c, p.N, run + c);
+                    else
+                        store_f32_32(reinterpret_cast<float *>(p.out) +
+                                         (size_t)row * p.N,
+                                     n0 + c, p.N, run + c);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// Second stage of the split schedule: y = sum_s ws[s] in slice order.
+__global__ void reduce_slices_kernel(const float *__restrict__ ws, int S,
+                                     int64_t MN, int out_kind, void *out) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= MN) return;
+    float v = ws[i];
+    for (int s = 1; s < S; ++s) v = __fadd_rn(v, ws[(int64_t)s * MN + i]);
+    if (out_kind == BI_OUT_BF16)
+        reinterpret_cast<uint16_t *>(out)[i] = f32_to_bf16(v);
+    else
+        reinterpret_cast<float *>(out)[i] = v;
+}
+
+__global__ void pack_gate_up_kernel(const uint4 *__restrict__ wg,
+                                    const uint4 *__restrict__ wu, int F,
+                                    int K8, uint4 *__restrict__ wgu) {
+    // Output row r: block b = r / 128, within-block j = r % 128;
+    // j < 64 -> gate row 64b + j, else up row 64b + j - 64.
+    const int64_t total = (int64_t)2 * F * K8;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / K8, c = i % K8;
+        const int64_t b = r / 128, j = r % 128;
+        const uint4 *src = j < 64 ? wg + (b * 64 + j) * K8
+                                  : wu + (b * 64 + j - 64) * K8;
+        wgu[i] = src[c];
+    }
+}
+
+template <bool FUSED, int STAGES>
+bi_status set_smem_attr() {
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute(gemm_kernel<FUSED, STAGES>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)smem_bytes(STAGES));
+    });
+    return bi_cuda_check(err, "gemm smem attribute");
+}
+
+}  // namespace
+
+extern "C" int bi_gemm_splits(int N, int K) {
+    // A pure function of the weight shape.  Aim for about two CTAs per SM of
+    // a 152-SM GB300 at small M, with at least 4 k-blocks per slice and at
+    // most 8 slices.
+    const int KB = (K + BK - 1) / BK;
+    const int tiles = (N + BN - 1) / BN;
+    int s = 304 / std::max(tiles, 1);
+    s = std::min(s, 8);
+    s = std::min(s, KB / 4);
+    return std::max(s, 1);
+}
+
+extern "C" size_t bi_gemm_workspace_size(int M, int N, int K) {
+    const int S = bi_gemm_splits(N, K);
+    if (S <= 1 || M <= 0 || N <= 0) return 0;
+    return (size_t)S * M * N * sizeof(float);
+}
+
+// Default schedule: fused once there are enough output tiles to fill the
+// GPU without splitting K.  Either schedule gives the same bits.
+bool bi_gemm_default_fused(int M, int N, int K) {
+    const int S = bi_gemm_splits(N, K);
+    const int64_t tiles = (int64_t)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+    return S > 1 && tiles >= 148;
+}
+
+bi_status bi_gemm_sched(const bi_bf16 *x, int M, int K, const bi_bf16 *W,
+                        int N, void *out, int out_kind, void *ws,
+                        size_t ws_bytes, int mode, cudaStream_t stream) {
+    BI_REQUIRE(M >= 0 && N > 0 && K > 0, "bi_gemm: bad shape M=%d N=%d K=%d",
+               M, N, K);
+    BI_REQUIRE(K % 8 == 0, "bi_gemm: K=%d must be a multiple of 8", K);
+    BI_REQUIRE(x && W && out, "bi_gemm: null pointer");
+    BI_REQUIRE(bi_aligned16(x) && bi_aligned16(W) && bi_aligned16(out),
+               "bi_gemm: pointers must be 16-byte aligned");
+    BI_REQUIRE(out_kind >= BI_OUT_PARTIALS && out_kind <= BI_OUT_SWIGLU,
+               "bi_gemm: bad out_kind %d", out_kind);
+    if (M == 0) return BI_OK;
+    const int S = bi_gemm_splits(N, K);
+    const int KB = (K + BK - 1) / BK;
+    const int mt = (M + BM - 1) / BM, nt = (N + BN - 1) / BN;
+    if (out_kind == BI_OUT_SWIGLU) {
+        BI_REQUIRE(N % BN == 0, "bi_gemm: SwiGLU needs N %% 128 == 0 (N=%d)", N);
+        if (S != 1)
+            return bi_fail(BI_ERR_UNSUPPORTED,
+                           "bi_gemm: SwiGLU epilogue needs one K slice");
+    }
+    bool fused;
+    if (mode == 1)
+        fused = false;
+    else if (mode == 2)
+        fused = true;
+    else
+        fused = bi_gemm_default_fused(M, N, K);
+    if (out_kind == BI_OUT_PARTIALS && S > 1) fused = false;
+    if (S == 1) fused = false;
+
+    CUtensorMap ta, tb;
+    bi_status st = bi_make_tmap_2d_bf16(&ta, x, K, M, (uint64_t)K * 2, BK, BM,
+                                        true);
+    if (st != BI_OK) return st;
+    st = bi_make_tmap_2d_bf16(&tb, W, K, N, (uint64_t)K * 2, BK, BN, true);
+    if (st != BI_OK) return st;
+
+    GemmArgs a;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.KB = KB;
+    a.S = S;
+    a.out_kind = out_kind;
+    a.out = out;
+    a.status = bi_status_ptr();
+
+    const bool need_reduce =
+        !fused && S > 1 && out_kind != BI_OUT_PARTIALS;
+    if (need_reduce) {
+        const size_t need = (size_t)S * M * N * sizeof(float);
+        if (!ws || ws_bytes < need)
+            return bi_fail(BI_ERR_WORKSPACE_TOO_SMALL,
+                           "bi_gemm: workspace %zu < %zu bytes", ws_bytes,
+                           need);
+        BI_REQUIRE(bi_aligned16(ws), "bi_gemm: workspace alignment");
+        a.out = ws;
+        a.out_kind = BI_OUT_PARTIALS;
+    }
+
+    if (fused) {
+        if ((st = set_smem_attr<true, STAGES_FUSED>()) != BI_OK) return st;
+        gemm_kernel<true, STAGES_FUSED>
+            <<<dim3(mt, nt, 1), THREADS, smem_bytes(STAGES_FUSED), stream>>>(
+                ta, tb, a);
+    } else {
+        if ((st = set_smem_attr<false, STAGES_SPLIT>()) != BI_OK) return st;
+        gemm_kernel<false, STAGES_SPLIT>
+            <<<dim3(mt, nt, S), THREADS, smem_bytes(STAGES_SPLIT), stream>>>(
+                ta, tb, a);
+    }
+    BI_LAUNCH_CHECK("gemm launch");
+    if (need_reduce) {
+        const int64_t MN = (int64_t)M * N;
+        reduce_slices_kernel<<<(unsigned)((MN + 255) / 256), 256, 0, stream>>>(
+            static_cast<const float *>(ws), S, MN, out_kind, out);
+        BI_LAUNCH_CHECK("gemm reduce launch");
+    }
+    return BI_OK;
+}
+
+extern "C" bi_status bi_gemm(const bi_bf16 *x, int M, int K, const bi_bf16 *W,
+                             int N, void *out, int out_kind, void *ws,
+                             size_t ws_bytes, void *stream) {
+    return bi_gemm_sched(x, M, K, W, N, out, out_kind, ws, ws_bytes, 0,
+                         bi_stream(stream));
+}
+
+extern "C" bi_status bi_pack_gate_up(const bi_bf16 *wg, const bi_bf16 *wu,
+                                     int F, int K, bi_bf16 *wgu,
+                                     void *stream) {
+    BI_REQUIRE(wg && wu && wgu, "bi_pack_gate_up: null pointer");
+    BI_REQUIRE(F > 0 && F % 64 == 0 && K > 0 && K % 8 == 0,
+               "bi_pack_gate_up: F=%d must be a multiple of 64, K=%d of 8", F,
+               K);
+    BI_REQUIRE(bi_aligned16(wg) && bi_aligned16(wu) && bi_aligned16(wgu),
+               "bi_pack_gate_up: pointers must be 16-byte aligned");
+    const int K8 = K / 8;
+    const int64_t total = (int64_t)2 * F * K8;
+    const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4096);
+    pack_gate_up_kernel<<<blocks, 256, 0, bi_stream(stream)>>>(
+        reinterpret_cast<const uint4 *>(wg), reinterpret_cast<const uint4 *>(wu),
+        F, K8, reinterpret_cast<uint4 *>(wgu));
+    BI_LAUNCH_CHECK("pack_gate_up launch");
+    return BI_OK;
+}

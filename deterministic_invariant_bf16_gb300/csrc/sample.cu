@@ -1,0 +1,247 @@
+// bi_argmax_logits and philox_sample: token selection from fp32 logits.
+//
+// argmax: ybb.press section 1 notes that batch-dependent rounding can flip
+// the argmax of the logits.  The comparison here is a total order
+// (NaN above everything with the lower index winning among NaNs, then the
+// larger value, then the lower index; -0 == +0), so the result is unique
+// whatever order the block visits the elements in.
+//
+// philox_sample: ybb.press section 6 item 3, one counter-based generator per
+// request derived from (request_id, step): seed = request_id * 1000003 + step
+// (mod 2^64).  The generator is Philox4x64-10 (Salmon, Moraes, Dror, Shaw,
+// "Parallel random numbers: as easy as 1, 2, 3", SC'11) with key (seed, 0)
+// and counter 0; u = (word0 >> 40) * 2^-24.  The token is found by inverse
+// CDF over p_i = exp((logit_i - max) / temperature) with fixed-order blocked
+// prefix sums: thread k sums its contiguous slice in index order, the
+// slice totals are scanned by a fixed shuffle pattern, so the result depends
+// on nothing but the row.
+#include <float.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace {
+
+constexpr int SEL_THREADS = 1024;
+
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+    const bool vn = isnan(v), bn = isnan(bv);
+    if (vn || bn) return vn && bn ? i < bi : vn;
+    if (v != bv) return v > bv;
+    return i < bi;
+}
+
+__device__ __forceinline__ void warp_best(float &v, int &i) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+        if (better(ov, oi, v, i)) {
+            v = ov;
+            i = oi;
+        }
+    }
+}
+
+// Best (value, index) of the block; valid in thread 0.
+__device__ __forceinline__ void block_best(float &v, int &i) {
+    __shared__ float sv[32];
+    __shared__ int si[32];
+    warp_best(v, i);
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        sv[w] = v;
+        si[w] = i;
+    }
+    __syncthreads();
+    if (w == 0) {
+        const int nw = blockDim.x >> 5;
+        v = lane < nw ? sv[lane] : -INFINITY;
+        i = lane < nw ? si[lane] : 0x7fffffff;
+        warp_best(v, i);
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(SEL_THREADS)
+    argmax_kernel(const float *__restrict__ logits, int V,
+                  int32_t *__restrict__ ids) {
+    const float *row = logits + (int64_t)blockIdx.x * V;
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    if ((V & 3) == 0) {
+        const float4 *r4 = reinterpret_cast<const float4 *>(row);
+        for (int k = threadIdx.x; k < V / 4; k += SEL_THREADS) {
+            const float4 x = r4[k];
+            const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (better(xs[e], 4 * k + e, bv, bi)) {
+                    bv = xs[e];
+                    bi = 4 * k + e;
+                }
+        }
+    } else {
+        for (int k = threadIdx.x; k < V; k += SEL_THREADS)
+            if (better(row[k], k, bv, bi)) {
+                bv = row[k];
+                bi = k;
+            }
+    }
+    block_best(bv, bi);
+    if (threadIdx.x == 0) ids[blockIdx.x] = bi;
+}
+
+// ---------------------------------------------------------------- Philox --
+
+struct U4 {
+    uint64_t x[4];
+};
+
+__device__ __forceinline__ U4 philox4x64_10(U4 c, uint64_t k0, uint64_t k1) {
+    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += W0;
+            k1 += W1;
+        }
+        const uint64_t hi0 = __umul64hi(M0, c.x[0]), lo0 = M0 * c.x[0];
+        const uint64_t hi1 = __umul64hi(M1, c.x[2]), lo1 = M1 * c.x[2];
+        U4 n;
+        n.x[0] = hi1 ^ c.x[1] ^ k0;
+        n.x[1] = lo1;
+        n.x[2] = hi0 ^ c.x[3] ^ k1;
+        n.x[3] = lo0;
+        c = n;
+    }
+    return c;
+}
+
+__device__ __forceinline__ float sample_uniform(uint64_t request_id,
+                                                uint64_t step) {
+    const uint64_t seed = request_id * 1000003ull + step;
+    U4 c = {{0, 0, 0, 0}};
+    const U4 o = philox4x64_10(c, seed, 0);
+    return (float)(o.x[0] >> 40) * 0x1.0p-24f;
+}
+
+// Inclusive scan of one value per thread over the block, fixed pattern:
+// Hillis-Steele inside each warp, then the warp totals scanned the same way
+// by warp 0.  Returns the exclusive prefix; *total gets the block sum.
+__device__ __forceinline__ float block_exclusive_scan(float v, float *total) {
+    __shared__ float wsum[32];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float n = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc = __fadd_rn(n, inc);
+    }
+    if (lane == 31) wsum[w] = inc;
+    __syncthreads();
+    if (w == 0) {
+        float x = lane < (int)(blockDim.x >> 5) ? wsum[lane] : 0.f;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float n = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x = __fadd_rn(n, x);
+        }
+        wsum[lane] = x;  // inclusive warp prefix
+    }
+    __syncthreads();
+    const float before_warp = w > 0 ? wsum[w - 1] : 0.f;
+    *total = wsum[(blockDim.x >> 5) - 1];
+    // Exclusive prefix of this thread: the warps before it plus the
+    // inclusive scan of the previous lane.
+    float prev = __shfl_up_sync(0xffffffffu, inc, 1);
+    if (lane == 0) prev = 0.f;
+    return lane == 0 ? before_warp : __fadd_rn(before_warp, prev);
+}
+
+__global__ void __launch_bounds__(SEL_THREADS)
+    sample_kernel(const float *__restrict__ logits, int V,
+                  const uint64_t *__restrict__ request_id,
+                  const uint64_t *__restrict__ step, float tau,
+                  int32_t *__restrict__ ids) {
+    const int t = blockIdx.x;
+    const float *row = logits + (int64_t)t * V;
+    // 1. maximum (exact; NaN ignored)
+    float mx = -INFINITY;
+    for (int k = threadIdx.x; k < V; k += SEL_THREADS) mx = fmaxf(mx, row[k]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    __shared__ float smx[32];
+    if ((threadIdx.x & 31) == 0) smx[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    mx = smx[0];
+    for (int i = 1; i < SEL_THREADS / 32; ++i) mx = fmaxf(mx, smx[i]);
+    // 2. contiguous slice sums in index order
+    const int per = (V + SEL_THREADS - 1) / SEL_THREADS;
+    const int lo = min(V, threadIdx.x * per), hi = min(V, lo + per);
+    float part = 0.f;
+    for (int k = lo; k < hi; ++k)
+        part = __fadd_rn(part, expf(__fdiv_rn(__fsub_rn(row[k], mx), tau)));
+    float total;
+    const float prefix = block_exclusive_scan(part, &total);
+    // 3. first index whose running sum exceeds u * total
+    const float target = __fmul_rn(sample_uniform(request_id[t], step[t]), total);
+    int first = 0x7fffffff;
+    float cdf = prefix;
+    for (int k = lo; k < hi; ++k) {
+        cdf = __fadd_rn(cdf, expf(__fdiv_rn(__fsub_rn(row[k], mx), tau)));
+        if (cdf > target) {
+            first = k;
+            break;
+        }
+    }
+    // Integer min/max over the block: order-free, so deterministic.
+    __shared__ int s_first, s_last;
+    if (threadIdx.x == 0) {
+        s_first = 0x7fffffff;
+        s_last = -1;
+    }
+    __syncthreads();
+    if (first != 0x7fffffff) atomicMin(&s_first, first);
+    // Last index with p > 0, for a row whose running sum never passes the
+    // target because of rounding.
+    int lp = -1;
+    for (int k = hi - 1; k >= lo; --k)
+        if (expf(__fdiv_rn(__fsub_rn(row[k], mx), tau)) > 0.f) {
+            lp = k;
+            break;
+        }
+    if (lp >= 0) atomicMax(&s_last, lp);
+    __syncthreads();
+    if (threadIdx.x == 0)
+        ids[t] = s_first != 0x7fffffff ? s_first : max(s_last, 0);
+}
+
+}  // namespace
+
+extern "C" bi_status bi_argmax_logits(const float *logits, int T, int V,
+                                      int32_t *ids, void *stream) {
+    BI_REQUIRE(T >= 0 && V > 0 && logits && ids, "bi_argmax_logits: bad args");
+    BI_REQUIRE(bi_aligned16(logits), "bi_argmax_logits: logits alignment");
+    if (T == 0) return BI_OK;
+    argmax_kernel<<<T, SEL_THREADS, 0, bi_stream(stream)>>>(logits, V, ids);
+    BI_LAUNCH_CHECK("argmax launch");
+    return BI_OK;
+}
+
+extern "C" bi_status philox_sample(const float *logits, int T, int V,
+                                   const uint64_t *request_id,
+                                   const uint64_t *step, float temperature,
+                                   int32_t *ids, void *stream) {
+    BI_REQUIRE(T >= 0 && V > 0 && logits && ids, "philox_sample: bad args");
+    BI_REQUIRE(temperature >= 0.f, "philox_sample: temperature < 0");
+    if (temperature == 0.f) return bi_argmax_logits(logits, T, V, ids, stream);
+    BI_REQUIRE(request_id && step, "philox_sample: null request_id/step");
+    if (T == 0) return BI_OK;
+    sample_kernel<<<T, SEL_THREADS, 0, bi_stream(stream)>>>(
+        logits, V, request_id, step, temperature, ids);
+    BI_LAUNCH_CHECK("sample launch");
+    return BI_OK;
+}

@@ -1,0 +1,327 @@
+/*
+ * bi.h - C ABI of libbi, a batch-invariant bf16 decoder library for GB300
+ * (sm_103a).
+ *
+ * What "batch-invariant" means here (ybb.press, "LLM 推理确定性工程深度实战",
+ * section 4 "Batch-Invariant Kernel"; Vosti abstract): every reduction in
+ * every kernel (GEMM K-loop, RMSNorm, softmax and attention over paged KV,
+ * logits argmax) runs in an order fixed by the data and by compile-time
+ * constants.  The order never depends on the batch size, on a row's position
+ * in the batch, on the query length, on the physical order of KV pages, nor
+ * on how many SMs happen to be free.  There are no floating-point atomics.
+ * A request's logits are therefore bitwise identical whatever batch it is
+ * served in, and across repeated runs.
+ *
+ * Conventions shared by every entry point
+ *   - Return value: bi_status.  BI_OK on success.  On failure nothing is
+ *     launched unless stated otherwise.  A thread-local message is kept for
+ *     bi_last_error().
+ *   - bf16 tensors are passed as bi_bf16* (the 16-bit pattern).  Every
+ *     tensor pointer is a DEVICE pointer owned by the caller unless its
+ *     name starts with h_ (host memory, also caller-owned).  The library
+ *     never frees caller memory, and it allocates none in any call listed
+ *     here: workspaces are passed in, sized by the *_workspace_size queries.
+ *   - All device work is enqueued on `stream` (a cudaStream_t passed as
+ *     void*; NULL is the legacy default stream) and is asynchronous, except
+ *     verify_commit_rollback, which synchronises `stream` to hand back its
+ *     small host outputs.
+ *   - Row-major layouts throughout.  "[T][H]" means T rows of H contiguous
+ *     elements.
+ *   - Device pointers must be 16-byte aligned; inner dimensions of bf16
+ *     matrices read by the tensor-core GEMM must be multiples of 8.
+ */
+#ifndef BI_H
+#define BI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t bi_bf16;
+
+typedef enum {
+    BI_OK = 0,
+    BI_ERR_INVALID_ARG = 1,        /* null/misaligned pointer, bad size */
+    BI_ERR_UNSUPPORTED = 2,        /* shape with no compiled instantiation */
+    BI_ERR_WORKSPACE_TOO_SMALL = 3,
+    BI_ERR_CUDA = 4,               /* a CUDA runtime/driver call failed */
+    BI_ERR_BOUNDS = 5,             /* a kernel saw an out-of-range index */
+    BI_ERR_TIMEOUT = 6             /* a bounded device wait ran out */
+} bi_status;
+
+/* Message for the last failing call on this thread ("" if none). */
+const char *bi_last_error(void);
+
+/* Reads and clears the device-side status word that kernels set when a
+ * bounded wait runs out (BI_ERR_TIMEOUT) or an index check fails
+ * (BI_ERR_BOUNDS).  Synchronises `stream`.  *h_status receives BI_OK or the
+ * first error recorded since the previous call. */
+bi_status bi_device_status(int32_t *h_status, void *stream);
+
+/* ------------------------------------------------------------------ GEMM --
+ * y = x W^T.  ybb.press section 2.2 (GEMM heuristics switch tile shape and
+ * split-K with (M, N, K); split-K with atomicAdd is run-to-run
+ * nondeterministic) and section 4 (fixed tile split, a fixed split count
+ * with a fixed-order second stage, no float atomics).
+ *
+ * x [M][K] bf16, W [N][K] bf16 (row n = output feature n, "K-major").
+ * fp32 accumulation on the tcgen05 tensor cores.  The tile is 128 x 128
+ * output elements for every M (rows past M are zero-filled, never read from
+ * memory).  The K range is cut into bi_gemm_splits(N, K) fixed slices of
+ * whole 64-column blocks; each slice is an independent fp32 chain in
+ * ascending k.  Slices are summed in slice order 0..S-1 by the consumer.
+ *
+ * out_kind selects what is written to `out`:
+ *   BI_OUT_PARTIALS  fp32 [S][M][N]: the S slice sums, unreduced.  The
+ *                    second stage is bi_rmsnorm (or bi_rope for q/k/v).
+ *   BI_OUT_F32       fp32 [M][N]: slices reduced in order (needs workspace
+ *                    bi_gemm_workspace_size(M, N, K) if S > 1).
+ *   BI_OUT_BF16      bf16 [M][N]: as F32, rounded to nearest even.
+ *   BI_OUT_SWIGLU    bf16 [M][N/2]: W holds gate and up rows interleaved in
+ *                    blocks of 64 (bi_pack_gate_up); out = silu(g) * u with
+ *                    silu(g) = g / (1 + e^-g) in fp32.  Needs S == 1.
+ */
+typedef enum {
+    BI_OUT_PARTIALS = 0,
+    BI_OUT_F32 = 1,
+    BI_OUT_BF16 = 2,
+    BI_OUT_SWIGLU = 3
+} bi_out_kind;
+
+/* Fixed split count for a weight of shape [N][K]: a pure function of (N, K),
+ * never of M. */
+int bi_gemm_splits(int N, int K);
+
+/* Bytes of workspace bi_gemm needs for (M, N, K) and BI_OUT_F32/BF16. */
+size_t bi_gemm_workspace_size(int M, int N, int K);
+
+bi_status bi_gemm(const bi_bf16 *x, int M, int K, const bi_bf16 *W, int N,
+                  void *out, int out_kind, void *ws, size_t ws_bytes,
+                  void *stream);
+
+/* Interleaves separate gate and up weights, each [F][K], into the [2F][K]
+ * layout BI_OUT_SWIGLU reads: 64 gate rows, then the 64 up rows of the same
+ * features, and so on.  F must be a multiple of 64.  A pure copy. */
+bi_status bi_pack_gate_up(const bi_bf16 *wg, const bi_bf16 *wu, int F, int K,
+                          bi_bf16 *wgu, void *stream);
+
+/* --------------------------------------------------------------- RMSNorm --
+ * y = x * (1 / sqrt(mean(x^2) + eps)) * w per row of length H, fused with
+ * the second stage of a split GEMM and the residual add (ybb.press section
+ * 4: the second stage sums partials 0..S-1 in that fixed order).
+ *
+ *   partials  fp32 [S][T][H] or NULL.  If given, v = sum_s partials[s] in
+ *             order s = 0..S-1; then, if residual is given,
+ *             residual = bf16(residual + v) and the norm reads the new
+ *             residual; else the norm reads bf16(v).
+ *   x         bf16 [T][H], used when partials is NULL and residual is NULL.
+ *   residual  bf16 [T][H] in/out, or NULL.  With partials NULL it is only
+ *             read.
+ *   w         bf16 [H] norm weight.  y bf16 [T][H] output.
+ * Per row: each thread sums fixed 8-element slices in order, then a fixed
+ * xor-shuffle tree, then warps in fixed order. */
+bi_status bi_rmsnorm(const float *partials, int S, const bi_bf16 *x,
+                     bi_bf16 *residual, const bi_bf16 *w, int T, int H,
+                     float eps, bi_bf16 *y, void *stream);
+
+/* Row gather h[t] = E[tokens[t]] from the untied embedding E [V][H]. */
+bi_status bi_embed(const int32_t *tokens, int T, const bi_bf16 *E, int V,
+                   int H, bi_bf16 *h, void *stream);
+
+/* ----------------------------------------------------- RoPE + KV append --
+ * Half-split rotary embedding (pairs (i, i + D/2), angle
+ * pos * theta^(-2i/D), no frequency scaling) of q and k, and the append of
+ * k and v to the paged cache (PagedAttention pages; Vosti: KV values tied to
+ * their logical positions, any physical page order).
+ *
+ *   qkv       fp32 [S][T][(Hq+2Hkv)D] slice partials of the QKV GEMM,
+ *             summed in order s = 0..S-1 and rounded to bf16 first; rows
+ *             are q heads, k heads, v heads.
+ *   pos       int32 [T] absolute position of each row.
+ *   row_req   int32 [T] page-table row of each row; < 0 marks a pad row
+ *             (nothing appended, q written as zeros).
+ *   q_out     bf16 [T][Hq][D] rotated queries.
+ *   k_pool, v_pool  bf16 [n_pages][Hkv][16][D]; row t's k and v land in
+ *             page page_table[row_req[t] * max_pages + pos[t] / 16], slot
+ *             pos[t] % 16.  Angles in double, rotation in fp32. */
+bi_status bi_rope(const float *qkv, int S, const int32_t *pos,
+                  const int32_t *row_req, int T, int Hq, int Hkv, int D,
+                  double theta, bi_bf16 *q_out, bi_bf16 *k_pool,
+                  bi_bf16 *v_pool, const int32_t *page_table, int max_pages,
+                  int n_pages, void *stream);
+
+/* ---------------------------------------------------------------- SwiGLU --
+ * out[i] = bf16(silu(g[i]) * u[i]), silu(g) = g / (1 + e^-g), fp32 inputs.
+ * (The model path fuses this into the gate/up GEMM, BI_OUT_SWIGLU.) */
+bi_status bi_swiglu(const float *g, const float *u, int64_t n, bi_bf16 *out,
+                    void *stream);
+
+/* ------------------------------------------------------------- attention --
+ * Causal grouped-query attention over the paged cache, in fixed 256-position
+ * KV chunks (Vosti: bitwise-equal outputs across batches, query lengths and
+ * paged layouts; ybb.press section 4: two-stage fixed-order reduction).
+ *
+ * For each (query row, query head h, chunk c of absolute positions
+ * [256c, 256c+256)) a partial (m, l, o) is computed from scratch:
+ * s_j = (q . k_j) / sqrt(D) on the tensor cores (dims in ascending 16-steps),
+ * masked past the row's context; m = max s; p_j = exp(s_j - m); l = sum p_j
+ * in a fixed order; o = sum bf16(p_j) v_j in ascending 16-key steps.  The
+ * chunks are then merged sequentially c = 0, 1, ...:
+ * m' = max(m, m_c), o = o e^(m - m') + o_c e^(m_c - m'), likewise l, and
+ * out = bf16(o / l).  Query head h reads KV head h / (Hq / Hkv).  Both
+ * kernels below run the same chunk and merge code, so a (request, position)
+ * gets the same bits from either.  Supported head_dim: 32 and 128;
+ * Hq / Hkv in {1, 2, 4, 8, 16}. */
+
+/* Workspace bytes for bi_paged_decode_attn with B rows and contexts of at
+ * most max_kv_len positions. */
+size_t bi_decode_attn_workspace_size(int B, int Hq, int D, int max_kv_len);
+
+/* One query per row.  q bf16 [B][Hq][D]; row_req int32 [B] page-table row;
+ * kv_len int32 [B] context length of each row, including its own position
+ * (1 <= kv_len <= max_kv_len, max_kv_len <= 16 * max_pages).
+ * out bf16 [B][Hq][D]. */
+bi_status bi_paged_decode_attn(const bi_bf16 *q, const bi_bf16 *k_pool,
+                               const bi_bf16 *v_pool,
+                               const int32_t *page_table, int max_pages,
+                               const int32_t *row_req, const int32_t *kv_len,
+                               int B, int max_kv_len, int Hq, int Hkv, int D,
+                               float scale, bi_bf16 *out, void *ws,
+                               size_t ws_bytes, void *stream);
+
+/* Several queries per request (prefill, verify).  Rows of segment r are
+ * cu_q[r] .. cu_q[r+1]-1 (device int32 [R+1], cu_q[0] = 0,
+ * cu_q[R] = T); seg_req int32 [R] is the segment's page-table row;
+ * pos int32 [T] the absolute position of each row (causal: a row attends to
+ * positions 0..pos).  Rows of a segment hold consecutive positions.  Rows
+ * with seg_req < 0 are pad rows and get zeros.  max_q is an upper bound on
+ * every segment's length, max_kv_len on every pos + 1.
+ * q bf16 [T][Hq][D] -> out bf16 [T][Hq][D]. */
+bi_status bi_prefill_attn(const bi_bf16 *q, const int32_t *cu_q,
+                          const int32_t *seg_req, int R, int T,
+                          const int32_t *pos, int max_q, int max_kv_len,
+                          const bi_bf16 *k_pool, const bi_bf16 *v_pool,
+                          const int32_t *page_table, int max_pages, int Hq,
+                          int Hkv, int D, float scale, bi_bf16 *out,
+                          void *stream);
+
+/* ------------------------------------------------------- token selection --
+ * Greedy: ids[t] = first index of the maximum of logits[t] (fp32 [T][V]).
+ * NaN counts as maximal and the first NaN wins; -0 equals +0.  Exact, so the
+ * result is unique (ybb.press section 1: a tiny perturbation flips argmax). */
+bi_status bi_argmax_logits(const float *logits, int T, int V, int32_t *ids,
+                           void *stream);
+
+/* Temperature sampling with a counter-based generator per request (ybb.press
+ * section 6, item 3): seed = (request_id * 1000003 + step) mod 2^64,
+ * u = (Philox4x64-10(counter 0, key (seed, 0)) word 0 >> 40) * 2^-24,
+ * p_i = exp((logits_i - max) / temperature), token = first i whose running
+ * sum exceeds u * sum(p) (fixed-order blocked prefix sums).  temperature 0
+ * means greedy.  request_id, step: device uint64 [T]. */
+bi_status philox_sample(const float *logits, int T, int V,
+                        const uint64_t *request_id, const uint64_t *step,
+                        float temperature, int32_t *ids, void *stream);
+
+/* ------------------------------------------------------------ the model --
+ * Pre-norm Llama decoder: embed, n_layers x (RMSNorm, QKV GEMM, RoPE + KV
+ * append, attention, O GEMM + residual, RMSNorm, gate/up GEMM with SwiGLU,
+ * down GEMM + residual), final RMSNorm, LM head with fp32 logits.  The
+ * handle keeps pointers only: weights, KV pools and workspace belong to the
+ * caller and must outlive it. */
+typedef struct {
+    int n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn, vocab;
+    float eps;
+    double theta;
+    int max_tokens;   /* most rows one forward call may carry */
+    int max_kv_len;   /* longest context any row may attend over */
+    int max_pages;    /* page-table row stride */
+    int n_pages;      /* pages in each layer's pool */
+} bi_model_cfg;
+
+typedef struct {
+    const bi_bf16 *embed;       /* [V][H] */
+    const bi_bf16 *final_norm;  /* [H] */
+    const bi_bf16 *lm_head;     /* [V][H] */
+    /* host arrays of n_layers device pointers each */
+    const bi_bf16 *const *attn_norm;  /* [H] */
+    const bi_bf16 *const *wqkv;       /* [(Hq+2Hkv)D][H] */
+    const bi_bf16 *const *wo;         /* [H][Hq D] */
+    const bi_bf16 *const *ffn_norm;   /* [H] */
+    const bi_bf16 *const *wgu;        /* [2F][H], bi_pack_gate_up layout */
+    const bi_bf16 *const *wd;         /* [H][F] */
+    bi_bf16 *const *k_pool;           /* [n_pages][Hkv][16][D] */
+    bi_bf16 *const *v_pool;
+} bi_model_weights;
+
+typedef struct bi_model bi_model;
+
+size_t bi_model_workspace_size(const bi_model_cfg *cfg);
+
+bi_status bi_model_create(const bi_model_cfg *cfg, const bi_model_weights *w,
+                          void *ws, size_t ws_bytes, bi_model **out);
+
+void bi_model_destroy(bi_model *m);
+
+/* One forward pass over T rows.
+ *   tokens, pos, row_req: device int32 [T] (row_req = page-table row,
+ *   < 0 for a pad row).
+ *   Decode (R == 0): every row is its own request at position pos[t] and
+ *   attends to positions 0..pos[t]; max_kv_len bounds pos + 1.
+ *   Prefill/verify (R > 0): rows are grouped into R segments by the device
+ *   arrays cu_q [R+1] and seg_req [R]; a segment's rows are one request's
+ *   consecutive positions; max_q bounds the segment length.
+ *   page_table: device int32 [slots][max_pages].
+ *   logits: device fp32 [T][V] (may be NULL if only ids are wanted);
+ *   ids: device int32 [T] greedy tokens, or NULL. */
+bi_status bi_model_forward(bi_model *m, int T, const int32_t *tokens,
+                           const int32_t *pos, const int32_t *row_req,
+                           int R, const int32_t *cu_q, const int32_t *seg_req,
+                           int max_q, int max_kv_len,
+                           const int32_t *page_table, float *logits,
+                           int32_t *ids, void *stream);
+
+/* --------------------------------------------------- LLM-42 verification --
+ * Grouped verification with commit and rollback ("LLM-42: Enabling
+ * Determinism in LLM Inference with Verified Speculation", section
+ * "核心方法": paper sections 4.2-4.3, Fig. 8).  Candidate windows of R
+ * requests are packed first-in first-out into one fixed BI_VERIFY_ROWS-row
+ * batch (pad rows after them), recomputed on the invariant path, and for
+ * each request:
+ *   j = first i with argmax_i != candidate_i, or w if none,
+ *   commit_len = j, kv_len' = kv_len + j, fix_token = argmax_j (or -1),
+ *   page-table entries at or past ceil(kv_len' / 16) become -1 and their
+ *   page ids are listed in h_freed.
+ * Window row i of request r sits at position h_kv_len[r] + i; its input
+ * token is h_last_token[r] for i = 0 and candidate i-1 after that, so the
+ * cache must hold the request's committed tokens except the last one, and
+ * pages for every window position must already be in the page table.
+ * Windows that do not fit after the first ones are not taken: *h_taken says
+ * how many were.
+ *   h_req, h_kv_len, h_last_token, h_win_len: host int32 [R]
+ *   h_candidates: host int32 [sum w], windows concatenated
+ *   page_table: device int32 [slots][max_pages], updated in place
+ *   kv_len: device int32 [slots], entry h_req[r] set to kv_len'
+ *   h_commit_len, h_fix_token: host int32 [R] outputs
+ *   h_freed: host int32 [freed_cap]; *h_n_freed receives the count
+ *   logits: device fp32 [BI_VERIFY_ROWS][V] scratch, kept for inspection.
+ * Synchronises `stream` before returning. */
+#define BI_VERIFY_ROWS 256
+
+bi_status verify_commit_rollback(bi_model *m, int R, const int32_t *h_req,
+                                 const int32_t *h_kv_len,
+                                 const int32_t *h_last_token,
+                                 const int32_t *h_win_len,
+                                 const int32_t *h_candidates,
+                                 int32_t *page_table, int32_t *kv_len,
+                                 int32_t *h_commit_len, int32_t *h_fix_token,
+                                 int32_t *h_freed, int freed_cap,
+                                 int32_t *h_n_freed, int32_t *h_taken,
+                                 float *logits, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BI_H */

@@ -1,0 +1,85 @@
+"""The C ABI library loads on a machine without a GPU, exports every entry
+point include/bi.h declares, and rejects bad arguments before launching."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def bi():
+    from deterministic_invariant_bf16_gb300 import build, binding
+    build.build()
+    return binding
+
+
+def declared_functions():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if not h.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^[A-Za-z_][\w \*]*?\b([a-z_][a-z0-9_]*)\s*\(",
+                             text, flags=re.M):
+            if not m.group(0).lstrip().startswith(("typedef", "#")):
+                names.add(m.group(1))
+    return names
+
+
+def test_every_declared_symbol_is_exported(bi):
+    names = declared_functions()
+    assert {"bi_gemm", "bi_rmsnorm", "bi_rope", "bi_swiglu",
+            "bi_paged_decode_attn", "bi_prefill_attn", "bi_argmax_logits",
+            "verify_commit_rollback", "philox_sample"} <= names
+    lib = ctypes.CDLL(bi.LIB_PATH)
+    missing = [n for n in sorted(names) if not hasattr(lib, n)]
+    assert not missing, missing
+    # and the binding wraps each of them under the same name
+    assert names <= set(bi.SIGNATURES)
+
+
+def test_split_counts_depend_only_on_weight_shape(bi):
+    # 8B shapes: QKV, O, gate/up (interleaved), down, LM head
+    s = {(n, k): bi.bi_gemm_splits(n, k) for n, k in
+         [(6144, 4096), (4096, 4096), (28672, 4096), (4096, 14336),
+          (128256, 4096), (384, 128), (512, 128)]}
+    assert s[(28672, 4096)] == 1 and s[(128256, 4096)] == 1
+    assert s[(512, 128)] == 1
+    assert all(1 <= v <= 8 for v in s.values())
+    assert bi.bi_gemm_workspace_size(1, 4096, 4096) == \
+        s[(4096, 4096)] * 4096 * 4 * (s[(4096, 4096)] > 1)
+
+
+def test_bad_arguments_fail_before_launch(bi):
+    lib = bi.lib()
+    # K not a multiple of 8
+    assert lib.bi_gemm(ctypes.c_void_p(16), 4, 7, ctypes.c_void_p(16), 8,
+                       ctypes.c_void_p(16), 1, None, 0, None) == 1
+    # null pointers
+    assert lib.bi_gemm(None, 4, 64, None, 8, None, 1, None, 0, None) == 1
+    assert b"null" in lib.bi_last_error()
+    # unsupported head dim
+    assert lib.bi_paged_decode_attn(
+        ctypes.c_void_p(16), ctypes.c_void_p(16), ctypes.c_void_p(16),
+        ctypes.c_void_p(16), 4, ctypes.c_void_p(16), ctypes.c_void_p(16),
+        1, 16, 4, 4, 64, 0.1, ctypes.c_void_p(16), ctypes.c_void_p(16),
+        1 << 20, None) == 2
+    # verify needs a model
+    assert lib.verify_commit_rollback(None, 1, *([None] * 5), None, None,
+                                      None, None, None, 0, None, None, None,
+                                      None) == 1
+    cfg = bi.ModelCfg(n_layers=1, hidden=128, n_heads=4, n_kv_heads=4,
+                      head_dim=64, ffn=256, vocab=512, eps=1e-5, theta=1e4,
+                      max_tokens=8, max_kv_len=64, max_pages=4, n_pages=8)
+    assert bi.bi_model_workspace_size(cfg) == 0   # head_dim 64 unsupported
+    cfg.head_dim = 32
+    assert bi.bi_model_workspace_size(cfg) > 0
+
+
+def test_decode_workspace_formula(bi):
+    assert bi.bi_decode_attn_workspace_size(3, 32, 128, 257) == \
+        3 * 32 * 2 * 132 * 4

@@ -1,0 +1,322 @@
+"""Per-kernel GPU tests through the C ABI: RMSNorm with the fused
+split-reduction and residual, RoPE + paged KV append, decode and prefill
+attention over permuted pages, argmax and Philox sampling.  Each kernel is
+checked against the oracle and bitwise against itself across batch
+composition, row position, query length and page layout (Vosti abstract;
+ybb.press section 4)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import bits, from_bits, norm_rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def bi():
+    from deterministic_invariant_bf16_gb300 import binding, build
+    build.build()
+    binding.lib()
+    return binding
+
+
+def randn_bf16(shape, seed, std=1.0):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    return (torch.randn(shape, generator=g, device="cuda") * std).to(
+        torch.bfloat16)
+
+
+def sync_ok(bi):
+    torch.cuda.synchronize()
+    assert bi.bi_device_status() == 0
+
+
+def ulp_diff(a_bits, b_bits):
+    return np.abs(a_bits.astype(np.int32) - b_bits.astype(np.int32))
+
+
+# ------------------------------------------------------------- RMSNorm --
+
+@pytest.mark.parametrize("H", [128, 4096])
+def test_rmsnorm_fused_reduce_residual(bi, orc, H):
+    T, S = 37, 3
+    g = torch.Generator(device="cuda").manual_seed(H)
+    parts = torch.randn(S, T, H, generator=g, device="cuda") * 0.3
+    h0 = randn_bf16((T, H), 2)
+    w = randn_bf16((H,), 3)
+    res = h0.clone()
+    y = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    bi.bi_rmsnorm(parts, S, None, res, w, T, H, 1e-5, y)
+    sync_ok(bi)
+    p = parts.cpu().numpy()
+    v = (p[0] + p[1]) + p[2]                         # slice order 0, 1, 2
+    ref_res = orc.bf16_bits(orc.bf16_value(bits(h0)) + v)
+    assert np.array_equal(bits(res), ref_res)       # same fp32 operations
+    ref_y = orc.bf16_bits(orc.rmsnorm(orc.bf16_value(ref_res), bits(w), 1e-5))
+    d = ulp_diff(bits(y), ref_y)
+    assert d.max() <= 1 and (d == 0).mean() > 0.98
+    # row invariance: each row alone gives the same bits
+    for t in (0, 19, 36):
+        r1 = h0[t:t + 1].clone()
+        y1 = torch.empty(1, H, dtype=torch.bfloat16, device="cuda")
+        p1 = parts[:, t:t + 1].contiguous()
+        bi.bi_rmsnorm(p1, S, None, r1, w, 1, H, 1e-5, y1)
+        sync_ok(bi)
+        assert np.array_equal(bits(y1)[0], bits(y)[t])
+        assert np.array_equal(bits(r1)[0], bits(res)[t])
+    # plain input (no partials, no residual)
+    y2 = torch.empty_like(y)
+    bi.bi_rmsnorm(None, 0, h0, None, w, T, H, 1e-5, y2)
+    sync_ok(bi)
+    ref2 = orc.bf16_bits(orc.rmsnorm(orc.bf16_value(bits(h0)), bits(w), 1e-5))
+    assert ulp_diff(bits(y2), ref2).max() <= 1
+
+
+# ---------------------------------------------------------- RoPE + KV --
+
+def test_rope_and_paged_append(bi, orc):
+    T, Hq, Hkv, D, S, theta = 21, 8, 2, 128, 2, 5e5
+    QKV = (Hq + 2 * Hkv) * D
+    g = torch.Generator(device="cuda").manual_seed(7)
+    parts = torch.randn(S, T, QKV, generator=g, device="cuda")
+    rng = np.random.default_rng(8)
+    pos = rng.integers(0, 3000, size=T).astype(np.int32)
+    slots = rng.integers(0, 4, size=T).astype(np.int32)
+    slots[3] = -1                                   # a pad row
+    max_pages, n_pages = 200, 900
+    table = rng.permutation(n_pages)[:4 * max_pages].reshape(4, max_pages)
+    table = table.astype(np.int32)
+    kp = torch.zeros(n_pages, Hkv, 16, D, dtype=torch.bfloat16, device="cuda")
+    vp = torch.zeros_like(kp)
+    q = torch.empty(T, Hq, D, dtype=torch.bfloat16, device="cuda")
+    bi.bi_rope(parts, S, torch.from_numpy(pos).cuda(),
+               torch.from_numpy(slots).cuda(), Hq, Hkv, D, theta, q, kp, vp,
+               torch.from_numpy(table).cuda())
+    sync_ok(bi)
+    p = parts.cpu().numpy()
+    qkv = orc.bf16r(p[0] + p[1])
+    rq = orc.bf16_bits(orc.rope(qkv[:, :Hq * D].reshape(T, Hq, D), pos, theta))
+    rk = orc.bf16_bits(orc.rope(qkv[:, Hq * D:(Hq + Hkv) * D].reshape(
+        T, Hkv, D), pos, theta))
+    rv = orc.bf16_bits(qkv[:, (Hq + Hkv) * D:].reshape(T, Hkv, D))
+    live = slots >= 0
+    assert ulp_diff(bits(q)[live], rq[live]).max() <= 1
+    assert np.all(bits(q)[~live] == 0)
+    kb, vb = bits(kp), bits(vp)
+    for t in np.nonzero(live)[0]:
+        pg = table[slots[t], pos[t] // 16]
+        assert ulp_diff(kb[pg, :, pos[t] % 16], rk[t]).max() <= 1
+        assert np.array_equal(vb[pg, :, pos[t] % 16], rv[t])
+
+
+# ----------------------------------------------------------- attention --
+
+class PagedKV:
+    """Random KV contents for R requests, stored in a NaN-filled pool under
+    a random page order; the logical caches are kept for the oracle."""
+
+    def __init__(self, lens, Hkv, D, seed, n_pages=None, nan_fill=True):
+        rng = np.random.default_rng(seed)
+        self.lens = np.asarray(lens)
+        self.Hkv, self.D = Hkv, D
+        L = int(self.lens.max())
+        R = len(lens)
+        self.k = orc_bf16(rng.normal(size=(R, L, Hkv, D)))
+        self.v = orc_bf16(rng.normal(size=(R, L, Hkv, D)))
+        self.max_pages = -(-L // 16) + 1
+        need = int(sum(-(-n // 16) for n in lens))
+        self.n_pages = n_pages or need + 7
+        self.place(rng.permutation(self.n_pages), nan_fill)
+
+    def place(self, perm, nan_fill=True):
+        R = len(self.lens)
+        table = np.full((R, self.max_pages), -1, np.int32)
+        fill = 0x7fc0 if nan_fill else 0
+        kp = np.full((self.n_pages, self.Hkv, 16, self.D), fill, np.uint16)
+        vp = kp.copy()
+        at = 0
+        for r, n in enumerate(self.lens):
+            for pi in range(-(-n // 16)):
+                pg = int(perm[at])
+                at += 1
+                table[r, pi] = pg
+                lo, hi = pi * 16, min(n, pi * 16 + 16)
+                kp[pg, :, :hi - lo] = self.k[r, lo:hi].transpose(1, 0, 2)
+                vp[pg, :, :hi - lo] = self.v[r, lo:hi].transpose(1, 0, 2)
+        self.table = torch.from_numpy(table).cuda()
+        self.kp = from_bits(kp)
+        self.vp = from_bits(vp)
+
+
+def orc_bf16(x):
+    import oracle
+    return oracle.bf16_bits(np.asarray(x, np.float32))
+
+
+def decode(bi, q, kv, rows, kv_len):
+    B, Hq, D = q.shape
+    max_kv = int(max(kv_len))
+    ws = torch.empty(bi.bi_decode_attn_workspace_size(B, Hq, D, max_kv) // 4,
+                     dtype=torch.float32, device="cuda")
+    out = torch.empty_like(q)
+    bi.bi_paged_decode_attn(q, kv.kp, kv.vp, kv.table,
+                            torch.tensor(rows, dtype=torch.int32).cuda(),
+                            torch.tensor(kv_len, dtype=torch.int32).cuda(),
+                            max_kv, 1 / math.sqrt(D), out, ws)
+    return out
+
+
+def prefill(bi, q, kv, segs):
+    """segs: list of (request, first position, n rows); q rows in order."""
+    cu, sr, pos = [0], [], []
+    for r, p0, n in segs:
+        cu.append(cu[-1] + n)
+        sr.append(r)
+        pos += list(range(p0, p0 + n))
+    out = torch.empty_like(q)
+    bi.bi_prefill_attn(q, torch.tensor(cu, dtype=torch.int32).cuda(),
+                       torch.tensor(sr, dtype=torch.int32).cuda(),
+                       torch.tensor(pos, dtype=torch.int32).cuda(),
+                       max(n for _, _, n in segs), max(pos) + 1, kv.kp, kv.vp,
+                       kv.table, 1 / math.sqrt(q.shape[2]), out)
+    return out, pos
+
+
+def attn_ref(orc, q, kv, rows, positions):
+    D = q.shape[2]
+    return orc.attention(orc.bf16_value(bits(q)), orc.bf16_value(kv.k),
+                         orc.bf16_value(kv.v), np.asarray(rows, np.int32),
+                         np.asarray(positions, np.int32),
+                         np.float32(1 / math.sqrt(D)))
+
+
+def check_close(got_bits, ref, orc):
+    got = orc.bf16_value(got_bits).astype(np.float64)
+    T, H, D = ref.shape
+    for t in range(T):
+        for h in range(H):
+            assert norm_rel_err(got[t, h], ref[t, h]) < 1e-2, (t, h)
+    assert np.abs(got - ref).max() < 2e-2
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(32, 8, 128), (4, 4, 32)])
+def test_decode_attention(bi, orc, Hq, Hkv, D):
+    lens = [1, 15, 16, 17, 255, 256, 257, 700, 1500, 40]
+    kv = PagedKV(lens, Hkv, D, seed=31)
+    q = randn_bf16((len(lens), Hq, D), 32)
+    rows = list(range(len(lens)))
+    out = decode(bi, q, kv, rows, lens)
+    sync_ok(bi)
+    ref = attn_ref(orc, q, kv, rows, np.array(lens) - 1)
+    check_close(bits(out), ref, orc)
+    full = bits(out)
+    # each request alone, and the batch in reverse order: same bits
+    for b in (0, 6, 8):
+        one = decode(bi, q[b:b + 1].contiguous(), kv, [b], [lens[b]])
+        sync_ok(bi)
+        assert np.array_equal(bits(one)[0], full[b])
+    rev = decode(bi, q.flip(0).contiguous(), kv, rows[::-1], lens[::-1])
+    sync_ok(bi)
+    assert np.array_equal(bits(rev)[::-1], full)
+    # another physical page order: same bits
+    kv.place(np.random.default_rng(99).permutation(kv.n_pages))
+    again = decode(bi, q, kv, rows, lens)
+    sync_ok(bi)
+    assert np.array_equal(bits(again), full)
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(32, 8, 128), (4, 4, 32)])
+def test_prefill_matches_decode_bitwise(bi, orc, Hq, Hkv, D):
+    """Query-length invariance (Vosti): a position computed inside a window
+    of many queries equals the same position decoded on its own."""
+    lens = [300, 530, 64, 1030]
+    kv = PagedKV(lens, Hkv, D, seed=41)
+    segs = [(0, 250, 50), (1, 470, 60), (2, 0, 64), (3, 1000, 17),
+            (3, 1017, 13)]
+    T = sum(n for _, _, n in segs)
+    q = randn_bf16((T, Hq, D), 42)
+    out, pos = prefill(bi, q, kv, segs)
+    sync_ok(bi)
+    rows = sum([[r] * n for r, _, n in segs], [])
+    ref = attn_ref(orc, q, kv, rows, pos)
+    check_close(bits(out), ref, orc)
+    dec = decode(bi, q, kv, rows, [p + 1 for p in pos])
+    sync_ok(bi)
+    assert np.array_equal(bits(dec), bits(out))
+    # segments split differently (chunked prefill): same bits
+    segs2 = [(0, 250, 7), (0, 257, 43), (1, 470, 60), (2, 0, 1), (2, 1, 63),
+             (3, 1000, 30)]
+    out2, pos2 = prefill(bi, q, kv, segs2)
+    sync_ok(bi)
+    assert pos2 == pos and np.array_equal(bits(out2), bits(out))
+
+
+# -------------------------------------------------------------- argmax --
+
+def test_argmax_exact(bi, orc):
+    T, V = 40, 128256
+    g = torch.Generator(device="cuda").manual_seed(51)
+    x = torch.randn(T, V, generator=g, device="cuda")
+    x[3, [100, 90000]] = 50.0          # tie: lower index
+    x[4, 777] = float("nan")
+    x[5, [10, 20]] = float("nan")      # first NaN
+    x[6] = 0.0
+    x[6, 0] = -0.0
+    x[7] = float("-inf")
+    x[8, -1] = float("inf")
+    ids = torch.empty(T, dtype=torch.int32, device="cuda")
+    bi.bi_argmax_logits(x, ids)
+    sync_ok(bi)
+    assert np.array_equal(ids.cpu().numpy(), orc.argmax(x.cpu().numpy()))
+    # rows are independent of the batch they are in
+    one = torch.empty(1, dtype=torch.int32, device="cuda")
+    bi.bi_argmax_logits(x[17:18].contiguous(), one)
+    sync_ok(bi)
+    assert one.item() == ids[17].item()
+    x2 = torch.randn(9, 513, generator=g, device="cuda")  # V % 4 != 0
+    ids2 = torch.empty(9, dtype=torch.int32, device="cuda")
+    bi.bi_argmax_logits(x2, ids2)
+    sync_ok(bi)
+    assert np.array_equal(ids2.cpu().numpy(), orc.argmax(x2.cpu().numpy()))
+
+
+# -------------------------------------------------------------- Philox --
+
+def test_philox_sample_against_oracle(bi, orc):
+    import oracle
+    T, V, tau = 3000, 512, 0.8
+    g = torch.Generator(device="cuda").manual_seed(61)
+    x = torch.randn(T, V, generator=g, device="cuda") * 2
+    rid = torch.arange(T, dtype=torch.int64, device="cuda") * 7919 + 3
+    step = torch.arange(T, dtype=torch.int64, device="cuda") % 37
+    ids = torch.empty(T, dtype=torch.int32, device="cuda")
+    bi.philox_sample(x, rid, step, tau, ids)
+    sync_ok(bi)
+    got = ids.cpu().numpy()
+    xl = x.cpu().numpy()
+    ref = orc.philox_sample(xl, rid.cpu().numpy().astype(np.uint64),
+                            step.cpu().numpy().astype(np.uint64), tau)
+    mism = np.nonzero(got != ref)[0]
+    assert len(mism) <= T // 100
+    # every disagreement sits on a CDF boundary within fp32 rounding
+    for t in mism:
+        p = np.exp((xl[t].astype(np.float64) - xl[t].max()) / tau)
+        cdf = np.cumsum(p)
+        u = oracle.sample_uniform(oracle.sample_seed(int(rid[t]),
+                                                      int(step[t])))
+        target = u * cdf[-1]
+        k = min(got[t], ref[t])
+        assert abs(cdf[k] - target) < 1e-4 * cdf[-1]
+    # temperature 0 is greedy
+    bi.philox_sample(x, rid, step, 0.0, ids)
+    sync_ok(bi)
+    assert np.array_equal(ids.cpu().numpy(), orc.argmax(xl))
+    # rows are independent of the batch
+    one = torch.empty(1, dtype=torch.int32, device="cuda")
+    bi.philox_sample(x[5:6].contiguous(), rid[5:6].contiguous(),
+                     step[5:6].contiguous(), tau, one)
+    sync_ok(bi)
+    assert one.item() == got[5]
