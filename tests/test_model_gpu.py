@@ -1,0 +1,363 @@
+"""Whole-model GPU tests.
+
+* The tiny random-init decoder: 8 requests with 16-token prompts decode 16
+  greedy tokens each, once one request at a time and once all together, with
+  the KV pages in a different random physical order each time.  Logits must
+  be bitwise identical (Vosti abstract; ybb.press section 8 item 1), and
+  agree with the oracle within a norm-wise relative error of 2e-2.
+* LLM-42 grouped verification ("LLM-42: Enabling Determinism in LLM
+  Inference with Verified Speculation", section "核心方法", paper sections
+  4.2-4.3): commit lengths equal the first perturbed index, the fix token is
+  the unperturbed token, the KV cache is cut back, and results do not depend
+  on how windows are grouped.
+* One Llama-3.1-8B-shaped layer in decode, against the oracle layer with
+  teacher forcing."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import bits, norm_rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from deterministic_invariant_bf16_gb300 import binding, build
+    build.build()
+    binding.lib()
+    return binding
+
+
+def np16(t):
+    return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def oracle_weights(w):
+    return dict(embed=np16(w["embed"]), final_norm=np16(w["final_norm"]),
+                lm_head=np16(w["lm_head"]),
+                layers=[{k: np16(v) for k, v in lw.items()}
+                        for lw in w["layers"]])
+
+
+@pytest.fixture(scope="module")
+def tiny(lib):
+    from deterministic_invariant_bf16_gb300 import engine, synth
+    w_cpu = synth.make_weights(synth.TINY, 0, "cpu")
+    return synth.TINY, w_cpu, engine.to_device(w_cpu)
+
+
+def new_engine(tiny, page_seed, n_slots=16, max_kv_len=128, n_pages=160):
+    from deterministic_invariant_bf16_gb300 import engine
+    shape, _, w = tiny
+    return engine.Engine(shape, w, max_tokens=256, max_kv_len=max_kv_len,
+                         n_slots=n_slots, n_pages=n_pages,
+                         page_seed=page_seed)
+
+
+def greedy_run(eng, prompts, n_new, groups):
+    """Prefill then decode n_new greedy tokens; returns per request the
+    logits rows [n_new, V] (the row whose argmax is each new token) and the
+    new tokens."""
+    R = len(prompts)
+    logits_out = [[] for _ in range(R)]
+    toks = [[] for _ in range(R)]
+    for group in groups:
+        for r in group:
+            eng.reserve(r, len(prompts[r]) + n_new)
+        lg = eng.prefill([(r, prompts[r], 0) for r in group])
+        last = np.cumsum([len(prompts[r]) for r in group]) - 1
+        ids = torch.empty(len(group), dtype=torch.int32, device="cuda")
+        # greedy ids of the last prompt rows through the library's argmax
+        from deterministic_invariant_bf16_gb300 import binding as bi
+        bi.bi_argmax_logits(lg[torch.from_numpy(last).cuda()].contiguous(),
+                            ids)
+        for i, r in enumerate(group):
+            logits_out[r].append(lg[last[i]].cpu().numpy())
+            toks[r].append(int(ids[i].item()))
+        for step in range(1, n_new):
+            cur = [toks[r][-1] for r in group]
+            pos = [len(prompts[r]) + step - 1 for r in group]
+            lg = eng.decode(cur, pos, list(group), ids=ids)
+            for i, r in enumerate(group):
+                logits_out[r].append(lg[i].cpu().numpy())
+                toks[r].append(int(ids[i].item()))
+    torch.cuda.synchronize()
+    return [np.stack(l) for l in logits_out], toks
+
+
+def prompts8(shape):
+    from deterministic_invariant_bf16_gb300 import synth
+    rng = np.random.default_rng(1001)
+    return [synth.token_ids(16, shape.vocab, rng) for _ in range(8)]
+
+
+def test_tiny_decoder_batch1_vs_batch8_permuted_pages(tiny, lib):
+    shape = tiny[0]
+    prompts = prompts8(shape)
+    eng1 = new_engine(tiny, page_seed=1)
+    l1, t1 = greedy_run(eng1, prompts, 16, [[r] for r in range(8)])
+    eng8 = new_engine(tiny, page_seed=2)
+    l8, t8 = greedy_run(eng8, prompts, 16, [list(range(8))])
+    assert t1 == t8
+    for r in range(8):
+        assert np.array_equal(l1[r].view(np.uint32), l8[r].view(np.uint32))
+    # a third run with yet another page order and batch split 3 + 5
+    eng3 = new_engine(tiny, page_seed=3)
+    l3, t3 = greedy_run(eng3, prompts, 16, [[5, 1, 7], [0, 2, 3, 4, 6]])
+    assert t3 == t8
+    for r in range(8):
+        assert np.array_equal(l3[r].view(np.uint32), l8[r].view(np.uint32))
+    assert lib.bi_device_status() == 0
+
+
+def test_tiny_decoder_matches_oracle(tiny, orc):
+    shape, w_cpu, _ = tiny
+    prompts = prompts8(shape)
+    eng = new_engine(tiny, page_seed=4)
+    lg, toks = greedy_run(eng, prompts, 16, [list(range(8))])
+    ow = oracle_weights(w_cpu)
+    cfg = orc.Cfg()
+    for r in range(8):
+        seq = list(prompts[r]) + toks[r][:-1]
+        caches = orc.new_caches(cfg, 1, len(seq) + 1)
+        ref = orc.model_forward(seq, np.zeros(len(seq), np.int32),
+                                np.arange(len(seq), dtype=np.int32), ow,
+                                caches, cfg)
+        ref = ref[len(prompts[r]) - 1:]
+        assert norm_rel_err(lg[r], ref) < 2e-2
+        # argmax of the GPU's logits, computed by the oracle: bit-exact ids
+        assert list(orc.argmax(lg[r])) == toks[r]
+
+
+def test_query_length_invariance_at_model_level(tiny):
+    """Feeding a prompt one token per decode call gives the same logits as
+    prefilling it in one call (prefill/decode invariance; Vosti abstract)."""
+    shape = tiny[0]
+    prompt = prompts8(shape)[3]
+    eng = new_engine(tiny, page_seed=5)
+    eng.reserve(0, 17)
+    whole = eng.prefill([(0, prompt, 0)]).cpu().numpy()
+    eng2 = new_engine(tiny, page_seed=6)
+    eng2.reserve(2, 17)
+    rows = []
+    for p, t in enumerate(prompt):
+        rows.append(eng2.decode([int(t)], [p], [2]).cpu().numpy()[0])
+    assert np.array_equal(np.stack(rows).view(np.uint32),
+                          whole.view(np.uint32))
+
+
+def test_repeated_runs_identical(tiny):
+    shape = tiny[0]
+    prompts = prompts8(shape)[:3]
+    a, _ = greedy_run(new_engine(tiny, 7), prompts, 4, [[0, 1, 2]])
+    b, _ = greedy_run(new_engine(tiny, 7), prompts, 4, [[0, 1, 2]])
+    for x, y in zip(a, b):
+        assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
+
+
+# ---------------------------------------------------------------- verify --
+
+def _decode_reference(tiny, prompts, n_new):
+    eng = new_engine(tiny, page_seed=11)
+    lg, toks = greedy_run(eng, prompts, n_new, [list(range(len(prompts)))])
+    return lg, toks
+
+
+@pytest.mark.parametrize("windows,group", [(32, None), (16, None), (64, None)])
+def test_verify_commit_rollback(tiny, orc, windows, group):
+    """Candidates are the invariant greedy tokens, with one token perturbed
+    in some windows.  j must equal the perturbed index (or w), the fix token
+    the original token, kv_len and the page table must be cut back."""
+    shape = tiny[0]
+    n_req = 256 // windows
+    from deterministic_invariant_bf16_gb300 import synth
+    rng = np.random.default_rng(2000 + windows)
+    prompts = [synth.token_ids(int(n), shape.vocab, rng)
+               for n in rng.integers(4, 20, size=n_req)]
+    n_new = windows + 8
+    ref_lg, ref_toks = _decode_reference(tiny, prompts, n_new)
+    eng = new_engine(tiny, page_seed=12, max_kv_len=128)
+    # committed: prompt + first k generated tokens; cache holds all but the
+    # last committed token.
+    ks = rng.integers(1, 8, size=n_req)
+    for r in range(n_req):
+        eng.reserve(r, len(prompts[r]) + n_new)
+        eng.prefill([(r, list(prompts[r]) + ref_toks[r][:ks[r] - 1], 0)])
+    pert = [int(rng.integers(0, windows)) if r % 3 != 2 else -1
+            for r in range(n_req)]
+    slots, kv, last, wins = [], [], [], []
+    for r in range(n_req):
+        committed = list(prompts[r]) + ref_toks[r][:ks[r]]
+        cand = list(ref_toks[r][ks[r]:ks[r] + windows])
+        if pert[r] >= 0:
+            cand[pert[r]] = (cand[pert[r]] + 1 + r) % shape.vocab
+        slots.append(r)
+        kv.append(len(committed) - 1)
+        last.append(committed[-1])
+        wins.append(cand)
+    logits = torch.empty(256, shape.vocab, dtype=torch.float32, device="cuda")
+    taken, commit, fix, freed = eng.verify(slots, kv, last, wins, logits)
+    assert taken == n_req
+    for r in range(n_req):
+        expect_j = pert[r] if pert[r] >= 0 else windows
+        j, new_len, fx, keep = orc.commit_rule(kv[r], wins[r], [
+            ref_toks[r][ks[r] + i] for i in range(windows)])
+        assert commit[r] == expect_j == j
+        assert fix[r] == fx
+        if expect_j < windows:
+            assert fix[r] == ref_toks[r][ks[r] + expect_j]
+    kvd = eng.kv_len.cpu().numpy()
+    table = eng.page_table.cpu().numpy()
+    for r in range(n_req):
+        assert kvd[r] == kv[r] + commit[r]
+        keep = -(-int(kvd[r]) // 16)
+        assert np.all(table[r, keep:] == -1) and np.all(table[r, :keep] >= 0)
+    # verify logits equal the invariant decode logits at the same positions,
+    # for every row whose inputs are unperturbed (rows up to the perturbed
+    # candidate)
+    lv = logits.cpu().numpy()
+    row = 0
+    for r in range(n_req):
+        upto = windows if pert[r] < 0 else pert[r] + 1
+        for i in range(upto):
+            want = ref_lg[r][ks[r] + i]
+            assert np.array_equal(lv[row + i].view(np.uint32),
+                                  want.view(np.uint32)), (r, i)
+        row += windows
+    # the oracle's commit rule on the GPU's verified ids: bit-exact
+    ver = orc.argmax(lv)
+    row = 0
+    for r in range(n_req):
+        j, _, fx, _ = orc.commit_rule(kv[r], wins[r], ver[row:row + windows])
+        assert (j, fx) == (commit[r], fix[r])
+        row += windows
+    # rollback then re-decode reproduces the fix token
+    for r in range(n_req):
+        if commit[r] < windows:
+            pos = kv[r] + commit[r]
+            tok = ([last[r]] + wins[r])[commit[r]]
+            eng.reserve(r, pos + 1)
+            ids = torch.empty(1, dtype=torch.int32, device="cuda")
+            eng.decode([tok], [pos], [r], ids=ids)
+            assert ids.item() == fix[r]
+
+
+def test_verify_grouping_invariance(tiny):
+    """The same windows packed in a different order / split over two verify
+    batches commit exactly the same (grouped verification keeps a fixed
+    shape; the result of a window must not depend on its neighbours)."""
+    shape = tiny[0]
+    from deterministic_invariant_bf16_gb300 import synth
+    rng = np.random.default_rng(3000)
+    n_req, w = 8, 24
+    prompts = [synth.token_ids(int(n), shape.vocab, rng)
+               for n in rng.integers(4, 12, size=n_req)]
+    _, ref_toks = _decode_reference(tiny, prompts, w + 4)
+    wins = []
+    for r in range(n_req):
+        c = list(ref_toks[r][1:1 + w])
+        c[(5 * r) % w] = (c[(5 * r) % w] + 3) % shape.vocab
+        wins.append(c)
+
+    def run(order, batches, seed):
+        eng = new_engine(tiny, page_seed=seed)
+        for r in range(n_req):
+            eng.reserve(r, len(prompts[r]) + w + 4)
+            eng.prefill([(r, list(prompts[r]), 0)])
+        res = {}
+        for part in np.array_split(np.array(order), batches):
+            part = list(part)
+            taken, commit, fix, _ = eng.verify(
+                part, [len(prompts[r]) for r in part],
+                [ref_toks[r][0] for r in part], [wins[r] for r in part])
+            assert taken == len(part)
+            for r, j, f in zip(part, commit, fix):
+                res[r] = (int(j), int(f))
+        return res
+
+    a = run(list(range(n_req)), 1, 21)
+    b = run(list(rng.permutation(n_req)), 2, 22)
+    assert a == b
+    assert all(a[r][0] == (5 * r) % w for r in range(n_req))
+
+
+# ------------------------------------------------------ one 8B layer --
+
+def test_one_8b_layer_decode_against_oracle(lib, orc):
+    """Config: Llama-3.1-8B layer (hidden 4096, 32/8 heads of 128, FFN
+    14336, theta 5e5), decode batch of 64 with lognormal contexts (median
+    512, sigma 1, clipped 16..4096), page size 16 in random order.  The layer
+    runs through the C ABI ops in model order; sampled rows are compared
+    with the oracle layer fed the same input and the same cache."""
+    from deterministic_invariant_bf16_gb300 import synth
+    bi = lib
+    S = synth.LLAMA8B
+    H, Hq, Hkv, D, F = S.hidden, S.n_heads, S.n_kv_heads, S.head_dim, S.ffn
+    B = 64
+    rng = np.random.default_rng(1003)
+    lens = synth.lognormal_lengths(B, 512, 1.0, 16, 4096, rng)
+    w = synth.make_weights(S, 3, "cuda", n_layers=1)["layers"][0]
+    table, n_pages = synth.paged_layout(lens, 16, rng, extra_pages=3)
+    kp = synth.normal_bf16((n_pages, Hkv, 16, D), 1.0, 77, "cuda")
+    vp = synth.normal_bf16((n_pages, Hkv, 16, D), 1.0, 78, "cuda")
+    pt = torch.from_numpy(table).cuda()
+    h_in = synth.normal_bf16((B, H), 1.0, 79, "cuda")
+    pos = torch.from_numpy((lens - 1).astype(np.int32)).cuda()
+    rows = torch.arange(B, dtype=torch.int32, device="cuda")
+    kvl = torch.from_numpy(lens.astype(np.int32)).cuda()
+    wgu = torch.empty(2 * F, H, dtype=torch.bfloat16, device="cuda")
+    bi.bi_pack_gate_up(w["wg"], w["wu"], wgu)
+
+    def gemm_slices(x, W):
+        M, K = x.shape
+        N = W.shape[0]
+        s = bi.bi_gemm_splits(N, K)
+        out = torch.empty(s, M, N, dtype=torch.float32, device="cuda")
+        bi.bi_gemm(x, W, out, bi.OUT_PARTIALS)
+        return out, s
+
+    h = h_in.clone()
+    x = torch.empty(B, H, dtype=torch.bfloat16, device="cuda")
+    bi.bi_rmsnorm(None, 0, None, h, w["attn_norm"], B, H, S.eps, x)
+    qkv, s1 = gemm_slices(x, w["wqkv"])
+    q = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
+    bi.bi_rope(qkv, s1, pos, rows, Hq, Hkv, D, S.theta, q, kp, vp, pt)
+    ws = torch.empty(bi.bi_decode_attn_workspace_size(B, Hq, D, 4096) // 4,
+                     dtype=torch.float32, device="cuda")
+    a = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
+    bi.bi_paged_decode_attn(q, kp, vp, pt, rows, kvl, 4096, 1 / math.sqrt(D),
+                            a, ws)
+    o, s2 = gemm_slices(a.view(B, Hq * D), w["wo"])
+    bi.bi_rmsnorm(o, s2, None, h, w["ffn_norm"], B, H, S.eps, x)
+    f = torch.empty(B, F, dtype=torch.bfloat16, device="cuda")
+    bi.bi_gemm(x, wgu, f, bi.OUT_SWIGLU)
+    d, s3 = gemm_slices(f, w["wd"])
+    y = torch.empty(B, H, dtype=torch.bfloat16, device="cuda")
+    bi.bi_rmsnorm(d, s3, None, h, w["attn_norm"], B, H, S.eps, y)
+    torch.cuda.synchronize()
+    assert bi.bi_device_status() == 0
+    h_out = orc.bf16_value(bits(h))
+
+    import oracle
+    cfg = oracle.Cfg(n_layers=1, hidden=H, n_heads=Hq, n_kv_heads=Hkv,
+                     head_dim=D, ffn=F, vocab=16, eps=S.eps, theta=S.theta)
+    lw = {k: np16(v) for k, v in w.items()}
+    kb, vb = bits(kp), bits(vp)
+    for b in (0, 17, 63):
+        L = int(lens[b])
+        kc = np.zeros((1, L, Hkv, D), np.float32)
+        vc = np.zeros_like(kc)
+        for p in range(L):
+            pg = table[b, p // 16]
+            kc[0, p] = orc.bf16_value(kb[pg, :, p % 16])
+            vc[0, p] = orc.bf16_value(vb[pg, :, p % 16])
+        ref = orc.decoder_layer(orc.bf16_value(bits(h_in[b:b + 1])),
+                                np.zeros(1, np.int32),
+                                np.array([L - 1], np.int32), lw, kc, vc, cfg)
+        assert norm_rel_err(h_out[b], ref[0]) < 1e-2
+        # the branch alone (h_out - h_in) must also agree closely
+        hin = orc.bf16_value(bits(h_in[b]))
+        assert norm_rel_err(h_out[b] - hin, ref[0] - hin) < 3e-2
