@@ -1,0 +1,696 @@
+#!/usr/bin/env python3
+"""Benchmark: batch-invariant decode tokens/s of a Llama-3.1-8B-shaped bf16
+decoder on one GB300, with the roofline fraction of the dominant kernel.
+
+Workload (LLM-42 grouped verification on the full 32-layer model; "LLM-42:
+Enabling Determinism in LLM Inference with Verified Speculation", sections
+4.3 and 5.1): 256 requests with ShareGPT-like lengths (prompts lognormal
+median 256 clipped 4..2048, outputs lognormal median 200 clipped 16..1024;
+each request is caught at a uniform point of its output), 10% of them flagged
+deterministic.  Random-init weights N(0, 0.02); the KV cache of the already
+processed tokens is N(0, 1) bf16 in randomly ordered 16-token pages.
+
+One step = 10 invariant decode iterations of all 256 requests (greedy for
+flagged requests, Philox temperature sampling keyed by (request, step) for
+the rest) followed by one fixed 256-row grouped verification of 8 flagged
+requests' 32-token candidate windows with commit and rollback.  Ten
+iterations per verify is the ratio 10% deterministic traffic implies
+(26 flagged requests x 10 tokens ~ one 256-row verify batch).  The metric
+counts decoded tokens: 10 x 256 per step.
+
+Run with no flags for one GPU.  Under torchrun (N > 1) every rank runs an
+independent replica (the path has no exchange step) and the line reports the
+aggregate over ranks with max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "batch-invariant decode tok/s (8B-shape bf16) + % of tensor/HBM roofline"
+UNIT = "tok/s"
+WORKLOAD = "llm42-grouped-verify-8b-decode"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--batch", type=int, default=256)
+    ap.add_argument("--iters", type=int, default=10)
+    ap.add_argument("--layers", type=int, default=32)
+    ap.add_argument("--no-comparator", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- workload --
+
+def make_workload(batch, iters, seed=1003):
+    from deterministic_invariant_bf16_gb300 import synth
+    rng = np.random.default_rng(seed)
+    prompts = synth.lognormal_lengths(batch, 256, 1.0, 4, 2048, rng)
+    outputs = synth.lognormal_lengths(batch, 200, 1.0, 16, 1024, rng)
+    progress = rng.uniform(0.0, 1.0, size=batch)
+    ctx = (prompts + np.floor(progress * outputs)).astype(np.int64)
+    n_flag = max(1, int(round(0.10 * batch)))
+    n_ver = min(8, n_flag)
+    window = 256 // n_ver
+    return dict(batch=batch, iters=iters, ctx=ctx, prompts=prompts,
+                outputs=outputs, n_flag=n_flag, n_ver=n_ver, window=window,
+                headroom=iters + window + 2,
+                first_tokens=synth.token_ids(batch, synth.LLAMA8B.vocab, rng),
+                rng=rng)
+
+
+# ------------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"),
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1])]
+        mx = [num(r[2]) for r in rows if num(r[2])]
+        power = [num(r[3]) for r in rows if num(r[3])]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# ------------------------------------------------------------------ helpers --
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return dict(hbm=p["hbm_gbs"], bf16=p["bf16_tflops"],
+                    bf16_sus=p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
+
+
+def src_hash(name):
+    path = os.path.join(ROOT, "deterministic_invariant_bf16_gb300", "csrc",
+                        name)
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def recorded_traffic(kernel_class):
+    """Per-launch DRAM bytes from the committed ncu summary for this kernel
+    class, or None when missing or when the kernel source has changed since
+    the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path)).get(kernel_class)
+    if not rec or rec.get("source_sha") != src_hash(rec["source"]):
+        return None
+    return rec.get("bytes_per_launch")
+
+
+def aggregate(ms_local, tokens_per_step_per_rank, world, dist=None,
+              device="cpu"):
+    """Replicas: every rank decodes its own requests; the step time is the
+    slowest rank's and the throughput counts every rank's tokens."""
+    ms = float(ms_local)
+    if world > 1 and dist is not None:
+        import torch
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, tokens_per_step_per_rank * world / (ms / 1000.0)
+
+
+# --------------------------------------------------------------- our arm ----
+
+class Bench:
+    def __init__(self, args, device):
+        import torch
+        from deterministic_invariant_bf16_gb300 import binding as bi
+        from deterministic_invariant_bf16_gb300 import engine, synth
+        self.torch, self.bi = torch, bi
+        self.args = args
+        self.dev = device
+        self.shape = synth.LLAMA8B
+        wl = make_workload(args.batch, args.iters)
+        self.wl = wl
+        B, it = wl["batch"], wl["iters"]
+        ctx = wl["ctx"]
+        max_kv = int(ctx.max()) + wl["headroom"]
+        need = int(sum(-(-(int(c) + wl["headroom"]) // 16) for c in ctx))
+        self.weights = synth.make_weights(self.shape, 4, device,
+                                          n_layers=args.layers)
+        self.eng = engine.Engine(self.shape, self.weights, max_tokens=256,
+                                 max_kv_len=max_kv, n_slots=B,
+                                 n_pages=need + 64, page_seed=5)
+        for r in range(B):
+            self.eng.reserve(r, int(ctx[r]) + wl["headroom"])
+        g = torch.Generator(device=device).manual_seed(6)
+        for kp, vp in zip(self.eng.k_pool, self.eng.v_pool):
+            kp.normal_(generator=g)
+            vp.normal_(generator=g)
+        i32 = dict(dtype=torch.int32, device=device)
+        self.slots = torch.arange(B, **i32)
+        self.tok0 = torch.from_numpy(wl["first_tokens"]).to(device)
+        self.pos = torch.stack([torch.from_numpy(ctx + i).to(device).int()
+                                for i in range(it)])
+        self.maxkv = [int(ctx.max()) + i + 1 for i in range(it)]
+        self.ids = torch.empty(it, B, **i32)
+        self.logits = torch.empty(B, self.shape.vocab, dtype=torch.float32,
+                                  device=device)
+        self.vlogits = torch.empty(bi.VERIFY_ROWS, self.shape.vocab,
+                                   dtype=torch.float32, device=device)
+        self.rid = torch.arange(B, dtype=torch.int64, device=device) + 1000
+        self.stepv = torch.stack([torch.from_numpy(ctx + i).to(device)
+                                  for i in range(it)]).long()
+        self.tau = 0.7
+        self.n_flag = wl["n_flag"]
+        self._make_candidates()
+
+    def decode_iters(self, n=None):
+        bi, eng = self.bi, self.eng
+        F = self.n_flag
+        for i in range(n or self.wl["iters"]):
+            src = self.tok0 if i == 0 else self.ids[i - 1]
+            eng.decode(src, self.pos[i], self.slots, logits=self.logits,
+                       max_kv_len=self.maxkv[i])
+            ids = self.ids[i]
+            bi.bi_argmax_logits(self.logits[:F], ids[:F])
+            bi.philox_sample(self.logits[F:], self.rid[F:],
+                             self.stepv[i % len(self.stepv)][F:], self.tau,
+                             ids[F:])
+
+    def _make_candidates(self):
+        """Candidate windows of the verified requests: their own invariant
+        greedy continuation (32 decode iterations run once here), with each
+        candidate perturbed with probability 0.003 to force mismatches."""
+        wl = self.wl
+        nv, w = wl["n_ver"], wl["window"]
+        ctx = wl["ctx"]
+        keep_pos, keep_maxkv = self.pos, self.maxkv
+        self.pos = self.torch.stack([self.torch.from_numpy(ctx + i).to(
+            self.dev).int() for i in range(w)])
+        self.maxkv = [int(ctx.max()) + i + 1 for i in range(w)]
+        keep_ids = self.ids
+        self.ids = self.torch.empty(w, wl["batch"], dtype=self.torch.int32,
+                                    device=self.dev)
+        self.decode_iters(w)
+        cand = self.ids[:, :nv].T.cpu().numpy().copy()
+        self.pos, self.maxkv, self.ids = keep_pos, keep_maxkv, keep_ids
+        rng = wl["rng"]
+        flip = rng.uniform(size=cand.shape) < 0.003
+        V = self.shape.vocab
+        cand[flip] = (cand[flip] + 1 + rng.integers(0, V - 1, size=flip.sum())) % V
+        self.cand = [list(map(int, c)) for c in cand]
+        self.v_slots = list(range(nv))
+        self.v_kv = [int(c) for c in ctx[:nv]]
+        self.v_last = [int(t) for t in wl["first_tokens"][:nv]]
+        self.commits = []
+
+    def verify(self):
+        wl = self.wl
+        taken, commit, fix, freed = self.eng.verify(
+            self.v_slots, self.v_kv, self.v_last, self.cand,
+            logits=self.vlogits)
+        self.commits.append((taken, commit.copy(), fix.copy()))
+        for r in self.v_slots:  # pages for the next step's positions
+            self.eng.reserve(r, int(wl["ctx"][r]) + wl["headroom"])
+
+    def step(self):
+        self.decode_iters()
+        self.verify()
+
+
+def algorithmic_bytes(b, cls, launches_per_step):
+    """Algorithmic bytes per launch of a kernel class in one step (HBM
+    traffic an ideal kernel must move)."""
+    wl, S = b.wl, b.shape
+    B, it = wl["batch"], wl["iters"]
+    H, F, D = S.hidden, S.ffn, S.head_dim
+    Hq, Hkv = S.n_heads, S.n_kv_heads
+    QKV = S.qkv_dim
+    ctx = wl["ctx"]
+    bi = b.bi
+    if cls == "attn":
+        # decode chunk kernel: K and V of every visible position, the
+        # queries, and one (m, l, o) partial per (row, head, chunk)
+        kv = sum(float((ctx + i + 1).sum()) for i in range(it)) / it
+        chunks = sum(float(np.ceil((ctx + i + 1) / 256).sum())
+                     for i in range(it)) / it
+        return (kv * Hkv * D * 2 * 2 + B * Hq * D * 2 +
+                chunks * Hq * (D + 4) * 4)
+    gemms = {"gemm_qkv": (QKV, H), "gemm_o": (H, Hq * D),
+             "gemm_gate_up": (2 * F, H), "gemm_down": (H, F),
+             "lm_head": (S.vocab, H)}
+    if cls in gemms:
+        N, K = gemms[cls]
+        s = bi.bi_gemm_splits(N, K)
+        out = B * N * 4 * s if cls in ("gemm_qkv", "gemm_o", "gemm_down") else (
+            B * N // 2 * 2 if cls == "gemm_gate_up" else B * N * 4)
+        return 2.0 * N * K + 2.0 * B * K + out
+    return None
+
+
+def gemm_flops(b, cls):
+    S = b.shape
+    B = b.wl["batch"]
+    dims = {"gemm_qkv": (S.qkv_dim, S.hidden), "gemm_o": (S.hidden, S.q_dim),
+            "gemm_gate_up": (2 * S.ffn, S.hidden),
+            "gemm_down": (S.hidden, S.ffn), "lm_head": (S.vocab, S.hidden)}
+    if cls not in dims:
+        return None
+    N, K = dims[cls]
+    return 2.0 * B * N * K
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = "cuda:%d" % local
+    from deterministic_invariant_bf16_gb300 import binding as bi
+    from deterministic_invariant_bf16_gb300 import build
+    build.build()
+    bi.lib()
+    b = Bench(args, dev)
+    B, it = b.wl["batch"], b.wl["iters"]
+    tokens_per_step = B * it
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        b.step()
+    torch.cuda.synchronize()
+    # ---- device-resident timed region (inputs are in HBM: weights 16 GB,
+    # KV ~20 GB, far beyond the 129 MB L2, so no flush is needed)
+    bi.bi_model_profile(b.eng.handle, True)
+    barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    stream = torch.cuda.current_stream()
+    e0.record(stream)
+    for _ in range(args.steps):
+        b.step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    prof = bi.bi_model_profile_read(b.eng.handle)
+    bi.bi_model_profile(b.eng.handle, False)
+    status = bi.bi_device_status()
+    ms, value = aggregate(ms, tokens_per_step, world,
+                          dist if world > 1 else None, dev)
+
+    # ---- end to end through the public API with host buffers: every step
+    # uploads its inputs from pinned host memory and reads back the tokens.
+    h_in_tok = b.tok0.cpu().pin_memory()
+    h_in_pos = b.pos.cpu().pin_memory()
+    h_in_step = b.stepv.cpu().pin_memory()
+    h_out = torch.empty(it, B, dtype=torch.int32).pin_memory()
+    bytes_in = (h_in_tok.numel() * 4 + h_in_pos.numel() * 4 +
+                h_in_step.numel() * 8)
+    bytes_out = h_out.numel() * 4
+    barrier()
+    torch.cuda.synchronize()
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(args.steps):
+        b.tok0.copy_(h_in_tok, non_blocking=True)
+        b.pos.copy_(h_in_pos, non_blocking=True)
+        b.stepv.copy_(h_in_step, non_blocking=True)
+        b.step()
+        h_out.copy_(b.ids, non_blocking=True)
+        stream.synchronize()
+    e3.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e, v_e2e = aggregate(e2.elapsed_time(e3) / args.steps,
+                              tokens_per_step, world,
+                              dist if world > 1 else None, dev)
+    e2e = {"value": v_e2e, "unit": UNIT,
+           "h2d_bytes_per_step": bytes_in,
+           "d2h_bytes_per_step": bytes_out + 3 * 4 * b.wl["n_ver"]}
+
+    # ---- roofline of the dominant kernel (largest share of device time)
+    pk = peaks()
+    shares = {k: v[0] for k, v in prof.items() if v[1] > 0}
+    dom = max(shares, key=shares.get)
+    n_launch = prof[dom][1]
+    avg_ms = prof[dom][0] / n_launch
+    flops = gemm_flops(b, dom)
+    ab = algorithmic_bytes(b, dom, n_launch / args.steps)
+    hbm_time = ab / (pk["hbm"] * 1e9) if ab else 0.0
+    ten_time = flops / (pk["bf16_sus"] * 1e12) if flops else 0.0
+    if flops and ten_time > hbm_time:
+        ach = flops / (avg_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": pk["bf16_sus"],
+                "unit": "TFLOP/s", "frac": ach / pk["bf16_sus"]}
+    else:
+        ach = ab / (avg_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": pk["hbm"],
+                "unit": "GB/s", "frac": ach / pk["hbm"]}
+    roof["traffic"] = recorded_traffic(dom)
+    roof["kernel"] = dom
+    roof["peak_source"] = pk["source"]
+    roof["algorithmic_bytes_per_launch"] = ab
+    roof["avg_launch_ms"] = avg_ms
+    total_ms = sum(v[0] for v in prof.values())
+    kernels = {}
+    for k, (kms, cnt) in prof.items():
+        if cnt == 0:
+            continue
+        entry = {"ms_per_step": kms / args.steps, "launches_per_step":
+                 cnt / args.steps, "share": kms / total_ms}
+        abk = algorithmic_bytes(b, k, cnt / args.steps)
+        if abk:
+            entry["GBps"] = abk / (kms / cnt / 1e3) / 1e9
+            entry["hbm_frac"] = entry["GBps"] / pk["hbm"]
+        fl = gemm_flops(b, k)
+        if fl:
+            entry["TFLOPs"] = fl / (kms / cnt / 1e3) / 1e12
+        kernels[k] = entry
+
+    launches = sum(v[1] for v in prof.values()) / args.steps
+    # kernels the profile does not bracket: per decode iteration the
+    # kv-length setup, the greedy argmax and the Philox sampler; per verify
+    # the commit kernel.  Every bracketed class is one kernel per launch.
+    launches += 3 * it + 1
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (random-init weights, random KV)",
+        "config": {"workload": WORKLOAD, "model": "llama-3.1-8b-shape",
+                   "layers": args.layers, "batch": B,
+                   "decode_iters_per_step": it,
+                   "verify_rows_per_step": 256,
+                   "verify_windows": "%d x %d" % (b.wl["n_ver"],
+                                                  b.wl["window"]),
+                   "deterministic_fraction": b.wl["n_flag"] / B,
+                   "mean_context": float(b.wl["ctx"].mean()),
+                   "l2": "inputs larger than L2 (weights + KV >> 129 MB)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "e2e": e2e,
+        "gpu_launches": int(round(launches * args.steps)),
+        "roofline": roof,
+        "kernels": kernels,
+        "clocks": clk,
+        "device_status": status,
+        "verify_commits": [int(x) for x in b.commits[-1][1]],
+    }
+    if rank == 0 and not args.no_comparator:
+        line["comparator"] = run_comparator(b, args)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args, b.wl, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------- comparator --
+
+def run_comparator(b, args):
+    """The same decode iterations with every GEMM through torch.matmul
+    (cuBLAS default heuristics), the library's norm / RoPE / attention /
+    argmax around them, against the invariant path's decode iterations alone.
+    Run with the default bf16 reduced-precision setting and with it off
+    (ybb.press section 5)."""
+    import torch
+    bi = b.bi
+    eng = b.eng
+    S = b.shape
+    B, it = b.wl["batch"], b.wl["iters"]
+    H, F, D, Hq, Hkv = S.hidden, S.ffn, S.head_dim, S.n_heads, S.n_kv_heads
+    dev = b.dev
+    x = torch.empty(B, H, dtype=torch.bfloat16, device=dev)
+    h = torch.empty(B, H, dtype=torch.bfloat16, device=dev)
+    q = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev)
+    a = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev)
+    kvl = torch.empty(B, dtype=torch.int32, device=dev)
+    ws = torch.empty(bi.bi_decode_attn_workspace_size(
+        B, Hq, D, eng.max_kv_len) // 4, dtype=torch.float32, device=dev)
+    W = b.weights
+    scale = 1.0 / math.sqrt(D)
+
+    def fwd(tok, pos, maxkv):
+        torch.index_select(W["embed"], 0, tok, out=h)
+        kvl.copy_(pos + 1)
+        d = None
+        for l, lw in enumerate(W["layers"]):
+            if d is None:
+                bi.bi_rmsnorm(None, 0, None, h, lw["attn_norm"], B, H, S.eps, x)
+            else:
+                bi.bi_rmsnorm(d, 1, None, h, lw["attn_norm"], B, H, S.eps, x)
+            qkv = torch.matmul(x, lw["wqkv"].T).float()
+            bi.bi_rope(qkv, 1, pos, b.slots, Hq, Hkv, D, S.theta, q,
+                       eng.k_pool[l], eng.v_pool[l], eng.page_table)
+            bi.bi_paged_decode_attn(q, eng.k_pool[l], eng.v_pool[l],
+                                    eng.page_table, b.slots, kvl, maxkv, scale,
+                                    a, ws)
+            o = torch.matmul(a.view(B, Hq * D), lw["wo"].T).float()
+            bi.bi_rmsnorm(o, 1, None, h, lw["ffn_norm"], B, H, S.eps, x)
+            g = torch.matmul(x, lw["wg"].T)
+            u = torch.matmul(x, lw["wu"].T)
+            f = torch.nn.functional.silu(g) * u
+            d = torch.matmul(f, lw["wd"].T).float()
+        bi.bi_rmsnorm(d, 1, None, h, W["final_norm"], B, H, S.eps, x)
+        return torch.matmul(x, W["lm_head"].T).float()
+
+    def run_cmp():
+        cur = b.tok0.clone()
+        for i in range(it):
+            lg = fwd(cur, b.pos[i], b.maxkv[i])
+            ids = b.ids[i]
+            bi.bi_argmax_logits(lg, ids)
+            cur = ids
+
+    def timed(fn, reps):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    reps = max(2, min(args.steps, 4))
+    ours_ms = timed(b.decode_iters, reps)
+    out = {"what": "same decode iterations, GEMMs via torch.matmul (cuBLAS)",
+           "invariant_decode_tok_s": B * it / (ours_ms / 1e3)}
+    flag = torch.backends.cuda.matmul.allow_bf16_reduced_precision_reduction
+    for name, val in (("cublas_default", flag), ("cublas_no_reduced_bf16", False)):
+        torch.backends.cuda.matmul.allow_bf16_reduced_precision_reduction = val
+        cms = timed(run_cmp, reps)
+        out[name + "_tok_s"] = B * it / (cms / 1e3)
+    torch.backends.cuda.matmul.allow_bf16_reduced_precision_reduction = flag
+    out["invariant_over_default"] = (out["invariant_decode_tok_s"] /
+                                     out["cublas_default_tok_s"])
+    return out
+
+
+# -------------------------------------------------------------- CPU oracle --
+
+_ORACLE_W = {}
+
+
+def oracle_weights():
+    """One random 8B-shape layer, the final norm, the LM head and embedding
+    rows, generated once on the host (bf16 bit patterns)."""
+    if not _ORACLE_W:
+        import torch
+        from deterministic_invariant_bf16_gb300 import synth
+        S = synth.LLAMA8B
+
+        def u16(t):
+            return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+        w = synth.make_weights(synth.ModelShape(
+            n_layers=1, hidden=S.hidden, n_heads=S.n_heads,
+            n_kv_heads=S.n_kv_heads, head_dim=S.head_dim, ffn=S.ffn,
+            vocab=256, eps=S.eps, theta=S.theta), 7, "cpu")
+        _ORACLE_W["layer"] = {k: u16(v) for k, v in w["layers"][0].items()}
+        _ORACLE_W["final_norm"] = u16(w["final_norm"])
+        _ORACLE_W["embed"] = u16(w["embed"])
+        _ORACLE_W["lm_head"] = u16(synth.normal_bf16((S.vocab, S.hidden),
+                                                     0.02, 9, "cpu"))
+    return _ORACLE_W
+
+
+def oracle_sample(wl, seconds, n_layers=32, max_requests=16):
+    """Time the oracle on a bounded sample of the workload: one decode token
+    for each of a few requests through the full layer stack and LM head.
+    One random layer's weights serve every layer (the oracle's cost does not
+    depend on the values); each request's cache holds random bf16 values."""
+    import oracle
+    from deterministic_invariant_bf16_gb300 import synth
+    S = synth.LLAMA8B
+    cfg = oracle.Cfg(n_layers=n_layers, hidden=S.hidden, n_heads=S.n_heads,
+                     n_kv_heads=S.n_kv_heads, head_dim=S.head_dim, ffn=S.ffn,
+                     vocab=S.vocab, eps=S.eps, theta=S.theta)
+    W = oracle_weights()
+    lw, lm, fnorm, emb = W["layer"], W["lm_head"], W["final_norm"], W["embed"]
+    rng = np.random.default_rng(8)
+    ctx = wl["ctx"]
+    # requests spread over the context distribution (the median alone when
+    # only one is asked for)
+    srt = np.argsort(ctx)
+    if max_requests == 1:
+        order = srt[[len(ctx) // 2]]
+    else:
+        order = srt[np.linspace(0, len(ctx) - 1, max_requests).astype(int)]
+    done, t_compute = 0, 0.0
+    for r in order:
+        L = int(ctx[r])
+        h = oracle.bf16_value(emb[[int(wl["first_tokens"][r]) % emb.shape[0]]])
+        for _ in range(n_layers):
+            kc = oracle.bf16r(rng.standard_normal((1, L + 1, S.n_kv_heads,
+                                                   S.head_dim), np.float32))
+            vc = oracle.bf16r(rng.standard_normal(kc.shape, np.float32))
+            t0 = time.perf_counter()
+            h = oracle.decoder_layer(h, np.zeros(1, np.int32),
+                                     np.array([L], np.int32), lw, kc, vc, cfg)
+            t_compute += time.perf_counter() - t0
+        t0 = time.perf_counter()
+        x = oracle.bf16_bits(oracle.rmsnorm(h, fnorm, cfg.eps))
+        logits = oracle.gemm(x, lm)
+        oracle.argmax(logits)
+        t_compute += time.perf_counter() - t0
+        done += 1
+        if t_compute >= seconds:
+            break
+    return done, t_compute
+
+
+def cpu_baseline(args, wl, seconds):
+    done, t = oracle_sample(wl, seconds, n_layers=args.layers)
+    cores = len(os.sched_getaffinity(0))
+    return {"value": done / t, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "threads": int(os.environ.get("OMP_NUM_THREADS", cores)),
+            "sample": "%d decode tokens (one per request, contexts spread over "
+                      "the workload), %d layers + LM head, %.1f s of oracle "
+                      "compute" % (done, args.layers, t)}
+
+
+def run_reference(args):
+    """The oracle arm: the CPU oracle, as it stands, on the host cores; each
+    step is one decode token of one request through the full model."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = make_workload(args.batch, args.iters)
+    from oracle import build as obuild
+    obuild.build()
+    for _ in range(args.warmup):
+        oracle_sample(wl, 0.0, n_layers=args.layers, max_requests=1)
+    t_tot, n_tot = 0.0, 0
+    for _ in range(args.steps):
+        n, t = oracle_sample(wl, 0.0, n_layers=args.layers, max_requests=1)
+        t_tot += t
+        n_tot += n
+    value = n_tot / t_tot
+    cores = len(os.sched_getaffinity(0))
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "impl": "reference",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * t_tot / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "model": "llama-3.1-8b-shape",
+                       "layers": args.layers, "batch": args.batch},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores,
+                             "kind": "oracle",
+                             "sample": "one decode token of one request per "
+                                       "step, full layer stack + LM head"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -82,6 +82,9 @@ SIGNATURES = {
                          ctypes.POINTER(V)], I),
     "bi_model_destroy": ([V], None),
     "bi_model_forward": ([V, I, V, V, V, I, V, V, I, I, V, V, V, V], I),
+    "bi_model_profile": ([V, I], I),
+    "bi_model_profile_read": ([V, ctypes.POINTER(ctypes.c_double),
+                               ctypes.POINTER(ctypes.c_int64)], I),
     "verify_commit_rollback": ([V, I, I32P, I32P, I32P, I32P, I32P, V, V,
                                 I32P, I32P, I32P, I, I32P, I32P, V, V], I),
 }
@@ -248,6 +251,24 @@ def bi_model_forward(handle, tokens, pos, row_req, cu_q, seg_req, max_q,
                                   R, _p(cu_q), _p(seg_req), max_q, max_kv_len,
                                   _p(page_table), _p(logits), _p(ids),
                                   _stream(stream)))
+
+
+PROF_CLASSES = ["attn", "attn_merge", "gemm_qkv", "gemm_o", "gemm_gate_up",
+                "gemm_down", "lm_head", "norm", "rope", "other",
+                "attn_prefill"]
+
+
+def bi_model_profile(handle, enable):
+    _check(lib().bi_model_profile(handle, 1 if enable else 0))
+
+
+def bi_model_profile_read(handle):
+    """Returns {class name: (milliseconds, launches)}."""
+    n = len(PROF_CLASSES)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    _check(lib().bi_model_profile_read(handle, ms, cnt))
+    return {name: (ms[i], cnt[i]) for i, name in enumerate(PROF_CLASSES)}
 
 
 def verify_commit_rollback(handle, req, kv_len_host, last_token, win_len,

@@ -511,11 +511,16 @@ extern "C" size_t bi_decode_attn_workspace_size(int B, int Hq, int D,
     return (size_t)B * Hq * C * (D + 4) * sizeof(float);
 }
 
-extern "C" bi_status bi_paged_decode_attn(
-    const bi_bf16 *q, const bi_bf16 *k_pool, const bi_bf16 *v_pool,
-    const int32_t *page_table, int max_pages, const int32_t *row_req,
-    const int32_t *kv_len, int B, int max_kv_len, int Hq, int Hkv, int D,
-    float scale, bi_bf16 *out, void *ws, size_t ws_bytes, void *stream) {
+// Decode attention with the pool size known (page ids are range-checked
+// against it).  stages: bit 0 runs the chunk kernel, bit 1 the merge.
+bi_status bi_decode_attn_pool(const bi_bf16 *q, const bi_bf16 *k_pool,
+                              const bi_bf16 *v_pool, const int32_t *page_table,
+                              int max_pages, int n_pages,
+                              const int32_t *row_req, const int32_t *kv_len,
+                              int B, int max_kv_len, int Hq, int Hkv, int D,
+                              float scale, bi_bf16 *out, void *ws,
+                              size_t ws_bytes, int stages,
+                              cudaStream_t s) {
     BI_REQUIRE(B >= 0 && max_kv_len > 0 && max_kv_len <= 16 * max_pages,
                "bi_paged_decode_attn: B=%d max_kv_len=%d max_pages=%d", B,
                max_kv_len, max_pages);
@@ -535,39 +540,58 @@ extern "C" bi_status bi_paged_decode_attn(
         return bi_fail(BI_ERR_WORKSPACE_TOO_SMALL,
                        "bi_paged_decode_attn: workspace %zu < %zu", ws_bytes,
                        need);
-    // Pool size in pages is not passed here; bounds on page ids are checked
-    // against INT32_MAX only (the model driver passes the real count).
-    const int n_pages = 0x7fffffff;
     const int Cmax = (max_kv_len + CHUNK - 1) / CHUNK;
     const int G = Hq / Hkv;
-    cudaStream_t s = bi_stream(stream);
     int32_t *status = bi_status_ptr();
-    dim3 grid(Cmax, Hkv, B);
-    bi_status st;
-    if (D == 128) {
-        static std::once_flag f;
-        static bi_status fs;
-        std::call_once(f, [] { fs = set_attr(decode_chunk_kernel<128>, Smem<128>::BYTES); });
-        if ((st = fs) != BI_OK) return st;
-        decode_chunk_kernel<128><<<grid, ATT_THREADS, Smem<128>::BYTES, s>>>(
-            q, k_pool, v_pool, page_table, max_pages, n_pages, row_req, kv_len,
-            Hq, Hkv, G, scale, static_cast<float *>(ws), Cmax, status);
-    } else {
-        decode_chunk_kernel<32><<<grid, ATT_THREADS, Smem<32>::BYTES, s>>>(
-            q, k_pool, v_pool, page_table, max_pages, n_pages, row_req, kv_len,
-            Hq, Hkv, G, scale, static_cast<float *>(ws), Cmax, status);
+    if (stages & 1) {
+        dim3 grid(Cmax, Hkv, B);
+        if (D == 128) {
+            static std::once_flag f;
+            static bi_status fs;
+            std::call_once(f, [] {
+                fs = set_attr(decode_chunk_kernel<128>, Smem<128>::BYTES);
+            });
+            if (fs != BI_OK) return fs;
+            decode_chunk_kernel<128><<<grid, ATT_THREADS, Smem<128>::BYTES, s>>>(
+                q, k_pool, v_pool, page_table, max_pages, n_pages, row_req,
+                kv_len, Hq, Hkv, G, scale, static_cast<float *>(ws), Cmax,
+                status);
+        } else {
+            decode_chunk_kernel<32><<<grid, ATT_THREADS, Smem<32>::BYTES, s>>>(
+                q, k_pool, v_pool, page_table, max_pages, n_pages, row_req,
+                kv_len, Hq, Hkv, G, scale, static_cast<float *>(ws), Cmax,
+                status);
+        }
+        BI_LAUNCH_CHECK("decode attention launch");
     }
-    BI_LAUNCH_CHECK("decode attention launch");
-    const int warps = B * Hq;
-    const int blocks = (warps * 32 + 255) / 256;
-    if (D == 128)
-        decode_merge_kernel<128><<<blocks, 256, 0, s>>>(
-            static_cast<const float *>(ws), kv_len, row_req, B, Hq, Cmax, out);
-    else
-        decode_merge_kernel<32><<<blocks, 256, 0, s>>>(
-            static_cast<const float *>(ws), kv_len, row_req, B, Hq, Cmax, out);
-    BI_LAUNCH_CHECK("decode merge launch");
+    if (stages & 2) {
+        const int warps = B * Hq;
+        const int blocks = (warps * 32 + 255) / 256;
+        if (D == 128)
+            decode_merge_kernel<128><<<blocks, 256, 0, s>>>(
+                static_cast<const float *>(ws), kv_len, row_req, B, Hq, Cmax,
+                out);
+        else
+            decode_merge_kernel<32><<<blocks, 256, 0, s>>>(
+                static_cast<const float *>(ws), kv_len, row_req, B, Hq, Cmax,
+                out);
+        BI_LAUNCH_CHECK("decode merge launch");
+    }
     return BI_OK;
+}
+
+extern "C" bi_status bi_paged_decode_attn(
+    const bi_bf16 *q, const bi_bf16 *k_pool, const bi_bf16 *v_pool,
+    const int32_t *page_table, int max_pages, const int32_t *row_req,
+    const int32_t *kv_len, int B, int max_kv_len, int Hq, int Hkv, int D,
+    float scale, bi_bf16 *out, void *ws, size_t ws_bytes, void *stream) {
+    // The pool size is not an argument of this entry point, so page ids are
+    // range-checked against INT32_MAX only; the model driver passes the
+    // real pool size.
+    return bi_decode_attn_pool(q, k_pool, v_pool, page_table, max_pages,
+                               0x7fffffff, row_req, kv_len, B, max_kv_len, Hq,
+                               Hkv, D, scale, out, ws, ws_bytes, 3,
+                               bi_stream(stream));
 }
 
 bi_status bi_prefill_attn_pool(const bi_bf16 *q, const int32_t *cu_q,

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "../../include/bi.h"
@@ -23,3 +24,20 @@ bi_status bi_make_tmap_2d_bf16(CUtensorMap *map, const void *base,
 bi_status bi_gemm_sched(const bi_bf16 *x, int M, int K, const bi_bf16 *W,
                         int N, void *out, int out_kind, void *ws,
                         size_t ws_bytes, int mode, cudaStream_t stream);
+
+// Attention with the KV pool size known, for the model driver.
+bi_status bi_decode_attn_pool(const bi_bf16 *q, const bi_bf16 *k_pool,
+                              const bi_bf16 *v_pool, const int32_t *page_table,
+                              int max_pages, int n_pages,
+                              const int32_t *row_req, const int32_t *kv_len,
+                              int B, int max_kv_len, int Hq, int Hkv, int D,
+                              float scale, bi_bf16 *out, void *ws,
+                              size_t ws_bytes, int stages, cudaStream_t s);
+bi_status bi_prefill_attn_pool(const bi_bf16 *q, const int32_t *cu_q,
+                               const int32_t *seg_req, int R, int T,
+                               const int32_t *pos, int max_q, int max_kv_len,
+                               const bi_bf16 *k_pool, const bi_bf16 *v_pool,
+                               const int32_t *page_table, int max_pages,
+                               int n_pages, int Hq, int Hkv, int D,
+                               float scale, bi_bf16 *out, cudaStream_t stream);
+bool bi_gemm_default_fused(int M, int N, int K);

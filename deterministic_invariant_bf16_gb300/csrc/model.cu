@@ -24,16 +24,36 @@
 #include "common.cuh"
 #include "internal.h"
 
-bi_status bi_prefill_attn_pool(const bi_bf16 *q, const int32_t *cu_q,
-                               const int32_t *seg_req, int R, int T,
-                               const int32_t *pos, int max_q, int max_kv_len,
-                               const bi_bf16 *k_pool, const bi_bf16 *v_pool,
-                               const int32_t *page_table, int max_pages,
-                               int n_pages, int Hq, int Hkv, int D,
-                               float scale, bi_bf16 *out, cudaStream_t stream);
-bool bi_gemm_default_fused(int M, int N, int K);
-
 namespace {
+
+// Per-kernel-class event timing (bi_model_profile).  Events come from a pool
+// that grows on first use and is reused by later measurement windows.
+struct Profiler {
+    bool on = false;
+    std::vector<cudaEvent_t> ev;
+    size_t next = 0;
+    std::vector<std::pair<int, size_t>> marks;  // (class, start index)
+
+    int begin(cudaStream_t s) {
+        if (!on) return -1;
+        while (ev.size() < next + 2) {
+            cudaEvent_t e;
+            if (cudaEventCreate(&e) != cudaSuccess) return -1;
+            ev.push_back(e);
+        }
+        cudaEventRecord(ev[next], s);
+        return (int)next;
+    }
+    void end(int cls, int start, cudaStream_t s) {
+        if (start < 0) return;
+        cudaEventRecord(ev[start + 1], s);
+        marks.emplace_back(cls, (size_t)start);
+        next = start + 2;
+    }
+    ~Profiler() {
+        for (cudaEvent_t e : ev) cudaEventDestroy(e);
+    }
+};
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -151,7 +171,36 @@ struct bi_model {
     const bi_bf16 *embed, *final_norm, *lm_head;
     std::vector<const bi_bf16 *> attn_norm, wqkv, wo, ffn_norm, wgu, wd;
     std::vector<bi_bf16 *> kpool, vpool;
+    Profiler prof;
 };
+
+extern "C" bi_status bi_model_profile(bi_model *m, int enable) {
+    BI_REQUIRE(m, "bi_model_profile: null model");
+    m->prof.on = enable != 0;
+    m->prof.next = 0;
+    m->prof.marks.clear();
+    return BI_OK;
+}
+
+extern "C" bi_status bi_model_profile_read(bi_model *m, double *h_ms,
+                                           int64_t *h_launches) {
+    BI_REQUIRE(m && h_ms && h_launches, "bi_model_profile_read: null pointer");
+    for (int c = 0; c < BI_PROF_CLASSES; ++c) {
+        h_ms[c] = 0.0;
+        h_launches[c] = 0;
+    }
+    for (auto &mk : m->prof.marks) {
+        cudaEvent_t a = m->prof.ev[mk.second], b = m->prof.ev[mk.second + 1];
+        bi_status st = bi_cuda_check(cudaEventSynchronize(b), "profile sync");
+        if (st != BI_OK) return st;
+        float ms = 0.f;
+        st = bi_cuda_check(cudaEventElapsedTime(&ms, a, b), "profile elapsed");
+        if (st != BI_OK) return st;
+        h_ms[mk.first] += ms;
+        h_launches[mk.first] += 1;
+    }
+    return BI_OK;
+}
 
 static bi_status check_cfg(const bi_model_cfg *c) {
     BI_REQUIRE(c, "bi_model: null cfg");
@@ -283,7 +332,16 @@ extern "C" bi_status bi_model_forward(bi_model *m, int T, const int32_t *tokens,
         if ((st = (expr)) != BI_OK) return st; \
     } while (0)
 
-    BI_TRY(bi_embed(tokens, T, m->embed, c.vocab, H, h, s));
+    Profiler &P = m->prof;
+    int ev;
+#define BI_TIMED(cls, expr)           \
+    do {                              \
+        ev = P.begin(s);              \
+        BI_TRY(expr);                 \
+        P.end((cls), ev, s);          \
+    } while (0)
+
+    BI_TIMED(BI_PROF_OTHER, bi_embed(tokens, T, m->embed, c.vocab, H, h, s));
     if (R == 0) {
         kvlen_kernel<<<(T + 255) / 256, 256, 0, s>>>(pos, T, kvlen);
         BI_LAUNCH_CHECK("kvlen launch");
@@ -291,37 +349,60 @@ extern "C" bi_status bi_model_forward(bi_model *m, int T, const int32_t *tokens,
     int s_d = 0;
     for (int l = 0; l < c.n_layers; ++l) {
         if (l == 0)
-            BI_TRY(bi_rmsnorm(nullptr, 0, nullptr, h, m->attn_norm[l], T, H,
-                              c.eps, x, s));
+            BI_TIMED(BI_PROF_NORM,
+                     bi_rmsnorm(nullptr, 0, nullptr, h, m->attn_norm[l], T, H,
+                                c.eps, x, s));
         else
-            BI_TRY(bi_rmsnorm(d, s_d, nullptr, h, m->attn_norm[l], T, H, c.eps,
-                              x, s));
+            BI_TIMED(BI_PROF_NORM, bi_rmsnorm(d, s_d, nullptr, h,
+                                              m->attn_norm[l], T, H, c.eps, x,
+                                              s));
         int s_qkv = 0, s_o = 0;
-        BI_TRY(gemm_slices(x, T, H, m->wqkv[l], QKV, qkv, &s_qkv, s));
-        BI_TRY(bi_rope(qkv, s_qkv, pos, row_req, T, Hq, Hkv, D, c.theta, q,
-                       m->kpool[l], m->vpool[l], page_table, c.max_pages,
-                       c.n_pages, s));
-        if (R == 0)
-            BI_TRY(bi_paged_decode_attn(q, m->kpool[l], m->vpool[l],
-                                        page_table, c.max_pages, row_req,
-                                        kvlen, T, max_kv_len, Hq, Hkv, D,
-                                        scale, attn, att_ws, att_ws_bytes, s));
-        else
-            BI_TRY(bi_prefill_attn_pool(q, cu_q, seg_req, R, T, pos, max_q,
-                                        max_kv_len, m->kpool[l], m->vpool[l],
-                                        page_table, c.max_pages, c.n_pages, Hq,
-                                        Hkv, D, scale, attn, s));
-        BI_TRY(gemm_slices(attn, T, QD, m->wo[l], H, o, &s_o, s));
-        BI_TRY(bi_rmsnorm(o, s_o, nullptr, h, m->ffn_norm[l], T, H, c.eps, x,
-                          s));
-        BI_TRY(bi_gemm_sched(x, T, H, m->wgu[l], 2 * F, f, BI_OUT_SWIGLU,
-                             nullptr, 0, 0, s));
-        BI_TRY(gemm_slices(f, T, F, m->wd[l], H, d, &s_d, s));
+        BI_TIMED(BI_PROF_GEMM_QKV,
+                 gemm_slices(x, T, H, m->wqkv[l], QKV, qkv, &s_qkv, s));
+        BI_TIMED(BI_PROF_ROPE,
+                 bi_rope(qkv, s_qkv, pos, row_req, T, Hq, Hkv, D, c.theta, q,
+                         m->kpool[l], m->vpool[l], page_table, c.max_pages,
+                         c.n_pages, s));
+        if (R == 0) {
+            BI_TIMED(BI_PROF_ATTN,
+                     bi_decode_attn_pool(q, m->kpool[l], m->vpool[l],
+                                         page_table, c.max_pages, c.n_pages,
+                                         row_req, kvlen, T, max_kv_len, Hq,
+                                         Hkv, D, scale, attn, att_ws,
+                                         att_ws_bytes, 1, s));
+            BI_TIMED(BI_PROF_ATTN_MERGE,
+                     bi_decode_attn_pool(q, m->kpool[l], m->vpool[l],
+                                         page_table, c.max_pages, c.n_pages,
+                                         row_req, kvlen, T, max_kv_len, Hq,
+                                         Hkv, D, scale, attn, att_ws,
+                                         att_ws_bytes, 2, s));
+        } else {
+            BI_TIMED(BI_PROF_ATTN_PREFILL,
+                     bi_prefill_attn_pool(q, cu_q, seg_req, R, T, pos, max_q,
+                                          max_kv_len, m->kpool[l],
+                                          m->vpool[l], page_table, c.max_pages,
+                                          c.n_pages, Hq, Hkv, D, scale, attn,
+                                          s));
+        }
+        BI_TIMED(BI_PROF_GEMM_O,
+                 gemm_slices(attn, T, QD, m->wo[l], H, o, &s_o, s));
+        BI_TIMED(BI_PROF_NORM, bi_rmsnorm(o, s_o, nullptr, h, m->ffn_norm[l],
+                                          T, H, c.eps, x, s));
+        BI_TIMED(BI_PROF_GEMM_GATE_UP,
+                 bi_gemm_sched(x, T, H, m->wgu[l], 2 * F, f, BI_OUT_SWIGLU,
+                               nullptr, 0, 0, s));
+        BI_TIMED(BI_PROF_GEMM_DOWN,
+                 gemm_slices(f, T, F, m->wd[l], H, d, &s_d, s));
     }
-    BI_TRY(bi_rmsnorm(d, s_d, nullptr, h, m->final_norm, T, H, c.eps, x, s));
-    BI_TRY(bi_gemm_sched(x, T, H, m->lm_head, c.vocab, logits, BI_OUT_F32,
-                         nullptr, 0, 0, s));
-    if (ids) BI_TRY(bi_argmax_logits(logits, T, c.vocab, ids, s));
+    BI_TIMED(BI_PROF_NORM, bi_rmsnorm(d, s_d, nullptr, h, m->final_norm, T, H,
+                                      c.eps, x, s));
+    BI_TIMED(BI_PROF_LM_HEAD,
+             bi_gemm_sched(x, T, H, m->lm_head, c.vocab, logits, BI_OUT_F32,
+                           nullptr, 0, 0, s));
+    if (ids)
+        BI_TIMED(BI_PROF_OTHER,
+                 bi_argmax_logits(logits, T, c.vocab, ids, s));
+#undef BI_TIMED
 #undef BI_TRY
     return BI_OK;
 }

@@ -283,6 +283,34 @@ bi_status bi_model_forward(bi_model *m, int T, const int32_t *tokens,
                            const int32_t *page_table, float *logits,
                            int32_t *ids, void *stream);
 
+/* Per-kernel-class timing of bi_model_forward for roofline accounting:
+ * while enabled, every launch of a class is bracketed by CUDA events recorded
+ * on the forward's stream (events are created by the library on first use
+ * and reused; no device memory is allocated).  bi_model_profile(m, 1) opens
+ * a new measurement window, bi_model_profile(m, 0) stops recording.
+ * bi_model_profile_read waits for the recorded events and writes, per class,
+ * the summed device milliseconds and the launch count into host arrays of
+ * BI_PROF_CLASSES entries.  Classes: */
+enum {
+    BI_PROF_ATTN = 0,         /* decode chunk kernel */
+    BI_PROF_ATTN_MERGE = 1,   /* decode chunk merge */
+    BI_PROF_GEMM_QKV = 2,
+    BI_PROF_GEMM_O = 3,
+    BI_PROF_GEMM_GATE_UP = 4, /* with the SwiGLU epilogue */
+    BI_PROF_GEMM_DOWN = 5,
+    BI_PROF_LM_HEAD = 6,
+    BI_PROF_NORM = 7,         /* RMSNorm with the fused split reduction */
+    BI_PROF_ROPE = 8,         /* RoPE, QKV reduction and KV append */
+    BI_PROF_OTHER = 9,        /* embedding gather, argmax */
+    BI_PROF_ATTN_PREFILL = 10, /* prefill / verify attention */
+    BI_PROF_CLASSES = 11
+};
+
+bi_status bi_model_profile(bi_model *m, int enable);
+
+bi_status bi_model_profile_read(bi_model *m, double *h_ms,
+                                int64_t *h_launches);
+
 /* --------------------------------------------------- LLM-42 verification --
  * Grouped verification with commit and rollback ("LLM-42: Enabling
  * Determinism in LLM Inference with Verified Speculation", section

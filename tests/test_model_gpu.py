@@ -325,11 +325,12 @@ def test_one_8b_layer_decode_against_oracle(lib, orc):
     qkv, s1 = gemm_slices(x, w["wqkv"])
     q = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
     bi.bi_rope(qkv, s1, pos, rows, Hq, Hkv, D, S.theta, q, kp, vp, pt)
-    ws = torch.empty(bi.bi_decode_attn_workspace_size(B, Hq, D, 4096) // 4,
+    max_kv = int(lens.max())
+    ws = torch.empty(bi.bi_decode_attn_workspace_size(B, Hq, D, max_kv) // 4,
                      dtype=torch.float32, device="cuda")
     a = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
-    bi.bi_paged_decode_attn(q, kp, vp, pt, rows, kvl, 4096, 1 / math.sqrt(D),
-                            a, ws)
+    bi.bi_paged_decode_attn(q, kp, vp, pt, rows, kvl, max_kv,
+                            1 / math.sqrt(D), a, ws)
     o, s2 = gemm_slices(a.view(B, Hq * D), w["wo"])
     bi.bi_rmsnorm(o, s2, None, h, w["ffn_norm"], B, H, S.eps, x)
     f = torch.empty(B, F, dtype=torch.bfloat16, device="cuda")
