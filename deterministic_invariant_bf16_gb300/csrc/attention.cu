@@ -42,19 +42,29 @@ namespace {
 constexpr int CHUNK = 256;
 constexpr int ATT_THREADS = 128;  // 4 warps
 
+// Shared-memory pieces common to both kernels ("misc"): the 16-row query
+// tile, the bf16 P tile, the cross-warp reduction slots and the per-row
+// visible key counts.
 template <int D>
-struct Smem {
-    static constexpr int KV_BYTES = CHUNK * D * 2;
-    static constexpr int Q_BYTES = 16 * D * 2;
-    static constexpr int P_BYTES = 16 * CHUNK * 2;
-    static constexpr int K_OFF = 0;
-    static constexpr int V_OFF = K_OFF + KV_BYTES;
-    static constexpr int Q_OFF = V_OFF + KV_BYTES;
-    static constexpr int P_OFF = Q_OFF + Q_BYTES;
-    static constexpr int RED_OFF = P_OFF + P_BYTES;  // float [2][4][16]
-    static constexpr int LEN_OFF = RED_OFF + 2 * 4 * 16 * 4;  // int [16]
+struct Misc {
+    static constexpr int Q_OFF = 0;
+    static constexpr int P_OFF = Q_OFF + 16 * D * 2;
+    static constexpr int RED_OFF = P_OFF + 16 * CHUNK * 2;   // float [128]
+    static constexpr int LEN_OFF = RED_OFF + 128 * 4;        // int [16]
     static constexpr int BYTES = LEN_OFF + 16 * 4;
 };
+
+// One K or V tile of a chunk: 256 positions x D, bf16.
+template <int D>
+constexpr int tile_bytes() { return CHUNK * D * 2; }
+
+// Prefill layout: K tile, V tile, misc.
+template <int D>
+constexpr int prefill_smem() { return 2 * tile_bytes<D>() + Misc<D>::BYTES; }
+
+// Decode layout: a ring of three tile slots, misc.
+template <int D>
+constexpr int decode_smem() { return 3 * tile_bytes<D>() + Misc<D>::BYTES; }
 
 // Byte offset of 16-byte piece `ch` of row `row` in a tile of rows of
 // `nch` pieces, XOR-swizzled so that ldmatrix row groups hit distinct banks.
@@ -63,81 +73,75 @@ __device__ __forceinline__ uint32_t swz(int row, int ch, int nch) {
     return (uint32_t)(row * nch * 16 + ((ch ^ (row & m)) * 16));
 }
 
-// Issue cp.async copies of chunk c of KV head g of page-table row `req`
-// into the K and V tiles.  Positions >= valid_max are zero-filled.  Two
-// commit groups: K first, then V.
+// Issue (not commit) the cp.async copies of chunk c of KV head g of the
+// page-table row pt_row from `pool` into the tile at shared address `base`.
+// Positions >= valid_max are zero-filled.
 template <int D>
-__device__ __forceinline__ void load_chunk(
-    uint8_t *smem, const uint16_t *__restrict__ kp,
-    const uint16_t *__restrict__ vp, const int32_t *__restrict__ pt_row,
-    int max_pages, int n_pages, int Hkv, int g, int c, int valid_max,
-    int32_t *status) {
+__device__ __forceinline__ void load_tile(uint32_t base,
+                                          const uint16_t *__restrict__ pool,
+                                          const int32_t *__restrict__ pt_row,
+                                          int max_pages, int n_pages, int Hkv,
+                                          int g, int c, int valid_max,
+                                          int32_t *status) {
     constexpr int NCH = D / 8;
-    const uint32_t kbase = smem_u32(smem + Smem<D>::K_OFF);
-    const uint32_t vbase = smem_u32(smem + Smem<D>::V_OFF);
-#pragma unroll 1
-    for (int which = 0; which < 2; ++which) {
-        const uint16_t *pool = which ? vp : kp;
-        const uint32_t base = which ? vbase : kbase;
-        for (int idx = threadIdx.x; idx < CHUNK * NCH; idx += ATT_THREADS) {
-            const int key = idx / NCH, ch = idx % NCH;
-            const int p = c * CHUNK + key;
-            const uint16_t *src = pool;
-            uint32_t bytes = 0;
-            if (p < valid_max) {
-                const int pi = p >> 4;
-                const int pg = pi < max_pages ? pt_row[pi] : -1;
-                if (pg >= 0 && pg < n_pages) {
-                    src = pool + (((int64_t)pg * Hkv + g) * 16 + (p & 15)) * D +
-                          ch * 8;
-                    bytes = 16;
-                } else if (status) {
-                    bi_record_error(status, BI_ERR_BOUNDS);
-                }
+#pragma unroll 4
+    for (int idx = threadIdx.x; idx < CHUNK * NCH; idx += ATT_THREADS) {
+        const int key = idx / NCH, ch = idx % NCH;
+        const int p = c * CHUNK + key;
+        const uint16_t *src = pool;
+        uint32_t bytes = 0;
+        if (p < valid_max) {
+            const int pi = p >> 4;
+            const int pg = pi < max_pages ? pt_row[pi] : -1;
+            if (pg >= 0 && pg < n_pages) {
+                src = pool + (((int64_t)pg * Hkv + g) * 16 + (p & 15)) * D +
+                      ch * 8;
+                bytes = 16;
+            } else {
+                bi_record_error(status, BI_ERR_BOUNDS);
             }
-            cp_async16(base + swz(key, ch, NCH), src, bytes);
         }
-        cp_async_commit();
+        cp_async16(base + swz(key, ch, NCH), src, bytes);
     }
 }
 
-// Load the 16-row query tile: row r <- q_rows[r] (nullptr -> zeros).
+// Store the 16-row query tile: row r <- q + row_off[r] (row_off < 0 ->
+// zeros).
 template <int D>
-__device__ __forceinline__ void load_q(uint8_t *smem, const uint16_t *q,
-                                       const int64_t *row_off /* [16] */) {
+__device__ __forceinline__ void store_q(uint8_t *misc, const uint16_t *q,
+                                        const int64_t *row_off /* [16] */) {
     constexpr int NCH = D / 8;
     for (int idx = threadIdx.x; idx < 16 * NCH; idx += ATT_THREADS) {
         const int r = idx / NCH, ch = idx % NCH;
         uint4 v = make_uint4(0, 0, 0, 0);
         if (row_off[r] >= 0)
             v = *reinterpret_cast<const uint4 *>(q + row_off[r] + ch * 8);
-        *reinterpret_cast<uint4 *>(smem + Smem<D>::Q_OFF + swz(r, ch, NCH)) = v;
+        *reinterpret_cast<uint4 *>(misc + Misc<D>::Q_OFF + swz(r, ch, NCH)) = v;
     }
 }
 
-// Partial (m, l, o) of the 16-row query tile against the chunk in shared
-// memory.  valid_len[r] (in shared memory) is how many leading keys of the
-// chunk row r may see.  On return each thread holds, for rows
-// rg = lane/4 and rg + 8: m[], l[] and o[nt][0..3] for its dims
-// (warp w: dims w*D/4 + 8*nt + 2*(lane%4) + {0,1}; o[nt][0..1] row rg,
-// o[nt][2..3] row rg + 8).  Must be entered with K loaded (and V at least
-// in flight as the last cp.async group).
+// ---------------------------------------------------------------------------
+// The partial (m, l, o) of the 16-row query tile against one chunk, in two
+// phases so that the caller can overlap the V copy with phase 1.
+//
+// Phase 1 (needs the Q tile, valid_len and the K tile visible): scores
+// s = (q . k) * scale with mma.sync m16n8k16 (warp w takes keys
+// [64w, 64w + 64), dims in ascending 16-steps), masked past each row's
+// visible count, the row maximum m, p = exp(s - m), the bf16 P tile and the
+// per-warp partial row sums (each thread adds its 16 values in key order,
+// then a quad xor-tree over lanes 1, 2).  Every thread returns m for its
+// rows rg = lane/4 and rg + 8.  Ends after writing shared memory; the caller
+// must __syncthreads before phase 2.
 template <int D>
-__device__ __forceinline__ void chunk_partial(uint8_t *smem, float scale,
-                                              float m[2], float l[2],
-                                              float o[D / 32][4]) {
+__device__ __forceinline__ void chunk_phase1(uint32_t ktile, uint8_t *misc,
+                                             float scale, float m[2]) {
     constexpr int NCH = D / 8;
-    constexpr int NTV = D / 32;  // PV n-tiles of 8 dims per warp
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rg = lane >> 2, tq = lane & 3;
-    const uint32_t kbase = smem_u32(smem + Smem<D>::K_OFF);
-    const uint32_t vbase = smem_u32(smem + Smem<D>::V_OFF);
-    const uint32_t qbase = smem_u32(smem + Smem<D>::Q_OFF);
-    const uint32_t pbase = smem_u32(smem + Smem<D>::P_OFF);
-    float *red = reinterpret_cast<float *>(smem + Smem<D>::RED_OFF);
-    const int *valid_len = reinterpret_cast<const int *>(smem + Smem<D>::LEN_OFF);
+    const uint32_t qbase = smem_u32(misc + Misc<D>::Q_OFF);
+    float *red = reinterpret_cast<float *>(misc + Misc<D>::RED_OFF);
+    const int *valid_len = reinterpret_cast<const int *>(misc + Misc<D>::LEN_OFF);
 
-    // ---- scores: warp w takes keys [64w, 64w + 64) as 8 n-tiles.
     float sc[8][4];
 #pragma unroll
     for (int i = 0; i < 8; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
@@ -154,7 +158,7 @@ __device__ __forceinline__ void chunk_partial(uint8_t *smem, float scale,
             const int key = 64 * warp + 16 * np + (lane & 7) + 8 * (lane >> 4);
             const int ch = 2 * ks + ((lane >> 3) & 1);
             uint32_t b0, b1, b2, b3;
-            ldsm_x4(kbase + swz(key, ch, NCH), b0, b1, b2, b3);
+            ldsm_x4(ktile + swz(key, ch, NCH), b0, b1, b2, b3);
             mma_16816(sc[2 * np], a0, a1, a2, a3, b0, b1);
             mma_16816(sc[2 * np + 1], a0, a1, a2, a3, b2, b3);
         }
@@ -185,15 +189,15 @@ __device__ __forceinline__ void chunk_partial(uint8_t *smem, float scale,
         red[warp * 16 + rg + 8] = mx1;
     }
     __syncthreads();
-    float m0 = fmaxf(fmaxf(red[rg], red[16 + rg]), fmaxf(red[32 + rg], red[48 + rg]));
-    float m1 = fmaxf(fmaxf(red[8 + rg], red[24 + rg]),
-                     fmaxf(red[40 + rg], red[56 + rg]));
+    const float m0 = fmaxf(fmaxf(red[rg], red[16 + rg]),
+                           fmaxf(red[32 + rg], red[48 + rg]));
+    const float m1 = fmaxf(fmaxf(red[8 + rg], red[24 + rg]),
+                           fmaxf(red[40 + rg], red[56 + rg]));
     const float mu0 = m0 == -INFINITY ? 0.f : m0;
     const float mu1 = m1 == -INFINITY ? 0.f : m1;
 
-    // ---- p = exp(s - m), row sums, P tile (bf16) for the PV product.
     float l0 = 0.f, l1 = 0.f;
-    uint8_t *P = smem + Smem<D>::P_OFF;
+    uint8_t *P = misc + Misc<D>::P_OFF;
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
         const float p00 = expf(__fsub_rn(sc[nt][0], mu0));
@@ -217,18 +221,30 @@ __device__ __forceinline__ void chunk_partial(uint8_t *smem, float scale,
         red[64 + warp * 16 + rg] = l0;
         red[64 + warp * 16 + rg + 8] = l1;
     }
-    cp_async_wait<0>();  // V has landed (this thread's copies)
-    __syncthreads();     // ... and everyone's; P and row sums visible
     m[0] = m0;
     m[1] = m1;
+}
+
+// Phase 2 (after a __syncthreads that follows phase 1 and the V copy): the
+// row sums l = ((w0 + w1) + w2) + w3 over the per-warp partials and
+// o = P V with mma.sync (warp w takes dims [w*D/4, (w+1)*D/4), keys in
+// ascending 16-steps).  Each thread gets o[nt][0..1] for row rg and
+// o[nt][2..3] for row rg + 8, dims w*D/4 + 8*nt + 2*(lane%4) + {0,1}.
+template <int D>
+__device__ __forceinline__ void chunk_phase2(uint32_t vtile, uint8_t *misc,
+                                             float l[2], float o[D / 32][4]) {
+    constexpr int NCH = D / 8;
+    constexpr int NTV = D / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rg = lane >> 2;
+    const uint32_t pbase = smem_u32(misc + Misc<D>::P_OFF);
+    const float *red = reinterpret_cast<const float *>(misc + Misc<D>::RED_OFF);
     l[0] = __fadd_rn(__fadd_rn(__fadd_rn(red[64 + rg], red[80 + rg]),
                                red[96 + rg]),
                      red[112 + rg]);
     l[1] = __fadd_rn(__fadd_rn(__fadd_rn(red[72 + rg], red[88 + rg]),
                                red[104 + rg]),
                      red[120 + rg]);
-
-    // ---- o = P V: warp w takes dims [w*D/4, (w+1)*D/4), keys in order.
 #pragma unroll
     for (int nt = 0; nt < NTV; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
 #pragma unroll 4
@@ -245,14 +261,14 @@ __device__ __forceinline__ void chunk_partial(uint8_t *smem, float scale,
             for (int np = 0; np < NTV / 2; ++np) {
                 const int dim = warp * (D / 4) + 16 * np + 8 * (lane >> 4);
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(vbase + swz(key, dim >> 3, NCH), b0, b1, b2, b3);
+                ldsm_x4_t(vtile + swz(key, dim >> 3, NCH), b0, b1, b2, b3);
                 mma_16816(o[2 * np], a0, a1, a2, a3, b0, b1);
                 mma_16816(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
             }
         } else {
             const int dim = warp * (D / 4);
             uint32_t b0, b1;
-            ldsm_x2_t(vbase + swz(key, dim >> 3, NCH), b0, b1);
+            ldsm_x2_t(vtile + swz(key, dim >> 3, NCH), b0, b1);
             mma_16816(o[0], a0, a1, a2, a3, b0, b1);
         }
     }
@@ -276,59 +292,147 @@ __device__ __forceinline__ float merge_value(float O, float o, float a,
 template <int D>
 constexpr int rec_floats() { return D + 4; }
 
-template <int D>
-__global__ void __launch_bounds__(ATT_THREADS)
-    decode_chunk_kernel(const uint16_t *__restrict__ q,
-                        const uint16_t *__restrict__ kp,
-                        const uint16_t *__restrict__ vp,
-                        const int32_t *__restrict__ page_table, int max_pages,
-                        int n_pages, const int32_t *__restrict__ row_req,
-                        const int32_t *__restrict__ kv_len, int Hq, int Hkv,
-                        int G, float scale, float *__restrict__ ws, int Cmax,
-                        int32_t *status) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int c = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
-    const int L = kv_len[b];
-    const int req = row_req[b];
-    if (req < 0 || L <= c * CHUNK) return;
-    if (L > Cmax * CHUNK) {
-        if (threadIdx.x == 0 && c == 0) bi_record_error(status, BI_ERR_BOUNDS);
-        return;
+// Number of chunks of each decode row (0 for pad rows), as an exclusive
+// prefix: prefix[b] = sum of the counts of rows 0..b-1, prefix[B] = total.
+// One block; the integer scan is exact, so its order does not matter.
+__global__ void chunk_prefix_kernel(const int32_t *__restrict__ kv_len,
+                                    const int32_t *__restrict__ row_req, int B,
+                                    int Cmax, int32_t *__restrict__ prefix) {
+    __shared__ int carry, wsum[32];
+    if (threadIdx.x == 0) carry = 0;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    for (int base = 0; base < B; base += blockDim.x) {
+        const int b = base + threadIdx.x;
+        int cnt = 0;
+        if (b < B && row_req[b] >= 0) {
+            const int L = kv_len[b];
+            if (L > 0 && L <= Cmax * CHUNK) cnt = (L + CHUNK - 1) / CHUNK;
+        }
+        int inc = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += n;
+        }
+        if (lane == 31) wsum[w] = inc;
+        __syncthreads();
+        if (w == 0) {
+            int x = lane < (int)(blockDim.x >> 5) ? wsum[lane] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += n;
+            }
+            wsum[lane] = x;
+        }
+        __syncthreads();
+        const int before = carry + (w > 0 ? wsum[w - 1] : 0);
+        if (b < B) prefix[b] = before + inc - cnt;
+        __syncthreads();
+        if (threadIdx.x == blockDim.x - 1) carry = before + inc;
+        __syncthreads();
     }
-    int *valid_len = reinterpret_cast<int *>(smem + Smem<D>::LEN_OFF);
-    const int vl = min(CHUNK, L - c * CHUNK);
-    if (threadIdx.x < 16) valid_len[threadIdx.x] = threadIdx.x < G ? vl : 0;
+    if (threadIdx.x == 0) prefix[B] = carry;
+}
+
+// Decode chunk partials, persistent: CTA k takes work items k, k + grid,
+// k + 2 grid, ...; item i is KV head i % Hkv of chunk j = i / Hkv in the
+// row-major list of (row, chunk) pairs.  K and V tiles stream through a ring
+// of three shared-memory slots (item n: K in slot 2n mod 3, V in slot
+// 2n + 1 mod 3), so the copies of item n + 1 are in flight while item n is
+// computed.  The arithmetic of each item is chunk_phase1 + chunk_phase2,
+// exactly as in the prefill kernel.
+template <int D>
+__global__ void __launch_bounds__(ATT_THREADS, 1)
+    decode_chunks_kernel(const uint16_t *__restrict__ q,
+                         const uint16_t *__restrict__ kp,
+                         const uint16_t *__restrict__ vp,
+                         const int32_t *__restrict__ page_table, int max_pages,
+                         int n_pages, const int32_t *__restrict__ row_req,
+                         const int32_t *__restrict__ kv_len, int B, int Hq,
+                         int Hkv, int G, float scale, float *__restrict__ ws,
+                         int Cmax, const int32_t *__restrict__ prefix,
+                         int32_t *status) {
+    extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int64_t row_off[16];
-    if (threadIdx.x < 16)
-        row_off[threadIdx.x] =
-            threadIdx.x < G ? ((int64_t)b * Hq + g * G + threadIdx.x) * D : -1;
-    load_chunk<D>(smem, kp, vp, page_table + (int64_t)req * max_pages,
-                  max_pages, n_pages, Hkv, g, c, L, status);
-    __syncthreads();
-    load_q<D>(smem, q, row_off);
-    cp_async_wait<1>();  // K landed
-    __syncthreads();
-    float m[2], l[2], o[D / 32][4];
-    chunk_partial<D>(smem, scale, m, l, o);
+    constexpr int TB = tile_bytes<D>();
+    uint8_t *misc = smem + 3 * TB;
+    const uint32_t slot0 = smem_u32(smem);
+    const int total = prefix[B] * Hkv;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rg = lane >> 2, tq = lane & 3;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const int r = rg + 8 * half;
-        if (r >= G) continue;
-        float *rec = ws + (((int64_t)b * Hq + g * G + r) * Cmax + c) *
-                              rec_floats<D>();
-        if (warp == 0 && tq == 0) {
-            rec[0] = m[half];
-            rec[1] = l[half];
+
+    // item n of this CTA -> (row b, head g, chunk c); false past the end
+    auto item = [&](int n, int &b, int &g, int &c) -> bool {
+        const int i = blockIdx.x + n * gridDim.x;
+        if (i >= total) return false;
+        g = i % Hkv;
+        const int j = i / Hkv;
+        int lo = 0, hi = B;  // largest b with prefix[b] <= j
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (prefix[mid] <= j) lo = mid; else hi = mid;
         }
-#pragma unroll
-        for (int nt = 0; nt < D / 32; ++nt) {
-            const int dim = warp * (D / 4) + 8 * nt + 2 * tq;
-            *reinterpret_cast<float2 *>(rec + 4 + dim) =
-                make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
+        b = lo;
+        c = j - prefix[b];
+        return true;
+    };
+    auto issue = [&](int n, bool is_v, int slot) {
+        int b, g, c;
+        if (item(n, b, g, c))
+            load_tile<D>(slot0 + slot * TB, is_v ? vp : kp,
+                         page_table + (int64_t)row_req[b] * max_pages,
+                         max_pages, n_pages, Hkv, g, c, kv_len[b], status);
+        cp_async_commit();
+    };
+
+    issue(0, false, 0);
+    issue(0, true, 1);
+    issue(1, false, 2);
+    int b, g, c;
+    for (int n = 0; item(n, b, g, c); ++n) {
+        const int L = kv_len[b];
+        int *valid_len = reinterpret_cast<int *>(misc + Misc<D>::LEN_OFF);
+        if (threadIdx.x < 16) {
+            valid_len[threadIdx.x] =
+                threadIdx.x < G ? min(CHUNK, L - c * CHUNK) : 0;
+            row_off[threadIdx.x] =
+                threadIdx.x < G ? ((int64_t)b * Hq + g * G + threadIdx.x) * D
+                                : -1;
         }
+        __syncthreads();
+        store_q<D>(misc, q, row_off);
+        cp_async_wait<2>();  // K of item n
+        __syncthreads();
+        float m[2], l[2], o[D / 32][4];
+        chunk_phase1<D>(slot0 + ((2 * n) % 3) * TB, misc, scale, m);
+        __syncthreads();     // K slot free, P and row sums visible
+        issue(n + 1, true, (2 * n) % 3);
+        cp_async_wait<2>();  // V of item n
+        __syncthreads();
+        chunk_phase2<D>(slot0 + ((2 * n + 1) % 3) * TB, misc, l, o);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int r = rg + 8 * half;
+            if (r >= G) continue;
+            float *rec = ws + (((int64_t)b * Hq + g * G + r) * Cmax + c) *
+                                  rec_floats<D>();
+            if (warp == 0 && tq == 0) {
+                rec[0] = m[half];
+                rec[1] = l[half];
+            }
+#pragma unroll
+            for (int nt = 0; nt < D / 32; ++nt) {
+                const int dim = warp * (D / 4) + 8 * nt + 2 * tq;
+                *reinterpret_cast<float2 *>(rec + 4 + dim) =
+                    make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
+            }
+        }
+        __syncthreads();     // V slot free
+        issue(n + 2, false, (2 * n + 1) % 3);
     }
+    cp_async_wait<0>();
 }
 
 // Second stage of decode: one warp per (row, head) merges chunks 0..C-1.
@@ -384,6 +488,9 @@ __global__ void __launch_bounds__(ATT_THREADS)
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int64_t row_off[16];
     __shared__ int s_info[4];  // t0, nq, req, valid_max
+    constexpr int TB = tile_bytes<D>();
+    const uint32_t ktile = smem_u32(smem), vtile = ktile + TB;
+    uint8_t *misc = smem + 2 * TB;
     const int g = blockIdx.y;
     const int QPT = 16 / G;
     if (threadIdx.x == 0) {
@@ -424,7 +531,7 @@ __global__ void __launch_bounds__(ATT_THREADS)
             qi < nq ? ((int64_t)(t0 + qi) * Hq + g * G + hh) * D : -1;
     }
     const int32_t *pt_row = page_table + (int64_t)req * max_pages;
-    int *valid_len = reinterpret_cast<int *>(smem + Smem<D>::LEN_OFF);
+    int *valid_len = reinterpret_cast<int *>(misc + Misc<D>::LEN_OFF);
     const int p_r0 = (rg / G) < nq ? pos[t0 + rg / G] : -1;
     const int p_r1 = ((rg + 8) / G) < nq ? pos[t0 + (rg + 8) / G] : -1;
     const int C = (vmax + CHUNK - 1) / CHUNK;
@@ -437,16 +544,23 @@ __global__ void __launch_bounds__(ATT_THREADS)
             const int pr = qi < nq ? pos[t0 + qi] : -1;
             valid_len[threadIdx.x] = max(0, min(CHUNK, pr + 1 - c * CHUNK));
         }
-        load_chunk<D>(smem, kp, vp, pt_row, max_pages, n_pages, Hkv, g, c,
-                      vmax, status);
+        load_tile<D>(ktile, kp, pt_row, max_pages, n_pages, Hkv, g, c, vmax,
+                     status);
+        cp_async_commit();
+        load_tile<D>(vtile, vp, pt_row, max_pages, n_pages, Hkv, g, c, vmax,
+                     status);
+        cp_async_commit();
         if (c == 0) {
             __syncthreads();
-            load_q<D>(smem, q, row_off);
+            store_q<D>(misc, q, row_off);
         }
         cp_async_wait<1>();
         __syncthreads();
         float m[2], l[2], o[D / 32][4];
-        chunk_partial<D>(smem, scale, m, l, o);
+        chunk_phase1<D>(ktile, misc, scale, m);
+        cp_async_wait<0>();
+        __syncthreads();
+        chunk_phase2<D>(vtile, misc, l, o);
         const int pr[2] = {p_r0, p_r1};
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -502,17 +616,22 @@ bool group_ok(int Hq, int Hkv) {
     return G == 1 || G == 2 || G == 4 || G == 8 || G == 16;
 }
 
+size_t records_bytes(int B, int Hq, int D, int max_kv_len) {
+    const int C = (max_kv_len + CHUNK - 1) / CHUNK;
+    return ((size_t)B * Hq * C * (D + 4) * sizeof(float) + 255) & ~size_t(255);
+}
+
 }  // namespace
 
 extern "C" size_t bi_decode_attn_workspace_size(int B, int Hq, int D,
                                                 int max_kv_len) {
     if (B <= 0 || Hq <= 0 || D <= 0 || max_kv_len <= 0) return 0;
-    const int C = (max_kv_len + CHUNK - 1) / CHUNK;
-    return (size_t)B * Hq * C * (D + 4) * sizeof(float);
+    return records_bytes(B, Hq, D, max_kv_len) +
+           (((size_t)(B + 1) * sizeof(int32_t) + 255) & ~size_t(255));
 }
 
 // Decode attention with the pool size known (page ids are range-checked
-// against it).  stages: bit 0 runs the chunk kernel, bit 1 the merge.
+// against it).  stages: bit 0 runs the chunk kernels, bit 1 the merge.
 bi_status bi_decode_attn_pool(const bi_bf16 *q, const bi_bf16 *k_pool,
                               const bi_bf16 *v_pool, const int32_t *page_table,
                               int max_pages, int n_pages,
@@ -542,25 +661,37 @@ bi_status bi_decode_attn_pool(const bi_bf16 *q, const bi_bf16 *k_pool,
                        need);
     const int Cmax = (max_kv_len + CHUNK - 1) / CHUNK;
     const int G = Hq / Hkv;
+    float *rec = static_cast<float *>(ws);
+    int32_t *prefix = reinterpret_cast<int32_t *>(
+        static_cast<uint8_t *>(ws) + records_bytes(B, Hq, D, max_kv_len));
     int32_t *status = bi_status_ptr();
     if (stages & 1) {
-        dim3 grid(Cmax, Hkv, B);
+        chunk_prefix_kernel<<<1, 1024, 0, s>>>(kv_len, row_req, B, Cmax,
+                                               prefix);
+        BI_LAUNCH_CHECK("decode chunk prefix launch");
+        const int grid = bi_sm_count();
         if (D == 128) {
             static std::once_flag f;
             static bi_status fs;
             std::call_once(f, [] {
-                fs = set_attr(decode_chunk_kernel<128>, Smem<128>::BYTES);
+                fs = set_attr(decode_chunks_kernel<128>, decode_smem<128>());
             });
             if (fs != BI_OK) return fs;
-            decode_chunk_kernel<128><<<grid, ATT_THREADS, Smem<128>::BYTES, s>>>(
+            decode_chunks_kernel<128><<<grid, ATT_THREADS, decode_smem<128>(),
+                                        s>>>(
                 q, k_pool, v_pool, page_table, max_pages, n_pages, row_req,
-                kv_len, Hq, Hkv, G, scale, static_cast<float *>(ws), Cmax,
-                status);
+                kv_len, B, Hq, Hkv, G, scale, rec, Cmax, prefix, status);
         } else {
-            decode_chunk_kernel<32><<<grid, ATT_THREADS, Smem<32>::BYTES, s>>>(
+            static std::once_flag f;
+            static bi_status fs;
+            std::call_once(f, [] {
+                fs = set_attr(decode_chunks_kernel<32>, decode_smem<32>());
+            });
+            if (fs != BI_OK) return fs;
+            decode_chunks_kernel<32><<<grid, ATT_THREADS, decode_smem<32>(),
+                                       s>>>(
                 q, k_pool, v_pool, page_table, max_pages, n_pages, row_req,
-                kv_len, Hq, Hkv, G, scale, static_cast<float *>(ws), Cmax,
-                status);
+                kv_len, B, Hq, Hkv, G, scale, rec, Cmax, prefix, status);
         }
         BI_LAUNCH_CHECK("decode attention launch");
     }
@@ -569,12 +700,10 @@ bi_status bi_decode_attn_pool(const bi_bf16 *q, const bi_bf16 *k_pool,
         const int blocks = (warps * 32 + 255) / 256;
         if (D == 128)
             decode_merge_kernel<128><<<blocks, 256, 0, s>>>(
-                static_cast<const float *>(ws), kv_len, row_req, B, Hq, Cmax,
-                out);
+                rec, kv_len, row_req, B, Hq, Cmax, out);
         else
             decode_merge_kernel<32><<<blocks, 256, 0, s>>>(
-                static_cast<const float *>(ws), kv_len, row_req, B, Hq, Cmax,
-                out);
+                rec, kv_len, row_req, B, Hq, Cmax, out);
         BI_LAUNCH_CHECK("decode merge launch");
     }
     return BI_OK;
@@ -626,13 +755,15 @@ bi_status bi_prefill_attn_pool(const bi_bf16 *q, const int32_t *cu_q,
     if (D == 128) {
         static std::once_flag f;
         static bi_status fs;
-        std::call_once(f, [] { fs = set_attr(prefill_kernel<128>, Smem<128>::BYTES); });
+        std::call_once(f, [] {
+            fs = set_attr(prefill_kernel<128>, prefill_smem<128>());
+        });
         if (fs != BI_OK) return fs;
-        prefill_kernel<128><<<grid, ATT_THREADS, Smem<128>::BYTES, stream>>>(
+        prefill_kernel<128><<<grid, ATT_THREADS, prefill_smem<128>(), stream>>>(
             q, cu_q, seg_req, R, pos, k_pool, v_pool, page_table, max_pages,
             n_pages, Hq, Hkv, G, scale, max_kv_len, out, status);
     } else {
-        prefill_kernel<32><<<grid, ATT_THREADS, Smem<32>::BYTES, stream>>>(
+        prefill_kernel<32><<<grid, ATT_THREADS, prefill_smem<32>(), stream>>>(
             q, cu_q, seg_req, R, pos, k_pool, v_pool, page_table, max_pages,
             n_pages, Hq, Hkv, G, scale, max_kv_len, out, status);
     }

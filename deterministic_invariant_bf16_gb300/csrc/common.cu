@@ -46,6 +46,23 @@ int32_t *bi_status_ptr() {
     return ptrs[dev];
 }
 
+int bi_sm_count() {
+    static std::mutex mu;
+    static int counts[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    std::lock_guard<std::mutex> lock(mu);
+    if (counts[dev] <= 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                cudaSuccess ||
+            n <= 0)
+            n = 1;
+        counts[dev] = n;
+    }
+    return counts[dev];
+}
+
 extern "C" bi_status bi_device_status(int32_t *h_status, void *stream) {
     BI_REQUIRE(h_status, "bi_device_status: null output");
     int32_t *d = bi_status_ptr();

@@ -43,8 +43,9 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
 constexpr uint32_t IDESC = make_idesc_bf16(BM, BN);
 
-constexpr int STAGES_SPLIT = 3;  // ~97 KB: two CTAs per SM
-constexpr int STAGES_FUSED = 6;  // ~193 KB: one CTA per SM
+// One persistent CTA per SM: six 32 KB stages (~193 KB of shared memory).
+constexpr int STAGES_SPLIT = 6;
+constexpr int STAGES_FUSED = 6;
 
 constexpr size_t smem_bytes(int stages) {
     return 1024 /* alignment slack */ + (size_t)stages * STAGE_BYTES + 256;
@@ -52,6 +53,8 @@ constexpr size_t smem_bytes(int stages) {
 
 struct GemmArgs {
     int M, N, K, KB, S;
+    int MT;     // m-tiles
+    int units;  // work units (see unit_coords)
     int out_kind;
     void *out;
     int32_t *status;
@@ -92,8 +95,35 @@ __device__ __forceinline__ float swiglu1(float g, float u) {
     return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
 }
 
+// Persistent CTA: one per SM, looping over work units.  A unit is one
+// (m-tile, n-tile, slice) in the split schedule and one (m-tile, n-tile)
+// with all its slices in the fused schedule.  Units are numbered with the
+// m-tile fastest, so CTAs that run at the same time on neighbouring units
+// read the same weight tile (the second read hits L2).  CTA k takes units
+// k, k + grid, k + 2 grid, ...  The shared-memory ring runs on across unit
+// boundaries, and the two TMEM accumulators alternate between consecutive
+// slices, so the epilogue of one slice overlaps the MMAs of the next.
+template <bool FUSED>
+__device__ __forceinline__ void unit_coords(const GemmArgs &p, int u, int &m0,
+                                            int &n0, int &nt, int &s_lo,
+                                            int &s_hi) {
+    const int mt = u % p.MT;
+    int rest = u / p.MT;
+    if (FUSED) {
+        nt = rest;
+        s_lo = 0;
+        s_hi = p.S;
+    } else {
+        s_lo = rest % p.S;
+        s_hi = s_lo + 1;
+        nt = rest / p.S;
+    }
+    m0 = mt * BM;
+    n0 = nt * BN;
+}
+
 template <bool FUSED, int STAGES>
-__global__ void __launch_bounds__(THREADS, FUSED ? 1 : 2)
+__global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                 const __grid_constant__ CUtensorMap tmB, GemmArgs p) {
     extern __shared__ uint8_t smem_raw[];
@@ -107,11 +137,8 @@ __global__ void __launch_bounds__(THREADS, FUSED ? 1 : 2)
     uint64_t *acc_empty = acc_full + 2;    // [2]
     uint32_t *tslot = reinterpret_cast<uint32_t *>(acc_empty + 2);
 
-    constexpr uint32_t TMEM_COLS = FUSED ? 2 * BN : BN;
+    constexpr uint32_t TMEM_COLS = 2 * BN;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
-    const int s_lo = FUSED ? 0 : blockIdx.z;
-    const int s_hi = FUSED ? p.S : blockIdx.z + 1;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
@@ -136,144 +163,162 @@ __global__ void __launch_bounds__(THREADS, FUSED ? 1 : 2)
         tma_prefetch_desc(&tmB);
         int it = 0;
         bool ok = true;
-        for (int s = s_lo; s < s_hi && ok; ++s) {
-            const int kb0 = (int)((int64_t)s * p.KB / p.S);
-            const int kb1 = (int)((int64_t)(s + 1) * p.KB / p.S);
-            for (int kb = kb0; kb < kb1; ++kb, ++it) {
-                const int st = it % STAGES;
-                const uint32_t round = it / STAGES;
-                if (round > 0 && !mbar_wait(&empty[st], (round - 1) & 1,
-                                            p.status)) {
-                    ok = false;
-                    break;
+        for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+            int m0, n0, nt, s_lo, s_hi;
+            unit_coords<FUSED>(p, u, m0, n0, nt, s_lo, s_hi);
+            for (int s = s_lo; s < s_hi && ok; ++s) {
+                const int kb0 = (int)((int64_t)s * p.KB / p.S);
+                const int kb1 = (int)((int64_t)(s + 1) * p.KB / p.S);
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    const int st = it % STAGES;
+                    const uint32_t round = it / STAGES;
+                    if (round > 0 && !mbar_wait(&empty[st], (round - 1) & 1,
+                                                p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[st], STAGE_BYTES);
+                    tma_load_2d(sA + st * A_BYTES, &tmA, kb * BK, m0,
+                                &full[st]);
+                    tma_load_2d(sB + st * B_BYTES, &tmB, kb * BK, n0,
+                                &full[st]);
                 }
-                mbar_arrive_expect_tx(&full[st], STAGE_BYTES);
-                tma_load_2d(sA + st * A_BYTES, &tmA, kb * BK, m0, &full[st]);
-                tma_load_2d(sB + st * B_BYTES, &tmB, kb * BK, n0, &full[st]);
             }
         }
         if (!ok) {
             // Let the copies already issued land before the CTA exits.
-            for (int j = std::max(0, it - STAGES); j < it; ++j)
+            for (int j = it > STAGES ? it - STAGES : 0; j < it; ++j)
                 mbar_wait(&full[j % STAGES], (j / STAGES) & 1, p.status);
         }
     } else if (warp == 1 && lane == 0) {
         // --------------------------------------------------------- MMA --
-        int it = 0;
+        int it = 0, acc = 0;
         bool ok = true;
-        for (int s = s_lo, j = 0; s < s_hi; ++s, ++j) {
-            const int buf = FUSED ? (j & 1) : 0;
-            if (FUSED && j >= 2 &&
-                !mbar_wait(&acc_empty[buf], ((j >> 1) - 1) & 1, p.status))
-                ok = false;
-            tc_fence_after();
-            const uint32_t d_tmem = tmem + buf * BN;
-            const int kb0 = (int)((int64_t)s * p.KB / p.S);
-            const int kb1 = (int)((int64_t)(s + 1) * p.KB / p.S);
-            for (int kb = kb0; kb < kb1 && ok; ++kb, ++it) {
-                const int st = it % STAGES;
-                if (!mbar_wait(&full[st], (it / STAGES) & 1, p.status)) {
+        for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+            int m0, n0, nt, s_lo, s_hi;
+            unit_coords<FUSED>(p, u, m0, n0, nt, s_lo, s_hi);
+            for (int s = s_lo; s < s_hi && ok; ++s, ++acc) {
+                const int buf = acc & 1;
+                if (acc >= 2 &&
+                    !mbar_wait(&acc_empty[buf], ((acc >> 1) - 1) & 1,
+                               p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t a = smem_u32(sA + st * A_BYTES);
-                const uint32_t b = smem_u32(sB + st * B_BYTES);
+                const uint32_t d_tmem = tmem + buf * BN;
+                const int kb0 = (int)((int64_t)s * p.KB / p.S);
+                const int kb1 = (int)((int64_t)(s + 1) * p.KB / p.S);
+                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                    const int st = it % STAGES;
+                    if (!mbar_wait(&full[st], (it / STAGES) & 1, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a = smem_u32(sA + st * A_BYTES);
+                    const uint32_t b = smem_u32(sB + st * B_BYTES);
 #pragma unroll
-                for (int k = 0; k < BK / 16; ++k)
-                    tc_mma_bf16(d_tmem, make_sw128_desc(a + 32 * k),
-                                make_sw128_desc(b + 32 * k), IDESC,
-                                (kb > kb0 || k > 0) ? 1u : 0u);
-                tc_commit(&empty[st]);
+                    for (int k = 0; k < BK / 16; ++k)
+                        tc_mma_bf16(d_tmem, make_sw128_desc(a + 32 * k),
+                                    make_sw128_desc(b + 32 * k), IDESC,
+                                    (kb > kb0 || k > 0) ? 1u : 0u);
+                    tc_commit(&empty[st]);
+                }
+                tc_commit(&acc_full[buf]);
             }
-            tc_commit(&acc_full[buf]);
         }
     } else if (warp >= 2) {
         // ---------------------------------------------------- epilogue --
         const int q = warp & 3;
-        const int row = m0 + q * 32 + lane;
-        const bool live = row < p.M;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
         float run[FUSED ? BN : 1];
+        int acc = 0;
         bool ok = true;
-        for (int s = s_lo, j = 0; s < s_hi; ++s, ++j) {
-            const int buf = FUSED ? (j & 1) : 0;
-            if (!mbar_wait(&acc_full[buf], FUSED ? ((j >> 1) & 1) : 0,
-                           p.status)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t base = lane_addr + buf * BN;
-            if (FUSED) {
+        for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+            int m0, n0, nt, s_lo, s_hi;
+            unit_coords<FUSED>(p, u, m0, n0, nt, s_lo, s_hi);
+            const int row = m0 + q * 32 + lane;
+            const bool live = row < p.M;
+            for (int s = s_lo, j = 0; s < s_hi; ++s, ++j, ++acc) {
+                const int buf = acc & 1;
+                if (!mbar_wait(&acc_full[buf], (acc >> 1) & 1, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t base = lane_addr + buf * BN;
+                if (FUSED) {
 #pragma unroll
-                for (int c = 0; c < BN; c += 32) {
-                    float v[32];
-                    tmem_ld_32cols(base + c, v);
+                    for (int c = 0; c < BN; c += 32) {
+                        float v[32];
+                        tmem_ld_32cols(base + c, v);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        run[c + i] = (j == 0) ? v[i] : __fadd_rn(run[c + i], v[i]);
+                        for (int i = 0; i < 32; ++i)
+                            run[c + i] =
+                                (j == 0) ? v[i] : __fadd_rn(run[c + i], v[i]);
+                    }
+                } else if (p.out_kind == BI_OUT_SWIGLU) {
+                    const int f0 = nt * (BN / 2);
+                    const int NO = p.N / 2;
+#pragma unroll
+                    for (int c = 0; c < BN / 2; c += 32) {
+                        float g[32], uu[32];
+                        tmem_ld_32cols(base + c, g);
+                        tmem_ld_32cols(base + BN / 2 + c, uu);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) g[i] = swiglu1(g[i], uu[i]);
+                        if (live)
+                            store_bf16_32(reinterpret_cast<uint16_t *>(p.out) +
+                                              (size_t)row * NO,
+                                          f0 + c, NO, g);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < BN; c += 32) {
+                        float v[32];
+                        tmem_ld_32cols(base + c, v);
+                        if (!live) continue;
+                        if (p.out_kind == BI_OUT_BF16)
+                            store_bf16_32(reinterpret_cast<uint16_t *>(p.out) +
+                                              (size_t)row * p.N,
+                                          n0 + c, p.N, v);
+                        else  // partial slice s (or the only slice)
+                            store_f32_32(reinterpret_cast<float *>(p.out) +
+                                             ((size_t)s * p.M + row) * p.N,
+                                         n0 + c, p.N, v);
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[buf]);
-            } else if (p.out_kind == BI_OUT_SWIGLU) {
-                const int f0 = blockIdx.y * (BN / 2);
-                const int NO = p.N / 2;
+            }
+            if (FUSED && ok && live) {
+                if (p.out_kind == BI_OUT_SWIGLU) {
+                    const int f0 = nt * (BN / 2);
+                    const int NO = p.N / 2;
 #pragma unroll
-                for (int c = 0; c < BN / 2; c += 32) {
-                    float g[32], u[32];
-                    tmem_ld_32cols(base + c, g);
-                    tmem_ld_32cols(base + BN / 2 + c, u);
+                    for (int c = 0; c < BN / 2; c += 32) {
+                        float g[32];
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) g[i] = swiglu1(g[i], u[i]);
-                    if (live)
+                        for (int i = 0; i < 32; ++i)
+                            g[i] = swiglu1(run[c + i], run[BN / 2 + c + i]);
                         store_bf16_32(reinterpret_cast<uint16_t *>(p.out) +
                                           (size_t)row * NO,
                                       f0 + c, NO, g);
-                }
-            } else {
+                    }
+                } else {
 #pragma unroll
-                for (int c = 0; c < BN; c += 32) {
-                    float v[32];
-                    tmem_ld_32cols(base + c, v);
-                    if (!live) continue;
-                    if (p.out_kind == BI_OUT_BF16)
-                        store_bf16_32(reinterpret_cast<uint16_t *>(p.out) +
-                                          (size_t)row * p.N,
-                                      n0 + c, p.N, v);
-                    else  // partial slice s (or the only slice)
-                        store_f32_32(reinterpret_cast<float *>(p.out) +
-                                         ((size_t)s * p.M + row) * p.N,
-                                     n0 + c, p.N, v);
-                }
-            }
-        }
-        if (FUSED && ok && live) {
-            if (p.out_kind == BI_OUT_SWIGLU) {
-                const int f0 = blockIdx.y * (BN / 2);
-                const int NO = p.N / 2;
-#pragma unroll
-                for (int c = 0; c < BN / 2; c += 32) {
-                    float g[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        g[i] = swiglu1(run[c + i], run[BN / 2 + c + i]);
-                    store_bf16_32(reinterpret_cast<uint16_t *>(p.out) +
-                                      (size_t)row * NO,
-                                  f0 + c, NO, g);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < BN; c += 32) {
-                    if (p.out_kind == BI_OUT_BF16)
-                        store_bf16_32(reinterpret_cast<uint16_t *>(p.out) +
-                                          (size_t)row * p.N,
-                                      n0 + c, p.N, run + c);
-                    else
-                        store_f32_32(reinterpret_cast<float *>(p.out) +
-                                         (size_t)row * p.N,
-                                     n0 + c, p.N, run + c);
+                    for (int c = 0; c < BN; c += 32) {
+                        if (p.out_kind == BI_OUT_BF16)
+                            store_bf16_32(reinterpret_cast<uint16_t *>(p.out) +
+                                              (size_t)row * p.N,
+                                          n0 + c, p.N, run + c);
+                        else
+                            store_f32_32(reinterpret_cast<float *>(p.out) +
+                                             (size_t)row * p.N,
+                                         n0 + c, p.N, run + c);
+                    }
                 }
             }
         }
@@ -417,16 +462,17 @@ bi_status bi_gemm_sched(const bi_bf16 *x, int M, int K, const bi_bf16 *W,
         a.out_kind = BI_OUT_PARTIALS;
     }
 
+    a.MT = mt;
+    a.units = fused ? mt * nt : mt * nt * S;
+    const int grid = std::min(a.units, bi_sm_count());
     if (fused) {
         if ((st = set_smem_attr<true, STAGES_FUSED>()) != BI_OK) return st;
         gemm_kernel<true, STAGES_FUSED>
-            <<<dim3(mt, nt, 1), THREADS, smem_bytes(STAGES_FUSED), stream>>>(
-                ta, tb, a);
+            <<<grid, THREADS, smem_bytes(STAGES_FUSED), stream>>>(ta, tb, a);
     } else {
         if ((st = set_smem_attr<false, STAGES_SPLIT>()) != BI_OK) return st;
         gemm_kernel<false, STAGES_SPLIT>
-            <<<dim3(mt, nt, S), THREADS, smem_bytes(STAGES_SPLIT), stream>>>(
-                ta, tb, a);
+            <<<grid, THREADS, smem_bytes(STAGES_SPLIT), stream>>>(ta, tb, a);
     }
     BI_LAUNCH_CHECK("gemm launch");
     if (need_reduce) {

@@ -12,6 +12,9 @@
 // runtime cannot provide it).
 int32_t *bi_status_ptr();
 
+// Number of SMs of the current device (queried once per device).
+int bi_sm_count();
+
 // 2-D bf16 tensor map over a row-major [outer][inner] array.
 bi_status bi_make_tmap_2d_bf16(CUtensorMap *map, const void *base,
                                uint64_t inner, uint64_t outer,

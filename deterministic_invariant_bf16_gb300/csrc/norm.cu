@@ -17,8 +17,11 @@ namespace {
 constexpr int NORM_THREADS = 256;
 constexpr int NORM_MAX_VEC = 8;  // H <= 8 * 8 * 256 = 16384
 
+// S (the number of split slices, 0 = no partials) is a template argument so
+// that all S loads of a slice group are issued before the in-order adds.
+template <int S>
 __global__ void __launch_bounds__(NORM_THREADS)
-    rmsnorm_kernel(const float *__restrict__ partials, int S,
+    rmsnorm_kernel(const float *__restrict__ partials,
                    const uint16_t *__restrict__ x, uint16_t *residual,
                    const uint16_t *__restrict__ w, int T, int H, float eps,
                    uint16_t *__restrict__ y) {
@@ -34,14 +37,20 @@ __global__ void __launch_bounds__(NORM_THREADS)
         const int vi = tid + k * NORM_THREADS;
         if (vi >= nvec) break;
         const int64_t off = row + (int64_t)vi * 8;
-        if (partials) {
-            const float4 *p0 = reinterpret_cast<const float4 *>(partials + off);
-            float4 a = p0[0], b = p0[1];
-            float acc[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            for (int s = 1; s < S; ++s) {
+        if (S > 0) {
+            float4 pa[S > 0 ? S : 1][2];
+#pragma unroll
+            for (int s = 0; s < S; ++s) {
                 const float4 *ps =
                     reinterpret_cast<const float4 *>(partials + s * TH + off);
-                float4 c = ps[0], d = ps[1];
+                pa[s][0] = __ldcs(ps);
+                pa[s][1] = __ldcs(ps + 1);
+            }
+            float acc[8] = {pa[0][0].x, pa[0][0].y, pa[0][0].z, pa[0][0].w,
+                            pa[0][1].x, pa[0][1].y, pa[0][1].z, pa[0][1].w};
+#pragma unroll
+            for (int s = 1; s < S; ++s) {
+                const float4 c = pa[s][0], d = pa[s][1];
                 acc[0] = __fadd_rn(acc[0], c.x);
                 acc[1] = __fadd_rn(acc[1], c.y);
                 acc[2] = __fadd_rn(acc[2], c.z);
@@ -149,14 +158,25 @@ extern "C" bi_status bi_rmsnorm(const float *partials, int S,
     BI_REQUIRE(w && y, "bi_rmsnorm: null w or y");
     BI_REQUIRE(partials || x || residual,
                "bi_rmsnorm: need partials, x or residual");
-    BI_REQUIRE(!partials || S >= 1, "bi_rmsnorm: S=%d", S);
+    BI_REQUIRE(!partials || (S >= 1 && S <= 8), "bi_rmsnorm: S=%d not in 1..8",
+               S);
     BI_REQUIRE((!partials || bi_aligned16(partials)) && (!x || bi_aligned16(x)) &&
                    (!residual || bi_aligned16(residual)) && bi_aligned16(w) &&
                    bi_aligned16(y),
                "bi_rmsnorm: pointers must be 16-byte aligned");
     if (T == 0) return BI_OK;
-    rmsnorm_kernel<<<T, NORM_THREADS, 0, bi_stream(stream)>>>(
-        partials, partials ? S : 0, x, residual, w, T, H, eps, y);
+    cudaStream_t s = bi_stream(stream);
+    switch (partials ? S : 0) {
+#define BI_NORM_CASE(n)                                                      \
+    case n:                                                                  \
+        rmsnorm_kernel<n><<<T, NORM_THREADS, 0, s>>>(partials, x, residual,  \
+                                                     w, T, H, eps, y);       \
+        break;
+        BI_NORM_CASE(0) BI_NORM_CASE(1) BI_NORM_CASE(2) BI_NORM_CASE(3)
+        BI_NORM_CASE(4) BI_NORM_CASE(5) BI_NORM_CASE(6) BI_NORM_CASE(7)
+        BI_NORM_CASE(8)
+#undef BI_NORM_CASE
+    }
     BI_LAUNCH_CHECK("rmsnorm launch");
     return BI_OK;
 }

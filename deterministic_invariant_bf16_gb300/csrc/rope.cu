@@ -19,15 +19,23 @@ namespace {
 
 constexpr int ROPE_THREADS = 256;
 
+// Slices summed in slice order and rounded to bf16.  S is a template
+// argument so that all S loads are in flight before the adds.
+template <int S>
 __device__ __forceinline__ float qkv_value(const float *__restrict__ qkv,
-                                           int S, int64_t TQ, int64_t off) {
-    float v = qkv[off];
-    for (int s = 1; s < S; ++s) v = __fadd_rn(v, qkv[s * TQ + off]);
+                                           int64_t TQ, int64_t off) {
+    float p[S];
+#pragma unroll
+    for (int s = 0; s < S; ++s) p[s] = __ldcs(qkv + s * TQ + off);
+    float v = p[0];
+#pragma unroll
+    for (int s = 1; s < S; ++s) v = __fadd_rn(v, p[s]);
     return bf16_to_f32(f32_to_bf16(v));
 }
 
+template <int S>
 __global__ void __launch_bounds__(ROPE_THREADS)
-    rope_kernel(const float *__restrict__ qkv, int S,
+    rope_kernel(const float *__restrict__ qkv,
                 const int32_t *__restrict__ pos,
                 const int32_t *__restrict__ row_req, int T, int Hq, int Hkv,
                 int D, double theta, uint16_t *__restrict__ q_out,
@@ -71,8 +79,8 @@ __global__ void __launch_bounds__(ROPE_THREADS)
     for (int e = threadIdx.x; e < pairs; e += blockDim.x) {
         const int head = e / half, i = e % half;
         const int64_t c0 = rowoff + (int64_t)head * D + i;
-        const float x0 = qkv_value(qkv, S, TQ, c0);
-        const float x1 = qkv_value(qkv, S, TQ, c0 + half);
+        const float x0 = qkv_value<S>(qkv, TQ, c0);
+        const float x1 = qkv_value<S>(qkv, TQ, c0 + half);
         const float c = cs[i], s = sn[i];
         const float y0 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, s));
         const float y1 = __fadd_rn(__fmul_rn(x1, c), __fmul_rn(x0, s));
@@ -92,7 +100,7 @@ __global__ void __launch_bounds__(ROPE_THREADS)
     if (page >= 0) {
         for (int e = threadIdx.x; e < Hkv * D; e += blockDim.x) {
             const int head = e / D, d = e % D;
-            const float v = qkv_value(qkv, S, TQ,
+            const float v = qkv_value<S>(qkv, TQ,
                                       rowoff + (int64_t)(Hq + Hkv) * D + e);
             v_pool[((page * Hkv + head) * 16 + slot) * (int64_t)D + d] =
                 f32_to_bf16(v);
@@ -108,16 +116,27 @@ extern "C" bi_status bi_rope(const float *qkv, int S, const int32_t *pos,
                              bi_bf16 *k_pool, bi_bf16 *v_pool,
                              const int32_t *page_table, int max_pages,
                              int n_pages, void *stream) {
-    BI_REQUIRE(T >= 0 && S >= 1 && Hq > 0 && Hkv > 0 && Hq % Hkv == 0,
+    BI_REQUIRE(T >= 0 && S >= 1 && S <= 8 && Hq > 0 && Hkv > 0 &&
+                   Hq % Hkv == 0,
                "bi_rope: bad shape T=%d S=%d Hq=%d Hkv=%d", T, S, Hq, Hkv);
     BI_REQUIRE(D % 2 == 0 && D <= 128 && D > 0, "bi_rope: D=%d", D);
     BI_REQUIRE(qkv && pos && row_req && q_out && k_pool && v_pool && page_table,
                "bi_rope: null pointer");
     BI_REQUIRE(max_pages > 0 && n_pages > 0, "bi_rope: empty page table/pool");
     if (T == 0) return BI_OK;
-    rope_kernel<<<T, ROPE_THREADS, 0, bi_stream(stream)>>>(
-        qkv, S, pos, row_req, T, Hq, Hkv, D, theta, q_out, k_pool, v_pool,
-        page_table, max_pages, n_pages, bi_status_ptr());
+    cudaStream_t st = bi_stream(stream);
+    int32_t *status = bi_status_ptr();
+    switch (S) {
+#define BI_ROPE_CASE(n)                                                       \
+    case n:                                                                   \
+        rope_kernel<n><<<T, ROPE_THREADS, 0, st>>>(                           \
+            qkv, pos, row_req, T, Hq, Hkv, D, theta, q_out, k_pool, v_pool,   \
+            page_table, max_pages, n_pages, status);                          \
+        break;
+        BI_ROPE_CASE(1) BI_ROPE_CASE(2) BI_ROPE_CASE(3) BI_ROPE_CASE(4)
+        BI_ROPE_CASE(5) BI_ROPE_CASE(6) BI_ROPE_CASE(7) BI_ROPE_CASE(8)
+#undef BI_ROPE_CASE
+    }
     BI_LAUNCH_CHECK("rope launch");
     return BI_OK;
 }
