@@ -72,6 +72,8 @@ SIGNATURES = {
     "bi_decode_attn_workspace_size": ([I, I, I, I], Z),
     "bi_paged_decode_attn": ([V, V, V, V, I, V, V, I, I, I, I, I, F, V, V, Z,
                               V], I),
+    "bi_paged_decode_attn_noalloc": ([V, V, V, V, I, V, V, I, I, I, I, I, F,
+                                      V, V], I),
     "bi_prefill_attn": ([V, V, V, I, I, V, I, I, V, V, V, I, I, I, I, F, V,
                          V], I),
     "bi_argmax_logits": ([V, I, I, V, V], I),
@@ -200,6 +202,24 @@ def bi_paged_decode_attn(q, k_pool, v_pool, page_table, row_req, kv_len,
         _p(q), _p(k_pool), _p(v_pool), _p(page_table), page_table.shape[1],
         _p(row_req), _p(kv_len), B, max_kv_len, Hq, Hkv, D_, scale, _p(out),
         _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
+
+
+def bi_paged_decode_attn_noalloc(q, k_pool, v_pool, page_table, row_req,
+                                 kv_len, max_kv_len, scale, out, stream=None):
+    """bi_paged_decode_attn without a workspace argument, for callers that
+    cannot allocate device memory: its scratch is a fixed array inside the
+    library (NOALLOC_SCRATCH_BYTES per GPU).  Calls that would need more
+    scratch raise BiError (BI_ERR_WORKSPACE_TOO_SMALL); calls that overlap
+    on the GPU share the array and must be ordered on one stream."""
+    B, Hq, D_ = q.shape
+    Hkv = k_pool.shape[1]
+    _check(lib().bi_paged_decode_attn_noalloc(
+        _p(q), _p(k_pool), _p(v_pool), _p(page_table), page_table.shape[1],
+        _p(row_req), _p(kv_len), B, max_kv_len, Hq, Hkv, D_, scale, _p(out),
+        _stream(stream)))
 
 
 def bi_prefill_attn(q, cu_q, seg_req, pos, max_q, max_kv_len, k_pool, v_pool,

@@ -723,6 +723,64 @@ extern "C" bi_status bi_paged_decode_attn(
                                bi_stream(stream));
 }
 
+// ------------------------------------------- allocation-free decode variant --
+//
+// Scratch of bi_paged_decode_attn_noalloc: the chunk partials live in this
+// fixed array instead of a caller-supplied workspace.  It is part of the
+// module, so every GPU that loads the library holds these bytes until the
+// process exits.  Host code cannot use the array's name as a device address;
+// its address is looked up once per device below.
+static __device__ __align__(256) uint8_t
+    g_decode_noalloc_scratch[BI_DECODE_ATTN_NOALLOC_SCRATCH_BYTES];
+
+// Device address of the scratch array on the current device, looked up with
+// cudaGetSymbolAddress the first time the variant runs on that device.
+static bi_status noalloc_scratch(void **out) {
+    static std::mutex mu;
+    static void *ptrs[64] = {nullptr};
+    int dev = 0;
+    bi_status st = bi_cuda_check(cudaGetDevice(&dev), "noalloc: cudaGetDevice");
+    if (st != BI_OK) return st;
+    if (dev < 0 || dev >= 64)
+        return bi_fail(BI_ERR_UNSUPPORTED, "noalloc: device %d", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptrs[dev]) {
+        void *p = nullptr;
+        st = bi_cuda_check(cudaGetSymbolAddress(&p, g_decode_noalloc_scratch),
+                           "noalloc: cudaGetSymbolAddress");
+        if (st != BI_OK) return st;
+        ptrs[dev] = p;
+    }
+    *out = ptrs[dev];
+    return BI_OK;
+}
+
+extern "C" bi_status bi_paged_decode_attn_noalloc(
+    const bi_bf16 *q, const bi_bf16 *k_pool, const bi_bf16 *v_pool,
+    const int32_t *page_table, int max_pages, const int32_t *row_req,
+    const int32_t *kv_len, int B, int max_kv_len, int Hq, int Hkv, int D,
+    float scale, bi_bf16 *out, void *stream) {
+    const size_t need = bi_decode_attn_workspace_size(B, Hq, D, max_kv_len);
+    if (need > (size_t)BI_DECODE_ATTN_NOALLOC_SCRATCH_BYTES)
+        return bi_fail(BI_ERR_WORKSPACE_TOO_SMALL,
+                       "bi_paged_decode_attn_noalloc: B=%d Hq=%d D=%d "
+                       "max_kv_len=%d needs %zu bytes of scratch, more than "
+                       "the fixed %d; use bi_paged_decode_attn with a "
+                       "workspace",
+                       B, Hq, D, max_kv_len, need,
+                       (int)BI_DECODE_ATTN_NOALLOC_SCRATCH_BYTES);
+    void *ws = nullptr;
+    bi_status st = noalloc_scratch(&ws);
+    if (st != BI_OK) return st;
+    // The chunk kernel writes every partial the merge kernel reads, so
+    // nothing left in the array by an earlier call is ever read.
+    return bi_decode_attn_pool(q, k_pool, v_pool, page_table, max_pages,
+                               0x7fffffff, row_req, kv_len, B, max_kv_len, Hq,
+                               Hkv, D, scale, out, ws,
+                               BI_DECODE_ATTN_NOALLOC_SCRATCH_BYTES, 3,
+                               bi_stream(stream));
+}
+
 bi_status bi_prefill_attn_pool(const bi_bf16 *q, const int32_t *cu_q,
                                const int32_t *seg_req, int R, int T,
                                const int32_t *pos, int max_q, int max_kv_len,

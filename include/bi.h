@@ -192,6 +192,40 @@ bi_status bi_paged_decode_attn(const bi_bf16 *q, const bi_bf16 *k_pool,
                                float scale, bi_bf16 *out, void *ws,
                                size_t ws_bytes, void *stream);
 
+/* Allocation-free variant of bi_paged_decode_attn (the pages have no
+ * counterpart of this entry point: it exists for callers of this library).
+ *
+ * For callers that cannot allocate device memory for a workspace: code whose
+ * device memory is owned and handed out by another runtime that offers no
+ * scratch buffer, or a latency-bound caller that must not enter an allocator
+ * on the decode path.  The chunk partials go to one fixed scratch array of
+ * BI_DECODE_ATTN_NOALLOC_SCRATCH_BYTES that is part of the library's device
+ * module: every GPU that loads the library holds it until the process exits.
+ * Arguments and results are those of bi_paged_decode_attn without ws and
+ * ws_bytes; the bits of `out` are identical to it.
+ *   - Calls whose bi_decode_attn_workspace_size(B, Hq, D, max_kv_len) exceeds
+ *     the scratch size return BI_ERR_WORKSPACE_TOO_SMALL without launching
+ *     (with D = 128 and Hq = 32: B * ceil(max_kv_len / 256) <= 992, e.g.
+ *     62 rows of up to 4096 positions or 248 rows of up to 1024).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream
+ *     capture.  No call allocates or frees device memory.
+ *   - Every call uses the same array.  Nothing in it needs to start at zero
+ *     (each call writes every partial it reads), but calls whose kernels
+ *     overlap on the GPU (different streams, no ordering between them) race
+ *     on it and give wrong results: order them on one stream. */
+#define BI_DECODE_ATTN_NOALLOC_SCRATCH_BYTES (16 * 1024 * 1024)
+
+bi_status bi_paged_decode_attn_noalloc(const bi_bf16 *q,
+                                       const bi_bf16 *k_pool,
+                                       const bi_bf16 *v_pool,
+                                       const int32_t *page_table,
+                                       int max_pages, const int32_t *row_req,
+                                       const int32_t *kv_len, int B,
+                                       int max_kv_len, int Hq, int Hkv, int D,
+                                       float scale, bi_bf16 *out,
+                                       void *stream);
+
 /* Several queries per request (prefill, verify).  Rows of segment r are
  * cu_q[r] .. cu_q[r+1]-1 (device int32 [R+1], cu_q[0] = 0,
  * cu_q[R] = T); seg_req int32 [R] is the segment's page-table row;
