@@ -7,30 +7,37 @@
 // depends only on its query vector, its position and the logical KV prefix:
 //
 //   chunk c covers absolute positions [256c, 256c + 256).  For each chunk a
-//   partial (m, l, o) is computed FROM SCRATCH by chunk_partial() below:
+//   partial (m, l, o) is computed FROM SCRATCH by chunk_phase1/chunk_phase2
+//   with NW compute warps (a compile-time constant per head dimension):
 //     s_j = (q . k_j) * scale   mma.sync m16n8k16, dims in ascending 16-steps
 //     s_j = -inf past the row's context
 //     m   = max_j s_j
 //     p_j = exp(s_j - m)
-//     l   = sum_j p_j           fixed order: per thread 16 values in key
-//                               order, quad xor-tree (1, 2), 4 warps in order
+//     l   = sum_j p_j           fixed order: per thread its values in key
+//                               order, quad xor-tree (1, 2), warps in order
 //     o   = sum_j bf16(p_j) v_j mma.sync, keys in ascending 16-steps
-//   chunks are merged in ascending c by merge_step():
+//   chunks are merged in ascending c by merge_scalars/merge_value:
 //     m' = max(m, m_c); a = exp(m - m'); b = exp(m_c - m')
 //     l  = l a + l_c b;  o = o a + o_c b;   out = bf16(o / l)
 //
-// Decode computes each chunk in its own CTA, stores the partials and merges
-// them in a second kernel; prefill loops over the chunks inside one CTA and
-// merges in registers.  Both run the same two functions with the same warp
-// and lane mapping, and every floating-point operation outside the MMAs is an
-// explicit round-to-nearest intrinsic, so no contraction can differ.  A row
-// sits in a 16-row MMA tile (decode: the G query heads of one KV head;
-// prefill: 16/G queries x G heads); the tensor core treats rows
-// independently, so the other rows of the tile do not matter.
+// Decode computes every (row, chunk, KV head) item in a persistent,
+// warp-specialised kernel: a producer warp looks up the pages and issues TMA
+// loads into a ring of shared-memory slots, the compute warps run the two
+// phases; a second kernel merges the stored partials.  Prefill loops over
+// the chunks of a 16-row query tile inside one CTA (cp.async loads) and
+// merges in registers.  Both run the same phase and merge functions with the
+// same warp and lane mapping on the same shared-memory tile layout, and every
+// floating-point operation outside the MMAs is an explicit round-to-nearest
+// intrinsic, so no contraction can differ.  A row sits in a 16-row MMA tile
+// (decode: the G query heads of one KV head; prefill: 16/G queries x G
+// heads); the tensor core treats rows independently, so the other rows of
+// the tile do not matter.
 //
-// KV pages are read with 16-byte cp.async copies into an XOR-swizzled shared
-// tile; positions past the context are zero-filled (stale pages may hold
-// NaN, and 0 * NaN would poison the PV product).
+// Positions past a row's context never contribute: their scores are
+// replaced by -inf (a select, so stale or NaN keys cannot leak) and their
+// p is 0 without evaluating exp (exp(-inf) is 0 as well), and the V rows past
+// the visible part of a chunk are zero-filled (0 * NaN would poison the PV
+// product).
 #include <algorithm>
 #include <mutex>
 
@@ -40,136 +47,103 @@
 namespace {
 
 constexpr int CHUNK = 256;
-constexpr int ATT_THREADS = 128;  // 4 warps
+constexpr int RING = 3;               // decode tile slots
 
-// Shared-memory pieces common to both kernels ("misc"): the 16-row query
-// tile, the bf16 P tile, the cross-warp reduction slots and the per-row
-// visible key counts.
+// Compute warps per chunk: 16 for head_dim 128 (each warp 16 keys in the
+// score phase, 8 dims in the PV phase), 4 for head_dim 32.
 template <int D>
-struct Misc {
-    static constexpr int Q_OFF = 0;
-    static constexpr int P_OFF = Q_OFF + 16 * D * 2;
-    static constexpr int RED_OFF = P_OFF + 16 * CHUNK * 2;   // float [128]
-    static constexpr int LEN_OFF = RED_OFF + 128 * 4;        // int [16]
-    static constexpr int BYTES = LEN_OFF + 16 * 4;
-};
+constexpr int nwarps() { return D == 128 ? 16 : 4; }
+template <int D>
+constexpr int cthreads() { return nwarps<D>() * 32; }
 
-// One K or V tile of a chunk: 256 positions x D, bf16.
+// Byte offset of 16-byte piece `ch` (0 .. D/8 - 1) of row `row` in a K, V
+// or Q tile of ROWS rows.  D = 128: two 64-column halves, each [ROWS][128 B]
+// laid out as the TMA 128-byte swizzle writes it (piece XOR row % 8), so
+// ldmatrix row groups hit distinct banks.  D = 32: plain [ROWS][64 B].
+template <int D, int ROWS>
+__device__ __forceinline__ uint32_t toff(int row, int ch) {
+    if constexpr (D == 128) {
+        return (uint32_t)((ch >> 3) * (ROWS * 128) + row * 128 +
+                          (((ch & 7) ^ (row & 7)) << 4));
+    } else {
+        return (uint32_t)(row * (D * 2) + ch * 16);
+    }
+}
+
+// P tile (bf16 [16][256]) offset: 32 pieces per row, XOR-swizzled.
+__device__ __forceinline__ uint32_t poff(int row, int ch) {
+    return (uint32_t)(row * 512 + ((ch ^ (row & 7)) << 4));
+}
+
 template <int D>
 constexpr int tile_bytes() { return CHUNK * D * 2; }
-
-// Prefill layout: K tile, V tile, misc.
 template <int D>
-constexpr int prefill_smem() { return 2 * tile_bytes<D>() + Misc<D>::BYTES; }
-
-// Decode layout: a ring of three tile slots, misc.
+constexpr int qtile_bytes() { return 16 * D * 2; }
+constexpr int P_BYTES = 16 * CHUNK * 2;
+// cross-warp slots: row maxima [NW][16], then row sums [NW][16]
 template <int D>
-constexpr int decode_smem() { return 3 * tile_bytes<D>() + Misc<D>::BYTES; }
+constexpr int red_bytes() { return 2 * nwarps<D>() * 16 * 4; }
 
-// Byte offset of 16-byte piece `ch` of row `row` in a tile of rows of
-// `nch` pieces, XOR-swizzled so that ldmatrix row groups hit distinct banks.
-__device__ __forceinline__ uint32_t swz(int row, int ch, int nch) {
-    const int m = nch >= 8 ? 7 : nch - 1;
-    return (uint32_t)(row * nch * 16 + ((ch ^ (row & m)) * 16));
-}
-
-// Issue (not commit) the cp.async copies of chunk c of KV head g of the
-// page-table row pt_row from `pool` into the tile at shared address `base`.
-// Positions >= valid_max are zero-filled.
-template <int D>
-__device__ __forceinline__ void load_tile(uint32_t base,
-                                          const uint16_t *__restrict__ pool,
-                                          const int32_t *__restrict__ pt_row,
-                                          int max_pages, int n_pages, int Hkv,
-                                          int g, int c, int valid_max,
-                                          int32_t *status) {
-    constexpr int NCH = D / 8;
-#pragma unroll 4
-    for (int idx = threadIdx.x; idx < CHUNK * NCH; idx += ATT_THREADS) {
-        const int key = idx / NCH, ch = idx % NCH;
-        const int p = c * CHUNK + key;
-        const uint16_t *src = pool;
-        uint32_t bytes = 0;
-        if (p < valid_max) {
-            const int pi = p >> 4;
-            const int pg = pi < max_pages ? pt_row[pi] : -1;
-            if (pg >= 0 && pg < n_pages) {
-                src = pool + (((int64_t)pg * Hkv + g) * 16 + (p & 15)) * D +
-                      ch * 8;
-                bytes = 16;
-            } else {
-                bi_record_error(status, BI_ERR_BOUNDS);
-            }
-        }
-        cp_async16(base + swz(key, ch, NCH), src, bytes);
-    }
-}
-
-// Store the 16-row query tile: row r <- q + row_off[r] (row_off < 0 ->
-// zeros).
-template <int D>
-__device__ __forceinline__ void store_q(uint8_t *misc, const uint16_t *q,
-                                        const int64_t *row_off /* [16] */) {
-    constexpr int NCH = D / 8;
-    for (int idx = threadIdx.x; idx < 16 * NCH; idx += ATT_THREADS) {
-        const int r = idx / NCH, ch = idx % NCH;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (row_off[r] >= 0)
-            v = *reinterpret_cast<const uint4 *>(q + row_off[r] + ch * 8);
-        *reinterpret_cast<uint4 *>(misc + Misc<D>::Q_OFF + swz(r, ch, NCH)) = v;
-    }
+// Barrier among the compute threads: the whole CTA (BAR = 0) or the compute
+// warps of the decode kernel (named barrier BAR).
+template <int D, int BAR>
+__device__ __forceinline__ void compute_sync() {
+    if constexpr (BAR == 0)
+        __syncthreads();
+    else
+        asm volatile("bar.sync %0, %1;" ::"n"(BAR), "n"(cthreads<D>())
+                     : "memory");
 }
 
 // ---------------------------------------------------------------------------
-// The partial (m, l, o) of the 16-row query tile against one chunk, in two
-// phases so that the caller can overlap the V copy with phase 1.
+// The partial (m, l, o) of a 16-row query tile against one chunk, in two
+// phases so that loads can overlap phase 1.
 //
-// Phase 1 (needs the Q tile, valid_len and the K tile visible): scores
-// s = (q . k) * scale with mma.sync m16n8k16 (warp w takes keys
-// [64w, 64w + 64), dims in ascending 16-steps), masked past each row's
-// visible count, the row maximum m, p = exp(s - m), the bf16 P tile and the
-// per-warp partial row sums (each thread adds its 16 values in key order,
-// then a quad xor-tree over lanes 1, 2).  Every thread returns m for its
-// rows rg = lane/4 and rg + 8.  Ends after writing shared memory; the caller
-// must __syncthreads before phase 2.
-template <int D>
-__device__ __forceinline__ void chunk_phase1(uint32_t ktile, uint8_t *misc,
-                                             float scale, float m[2]) {
-    constexpr int NCH = D / 8;
+// Phase 1 (Q and K tiles visible): scores s = (q . k) * scale with
+// mma.sync m16n8k16 (warp w takes keys [w*KPW, (w+1)*KPW), dims in ascending
+// 16-steps), masked past len0 (row rg = lane/4) and len1 (row rg + 8), the
+// row maximum m, p = exp(s - m), the bf16 P tile and the per-warp partial row
+// sums (each thread adds its values in key order, then a quad xor-tree over
+// lanes 1, 2).  Returns m for rows rg and rg + 8.  Ends after writing shared
+// memory; the caller must synchronise the compute threads before phase 2.
+template <int D, int BAR>
+__device__ __forceinline__ void chunk_phase1(uint32_t ktile, uint32_t qtile,
+                                             uint32_t ptile, float *red,
+                                             float scale, int len0, int len1,
+                                             float m[2]) {
+    constexpr int NW = nwarps<D>();
+    constexpr int KPW = CHUNK / NW;   // keys per warp
+    constexpr int NT = KPW / 8;       // score n-tiles per warp
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rg = lane >> 2, tq = lane & 3;
-    const uint32_t qbase = smem_u32(misc + Misc<D>::Q_OFF);
-    float *red = reinterpret_cast<float *>(misc + Misc<D>::RED_OFF);
-    const int *valid_len = reinterpret_cast<const int *>(misc + Misc<D>::LEN_OFF);
 
-    float sc[8][4];
+    float sc[NT][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+    for (int i = 0; i < NT; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
         uint32_t a0, a1, a2, a3;
         {
             const int r = (lane & 7) + 8 * ((lane >> 3) & 1);
             const int ch = 2 * ks + (lane >> 4);
-            ldsm_x4(qbase + swz(r, ch, NCH), a0, a1, a2, a3);
+            ldsm_x4(qtile + toff<D, 16>(r, ch), a0, a1, a2, a3);
         }
 #pragma unroll
-        for (int np = 0; np < 4; ++np) {
-            const int key = 64 * warp + 16 * np + (lane & 7) + 8 * (lane >> 4);
+        for (int np = 0; np < NT / 2; ++np) {
+            const int key = KPW * warp + 16 * np + (lane & 7) + 8 * (lane >> 4);
             const int ch = 2 * ks + ((lane >> 3) & 1);
             uint32_t b0, b1, b2, b3;
-            ldsm_x4(ktile + swz(key, ch, NCH), b0, b1, b2, b3);
+            ldsm_x4(ktile + toff<D, CHUNK>(key, ch), b0, b1, b2, b3);
             mma_16816(sc[2 * np], a0, a1, a2, a3, b0, b1);
             mma_16816(sc[2 * np + 1], a0, a1, a2, a3, b2, b3);
         }
     }
-    const int len0 = valid_len[rg], len1 = valid_len[rg + 8];
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
+    for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-            const int key = 64 * warp + 8 * nt + 2 * tq + e;
+            const int key = KPW * warp + 8 * nt + 2 * tq + e;
             float s0 = __fmul_rn(sc[nt][e], scale);
             float s1 = __fmul_rn(sc[nt][2 + e], scale);
             s0 = key < len0 ? s0 : -INFINITY;
@@ -188,63 +162,71 @@ __device__ __forceinline__ void chunk_phase1(uint32_t ktile, uint8_t *misc,
         red[warp * 16 + rg] = mx0;
         red[warp * 16 + rg + 8] = mx1;
     }
-    __syncthreads();
-    const float m0 = fmaxf(fmaxf(red[rg], red[16 + rg]),
-                           fmaxf(red[32 + rg], red[48 + rg]));
-    const float m1 = fmaxf(fmaxf(red[8 + rg], red[24 + rg]),
-                           fmaxf(red[40 + rg], red[56 + rg]));
+    compute_sync<D, BAR>();
+    float m0 = red[rg], m1 = red[8 + rg];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) {
+        m0 = fmaxf(m0, red[w * 16 + rg]);
+        m1 = fmaxf(m1, red[w * 16 + 8 + rg]);
+    }
     const float mu0 = m0 == -INFINITY ? 0.f : m0;
     const float mu1 = m1 == -INFINITY ? 0.f : m1;
 
     float l0 = 0.f, l1 = 0.f;
-    uint8_t *P = misc + Misc<D>::P_OFF;
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-        const float p00 = expf(__fsub_rn(sc[nt][0], mu0));
-        const float p01 = expf(__fsub_rn(sc[nt][1], mu0));
-        const float p10 = expf(__fsub_rn(sc[nt][2], mu1));
-        const float p11 = expf(__fsub_rn(sc[nt][3], mu1));
+    for (int nt = 0; nt < NT; ++nt) {
+        const int key = KPW * warp + 8 * nt + 2 * tq;  // even: a 4-byte pair
+        const float p00 = key < len0 ? expf(__fsub_rn(sc[nt][0], mu0)) : 0.f;
+        const float p01 = key + 1 < len0 ? expf(__fsub_rn(sc[nt][1], mu0)) : 0.f;
+        const float p10 = key < len1 ? expf(__fsub_rn(sc[nt][2], mu1)) : 0.f;
+        const float p11 = key + 1 < len1 ? expf(__fsub_rn(sc[nt][3], mu1)) : 0.f;
         l0 = __fadd_rn(__fadd_rn(l0, p00), p01);
         l1 = __fadd_rn(__fadd_rn(l1, p10), p11);
-        const int key = 64 * warp + 8 * nt + 2 * tq;  // even: a 4-byte pair
         const int ch = key >> 3, within = (key & 7) * 2;
-        *reinterpret_cast<uint32_t *>(P + swz(rg, ch, 32) + within) =
-            pack_bf16x2(p00, p01);
-        *reinterpret_cast<uint32_t *>(P + swz(rg + 8, ch, 32) + within) =
-            pack_bf16x2(p10, p11);
+        asm volatile("st.shared.b32 [%0], %1;" ::"r"(ptile + poff(rg, ch) +
+                                                       within),
+                     "r"(pack_bf16x2(p00, p01))
+                     : "memory");
+        asm volatile("st.shared.b32 [%0], %1;" ::"r"(ptile + poff(rg + 8, ch) +
+                                                       within),
+                     "r"(pack_bf16x2(p10, p11))
+                     : "memory");
     }
     l0 = __fadd_rn(l0, __shfl_xor_sync(0xffffffffu, l0, 1));
     l0 = __fadd_rn(l0, __shfl_xor_sync(0xffffffffu, l0, 2));
     l1 = __fadd_rn(l1, __shfl_xor_sync(0xffffffffu, l1, 1));
     l1 = __fadd_rn(l1, __shfl_xor_sync(0xffffffffu, l1, 2));
     if (tq == 0) {
-        red[64 + warp * 16 + rg] = l0;
-        red[64 + warp * 16 + rg + 8] = l1;
+        red[NW * 16 + warp * 16 + rg] = l0;
+        red[NW * 16 + warp * 16 + rg + 8] = l1;
     }
     m[0] = m0;
     m[1] = m1;
 }
 
-// Phase 2 (after a __syncthreads that follows phase 1 and the V copy): the
-// row sums l = ((w0 + w1) + w2) + w3 over the per-warp partials and
-// o = P V with mma.sync (warp w takes dims [w*D/4, (w+1)*D/4), keys in
-// ascending 16-steps).  Each thread gets o[nt][0..1] for row rg and
-// o[nt][2..3] for row rg + 8, dims w*D/4 + 8*nt + 2*(lane%4) + {0,1}.
+// Phase 2 (after a compute-thread barrier that follows phase 1 and the V
+// copy): the row sums l = (..((w0 + w1) + w2) ..) + w_{NW-1} over the
+// per-warp partials, and o = P V with mma.sync (warp w takes dims
+// [w*DPW, (w+1)*DPW), keys in ascending 16-steps).  Each thread gets
+// o[nt][0..1] for row rg and o[nt][2..3] for row rg + 8, dims
+// w*DPW + 8*nt + 2*(lane%4) + {0,1}.
 template <int D>
-__device__ __forceinline__ void chunk_phase2(uint32_t vtile, uint8_t *misc,
-                                             float l[2], float o[D / 32][4]) {
-    constexpr int NCH = D / 8;
-    constexpr int NTV = D / 32;
+__device__ __forceinline__ void chunk_phase2(uint32_t vtile, uint32_t ptile,
+                                             const float *red, float l[2],
+                                             float o[][4]) {
+    constexpr int NW = nwarps<D>();
+    constexpr int DPW = D / NW;       // dims per warp
+    constexpr int NTV = DPW / 8;      // PV n-tiles per warp
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rg = lane >> 2;
-    const uint32_t pbase = smem_u32(misc + Misc<D>::P_OFF);
-    const float *red = reinterpret_cast<const float *>(misc + Misc<D>::RED_OFF);
-    l[0] = __fadd_rn(__fadd_rn(__fadd_rn(red[64 + rg], red[80 + rg]),
-                               red[96 + rg]),
-                     red[112 + rg]);
-    l[1] = __fadd_rn(__fadd_rn(__fadd_rn(red[72 + rg], red[88 + rg]),
-                               red[104 + rg]),
-                     red[120 + rg]);
+    float la = red[NW * 16 + rg], lb = red[NW * 16 + 8 + rg];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) {
+        la = __fadd_rn(la, red[NW * 16 + w * 16 + rg]);
+        lb = __fadd_rn(lb, red[NW * 16 + w * 16 + 8 + rg]);
+    }
+    l[0] = la;
+    l[1] = lb;
 #pragma unroll
     for (int nt = 0; nt < NTV; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
 #pragma unroll 4
@@ -253,22 +235,23 @@ __device__ __forceinline__ void chunk_phase2(uint32_t vtile, uint8_t *misc,
         {
             const int r = (lane & 7) + 8 * ((lane >> 3) & 1);
             const int ch = 2 * kk + (lane >> 4);
-            ldsm_x4(pbase + swz(r, ch, 32), a0, a1, a2, a3);
+            ldsm_x4(ptile + poff(r, ch), a0, a1, a2, a3);
         }
         const int key = 16 * kk + (lane & 7) + 8 * ((lane >> 3) & 1);
         if constexpr (NTV >= 2) {
 #pragma unroll
             for (int np = 0; np < NTV / 2; ++np) {
-                const int dim = warp * (D / 4) + 16 * np + 8 * (lane >> 4);
+                const int dim = warp * DPW + 16 * np + 8 * (lane >> 4);
                 uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(vtile + swz(key, dim >> 3, NCH), b0, b1, b2, b3);
+                ldsm_x4_t(vtile + toff<D, CHUNK>(key, dim >> 3), b0, b1, b2,
+                          b3);
                 mma_16816(o[2 * np], a0, a1, a2, a3, b0, b1);
                 mma_16816(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
             }
         } else {
-            const int dim = warp * (D / 4);
+            const int dim = warp * DPW;
             uint32_t b0, b1;
-            ldsm_x2_t(vtile + swz(key, dim >> 3, NCH), b0, b1);
+            ldsm_x2_t(vtile + toff<D, CHUNK>(key, dim >> 3), b0, b1);
             mma_16816(o[0], a0, a1, a2, a3, b0, b1);
         }
     }
@@ -292,12 +275,30 @@ __device__ __forceinline__ float merge_value(float O, float o, float a,
 template <int D>
 constexpr int rec_floats() { return D + 4; }
 
-// Number of chunks of each decode row (0 for pad rows), as an exclusive
-// prefix: prefix[b] = sum of the counts of rows 0..b-1, prefix[B] = total.
-// One block; the integer scan is exact, so its order does not matter.
-__global__ void chunk_prefix_kernel(const int32_t *__restrict__ kv_len,
-                                    const int32_t *__restrict__ row_req, int B,
-                                    int Cmax, int32_t *__restrict__ prefix) {
+// Zero the 16-byte pieces of rows [from, 256) of a tile (compute threads).
+template <int D>
+__device__ __forceinline__ void zero_rows(uint32_t tile, int from) {
+    constexpr int NCH = D / 8;
+    for (int idx = threadIdx.x; idx < (CHUNK - from) * NCH;
+         idx += cthreads<D>()) {
+        const int row = from + idx / NCH, ch = idx % NCH;
+        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(
+                         tile + toff<D, CHUNK>(row, ch)),
+                     "r"(0)
+                     : "memory");
+    }
+}
+
+// ------------------------------------------------------------------ decode --
+
+// Work list of the decode kernels: for each row b with row_req >= 0 and a
+// context within bounds, C_b = ceil(kv_len / 256) chunks.  prefix[b] is the
+// exclusive prefix of C_b (prefix[B] = total) and items[prefix[b] + c] =
+// (b, c).  One block; integer scans are exact, so their order is free.
+__global__ void build_items_kernel(const int32_t *__restrict__ kv_len,
+                                   const int32_t *__restrict__ row_req, int B,
+                                   int Cmax, int32_t *__restrict__ prefix,
+                                   int2 *__restrict__ items) {
     __shared__ int carry, wsum[32];
     if (threadIdx.x == 0) carry = 0;
     __syncthreads();
@@ -327,91 +328,167 @@ __global__ void chunk_prefix_kernel(const int32_t *__restrict__ kv_len,
             wsum[lane] = x;
         }
         __syncthreads();
-        const int before = carry + (w > 0 ? wsum[w - 1] : 0);
-        if (b < B) prefix[b] = before + inc - cnt;
+        const int before = carry + (w > 0 ? wsum[w - 1] : 0) + inc - cnt;
+        if (b < B) {
+            prefix[b] = before;
+            for (int c = 0; c < cnt; ++c) items[before + c] = make_int2(b, c);
+        }
         __syncthreads();
-        if (threadIdx.x == blockDim.x - 1) carry = before + inc;
+        if (threadIdx.x == blockDim.x - 1) carry = before + cnt;
         __syncthreads();
     }
     if (threadIdx.x == 0) prefix[B] = carry;
 }
 
-// Decode chunk partials, persistent: CTA k takes work items k, k + grid,
-// k + 2 grid, ...; item i is KV head i % Hkv of chunk j = i / Hkv in the
-// row-major list of (row, chunk) pairs.  K and V tiles stream through a ring
-// of three shared-memory slots (item n: K in slot 2n mod 3, V in slot
-// 2n + 1 mod 3), so the copies of item n + 1 are in flight while item n is
-// computed.  The arithmetic of each item is chunk_phase1 + chunk_phase2,
-// exactly as in the prefill kernel.
+// Shared-memory layout of the decode kernel (offsets from a 1024-aligned
+// base): RING tile slots, RING query slots, the P tile, the reduction slots,
+// then the mbarriers.
 template <int D>
-__global__ void __launch_bounds__(ATT_THREADS, 1)
-    decode_chunks_kernel(const uint16_t *__restrict__ q,
-                         const uint16_t *__restrict__ kp,
-                         const uint16_t *__restrict__ vp,
+struct DecSmem {
+    static constexpr int SLOT = 0;
+    static constexpr int QSLOT = SLOT + RING * tile_bytes<D>();
+    static constexpr int P = QSLOT + RING * qtile_bytes<D>();
+    static constexpr int RED = P + P_BYTES;
+    static constexpr int BAR = RED + red_bytes<D>();     // full[], empty[]
+    static constexpr int BYTES = BAR + 2 * RING * 8;
+    static constexpr int ALLOC = BYTES + 1024;           // alignment slack
+};
+
+// Persistent decode chunk kernel.  CTA k takes work items k, k + grid,
+// k + 2 grid, ...; item i is KV head i % Hkv of list entry i / Hkv.  Item n
+// of a CTA loads K (with the Q rows) into slot 2n mod RING and V into slot
+// 2n + 1 mod RING.  The last warp is the producer: it waits for a slot to be
+// freed, reads the chunk's page ids (one lane per page) and issues one TMA
+// box per page and 64-column half.  The compute warps wait for the tiles,
+// run the two phases and store the partial record.
+template <int D>
+__global__ void __launch_bounds__(cthreads<D>() + 32, 1)
+    decode_chunks_kernel(const __grid_constant__ CUtensorMap kmap,
+                         const __grid_constant__ CUtensorMap vmap,
+                         const __grid_constant__ CUtensorMap qmap,
                          const int32_t *__restrict__ page_table, int max_pages,
                          int n_pages, const int32_t *__restrict__ row_req,
-                         const int32_t *__restrict__ kv_len, int B, int Hq,
-                         int Hkv, int G, float scale, float *__restrict__ ws,
-                         int Cmax, const int32_t *__restrict__ prefix,
-                         int32_t *status) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ int64_t row_off[16];
-    constexpr int TB = tile_bytes<D>();
-    uint8_t *misc = smem + 3 * TB;
-    const uint32_t slot0 = smem_u32(smem);
-    const int total = prefix[B] * Hkv;
+                         const int32_t *__restrict__ kv_len, int Hq, int Hkv,
+                         int G, float scale, float *__restrict__ ws, int Cmax,
+                         const int32_t *__restrict__ prefix, int B,
+                         const int2 *__restrict__ items, int32_t *status) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    using L = DecSmem<D>;
+    constexpr int NW = nwarps<D>();
+    constexpr int DPW = D / NW;
+    constexpr int TB = tile_bytes<D>(), QB = qtile_bytes<D>();
+    constexpr int HALVES = D == 128 ? 2 : 1;
+    constexpr int BOX_W = D == 128 ? 64 : D;            // columns per box
+    constexpr int PAGE_BYTES = 16 * BOX_W * 2;          // one box
+    constexpr int HALF_TILE = CHUNK * BOX_W * 2;        // one half of a tile
+    constexpr int HALF_Q = 16 * BOX_W * 2;
+    const uint32_t base = smem_u32(smem);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::BAR);
+    uint64_t *empty = full + RING;
+    float *red = reinterpret_cast<float *>(smem + L::RED);
+    const uint32_t ptile = base + L::P;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = prefix[B] * Hkv;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < RING; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], NW);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    if (warp == NW) {
+        // ------------------------------------------------------ producer --
+        if (lane == 0) {
+            tma_prefetch_desc(&kmap);
+            tma_prefetch_desc(&vmap);
+            tma_prefetch_desc(&qmap);
+        }
+        bool ok = true;
+        for (int n = 0; ok; ++n) {
+            const int i = blockIdx.x + n * gridDim.x;
+            if (i >= total) break;
+            const int g = i % Hkv;
+            const int2 bc = items[i / Hkv];
+            const int b = bc.x, c = bc.y;
+            const int Lb = kv_len[b];
+            const int vl = min(CHUNK, Lb - c * CHUNK);
+            const int npg = (vl + 15) >> 4;
+            const int32_t *pt_row = page_table + (int64_t)row_req[b] * max_pages;
+            int pg = -1;
+            if (lane < npg) {
+                const int pi = c * 16 + lane;
+                pg = pi < max_pages ? pt_row[pi] : -1;
+                if (pg < 0 || pg >= n_pages) {
+                    bi_record_error(status, BI_ERR_BOUNDS);
+                    pg = -1;
+                }
+            }
+            const unsigned have = __ballot_sync(0xffffffffu, pg >= 0);
+            const int nvalid = __popc(have);
+            for (int kv = 0; kv < 2 && ok; ++kv) {
+                const int j = 2 * n + kv;
+                const int slot = j % RING;
+                const int use = j / RING;
+                bool w_ok = true;
+                if (lane == 0 && use > 0)
+                    w_ok = mbar_wait(&empty[slot], (use - 1) & 1, status);
+                ok = __shfl_sync(0xffffffffu, w_ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
+                if (lane == 0)
+                    mbar_arrive_expect_tx(
+                        &full[slot],
+                        nvalid * HALVES * PAGE_BYTES +
+                            (kv == 0 ? HALVES * HALF_Q : 0));
+                __syncwarp();
+                const CUtensorMap *map = kv == 0 ? &kmap : &vmap;
+                if (pg >= 0) {
+                    const int row = (pg * Hkv + g) * 16;
+#pragma unroll
+                    for (int h = 0; h < HALVES; ++h)
+                        tma_load_2d(smem + L::SLOT + slot * TB + h * HALF_TILE +
+                                        lane * PAGE_BYTES,
+                                    map, h * BOX_W, row, &full[slot]);
+                }
+                if (kv == 0 && lane == 0) {
+#pragma unroll
+                    for (int h = 0; h < HALVES; ++h)
+                        tma_load_2d(smem + L::QSLOT + slot * QB + h * HALF_Q,
+                                    &qmap, h * BOX_W, b * Hq + g * G,
+                                    &full[slot]);
+                }
+            }
+        }
+        return;
+    }
+
+    // ------------------------------------------------------- compute --
     const int rg = lane >> 2, tq = lane & 3;
-
-    // item n of this CTA -> (row b, head g, chunk c); false past the end
-    auto item = [&](int n, int &b, int &g, int &c) -> bool {
+    for (int n = 0;; ++n) {
         const int i = blockIdx.x + n * gridDim.x;
-        if (i >= total) return false;
-        g = i % Hkv;
-        const int j = i / Hkv;
-        int lo = 0, hi = B;  // largest b with prefix[b] <= j
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (prefix[mid] <= j) lo = mid; else hi = mid;
-        }
-        b = lo;
-        c = j - prefix[b];
-        return true;
-    };
-    auto issue = [&](int n, bool is_v, int slot) {
-        int b, g, c;
-        if (item(n, b, g, c))
-            load_tile<D>(slot0 + slot * TB, is_v ? vp : kp,
-                         page_table + (int64_t)row_req[b] * max_pages,
-                         max_pages, n_pages, Hkv, g, c, kv_len[b], status);
-        cp_async_commit();
-    };
-
-    issue(0, false, 0);
-    issue(0, true, 1);
-    issue(1, false, 2);
-    int b, g, c;
-    for (int n = 0; item(n, b, g, c); ++n) {
-        const int L = kv_len[b];
-        int *valid_len = reinterpret_cast<int *>(misc + Misc<D>::LEN_OFF);
-        if (threadIdx.x < 16) {
-            valid_len[threadIdx.x] =
-                threadIdx.x < G ? min(CHUNK, L - c * CHUNK) : 0;
-            row_off[threadIdx.x] =
-                threadIdx.x < G ? ((int64_t)b * Hq + g * G + threadIdx.x) * D
-                                : -1;
-        }
-        __syncthreads();
-        store_q<D>(misc, q, row_off);
-        cp_async_wait<2>();  // K of item n
-        __syncthreads();
-        float m[2], l[2], o[D / 32][4];
-        chunk_phase1<D>(slot0 + ((2 * n) % 3) * TB, misc, scale, m);
-        __syncthreads();     // K slot free, P and row sums visible
-        issue(n + 1, true, (2 * n) % 3);
-        cp_async_wait<2>();  // V of item n
-        __syncthreads();
-        chunk_phase2<D>(slot0 + ((2 * n + 1) % 3) * TB, misc, l, o);
+        if (i >= total) break;
+        const int g = i % Hkv;
+        const int2 bc = items[i / Hkv];
+        const int b = bc.x, c = bc.y;
+        const int vl = min(CHUNK, kv_len[b] - c * CHUNK);
+        const int len0 = rg < G ? vl : 0, len1 = rg + 8 < G ? vl : 0;
+        const int sk = (2 * n) % RING, sv = (2 * n + 1) % RING;
+        if (!mbar_wait(&full[sk], ((2 * n) / RING) & 1, status)) break;
+        float m[2], l[2], o[DPW / 8][4];
+        chunk_phase1<D, 1>(base + L::SLOT + sk * TB, base + L::QSLOT + sk * QB,
+                           ptile, red, scale, len0, len1, m);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[sk]);
+        if (!mbar_wait(&full[sv], ((2 * n + 1) / RING) & 1, status)) break;
+        const uint32_t vtile = base + L::SLOT + sv * TB;
+        if (vl < CHUNK) zero_rows<D>(vtile, vl);
+        compute_sync<D, 1>();
+        chunk_phase2<D>(vtile, ptile, red, l, o);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             const int r = rg + 8 * half;
@@ -423,16 +500,16 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 rec[1] = l[half];
             }
 #pragma unroll
-            for (int nt = 0; nt < D / 32; ++nt) {
-                const int dim = warp * (D / 4) + 8 * nt + 2 * tq;
+            for (int nt = 0; nt < DPW / 8; ++nt) {
+                const int dim = warp * DPW + 8 * nt + 2 * tq;
                 *reinterpret_cast<float2 *>(rec + 4 + dim) =
                     make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
             }
         }
-        __syncthreads();     // V slot free
-        issue(n + 2, false, (2 * n + 1) % 3);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[sv]);
     }
-    cp_async_wait<0>();
 }
 
 // Second stage of decode: one warp per (row, head) merges chunks 0..C-1.
@@ -471,10 +548,48 @@ __global__ void decode_merge_kernel(const float *__restrict__ ws,
         dst[lane * PER + i] = f32_to_bf16(__fdiv_rn(O[i], Ls));
 }
 
+// ----------------------------------------------------------------- prefill --
+
+// Issue (not commit) cp.async copies of chunk c of KV head g of page-table
+// row pt_row into a tile.  Positions >= valid_max are zero-filled.
+template <int D>
+__device__ __forceinline__ void load_tile(uint32_t tile,
+                                          const uint16_t *__restrict__ pool,
+                                          const int32_t *__restrict__ pt_row,
+                                          int max_pages, int n_pages, int Hkv,
+                                          int g, int c, int valid_max,
+                                          int32_t *status) {
+    constexpr int NCH = D / 8;
+#pragma unroll 4
+    for (int idx = threadIdx.x; idx < CHUNK * NCH; idx += cthreads<D>()) {
+        const int key = idx / NCH, ch = idx % NCH;
+        const int p = c * CHUNK + key;
+        const uint16_t *src = pool;
+        uint32_t bytes = 0;
+        if (p < valid_max) {
+            const int pi = p >> 4;
+            const int pg = pi < max_pages ? pt_row[pi] : -1;
+            if (pg >= 0 && pg < n_pages) {
+                src = pool + (((int64_t)pg * Hkv + g) * 16 + (p & 15)) * D +
+                      ch * 8;
+                bytes = 16;
+            } else {
+                bi_record_error(status, BI_ERR_BOUNDS);
+            }
+        }
+        cp_async16(tile + toff<D, CHUNK>(key, ch), src, bytes);
+    }
+}
+
+template <int D>
+constexpr int prefill_smem() {
+    return 2 * tile_bytes<D>() + qtile_bytes<D>() + P_BYTES + red_bytes<D>();
+}
+
 // Prefill / verify: CTA = (16-row tile of one segment, KV head g); loops
 // over the chunks and merges in registers with the same functions.
 template <int D>
-__global__ void __launch_bounds__(ATT_THREADS)
+__global__ void __launch_bounds__(cthreads<D>())
     prefill_kernel(const uint16_t *__restrict__ q,
                    const int32_t *__restrict__ cu_q,
                    const int32_t *__restrict__ seg_req, int R,
@@ -485,12 +600,17 @@ __global__ void __launch_bounds__(ATT_THREADS)
                    int n_pages, int Hq, int Hkv, int G, float scale,
                    int max_kv_len, uint16_t *__restrict__ out,
                    int32_t *status) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ int64_t row_off[16];
+    extern __shared__ __align__(1024) uint8_t smem[];
     __shared__ int s_info[4];  // t0, nq, req, valid_max
     constexpr int TB = tile_bytes<D>();
+    constexpr int NCH = D / 8;
+    constexpr int NT = cthreads<D>();
+    constexpr int DPW = D / nwarps<D>();
     const uint32_t ktile = smem_u32(smem), vtile = ktile + TB;
-    uint8_t *misc = smem + 2 * TB;
+    const uint32_t qtile = vtile + TB;
+    const uint32_t ptile = qtile + qtile_bytes<D>();
+    float *red = reinterpret_cast<float *>(smem + 2 * TB + qtile_bytes<D>() +
+                                           P_BYTES);
     const int g = blockIdx.y;
     const int QPT = 16 / G;
     if (threadIdx.x == 0) {
@@ -519,48 +639,48 @@ __global__ void __launch_bounds__(ATT_THREADS)
     const int rg = lane >> 2, tq = lane & 3;
     if (req < 0 || vmax > max_kv_len) {
         if (req >= 0 && threadIdx.x == 0) bi_record_error(status, BI_ERR_BOUNDS);
-        for (int idx = threadIdx.x; idx < nq * G * D; idx += ATT_THREADS) {
+        for (int idx = threadIdx.x; idx < nq * G * D; idx += NT) {
             const int qi = idx / (G * D), rem = idx % (G * D);
             out[((int64_t)(t0 + qi) * Hq + g * G) * D + rem] = 0;
         }
         return;
     }
-    if (threadIdx.x < 16) {
-        const int qi = threadIdx.x / G, hh = threadIdx.x % G;
-        row_off[threadIdx.x] =
-            qi < nq ? ((int64_t)(t0 + qi) * Hq + g * G + hh) * D : -1;
+    // query tile: row r = (query qi, head hh) with r = qi * G + hh
+    for (int idx = threadIdx.x; idx < 16 * NCH; idx += NT) {
+        const int r = idx / NCH, ch = idx % NCH;
+        const int qi = r / G, hh = r % G;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (qi < nq)
+            v = *reinterpret_cast<const uint4 *>(
+                q + ((int64_t)(t0 + qi) * Hq + g * G + hh) * D + ch * 8);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                         qtile + toff<D, 16>(r, ch)),
+                     "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                     : "memory");
     }
     const int32_t *pt_row = page_table + (int64_t)req * max_pages;
-    int *valid_len = reinterpret_cast<int *>(misc + Misc<D>::LEN_OFF);
     const int p_r0 = (rg / G) < nq ? pos[t0 + rg / G] : -1;
     const int p_r1 = ((rg + 8) / G) < nq ? pos[t0 + (rg + 8) / G] : -1;
     const int C = (vmax + CHUNK - 1) / CHUNK;
 
-    float M[2] = {0.f, 0.f}, Ls[2] = {0.f, 0.f}, O[D / 32][4];
+    float M[2] = {0.f, 0.f}, Ls[2] = {0.f, 0.f}, O[DPW / 8][4];
     for (int c = 0; c < C; ++c) {
         __syncthreads();  // previous chunk fully consumed
-        if (threadIdx.x < 16) {
-            const int qi = threadIdx.x / G;
-            const int pr = qi < nq ? pos[t0 + qi] : -1;
-            valid_len[threadIdx.x] = max(0, min(CHUNK, pr + 1 - c * CHUNK));
-        }
         load_tile<D>(ktile, kp, pt_row, max_pages, n_pages, Hkv, g, c, vmax,
                      status);
         cp_async_commit();
         load_tile<D>(vtile, vp, pt_row, max_pages, n_pages, Hkv, g, c, vmax,
                      status);
         cp_async_commit();
-        if (c == 0) {
-            __syncthreads();
-            store_q<D>(misc, q, row_off);
-        }
+        const int len0 = max(0, min(CHUNK, p_r0 + 1 - c * CHUNK));
+        const int len1 = max(0, min(CHUNK, p_r1 + 1 - c * CHUNK));
         cp_async_wait<1>();
         __syncthreads();
-        float m[2], l[2], o[D / 32][4];
-        chunk_phase1<D>(ktile, misc, scale, m);
+        float m[2], l[2], o[DPW / 8][4];
+        chunk_phase1<D, 0>(ktile, qtile, ptile, red, scale, len0, len1, m);
         cp_async_wait<0>();
         __syncthreads();
-        chunk_phase2<D>(vtile, misc, l, o);
+        chunk_phase2<D>(vtile, ptile, red, l, o);
         const int pr[2] = {p_r0, p_r1};
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
@@ -569,7 +689,7 @@ __global__ void __launch_bounds__(ATT_THREADS)
                 M[half] = m[half];
                 Ls[half] = l[half];
 #pragma unroll
-                for (int nt = 0; nt < D / 32; ++nt) {
+                for (int nt = 0; nt < DPW / 8; ++nt) {
                     O[nt][2 * half] = o[nt][2 * half];
                     O[nt][2 * half + 1] = o[nt][2 * half + 1];
                 }
@@ -577,7 +697,7 @@ __global__ void __launch_bounds__(ATT_THREADS)
                 float a, bb;
                 merge_scalars(M[half], Ls[half], m[half], l[half], a, bb);
 #pragma unroll
-                for (int nt = 0; nt < D / 32; ++nt) {
+                for (int nt = 0; nt < DPW / 8; ++nt) {
                     O[nt][2 * half] = merge_value(O[nt][2 * half],
                                                   o[nt][2 * half], a, bb);
                     O[nt][2 * half + 1] = merge_value(
@@ -594,14 +714,16 @@ __global__ void __launch_bounds__(ATT_THREADS)
         const int qi = r / G, hh = r % G;
         uint16_t *dst = out + ((int64_t)(t0 + qi) * Hq + g * G + hh) * D;
 #pragma unroll
-        for (int nt = 0; nt < D / 32; ++nt) {
-            const int dim = warp * (D / 4) + 8 * nt + 2 * tq;
+        for (int nt = 0; nt < DPW / 8; ++nt) {
+            const int dim = warp * DPW + 8 * nt + 2 * tq;
             *reinterpret_cast<uint32_t *>(dst + dim) =
                 pack_bf16x2(__fdiv_rn(O[nt][2 * half], Ls[half]),
                             __fdiv_rn(O[nt][2 * half + 1], Ls[half]));
         }
     }
 }
+
+// ------------------------------------------------------------------- host --
 
 template <typename K>
 bi_status set_attr(K kernel, int bytes) {
@@ -616,9 +738,35 @@ bool group_ok(int Hq, int Hkv) {
     return G == 1 || G == 2 || G == 4 || G == 8 || G == 16;
 }
 
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+
 size_t records_bytes(int B, int Hq, int D, int max_kv_len) {
     const int C = (max_kv_len + CHUNK - 1) / CHUNK;
-    return ((size_t)B * Hq * C * (D + 4) * sizeof(float) + 255) & ~size_t(255);
+    return up256((size_t)B * Hq * C * (D + 4) * sizeof(float));
+}
+
+template <int D>
+bi_status launch_decode_chunks(const CUtensorMap &km, const CUtensorMap &vm,
+                               const CUtensorMap &qm,
+                               const int32_t *page_table, int max_pages,
+                               int n_pages, const int32_t *row_req,
+                               const int32_t *kv_len, int Hq, int Hkv, int G,
+                               float scale, float *rec, int Cmax,
+                               const int32_t *prefix, int B,
+                               const int2 *items, int32_t *status,
+                               cudaStream_t s) {
+    static std::once_flag f;
+    static bi_status fs;
+    std::call_once(f, [] {
+        fs = set_attr(decode_chunks_kernel<D>, DecSmem<D>::ALLOC);
+    });
+    if (fs != BI_OK) return fs;
+    decode_chunks_kernel<D>
+        <<<bi_sm_count(), cthreads<D>() + 32, DecSmem<D>::ALLOC, s>>>(
+            km, vm, qm, page_table, max_pages, n_pages, row_req, kv_len, Hq,
+            Hkv, G, scale, rec, Cmax, prefix, B, items, status);
+    BI_LAUNCH_CHECK("decode attention launch");
+    return BI_OK;
 }
 
 }  // namespace
@@ -626,8 +774,10 @@ size_t records_bytes(int B, int Hq, int D, int max_kv_len) {
 extern "C" size_t bi_decode_attn_workspace_size(int B, int Hq, int D,
                                                 int max_kv_len) {
     if (B <= 0 || Hq <= 0 || D <= 0 || max_kv_len <= 0) return 0;
+    const int C = (max_kv_len + CHUNK - 1) / CHUNK;
     return records_bytes(B, Hq, D, max_kv_len) +
-           (((size_t)(B + 1) * sizeof(int32_t) + 255) & ~size_t(255));
+           up256((size_t)(B + 1) * sizeof(int32_t)) +
+           up256((size_t)B * C * sizeof(int2));
 }
 
 // Decode attention with the pool size known (page ids are range-checked
@@ -653,6 +803,7 @@ bi_status bi_decode_attn_pool(const bi_bf16 *q, const bi_bf16 *k_pool,
     BI_REQUIRE(bi_aligned16(q) && bi_aligned16(k_pool) && bi_aligned16(v_pool) &&
                    bi_aligned16(out) && bi_aligned16(ws),
                "bi_paged_decode_attn: pointers must be 16-byte aligned");
+    BI_REQUIRE(n_pages > 0, "bi_paged_decode_attn: n_pages=%d", n_pages);
     if (B == 0) return BI_OK;
     const size_t need = bi_decode_attn_workspace_size(B, Hq, D, max_kv_len);
     if (!ws || ws_bytes < need)
@@ -662,38 +813,43 @@ bi_status bi_decode_attn_pool(const bi_bf16 *q, const bi_bf16 *k_pool,
     const int Cmax = (max_kv_len + CHUNK - 1) / CHUNK;
     const int G = Hq / Hkv;
     float *rec = static_cast<float *>(ws);
-    int32_t *prefix = reinterpret_cast<int32_t *>(
-        static_cast<uint8_t *>(ws) + records_bytes(B, Hq, D, max_kv_len));
+    uint8_t *after = static_cast<uint8_t *>(ws) +
+                     records_bytes(B, Hq, D, max_kv_len);
+    int32_t *prefix = reinterpret_cast<int32_t *>(after);
+    int2 *items = reinterpret_cast<int2 *>(
+        after + up256((size_t)(B + 1) * sizeof(int32_t)));
     int32_t *status = bi_status_ptr();
     if (stages & 1) {
-        chunk_prefix_kernel<<<1, 1024, 0, s>>>(kv_len, row_req, B, Cmax,
-                                               prefix);
-        BI_LAUNCH_CHECK("decode chunk prefix launch");
-        const int grid = bi_sm_count();
-        if (D == 128) {
-            static std::once_flag f;
-            static bi_status fs;
-            std::call_once(f, [] {
-                fs = set_attr(decode_chunks_kernel<128>, decode_smem<128>());
-            });
-            if (fs != BI_OK) return fs;
-            decode_chunks_kernel<128><<<grid, ATT_THREADS, decode_smem<128>(),
-                                        s>>>(
-                q, k_pool, v_pool, page_table, max_pages, n_pages, row_req,
-                kv_len, B, Hq, Hkv, G, scale, rec, Cmax, prefix, status);
-        } else {
-            static std::once_flag f;
-            static bi_status fs;
-            std::call_once(f, [] {
-                fs = set_attr(decode_chunks_kernel<32>, decode_smem<32>());
-            });
-            if (fs != BI_OK) return fs;
-            decode_chunks_kernel<32><<<grid, ATT_THREADS, decode_smem<32>(),
-                                       s>>>(
-                q, k_pool, v_pool, page_table, max_pages, n_pages, row_req,
-                kv_len, B, Hq, Hkv, G, scale, rec, Cmax, prefix, status);
-        }
-        BI_LAUNCH_CHECK("decode attention launch");
+        // Pools as 2-D [rows][D] bf16, rows = (page * Hkv + head) * 16 + slot;
+        // queries as [B * Hq][D].  Boxes of 16 rows x 64 columns (D = 128,
+        // 128-byte swizzle) or 16 x 32 (D = 32, no swizzle).
+        const uint64_t pool_rows = (uint64_t)n_pages * Hkv * 16;
+        const uint32_t bw = D == 128 ? 64 : D;
+        CUtensorMap km, vm, qm;
+        bi_status st;
+        if ((st = bi_make_tmap_2d_bf16(&km, k_pool, D, pool_rows, D * 2, bw, 16,
+                                       D == 128)) != BI_OK)
+            return st;
+        if ((st = bi_make_tmap_2d_bf16(&vm, v_pool, D, pool_rows, D * 2, bw, 16,
+                                       D == 128)) != BI_OK)
+            return st;
+        if ((st = bi_make_tmap_2d_bf16(&qm, q, D, (uint64_t)B * Hq, D * 2, bw,
+                                       16, D == 128)) != BI_OK)
+            return st;
+        build_items_kernel<<<1, 1024, 0, s>>>(kv_len, row_req, B, Cmax, prefix,
+                                              items);
+        BI_LAUNCH_CHECK("decode item list launch");
+        if (D == 128)
+            st = launch_decode_chunks<128>(km, vm, qm, page_table, max_pages,
+                                           n_pages, row_req, kv_len, Hq, Hkv,
+                                           G, scale, rec, Cmax, prefix, B,
+                                           items, status, s);
+        else
+            st = launch_decode_chunks<32>(km, vm, qm, page_table, max_pages,
+                                          n_pages, row_req, kv_len, Hq, Hkv, G,
+                                          scale, rec, Cmax, prefix, B, items,
+                                          status, s);
+        if (st != BI_OK) return st;
     }
     if (stages & 2) {
         const int warps = B * Hq;
@@ -709,18 +865,20 @@ bi_status bi_decode_attn_pool(const bi_bf16 *q, const bi_bf16 *k_pool,
     return BI_OK;
 }
 
+// Without the pool size the 2-D maps of the pools are given the largest row
+// count a page id (int32) can address; page ids are trusted below it.
+static int unbounded_pages(int Hkv) { return 0x7fffffff / (Hkv * 16); }
+
 extern "C" bi_status bi_paged_decode_attn(
     const bi_bf16 *q, const bi_bf16 *k_pool, const bi_bf16 *v_pool,
     const int32_t *page_table, int max_pages, const int32_t *row_req,
     const int32_t *kv_len, int B, int max_kv_len, int Hq, int Hkv, int D,
     float scale, bi_bf16 *out, void *ws, size_t ws_bytes, void *stream) {
-    // The pool size is not an argument of this entry point, so page ids are
-    // range-checked against INT32_MAX only; the model driver passes the
-    // real pool size.
+    BI_REQUIRE(Hkv > 0, "bi_paged_decode_attn: Hkv=%d", Hkv);
     return bi_decode_attn_pool(q, k_pool, v_pool, page_table, max_pages,
-                               0x7fffffff, row_req, kv_len, B, max_kv_len, Hq,
-                               Hkv, D, scale, out, ws, ws_bytes, 3,
-                               bi_stream(stream));
+                               unbounded_pages(Hkv), row_req, kv_len, B,
+                               max_kv_len, Hq, Hkv, D, scale, out, ws,
+                               ws_bytes, 3, bi_stream(stream));
 }
 
 // ------------------------------------------- allocation-free decode variant --
@@ -769,14 +927,16 @@ extern "C" bi_status bi_paged_decode_attn_noalloc(
                        "workspace",
                        B, Hq, D, max_kv_len, need,
                        (int)BI_DECODE_ATTN_NOALLOC_SCRATCH_BYTES);
+    BI_REQUIRE(Hkv > 0, "bi_paged_decode_attn_noalloc: Hkv=%d", Hkv);
     void *ws = nullptr;
     bi_status st = noalloc_scratch(&ws);
     if (st != BI_OK) return st;
-    // The chunk kernel writes every partial the merge kernel reads, so
-    // nothing left in the array by an earlier call is ever read.
+    // The chunk kernel writes every partial the merge kernel reads, and the
+    // item list is rebuilt by every call, so nothing left in the array by an
+    // earlier call is ever read.
     return bi_decode_attn_pool(q, k_pool, v_pool, page_table, max_pages,
-                               0x7fffffff, row_req, kv_len, B, max_kv_len, Hq,
-                               Hkv, D, scale, out, ws,
+                               unbounded_pages(Hkv), row_req, kv_len, B,
+                               max_kv_len, Hq, Hkv, D, scale, out, ws,
                                BI_DECODE_ATTN_NOALLOC_SCRATCH_BYTES, 3,
                                bi_stream(stream));
 }
@@ -817,11 +977,19 @@ bi_status bi_prefill_attn_pool(const bi_bf16 *q, const int32_t *cu_q,
             fs = set_attr(prefill_kernel<128>, prefill_smem<128>());
         });
         if (fs != BI_OK) return fs;
-        prefill_kernel<128><<<grid, ATT_THREADS, prefill_smem<128>(), stream>>>(
+        prefill_kernel<128><<<grid, cthreads<128>(), prefill_smem<128>(),
+                              stream>>>(
             q, cu_q, seg_req, R, pos, k_pool, v_pool, page_table, max_pages,
             n_pages, Hq, Hkv, G, scale, max_kv_len, out, status);
     } else {
-        prefill_kernel<32><<<grid, ATT_THREADS, prefill_smem<32>(), stream>>>(
+        static std::once_flag f;
+        static bi_status fs;
+        std::call_once(f, [] {
+            fs = set_attr(prefill_kernel<32>, prefill_smem<32>());
+        });
+        if (fs != BI_OK) return fs;
+        prefill_kernel<32><<<grid, cthreads<32>(), prefill_smem<32>(),
+                             stream>>>(
             q, cu_q, seg_req, R, pos, k_pool, v_pool, page_table, max_pages,
             n_pages, Hq, Hkv, G, scale, max_kv_len, out, status);
     }
