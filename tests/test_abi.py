@@ -81,11 +81,12 @@ def test_bad_arguments_fail_before_launch(bi):
 
 
 def test_decode_workspace_formula(bi):
-    # chunk partials (m, l, pad, o[D]) per (row, head, chunk), then the
-    # per-row chunk prefix (B + 1 ints), each rounded up to 256 bytes
+    # chunk partials (m, l, pad, o[D]) per (row, head, chunk), the per-row
+    # chunk prefix (B + 1 ints) and the (row, chunk) work list (8 bytes per
+    # entry), each rounded up to 256 bytes
     def up(n):
         return (n + 255) // 256 * 256
     assert bi.bi_decode_attn_workspace_size(3, 32, 128, 257) == \
-        up(3 * 32 * 2 * 132 * 4) + up(4 * 4)
+        up(3 * 32 * 2 * 132 * 4) + up(4 * 4) + up(3 * 2 * 8)
     assert bi.bi_decode_attn_workspace_size(1, 4, 32, 16) == \
-        up(1 * 4 * 1 * 36 * 4) + up(2 * 4)
+        up(1 * 4 * 1 * 36 * 4) + up(2 * 4) + up(1 * 1 * 8)
