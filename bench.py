@@ -306,27 +306,25 @@ def algorithmic_bytes(b, cls, launches_per_step):
         chunks = sum(float(np.ceil((ctx + i + 1) / 256).sum())
                      for i in range(it)) / it
         return chunks * Hq * (D + 4) * 4 + B * Hq * D * 2
-    s_qkv = bi.bi_gemm_splits(QKV, H)
-    s_o = bi.bi_gemm_splits(H, Hq * D)
-    s_d = bi.bi_gemm_splits(H, F)
+    # Algorithmic bytes count each tensor the step must read or write once:
+    # a GEMM reads its weight and input and writes its fp32 (or bf16)
+    # result; split-K slices are an implementation choice and not counted.
     if cls == "rope":
-        return s_qkv * B * QKV * 4.0 + B * QKV * 2.0
+        # the fp32 q/k/v row in, q out, k and v appended to the cache
+        return B * QKV * 4.0 + B * QKV * 2.0
     if cls == "norm":
         # per forward: the first attention norm reads the embedded rows; each
-        # later norm sums its slices, updates the residual and writes y
+        # later norm reads the fp32 projection output, updates the residual
+        # and writes y
         Lr = b.args.layers
-        per_fwd = (B * H * 4.0 +
-                   Lr * (s_o * B * H * 4.0 + 3 * B * H * 2.0) +
-                   Lr * (s_d * B * H * 4.0 + 3 * B * H * 2.0))
+        per_fwd = (B * H * 4.0 + 2 * Lr * (B * H * 4.0 + 3 * B * H * 2.0))
         return per_fwd / (2 * Lr + 1)
     gemms = {"gemm_qkv": (QKV, H), "gemm_o": (H, Hq * D),
              "gemm_gate_up": (2 * F, H), "gemm_down": (H, F),
              "lm_head": (S.vocab, H)}
     if cls in gemms:
         N, K = gemms[cls]
-        s = bi.bi_gemm_splits(N, K)
-        out = B * N * 4 * s if cls in ("gemm_qkv", "gemm_o", "gemm_down") else (
-            B * N // 2 * 2 if cls == "gemm_gate_up" else B * N * 4)
+        out = B * N // 2 * 2 if cls == "gemm_gate_up" else B * N * 4
         return 2.0 * N * K + 2.0 * B * K + out
     return None
 

@@ -535,13 +535,31 @@ __global__ void decode_merge_kernel(const float *__restrict__ ws,
     float M = rec[0], Ls = rec[1], O[PER];
 #pragma unroll
     for (int i = 0; i < PER; ++i) O[i] = rec[4 + lane * PER + i];
-    for (int c = 1; c < C; ++c) {
-        const float *rc = rec + (int64_t)c * rec_floats<D>();
-        float a, bb;
-        merge_scalars(M, Ls, rc[0], rc[1], a, bb);
+    // Records are loaded four at a time (independent loads in flight), then
+    // merged strictly in chunk order.
+    constexpr int BATCH = 4;
+    for (int c0 = 1; c0 < C; c0 += BATCH) {
+        float mb[BATCH], lb[BATCH], ob[BATCH][PER];
 #pragma unroll
-        for (int i = 0; i < PER; ++i)
-            O[i] = merge_value(O[i], rc[4 + lane * PER + i], a, bb);
+        for (int j = 0; j < BATCH; ++j) {
+            const int c = c0 + j;
+            if (c < C) {
+                const float *rc = rec + (int64_t)c * rec_floats<D>();
+                mb[j] = rc[0];
+                lb[j] = rc[1];
+#pragma unroll
+                for (int i = 0; i < PER; ++i) ob[j][i] = rc[4 + lane * PER + i];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < BATCH; ++j) {
+            if (c0 + j >= C) break;
+            float a, bb;
+            merge_scalars(M, Ls, mb[j], lb[j], a, bb);
+#pragma unroll
+            for (int i = 0; i < PER; ++i)
+                O[i] = merge_value(O[i], ob[j][i], a, bb);
+        }
     }
 #pragma unroll
     for (int i = 0; i < PER; ++i)

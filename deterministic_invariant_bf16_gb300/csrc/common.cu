@@ -104,6 +104,33 @@ static encode_tiled_fn get_encode() {
     return fn;
 }
 
+bi_status bi_make_tmap_3d(CUtensorMap *map, const void *base, bool f32,
+                          uint64_t d0, uint64_t d1, uint64_t d2,
+                          uint32_t box0, uint32_t box1) {
+    encode_tiled_fn enc = get_encode();
+    if (!enc)
+        return bi_fail(BI_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+    const uint64_t es = f32 ? 4 : 2;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0 * es, d0 * d1 * es};
+    cuuint32_t box[3] = {box0, box1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map,
+                     f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                         : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                     3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return bi_fail(BI_ERR_INVALID_ARG,
+                       "cuTensorMapEncodeTiled (3-D) failed (%d): dims %llu x "
+                       "%llu x %llu",
+                       (int)r, (unsigned long long)d0, (unsigned long long)d1,
+                       (unsigned long long)d2);
+    return BI_OK;
+}
+
 bi_status bi_make_tmap_2d_bf16(CUtensorMap *map, const void *base,
                                uint64_t inner, uint64_t outer,
                                uint64_t row_stride_bytes, uint32_t box_inner,

@@ -16,18 +16,21 @@
 //   - Slices are summed in fp32 in slice order: ((p0 + p1) + p2) + ...
 //
 // Two schedules give the same bits:
-//   split: one CTA per (m-tile, n-tile, slice); slices go to memory as fp32
-//          partials and a consumer (bi_rmsnorm, bi_rope, or the reduce
-//          kernel here) sums them in order.  Fills the GPU at small M.
-//   fused: one CTA per (m-tile, n-tile) runs the slices one after another
-//          into two alternating TMEM accumulators; the epilogue warps add
-//          each finished slice to a register running sum in slice order.
-//          No partial traffic; used when there are enough tiles.
+//   split: a work unit is one (m-tile, n-tile, slice); slices go to memory
+//          as fp32 partials and a consumer (bi_rmsnorm, bi_rope, or the
+//          reduce kernel here) sums them in order.  Fills the GPU at small M.
+//   fused: a work unit is one (m-tile, n-tile) with all its slices run one
+//          after another; the epilogue warps add each finished slice to a
+//          register running sum in slice order.  No partial traffic; used
+//          when there are enough tiles.
 //
-// CTA layout (192 threads): warp 0 lane 0 issues TMA loads into a ring of
-// shared-memory stages; warp 1 owns the TMEM allocation and lane 0 issues
-// the MMAs; warps 2-5 are the epilogue (warp w reads TMEM lanes
-// 32*(w%4) .. 32*(w%4)+31, i.e. tile rows).  Every wait is bounded.
+// Persistent CTAs (one per SM, 192 threads) loop over work units: warp 0
+// lane 0 issues TMA loads into a ring of shared-memory stages; warp 1 owns
+// the TMEM allocation and lane 0 issues the MMAs into a ring of four TMEM
+// accumulators; warps 2-5 are the epilogue (warp w reads TMEM lanes
+// 32*(w%4) .. 32*(w%4)+31, i.e. tile rows), staging each 32-row piece of the
+// result in a 128-byte-swizzled shared buffer and writing it with a TMA
+// store, which clips rows past M and columns past N.  Every wait is bounded.
 #include <algorithm>
 #include <mutex>
 
@@ -42,13 +45,14 @@ constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
 constexpr uint32_t IDESC = make_idesc_bf16(BM, BN);
+constexpr int STAGES = 5;                 // 160 KB of operand stages
+constexpr int NACC = 4;                   // TMEM accumulators (4 x 128 cols)
+constexpr int STORE_BYTES = 32 * 128;     // one staged store: 32 rows x 128 B
+constexpr int EPI_BYTES = 4 * 2 * STORE_BYTES;  // 4 warps x double buffer
 
-// One persistent CTA per SM: six 32 KB stages (~193 KB of shared memory).
-constexpr int STAGES_SPLIT = 6;
-constexpr int STAGES_FUSED = 6;
-
-constexpr size_t smem_bytes(int stages) {
-    return 1024 /* alignment slack */ + (size_t)stages * STAGE_BYTES + 256;
+constexpr size_t smem_bytes() {
+    return 1024 /* alignment slack */ + (size_t)STAGES * STAGE_BYTES +
+           EPI_BYTES + 256;
 }
 
 struct GemmArgs {
@@ -56,53 +60,17 @@ struct GemmArgs {
     int MT;     // m-tiles
     int units;  // work units (see unit_coords)
     int out_kind;
-    void *out;
     int32_t *status;
 };
-
-__device__ __forceinline__ void store_f32_32(float *dst, int n, int N,
-                                             const float *v) {
-    if (n + 32 <= N && (N & 3) == 0) {
-        float4 *d4 = reinterpret_cast<float4 *>(dst + n);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2],
-                                v[4 * i + 3]);
-    } else {
-        for (int i = 0; i < 32; ++i)
-            if (n + i < N) dst[n + i] = v[i];
-    }
-}
-
-__device__ __forceinline__ void store_bf16_32(uint16_t *dst, int n, int N,
-                                              const float *v) {
-    if (n + 32 <= N && (N & 7) == 0) {
-        uint4 *d4 = reinterpret_cast<uint4 *>(dst + n);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            d4[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]),
-                               pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                               pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
-                               pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
-    } else {
-        for (int i = 0; i < 32; ++i)
-            if (n + i < N) dst[n + i] = f32_to_bf16(v[i]);
-    }
-}
 
 // silu(g) * u = (g / (1 + e^-g)) * u, each operation rounded separately.
 __device__ __forceinline__ float swiglu1(float g, float u) {
     return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
 }
 
-// Persistent CTA: one per SM, looping over work units.  A unit is one
-// (m-tile, n-tile, slice) in the split schedule and one (m-tile, n-tile)
-// with all its slices in the fused schedule.  Units are numbered with the
-// m-tile fastest, so CTAs that run at the same time on neighbouring units
-// read the same weight tile (the second read hits L2).  CTA k takes units
-// k, k + grid, k + 2 grid, ...  The shared-memory ring runs on across unit
-// boundaries, and the two TMEM accumulators alternate between consecutive
-// slices, so the epilogue of one slice overlaps the MMAs of the next.
+// Unit u of the schedule.  Units are numbered with the m-tile fastest, so
+// CTAs that run at the same time on neighbouring units read the same weight
+// tile (the second read hits L2).
 template <bool FUSED>
 __device__ __forceinline__ void unit_coords(const GemmArgs &p, int u, int &m0,
                                             int &n0, int &nt, int &s_lo,
@@ -122,22 +90,65 @@ __device__ __forceinline__ void unit_coords(const GemmArgs &p, int u, int &m0,
     n0 = nt * BN;
 }
 
-template <bool FUSED, int STAGES>
+// Epilogue store of one 32-row x 128-byte piece: the calling warp's lane r
+// holds row r as 32 words.  The piece goes into this warp's staging buffer
+// in the layout of the 128-byte TMA swizzle (16-byte unit j of row r at
+// unit j ^ (r % 8), conflict-free for st.shared.v4) and out with one TMA
+// store at (x, y, z).  Two buffers alternate; before reusing one, lane 0
+// waits until the store issued from it has finished reading it.
+struct Stager {
+    uint8_t *buf;   // this warp's two buffers
+    int count;
+
+    __device__ __forceinline__ void put(const CUtensorMap *map,
+                                       const uint32_t *w, int x, int y, int z,
+                                       bool issue) {
+        const int lane = threadIdx.x & 31;
+        uint8_t *b = buf + (count & 1) * STORE_BYTES;
+        if (count >= 2) {
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t addr =
+                smem_u32(b) + lane * 128 + ((j ^ (lane & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                         "r"(w[4 * j]), "r"(w[4 * j + 1]), "r"(w[4 * j + 2]),
+                         "r"(w[4 * j + 3])
+                         : "memory");
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            // One bulk group per piece (empty when the piece lies wholly
+            // outside the output), so the wait above always covers the
+            // store that last read this buffer.
+            if (issue) tma_store_3d(map, b, x, y, z);
+            bulk_commit();
+        }
+        ++count;
+    }
+};
+
+template <bool FUSED>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                const __grid_constant__ CUtensorMap tmB, GemmArgs p) {
+                const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmO, GemmArgs p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + STAGES * A_BYTES;
-    uint64_t *full = reinterpret_cast<uint64_t *>(sB + STAGES * B_BYTES);
+    uint8_t *sE = sB + STAGES * B_BYTES;  // epilogue staging, 1024-aligned
+    uint64_t *full = reinterpret_cast<uint64_t *>(sE + EPI_BYTES);
     uint64_t *empty = full + STAGES;
-    uint64_t *acc_full = empty + STAGES;   // [2]
-    uint64_t *acc_empty = acc_full + 2;    // [2]
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(acc_empty + 2);
+    uint64_t *acc_full = empty + STAGES;     // [NACC]
+    uint64_t *acc_empty = acc_full + NACC;   // [NACC]
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(acc_empty + NACC);
 
-    constexpr uint32_t TMEM_COLS = 2 * BN;
+    constexpr uint32_t TMEM_COLS = NACC * BN;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -145,7 +156,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NACC; ++i) {
             mbar_init(&acc_full[i], 1);
             mbar_init(&acc_empty[i], 4);
         }
@@ -198,9 +209,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             int m0, n0, nt, s_lo, s_hi;
             unit_coords<FUSED>(p, u, m0, n0, nt, s_lo, s_hi);
             for (int s = s_lo; s < s_hi && ok; ++s, ++acc) {
-                const int buf = acc & 1;
-                if (acc >= 2 &&
-                    !mbar_wait(&acc_empty[buf], ((acc >> 1) - 1) & 1,
+                const int buf = acc % NACC;
+                if (acc >= NACC &&
+                    !mbar_wait(&acc_empty[buf], ((acc / NACC) - 1) & 1,
                                p.status)) {
                     ok = false;
                     break;
@@ -232,17 +243,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ---------------------------------------------------- epilogue --
         const int q = warp & 3;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        Stager stg{sE + (warp - 2) * 2 * STORE_BYTES, 0};
         float run[FUSED ? BN : 1];
         int acc = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
             int m0, n0, nt, s_lo, s_hi;
             unit_coords<FUSED>(p, u, m0, n0, nt, s_lo, s_hi);
-            const int row = m0 + q * 32 + lane;
-            const bool live = row < p.M;
+            const int row0 = m0 + q * 32;
+            const bool rows_live = row0 < p.M;
             for (int s = s_lo, j = 0; s < s_hi; ++s, ++j, ++acc) {
-                const int buf = acc & 1;
-                if (!mbar_wait(&acc_full[buf], (acc >> 1) & 1, p.status)) {
+                const int buf = acc % NACC;
+                if (!mbar_wait(&acc_full[buf], (acc / NACC) & 1, p.status)) {
                     ok = false;
                     break;
                 }
@@ -259,69 +271,78 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 (j == 0) ? v[i] : __fadd_rn(run[c + i], v[i]);
                     }
                 } else if (p.out_kind == BI_OUT_SWIGLU) {
-                    const int f0 = nt * (BN / 2);
-                    const int NO = p.N / 2;
+                    uint32_t w[32];
 #pragma unroll
                     for (int c = 0; c < BN / 2; c += 32) {
                         float g[32], uu[32];
                         tmem_ld_32cols(base + c, g);
                         tmem_ld_32cols(base + BN / 2 + c, uu);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) g[i] = swiglu1(g[i], uu[i]);
-                        if (live)
-                            store_bf16_32(reinterpret_cast<uint16_t *>(p.out) +
-                                              (size_t)row * NO,
-                                          f0 + c, NO, g);
+                        for (int i = 0; i < 16; ++i)
+                            w[c / 2 + i] = pack_bf16x2(
+                                swiglu1(g[2 * i], uu[2 * i]),
+                                swiglu1(g[2 * i + 1], uu[2 * i + 1]));
                     }
-                } else {
+                    stg.put(&tmO, w, nt * (BN / 2), row0, 0, rows_live);
+                } else if (p.out_kind == BI_OUT_BF16) {
+#pragma unroll
+                    for (int c = 0; c < BN; c += 64) {
+                        uint32_t w[32];
+                        float v[32];
+                        tmem_ld_32cols(base + c, v);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+                        tmem_ld_32cols(base + c + 32, v);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            w[16 + i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+                        stg.put(&tmO, w, n0 + c, row0, 0,
+                                rows_live && n0 + c < p.N);
+                    }
+                } else {  // fp32: partial slice s (or the only slice)
 #pragma unroll
                     for (int c = 0; c < BN; c += 32) {
                         float v[32];
                         tmem_ld_32cols(base + c, v);
-                        if (!live) continue;
-                        if (p.out_kind == BI_OUT_BF16)
-                            store_bf16_32(reinterpret_cast<uint16_t *>(p.out) +
-                                              (size_t)row * p.N,
-                                          n0 + c, p.N, v);
-                        else  // partial slice s (or the only slice)
-                            store_f32_32(reinterpret_cast<float *>(p.out) +
-                                             ((size_t)s * p.M + row) * p.N,
-                                         n0 + c, p.N, v);
+                        stg.put(&tmO, reinterpret_cast<const uint32_t *>(v),
+                                n0 + c, row0, p.out_kind == BI_OUT_PARTIALS ? s : 0,
+                                rows_live && n0 + c < p.N);
                     }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&acc_empty[buf]);
             }
-            if (FUSED && ok && live) {
+            if (FUSED && ok) {
                 if (p.out_kind == BI_OUT_SWIGLU) {
-                    const int f0 = nt * (BN / 2);
-                    const int NO = p.N / 2;
+                    uint32_t w[32];
 #pragma unroll
-                    for (int c = 0; c < BN / 2; c += 32) {
-                        float g[32];
+                    for (int i = 0; i < 32; ++i)
+                        w[i] = pack_bf16x2(
+                            swiglu1(run[2 * i], run[BN / 2 + 2 * i]),
+                            swiglu1(run[2 * i + 1], run[BN / 2 + 2 * i + 1]));
+                    stg.put(&tmO, w, nt * (BN / 2), row0, 0, rows_live);
+                } else if (p.out_kind == BI_OUT_BF16) {
+#pragma unroll
+                    for (int c = 0; c < BN; c += 64) {
+                        uint32_t w[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            g[i] = swiglu1(run[c + i], run[BN / 2 + c + i]);
-                        store_bf16_32(reinterpret_cast<uint16_t *>(p.out) +
-                                          (size_t)row * NO,
-                                      f0 + c, NO, g);
+                            w[i] = pack_bf16x2(run[c + 2 * i], run[c + 2 * i + 1]);
+                        stg.put(&tmO, w, n0 + c, row0, 0,
+                                rows_live && n0 + c < p.N);
                     }
                 } else {
 #pragma unroll
-                    for (int c = 0; c < BN; c += 32) {
-                        if (p.out_kind == BI_OUT_BF16)
-                            store_bf16_32(reinterpret_cast<uint16_t *>(p.out) +
-                                              (size_t)row * p.N,
-                                          n0 + c, p.N, run + c);
-                        else
-                            store_f32_32(reinterpret_cast<float *>(p.out) +
-                                             (size_t)row * p.N,
-                                         n0 + c, p.N, run + c);
-                    }
+                    for (int c = 0; c < BN; c += 32)
+                        stg.put(&tmO,
+                                reinterpret_cast<const uint32_t *>(run + c),
+                                n0 + c, row0, 0, rows_live && n0 + c < p.N);
                 }
             }
         }
+        if (lane == 0) bulk_wait<0>();  // stores done before the CTA exits
     }
 
     tc_fence_before();
@@ -361,14 +382,14 @@ __global__ void pack_gate_up_kernel(const uint4 *__restrict__ wg,
     }
 }
 
-template <bool FUSED, int STAGES>
+template <bool FUSED>
 bi_status set_smem_attr() {
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
-        err = cudaFuncSetAttribute(gemm_kernel<FUSED, STAGES>,
+        err = cudaFuncSetAttribute(gemm_kernel<FUSED>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)smem_bytes(STAGES));
+                                   (int)smem_bytes());
     });
     return bi_cuda_check(err, "gemm smem attribute");
 }
@@ -376,9 +397,9 @@ bi_status set_smem_attr() {
 }  // namespace
 
 extern "C" int bi_gemm_splits(int N, int K) {
-    // A pure function of the weight shape.  Aim for about two CTAs per SM of
-    // a 152-SM GB300 at small M, with at least 4 k-blocks per slice and at
-    // most 8 slices.
+    // A pure function of the weight shape.  Aim for about two work units per
+    // SM of a 152-SM GB300 at small M, with at least 4 k-blocks per slice
+    // and at most 8 slices.
     const int KB = (K + BK - 1) / BK;
     const int tiles = (N + BN - 1) / BN;
     int s = 304 / std::max(tiles, 1);
@@ -393,12 +414,18 @@ extern "C" size_t bi_gemm_workspace_size(int M, int N, int K) {
     return (size_t)S * M * N * sizeof(float);
 }
 
-// Default schedule: fused once there are enough output tiles to fill the
-// GPU without splitting K.  Either schedule gives the same bits.
+// Default schedule.  Either schedule gives the same bits, so this is a pure
+// cost choice: fused when the split partials (written, then read by the
+// consumer) would move more bytes than the weight itself and there are
+// enough output tiles to keep a third of the GPU streaming, or when the
+// tiles alone fill the GPU.
 bool bi_gemm_default_fused(int M, int N, int K) {
     const int S = bi_gemm_splits(N, K);
+    if (S <= 1) return false;
     const int64_t tiles = (int64_t)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    return S > 1 && tiles >= 148;
+    const double partial_bytes = 2.0 * S * (double)M * N * 4.0;
+    const double weight_bytes = 2.0 * (double)N * K;
+    return tiles >= 148 || (tiles >= 48 && partial_bytes > weight_bytes);
 }
 
 bi_status bi_gemm_sched(const bi_bf16 *x, int M, int K, const bi_bf16 *W,
@@ -406,7 +433,8 @@ bi_status bi_gemm_sched(const bi_bf16 *x, int M, int K, const bi_bf16 *W,
                         size_t ws_bytes, int mode, cudaStream_t stream) {
     BI_REQUIRE(M >= 0 && N > 0 && K > 0, "bi_gemm: bad shape M=%d N=%d K=%d",
                M, N, K);
-    BI_REQUIRE(K % 8 == 0, "bi_gemm: K=%d must be a multiple of 8", K);
+    BI_REQUIRE(K % 8 == 0 && N % 8 == 0,
+               "bi_gemm: K=%d and N=%d must be multiples of 8", K, N);
     BI_REQUIRE(x && W && out, "bi_gemm: null pointer");
     BI_REQUIRE(bi_aligned16(x) && bi_aligned16(W) && bi_aligned16(out),
                "bi_gemm: pointers must be 16-byte aligned");
@@ -416,12 +444,8 @@ bi_status bi_gemm_sched(const bi_bf16 *x, int M, int K, const bi_bf16 *W,
     const int S = bi_gemm_splits(N, K);
     const int KB = (K + BK - 1) / BK;
     const int mt = (M + BM - 1) / BM, nt = (N + BN - 1) / BN;
-    if (out_kind == BI_OUT_SWIGLU) {
+    if (out_kind == BI_OUT_SWIGLU)
         BI_REQUIRE(N % BN == 0, "bi_gemm: SwiGLU needs N %% 128 == 0 (N=%d)", N);
-        if (S != 1)
-            return bi_fail(BI_ERR_UNSUPPORTED,
-                           "bi_gemm: SwiGLU epilogue needs one K slice");
-    }
     bool fused;
     if (mode == 1)
         fused = false;
@@ -431,8 +455,9 @@ bi_status bi_gemm_sched(const bi_bf16 *x, int M, int K, const bi_bf16 *W,
         fused = bi_gemm_default_fused(M, N, K);
     if (out_kind == BI_OUT_PARTIALS && S > 1) fused = false;
     if (S == 1) fused = false;
+    if (out_kind == BI_OUT_SWIGLU && S > 1) fused = true;
 
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, to;
     bi_status st = bi_make_tmap_2d_bf16(&ta, x, K, M, (uint64_t)K * 2, BK, BM,
                                         true);
     if (st != BI_OK) return st;
@@ -446,9 +471,9 @@ bi_status bi_gemm_sched(const bi_bf16 *x, int M, int K, const bi_bf16 *W,
     a.KB = KB;
     a.S = S;
     a.out_kind = out_kind;
-    a.out = out;
     a.status = bi_status_ptr();
 
+    void *dst = out;
     const bool need_reduce =
         !fused && S > 1 && out_kind != BI_OUT_PARTIALS;
     if (need_reduce) {
@@ -458,21 +483,32 @@ bi_status bi_gemm_sched(const bi_bf16 *x, int M, int K, const bi_bf16 *W,
                            "bi_gemm: workspace %zu < %zu bytes", ws_bytes,
                            need);
         BI_REQUIRE(bi_aligned16(ws), "bi_gemm: workspace alignment");
-        a.out = ws;
+        dst = ws;
         a.out_kind = BI_OUT_PARTIALS;
     }
+    // Output map: fp32 [planes][M][N] in 32 x 32 boxes, or bf16 [M][cols]
+    // in 64 x 32 boxes (128-byte rows, swizzled like the staging buffer).
+    if (a.out_kind == BI_OUT_PARTIALS)
+        st = bi_make_tmap_3d(&to, dst, true, N, M, S, 32, 32);
+    else if (a.out_kind == BI_OUT_F32)
+        st = bi_make_tmap_3d(&to, dst, true, N, M, 1, 32, 32);
+    else if (a.out_kind == BI_OUT_BF16)
+        st = bi_make_tmap_3d(&to, dst, false, N, M, 1, 64, 32);
+    else
+        st = bi_make_tmap_3d(&to, dst, false, N / 2, M, 1, 64, 32);
+    if (st != BI_OK) return st;
 
     a.MT = mt;
     a.units = fused ? mt * nt : mt * nt * S;
     const int grid = std::min(a.units, bi_sm_count());
     if (fused) {
-        if ((st = set_smem_attr<true, STAGES_FUSED>()) != BI_OK) return st;
-        gemm_kernel<true, STAGES_FUSED>
-            <<<grid, THREADS, smem_bytes(STAGES_FUSED), stream>>>(ta, tb, a);
+        if ((st = set_smem_attr<true>()) != BI_OK) return st;
+        gemm_kernel<true><<<grid, THREADS, smem_bytes(), stream>>>(ta, tb, to,
+                                                                   a);
     } else {
-        if ((st = set_smem_attr<false, STAGES_SPLIT>()) != BI_OK) return st;
-        gemm_kernel<false, STAGES_SPLIT>
-            <<<grid, THREADS, smem_bytes(STAGES_SPLIT), stream>>>(ta, tb, a);
+        if ((st = set_smem_attr<false>()) != BI_OK) return st;
+        gemm_kernel<false><<<grid, THREADS, smem_bytes(), stream>>>(ta, tb, to,
+                                                                    a);
     }
     BI_LAUNCH_CHECK("gemm launch");
     if (need_reduce) {

@@ -21,6 +21,12 @@ bi_status bi_make_tmap_2d_bf16(CUtensorMap *map, const void *base,
                                uint64_t row_stride_bytes, uint32_t box_inner,
                                uint32_t box_outer, bool swizzle128);
 
+// 3-D tensor map over a row-major [d2][d1][d0] array of fp32 (f32) or bf16,
+// box {box0, box1, 1}, 128-byte swizzle (box0 * element size must be 128).
+bi_status bi_make_tmap_3d(CUtensorMap *map, const void *base, bool f32,
+                          uint64_t d0, uint64_t d1, uint64_t d2,
+                          uint32_t box0, uint32_t box1);
+
 // GEMM with a forced schedule, for the model driver and the schedule test:
 // mode 0 = the default choice, 1 = every split in its own CTA,
 // 2 = every split of a tile in one CTA.
