@@ -397,12 +397,12 @@ bi_status set_smem_attr() {
 }  // namespace
 
 extern "C" int bi_gemm_splits(int N, int K) {
-    // A pure function of the weight shape.  Aim for about two work units per
-    // SM of a 152-SM GB300 at small M, with at least 4 k-blocks per slice
-    // and at most 8 slices.
+    // A pure function of the weight shape.  Aim for about one work unit per
+    // SM of a 152-SM GB300 at small M (two m-tiles give two per SM at
+    // M = 256), with at least 4 k-blocks per slice and at most 8 slices.
     const int KB = (K + BK - 1) / BK;
     const int tiles = (N + BN - 1) / BN;
-    int s = 304 / std::max(tiles, 1);
+    int s = 152 / std::max(tiles, 1);
     s = std::min(s, 8);
     s = std::min(s, KB / 4);
     return std::max(s, 1);
@@ -415,17 +415,14 @@ extern "C" size_t bi_gemm_workspace_size(int M, int N, int K) {
 }
 
 // Default schedule.  Either schedule gives the same bits, so this is a pure
-// cost choice: fused when the split partials (written, then read by the
-// consumer) would move more bytes than the weight itself and there are
-// enough output tiles to keep a third of the GPU streaming, or when the
-// tiles alone fill the GPU.
+// cost choice: fused once the output tiles alone fill the GPU.  (Measured on
+// the 8B decode shapes at M = 256: with 48-96 tiles the fused schedule loses
+// more to idle SMs than it saves in partial traffic.)
 bool bi_gemm_default_fused(int M, int N, int K) {
     const int S = bi_gemm_splits(N, K);
     if (S <= 1) return false;
     const int64_t tiles = (int64_t)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    const double partial_bytes = 2.0 * S * (double)M * N * 4.0;
-    const double weight_bytes = 2.0 * (double)N * K;
-    return tiles >= 148 || (tiles >= 48 && partial_bytes > weight_bytes);
+    return tiles >= 148;
 }
 
 bi_status bi_gemm_sched(const bi_bf16 *x, int M, int K, const bi_bf16 *W,

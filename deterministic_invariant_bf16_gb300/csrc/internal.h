@@ -50,3 +50,16 @@ bi_status bi_prefill_attn_pool(const bi_bf16 *q, const int32_t *cu_q,
                                int n_pages, int Hq, int Hkv, int D,
                                float scale, bi_bf16 *out, cudaStream_t stream);
 bool bi_gemm_default_fused(int M, int N, int K);
+
+// RoPE in two parts for the model driver: the (cos, sin) table of the rows'
+// positions ([T][D/2] float2), computed once per forward, and the rotation
+// + KV append reading it (table == nullptr computes the same values
+// in-kernel).
+bi_status bi_rope_table(const int32_t *pos, int T, int D, double theta,
+                        float2 *table, cudaStream_t s);
+bi_status bi_rope_apply(const float *qkv, int S, const float2 *table,
+                        const int32_t *pos, const int32_t *row_req, int T,
+                        int Hq, int Hkv, int D, double theta,
+                        bi_bf16 *q_out, bi_bf16 *k_pool, bi_bf16 *v_pool,
+                        const int32_t *page_table, int max_pages, int n_pages,
+                        cudaStream_t st);

@@ -58,7 +58,7 @@ struct Profiler {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-    size_t h, x, qkv, q, attn, o, f, d, att_ws, kvlen, vbuf, total;
+    size_t h, x, qkv, q, attn, o, f, d, att_ws, kvlen, rope, vbuf, total;
     int S_qkv, S_o, S_d;
 };
 
@@ -99,6 +99,7 @@ Layout layout(const bi_model_cfg &c, int max_pages_total) {
     L.att_ws = take(bi_decode_attn_workspace_size(T, c.n_heads, c.head_dim,
                                                   c.max_kv_len));
     L.kvlen = take((size_t)T * 4);
+    L.rope = take((size_t)T * (c.head_dim / 2) * 8);
     L.vbuf = take((size_t)(VerifyIdx::COUNT + max_pages_total) * 4);
     L.total = at;
     return L;
@@ -324,6 +325,7 @@ extern "C" bi_status bi_model_forward(bi_model *m, int T, const int32_t *tokens,
     float *d = reinterpret_cast<float *>(ws + m->L.d);
     void *att_ws = ws + m->L.att_ws;
     int32_t *kvlen = reinterpret_cast<int32_t *>(ws + m->L.kvlen);
+    float2 *rope_tab = reinterpret_cast<float2 *>(ws + m->L.rope);
     const size_t att_ws_bytes = m->L.kvlen - m->L.att_ws;
 
     bi_status st;
@@ -342,6 +344,7 @@ extern "C" bi_status bi_model_forward(bi_model *m, int T, const int32_t *tokens,
     } while (0)
 
     BI_TIMED(BI_PROF_OTHER, bi_embed(tokens, T, m->embed, c.vocab, H, h, s));
+    BI_TIMED(BI_PROF_ROPE, bi_rope_table(pos, T, D, c.theta, rope_tab, s));
     if (R == 0) {
         kvlen_kernel<<<(T + 255) / 256, 256, 0, s>>>(pos, T, kvlen);
         BI_LAUNCH_CHECK("kvlen launch");
@@ -360,9 +363,9 @@ extern "C" bi_status bi_model_forward(bi_model *m, int T, const int32_t *tokens,
         BI_TIMED(BI_PROF_GEMM_QKV,
                  gemm_slices(x, T, H, m->wqkv[l], QKV, qkv, &s_qkv, s));
         BI_TIMED(BI_PROF_ROPE,
-                 bi_rope(qkv, s_qkv, pos, row_req, T, Hq, Hkv, D, c.theta, q,
-                         m->kpool[l], m->vpool[l], page_table, c.max_pages,
-                         c.n_pages, s));
+                 bi_rope_apply(qkv, s_qkv, rope_tab, pos, row_req, T, Hq, Hkv,
+                               D, c.theta, q, m->kpool[l], m->vpool[l],
+                               page_table, c.max_pages, c.n_pages, s));
         if (R == 0) {
             BI_TIMED(BI_PROF_ATTN,
                      bi_decode_attn_pool(q, m->kpool[l], m->vpool[l],

@@ -8,6 +8,10 @@
 // and add rounded separately:
 //   x'_i       = x_i * cos - x_{i+D/2} * sin
 //   x'_{i+D/2} = x_{i+D/2} * cos + x_i * sin
+// The model driver computes the (cos, sin) table of a forward pass once
+// (rope_table_kernel) and every layer reads it; the stand-alone entry point
+// computes the same values inside each block.  Either way the fp32 values
+// come from the same double-precision expressions, so the bits agree.
 // Pages: PagedAttention-style pools [n_pages][Hkv][16][D]; the page of a
 // position is looked up in the request's page-table row, so any physical
 // page order gives the same logical cache (Vosti: KV tied to its logical
@@ -18,6 +22,25 @@
 namespace {
 
 constexpr int ROPE_THREADS = 256;
+
+// (cos, sin) of angle pos * theta^(-2i/D), in double, rounded to fp32.
+__device__ __forceinline__ float2 rope_cs(int p, int i, int D, double theta) {
+    const double inv_freq = pow(theta, -(2.0 * (double)i) / (double)D);
+    const double ang = (double)p * inv_freq;
+    return make_float2((float)cos(ang), (float)sin(ang));
+}
+
+__global__ void rope_table_kernel(const int32_t *__restrict__ pos, int T,
+                                  int D, double theta,
+                                  float2 *__restrict__ table) {
+    const int half = D / 2;
+    const int64_t n = (int64_t)T * half;
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int t = (int)(e / half), i = (int)(e % half);
+        table[e] = rope_cs(pos[t], i, D, theta);
+    }
+}
 
 // Slices summed in slice order and rounded to bf16.  S is a template
 // argument so that all S loads are in flight before the adds.
@@ -33,55 +56,56 @@ __device__ __forceinline__ float qkv_value(const float *__restrict__ qkv,
     return bf16_to_f32(f32_to_bf16(v));
 }
 
+// Block (t, y) handles row t, heads [y * HPB, (y + 1) * HPB) with
+// HPB = 256 / (D/2); thread -> (head, pair i).  Heads are q heads, then k
+// heads (rotated and appended), then v heads (appended as rounded).
 template <int S>
 __global__ void __launch_bounds__(ROPE_THREADS)
-    rope_kernel(const float *__restrict__ qkv,
+    rope_kernel(const float *__restrict__ qkv, const float2 *__restrict__ table,
                 const int32_t *__restrict__ pos,
                 const int32_t *__restrict__ row_req, int T, int Hq, int Hkv,
                 int D, double theta, uint16_t *__restrict__ q_out,
                 uint16_t *__restrict__ k_pool, uint16_t *__restrict__ v_pool,
                 const int32_t *__restrict__ page_table, int max_pages,
                 int n_pages, int32_t *status) {
-    __shared__ float cs[64], sn[64];
+    __shared__ float2 cs_s[64];
     const int t = blockIdx.x;
     const int half = D / 2;
+    const int hpb = ROPE_THREADS / half;
     const int QKV = (Hq + 2 * Hkv) * D;
     const int64_t TQ = (int64_t)T * QKV;
     const int64_t rowoff = (int64_t)t * QKV;
     const int p = pos[t];
     const int req = row_req[t];
+    const int i = threadIdx.x % half;
+    const int head = blockIdx.y * hpb + threadIdx.x / half;
 
-    for (int i = threadIdx.x; i < half; i += blockDim.x) {
-        const double inv_freq = pow(theta, -(2.0 * (double)i) / (double)D);
-        const double ang = (double)p * inv_freq;
-        cs[i] = (float)cos(ang);
-        sn[i] = (float)sin(ang);
+    if (!table) {
+        if (threadIdx.x < half) cs_s[threadIdx.x] = rope_cs(p, threadIdx.x, D, theta);
+        __syncthreads();
     }
+    if (head >= Hq + 2 * Hkv) return;
     int64_t page = -1;
-    if (req >= 0) {
+    if (req >= 0 && head >= Hq) {
         const int pi = p / 16;
         if (p < 0 || pi >= max_pages) {
-            if (threadIdx.x == 0) bi_record_error(status, BI_ERR_BOUNDS);
+            if (i == 0) bi_record_error(status, BI_ERR_BOUNDS);
         } else {
             const int pg = page_table[(int64_t)req * max_pages + pi];
             if (pg < 0 || pg >= n_pages) {
-                if (threadIdx.x == 0) bi_record_error(status, BI_ERR_BOUNDS);
+                if (i == 0) bi_record_error(status, BI_ERR_BOUNDS);
             } else {
                 page = pg;
             }
         }
     }
-    __syncthreads();
     const int slot = p & 15;
-
-    // q and k heads: one pair (i, i + D/2) per work item.
-    const int pairs = (Hq + Hkv) * half;
-    for (int e = threadIdx.x; e < pairs; e += blockDim.x) {
-        const int head = e / half, i = e % half;
-        const int64_t c0 = rowoff + (int64_t)head * D + i;
-        const float x0 = qkv_value<S>(qkv, TQ, c0);
-        const float x1 = qkv_value<S>(qkv, TQ, c0 + half);
-        const float c = cs[i], s = sn[i];
+    const int64_t c0 = rowoff + (int64_t)head * D + i;
+    const float x0 = qkv_value<S>(qkv, TQ, c0);
+    const float x1 = qkv_value<S>(qkv, TQ, c0 + half);
+    if (head < Hq + Hkv) {
+        const float2 cs = table ? table[(int64_t)t * half + i] : cs_s[i];
+        const float c = cs.x, s = cs.y;
         const float y0 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, s));
         const float y1 = __fadd_rn(__fmul_rn(x1, c), __fmul_rn(x0, s));
         if (head < Hq) {
@@ -95,43 +119,50 @@ __global__ void __launch_bounds__(ROPE_THREADS)
             kd[i] = f32_to_bf16(y0);
             kd[i + half] = f32_to_bf16(y1);
         }
-    }
-    // v heads: copied as rounded.
-    if (page >= 0) {
-        for (int e = threadIdx.x; e < Hkv * D; e += blockDim.x) {
-            const int head = e / D, d = e % D;
-            const float v = qkv_value<S>(qkv, TQ,
-                                      rowoff + (int64_t)(Hq + Hkv) * D + e);
-            v_pool[((page * Hkv + head) * 16 + slot) * (int64_t)D + d] =
-                f32_to_bf16(v);
-        }
+    } else if (page >= 0) {
+        uint16_t *vd = v_pool +
+                       ((page * Hkv + (head - Hq - Hkv)) * 16 + slot) * (int64_t)D;
+        vd[i] = f32_to_bf16(x0);
+        vd[i + half] = f32_to_bf16(x1);
     }
 }
 
 }  // namespace
 
-extern "C" bi_status bi_rope(const float *qkv, int S, const int32_t *pos,
-                             const int32_t *row_req, int T, int Hq, int Hkv,
-                             int D, double theta, bi_bf16 *q_out,
-                             bi_bf16 *k_pool, bi_bf16 *v_pool,
-                             const int32_t *page_table, int max_pages,
-                             int n_pages, void *stream) {
+bi_status bi_rope_table(const int32_t *pos, int T, int D, double theta,
+                        float2 *table, cudaStream_t s) {
+    if (T == 0) return BI_OK;
+    const int64_t n = (int64_t)T * (D / 2);
+    const int blocks = (int)((n + 255) / 256);
+    rope_table_kernel<<<blocks, 256, 0, s>>>(pos, T, D, theta, table);
+    BI_LAUNCH_CHECK("rope table launch");
+    return BI_OK;
+}
+
+bi_status bi_rope_apply(const float *qkv, int S, const float2 *table,
+                        const int32_t *pos, const int32_t *row_req, int T,
+                        int Hq, int Hkv, int D, double theta,
+                        bi_bf16 *q_out, bi_bf16 *k_pool, bi_bf16 *v_pool,
+                        const int32_t *page_table, int max_pages, int n_pages,
+                        cudaStream_t st) {
     BI_REQUIRE(T >= 0 && S >= 1 && S <= 8 && Hq > 0 && Hkv > 0 &&
                    Hq % Hkv == 0,
                "bi_rope: bad shape T=%d S=%d Hq=%d Hkv=%d", T, S, Hq, Hkv);
-    BI_REQUIRE(D % 2 == 0 && D <= 128 && D > 0, "bi_rope: D=%d", D);
+    BI_REQUIRE(D % 2 == 0 && D <= 128 && D >= 4 && ROPE_THREADS % (D / 2) == 0,
+               "bi_rope: D=%d", D);
     BI_REQUIRE(qkv && pos && row_req && q_out && k_pool && v_pool && page_table,
                "bi_rope: null pointer");
     BI_REQUIRE(max_pages > 0 && n_pages > 0, "bi_rope: empty page table/pool");
     if (T == 0) return BI_OK;
-    cudaStream_t st = bi_stream(stream);
     int32_t *status = bi_status_ptr();
+    const int hpb = ROPE_THREADS / (D / 2);
+    dim3 grid(T, (Hq + 2 * Hkv + hpb - 1) / hpb);
     switch (S) {
 #define BI_ROPE_CASE(n)                                                       \
     case n:                                                                   \
-        rope_kernel<n><<<T, ROPE_THREADS, 0, st>>>(                           \
-            qkv, pos, row_req, T, Hq, Hkv, D, theta, q_out, k_pool, v_pool,   \
-            page_table, max_pages, n_pages, status);                          \
+        rope_kernel<n><<<grid, ROPE_THREADS, 0, st>>>(                        \
+            qkv, table, pos, row_req, T, Hq, Hkv, D, theta, q_out, k_pool,    \
+            v_pool, page_table, max_pages, n_pages, status);                  \
         break;
         BI_ROPE_CASE(1) BI_ROPE_CASE(2) BI_ROPE_CASE(3) BI_ROPE_CASE(4)
         BI_ROPE_CASE(5) BI_ROPE_CASE(6) BI_ROPE_CASE(7) BI_ROPE_CASE(8)
@@ -139,4 +170,15 @@ extern "C" bi_status bi_rope(const float *qkv, int S, const int32_t *pos,
     }
     BI_LAUNCH_CHECK("rope launch");
     return BI_OK;
+}
+
+extern "C" bi_status bi_rope(const float *qkv, int S, const int32_t *pos,
+                             const int32_t *row_req, int T, int Hq, int Hkv,
+                             int D, double theta, bi_bf16 *q_out,
+                             bi_bf16 *k_pool, bi_bf16 *v_pool,
+                             const int32_t *page_table, int max_pages,
+                             int n_pages, void *stream) {
+    return bi_rope_apply(qkv, S, nullptr, pos, row_req, T, Hq, Hkv, D, theta,
+                         q_out, k_pool, v_pool, page_table, max_pages, n_pages,
+                         bi_stream(stream));
 }
