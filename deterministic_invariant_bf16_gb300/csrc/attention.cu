@@ -811,6 +811,7 @@ bi_status bi_decode_attn_pool(const bi_bf16 *q, const bi_bf16 *k_pool,
     BI_REQUIRE(B >= 0 && max_kv_len > 0 && max_kv_len <= 16 * max_pages,
                "bi_paged_decode_attn: B=%d max_kv_len=%d max_pages=%d", B,
                max_kv_len, max_pages);
+    if (B == 0) return BI_OK;
     if (D != 32 && D != 128)
         return bi_fail(BI_ERR_UNSUPPORTED, "bi_paged_decode_attn: D=%d", D);
     if (!group_ok(Hq, Hkv))
@@ -822,7 +823,6 @@ bi_status bi_decode_attn_pool(const bi_bf16 *q, const bi_bf16 *k_pool,
                    bi_aligned16(out) && bi_aligned16(ws),
                "bi_paged_decode_attn: pointers must be 16-byte aligned");
     BI_REQUIRE(n_pages > 0, "bi_paged_decode_attn: n_pages=%d", n_pages);
-    if (B == 0) return BI_OK;
     const size_t need = bi_decode_attn_workspace_size(B, Hq, D, max_kv_len);
     if (!ws || ws_bytes < need)
         return bi_fail(BI_ERR_WORKSPACE_TOO_SMALL,
@@ -971,6 +971,7 @@ bi_status bi_prefill_attn_pool(const bi_bf16 *q, const int32_t *cu_q,
                    max_kv_len <= 16 * max_pages,
                "bi_prefill_attn: R=%d T=%d max_q=%d max_kv_len=%d", R, T,
                max_q, max_kv_len);
+    if (T == 0 || R == 0) return BI_OK;
     if (D != 32 && D != 128)
         return bi_fail(BI_ERR_UNSUPPORTED, "bi_prefill_attn: D=%d", D);
     if (!group_ok(Hq, Hkv))
@@ -982,7 +983,6 @@ bi_status bi_prefill_attn_pool(const bi_bf16 *q, const int32_t *cu_q,
     BI_REQUIRE(bi_aligned16(q) && bi_aligned16(k_pool) && bi_aligned16(v_pool) &&
                    bi_aligned16(out),
                "bi_prefill_attn: pointers must be 16-byte aligned");
-    if (T == 0 || R == 0) return BI_OK;
     const int G = Hq / Hkv;
     const int QPT = 16 / G;
     const int tiles = (T + QPT - 1) / QPT + R;

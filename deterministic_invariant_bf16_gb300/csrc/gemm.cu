@@ -432,12 +432,12 @@ bi_status bi_gemm_sched(const bi_bf16 *x, int M, int K, const bi_bf16 *W,
                M, N, K);
     BI_REQUIRE(K % 8 == 0 && N % 8 == 0,
                "bi_gemm: K=%d and N=%d must be multiples of 8", K, N);
+    if (M == 0) return BI_OK;
     BI_REQUIRE(x && W && out, "bi_gemm: null pointer");
     BI_REQUIRE(bi_aligned16(x) && bi_aligned16(W) && bi_aligned16(out),
                "bi_gemm: pointers must be 16-byte aligned");
     BI_REQUIRE(out_kind >= BI_OUT_PARTIALS && out_kind <= BI_OUT_SWIGLU,
                "bi_gemm: bad out_kind %d", out_kind);
-    if (M == 0) return BI_OK;
     const int S = bi_gemm_splits(N, K);
     const int KB = (K + BK - 1) / BK;
     const int mt = (M + BM - 1) / BM, nt = (N + BN - 1) / BN;

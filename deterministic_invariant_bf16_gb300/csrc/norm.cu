@@ -155,6 +155,7 @@ extern "C" bi_status bi_rmsnorm(const float *partials, int S,
                    H <= NORM_MAX_VEC * 8 * NORM_THREADS,
                "bi_rmsnorm: H=%d must be a positive multiple of 8, <= 16384",
                H);
+    if (T == 0) return BI_OK;
     BI_REQUIRE(w && y, "bi_rmsnorm: null w or y");
     BI_REQUIRE(partials || x || residual,
                "bi_rmsnorm: need partials, x or residual");
@@ -164,7 +165,6 @@ extern "C" bi_status bi_rmsnorm(const float *partials, int S,
                    (!residual || bi_aligned16(residual)) && bi_aligned16(w) &&
                    bi_aligned16(y),
                "bi_rmsnorm: pointers must be 16-byte aligned");
-    if (T == 0) return BI_OK;
     cudaStream_t s = bi_stream(stream);
     switch (partials ? S : 0) {
 #define BI_NORM_CASE(n)                                                      \
@@ -185,10 +185,10 @@ extern "C" bi_status bi_embed(const int32_t *tokens, int T, const bi_bf16 *E,
                               int V, int H, bi_bf16 *h, void *stream) {
     BI_REQUIRE(T >= 0 && V > 0 && H > 0 && H % 8 == 0,
                "bi_embed: bad shape T=%d V=%d H=%d", T, V, H);
+    if (T == 0) return BI_OK;
     BI_REQUIRE(tokens && E && h, "bi_embed: null pointer");
     BI_REQUIRE(bi_aligned16(E) && bi_aligned16(h),
                "bi_embed: pointers must be 16-byte aligned");
-    if (T == 0) return BI_OK;
     embed_kernel<<<T, 128, 0, bi_stream(stream)>>>(
         tokens, reinterpret_cast<const uint4 *>(E), V, H / 8,
         reinterpret_cast<uint4 *>(h), bi_status_ptr());
@@ -198,8 +198,9 @@ extern "C" bi_status bi_embed(const int32_t *tokens, int T, const bi_bf16 *E,
 
 extern "C" bi_status bi_swiglu(const float *g, const float *u, int64_t n,
                                bi_bf16 *out, void *stream) {
-    BI_REQUIRE(n >= 0 && g && u && out, "bi_swiglu: bad arguments");
+    BI_REQUIRE(n >= 0, "bi_swiglu: n=%lld", (long long)n);
     if (n == 0) return BI_OK;
+    BI_REQUIRE(g && u && out, "bi_swiglu: null pointer");
     const int blocks = (int)std::min<int64_t>((n + 255) / 256, 152 * 16);
     swiglu_kernel<<<blocks, 256, 0, bi_stream(stream)>>>(g, u, n, out);
     BI_LAUNCH_CHECK("swiglu launch");

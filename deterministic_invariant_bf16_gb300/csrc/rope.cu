@@ -150,10 +150,10 @@ bi_status bi_rope_apply(const float *qkv, int S, const float2 *table,
                "bi_rope: bad shape T=%d S=%d Hq=%d Hkv=%d", T, S, Hq, Hkv);
     BI_REQUIRE(D % 2 == 0 && D <= 128 && D >= 4 && ROPE_THREADS % (D / 2) == 0,
                "bi_rope: D=%d", D);
+    if (T == 0) return BI_OK;
     BI_REQUIRE(qkv && pos && row_req && q_out && k_pool && v_pool && page_table,
                "bi_rope: null pointer");
     BI_REQUIRE(max_pages > 0 && n_pages > 0, "bi_rope: empty page table/pool");
-    if (T == 0) return BI_OK;
     int32_t *status = bi_status_ptr();
     const int hpb = ROPE_THREADS / (D / 2);
     dim3 grid(T, (Hq + 2 * Hkv + hpb - 1) / hpb);

@@ -223,9 +223,10 @@ __global__ void __launch_bounds__(SEL_THREADS)
 
 extern "C" bi_status bi_argmax_logits(const float *logits, int T, int V,
                                       int32_t *ids, void *stream) {
-    BI_REQUIRE(T >= 0 && V > 0 && logits && ids, "bi_argmax_logits: bad args");
-    BI_REQUIRE(bi_aligned16(logits), "bi_argmax_logits: logits alignment");
+    BI_REQUIRE(T >= 0 && V > 0, "bi_argmax_logits: T=%d V=%d", T, V);
     if (T == 0) return BI_OK;
+    BI_REQUIRE(logits && ids, "bi_argmax_logits: null pointer");
+    BI_REQUIRE(bi_aligned16(logits), "bi_argmax_logits: logits alignment");
     argmax_kernel<<<T, SEL_THREADS, 0, bi_stream(stream)>>>(logits, V, ids);
     BI_LAUNCH_CHECK("argmax launch");
     return BI_OK;
@@ -235,11 +236,12 @@ extern "C" bi_status philox_sample(const float *logits, int T, int V,
                                    const uint64_t *request_id,
                                    const uint64_t *step, float temperature,
                                    int32_t *ids, void *stream) {
-    BI_REQUIRE(T >= 0 && V > 0 && logits && ids, "philox_sample: bad args");
+    BI_REQUIRE(T >= 0 && V > 0, "philox_sample: T=%d V=%d", T, V);
     BI_REQUIRE(temperature >= 0.f, "philox_sample: temperature < 0");
+    if (T == 0) return BI_OK;
+    BI_REQUIRE(logits && ids, "philox_sample: null pointer");
     if (temperature == 0.f) return bi_argmax_logits(logits, T, V, ids, stream);
     BI_REQUIRE(request_id && step, "philox_sample: null request_id/step");
-    if (T == 0) return BI_OK;
     sample_kernel<<<T, SEL_THREADS, 0, bi_stream(stream)>>>(
         logits, V, request_id, step, temperature, ids);
     BI_LAUNCH_CHECK("sample launch");

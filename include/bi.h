@@ -29,6 +29,10 @@
  *     elements.
  *   - Device pointers must be 16-byte aligned; inner dimensions of bf16
  *     matrices read by the tensor-core GEMM must be multiples of 8.
+ *   - A call with zero rows (M, T, B or n equal to 0) is a no-op: once its
+ *     sizes pass their checks it returns BI_OK without reading its
+ *     pointers, which may then be null (an empty torch tensor has a null
+ *     data pointer).
  */
 #ifndef BI_H
 #define BI_H
