@@ -62,6 +62,7 @@ SIGNATURES = {
     "bi_last_error": ([], ctypes.c_char_p),
     "bi_device_status": ([I32P, V], I),
     "bi_gemm_splits": ([I, I], I),
+    "bi_gemm_tile_n": ([I, I], I),
     "bi_gemm_workspace_size": ([I, I, I], Z),
     "bi_gemm": ([V, I, I, V, I, V, I, V, Z, V], I),
     "bi_pack_gate_up": ([V, V, I, I, V, V], I),
@@ -138,6 +139,10 @@ def _i32(a):
 
 def bi_gemm_splits(N, K):
     return lib().bi_gemm_splits(N, K)
+
+
+def bi_gemm_tile_n(N, K):
+    return lib().bi_gemm_tile_n(N, K)
 
 
 def bi_gemm_workspace_size(M, N, K):

@@ -354,15 +354,21 @@ struct DecSmem {
     static constexpr int ALLOC = BYTES + 1024;           // alignment slack
 };
 
+// Items a CTA's prefetch warp may run ahead of its producer.
+constexpr int PF_AHEAD = 2;
+
 // Persistent decode chunk kernel.  CTA k takes work items k, k + grid,
 // k + 2 grid, ...; item i is KV head i % Hkv of list entry i / Hkv.  Item n
 // of a CTA loads K (with the Q rows) into slot 2n mod RING and V into slot
-// 2n + 1 mod RING.  The last warp is the producer: it waits for a slot to be
+// 2n + 1 mod RING.  Warp NW is the producer: it waits for a slot to be
 // freed, reads the chunk's page ids (one lane per page) and issues one TMA
-// box per page and 64-column half.  The compute warps wait for the tiles,
-// run the two phases and store the partial record.
+// box per page and 64-column half.  Warp NW + 1 walks the same items up to
+// PF_AHEAD ahead of the producer and asks L2 for their K and V pages, so
+// that DRAM reads start before a shared-memory slot is free for them.  The
+// compute warps wait for the tiles, run the two phases and store the
+// partial record.
 template <int D>
-__global__ void __launch_bounds__(cthreads<D>() + 32, 1)
+__global__ void __launch_bounds__(cthreads<D>() + 64, 1)
     decode_chunks_kernel(const __grid_constant__ CUtensorMap kmap,
                          const __grid_constant__ CUtensorMap vmap,
                          const __grid_constant__ CUtensorMap qmap,
@@ -371,8 +377,11 @@ __global__ void __launch_bounds__(cthreads<D>() + 32, 1)
                          const int32_t *__restrict__ kv_len, int Hq, int Hkv,
                          int G, float scale, float *__restrict__ ws, int Cmax,
                          const int32_t *__restrict__ prefix, int B,
-                         const int2 *__restrict__ items, int32_t *status) {
+                         const int2 *__restrict__ items,
+                         const bi_bf16 *__restrict__ k_pool,
+                         const bi_bf16 *__restrict__ v_pool, int32_t *status) {
     extern __shared__ uint8_t smem_raw[];
+    __shared__ int s_progress;  // items the producer has issued
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     using L = DecSmem<D>;
@@ -398,8 +407,48 @@ __global__ void __launch_bounds__(cthreads<D>() + 32, 1)
             mbar_init(&empty[i], NW);
         }
         mbar_fence_init();
+        s_progress = 0;
     }
     __syncthreads();
+    volatile int *progress = &s_progress;
+
+    if (warp == NW + 1) {
+        // ------------------------------------------------------ prefetch --
+        constexpr uint32_t PAGE_KV = 16 * D * 2;  // one (page, head) of K
+        for (int n = 0;; ++n) {
+            const int i = blockIdx.x + n * gridDim.x;
+            if (i >= total) break;
+            bool go = true;
+            if (lane == 0 && *progress + PF_AHEAD < n) {
+                const uint64_t t0 = bi_globaltimer();
+                while (*progress + PF_AHEAD < n) {
+                    __nanosleep(256);
+                    if (bi_globaltimer() - t0 > BI_WAIT_LIMIT_NS) {
+                        go = false;  // the producer stopped; nothing to do
+                        break;
+                    }
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, go ? 1 : 0, 0)) break;
+            const int g = i % Hkv;
+            const int2 bc = items[i / Hkv];
+            const int vl = min(CHUNK, kv_len[bc.x] - bc.y * CHUNK);
+            const int npg = (vl + 15) >> 4;
+            if (lane < npg) {
+                const int pi = bc.y * 16 + lane;
+                const int pg = pi < max_pages
+                                   ? page_table[(int64_t)row_req[bc.x] *
+                                                    max_pages + pi]
+                                   : -1;
+                if (pg >= 0 && pg < n_pages) {
+                    const int64_t off = ((int64_t)pg * Hkv + g) * 16 * D;
+                    prefetch_l2_bulk(k_pool + off, PAGE_KV);
+                    prefetch_l2_bulk(v_pool + off, PAGE_KV);
+                }
+            }
+        }
+        return;
+    }
 
     if (warp == NW) {
         // ------------------------------------------------------ producer --
@@ -462,7 +511,9 @@ __global__ void __launch_bounds__(cthreads<D>() + 32, 1)
                                     &full[slot]);
                 }
             }
+            if (lane == 0) *progress = n + 1;
         }
+        if (lane == 0) *progress = 0x3fffffff;  // release the prefetch warp
         return;
     }
 
@@ -771,7 +822,8 @@ bi_status launch_decode_chunks(const CUtensorMap &km, const CUtensorMap &vm,
                                const int32_t *kv_len, int Hq, int Hkv, int G,
                                float scale, float *rec, int Cmax,
                                const int32_t *prefix, int B,
-                               const int2 *items, int32_t *status,
+                               const int2 *items, const bi_bf16 *k_pool,
+                               const bi_bf16 *v_pool, int32_t *status,
                                cudaStream_t s) {
     static std::once_flag f;
     static bi_status fs;
@@ -780,9 +832,10 @@ bi_status launch_decode_chunks(const CUtensorMap &km, const CUtensorMap &vm,
     });
     if (fs != BI_OK) return fs;
     decode_chunks_kernel<D>
-        <<<bi_sm_count(), cthreads<D>() + 32, DecSmem<D>::ALLOC, s>>>(
+        <<<bi_sm_count(), cthreads<D>() + 64, DecSmem<D>::ALLOC, s>>>(
             km, vm, qm, page_table, max_pages, n_pages, row_req, kv_len, Hq,
-            Hkv, G, scale, rec, Cmax, prefix, B, items, status);
+            Hkv, G, scale, rec, Cmax, prefix, B, items, k_pool, v_pool,
+            status);
     BI_LAUNCH_CHECK("decode attention launch");
     return BI_OK;
 }
@@ -799,7 +852,9 @@ extern "C" size_t bi_decode_attn_workspace_size(int B, int Hq, int D,
 }
 
 // Decode attention with the pool size known (page ids are range-checked
-// against it).  stages: bit 0 runs the chunk kernels, bit 1 the merge.
+// against it).  stages: bit 0 runs the chunk kernels (after building the
+// work list, unless bit 2 says the list in `ws` is already built for these
+// kv_len and row_req), bit 1 the merge.
 bi_status bi_decode_attn_pool(const bi_bf16 *q, const bi_bf16 *k_pool,
                               const bi_bf16 *v_pool, const int32_t *page_table,
                               int max_pages, int n_pages,
@@ -854,19 +909,21 @@ bi_status bi_decode_attn_pool(const bi_bf16 *q, const bi_bf16 *k_pool,
         if ((st = bi_make_tmap_2d_bf16(&qm, q, D, (uint64_t)B * Hq, D * 2, bw,
                                        16, D == 128)) != BI_OK)
             return st;
-        build_items_kernel<<<1, 1024, 0, s>>>(kv_len, row_req, B, Cmax, prefix,
-                                              items);
-        BI_LAUNCH_CHECK("decode item list launch");
+        if (!(stages & 4)) {
+            build_items_kernel<<<1, 1024, 0, s>>>(kv_len, row_req, B, Cmax,
+                                                  prefix, items);
+            BI_LAUNCH_CHECK("decode item list launch");
+        }
         if (D == 128)
             st = launch_decode_chunks<128>(km, vm, qm, page_table, max_pages,
                                            n_pages, row_req, kv_len, Hq, Hkv,
                                            G, scale, rec, Cmax, prefix, B,
-                                           items, status, s);
+                                           items, k_pool, v_pool, status, s);
         else
             st = launch_decode_chunks<32>(km, vm, qm, page_table, max_pages,
                                           n_pages, row_req, kv_len, Hq, Hkv, G,
                                           scale, rec, Cmax, prefix, B, items,
-                                          status, s);
+                                          k_pool, v_pool, status, s);
         if (st != BI_OK) return st;
     }
     if (stages & 2) {

@@ -106,7 +106,7 @@ static encode_tiled_fn get_encode() {
 
 bi_status bi_make_tmap_3d(CUtensorMap *map, const void *base, bool f32,
                           uint64_t d0, uint64_t d1, uint64_t d2,
-                          uint32_t box0, uint32_t box1) {
+                          uint32_t box0, uint32_t box1, bool swizzle128) {
     encode_tiled_fn enc = get_encode();
     if (!enc)
         return bi_fail(BI_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
@@ -119,7 +119,9 @@ bi_status bi_make_tmap_3d(CUtensorMap *map, const void *base, bool f32,
                      f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                          : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                      3, const_cast<void *>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)

@@ -149,6 +149,15 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *m,
         : "memory");
 }
 
+// Hint to bring `bytes` (a multiple of 16, 16-byte aligned) at `src` into
+// L2: no shared memory, no completion to wait for.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *src,
+                                                 uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src),
+                 "r"(bytes)
+                 : "memory");
+}
+
 // 3-D tiled store of a shared-memory box to global memory (bulk-group
 // completion).  Elements outside the tensor are not written.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap *m,

@@ -6,31 +6,32 @@
 // kernel follows: one tile shape for every M, a split count fixed per weight
 // shape, a fixed-order second stage, no float atomics.
 //
-// Reduction order of one output y[m][n] (independent of M, of the row's
-// place in its tile, and of which CTA does the work):
-//   - K is cut into S = bi_gemm_splits(N, K) slices of whole 64-column
-//     blocks, slice s covering blocks [s*KB/S, (s+1)*KB/S).
-//   - Inside a slice: one tcgen05.mma chain (M=128, N=128, K=16 per
+// Tile plan.  A tile is 256 rows x BN columns, BN in {128, 192, 256}; K is
+// cut into S slices of whole 64-column blocks, slice s covering blocks
+// [s*KB/S, (s+1)*KB/S).  (BN, S) = gemm_plan(N, K) is a pure function of the
+// weight shape, never of M.  Reduction order of one output y[m][n]:
+//   - inside a slice: one tcgen05.mma chain (M=128, N=BN, K=16 per
 //     instruction) in ascending k, accumulating in fp32 in tensor memory,
-//     starting from zero.
-//   - Slices are summed in fp32 in slice order: ((p0 + p1) + p2) + ...
+//     starting from zero;
+//   - slices are summed in fp32 in slice order ((p0 + p1) + p2) + ... by
+//     the consumer (bi_rmsnorm, bi_rope, or the reduce kernels here).
 //
-// Two schedules give the same bits:
-//   split: a work unit is one (m-tile, n-tile, slice); slices go to memory
-//          as fp32 partials and a consumer (bi_rmsnorm, bi_rope, or the
-//          reduce kernel here) sums them in order.  Fills the GPU at small M.
-//   fused: a work unit is one (m-tile, n-tile) with all its slices run one
-//          after another; the epilogue warps add each finished slice to a
-//          register running sum in slice order.  No partial traffic; used
-//          when there are enough tiles.
+// Why 256-row tiles: on GB300 one SM ingests TMA loads at about 41 bytes
+// per clock whatever the box shape or the number of stages in flight
+// (measured with a load-only ring), so the projection GEMMs of a decode
+// batch are bound by the bytes each SM loads, (256 + BN) * 128 per k-block
+// here against 256 * 128 for 128 x 128 tiles: 1.3-1.75x fewer bytes per
+// multiply-add.  The plan picks BN and S to fill the 152 SMs with as few
+// bytes per SM as it can, counting the traffic of the fp32 partials.
 //
-// Persistent CTAs (one per SM, 192 threads) loop over work units: warp 0
-// lane 0 issues TMA loads into a ring of shared-memory stages; warp 1 owns
-// the TMEM allocation and lane 0 issues the MMAs into a ring of four TMEM
-// accumulators; warps 2-5 are the epilogue (warp w reads TMEM lanes
-// 32*(w%4) .. 32*(w%4)+31, i.e. tile rows), staging each 32-row piece of the
-// result in a 128-byte-swizzled shared buffer and writing it with a TMA
-// store, which clips rows past M and columns past N.  Every wait is bounded.
+// Persistent CTAs (one per SM, 192 threads) loop over work units (m-tile,
+// n-tile, slice), the m-tile fastest: warp 0 lane 0 issues TMA loads into a
+// ring of shared-memory stages (A: 256 x 64, B: BN x 64, 128-byte swizzle);
+// warp 1 owns the tensor memory and lane 0 issues, per 16-column step, one
+// MMA per 128-row half into the two halves of a TMEM accumulator; warps 2-5
+// are the epilogue (warp w reads TMEM lanes 32*(w%4) .. +31 of both halves),
+// staging 32-row pieces in shared memory and writing them with TMA stores,
+// which clip rows past M and columns past N.  Every wait is bounded.
 #include <algorithm>
 #include <mutex>
 
@@ -39,27 +40,39 @@
 
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 64;
-constexpr int A_BYTES = BM * BK * 2;
-constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int BM = 256;                   // tile rows
+constexpr int HALF = 128;                 // rows per MMA (one TMEM lane each)
+constexpr int BK = 64;                    // k-block: 128 bytes of bf16
+constexpr int A_BYTES = BM * BK * 2;      // 32 KB
 constexpr int THREADS = 192;
-constexpr uint32_t IDESC = make_idesc_bf16(BM, BN);
-constexpr int STAGES = 5;                 // 160 KB of operand stages
-constexpr int NACC = 4;                   // TMEM accumulators (4 x 128 cols)
 constexpr int STORE_BYTES = 32 * 128;     // one staged store: 32 rows x 128 B
 constexpr int EPI_BYTES = 4 * 2 * STORE_BYTES;  // 4 warps x double buffer
+constexpr int SMEM_LIMIT = 232448;        // opt-in shared memory per block
+constexpr int TMEM_COLS = 512;
+constexpr int MAX_SPLITS = 8;
+constexpr int PLAN_SMS = 152;             // SMs the plan fills (GB300)
 
-constexpr size_t smem_bytes() {
-    return 1024 /* alignment slack */ + (size_t)STAGES * STAGE_BYTES +
-           EPI_BYTES + 256;
-}
+template <int BN>
+struct Tile {
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int FIT = (SMEM_LIMIT - EPI_BYTES - 1024 - 256) / STAGE_BYTES;
+    static constexpr int STAGES = FIT < 4 ? FIT : 4;
+    static constexpr int ACC_COLS = 2 * BN;           // both halves
+    static constexpr int NACC = TMEM_COLS / ACC_COLS;  // accumulators in TMEM
+    static constexpr uint32_t IDESC = make_idesc_bf16(HALF, BN);
+    static constexpr size_t SMEM =
+        1024 + (size_t)STAGES * STAGE_BYTES + EPI_BYTES + 256;
+    static_assert(STAGES >= 2 && NACC >= 1, "tile does not fit");
+    static_assert(SMEM <= SMEM_LIMIT, "shared memory");
+};
 
 struct GemmArgs {
     int M, N, K, KB, S;
     int MT;     // m-tiles
-    int units;  // work units (see unit_coords)
+    int units;  // MT * n-tiles * S
     int out_kind;
+    int F;      // SwiGLU: output features (N / 2)
     int32_t *status;
 };
 
@@ -68,41 +81,36 @@ __device__ __forceinline__ float swiglu1(float g, float u) {
     return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
 }
 
-// Unit u of the schedule.  Units are numbered with the m-tile fastest, so
-// CTAs that run at the same time on neighbouring units read the same weight
-// tile (the second read hits L2).
-template <bool FUSED>
-__device__ __forceinline__ void unit_coords(const GemmArgs &p, int u, int &m0,
-                                            int &n0, int &nt, int &s_lo,
-                                            int &s_hi) {
-    const int mt = u % p.MT;
-    int rest = u / p.MT;
-    if (FUSED) {
-        nt = rest;
-        s_lo = 0;
-        s_hi = p.S;
-    } else {
-        s_lo = rest % p.S;
-        s_hi = s_lo + 1;
-        nt = rest / p.S;
-    }
-    m0 = mt * BM;
-    n0 = nt * BN;
+__device__ __forceinline__ int slice_lo(const GemmArgs &p, int s) {
+    return (int)((int64_t)s * p.KB / p.S);
 }
 
-// Epilogue store of one 32-row x 128-byte piece: the calling warp's lane r
-// holds row r as 32 words.  The piece goes into this warp's staging buffer
-// in the layout of the 128-byte TMA swizzle (16-byte unit j of row r at
-// unit j ^ (r % 8), conflict-free for st.shared.v4) and out with one TMA
-// store at (x, y, z).  Two buffers alternate; before reusing one, lane 0
-// waits until the store issued from it has finished reading it.
+// Unit u = (m-tile fastest, then slice, then n-tile).  CTAs that run at the
+// same time on neighbouring units read the same weight tile.
+__device__ __forceinline__ void unit_coords(const GemmArgs &p, int u, int &m0,
+                                            int &nt, int &s) {
+    const int mt = u % p.MT;
+    const int rest = u / p.MT;
+    s = rest % p.S;
+    nt = rest / p.S;
+    m0 = mt * BM;
+}
+
+// Epilogue store of one 32-row piece whose row r (lane r) is ROW_BYTES / 4
+// words.  128-byte rows go to the staging buffer in the layout of the
+// 128-byte TMA swizzle (16-byte unit j of row r at unit j ^ (r % 8),
+// conflict-free for st.shared.v4); 64-byte rows are stored plainly.  The
+// piece leaves with one TMA store at (x, y, z).  Two buffers alternate;
+// before reusing one, lane 0 waits until the store issued from it has
+// finished reading it.
 struct Stager {
     uint8_t *buf;   // this warp's two buffers
     int count;
 
+    template <int ROW_BYTES>
     __device__ __forceinline__ void put(const CUtensorMap *map,
-                                       const uint32_t *w, int x, int y, int z,
-                                       bool issue) {
+                                        const uint32_t *w, int x, int y, int z,
+                                        bool issue) {
         const int lane = threadIdx.x & 31;
         uint8_t *b = buf + (count & 1) * STORE_BYTES;
         if (count >= 2) {
@@ -110,9 +118,11 @@ struct Stager {
             __syncwarp();
         }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < ROW_BYTES / 16; ++j) {
             const uint32_t addr =
-                smem_u32(b) + lane * 128 + ((j ^ (lane & 7)) << 4);
+                ROW_BYTES == 128
+                    ? smem_u32(b) + lane * 128 + ((j ^ (lane & 7)) << 4)
+                    : smem_u32(b) + lane * ROW_BYTES + (j << 4);
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
                          "r"(w[4 * j]), "r"(w[4 * j + 1]), "r"(w[4 * j + 2]),
                          "r"(w[4 * j + 3])
@@ -131,24 +141,25 @@ struct Stager {
     }
 };
 
-template <bool FUSED>
+template <int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                 const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmO, GemmArgs p) {
+    using T = Tile<BN>;
+    constexpr int STAGES = T::STAGES, NACC = T::NACC;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + STAGES * A_BYTES;
-    uint8_t *sE = sB + STAGES * B_BYTES;  // epilogue staging, 1024-aligned
+    uint8_t *sE = sB + STAGES * T::B_BYTES;  // epilogue staging, 1024-aligned
     uint64_t *full = reinterpret_cast<uint64_t *>(sE + EPI_BYTES);
     uint64_t *empty = full + STAGES;
     uint64_t *acc_full = empty + STAGES;     // [NACC]
     uint64_t *acc_empty = acc_full + NACC;   // [NACC]
     uint32_t *tslot = reinterpret_cast<uint32_t *>(acc_empty + NACC);
 
-    constexpr uint32_t TMEM_COLS = NACC * BN;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
@@ -175,25 +186,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         int it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-            int m0, n0, nt, s_lo, s_hi;
-            unit_coords<FUSED>(p, u, m0, n0, nt, s_lo, s_hi);
-            for (int s = s_lo; s < s_hi && ok; ++s) {
-                const int kb0 = (int)((int64_t)s * p.KB / p.S);
-                const int kb1 = (int)((int64_t)(s + 1) * p.KB / p.S);
-                for (int kb = kb0; kb < kb1; ++kb, ++it) {
-                    const int st = it % STAGES;
-                    const uint32_t round = it / STAGES;
-                    if (round > 0 && !mbar_wait(&empty[st], (round - 1) & 1,
-                                                p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(&full[st], STAGE_BYTES);
-                    tma_load_2d(sA + st * A_BYTES, &tmA, kb * BK, m0,
-                                &full[st]);
-                    tma_load_2d(sB + st * B_BYTES, &tmB, kb * BK, n0,
-                                &full[st]);
+            int m0, nt, s;
+            unit_coords(p, u, m0, nt, s);
+            const int kb1 = slice_lo(p, s + 1);
+            for (int kb = slice_lo(p, s); kb < kb1; ++kb, ++it) {
+                const int st = it % STAGES;
+                const uint32_t round = it / STAGES;
+                if (round > 0 &&
+                    !mbar_wait(&empty[st], (round - 1) & 1, p.status)) {
+                    ok = false;
+                    break;
                 }
+                mbar_arrive_expect_tx(&full[st], T::STAGE_BYTES);
+                tma_load_2d(sA + st * A_BYTES, &tmA, kb * BK, m0, &full[st]);
+                tma_load_2d(sB + st * T::B_BYTES, &tmB, kb * BK, nt * BN,
+                            &full[st]);
             }
         }
         if (!ok) {
@@ -205,142 +212,106 @@ __global__ void __launch_bounds__(THREADS, 1)
         // --------------------------------------------------------- MMA --
         int it = 0, acc = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-            int m0, n0, nt, s_lo, s_hi;
-            unit_coords<FUSED>(p, u, m0, n0, nt, s_lo, s_hi);
-            for (int s = s_lo; s < s_hi && ok; ++s, ++acc) {
-                const int buf = acc % NACC;
-                if (acc >= NACC &&
-                    !mbar_wait(&acc_empty[buf], ((acc / NACC) - 1) & 1,
-                               p.status)) {
+        for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++acc) {
+            int m0, nt, s;
+            unit_coords(p, u, m0, nt, s);
+            const int buf = acc % NACC;
+            if (acc >= NACC &&
+                !mbar_wait(&acc_empty[buf], ((acc / NACC) - 1) & 1,
+                           p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d0 = tmem + buf * T::ACC_COLS, d1 = d0 + BN;
+            const int kb0 = slice_lo(p, s), kb1 = slice_lo(p, s + 1);
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const int st = it % STAGES;
+                if (!mbar_wait(&full[st], (it / STAGES) & 1, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem + buf * BN;
-                const int kb0 = (int)((int64_t)s * p.KB / p.S);
-                const int kb1 = (int)((int64_t)(s + 1) * p.KB / p.S);
-                for (int kb = kb0; kb < kb1; ++kb, ++it) {
-                    const int st = it % STAGES;
-                    if (!mbar_wait(&full[st], (it / STAGES) & 1, p.status)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a = smem_u32(sA + st * A_BYTES);
-                    const uint32_t b = smem_u32(sB + st * B_BYTES);
+                const uint32_t a = smem_u32(sA + st * A_BYTES);
+                const uint32_t b = smem_u32(sB + st * T::B_BYTES);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
-                        tc_mma_bf16(d_tmem, make_sw128_desc(a + 32 * k),
-                                    make_sw128_desc(b + 32 * k), IDESC,
-                                    (kb > kb0 || k > 0) ? 1u : 0u);
-                    tc_commit(&empty[st]);
+                for (int k = 0; k < BK / 16; ++k) {
+                    const uint64_t bd = make_sw128_desc(b + 32 * k);
+                    const uint32_t accumulate = (kb > kb0 || k > 0) ? 1u : 0u;
+                    tc_mma_bf16(d0, make_sw128_desc(a + 32 * k), bd, T::IDESC,
+                                accumulate);
+                    tc_mma_bf16(d1, make_sw128_desc(a + HALF * 128 + 32 * k),
+                                bd, T::IDESC, accumulate);
                 }
-                tc_commit(&acc_full[buf]);
+                tc_commit(&empty[st]);
             }
+            if (ok) tc_commit(&acc_full[buf]);
         }
     } else if (warp >= 2) {
         // ---------------------------------------------------- epilogue --
         const int q = warp & 3;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
         Stager stg{sE + (warp - 2) * 2 * STORE_BYTES, 0};
-        float run[FUSED ? BN : 1];
         int acc = 0;
-        bool ok = true;
-        for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-            int m0, n0, nt, s_lo, s_hi;
-            unit_coords<FUSED>(p, u, m0, n0, nt, s_lo, s_hi);
-            const int row0 = m0 + q * 32;
-            const bool rows_live = row0 < p.M;
-            for (int s = s_lo, j = 0; s < s_hi; ++s, ++j, ++acc) {
-                const int buf = acc % NACC;
-                if (!mbar_wait(&acc_full[buf], (acc / NACC) & 1, p.status)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t base = lane_addr + buf * BN;
-                if (FUSED) {
+        for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++acc) {
+            int m0, nt, s;
+            unit_coords(p, u, m0, nt, s);
+            const int n0 = nt * BN;
+            const int buf = acc % NACC;
+            if (!mbar_wait(&acc_full[buf], (acc / NACC) & 1, p.status)) break;
+            tc_fence_after();
 #pragma unroll
-                    for (int c = 0; c < BN; c += 32) {
-                        float v[32];
-                        tmem_ld_32cols(base + c, v);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            run[c + i] =
-                                (j == 0) ? v[i] : __fadd_rn(run[c + i], v[i]);
-                    }
-                } else if (p.out_kind == BI_OUT_SWIGLU) {
-                    uint32_t w[32];
-#pragma unroll
-                    for (int c = 0; c < BN / 2; c += 32) {
+            for (int h = 0; h < 2; ++h) {
+                const int row0 = m0 + h * HALF + q * 32;
+                const bool live = row0 < p.M;
+                const uint32_t base = lane_addr + buf * T::ACC_COLS + h * BN;
+                if (p.out_kind == BI_OUT_SWIGLU) {
+                    // gate columns [0, w), up columns [w, 2w) of this tile
+                    const int f0 = nt * (BN / 2);
+                    const int w = min(BN / 2, p.F - f0);
+                    for (int c = 0; c < w; c += 32) {
                         float g[32], uu[32];
+                        uint32_t wd[16];
                         tmem_ld_32cols(base + c, g);
-                        tmem_ld_32cols(base + BN / 2 + c, uu);
+                        tmem_ld_32cols(base + w + c, uu);
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            w[c / 2 + i] = pack_bf16x2(
-                                swiglu1(g[2 * i], uu[2 * i]),
-                                swiglu1(g[2 * i + 1], uu[2 * i + 1]));
+                            wd[i] = pack_bf16x2(swiglu1(g[2 * i], uu[2 * i]),
+                                                swiglu1(g[2 * i + 1],
+                                                        uu[2 * i + 1]));
+                        stg.put<64>(&tmO, wd, f0 + c, row0, 0, live);
                     }
-                    stg.put(&tmO, w, nt * (BN / 2), row0, 0, rows_live);
                 } else if (p.out_kind == BI_OUT_BF16) {
 #pragma unroll
                     for (int c = 0; c < BN; c += 64) {
-                        uint32_t w[32];
+                        uint32_t wd[32];
                         float v[32];
                         tmem_ld_32cols(base + c, v);
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+                            wd[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
                         tmem_ld_32cols(base + c + 32, v);
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            w[16 + i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-                        stg.put(&tmO, w, n0 + c, row0, 0,
-                                rows_live && n0 + c < p.N);
+                            wd[16 + i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+                        stg.put<128>(&tmO, wd, n0 + c, row0, 0,
+                                     live && n0 + c < p.N);
                     }
                 } else {  // fp32: partial slice s (or the only slice)
 #pragma unroll
                     for (int c = 0; c < BN; c += 32) {
                         float v[32];
                         tmem_ld_32cols(base + c, v);
-                        stg.put(&tmO, reinterpret_cast<const uint32_t *>(v),
-                                n0 + c, row0, p.out_kind == BI_OUT_PARTIALS ? s : 0,
-                                rows_live && n0 + c < p.N);
+                        stg.put<128>(&tmO, reinterpret_cast<const uint32_t *>(v),
+                                     n0 + c, row0,
+                                     p.out_kind == BI_OUT_PARTIALS ? s : 0,
+                                     live && n0 + c < p.N);
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&acc_empty[buf]);
             }
-            if (FUSED && ok) {
-                if (p.out_kind == BI_OUT_SWIGLU) {
-                    uint32_t w[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        w[i] = pack_bf16x2(
-                            swiglu1(run[2 * i], run[BN / 2 + 2 * i]),
-                            swiglu1(run[2 * i + 1], run[BN / 2 + 2 * i + 1]));
-                    stg.put(&tmO, w, nt * (BN / 2), row0, 0, rows_live);
-                } else if (p.out_kind == BI_OUT_BF16) {
-#pragma unroll
-                    for (int c = 0; c < BN; c += 64) {
-                        uint32_t w[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            w[i] = pack_bf16x2(run[c + 2 * i], run[c + 2 * i + 1]);
-                        stg.put(&tmO, w, n0 + c, row0, 0,
-                                rows_live && n0 + c < p.N);
-                    }
-                } else {
-#pragma unroll
-                    for (int c = 0; c < BN; c += 32)
-                        stg.put(&tmO,
-                                reinterpret_cast<const uint32_t *>(run + c),
-                                n0 + c, row0, 0, rows_live && n0 + c < p.N);
-                }
-            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
         }
         if (lane == 0) bulk_wait<0>();  // stores done before the CTA exits
     }
@@ -353,7 +324,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 }
 
-// Second stage of the split schedule: y = sum_s ws[s] in slice order.
+// Second stage: y = sum_s ws[s] in slice order.
 __global__ void reduce_slices_kernel(const float *__restrict__ ws, int S,
                                      int64_t MN, int out_kind, void *out) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -366,46 +337,114 @@ __global__ void reduce_slices_kernel(const float *__restrict__ ws, int S,
         reinterpret_cast<float *>(out)[i] = v;
 }
 
+// Second stage of SwiGLU with S > 1: gate and up sums (slice order) of
+// feature f, then silu(g) * u.  Columns follow the bi_pack_gate_up
+// interleave with blocks of w0 features.
+__global__ void reduce_swiglu_kernel(const float *__restrict__ ws, int S,
+                                     int M, int N, int F, int w0,
+                                     uint16_t *__restrict__ out) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)M * F) return;
+    const int64_t m = i / F;
+    const int f = (int)(i % F);
+    const int b = f / w0, j = f % w0;
+    const int w = min(w0, F - b * w0);
+    const int64_t gc = m * N + (int64_t)b * 2 * w0 + j, uc = gc + w;
+    const int64_t MN = (int64_t)M * N;
+    float g = ws[gc], u = ws[uc];
+    for (int s = 1; s < S; ++s) {
+        g = __fadd_rn(g, ws[s * MN + gc]);
+        u = __fadd_rn(u, ws[s * MN + uc]);
+    }
+    out[i] = f32_to_bf16(swiglu1(g, u));
+}
+
+// Row r of the interleaved weight: block b = r / (2 w0) holds features
+// [b w0, b w0 + w), w = min(w0, F - b w0): its first w rows are the gate
+// rows of those features, the next w the up rows.
 __global__ void pack_gate_up_kernel(const uint4 *__restrict__ wg,
                                     const uint4 *__restrict__ wu, int F,
-                                    int K8, uint4 *__restrict__ wgu) {
-    // Output row r: block b = r / 128, within-block j = r % 128;
-    // j < 64 -> gate row 64b + j, else up row 64b + j - 64.
+                                    int K8, int w0, uint4 *__restrict__ wgu) {
     const int64_t total = (int64_t)2 * F * K8;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = i / K8, c = i % K8;
-        const int64_t b = r / 128, j = r % 128;
-        const uint4 *src = j < 64 ? wg + (b * 64 + j) * K8
-                                  : wu + (b * 64 + j - 64) * K8;
+        const int b = (int)(r / (2 * w0)), j = (int)(r % (2 * w0));
+        const int w = min(w0, F - b * w0);
+        const uint4 *src = j < w ? wg + ((int64_t)b * w0 + j) * K8
+                                 : wu + ((int64_t)b * w0 + j - w) * K8;
         wgu[i] = src[c];
     }
 }
 
-template <bool FUSED>
+template <int BN>
 bi_status set_smem_attr() {
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
-        err = cudaFuncSetAttribute(gemm_kernel<FUSED>,
+        err = cudaFuncSetAttribute(gemm_kernel<BN>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)smem_bytes());
+                                   (int)Tile<BN>::SMEM);
     });
     return bi_cuda_check(err, "gemm smem attribute");
+}
+
+struct Plan {
+    int bn, s;
+};
+
+// (BN, S) for a weight of shape [N][K], from a time model of a 256-row
+// batch on a 152-SM GPU: the busiest SM loads waves * (256 + BN) * 128 *
+// ceil(KB / S) bytes at ~85 GB/s (waves = ceil(tiles * S / 152)), and for
+// S > 1 the S fp32 partial planes are written once and read once at
+// ~6 TB/s.  BN in {128, 192, 256}, S in 1 .. min(8, KB / 4); ties go to the
+// smaller S, then the smaller BN.  The model only ranks plans: any plan
+// gives M-invariant results, and the plan depends on (N, K) alone.
+Plan gemm_plan(int N, int K) {
+    const int KB = (K + BK - 1) / BK;
+    const int smax = std::max(1, std::min(MAX_SPLITS, KB / 4));
+    Plan best{128, 1};
+    double best_us = -1.0;
+    for (int s = 1; s <= smax; ++s) {
+        for (int bn : {128, 192, 256}) {
+            const int64_t units = (int64_t)((N + bn - 1) / bn) * s;
+            const int64_t waves = (units + PLAN_SMS - 1) / PLAN_SMS;
+            const double load_us = (double)waves * (256 + bn) * 128.0 *
+                                   ((KB + s - 1) / s) / 85e3;
+            const double part_us =
+                s > 1 ? 2.0 * s * 256.0 * N * 4.0 / 6e6 : 0.0;
+            const double us = load_us + part_us;
+            if (best_us < 0 || us < best_us) {
+                best_us = us;
+                best = {bn, s};
+            }
+        }
+    }
+    return best;
+}
+
+template <int BN>
+bi_status launch(const CUtensorMap &ta, const CUtensorMap &tb,
+                 const CUtensorMap &to, const GemmArgs &a,
+                 cudaStream_t stream) {
+    bi_status st = set_smem_attr<BN>();
+    if (st != BI_OK) return st;
+    const int grid = std::min(a.units, bi_sm_count());
+    gemm_kernel<BN><<<grid, THREADS, Tile<BN>::SMEM, stream>>>(ta, tb, to, a);
+    BI_LAUNCH_CHECK("gemm launch");
+    return BI_OK;
 }
 
 }  // namespace
 
 extern "C" int bi_gemm_splits(int N, int K) {
-    // A pure function of the weight shape.  Aim for about one work unit per
-    // SM of a 152-SM GB300 at small M (two m-tiles give two per SM at
-    // M = 256), with at least 4 k-blocks per slice and at most 8 slices.
-    const int KB = (K + BK - 1) / BK;
-    const int tiles = (N + BN - 1) / BN;
-    int s = 152 / std::max(tiles, 1);
-    s = std::min(s, 8);
-    s = std::min(s, KB / 4);
-    return std::max(s, 1);
+    if (N <= 0 || K <= 0) return 1;
+    return gemm_plan(N, K).s;
+}
+
+extern "C" int bi_gemm_tile_n(int N, int K) {
+    if (N <= 0 || K <= 0) return 128;
+    return gemm_plan(N, K).bn;
 }
 
 extern "C" size_t bi_gemm_workspace_size(int M, int N, int K) {
@@ -414,45 +453,29 @@ extern "C" size_t bi_gemm_workspace_size(int M, int N, int K) {
     return (size_t)S * M * N * sizeof(float);
 }
 
-// Default schedule.  Either schedule gives the same bits, so this is a pure
-// cost choice: fused once the output tiles alone fill the GPU.  (Measured on
-// the 8B decode shapes at M = 256: with 48-96 tiles the fused schedule loses
-// more to idle SMs than it saves in partial traffic.)
-bool bi_gemm_default_fused(int M, int N, int K) {
-    const int S = bi_gemm_splits(N, K);
-    if (S <= 1) return false;
-    const int64_t tiles = (int64_t)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    return tiles >= 148;
-}
-
-bi_status bi_gemm_sched(const bi_bf16 *x, int M, int K, const bi_bf16 *W,
-                        int N, void *out, int out_kind, void *ws,
-                        size_t ws_bytes, int mode, cudaStream_t stream) {
+extern "C" bi_status bi_gemm(const bi_bf16 *x, int M, int K, const bi_bf16 *W,
+                             int N, void *out, int out_kind, void *ws,
+                             size_t ws_bytes, void *stream_) {
     BI_REQUIRE(M >= 0 && N > 0 && K > 0, "bi_gemm: bad shape M=%d N=%d K=%d",
                M, N, K);
     BI_REQUIRE(K % 8 == 0 && N % 8 == 0,
                "bi_gemm: K=%d and N=%d must be multiples of 8", K, N);
+    BI_REQUIRE(out_kind >= BI_OUT_PARTIALS && out_kind <= BI_OUT_SWIGLU,
+               "bi_gemm: bad out_kind %d", out_kind);
+    if (out_kind == BI_OUT_SWIGLU)
+        BI_REQUIRE(N % 64 == 0,
+                   "bi_gemm: SwiGLU needs N %% 64 == 0 (N=%d, 2F with F a "
+                   "multiple of 32)",
+                   N);
     if (M == 0) return BI_OK;
     BI_REQUIRE(x && W && out, "bi_gemm: null pointer");
     BI_REQUIRE(bi_aligned16(x) && bi_aligned16(W) && bi_aligned16(out),
                "bi_gemm: pointers must be 16-byte aligned");
-    BI_REQUIRE(out_kind >= BI_OUT_PARTIALS && out_kind <= BI_OUT_SWIGLU,
-               "bi_gemm: bad out_kind %d", out_kind);
-    const int S = bi_gemm_splits(N, K);
+    cudaStream_t stream = bi_stream(stream_);
+    const Plan plan = gemm_plan(N, K);
+    const int S = plan.s, BN = plan.bn;
     const int KB = (K + BK - 1) / BK;
     const int mt = (M + BM - 1) / BM, nt = (N + BN - 1) / BN;
-    if (out_kind == BI_OUT_SWIGLU)
-        BI_REQUIRE(N % BN == 0, "bi_gemm: SwiGLU needs N %% 128 == 0 (N=%d)", N);
-    bool fused;
-    if (mode == 1)
-        fused = false;
-    else if (mode == 2)
-        fused = true;
-    else
-        fused = bi_gemm_default_fused(M, N, K);
-    if (out_kind == BI_OUT_PARTIALS && S > 1) fused = false;
-    if (S == 1) fused = false;
-    if (out_kind == BI_OUT_SWIGLU && S > 1) fused = true;
 
     CUtensorMap ta, tb, to;
     bi_status st = bi_make_tmap_2d_bf16(&ta, x, K, M, (uint64_t)K * 2, BK, BM,
@@ -467,12 +490,14 @@ bi_status bi_gemm_sched(const bi_bf16 *x, int M, int K, const bi_bf16 *W,
     a.K = K;
     a.KB = KB;
     a.S = S;
+    a.MT = mt;
+    a.units = mt * nt * S;
     a.out_kind = out_kind;
+    a.F = N / 2;
     a.status = bi_status_ptr();
 
     void *dst = out;
-    const bool need_reduce =
-        !fused && S > 1 && out_kind != BI_OUT_PARTIALS;
+    const bool need_reduce = S > 1 && out_kind != BI_OUT_PARTIALS;
     if (need_reduce) {
         const size_t need = (size_t)S * M * N * sizeof(float);
         if (!ws || ws_bytes < need)
@@ -483,62 +508,61 @@ bi_status bi_gemm_sched(const bi_bf16 *x, int M, int K, const bi_bf16 *W,
         dst = ws;
         a.out_kind = BI_OUT_PARTIALS;
     }
-    // Output map: fp32 [planes][M][N] in 32 x 32 boxes, or bf16 [M][cols]
-    // in 64 x 32 boxes (128-byte rows, swizzled like the staging buffer).
+    // Output map: fp32 [planes][M][N] in 32 x 32 boxes, bf16 [M][N] in
+    // 64 x 32 boxes (128-byte rows, swizzled like the staging buffer), or
+    // the SwiGLU bf16 [M][N/2] in plain 32 x 32 boxes (64-byte rows: a
+    // tile's output width is a multiple of 32, not of 64).
     if (a.out_kind == BI_OUT_PARTIALS)
-        st = bi_make_tmap_3d(&to, dst, true, N, M, S, 32, 32);
+        st = bi_make_tmap_3d(&to, dst, true, N, M, S, 32, 32, true);
     else if (a.out_kind == BI_OUT_F32)
-        st = bi_make_tmap_3d(&to, dst, true, N, M, 1, 32, 32);
+        st = bi_make_tmap_3d(&to, dst, true, N, M, 1, 32, 32, true);
     else if (a.out_kind == BI_OUT_BF16)
-        st = bi_make_tmap_3d(&to, dst, false, N, M, 1, 64, 32);
+        st = bi_make_tmap_3d(&to, dst, false, N, M, 1, 64, 32, true);
     else
-        st = bi_make_tmap_3d(&to, dst, false, N / 2, M, 1, 64, 32);
+        st = bi_make_tmap_3d(&to, dst, false, N / 2, M, 1, 32, 32, false);
     if (st != BI_OK) return st;
 
-    a.MT = mt;
-    a.units = fused ? mt * nt : mt * nt * S;
-    const int grid = std::min(a.units, bi_sm_count());
-    if (fused) {
-        if ((st = set_smem_attr<true>()) != BI_OK) return st;
-        gemm_kernel<true><<<grid, THREADS, smem_bytes(), stream>>>(ta, tb, to,
-                                                                   a);
-    } else {
-        if ((st = set_smem_attr<false>()) != BI_OK) return st;
-        gemm_kernel<false><<<grid, THREADS, smem_bytes(), stream>>>(ta, tb, to,
-                                                                    a);
-    }
-    BI_LAUNCH_CHECK("gemm launch");
+    if (BN == 128)
+        st = launch<128>(ta, tb, to, a, stream);
+    else if (BN == 192)
+        st = launch<192>(ta, tb, to, a, stream);
+    else
+        st = launch<256>(ta, tb, to, a, stream);
+    if (st != BI_OK) return st;
     if (need_reduce) {
-        const int64_t MN = (int64_t)M * N;
-        reduce_slices_kernel<<<(unsigned)((MN + 255) / 256), 256, 0, stream>>>(
-            static_cast<const float *>(ws), S, MN, out_kind, out);
+        if (out_kind == BI_OUT_SWIGLU) {
+            const int64_t MF = (int64_t)M * (N / 2);
+            reduce_swiglu_kernel<<<(unsigned)((MF + 255) / 256), 256, 0,
+                                   stream>>>(
+                static_cast<const float *>(ws), S, M, N, N / 2, BN / 2,
+                static_cast<uint16_t *>(out));
+        } else {
+            const int64_t MN = (int64_t)M * N;
+            reduce_slices_kernel<<<(unsigned)((MN + 255) / 256), 256, 0,
+                                   stream>>>(static_cast<const float *>(ws), S,
+                                             MN, out_kind, out);
+        }
         BI_LAUNCH_CHECK("gemm reduce launch");
     }
     return BI_OK;
 }
 
-extern "C" bi_status bi_gemm(const bi_bf16 *x, int M, int K, const bi_bf16 *W,
-                             int N, void *out, int out_kind, void *ws,
-                             size_t ws_bytes, void *stream) {
-    return bi_gemm_sched(x, M, K, W, N, out, out_kind, ws, ws_bytes, 0,
-                         bi_stream(stream));
-}
-
 extern "C" bi_status bi_pack_gate_up(const bi_bf16 *wg, const bi_bf16 *wu,
                                      int F, int K, bi_bf16 *wgu,
                                      void *stream) {
-    BI_REQUIRE(wg && wu && wgu, "bi_pack_gate_up: null pointer");
-    BI_REQUIRE(F > 0 && F % 64 == 0 && K > 0 && K % 8 == 0,
-               "bi_pack_gate_up: F=%d must be a multiple of 64, K=%d of 8", F,
+    BI_REQUIRE(F > 0 && F % 32 == 0 && K > 0 && K % 8 == 0,
+               "bi_pack_gate_up: F=%d must be a multiple of 32, K=%d of 8", F,
                K);
+    BI_REQUIRE(wg && wu && wgu, "bi_pack_gate_up: null pointer");
     BI_REQUIRE(bi_aligned16(wg) && bi_aligned16(wu) && bi_aligned16(wgu),
                "bi_pack_gate_up: pointers must be 16-byte aligned");
     const int K8 = K / 8;
+    const int w0 = bi_gemm_tile_n(2 * F, K) / 2;
     const int64_t total = (int64_t)2 * F * K8;
     const int blocks = (int)std::min<int64_t>((total + 255) / 256, 4096);
     pack_gate_up_kernel<<<blocks, 256, 0, bi_stream(stream)>>>(
         reinterpret_cast<const uint4 *>(wg), reinterpret_cast<const uint4 *>(wu),
-        F, K8, reinterpret_cast<uint4 *>(wgu));
+        F, K8, w0, reinterpret_cast<uint4 *>(wgu));
     BI_LAUNCH_CHECK("pack_gate_up launch");
     return BI_OK;
 }

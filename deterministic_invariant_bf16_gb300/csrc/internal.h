@@ -22,19 +22,17 @@ bi_status bi_make_tmap_2d_bf16(CUtensorMap *map, const void *base,
                                uint32_t box_outer, bool swizzle128);
 
 // 3-D tensor map over a row-major [d2][d1][d0] array of fp32 (f32) or bf16,
-// box {box0, box1, 1}, 128-byte swizzle (box0 * element size must be 128).
+// box {box0, box1, 1}; with swizzle128 the 128-byte swizzle (box0 * element
+// size must then be 128), else no swizzle.
 bi_status bi_make_tmap_3d(CUtensorMap *map, const void *base, bool f32,
                           uint64_t d0, uint64_t d1, uint64_t d2,
-                          uint32_t box0, uint32_t box1);
+                          uint32_t box0, uint32_t box1, bool swizzle128);
 
-// GEMM with a forced schedule, for the model driver and the schedule test:
-// mode 0 = the default choice, 1 = every split in its own CTA,
-// 2 = every split of a tile in one CTA.
-bi_status bi_gemm_sched(const bi_bf16 *x, int M, int K, const bi_bf16 *W,
-                        int N, void *out, int out_kind, void *ws,
-                        size_t ws_bytes, int mode, cudaStream_t stream);
 
-// Attention with the KV pool size known, for the model driver.
+
+// Attention with the KV pool size known, for the model driver.  Decode
+// stages: bit 0 chunk kernels (bit 2: reuse the work list already in ws),
+// bit 1 merge.
 bi_status bi_decode_attn_pool(const bi_bf16 *q, const bi_bf16 *k_pool,
                               const bi_bf16 *v_pool, const int32_t *page_table,
                               int max_pages, int n_pages,
@@ -49,7 +47,6 @@ bi_status bi_prefill_attn_pool(const bi_bf16 *q, const int32_t *cu_q,
                                const int32_t *page_table, int max_pages,
                                int n_pages, int Hq, int Hkv, int D,
                                float scale, bi_bf16 *out, cudaStream_t stream);
-bool bi_gemm_default_fused(int M, int N, int K);
 
 // RoPE in two parts for the model driver: the (cos, sin) table of the rows'
 // positions ([T][D/2] float2), computed once per forward, and the rotation

@@ -3,10 +3,9 @@
 //
 // The driver runs the pre-norm Llama block stack over caller-owned weights,
 // KV pools and workspace.  Every launch goes to the caller's stream, so a
-// caller may capture a whole forward pass in a CUDA graph.  The GEMM
-// schedule (split or fused, see gemm.cu) is chosen per call from the shape;
-// both schedules produce the same bits, so the choice never shows in the
-// result.
+// caller may capture a whole forward pass in a CUDA graph.  The GEMMs write
+// their fixed K slices as fp32 partials that the next kernel (RoPE, RMSNorm)
+// sums in slice order; the gate/up GEMM applies SwiGLU in its epilogue.
 //
 // Verification follows "LLM-42: Enabling Determinism in LLM Inference with
 // Verified Speculation", section "核心方法" (paper sections 4.2-4.3, Fig. 8):
@@ -58,7 +57,8 @@ struct Profiler {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Layout {
-    size_t h, x, qkv, q, attn, o, f, d, att_ws, kvlen, rope, vbuf, total;
+    size_t h, x, qkv, q, attn, o, f, d, gemm_ws, att_ws, kvlen, rope, vbuf,
+        total;
     int S_qkv, S_o, S_d;
 };
 
@@ -96,6 +96,10 @@ Layout layout(const bi_model_cfg &c, int max_pages_total) {
     L.o = take((size_t)L.S_o * T * H * 4);
     L.f = take((size_t)T * F * 2);
     L.d = take((size_t)L.S_d * T * H * 4);
+    // second-stage workspace of the gate/up and LM-head GEMMs (only for
+    // shapes with more than one K slice)
+    L.gemm_ws = take(std::max(bi_gemm_workspace_size(T, 2 * F, H),
+                              bi_gemm_workspace_size(T, c.vocab, H)));
     L.att_ws = take(bi_decode_attn_workspace_size(T, c.n_heads, c.head_dim,
                                                   c.max_kv_len));
     L.kvlen = take((size_t)T * 4);
@@ -277,16 +281,13 @@ extern "C" bi_status bi_model_create(const bi_model_cfg *cfg,
 
 extern "C" void bi_model_destroy(bi_model *m) { delete m; }
 
-// GEMM whose result a split-aware consumer reads: returns the number of
-// fp32 slices written to `out` (S for the split schedule, 1 for fused).
+// GEMM whose result a split-aware consumer reads: the S fp32 slice
+// partials go to `out`; *slices = S.
 static bi_status gemm_slices(const bi_bf16 *x, int M, int K, const bi_bf16 *W,
                              int N, float *out, int *slices,
                              cudaStream_t s) {
-    const bool fused = bi_gemm_default_fused(M, N, K);
-    *slices = fused ? 1 : bi_gemm_splits(N, K);
-    return bi_gemm_sched(x, M, K, W, N, out,
-                         fused ? BI_OUT_F32 : BI_OUT_PARTIALS, nullptr, 0,
-                         fused ? 2 : 1, s);
+    *slices = bi_gemm_splits(N, K);
+    return bi_gemm(x, M, K, W, N, out, BI_OUT_PARTIALS, nullptr, 0, s);
 }
 
 extern "C" bi_status bi_model_forward(bi_model *m, int T, const int32_t *tokens,
@@ -324,6 +325,8 @@ extern "C" bi_status bi_model_forward(bi_model *m, int T, const int32_t *tokens,
     bi_bf16 *f = reinterpret_cast<bi_bf16 *>(ws + m->L.f);
     float *d = reinterpret_cast<float *>(ws + m->L.d);
     void *att_ws = ws + m->L.att_ws;
+    void *gemm_ws = ws + m->L.gemm_ws;
+    const size_t gemm_ws_bytes = m->L.att_ws - m->L.gemm_ws;
     int32_t *kvlen = reinterpret_cast<int32_t *>(ws + m->L.kvlen);
     float2 *rope_tab = reinterpret_cast<float2 *>(ws + m->L.rope);
     const size_t att_ws_bytes = m->L.kvlen - m->L.att_ws;
@@ -372,7 +375,7 @@ extern "C" bi_status bi_model_forward(bi_model *m, int T, const int32_t *tokens,
                                          page_table, c.max_pages, c.n_pages,
                                          row_req, kvlen, T, max_kv_len, Hq,
                                          Hkv, D, scale, attn, att_ws,
-                                         att_ws_bytes, 1, s));
+                                         att_ws_bytes, l == 0 ? 1 : 1 | 4, s));
             BI_TIMED(BI_PROF_ATTN_MERGE,
                      bi_decode_attn_pool(q, m->kpool[l], m->vpool[l],
                                          page_table, c.max_pages, c.n_pages,
@@ -392,16 +395,16 @@ extern "C" bi_status bi_model_forward(bi_model *m, int T, const int32_t *tokens,
         BI_TIMED(BI_PROF_NORM, bi_rmsnorm(o, s_o, nullptr, h, m->ffn_norm[l],
                                           T, H, c.eps, x, s));
         BI_TIMED(BI_PROF_GEMM_GATE_UP,
-                 bi_gemm_sched(x, T, H, m->wgu[l], 2 * F, f, BI_OUT_SWIGLU,
-                               nullptr, 0, 0, s));
+                 bi_gemm(x, T, H, m->wgu[l], 2 * F, f, BI_OUT_SWIGLU,
+                         gemm_ws, gemm_ws_bytes, s));
         BI_TIMED(BI_PROF_GEMM_DOWN,
                  gemm_slices(f, T, F, m->wd[l], H, d, &s_d, s));
     }
     BI_TIMED(BI_PROF_NORM, bi_rmsnorm(d, s_d, nullptr, h, m->final_norm, T, H,
                                       c.eps, x, s));
     BI_TIMED(BI_PROF_LM_HEAD,
-             bi_gemm_sched(x, T, H, m->lm_head, c.vocab, logits, BI_OUT_F32,
-                           nullptr, 0, 0, s));
+             bi_gemm(x, T, H, m->lm_head, c.vocab, logits, BI_OUT_F32,
+                     gemm_ws, gemm_ws_bytes, s));
     if (ids)
         BI_TIMED(BI_PROF_OTHER,
                  bi_argmax_logits(logits, T, c.vocab, ids, s));

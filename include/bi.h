@@ -72,11 +72,12 @@ bi_status bi_device_status(int32_t *h_status, void *stream);
  * with a fixed-order second stage, no float atomics).
  *
  * x [M][K] bf16, W [N][K] bf16 (row n = output feature n, "K-major").
- * fp32 accumulation on the tcgen05 tensor cores.  The tile is 128 x 128
- * output elements for every M (rows past M are zero-filled, never read from
- * memory).  The K range is cut into bi_gemm_splits(N, K) fixed slices of
- * whole 64-column blocks; each slice is an independent fp32 chain in
- * ascending k.  Slices are summed in slice order 0..S-1 by the consumer.
+ * fp32 accumulation on the tcgen05 tensor cores.  The tile is 256 rows x
+ * bi_gemm_tile_n(N, K) columns for every M (rows past M are zero-filled,
+ * never read from memory).  The K range is cut into bi_gemm_splits(N, K)
+ * fixed slices of whole 64-column blocks; each slice is an independent fp32
+ * chain in ascending k.  Slices are summed in slice order 0..S-1 by the
+ * consumer.
  *
  * out_kind selects what is written to `out`:
  *   BI_OUT_PARTIALS  fp32 [S][M][N]: the S slice sums, unreduced.  The
@@ -84,9 +85,11 @@ bi_status bi_device_status(int32_t *h_status, void *stream);
  *   BI_OUT_F32       fp32 [M][N]: slices reduced in order (needs workspace
  *                    bi_gemm_workspace_size(M, N, K) if S > 1).
  *   BI_OUT_BF16      bf16 [M][N]: as F32, rounded to nearest even.
- *   BI_OUT_SWIGLU    bf16 [M][N/2]: W holds gate and up rows interleaved in
- *                    blocks of 64 (bi_pack_gate_up); out = silu(g) * u with
- *                    silu(g) = g / (1 + e^-g) in fp32.  Needs S == 1.
+ *   BI_OUT_SWIGLU    bf16 [M][N/2]: W holds gate and up rows interleaved
+ *                    as bi_pack_gate_up writes them; out = silu(g) * u with
+ *                    silu(g) = g / (1 + e^-g) in fp32 on the slice sums.
+ *                    N must be a multiple of 64; needs the workspace if
+ *                    S > 1.
  */
 typedef enum {
     BI_OUT_PARTIALS = 0,
@@ -95,11 +98,15 @@ typedef enum {
     BI_OUT_SWIGLU = 3
 } bi_out_kind;
 
-/* Fixed split count for a weight of shape [N][K]: a pure function of (N, K),
- * never of M. */
+/* Fixed split count S (1..8) and tile width (128, 192 or 256) for a weight
+ * of shape [N][K]: pure functions of (N, K), never of M.  They are the plan
+ * a time model of a 256-row batch on a 152-SM GB300 ranks fastest (bytes
+ * loaded by the busiest SM, plus the fp32 partial traffic when S > 1). */
 int bi_gemm_splits(int N, int K);
+int bi_gemm_tile_n(int N, int K);
 
-/* Bytes of workspace bi_gemm needs for (M, N, K) and BI_OUT_F32/BF16. */
+/* Bytes of workspace bi_gemm needs for (M, N, K) and BI_OUT_F32, BF16 or
+ * SWIGLU (S * M * N * 4 when S > 1, else 0). */
 size_t bi_gemm_workspace_size(int M, int N, int K);
 
 bi_status bi_gemm(const bi_bf16 *x, int M, int K, const bi_bf16 *W, int N,
@@ -107,8 +114,10 @@ bi_status bi_gemm(const bi_bf16 *x, int M, int K, const bi_bf16 *W, int N,
                   void *stream);
 
 /* Interleaves separate gate and up weights, each [F][K], into the [2F][K]
- * layout BI_OUT_SWIGLU reads: 64 gate rows, then the 64 up rows of the same
- * features, and so on.  F must be a multiple of 64.  A pure copy. */
+ * layout BI_OUT_SWIGLU reads, one block per GEMM tile: with
+ * w0 = bi_gemm_tile_n(2F, K) / 2, block b holds features [b w0, b w0 + w),
+ * w = min(w0, F - b w0), as w gate rows followed by the w up rows of the
+ * same features.  F must be a multiple of 32.  A pure copy. */
 bi_status bi_pack_gate_up(const bi_bf16 *wg, const bi_bf16 *wu, int F, int K,
                           bi_bf16 *wgu, void *stream);
 

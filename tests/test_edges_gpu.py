@@ -53,13 +53,18 @@ def test_host_refuses_bad_shapes(bi):
     W = dev((128, 60))   # K not a multiple of 8
     with pytest.raises(bi.BiError):
         bi.bi_gemm(dev((4, 60)), W, out, bi.OUT_F32)
-    # SwiGLU with more than one K slice is served by the fused schedule
+    # SwiGLU with more than one K slice needs the second-stage workspace
     K = 4096
     wgu = dev((256, K), seed=3)
     xs = dev((3, K), seed=4)
     sw = torch.empty(3, 128, dtype=torch.bfloat16, device="cuda")
     assert bi.bi_gemm_splits(256, K) > 1
-    bi.bi_gemm(xs, wgu, sw, bi.OUT_SWIGLU)
+    with pytest.raises(bi.BiError) as e:
+        bi.bi_gemm(xs, wgu, sw, bi.OUT_SWIGLU)
+    assert e.value.status == 3
+    ws = torch.empty(bi.bi_gemm_workspace_size(3, 256, K) // 4,
+                     dtype=torch.float32, device="cuda")
+    bi.bi_gemm(xs, wgu, sw, bi.OUT_SWIGLU, ws)
     torch.cuda.synchronize()
     assert bi.bi_device_status() == 0
 

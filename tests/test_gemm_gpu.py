@@ -1,7 +1,7 @@
 """bi_gemm on the GPU: parity with the oracle's sequential fp32 GEMM, exact
 results on integer data, and bitwise batch invariance (ybb.press sections
 1, 2.2 and 4: the same row must give the same bits for every M, every row
-position and every schedule)."""
+position and every tile plan)."""
 import numpy as np
 import pytest
 import torch
@@ -111,16 +111,15 @@ def test_batch_invariance_4096(bi, orc):
 @pytest.mark.parametrize("N,K", [(14336, 4096), (4096, 14336),
                                  (14336, 14336), (128256, 4096)])
 def test_batch_invariance_8b_shapes(bi, orc, N, K):
-    """The 8B FFN and LM-head shapes (and the literal N=K=14336 square).
-    For (14336, 4096) M=128 runs the split schedule and M=256 the fused one,
-    so their equality also pins schedule independence."""
+    """The 8B FFN and LM-head shapes (and the literal N=K=14336 square),
+    covering the 128-, 192- and 256-column tile plans."""
     W = randn_bf16((N, K), 21)
     x = randn_bf16((256, K), 22)
     _check_rows(bi, orc, x, W, [1, 64, 128], [0, 5, 128, 255], n_cols=24)
 
 
-def test_schedules_agree_at_prefill_size(bi):
-    """M=2048 (fused) against the same rows computed at M=64 (split)."""
+def test_rows_agree_at_prefill_size(bi):
+    """M=2048 (eight m-tiles) against the same rows computed at M=64."""
     W = randn_bf16((4096, 4096), 31)
     x = randn_bf16((2048, 4096), 32)
     big = f32bits(gemm(bi, x, W))
@@ -140,12 +139,47 @@ def test_bf16_and_swiglu_epilogues(bi, orc):
     wgu = torch.empty(2 * F, K, dtype=torch.bfloat16, device="cuda")
     bi.bi_pack_gate_up(wg, wu, wgu)
     torch.cuda.synchronize()
-    assert torch.equal(wgu[64:128], wu[:64]) and torch.equal(wgu[128:192],
-                                                             wg[64:128])
+    w0 = bi.bi_gemm_tile_n(2 * F, K) // 2
+    assert torch.equal(wgu[w0:2 * w0], wu[:w0]) and torch.equal(
+        wgu[2 * w0:3 * w0], wg[w0:2 * w0])
     sw = gemm(bi, x, wgu, bi.OUT_SWIGLU)
     g = gemm(bi, x, wg).cpu().numpy()
     u = gemm(bi, x, wu).cpu().numpy()
     ref = orc.bf16_bits(orc.swiglu(g, u)).astype(np.int32)
     diff = np.abs(bits(sw).astype(np.int32) - ref)
     assert diff.max() <= 1      # at most one bf16 ulp (expf last bit)
+    assert (diff == 0).mean() > 0.99
+
+
+def _swiglu_via_f32(bi, orc, x, wgu, F):
+    """SwiGLU of the F32 GEMM on the interleaved weight (the same plan, so
+    the same sums), de-interleaved on the host, by the oracle's formula."""
+    K = x.shape[1]
+    y = gemm(bi, x, wgu).cpu().numpy()
+    w0 = bi.bi_gemm_tile_n(2 * F, K) // 2
+    g = np.empty((x.shape[0], F), np.float32)
+    u = np.empty_like(g)
+    for b in range(-(-F // w0)):
+        w = min(w0, F - b * w0)
+        g[:, b * w0:b * w0 + w] = y[:, 2 * b * w0:2 * b * w0 + w]
+        u[:, b * w0:b * w0 + w] = y[:, 2 * b * w0 + w:2 * b * w0 + 2 * w]
+    return orc.bf16_bits(orc.swiglu(g, u)).astype(np.int32)
+
+
+@pytest.mark.parametrize("F,K,M", [(14336, 4096, 5), (256, 4096, 70)])
+def test_swiglu_tile_interleave(bi, orc, F, K, M):
+    """The 8B gate/up shape (192-column tiles: 96 features per tile and a
+    last tile of 32) and a shape with 8 K slices (partials reduced by the
+    second-stage kernel): bi_pack_gate_up's interleave and the SwiGLU
+    epilogue agree with the de-interleaved F32 GEMM to one bf16 ulp (the
+    last bit of expf)."""
+    x = randn_bf16((M, K), 61)
+    wg = randn_bf16((F, K), 62, 0.02)
+    wu = randn_bf16((F, K), 63, 0.02)
+    wgu = torch.empty(2 * F, K, dtype=torch.bfloat16, device="cuda")
+    bi.bi_pack_gate_up(wg, wu, wgu)
+    sw = gemm(bi, x, wgu, bi.OUT_SWIGLU)
+    ref = _swiglu_via_f32(bi, orc, x, wgu, F)
+    diff = np.abs(bits(sw).astype(np.int32) - ref)
+    assert diff.max() <= 1
     assert (diff == 0).mean() > 0.99
