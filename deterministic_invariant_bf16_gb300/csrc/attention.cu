@@ -100,30 +100,48 @@ __device__ __forceinline__ void compute_sync() {
 // phases so that loads can overlap phase 1.
 //
 // Phase 1 (Q and K tiles visible): scores s = (q . k) * scale with
-// mma.sync m16n8k16 (warp w takes keys [w*KPW, (w+1)*KPW), dims in ascending
-// 16-steps), masked past len0 (row rg = lane/4) and len1 (row rg + 8), the
+// mma.sync m16n8k16 (warp w takes keys [w*KPW, (w+1)*KPW)); the dims are
+// summed as two independent chains, the low and the high half of the dims
+// each in ascending 16-steps, added low + high (two chains halve the
+// dependent MMA latency), masked past len0 (row rg = lane/4) and len1 (row
+// rg + 8), the
 // row maximum m, p = exp(s - m), the bf16 P tile and the per-warp partial row
 // sums (each thread adds its values in key order, then a quad xor-tree over
 // lanes 1, 2).  Returns m for rows rg and rg + 8.  Ends after writing shared
 // memory; the caller must synchronise the compute threads before phase 2.
+// low8: only tile rows 0-7 are used (decode with G <= 8); rows 8-15 of Q
+// are then not loaded (their MMA rows come out as don't-care values, the
+// tensor core keeps rows independent) and their p is neither computed nor
+// stored, which halves the shared-memory reads of Q and P.
 template <int D, int BAR>
 __device__ __forceinline__ void chunk_phase1(uint32_t ktile, uint32_t qtile,
                                              uint32_t ptile, float *red,
                                              float scale, int len0, int len1,
-                                             float m[2]) {
+                                             float m[2], bool low8) {
     constexpr int NW = nwarps<D>();
     constexpr int KPW = CHUNK / NW;   // keys per warp
     constexpr int NT = KPW / 8;       // score n-tiles per warp
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rg = lane >> 2, tq = lane & 3;
 
-    float sc[NT][4];
+    constexpr int KS = D / 16;        // 16-dim steps
+    static_assert(KS % 2 == 0, "two chains over the dims");
+    float sc[NT][4], sh[NT][4];       // low-half and high-half chains
 #pragma unroll
-    for (int i = 0; i < NT; ++i) sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
+    for (int i = 0; i < NT; ++i)
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-        uint32_t a0, a1, a2, a3;
-        {
+        for (int e = 0; e < 4; ++e) sc[i][e] = sh[i][e] = 0.f;
+#pragma unroll
+    for (int step = 0; step < KS; ++step) {
+        // interleave the chains: low step j, then high step j
+        const int ks = (step >> 1) + (step & 1) * (KS / 2);
+        float(*acc)[4] = (step & 1) ? sh : sc;
+        uint32_t a0, a1 = 0, a2, a3 = 0;
+        if (low8) {
+            const int r = lane & 7;
+            const int ch = 2 * ks + ((lane >> 3) & 1);
+            ldsm_x2(qtile + toff<D, 16>(r, ch), a0, a2);
+        } else {
             const int r = (lane & 7) + 8 * ((lane >> 3) & 1);
             const int ch = 2 * ks + (lane >> 4);
             ldsm_x4(qtile + toff<D, 16>(r, ch), a0, a1, a2, a3);
@@ -134,10 +152,14 @@ __device__ __forceinline__ void chunk_phase1(uint32_t ktile, uint32_t qtile,
             const int ch = 2 * ks + ((lane >> 3) & 1);
             uint32_t b0, b1, b2, b3;
             ldsm_x4(ktile + toff<D, CHUNK>(key, ch), b0, b1, b2, b3);
-            mma_16816(sc[2 * np], a0, a1, a2, a3, b0, b1);
-            mma_16816(sc[2 * np + 1], a0, a1, a2, a3, b2, b3);
+            mma_16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
+            mma_16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
         }
     }
+#pragma unroll
+    for (int i = 0; i < NT; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[i][e] = __fadd_rn(sc[i][e], sh[i][e]);
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -163,12 +185,18 @@ __device__ __forceinline__ void chunk_phase1(uint32_t ktile, uint32_t qtile,
         red[warp * 16 + rg + 8] = mx1;
     }
     compute_sync<D, BAR>();
-    float m0 = red[rg], m1 = red[8 + rg];
+    // block maxima: lane tq of a quad reads warps tq, tq + 4, ..., then the
+    // quad combines (a maximum does not depend on the order)
+    float m0 = red[tq * 16 + rg], m1 = red[tq * 16 + 8 + rg];
 #pragma unroll
-    for (int w = 1; w < NW; ++w) {
+    for (int w = tq + 4; w < NW; w += 4) {
         m0 = fmaxf(m0, red[w * 16 + rg]);
         m1 = fmaxf(m1, red[w * 16 + 8 + rg]);
     }
+    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
+    m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
+    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
+    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
     const float mu0 = m0 == -INFINITY ? 0.f : m0;
     const float mu1 = m1 == -INFINITY ? 0.f : m1;
 
@@ -178,19 +206,23 @@ __device__ __forceinline__ void chunk_phase1(uint32_t ktile, uint32_t qtile,
         const int key = KPW * warp + 8 * nt + 2 * tq;  // even: a 4-byte pair
         const float p00 = key < len0 ? expf(__fsub_rn(sc[nt][0], mu0)) : 0.f;
         const float p01 = key + 1 < len0 ? expf(__fsub_rn(sc[nt][1], mu0)) : 0.f;
-        const float p10 = key < len1 ? expf(__fsub_rn(sc[nt][2], mu1)) : 0.f;
-        const float p11 = key + 1 < len1 ? expf(__fsub_rn(sc[nt][3], mu1)) : 0.f;
         l0 = __fadd_rn(__fadd_rn(l0, p00), p01);
-        l1 = __fadd_rn(__fadd_rn(l1, p10), p11);
         const int ch = key >> 3, within = (key & 7) * 2;
         asm volatile("st.shared.b32 [%0], %1;" ::"r"(ptile + poff(rg, ch) +
                                                        within),
                      "r"(pack_bf16x2(p00, p01))
                      : "memory");
-        asm volatile("st.shared.b32 [%0], %1;" ::"r"(ptile + poff(rg + 8, ch) +
-                                                       within),
-                     "r"(pack_bf16x2(p10, p11))
-                     : "memory");
+        if (!low8) {
+            const float p10 =
+                key < len1 ? expf(__fsub_rn(sc[nt][2], mu1)) : 0.f;
+            const float p11 =
+                key + 1 < len1 ? expf(__fsub_rn(sc[nt][3], mu1)) : 0.f;
+            l1 = __fadd_rn(__fadd_rn(l1, p10), p11);
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(
+                             ptile + poff(rg + 8, ch) + within),
+                         "r"(pack_bf16x2(p10, p11))
+                         : "memory");
+        }
     }
     l0 = __fadd_rn(l0, __shfl_xor_sync(0xffffffffu, l0, 1));
     l0 = __fadd_rn(l0, __shfl_xor_sync(0xffffffffu, l0, 2));
@@ -207,13 +239,15 @@ __device__ __forceinline__ void chunk_phase1(uint32_t ktile, uint32_t qtile,
 // Phase 2 (after a compute-thread barrier that follows phase 1 and the V
 // copy): the row sums l = (..((w0 + w1) + w2) ..) + w_{NW-1} over the
 // per-warp partials, and o = P V with mma.sync (warp w takes dims
-// [w*DPW, (w+1)*DPW), keys in ascending 16-steps).  Each thread gets
+// [w*DPW, (w+1)*DPW)); the 16 key steps form four independent chains,
+// chain j taking steps j, j + 4, j + 8, j + 12 in that order, and
+// o = (c0 + c1) + (c2 + c3).  Each thread gets
 // o[nt][0..1] for row rg and o[nt][2..3] for row rg + 8, dims
 // w*DPW + 8*nt + 2*(lane%4) + {0,1}.
 template <int D>
 __device__ __forceinline__ void chunk_phase2(uint32_t vtile, uint32_t ptile,
                                              const float *red, float l[2],
-                                             float o[][4]) {
+                                             float o[][4], bool low8) {
     constexpr int NW = nwarps<D>();
     constexpr int DPW = D / NW;       // dims per warp
     constexpr int NTV = DPW / 8;      // PV n-tiles per warp
@@ -227,12 +261,21 @@ __device__ __forceinline__ void chunk_phase2(uint32_t vtile, uint32_t ptile,
     }
     l[0] = la;
     l[1] = lb;
+    float oc[4][NTV][4];
 #pragma unroll
-    for (int nt = 0; nt < NTV; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-#pragma unroll 4
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int nt = 0; nt < NTV; ++nt)
+            oc[j][nt][0] = oc[j][nt][1] = oc[j][nt][2] = oc[j][nt][3] = 0.f;
+#pragma unroll
     for (int kk = 0; kk < CHUNK / 16; ++kk) {
-        uint32_t a0, a1, a2, a3;
-        {
+        float(*acc)[4] = oc[kk & 3];
+        uint32_t a0, a1 = 0, a2, a3 = 0;
+        if (low8) {  // P rows 8-15 unused (see chunk_phase1)
+            const int r = lane & 7;
+            const int ch = 2 * kk + ((lane >> 3) & 1);
+            ldsm_x2(ptile + poff(r, ch), a0, a2);
+        } else {
             const int r = (lane & 7) + 8 * ((lane >> 3) & 1);
             const int ch = 2 * kk + (lane >> 4);
             ldsm_x4(ptile + poff(r, ch), a0, a1, a2, a3);
@@ -245,16 +288,22 @@ __device__ __forceinline__ void chunk_phase2(uint32_t vtile, uint32_t ptile,
                 uint32_t b0, b1, b2, b3;
                 ldsm_x4_t(vtile + toff<D, CHUNK>(key, dim >> 3), b0, b1, b2,
                           b3);
-                mma_16816(o[2 * np], a0, a1, a2, a3, b0, b1);
-                mma_16816(o[2 * np + 1], a0, a1, a2, a3, b2, b3);
+                mma_16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
+                mma_16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
             }
         } else {
             const int dim = warp * DPW;
             uint32_t b0, b1;
             ldsm_x2_t(vtile + toff<D, CHUNK>(key, dim >> 3), b0, b1);
-            mma_16816(o[0], a0, a1, a2, a3, b0, b1);
+            mma_16816(acc[0], a0, a1, a2, a3, b0, b1);
         }
     }
+#pragma unroll
+    for (int nt = 0; nt < NTV; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            o[nt][e] = __fadd_rn(__fadd_rn(oc[0][nt][e], oc[1][nt][e]),
+                                 __fadd_rn(oc[2][nt][e], oc[3][nt][e]));
 }
 
 // One step of the fixed-order chunk merge.
@@ -531,15 +580,15 @@ __global__ void __launch_bounds__(cthreads<D>() + 64, 1)
         if (!mbar_wait(&full[sk], ((2 * n) / RING) & 1, status)) break;
         float m[2], l[2], o[DPW / 8][4];
         chunk_phase1<D, 1>(base + L::SLOT + sk * TB, base + L::QSLOT + sk * QB,
-                           ptile, red, scale, len0, len1, m);
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                           ptile, red, scale, len0, len1, m, G <= 8);
+        // the K slot was only read: the barrier alone orders the next copy
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[sk]);
         if (!mbar_wait(&full[sv], ((2 * n + 1) / RING) & 1, status)) break;
         const uint32_t vtile = base + L::SLOT + sv * TB;
         if (vl < CHUNK) zero_rows<D>(vtile, vl);
         compute_sync<D, 1>();
-        chunk_phase2<D>(vtile, ptile, red, l, o);
+        chunk_phase2<D>(vtile, ptile, red, l, o, G <= 8);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             const int r = rg + 8 * half;
@@ -557,7 +606,9 @@ __global__ void __launch_bounds__(cthreads<D>() + 64, 1)
                     make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
             }
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        // rows zeroed by these threads must be ordered before the next copy
+        // into the slot (a different proxy); a slot only read needs no fence
+        if (vl < CHUNK) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[sv]);
     }
@@ -746,10 +797,11 @@ __global__ void __launch_bounds__(cthreads<D>())
         cp_async_wait<1>();
         __syncthreads();
         float m[2], l[2], o[DPW / 8][4];
-        chunk_phase1<D, 0>(ktile, qtile, ptile, red, scale, len0, len1, m);
+        chunk_phase1<D, 0>(ktile, qtile, ptile, red, scale, len0, len1, m,
+                           false);
         cp_async_wait<0>();
         __syncthreads();
-        chunk_phase2<D>(vtile, ptile, red, l, o);
+        chunk_phase2<D>(vtile, ptile, red, l, o, false);
         const int pr[2] = {p_r0, p_r1};
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
