@@ -167,19 +167,23 @@ __device__ __forceinline__ void chunk_phase1(uint32_t ktile, uint32_t qtile,
         for (int e = 0; e < 2; ++e) {
             const int key = KPW * warp + 8 * nt + 2 * tq + e;
             float s0 = __fmul_rn(sc[nt][e], scale);
-            float s1 = __fmul_rn(sc[nt][2 + e], scale);
             s0 = key < len0 ? s0 : -INFINITY;
-            s1 = key < len1 ? s1 : -INFINITY;
             sc[nt][e] = s0;
-            sc[nt][2 + e] = s1;
             mx0 = fmaxf(mx0, s0);
-            mx1 = fmaxf(mx1, s1);
+            if (!low8) {
+                float s1 = __fmul_rn(sc[nt][2 + e], scale);
+                s1 = key < len1 ? s1 : -INFINITY;
+                sc[nt][2 + e] = s1;
+                mx1 = fmaxf(mx1, s1);
+            }
         }
     }
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    if (!low8) {
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    }
     if (tq == 0) {
         red[warp * 16 + rg] = mx0;
         red[warp * 16 + rg + 8] = mx1;
@@ -187,16 +191,19 @@ __device__ __forceinline__ void chunk_phase1(uint32_t ktile, uint32_t qtile,
     compute_sync<D, BAR>();
     // block maxima: lane tq of a quad reads warps tq, tq + 4, ..., then the
     // quad combines (a maximum does not depend on the order)
-    float m0 = red[tq * 16 + rg], m1 = red[tq * 16 + 8 + rg];
+    float m0 = red[tq * 16 + rg], m1 = -INFINITY;
 #pragma unroll
-    for (int w = tq + 4; w < NW; w += 4) {
-        m0 = fmaxf(m0, red[w * 16 + rg]);
-        m1 = fmaxf(m1, red[w * 16 + 8 + rg]);
-    }
+    for (int w = tq + 4; w < NW; w += 4) m0 = fmaxf(m0, red[w * 16 + rg]);
     m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 1));
     m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, 2));
-    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
-    m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
+    if (!low8) {
+        m1 = red[tq * 16 + 8 + rg];
+#pragma unroll
+        for (int w = tq + 4; w < NW; w += 4)
+            m1 = fmaxf(m1, red[w * 16 + 8 + rg]);
+        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 1));
+        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 2));
+    }
     const float mu0 = m0 == -INFINITY ? 0.f : m0;
     const float mu1 = m1 == -INFINITY ? 0.f : m1;
 
@@ -244,23 +251,32 @@ __device__ __forceinline__ void chunk_phase1(uint32_t ktile, uint32_t qtile,
 // o = (c0 + c1) + (c2 + c3).  Each thread gets
 // o[nt][0..1] for row rg and o[nt][2..3] for row rg + 8, dims
 // w*DPW + 8*nt + 2*(lane%4) + {0,1}.
+// need_l: this thread uses l (else l is left 0 and the sums are skipped).
 template <int D>
 __device__ __forceinline__ void chunk_phase2(uint32_t vtile, uint32_t ptile,
                                              const float *red, float l[2],
-                                             float o[][4], bool low8) {
+                                             float o[][4], bool low8,
+                                             bool need_l) {
     constexpr int NW = nwarps<D>();
     constexpr int DPW = D / NW;       // dims per warp
     constexpr int NTV = DPW / 8;      // PV n-tiles per warp
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rg = lane >> 2;
-    float la = red[NW * 16 + rg], lb = red[NW * 16 + 8 + rg];
+    l[0] = l[1] = 0.f;
+    if (need_l) {
+        float la = red[NW * 16 + rg];
 #pragma unroll
-    for (int w = 1; w < NW; ++w) {
-        la = __fadd_rn(la, red[NW * 16 + w * 16 + rg]);
-        lb = __fadd_rn(lb, red[NW * 16 + w * 16 + 8 + rg]);
+        for (int w = 1; w < NW; ++w)
+            la = __fadd_rn(la, red[NW * 16 + w * 16 + rg]);
+        l[0] = la;
+        if (!low8) {
+            float lb = red[NW * 16 + 8 + rg];
+#pragma unroll
+            for (int w = 1; w < NW; ++w)
+                lb = __fadd_rn(lb, red[NW * 16 + w * 16 + 8 + rg]);
+            l[1] = lb;
+        }
     }
-    l[0] = la;
-    l[1] = lb;
     float oc[4][NTV][4];
 #pragma unroll
     for (int j = 0; j < 4; ++j)
@@ -568,13 +584,25 @@ __global__ void __launch_bounds__(cthreads<D>() + 64, 1)
 
     // ------------------------------------------------------- compute --
     const int rg = lane >> 2, tq = lane & 3;
+    // (row, chunk, visible length) of the next item, loaded one item ahead
+    int nb = 0, nc = 0, nvl = 0;
+    if (blockIdx.x < total) {
+        const int2 bc = items[blockIdx.x / Hkv];
+        nb = bc.x;
+        nc = bc.y;
+        nvl = min(CHUNK, kv_len[nb] - nc * CHUNK);
+    }
     for (int n = 0;; ++n) {
         const int i = blockIdx.x + n * gridDim.x;
         if (i >= total) break;
         const int g = i % Hkv;
-        const int2 bc = items[i / Hkv];
-        const int b = bc.x, c = bc.y;
-        const int vl = min(CHUNK, kv_len[b] - c * CHUNK);
+        const int b = nb, c = nc, vl = nvl;
+        if (i + (int)gridDim.x < total) {
+            const int2 bc = items[(i + gridDim.x) / Hkv];
+            nb = bc.x;
+            nc = bc.y;
+            nvl = min(CHUNK, kv_len[nb] - nc * CHUNK);
+        }
         const int len0 = rg < G ? vl : 0, len1 = rg + 8 < G ? vl : 0;
         const int sk = (2 * n) % RING, sv = (2 * n + 1) % RING;
         if (!mbar_wait(&full[sk], ((2 * n) / RING) & 1, status)) break;
@@ -588,7 +616,8 @@ __global__ void __launch_bounds__(cthreads<D>() + 64, 1)
         const uint32_t vtile = base + L::SLOT + sv * TB;
         if (vl < CHUNK) zero_rows<D>(vtile, vl);
         compute_sync<D, 1>();
-        chunk_phase2<D>(vtile, ptile, red, l, o, G <= 8);
+        // only warp 0 stores (m, l)
+        chunk_phase2<D>(vtile, ptile, red, l, o, G <= 8, warp == 0);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             const int r = rg + 8 * half;
@@ -801,7 +830,7 @@ __global__ void __launch_bounds__(cthreads<D>())
                            false);
         cp_async_wait<0>();
         __syncthreads();
-        chunk_phase2<D>(vtile, ptile, red, l, o, false);
+        chunk_phase2<D>(vtile, ptile, red, l, o, false, true);
         const int pr[2] = {p_r0, p_r1};
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
