@@ -42,24 +42,54 @@ __global__ void rope_table_kernel(const int32_t *__restrict__ pos, int T,
     }
 }
 
-// Slices summed in slice order and rounded to bf16.  S is a template
-// argument so that all S loads are in flight before the adds.
-template <int S>
-__device__ __forceinline__ float qkv_value(const float *__restrict__ qkv,
-                                           int64_t TQ, int64_t off) {
-    float p[S];
+// Slices summed in slice order and rounded to bf16, for PAIRS consecutive
+// elements (one float4 per slice when PAIRS = 4).  S is a template argument
+// so that all S loads are in flight before the adds.
+template <int S, int PAIRS>
+__device__ __forceinline__ void qkv_values(const float *__restrict__ qkv,
+                                           int64_t TQ, int64_t off,
+                                           float *out) {
+    float p[S][PAIRS];
 #pragma unroll
-    for (int s = 0; s < S; ++s) p[s] = __ldcs(qkv + s * TQ + off);
-    float v = p[0];
+    for (int s = 0; s < S; ++s) {
+        if constexpr (PAIRS == 4) {
+            const float4 v = __ldcs(reinterpret_cast<const float4 *>(
+                qkv + s * TQ + off));
+            p[s][0] = v.x;
+            p[s][1] = v.y;
+            p[s][2] = v.z;
+            p[s][3] = v.w;
+        } else {
+            p[s][0] = __ldcs(qkv + s * TQ + off);
+        }
+    }
 #pragma unroll
-    for (int s = 1; s < S; ++s) v = __fadd_rn(v, p[s]);
-    return bf16_to_f32(f32_to_bf16(v));
+    for (int k = 0; k < PAIRS; ++k) {
+        float v = p[0][k];
+#pragma unroll
+        for (int s = 1; s < S; ++s) v = __fadd_rn(v, p[s][k]);
+        out[k] = bf16_to_f32(f32_to_bf16(v));
+    }
+}
+
+// PAIRS bf16 values to 2 * PAIRS bytes of memory (one 8-byte store for 4).
+template <int PAIRS>
+__device__ __forceinline__ void store_bf16(uint16_t *dst, const float *v,
+                                           bool zero) {
+    if constexpr (PAIRS == 4) {
+        *reinterpret_cast<uint2 *>(dst) =
+            zero ? make_uint2(0, 0)
+                 : make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+    } else {
+        dst[0] = zero ? 0 : f32_to_bf16(v[0]);
+    }
 }
 
 // Block (t, y) handles row t, heads [y * HPB, (y + 1) * HPB) with
-// HPB = 256 / (D/2); thread -> (head, pair i).  Heads are q heads, then k
-// heads (rotated and appended), then v heads (appended as rounded).
-template <int S>
+// HPB = 256 / (D / (2 PAIRS)); thread -> (head, pairs i .. i + PAIRS - 1).
+// Heads are q heads, then k heads (rotated and appended), then v heads
+// (appended as rounded).
+template <int S, int PAIRS>
 __global__ void __launch_bounds__(ROPE_THREADS)
     rope_kernel(const float *__restrict__ qkv, const float2 *__restrict__ table,
                 const int32_t *__restrict__ pos,
@@ -71,14 +101,15 @@ __global__ void __launch_bounds__(ROPE_THREADS)
     __shared__ float2 cs_s[64];
     const int t = blockIdx.x;
     const int half = D / 2;
-    const int hpb = ROPE_THREADS / half;
+    const int tph = half / PAIRS;  // threads per head
+    const int hpb = ROPE_THREADS / tph;
     const int QKV = (Hq + 2 * Hkv) * D;
     const int64_t TQ = (int64_t)T * QKV;
     const int64_t rowoff = (int64_t)t * QKV;
     const int p = pos[t];
     const int req = row_req[t];
-    const int i = threadIdx.x % half;
-    const int head = blockIdx.y * hpb + threadIdx.x / half;
+    const int i = (threadIdx.x % tph) * PAIRS;
+    const int head = blockIdx.y * hpb + threadIdx.x / tph;
 
     if (!table) {
         if (threadIdx.x < half) cs_s[threadIdx.x] = rope_cs(p, threadIdx.x, D, theta);
@@ -101,29 +132,35 @@ __global__ void __launch_bounds__(ROPE_THREADS)
     }
     const int slot = p & 15;
     const int64_t c0 = rowoff + (int64_t)head * D + i;
-    const float x0 = qkv_value<S>(qkv, TQ, c0);
-    const float x1 = qkv_value<S>(qkv, TQ, c0 + half);
+    float x0[PAIRS], x1[PAIRS];
+    qkv_values<S, PAIRS>(qkv, TQ, c0, x0);
+    qkv_values<S, PAIRS>(qkv, TQ, c0 + half, x1);
     if (head < Hq + Hkv) {
-        const float2 cs = table ? table[(int64_t)t * half + i] : cs_s[i];
-        const float c = cs.x, s = cs.y;
-        const float y0 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, s));
-        const float y1 = __fadd_rn(__fmul_rn(x1, c), __fmul_rn(x0, s));
+        float y0[PAIRS], y1[PAIRS];
+#pragma unroll
+        for (int k = 0; k < PAIRS; ++k) {
+            const float2 cs = table ? table[(int64_t)t * half + i + k]
+                                    : cs_s[i + k];
+            const float c = cs.x, s = cs.y;
+            y0[k] = __fsub_rn(__fmul_rn(x0[k], c), __fmul_rn(x1[k], s));
+            y1[k] = __fadd_rn(__fmul_rn(x1[k], c), __fmul_rn(x0[k], s));
+        }
         if (head < Hq) {
             uint16_t *qd = q_out + ((int64_t)t * Hq + head) * D;
-            const bool live = req >= 0;
-            qd[i] = live ? f32_to_bf16(y0) : 0;
-            qd[i + half] = live ? f32_to_bf16(y1) : 0;
+            const bool pad = req < 0;
+            store_bf16<PAIRS>(qd + i, y0, pad);
+            store_bf16<PAIRS>(qd + i + half, y1, pad);
         } else if (page >= 0) {
             uint16_t *kd = k_pool +
                            ((page * Hkv + (head - Hq)) * 16 + slot) * (int64_t)D;
-            kd[i] = f32_to_bf16(y0);
-            kd[i + half] = f32_to_bf16(y1);
+            store_bf16<PAIRS>(kd + i, y0, false);
+            store_bf16<PAIRS>(kd + i + half, y1, false);
         }
     } else if (page >= 0) {
         uint16_t *vd = v_pool +
                        ((page * Hkv + (head - Hq - Hkv)) * 16 + slot) * (int64_t)D;
-        vd[i] = f32_to_bf16(x0);
-        vd[i + half] = f32_to_bf16(x1);
+        store_bf16<PAIRS>(vd + i, x0, false);
+        store_bf16<PAIRS>(vd + i + half, x1, false);
     }
 }
 
@@ -154,15 +191,26 @@ bi_status bi_rope_apply(const float *qkv, int S, const float2 *table,
     BI_REQUIRE(qkv && pos && row_req && q_out && k_pool && v_pool && page_table,
                "bi_rope: null pointer");
     BI_REQUIRE(max_pages > 0 && n_pages > 0, "bi_rope: empty page table/pool");
+    BI_REQUIRE(bi_aligned16(qkv) && bi_aligned16(q_out) &&
+                   bi_aligned16(k_pool) && bi_aligned16(v_pool),
+               "bi_rope: pointers must be 16-byte aligned");
     int32_t *status = bi_status_ptr();
-    const int hpb = ROPE_THREADS / (D / 2);
+    // four pairs per thread (16-byte loads) when D / 2 is a multiple of 4
+    const bool vec = (D / 2) % 4 == 0;
+    const int tph = vec ? D / 8 : D / 2;
+    const int hpb = ROPE_THREADS / tph;
     dim3 grid(T, (Hq + 2 * Hkv + hpb - 1) / hpb);
     switch (S) {
 #define BI_ROPE_CASE(n)                                                       \
     case n:                                                                   \
-        rope_kernel<n><<<grid, ROPE_THREADS, 0, st>>>(                        \
-            qkv, table, pos, row_req, T, Hq, Hkv, D, theta, q_out, k_pool,    \
-            v_pool, page_table, max_pages, n_pages, status);                  \
+        if (vec)                                                              \
+            rope_kernel<n, 4><<<grid, ROPE_THREADS, 0, st>>>(                 \
+                qkv, table, pos, row_req, T, Hq, Hkv, D, theta, q_out,        \
+                k_pool, v_pool, page_table, max_pages, n_pages, status);      \
+        else                                                                  \
+            rope_kernel<n, 1><<<grid, ROPE_THREADS, 0, st>>>(                 \
+                qkv, table, pos, row_req, T, Hq, Hkv, D, theta, q_out,        \
+                k_pool, v_pool, page_table, max_pages, n_pages, status);      \
         break;
         BI_ROPE_CASE(1) BI_ROPE_CASE(2) BI_ROPE_CASE(3) BI_ROPE_CASE(4)
         BI_ROPE_CASE(5) BI_ROPE_CASE(6) BI_ROPE_CASE(7) BI_ROPE_CASE(8)
