@@ -56,6 +56,9 @@ def parse():
     ap.add_argument("--no-comparator", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the decode iterations one call at a time "
+                         "instead of replaying them as one CUDA graph")
     return ap.parse_args()
 
 
@@ -279,8 +282,28 @@ class Bench:
         for r in self.v_slots:  # pages for the next step's positions
             self.eng.reserve(r, int(wl["ctx"][r]) + wl["headroom"])
 
-    def step(self):
-        self.decode_iters()
+    def capture(self):
+        """Capture one step's decode iterations (the library's calls, same
+        buffers and arguments) as a CUDA graph; the verify part syncs with
+        the host and stays eager."""
+        torch = self.torch
+        torch.cuda.synchronize()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            self.decode_iters()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.decode_iters()
+        torch.cuda.synchronize()
+
+    def step(self, graph=False):
+        if graph and getattr(self, "graph", None) is not None:
+            self.graph.replay()
+        else:
+            self.decode_iters()
         self.verify()
 
 
@@ -366,6 +389,11 @@ def run_ours(args):
     for _ in range(args.warmup):
         b.step()
     torch.cuda.synchronize()
+    use_graph = not args.no_graph
+    if use_graph:
+        b.capture()
+        b.step(graph=True)
+        torch.cuda.synchronize()
     # ---- device-resident timed region (inputs are in HBM: weights 16 GB,
     # KV ~20 GB, far beyond the 129 MB L2, so no flush is needed)
     barrier()
@@ -377,7 +405,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     e0.record(stream)
     for _ in range(args.steps):
-        b.step()
+        b.step(graph=use_graph)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -490,7 +518,9 @@ def run_ours(args):
                    "deterministic_fraction": b.wl["n_flag"] / B,
                    "mean_context": float(b.wl["ctx"].mean()),
                    "l2": "inputs larger than L2 (weights + KV >> 129 MB)",
-                   "parallelism": "replicas" if world > 1 else "single"},
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "decode_launch": "cuda_graph" if use_graph else "eager",
+                   "e2e_launch": "eager"},
         "e2e": e2e,
         "gpu_launches": int(round(launches * args.steps)),
         "roofline": roof,
