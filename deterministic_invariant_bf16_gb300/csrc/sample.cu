@@ -186,15 +186,25 @@ __global__ void __launch_bounds__(SEL_THREADS)
         part = __fadd_rn(part, expf(__fdiv_rn(__fsub_rn(row[k], mx), tau)));
     float total;
     const float prefix = block_exclusive_scan(part, &total);
-    // 3. first index whose running sum exceeds u * total
+    // 3. first index whose running sum exceeds u * total.  A slice whose
+    // running sum cannot pass the target is skipped: for its n terms and
+    // u = 2^-24 the slice's last running sum is at most
+    // (prefix + sum p) (1 + u)^n (each rounded add of non-negative terms
+    // grows by at most 1 + u) and sum p <= part / (1 - u)^(n - 1); both
+    // factors are below f = 1 + 2 (n + 1) u while n u < 1/2, so with the
+    // bound in double the skip never changes the result of the full scan.
     const float target = __fmul_rn(sample_uniform(request_id[t], step[t]), total);
     int first = 0x7fffffff;
-    float cdf = prefix;
-    for (int k = lo; k < hi; ++k) {
-        cdf = __fadd_rn(cdf, expf(__fdiv_rn(__fsub_rn(row[k], mx), tau)));
-        if (cdf > target) {
-            first = k;
-            break;
+    const double f = 1.0 + 2.0 * (double)(hi - lo + 1) * 0x1p-24;
+    const double bound = ((double)prefix + (double)part * f) * f;
+    if (bound > (double)target) {
+        float cdf = prefix;
+        for (int k = lo; k < hi; ++k) {
+            cdf = __fadd_rn(cdf, expf(__fdiv_rn(__fsub_rn(row[k], mx), tau)));
+            if (cdf > target) {
+                first = k;
+                break;
+            }
         }
     }
     // Integer min/max over the block: order-free, so deterministic.
@@ -205,8 +215,13 @@ __global__ void __launch_bounds__(SEL_THREADS)
     }
     __syncthreads();
     if (first != 0x7fffffff) atomicMin(&s_first, first);
-    // Last index with p > 0, for a row whose running sum never passes the
-    // target because of rounding.
+    __syncthreads();
+    if (s_first != 0x7fffffff) {
+        if (threadIdx.x == 0) ids[t] = s_first;
+        return;
+    }
+    // No running sum passed the target (rounding): the last index with
+    // p > 0.
     int lp = -1;
     for (int k = hi - 1; k >= lo; --k)
         if (expf(__fdiv_rn(__fsub_rn(row[k], mx), tau)) > 0.f) {
@@ -215,8 +230,7 @@ __global__ void __launch_bounds__(SEL_THREADS)
         }
     if (lp >= 0) atomicMax(&s_last, lp);
     __syncthreads();
-    if (threadIdx.x == 0)
-        ids[t] = s_first != 0x7fffffff ? s_first : max(s_last, 0);
+    if (threadIdx.x == 0) ids[t] = max(s_last, 0);
 }
 
 }  // namespace
