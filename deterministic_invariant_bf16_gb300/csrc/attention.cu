@@ -707,10 +707,10 @@ __device__ __forceinline__ void load_tile(uint32_t tile,
                                           const int32_t *__restrict__ pt_row,
                                           int max_pages, int n_pages, int Hkv,
                                           int g, int c, int valid_max,
-                                          int32_t *status) {
+                                          int32_t *status, int nthreads) {
     constexpr int NCH = D / 8;
 #pragma unroll 4
-    for (int idx = threadIdx.x; idx < CHUNK * NCH; idx += cthreads<D>()) {
+    for (int idx = threadIdx.x; idx < CHUNK * NCH; idx += nthreads) {
         const int key = idx / NCH, ch = idx % NCH;
         const int p = c * CHUNK + key;
         const uint16_t *src = pool;
@@ -816,10 +816,10 @@ __global__ void __launch_bounds__(cthreads<D>())
     for (int c = 0; c < C; ++c) {
         __syncthreads();  // previous chunk fully consumed
         load_tile<D>(ktile, kp, pt_row, max_pages, n_pages, Hkv, g, c, vmax,
-                     status);
+                     status, NT);
         cp_async_commit();
         load_tile<D>(vtile, vp, pt_row, max_pages, n_pages, Hkv, g, c, vmax,
-                     status);
+                     status, NT);
         cp_async_commit();
         const int len0 = max(0, min(CHUNK, p_r0 + 1 - c * CHUNK));
         const int len1 = max(0, min(CHUNK, p_r1 + 1 - c * CHUNK));
@@ -873,6 +873,662 @@ __global__ void __launch_bounds__(cthreads<D>())
     }
 }
 
+// ------------------------------------------- tensor-core chunk (head_dim 128) --
+//
+// For head_dim 128 the chunk partial runs on the tcgen05 tensor cores; decode
+// and prefill both use the functions below, so their bits agree.  Per
+// 16-row query tile and 256-key chunk:
+//   S^T[key][row] = sum_d K[key][d] Q[row][d]: two MMA chains (keys 0-127
+//     and 128-255; M = 128 keys, N = 16 rows), each over the dims in
+//     ascending 16-steps, fp32 in tensor memory;
+//   s = S^T * scale, -inf past the row's visible length; m = block maximum;
+//   p = exp(s - m) (0 when masked); l = per-warp xor-tree sums over 32 keys
+//   (16, 8, 4, 2, 1), then (((w0 + w1) + w2) .. + w7) over the 8 warps;
+//   O^T[dim][row] = sum_key V[key][dim] bf16(p)[row][key]: one MMA chain
+//   (M = 128 dims, N = 16 rows) over the keys in ascending 16-steps, with V
+//   read in place as an MN-major operand.
+// V rows past a chunk's visible part are zero when the PV MMAs read them
+// (0 * NaN would poison the sum); K rows there are never used (masked).
+namespace tca {
+
+constexpr int SW = 8;                         // softmax warps, thread = key
+constexpr int STHREADS = SW * 32;
+constexpr uint32_t IDESC_QK = make_idesc_bf16(128, 16);
+constexpr uint32_t IDESC_PV = make_idesc_bf16(128, 16) | (1u << 15);
+constexpr int P_TILE = 16 * CHUNK * 2;        // bf16 [16][256], 8 KB
+constexpr int RED_FLOATS = 2 * SW * 16;       // maxima then sums, [8][16] each
+
+// P tile, the B operand of the PV MMAs (K-major, 128-byte swizzle): keys in
+// groups of 64 (2 KB each), row r at r * 128 B, 16-byte unit j at j ^ (r % 8).
+__device__ __forceinline__ uint32_t poff(int row, int key) {
+    return (uint32_t)((key >> 6) * 2048 + row * 128 +
+                      ((((key & 63) >> 3) ^ (row & 7)) << 4) + (key & 7) * 2);
+}
+
+// S^T into TMEM columns d .. d + 31 (keys 0-127 in d .. d + 15, keys
+// 128-255 in d + 16 .. d + 31; lane = key % 128).  K tile: the 2-half
+// [256][128 B] layout the TMA writes; Q tile: 2 halves of [16][128 B].
+__device__ __forceinline__ void issue_qk(uint32_t d, uint32_t ktile,
+                                         uint32_t qtile) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t a = ktile + (kk >> 2) * (CHUNK * 128) +
+                               h * (128 * 128) + (kk & 3) * 32;
+            const uint32_t b = qtile + (kk >> 2) * (16 * 128) + (kk & 3) * 32;
+            tc_mma_bf16(d + h * 16, make_sw128_desc(a), make_sw128_desc(b),
+                        IDESC_QK, kk > 0 ? 1u : 0u);
+        }
+}
+
+// O^T into TMEM columns d .. d + 15 (lane = dim).  The V tile's two 64-dim
+// halves are the MN atoms (32 KB apart), 8-key row groups the K atoms.
+__device__ __forceinline__ void issue_pv(uint32_t d, uint32_t vtile,
+                                         uint32_t ptile) {
+#pragma unroll
+    for (int kk = 0; kk < CHUNK / 16; ++kk) {
+        const uint32_t a = vtile + kk * 2048;
+        const uint32_t b = ptile + (kk >> 2) * 2048 + (kk & 3) * 32;
+        tc_mma_bf16(d, make_sw128_desc_mn(a, CHUNK * 128, 1024),
+                    make_sw128_desc(b), IDESC_PV, kk > 0 ? 1u : 0u);
+    }
+}
+
+__device__ __forceinline__ void sync_softmax() {
+    asm volatile("bar.sync 1, %0;" ::"n"(STHREADS) : "memory");
+}
+
+// Softmax of one chunk by the 256 softmax threads (thread t <-> key t), for
+// rows 0 .. nr-1 of the tile: reads S^T at s_tmem, applies scale and the
+// per-row visible lengths, writes m[r] (every thread), the warp sums to
+// red + 128 and bf16(p) to the P tile.  Rows >= nr are not touched.
+__device__ __forceinline__ void softmax(uint32_t s_tmem, float scale,
+                                        const int (&len)[16], int nr,
+                                        uint32_t ptile, float *red,
+                                        float (&m)[16]) {
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int key = (w >> 2) * 128 + (w & 3) * 32 + lane;
+    float v[16];
+    tmem_ld_16cols(s_tmem + ((uint32_t)((w & 3) * 32) << 16) + (w >> 2) * 16,
+                   v);
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        if (r >= nr) break;
+        float s = __fmul_rn(v[r], scale);
+        s = key < len[r] ? s : -INFINITY;
+        v[r] = s;
+        float mx = s;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1)
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) red[w * 16 + r] = mx;
+    }
+    sync_softmax();
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+        if (r >= nr) break;
+        float mm = red[r];
+#pragma unroll
+        for (int x = 1; x < SW; ++x) mm = fmaxf(mm, red[x * 16 + r]);
+        m[r] = mm;
+        const float mu = mm == -INFINITY ? 0.f : mm;
+        const float p = key < len[r] ? expf(__fsub_rn(v[r], mu)) : 0.f;
+        float l = p;
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1)
+            l = __fadd_rn(l, __shfl_xor_sync(0xffffffffu, l, o));
+        if (lane == 0) red[SW * 16 + w * 16 + r] = l;
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(ptile + poff(r, key)),
+                     "h"(f32_to_bf16(p))
+                     : "memory");
+    }
+}
+
+// Block row sum of row r from the warp sums (fixed warp order).
+__device__ __forceinline__ float row_sum(const float *red, int r) {
+    float l = red[SW * 16 + r];
+#pragma unroll
+    for (int x = 1; x < SW; ++x) l = __fadd_rn(l, red[SW * 16 + x * 16 + r]);
+    return l;
+}
+
+// Rows [from, to) of both 64-dim halves of a V tile set to zero.
+__device__ __forceinline__ void zero_v_rows(uint8_t *vtile, int from, int to,
+                                            int tid, int nthreads) {
+    for (int idx = tid; idx < (to - from) * 16; idx += nthreads) {
+        const int row = from + (idx >> 4), u = idx & 15;
+        *reinterpret_cast<uint4 *>(vtile + (u >> 3) * (CHUNK * 128) +
+                                   row * 128 + (u & 7) * 16) =
+            make_uint4(0, 0, 0, 0);
+    }
+}
+
+// Decode kernel shared-memory layout (offsets from a 1024-aligned base).
+struct DecL {
+    static constexpr int TB = CHUNK * 128 * 2;          // K or V tile, 64 KB
+    static constexpr int QB = 16 * 128 * 2;             // Q tile, 4 KB
+    static constexpr int SLOT = 0;
+    static constexpr int QSLOT = SLOT + RING * TB;
+    static constexpr int P = QSLOT + RING * QB;          // 2 P tiles
+    static constexpr int RED = P + 2 * P_TILE;           // 2 x [2][8][16] f32
+    static constexpr int BAR = RED + 2 * RED_FLOATS * 4;
+    // full[RING], empty[RING], s_full[2], p_full[2], p_empty[2], o_full[2],
+    // o_empty[2], then the TMEM address
+    static constexpr int BYTES = BAR + (2 * RING + 10) * 8 + 16;
+    static constexpr int ALLOC = BYTES + 1024;
+};
+constexpr int DEC_THREADS = (SW + 3) * 32;  // softmax, MMA, producer, prefetch
+
+}  // namespace tca
+
+// Persistent decode chunk kernel on the tensor cores (head_dim 128).  CTA k
+// takes items k, k + grid, ...; item i is KV head i % Hkv of list entry
+// i / Hkv; item n of a CTA uses ring slots 2n (K, Q) and 2n + 1 (V) mod RING.
+//   warps 0-7   softmax and epilogue (thread t <-> key t of the chunk);
+//   warp 8      owns the tensor memory; lane 0 issues the MMAs: S^T of item
+//               n + 2 is issued as soon as item n's softmax has read S^T
+//               (two S buffers), O^T of item n once its P tile is written
+//               (two P tiles, two O buffers);
+//   warp 9      producer: page ids -> TMA boxes (K only for visible pages,
+//               V for all 16 pages, missing ones as zero-filled boxes);
+//   warp 10     asks L2 for the K/V pages of the next items.
+__global__ void __launch_bounds__(tca::DEC_THREADS, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                     const __grid_constant__ CUtensorMap vmap,
+                     const __grid_constant__ CUtensorMap qmap,
+                     const int32_t *__restrict__ page_table, int max_pages,
+                     int n_pages, const int32_t *__restrict__ row_req,
+                     const int32_t *__restrict__ kv_len, int Hq, int Hkv,
+                     int G, float scale, float *__restrict__ ws, int Cmax,
+                     const int32_t *__restrict__ prefix, int B,
+                     const int2 *__restrict__ items,
+                     const bi_bf16 *__restrict__ k_pool,
+                     const bi_bf16 *__restrict__ v_pool, int32_t *status) {
+    using namespace tca;
+    constexpr int D = 128;
+    constexpr int PAGE_BYTES = 16 * 64 * 2;   // one box: 16 rows x 64 dims
+    constexpr int HALF_TILE = CHUNK * 128;
+    constexpr int HALF_Q = 16 * 128;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ int s_progress;  // items the producer has issued
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t base = smem_u32(smem);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + DecL::BAR);
+    uint64_t *empty = full + RING;
+    uint64_t *s_full = empty + RING;
+    uint64_t *p_full = s_full + 2;
+    uint64_t *p_empty = p_full + 2;
+    uint64_t *o_full = p_empty + 2;
+    uint64_t *o_empty = o_full + 2;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(o_empty + 2);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = prefix[B] * Hkv;
+    int n_items = 0;  // items of this CTA
+    if ((int)blockIdx.x < total)
+        n_items = (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < RING; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], SW);
+            mbar_init(&p_empty[i], 1);
+            mbar_init(&o_full[i], 1);
+            mbar_init(&o_empty[i], 4);
+        }
+        mbar_fence_init();
+        s_progress = 0;
+    }
+    if (warp < SW) {
+        // both P tiles start at zero: rows >= G are never written again
+        for (int i = threadIdx.x; i < 2 * P_TILE / 16; i += STHREADS)
+            reinterpret_cast<uint4 *>(smem + DecL::P)[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+    }
+    if (warp == SW) tmem_alloc(tslot, 128);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    volatile int *progress = &s_progress;
+
+    if (warp == SW + 2) {
+        // ------------------------------------------------------ prefetch --
+        constexpr uint32_t PAGE_KV = 16 * D * 2;
+        for (int n = 0; n < n_items; ++n) {
+            const int i = blockIdx.x + n * gridDim.x;
+            bool go = true;
+            if (lane == 0 && *progress + 2 < n) {
+                const uint64_t t0 = bi_globaltimer();
+                while (*progress + 2 < n) {
+                    __nanosleep(256);
+                    if (bi_globaltimer() - t0 > BI_WAIT_LIMIT_NS) {
+                        go = false;
+                        break;
+                    }
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, go ? 1 : 0, 0)) break;
+            const int g = i % Hkv;
+            const int2 bc = items[i / Hkv];
+            const int vl = min(CHUNK, kv_len[bc.x] - bc.y * CHUNK);
+            if (lane < ((vl + 15) >> 4)) {
+                const int pi = bc.y * 16 + lane;
+                const int pg = pi < max_pages
+                                   ? page_table[(int64_t)row_req[bc.x] *
+                                                    max_pages + pi]
+                                   : -1;
+                if (pg >= 0 && pg < n_pages) {
+                    const int64_t off = ((int64_t)pg * Hkv + g) * 16 * D;
+                    prefetch_l2_bulk(k_pool + off, PAGE_KV);
+                    prefetch_l2_bulk(v_pool + off, PAGE_KV);
+                }
+            }
+        }
+        return;
+    }
+
+    if (warp == SW + 1) {
+        // ------------------------------------------------------ producer --
+        if (lane == 0) {
+            tma_prefetch_desc(&kmap);
+            tma_prefetch_desc(&vmap);
+            tma_prefetch_desc(&qmap);
+        }
+        bool ok = true;
+        for (int n = 0; n < n_items && ok; ++n) {
+            const int i = blockIdx.x + n * gridDim.x;
+            const int g = i % Hkv;
+            const int2 bc = items[i / Hkv];
+            const int b = bc.x, c = bc.y;
+            const int vl = min(CHUNK, kv_len[b] - c * CHUNK);
+            const int npg = (vl + 15) >> 4;
+            const int32_t *pt_row = page_table + (int64_t)row_req[b] * max_pages;
+            int pg = -1;
+            if (lane < npg) {
+                const int pi = c * 16 + lane;
+                pg = pi < max_pages ? pt_row[pi] : -1;
+                if (pg < 0 || pg >= n_pages) {
+                    bi_record_error(status, BI_ERR_BOUNDS);
+                    pg = -1;
+                }
+            }
+            const int nvalid = __popc(__ballot_sync(0xffffffffu, pg >= 0));
+            for (int kv = 0; kv < 2 && ok; ++kv) {
+                const int j = 2 * n + kv;
+                const int slot = j % RING;
+                const int use = j / RING;
+                bool w_ok = true;
+                if (lane == 0 && use > 0)
+                    w_ok = mbar_wait(&empty[slot], (use - 1) & 1, status);
+                ok = __shfl_sync(0xffffffffu, w_ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
+                // K: the visible pages (+ Q).  V: all 16 pages, the ones
+                // without data as boxes wholly above row 0 (zero-filled).
+                if (lane == 0)
+                    mbar_arrive_expect_tx(
+                        &full[slot], kv == 0 ? nvalid * 2 * PAGE_BYTES +
+                                                   2 * HALF_Q
+                                             : 16 * 2 * PAGE_BYTES);
+                __syncwarp();
+                uint8_t *tile = smem + DecL::SLOT + slot * DecL::TB;
+                if (lane < 16 && (kv == 1 || pg >= 0)) {
+                    const int row = pg >= 0 ? (pg * Hkv + g) * 16 : -16;
+                    const CUtensorMap *map = kv == 0 ? &kmap : &vmap;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_2d(tile + h * HALF_TILE + lane * PAGE_BYTES,
+                                    map, h * 64, row, &full[slot]);
+                }
+                if (kv == 0 && lane == 0) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_2d(smem + DecL::QSLOT + slot * DecL::QB +
+                                        h * HALF_Q,
+                                    &qmap, h * 64, b * Hq + g * G,
+                                    &full[slot]);
+                }
+            }
+            if (lane == 0) *progress = n + 1;
+        }
+        if (lane == 0) *progress = 0x3fffffff;  // release the prefetch warp
+        return;
+    }
+
+    if (warp == SW) {
+        // ----------------------------------------------------------- MMA --
+        // Event loop: the S^T MMAs of item nq (once its K tile has landed
+        // and S^T buffer nq % 2 is free, i.e. the PV MMAs of item nq - 2 are
+        // issued) and the PV MMAs of item np (once its P tile is written and
+        // O^T buffer np % 2 has been read), whichever is ready first, each
+        // in item order.  Gives up after a stall of the wait limit.
+        if (lane == 0) {
+            int nq = 0, np = 0;
+            uint64_t t0 = bi_globaltimer();
+            while (np < n_items) {
+                bool did = false;
+                if (nq < n_items && nq < np + 2) {
+                    const int sk = (2 * nq) % RING;
+                    if (mbar_try_wait(&full[sk], ((2 * nq) / RING) & 1)) {
+                        tc_fence_after();
+                        issue_qk(tmem + (nq & 1) * 32,
+                                 base + DecL::SLOT + sk * DecL::TB,
+                                 base + DecL::QSLOT + sk * DecL::QB);
+                        tc_commit(&s_full[nq & 1]);
+                        tc_commit(&empty[sk]);
+                        ++nq;
+                        did = true;
+                    }
+                }
+                if (np < nq) {
+                    const int bf = np & 1;
+                    if (mbar_try_wait(&p_full[bf], (np >> 1) & 1) &&
+                        (np < 2 ||
+                         mbar_try_wait(&o_empty[bf], ((np - 2) >> 1) & 1))) {
+                        const int sv = (2 * np + 1) % RING;
+                        tc_fence_after();
+                        issue_pv(tmem + 64 + bf * 16,
+                                 base + DecL::SLOT + sv * DecL::TB,
+                                 base + DecL::P + bf * P_TILE);
+                        tc_commit(&o_full[bf]);
+                        tc_commit(&p_empty[bf]);
+                        tc_commit(&empty[sv]);
+                        ++np;
+                        did = true;
+                    }
+                }
+                if (did) {
+                    t0 = bi_globaltimer();
+                } else if (bi_globaltimer() - t0 > BI_WAIT_LIMIT_NS) {
+                    bi_record_error(status, BI_ERR_TIMEOUT);
+                    break;
+                }
+            }
+            // the last epilogues have read O^T before the memory is freed
+            for (int n = max(0, np - 2); n < np; ++n)
+                mbar_wait(&o_empty[n & 1], (n >> 1) & 1, status);
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 128);
+        return;
+    }
+
+    // ------------------------------------------------ softmax + epilogue --
+    const int tid = threadIdx.x;  // 0 .. 255
+    float m[16], m_prev[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) m_prev[r] = 0.f;
+    int pb = 0, pc = 0, pg_ = 0;  // previous item: row, chunk, KV head
+    // (row, chunk, visible length) of the next item, loaded one item ahead
+    int nb = 0, nc = 0, nvl = 0;
+    if (n_items > 0) {
+        const int2 bc = items[blockIdx.x / Hkv];
+        nb = bc.x;
+        nc = bc.y;
+        nvl = min(CHUNK, kv_len[nb] - nc * CHUNK);
+    }
+    // epilogue of item e (buffer e & 1): records of rows < G
+    auto epilogue = [&](int e) -> bool {
+        const int bf = e & 1;
+        const float *red = reinterpret_cast<const float *>(
+            smem + DecL::RED + bf * RED_FLOATS * 4);
+        if (warp == 4 && lane < G) {
+            float *rec = ws + (((int64_t)pb * Hq + pg_ * G + lane) * Cmax +
+                               pc) * rec_floats<D>();
+            float mm = m_prev[0];
+#pragma unroll
+            for (int r = 1; r < 16; ++r)
+                if (r == lane) mm = m_prev[r];
+            rec[0] = mm;
+            rec[1] = row_sum(red, lane);
+        }
+        if (warp < 4) {
+            if (!mbar_wait(&o_full[bf], (e >> 1) & 1, status)) return false;
+            tc_fence_after();
+            float o[16];
+            tmem_ld_16cols(tmem + 64 + bf * 16 + ((uint32_t)(warp * 32) << 16),
+                           o);
+            const int dim = warp * 32 + lane;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                if (r >= G) break;
+                ws[(((int64_t)pb * Hq + pg_ * G + r) * Cmax + pc) *
+                       rec_floats<D>() + 4 + dim] = o[r];
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_empty[bf]);
+        }
+        return true;
+    };
+    bool ok = true;
+    for (int n = 0; n < n_items && ok; ++n) {
+        const int i = blockIdx.x + n * gridDim.x;
+        const int g = i % Hkv;
+        const int b = nb, c = nc, vl = nvl;
+        if (n + 1 < n_items) {
+            const int2 bc = items[(i + gridDim.x) / Hkv];
+            nb = bc.x;
+            nc = bc.y;
+            nvl = min(CHUNK, kv_len[nb] - nc * CHUNK);
+        }
+        const int bf = n & 1;
+        float *red = reinterpret_cast<float *>(smem + DecL::RED +
+                                               bf * RED_FLOATS * 4);
+        const uint32_t ptile = base + DecL::P + bf * P_TILE;
+        if (!mbar_wait(&s_full[bf], (n >> 1) & 1, status) ||
+            (n >= 2 && !mbar_wait(&p_empty[bf], ((n - 2) >> 1) & 1, status))) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        int len[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) len[r] = r < G ? vl : 0;
+        softmax(tmem + bf * 32, scale, len, G, ptile, red, m);
+        // V rows past the context inside the last visible page
+        const int sv = (2 * n + 1) % RING;
+        if (!mbar_wait(&full[sv], ((2 * n + 1) / RING) & 1, status)) {
+            ok = false;
+            break;
+        }
+        if (vl & 15)
+            zero_v_rows(smem + DecL::SLOT + sv * DecL::TB, vl, (vl + 15) & ~15,
+                        tid, STHREADS);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[bf]);
+        if (n > 0) ok = epilogue(n - 1);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) m_prev[r] = m[r];
+        pb = b;
+        pc = c;
+        pg_ = g;
+    }
+    if (ok && n_items > 0) {
+        sync_softmax();  // every warp's row sums of the last item are in
+        epilogue(n_items - 1);
+    }
+}
+
+// Prefill / verify on the tensor cores (head_dim 128): CTA = (16-row tile of
+// one segment, KV head g); loops over the chunks with the functions above
+// (cp.async fills the same tile layouts the TMA writes for decode) and
+// merges the chunk partials in registers in chunk order, as the decode merge
+// kernel does, so prefill and decode rows agree bit for bit.
+namespace tca {
+struct PreL {
+    static constexpr int TB = CHUNK * 128 * 2;
+    static constexpr int K = 0, V = TB, Q = 2 * TB, P = Q + 16 * 128 * 2;
+    static constexpr int RED = P + P_TILE;
+    static constexpr int BAR = RED + RED_FLOATS * 4;   // s_full, o_full, tmem
+    static constexpr int BYTES = BAR + 2 * 8 + 16;
+    static constexpr int ALLOC = BYTES + 1024;
+};
+constexpr int PRE_THREADS = STHREADS + 32;
+}  // namespace tca
+
+__global__ void __launch_bounds__(tca::PRE_THREADS, 1)
+    prefill_tc_kernel(const uint16_t *__restrict__ q,
+                      const int32_t *__restrict__ cu_q,
+                      const int32_t *__restrict__ seg_req, int R,
+                      const int32_t *__restrict__ pos,
+                      const uint16_t *__restrict__ kp,
+                      const uint16_t *__restrict__ vp,
+                      const int32_t *__restrict__ page_table, int max_pages,
+                      int n_pages, int Hq, int Hkv, int G, float scale,
+                      int max_kv_len, uint16_t *__restrict__ out,
+                      int32_t *status) {
+    using namespace tca;
+    constexpr int D = 128;
+    constexpr int NCH = D / 8;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ int s_info[4];  // t0, nq, req, valid_max
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t base = smem_u32(smem);
+    const uint32_t ktile = base + PreL::K, vtile = base + PreL::V;
+    const uint32_t qtile = base + PreL::Q, ptile = base + PreL::P;
+    float *red = reinterpret_cast<float *>(smem + PreL::RED);
+    uint64_t *bar_s = reinterpret_cast<uint64_t *>(smem + PreL::BAR);
+    uint64_t *bar_o = bar_s + 1;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar_o + 1);
+    const int g = blockIdx.y;
+    const int QPT = 16 / G;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        int tile = blockIdx.x, r = 0, t0 = -1, nq = 0;
+        for (; r < R; ++r) {
+            const int len = cu_q[r + 1] - cu_q[r];
+            const int nt = (len + QPT - 1) / QPT;
+            if (tile < nt) {
+                t0 = cu_q[r] + tile * QPT;
+                nq = min(QPT, len - tile * QPT);
+                break;
+            }
+            tile -= nt;
+        }
+        s_info[0] = t0;
+        s_info[1] = nq;
+        s_info[2] = t0 >= 0 ? seg_req[r] : -1;
+        s_info[3] = t0 >= 0 ? pos[t0 + nq - 1] + 1 : 0;
+        mbar_init(bar_s, 1);
+        mbar_init(bar_o, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    const int t0 = s_info[0], nq = s_info[1], req = s_info[2];
+    const int vmax = s_info[3];
+    if (t0 < 0) return;
+    if (req < 0 || vmax > max_kv_len) {
+        if (req >= 0 && threadIdx.x == 0) bi_record_error(status, BI_ERR_BOUNDS);
+        for (int idx = threadIdx.x; idx < nq * G * D; idx += PRE_THREADS) {
+            const int qi = idx / (G * D), rem = idx % (G * D);
+            out[((int64_t)(t0 + qi) * Hq + g * G) * D + rem] = 0;
+        }
+        return;
+    }
+    // query tile: row r = (query r / G, head r % G)
+    for (int idx = threadIdx.x; idx < 16 * NCH; idx += PRE_THREADS) {
+        const int r = idx / NCH, ch = idx % NCH;
+        const int qi = r / G, hh = r % G;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (qi < nq)
+            v = *reinterpret_cast<const uint4 *>(
+                q + ((int64_t)(t0 + qi) * Hq + g * G + hh) * D + ch * 8);
+        *reinterpret_cast<uint4 *>(smem + PreL::Q + toff<D, 16>(r, ch)) = v;
+    }
+    if (warp == SW) tmem_alloc(tslot, 64);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const int32_t *pt_row = page_table + (int64_t)req * max_pages;
+    int prow[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r)
+        prow[r] = (r / G) < nq ? pos[t0 + r / G] : -1;
+    const int C = (vmax + CHUNK - 1) / CHUNK;
+    float M[16], L[16], O[16], m[16];
+    const int dim = (warp & 3) * 32 + lane;
+    for (int c = 0; c < C; ++c) {
+        __syncthreads();  // the previous chunk's MMAs are done with K, V, P
+        load_tile<D>(ktile, kp, pt_row, max_pages, n_pages, Hkv, g, c, vmax,
+                     status, PRE_THREADS);
+        load_tile<D>(vtile, vp, pt_row, max_pages, n_pages, Hkv, g, c, vmax,
+                     status, PRE_THREADS);
+        cp_async_commit();
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (warp == SW && lane == 0) {
+            tc_fence_after();
+            issue_qk(tmem, ktile, qtile);
+            tc_commit(bar_s);
+        }
+        int len[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            len[r] = max(0, min(CHUNK, prow[r] + 1 - c * CHUNK));
+        if (warp < SW) {
+            mbar_wait(bar_s, c & 1, status);
+            tc_fence_after();
+            softmax(tmem, scale, len, 16, ptile, red, m);
+            fence_proxy_async_smem();
+            tc_fence_before();
+        }
+        __syncthreads();  // P written, S^T read
+        if (warp == SW && lane == 0) {
+            tc_fence_after();
+            issue_pv(tmem + 32, vtile, ptile);
+            tc_commit(bar_o);
+        }
+        if (warp < 4) {
+            mbar_wait(bar_o, c & 1, status);
+            tc_fence_after();
+            float o[16];
+            tmem_ld_16cols(tmem + 32 + ((uint32_t)(warp * 32) << 16), o);
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                if (len[r] <= 0) continue;  // chunk not visible to the row
+                const float l = row_sum(red, r);
+                if (c == 0) {
+                    M[r] = m[r];
+                    L[r] = l;
+                    O[r] = o[r];
+                } else {
+                    float a, bb;
+                    merge_scalars(M[r], L[r], m[r], l, a, bb);
+                    O[r] = merge_value(O[r], o[r], a, bb);
+                }
+            }
+            tc_fence_before();
+        }
+    }
+    if (warp < 4) {
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const int qi = r / G, hh = r % G;
+            if (qi >= nq) continue;
+            out[((int64_t)(t0 + qi) * Hq + g * G + hh) * D + dim] =
+                f32_to_bf16(__fdiv_rn(O[r], L[r]));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == SW) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 64);
+    }
+}
+
 // ------------------------------------------------------------------- host --
 
 template <typename K>
@@ -908,15 +1564,26 @@ bi_status launch_decode_chunks(const CUtensorMap &km, const CUtensorMap &vm,
                                cudaStream_t s) {
     static std::once_flag f;
     static bi_status fs;
-    std::call_once(f, [] {
-        fs = set_attr(decode_chunks_kernel<D>, DecSmem<D>::ALLOC);
-    });
-    if (fs != BI_OK) return fs;
-    decode_chunks_kernel<D>
-        <<<bi_sm_count(), cthreads<D>() + 64, DecSmem<D>::ALLOC, s>>>(
-            km, vm, qm, page_table, max_pages, n_pages, row_req, kv_len, Hq,
-            Hkv, G, scale, rec, Cmax, prefix, B, items, k_pool, v_pool,
-            status);
+    if constexpr (D == 128) {
+        std::call_once(f, [] {
+            fs = set_attr(decode_tc_kernel, tca::DecL::ALLOC);
+        });
+        if (fs != BI_OK) return fs;
+        decode_tc_kernel<<<bi_sm_count(), tca::DEC_THREADS, tca::DecL::ALLOC,
+                           s>>>(km, vm, qm, page_table, max_pages, n_pages,
+                                row_req, kv_len, Hq, Hkv, G, scale, rec, Cmax,
+                                prefix, B, items, k_pool, v_pool, status);
+    } else {
+        std::call_once(f, [] {
+            fs = set_attr(decode_chunks_kernel<D>, DecSmem<D>::ALLOC);
+        });
+        if (fs != BI_OK) return fs;
+        decode_chunks_kernel<D>
+            <<<bi_sm_count(), cthreads<D>() + 64, DecSmem<D>::ALLOC, s>>>(
+                km, vm, qm, page_table, max_pages, n_pages, row_req, kv_len,
+                Hq, Hkv, G, scale, rec, Cmax, prefix, B, items, k_pool, v_pool,
+                status);
+    }
     BI_LAUNCH_CHECK("decode attention launch");
     return BI_OK;
 }
@@ -1130,11 +1797,11 @@ bi_status bi_prefill_attn_pool(const bi_bf16 *q, const int32_t *cu_q,
         static std::once_flag f;
         static bi_status fs;
         std::call_once(f, [] {
-            fs = set_attr(prefill_kernel<128>, prefill_smem<128>());
+            fs = set_attr(prefill_tc_kernel, tca::PreL::ALLOC);
         });
         if (fs != BI_OK) return fs;
-        prefill_kernel<128><<<grid, cthreads<128>(), prefill_smem<128>(),
-                              stream>>>(
+        prefill_tc_kernel<<<grid, tca::PRE_THREADS, tca::PreL::ALLOC,
+                            stream>>>(
             q, cu_q, seg_req, R, pos, k_pool, v_pool, page_table, max_pages,
             n_pages, Hq, Hkv, G, scale, max_kv_len, out, status);
     } else {

@@ -287,6 +287,39 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, float *v) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Each thread of the warp reads 16 consecutive fp32 columns of its own TMEM
+// lane (the warp's 32-lane quarter is fixed by warp id % 4).
+__device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, float *v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]),
+          "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]),
+          "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory descriptor of an MN-major operand stored with the 128-byte
+// swizzle: 8-row atoms of 128 bytes (64 elements of M or N per row, 8 of
+// K per atom); lbo = byte distance between atoms along M/N, sbo = byte
+// distance between atoms along K.
+__device__ __forceinline__ uint64_t make_sw128_desc_mn(uint32_t smem_addr,
+                                                      uint32_t lbo,
+                                                      uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr >> 4) & 0x3fffu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3fffu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3fffu) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
 // ------------------------------------------------------- mma.sync helpers --
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0,
