@@ -940,49 +940,59 @@ __device__ __forceinline__ void sync_softmax() {
 }
 
 // Softmax of one chunk by the 256 softmax threads (thread t <-> key t), for
-// rows 0 .. nr-1 of the tile: reads S^T at s_tmem, applies scale and the
+// rows 0 .. NR-1 of the tile: reads S^T at s_tmem, applies scale and the
 // per-row visible lengths, writes m[r] (every thread), the warp sums to
-// red + 128 and bf16(p) to the P tile.  Rows >= nr are not touched.
+// red + 128 and bf16(p) to the P tile.  Rows >= NR are not touched.  The
+// reductions of the NR rows run stage by stage across the rows (independent
+// shuffle chains side by side); each row's own operations and their order
+// do not depend on NR.
+template <int NR>
 __device__ __forceinline__ void softmax(uint32_t s_tmem, float scale,
-                                        const int (&len)[16], int nr,
-                                        uint32_t ptile, float *red,
-                                        float (&m)[16]) {
+                                        const int (&len)[16], uint32_t ptile,
+                                        float *red, float (&m)[16]) {
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int key = (w >> 2) * 128 + (w & 3) * 32 + lane;
-    float v[16];
+    float v[16], x[NR];
     tmem_ld_16cols(s_tmem + ((uint32_t)((w & 3) * 32) << 16) + (w >> 2) * 16,
                    v);
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-        if (r >= nr) break;
+    for (int r = 0; r < NR; ++r) {
         float s = __fmul_rn(v[r], scale);
         s = key < len[r] ? s : -INFINITY;
         v[r] = s;
-        float mx = s;
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1)
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (lane == 0) red[w * 16 + r] = mx;
+        x[r] = s;
     }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1)
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+            x[r] = fmaxf(x[r], __shfl_xor_sync(0xffffffffu, x[r], o));
+    if (lane == 0)
+#pragma unroll
+        for (int r = 0; r < NR; ++r) red[w * 16 + r] = x[r];
     sync_softmax();
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-        if (r >= nr) break;
+    for (int r = 0; r < NR; ++r) {
         float mm = red[r];
 #pragma unroll
-        for (int x = 1; x < SW; ++x) mm = fmaxf(mm, red[x * 16 + r]);
+        for (int k = 1; k < SW; ++k) mm = fmaxf(mm, red[k * 16 + r]);
         m[r] = mm;
         const float mu = mm == -INFINITY ? 0.f : mm;
         const float p = key < len[r] ? expf(__fsub_rn(v[r], mu)) : 0.f;
-        float l = p;
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1)
-            l = __fadd_rn(l, __shfl_xor_sync(0xffffffffu, l, o));
-        if (lane == 0) red[SW * 16 + w * 16 + r] = l;
+        v[r] = p;
+        x[r] = p;
         asm volatile("st.shared.b16 [%0], %1;" ::"r"(ptile + poff(r, key)),
                      "h"(f32_to_bf16(p))
                      : "memory");
     }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1)
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+            x[r] = __fadd_rn(x[r], __shfl_xor_sync(0xffffffffu, x[r], o));
+    if (lane == 0)
+#pragma unroll
+        for (int r = 0; r < NR; ++r) red[SW * 16 + w * 16 + r] = x[r];
 }
 
 // Block row sum of row r from the warp sums (fixed warp order).
@@ -1020,11 +1030,16 @@ struct DecL {
 };
 constexpr int DEC_THREADS = (SW + 3) * 32;  // softmax, MMA, producer, prefetch
 
+// Position of the K and V loads of item n in the ring's load sequence.
+__device__ __forceinline__ int k_load(int n) { return 2 * n; }
+__device__ __forceinline__ int v_load(int n) { return 2 * n + 1; }
+
 }  // namespace tca
 
 // Persistent decode chunk kernel on the tensor cores (head_dim 128).  CTA k
 // takes items k, k + grid, ...; item i is KV head i % Hkv of list entry
-// i / Hkv; item n of a CTA uses ring slots 2n (K, Q) and 2n + 1 (V) mod RING.
+// i / Hkv.  The ring loads K0 V0 K1 V1 ..., load j in slot j mod RING
+// (k_load / v_load below).
 //   warps 0-7   softmax and epilogue (thread t <-> key t of the chunk);
 //   warp 8      owns the tensor memory; lane 0 issues the MMAs: S^T of item
 //               n + 2 is issued as soon as item n's softmax has read S^T
@@ -1141,7 +1156,10 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
             tma_prefetch_desc(&qmap);
         }
         bool ok = true;
-        for (int n = 0; n < n_items && ok; ++n) {
+        // load t of the sequence: the K (t even) or V (t odd) of item t / 2
+        for (int t = 0; t < 2 * n_items && ok; ++t) {
+            const bool is_k = (t & 1) == 0;
+            const int n = t >> 1;
             const int i = blockIdx.x + n * gridDim.x;
             const int g = i % Hkv;
             const int2 bc = items[i / Hkv];
@@ -1154,47 +1172,41 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
                 const int pi = c * 16 + lane;
                 pg = pi < max_pages ? pt_row[pi] : -1;
                 if (pg < 0 || pg >= n_pages) {
-                    bi_record_error(status, BI_ERR_BOUNDS);
+                    if (is_k) bi_record_error(status, BI_ERR_BOUNDS);
                     pg = -1;
                 }
             }
             const int nvalid = __popc(__ballot_sync(0xffffffffu, pg >= 0));
-            for (int kv = 0; kv < 2 && ok; ++kv) {
-                const int j = 2 * n + kv;
-                const int slot = j % RING;
-                const int use = j / RING;
-                bool w_ok = true;
-                if (lane == 0 && use > 0)
-                    w_ok = mbar_wait(&empty[slot], (use - 1) & 1, status);
-                ok = __shfl_sync(0xffffffffu, w_ok ? 1 : 0, 0) != 0;
-                if (!ok) break;
-                // K: the visible pages (+ Q).  V: all 16 pages, the ones
-                // without data as boxes wholly above row 0 (zero-filled).
-                if (lane == 0)
-                    mbar_arrive_expect_tx(
-                        &full[slot], kv == 0 ? nvalid * 2 * PAGE_BYTES +
-                                                   2 * HALF_Q
-                                             : 16 * 2 * PAGE_BYTES);
-                __syncwarp();
-                uint8_t *tile = smem + DecL::SLOT + slot * DecL::TB;
-                if (lane < 16 && (kv == 1 || pg >= 0)) {
-                    const int row = pg >= 0 ? (pg * Hkv + g) * 16 : -16;
-                    const CUtensorMap *map = kv == 0 ? &kmap : &vmap;
+            const int slot = t % RING;
+            const int use = t / RING;
+            bool w_ok = true;
+            if (lane == 0 && use > 0)
+                w_ok = mbar_wait(&empty[slot], (use - 1) & 1, status);
+            ok = __shfl_sync(0xffffffffu, w_ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
+            // K: the visible pages (+ Q).  V: all 16 pages, the ones
+            // without data as boxes wholly above row 0 (zero-filled).
+            if (lane == 0)
+                mbar_arrive_expect_tx(&full[slot],
+                                      is_k ? nvalid * 2 * PAGE_BYTES + 2 * HALF_Q
+                                           : 16 * 2 * PAGE_BYTES);
+            __syncwarp();
+            uint8_t *tile = smem + DecL::SLOT + slot * DecL::TB;
+            if (lane < 16 && (!is_k || pg >= 0)) {
+                const int row = pg >= 0 ? (pg * Hkv + g) * 16 : -16;
+                const CUtensorMap *map = is_k ? &kmap : &vmap;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h)
-                        tma_load_2d(tile + h * HALF_TILE + lane * PAGE_BYTES,
-                                    map, h * 64, row, &full[slot]);
-                }
-                if (kv == 0 && lane == 0) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-                        tma_load_2d(smem + DecL::QSLOT + slot * DecL::QB +
-                                        h * HALF_Q,
-                                    &qmap, h * 64, b * Hq + g * G,
-                                    &full[slot]);
-                }
+                for (int h = 0; h < 2; ++h)
+                    tma_load_2d(tile + h * HALF_TILE + lane * PAGE_BYTES, map,
+                                h * 64, row, &full[slot]);
             }
-            if (lane == 0) *progress = n + 1;
+            if (is_k && lane == 0) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    tma_load_2d(smem + DecL::QSLOT + slot * DecL::QB + h * HALF_Q,
+                                &qmap, h * 64, b * Hq + g * G, &full[slot]);
+                *progress = n + 1;
+            }
         }
         if (lane == 0) *progress = 0x3fffffff;  // release the prefetch warp
         return;
@@ -1213,8 +1225,8 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
             while (np < n_items) {
                 bool did = false;
                 if (nq < n_items && nq < np + 2) {
-                    const int sk = (2 * nq) % RING;
-                    if (mbar_try_wait(&full[sk], ((2 * nq) / RING) & 1)) {
+                    const int jk = k_load(nq), sk = jk % RING;
+                    if (mbar_try_wait(&full[sk], (jk / RING) & 1)) {
                         tc_fence_after();
                         issue_qk(tmem + (nq & 1) * 32,
                                  base + DecL::SLOT + sk * DecL::TB,
@@ -1230,7 +1242,7 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
                     if (mbar_try_wait(&p_full[bf], (np >> 1) & 1) &&
                         (np < 2 ||
                          mbar_try_wait(&o_empty[bf], ((np - 2) >> 1) & 1))) {
-                        const int sv = (2 * np + 1) % RING;
+                        const int sv = v_load(np) % RING;
                         tc_fence_after();
                         issue_pv(tmem + 64 + bf * 16,
                                  base + DecL::SLOT + sv * DecL::TB,
@@ -1331,10 +1343,13 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
         int len[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) len[r] = r < G ? vl : 0;
-        softmax(tmem + bf * 32, scale, len, G, ptile, red, m);
+        if (G <= 4)
+            softmax<4>(tmem + bf * 32, scale, len, ptile, red, m);
+        else
+            softmax<16>(tmem + bf * 32, scale, len, ptile, red, m);
         // V rows past the context inside the last visible page
-        const int sv = (2 * n + 1) % RING;
-        if (!mbar_wait(&full[sv], ((2 * n + 1) / RING) & 1, status)) {
+        const int jv = v_load(n), sv = jv % RING;
+        if (!mbar_wait(&full[sv], (jv / RING) & 1, status)) {
             ok = false;
             break;
         }
@@ -1359,29 +1374,32 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
 }
 
 // Prefill / verify on the tensor cores (head_dim 128): CTA = (16-row tile of
-// one segment, KV head g); loops over the chunks with the functions above
-// (cp.async fills the same tile layouts the TMA writes for decode) and
+// one segment, KV head g); loops over the chunks with the functions above and
 // merges the chunk partials in registers in chunk order, as the decode merge
-// kernel does, so prefill and decode rows agree bit for bit.
+// kernel does, so prefill and decode rows agree bit for bit.  Warp 8 issues
+// the TMA page loads (the tile layouts decode uses) and the MMAs: chunk c + 1's
+// K is loaded once chunk c's scores are done, its V once chunk c's PV
+// products are done, so the loads overlap the softmax and the merge.
 namespace tca {
 struct PreL {
     static constexpr int TB = CHUNK * 128 * 2;
     static constexpr int K = 0, V = TB, Q = 2 * TB, P = Q + 16 * 128 * 2;
     static constexpr int RED = P + P_TILE;
-    static constexpr int BAR = RED + RED_FLOATS * 4;   // s_full, o_full, tmem
-    static constexpr int BYTES = BAR + 2 * 8 + 16;
+    // k_full, v_full, s_full, p_full, o_full, then the TMEM address
+    static constexpr int BAR = RED + RED_FLOATS * 4;
+    static constexpr int BYTES = BAR + 5 * 8 + 16;
     static constexpr int ALLOC = BYTES + 1024;
 };
 constexpr int PRE_THREADS = STHREADS + 32;
 }  // namespace tca
 
 __global__ void __launch_bounds__(tca::PRE_THREADS, 1)
-    prefill_tc_kernel(const uint16_t *__restrict__ q,
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap,
+                      const uint16_t *__restrict__ q,
                       const int32_t *__restrict__ cu_q,
                       const int32_t *__restrict__ seg_req, int R,
                       const int32_t *__restrict__ pos,
-                      const uint16_t *__restrict__ kp,
-                      const uint16_t *__restrict__ vp,
                       const int32_t *__restrict__ page_table, int max_pages,
                       int n_pages, int Hq, int Hkv, int G, float scale,
                       int max_kv_len, uint16_t *__restrict__ out,
@@ -1389,6 +1407,7 @@ __global__ void __launch_bounds__(tca::PRE_THREADS, 1)
     using namespace tca;
     constexpr int D = 128;
     constexpr int NCH = D / 8;
+    constexpr int PAGE_BYTES = 16 * 64 * 2;   // one box: 16 rows x 64 dims
     extern __shared__ uint8_t smem_raw[];
     __shared__ int s_info[4];  // t0, nq, req, valid_max
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -1397,9 +1416,10 @@ __global__ void __launch_bounds__(tca::PRE_THREADS, 1)
     const uint32_t ktile = base + PreL::K, vtile = base + PreL::V;
     const uint32_t qtile = base + PreL::Q, ptile = base + PreL::P;
     float *red = reinterpret_cast<float *>(smem + PreL::RED);
-    uint64_t *bar_s = reinterpret_cast<uint64_t *>(smem + PreL::BAR);
-    uint64_t *bar_o = bar_s + 1;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(bar_o + 1);
+    uint64_t *k_full = reinterpret_cast<uint64_t *>(smem + PreL::BAR);
+    uint64_t *v_full = k_full + 1, *s_full = k_full + 2, *p_full = k_full + 3;
+    uint64_t *o_full = k_full + 4;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(k_full + 5);
     const int g = blockIdx.y;
     const int QPT = 16 / G;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1419,8 +1439,11 @@ __global__ void __launch_bounds__(tca::PRE_THREADS, 1)
         s_info[1] = nq;
         s_info[2] = t0 >= 0 ? seg_req[r] : -1;
         s_info[3] = t0 >= 0 ? pos[t0 + nq - 1] + 1 : 0;
-        mbar_init(bar_s, 1);
-        mbar_init(bar_o, 1);
+        mbar_init(k_full, 1);
+        mbar_init(v_full, 1);
+        mbar_init(s_full, 1);
+        mbar_init(p_full, SW);
+        mbar_init(o_full, 1);
         mbar_fence_init();
     }
     __syncthreads();
@@ -1445,80 +1468,135 @@ __global__ void __launch_bounds__(tca::PRE_THREADS, 1)
                 q + ((int64_t)(t0 + qi) * Hq + g * G + hh) * D + ch * 8);
         *reinterpret_cast<uint4 *>(smem + PreL::Q + toff<D, 16>(r, ch)) = v;
     }
+    fence_proxy_async_smem();
     if (warp == SW) tmem_alloc(tslot, 64);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const int32_t *pt_row = page_table + (int64_t)req * max_pages;
-    int prow[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r)
-        prow[r] = (r / G) < nq ? pos[t0 + r / G] : -1;
     const int C = (vmax + CHUNK - 1) / CHUNK;
-    float M[16], L[16], O[16], m[16];
-    const int dim = (warp & 3) * 32 + lane;
-    for (int c = 0; c < C; ++c) {
-        __syncthreads();  // the previous chunk's MMAs are done with K, V, P
-        load_tile<D>(ktile, kp, pt_row, max_pages, n_pages, Hkv, g, c, vmax,
-                     status, PRE_THREADS);
-        load_tile<D>(vtile, vp, pt_row, max_pages, n_pages, Hkv, g, c, vmax,
-                     status, PRE_THREADS);
-        cp_async_commit();
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (warp == SW && lane == 0) {
-            tc_fence_after();
-            issue_qk(tmem, ktile, qtile);
-            tc_commit(bar_s);
-        }
-        int len[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r)
-            len[r] = max(0, min(CHUNK, prow[r] + 1 - c * CHUNK));
-        if (warp < SW) {
-            mbar_wait(bar_s, c & 1, status);
-            tc_fence_after();
-            softmax(tmem, scale, len, 16, ptile, red, m);
-            fence_proxy_async_smem();
-            tc_fence_before();
-        }
-        __syncthreads();  // P written, S^T read
-        if (warp == SW && lane == 0) {
-            tc_fence_after();
-            issue_pv(tmem + 32, vtile, ptile);
-            tc_commit(bar_o);
-        }
-        if (warp < 4) {
-            mbar_wait(bar_o, c & 1, status);
-            tc_fence_after();
-            float o[16];
-            tmem_ld_16cols(tmem + 32 + ((uint32_t)(warp * 32) << 16), o);
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                if (len[r] <= 0) continue;  // chunk not visible to the row
-                const float l = row_sum(red, r);
-                if (c == 0) {
-                    M[r] = m[r];
-                    L[r] = l;
-                    O[r] = o[r];
-                } else {
-                    float a, bb;
-                    merge_scalars(M[r], L[r], m[r], l, a, bb);
-                    O[r] = merge_value(O[r], o[r], a, bb);
+
+    if (warp == SW) {
+        // ------------------------------------------------ loads and MMAs --
+        // Pages of chunk c: lane p < 16 loads page 16c + p (a zero-filled box
+        // past the tile's last visible position or for a missing page).
+        auto load = [&](int c, bool is_k) {
+            int pg = -1;
+            if (lane < 16) {
+                const int pi = c * 16 + lane;
+                if (c * CHUNK + lane * 16 < vmax && pi < max_pages) {
+                    pg = pt_row[pi];
+                    if (pg < 0 || pg >= n_pages) {
+                        if (is_k) bi_record_error(status, BI_ERR_BOUNDS);
+                        pg = -1;
+                    }
                 }
             }
-            tc_fence_before();
-        }
-    }
-    if (warp < 4) {
+            uint64_t *bar = is_k ? k_full : v_full;
+            if (lane == 0) mbar_arrive_expect_tx(bar, 16 * 2 * PAGE_BYTES);
+            __syncwarp();
+            if (lane < 16) {
+                const int row = pg >= 0 ? (pg * Hkv + g) * 16 : -16;
+                uint8_t *tile = smem + (is_k ? PreL::K : PreL::V);
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const int qi = r / G, hh = r % G;
-            if (qi >= nq) continue;
-            out[((int64_t)(t0 + qi) * Hq + g * G + hh) * D + dim] =
-                f32_to_bf16(__fdiv_rn(O[r], L[r]));
+                for (int h = 0; h < 2; ++h)
+                    tma_load_2d(tile + h * (CHUNK * 128) + lane * PAGE_BYTES,
+                                is_k ? &kmap : &vmap, h * 64, row, bar);
+            }
+        };
+        if (lane == 0) {
+            tma_prefetch_desc(&kmap);
+            tma_prefetch_desc(&vmap);
+        }
+        load(0, true);
+        load(0, false);
+        for (int c = 0; c < C; ++c) {
+            bool ok = true;
+            if (lane == 0) {
+                ok = mbar_wait(k_full, c & 1, status);
+                if (ok) {
+                    tc_fence_after();
+                    issue_qk(tmem, ktile, qtile);
+                    tc_commit(s_full);
+                    ok = mbar_wait(s_full, c & 1, status);  // K read
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+            if (c + 1 < C) load(c + 1, true);
+            if (lane == 0) {
+                ok = mbar_wait(p_full, c & 1, status);  // P written, V zeroed
+                if (ok) {
+                    tc_fence_after();
+                    issue_pv(tmem + 32, vtile, ptile);
+                    tc_commit(o_full);
+                    ok = mbar_wait(o_full, c & 1, status);  // V, P read
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+            if (c + 1 < C) load(c + 1, false);
+        }
+    } else {
+        // -------------------------------------------- softmax and merge --
+        int prow[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            prow[r] = (r / G) < nq ? pos[t0 + r / G] : -1;
+        float M[16], L[16], O[16], m[16];
+        for (int c = 0; c < C; ++c) {
+            int len[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r)
+                len[r] = max(0, min(CHUNK, prow[r] + 1 - c * CHUNK));
+            // the previous chunk's PV products are done with P
+            if (c > 0 && !mbar_wait(o_full, (c - 1) & 1, status)) break;
+            if (!mbar_wait(s_full, c & 1, status)) break;
+            tc_fence_after();
+            softmax<16>(tmem, scale, len, ptile, red, m);
+            // V rows past the tile's last visible position in the last page
+            if (!mbar_wait(v_full, c & 1, status)) break;
+            const int vl = min(CHUNK, vmax - c * CHUNK);
+            if (vl & 15)
+                zero_v_rows(smem + PreL::V, vl, (vl + 15) & ~15, threadIdx.x,
+                            STHREADS);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+            if (warp < 4) {
+                if (!mbar_wait(o_full, c & 1, status)) break;
+                tc_fence_after();
+                float o[16];
+                tmem_ld_16cols(tmem + 32 + ((uint32_t)(warp * 32) << 16), o);
+                sync_softmax();  // every warp's row sums are in
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    if (len[r] <= 0) continue;  // chunk not visible to the row
+                    const float l = row_sum(red, r);
+                    if (c == 0) {
+                        M[r] = m[r];
+                        L[r] = l;
+                        O[r] = o[r];
+                    } else {
+                        float a, bb;
+                        merge_scalars(M[r], L[r], m[r], l, a, bb);
+                        O[r] = merge_value(O[r], o[r], a, bb);
+                    }
+                }
+                tc_fence_before();
+            } else {
+                sync_softmax();
+            }
+        }
+        if (warp < 4) {
+            const int dim = warp * 32 + lane;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                const int qi = r / G, hh = r % G;
+                if (qi >= nq) continue;
+                out[((int64_t)(t0 + qi) * Hq + g * G + hh) * D + dim] =
+                    f32_to_bf16(__fdiv_rn(O[r], L[r]));
+            }
         }
     }
     tc_fence_before();
@@ -1800,10 +1878,19 @@ bi_status bi_prefill_attn_pool(const bi_bf16 *q, const int32_t *cu_q,
             fs = set_attr(prefill_tc_kernel, tca::PreL::ALLOC);
         });
         if (fs != BI_OK) return fs;
+        const uint64_t pool_rows = (uint64_t)n_pages * Hkv * 16;
+        CUtensorMap km, vm;
+        bi_status st;
+        if ((st = bi_make_tmap_2d_bf16(&km, k_pool, D, pool_rows, D * 2, 64, 16,
+                                       true)) != BI_OK)
+            return st;
+        if ((st = bi_make_tmap_2d_bf16(&vm, v_pool, D, pool_rows, D * 2, 64, 16,
+                                       true)) != BI_OK)
+            return st;
         prefill_tc_kernel<<<grid, tca::PRE_THREADS, tca::PreL::ALLOC,
                             stream>>>(
-            q, cu_q, seg_req, R, pos, k_pool, v_pool, page_table, max_pages,
-            n_pages, Hq, Hkv, G, scale, max_kv_len, out, status);
+            km, vm, q, cu_q, seg_req, R, pos, page_table, max_pages, n_pages,
+            Hq, Hkv, G, scale, max_kv_len, out, status);
     } else {
         static std::once_flag f;
         static bi_status fs;
@@ -1828,6 +1915,7 @@ extern "C" bi_status bi_prefill_attn(
     void *stream) {
     return bi_prefill_attn_pool(q, cu_q, seg_req, R, T, pos, max_q, max_kv_len,
                                 k_pool, v_pool, page_table, max_pages,
-                                0x7fffffff, Hq, Hkv, D, scale, out,
+                                Hkv > 0 ? unbounded_pages(Hkv) : 1, Hq, Hkv, D,
+                                scale, out,
                                 bi_stream(stream));
 }
