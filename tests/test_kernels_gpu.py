@@ -228,6 +228,36 @@ def test_decode_attention(bi, orc, Hq, Hkv, D):
     assert np.array_equal(bits(again), full)
 
 
+@pytest.mark.parametrize("D", [128, 32])
+def test_decode_work_list_over_many_rows(bi, orc, D):
+    """More rows than the work-list builder has threads (two batches of
+    1024), a mix of full and partial chunks: sampled rows against the oracle,
+    and the whole batch bitwise equal after a shuffle of its rows (which
+    reorders the work list and so changes the CTA that computes each
+    chunk)."""
+    rng = np.random.default_rng(7)
+    lens = rng.integers(1, 200, 1100)
+    lens[::97] = 256
+    lens[5::89] = 16
+    lens[11::101] = 300
+    kv = PagedKV(lens, 1, D, seed=71)
+    B = len(lens)
+    q = randn_bf16((B, 4, D), 72)
+    rows = list(range(B))
+    out = decode(bi, q, kv, rows, lens)
+    sync_ok(bi)
+    full = bits(out)
+    pick = np.sort(rng.choice(B, 24, replace=False))
+    ref = attn_ref(orc, q[torch.from_numpy(pick).cuda()], kv, pick,
+                   lens[pick] - 1)
+    check_close(full[pick], ref, orc)
+    perm = rng.permutation(B)
+    shuf = decode(bi, q[torch.from_numpy(perm).cuda()].contiguous(), kv,
+                  list(perm), lens[perm])
+    sync_ok(bi)
+    assert np.array_equal(bits(shuf), full[perm])
+
+
 @pytest.mark.parametrize("Hq,Hkv,D", [(32, 8, 128), (4, 4, 32)])
 def test_prefill_matches_decode_bitwise(bi, orc, Hq, Hkv, D):
     """Query-length invariance (Vosti): a position computed inside a window
