@@ -52,18 +52,24 @@ constexpr int TMEM_COLS = 512;
 constexpr int MAX_SPLITS = 8;
 constexpr int PLAN_SMS = 152;             // SMs the plan fills (GB300)
 
-template <int BN>
+// ONE: every CTA runs at most one work unit.  Its epilogue then starts only
+// after every load of the CTA has landed and every MMA has read its stage,
+// so the epilogue staging reuses the first stage of the ring and the ring
+// gets the space (BN = 192: four stages instead of three).
+template <int BN, bool ONE = false>
 struct Tile {
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int FIT = (SMEM_LIMIT - EPI_BYTES - 1024 - 256) / STAGE_BYTES;
+    static constexpr int EPI_OWN = ONE ? 0 : EPI_BYTES;  // staging of its own
+    static constexpr int FIT = (SMEM_LIMIT - EPI_OWN - 1024 - 256) / STAGE_BYTES;
     static constexpr int STAGES = FIT < 4 ? FIT : 4;
     static constexpr int ACC_COLS = 2 * BN;           // both halves
     static constexpr int NACC = TMEM_COLS / ACC_COLS;  // accumulators in TMEM
     static constexpr uint32_t IDESC = make_idesc_bf16(HALF, BN);
     static constexpr size_t SMEM =
-        1024 + (size_t)STAGES * STAGE_BYTES + EPI_BYTES + 256;
+        1024 + (size_t)STAGES * STAGE_BYTES + EPI_OWN + 256;
     static_assert(STAGES >= 2 && NACC >= 1, "tile does not fit");
+    static_assert(ONE ? A_BYTES >= EPI_BYTES : true, "staging in stage 0");
     static_assert(SMEM <= SMEM_LIMIT, "shared memory");
 };
 
@@ -141,20 +147,22 @@ struct Stager {
     }
 };
 
-template <int BN>
+template <int BN, bool ONE>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                 const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmO, GemmArgs p) {
-    using T = Tile<BN>;
+    using T = Tile<BN, ONE>;
     constexpr int STAGES = T::STAGES, NACC = T::NACC;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *sA = smem;
     uint8_t *sB = smem + STAGES * A_BYTES;
-    uint8_t *sE = sB + STAGES * T::B_BYTES;  // epilogue staging, 1024-aligned
-    uint64_t *full = reinterpret_cast<uint64_t *>(sE + EPI_BYTES);
+    // epilogue staging, 1024-aligned: its own region, or stage 0's A tile
+    uint8_t *sE = ONE ? sA : sB + STAGES * T::B_BYTES;
+    uint64_t *full =
+        reinterpret_cast<uint64_t *>(sB + STAGES * T::B_BYTES + T::EPI_OWN);
     uint64_t *empty = full + STAGES;
     uint64_t *acc_full = empty + STAGES;     // [NACC]
     uint64_t *acc_empty = acc_full + NACC;   // [NACC]
@@ -377,14 +385,14 @@ __global__ void pack_gate_up_kernel(const uint4 *__restrict__ wg,
     }
 }
 
-template <int BN>
+template <int BN, bool ONE>
 bi_status set_smem_attr() {
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
-        err = cudaFuncSetAttribute(gemm_kernel<BN>,
+        err = cudaFuncSetAttribute(gemm_kernel<BN, ONE>,
                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)Tile<BN>::SMEM);
+                                   (int)Tile<BN, ONE>::SMEM);
     });
     return bi_cuda_check(err, "gemm smem attribute");
 }
@@ -427,10 +435,18 @@ template <int BN>
 bi_status launch(const CUtensorMap &ta, const CUtensorMap &tb,
                  const CUtensorMap &to, const GemmArgs &a,
                  cudaStream_t stream) {
-    bi_status st = set_smem_attr<BN>();
-    if (st != BI_OK) return st;
     const int grid = std::min(a.units, bi_sm_count());
-    gemm_kernel<BN><<<grid, THREADS, Tile<BN>::SMEM, stream>>>(ta, tb, to, a);
+    if (a.units <= grid) {  // one unit per CTA
+        bi_status st = set_smem_attr<BN, true>();
+        if (st != BI_OK) return st;
+        gemm_kernel<BN, true><<<grid, THREADS, Tile<BN, true>::SMEM, stream>>>(
+            ta, tb, to, a);
+    } else {
+        bi_status st = set_smem_attr<BN, false>();
+        if (st != BI_OK) return st;
+        gemm_kernel<BN, false>
+            <<<grid, THREADS, Tile<BN, false>::SMEM, stream>>>(ta, tb, to, a);
+    }
     BI_LAUNCH_CHECK("gemm launch");
     return BI_OK;
 }
