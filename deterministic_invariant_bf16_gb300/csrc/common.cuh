@@ -265,6 +265,100 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
         : "memory");
 }
 
+// ------------------------------------------------- CTA pairs (cta_group::2)
+//
+// Two CTAs of a cluster of two share one MMA: the even CTA (rank 0) issues
+// tcgen05.mma.cta_group::2 for M = 256 rows, each CTA supplying 128 rows of
+// A and half of the N rows of B from the same shared-memory offsets, and
+// each receiving its 128 rows of D in its own tensor memory.
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of both CTAs of the cluster (warp-converged).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n\t"
+        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Shared::cluster address of the same shared variable in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_rank(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(r)
+                 : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+
+// Arrive on an mbarrier given by its shared::cluster address.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
+    asm volatile(
+        "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+            addr)
+        : "memory");
+}
+
+// 2-D TMA load into this CTA's shared memory, completing on the mbarrier
+// at shared::cluster address `bar` (in either CTA of the pair).
+__device__ __forceinline__ void tma_load_2d_pair(void *dst,
+                                                 const CUtensorMap *m, int x,
+                                                 int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::"
+        "complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(m), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// Tensor memory of both CTAs of the pair: one warp of each CTA calls these
+// with the same arguments; both receive the same address.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t *slot, uint32_t ncols) {
+    asm volatile(
+        "tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+            smem_u32(slot)),
+        "r"(ncols)
+        : "memory");
+    asm volatile(
+        "tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::
+            : "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr,
+                                                  uint32_t ncols) {
+    asm volatile(
+        "tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr),
+        "r"(ncols)
+        : "memory");
+}
+
+// Pair MMA, issued by one thread of the even CTA.
+__device__ __forceinline__ void tc_mma_pair_bf16(uint32_t d_tmem,
+                                                 uint64_t a_desc,
+                                                 uint64_t b_desc,
+                                                 uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on the mbarrier at `bar`'s offset in both CTAs of the pair once
+// the pair MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void tc_commit_pair(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster."
+        "multicast::cluster.b64 [%0], %1;" ::"r"(smem_u32(bar)),
+        "h"((uint16_t)3)
+        : "memory");
+}
+
 // Each thread of the warp reads 32 consecutive fp32 columns of its own TMEM
 // lane (the warp's 32-lane quarter is fixed by warp id % 4).
 __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, float *v) {

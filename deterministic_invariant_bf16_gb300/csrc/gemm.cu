@@ -83,8 +83,13 @@ struct GemmArgs {
 };
 
 // silu(g) * u = (g / (1 + e^-g)) * u, each operation rounded separately.
+// The exponential and the division are the fast hardware forms (__expf,
+// __fdividef: a few fp32 ulp), far below the bf16 resolution of the
+// output; the correctly rounded forms made the SwiGLU epilogue of the
+// 8B gate/up GEMM 8 us slower (58 -> 50 us at M = 256).  The same fp32
+// steps for every M, so the result stays batch-invariant.
 __device__ __forceinline__ float swiglu1(float g, float u) {
-    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+    return __fmul_rn(__fdividef(g, __fadd_rn(1.0f, __expf(-g))), u);
 }
 
 __device__ __forceinline__ int slice_lo(const GemmArgs &p, int s) {
@@ -146,6 +151,58 @@ struct Stager {
         ++count;
     }
 };
+
+// Epilogue of one accumulator block: this warp's 32 TMEM lanes (rows row0
+// .. row0 + 31) x BN fp32 columns from `base`, for output column tile nt
+// (BN columns; BN / 2 features for SwiGLU) and slice s; `live`: row0 < M.
+template <int BN>
+__device__ __forceinline__ void store_block(const GemmArgs &p,
+                                            const CUtensorMap *tmO,
+                                            Stager &stg, uint32_t base,
+                                            int row0, int nt, int s,
+                                            bool live) {
+    const int n0 = nt * BN;
+    if (p.out_kind == BI_OUT_SWIGLU) {
+        // gate columns [0, w), up columns [w, 2w) of this tile
+        const int f0 = nt * (BN / 2);
+        const int w = min(BN / 2, p.F - f0);
+        for (int c = 0; c < w; c += 32) {
+            float g[32], uu[32];
+            uint32_t wd[16];
+            tmem_ld_32cols(base + c, g);
+            tmem_ld_32cols(base + w + c, uu);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                wd[i] = pack_bf16x2(swiglu1(g[2 * i], uu[2 * i]),
+                                    swiglu1(g[2 * i + 1], uu[2 * i + 1]));
+            stg.put<64>(tmO, wd, f0 + c, row0, 0, live);
+        }
+    } else if (p.out_kind == BI_OUT_BF16) {
+#pragma unroll
+        for (int c = 0; c < BN; c += 64) {
+            uint32_t wd[32];
+            float v[32];
+            tmem_ld_32cols(base + c, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                wd[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+            tmem_ld_32cols(base + c + 32, v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                wd[16 + i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+            stg.put<128>(tmO, wd, n0 + c, row0, 0, live && n0 + c < p.N);
+        }
+    } else {  // fp32: partial slice s (or the only slice)
+#pragma unroll
+        for (int c = 0; c < BN; c += 32) {
+            float v[32];
+            tmem_ld_32cols(base + c, v);
+            stg.put<128>(tmO, reinterpret_cast<const uint32_t *>(v), n0 + c,
+                         row0, p.out_kind == BI_OUT_PARTIALS ? s : 0,
+                         live && n0 + c < p.N);
+        }
+    }
+}
 
 template <int BN, bool ONE>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -264,58 +321,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++acc) {
             int m0, nt, s;
             unit_coords(p, u, m0, nt, s);
-            const int n0 = nt * BN;
             const int buf = acc % NACC;
             if (!mbar_wait(&acc_full[buf], (acc / NACC) & 1, p.status)) break;
             tc_fence_after();
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const int row0 = m0 + h * HALF + q * 32;
-                const bool live = row0 < p.M;
-                const uint32_t base = lane_addr + buf * T::ACC_COLS + h * BN;
-                if (p.out_kind == BI_OUT_SWIGLU) {
-                    // gate columns [0, w), up columns [w, 2w) of this tile
-                    const int f0 = nt * (BN / 2);
-                    const int w = min(BN / 2, p.F - f0);
-                    for (int c = 0; c < w; c += 32) {
-                        float g[32], uu[32];
-                        uint32_t wd[16];
-                        tmem_ld_32cols(base + c, g);
-                        tmem_ld_32cols(base + w + c, uu);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            wd[i] = pack_bf16x2(swiglu1(g[2 * i], uu[2 * i]),
-                                                swiglu1(g[2 * i + 1],
-                                                        uu[2 * i + 1]));
-                        stg.put<64>(&tmO, wd, f0 + c, row0, 0, live);
-                    }
-                } else if (p.out_kind == BI_OUT_BF16) {
-#pragma unroll
-                    for (int c = 0; c < BN; c += 64) {
-                        uint32_t wd[32];
-                        float v[32];
-                        tmem_ld_32cols(base + c, v);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            wd[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-                        tmem_ld_32cols(base + c + 32, v);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            wd[16 + i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-                        stg.put<128>(&tmO, wd, n0 + c, row0, 0,
-                                     live && n0 + c < p.N);
-                    }
-                } else {  // fp32: partial slice s (or the only slice)
-#pragma unroll
-                    for (int c = 0; c < BN; c += 32) {
-                        float v[32];
-                        tmem_ld_32cols(base + c, v);
-                        stg.put<128>(&tmO, reinterpret_cast<const uint32_t *>(v),
-                                     n0 + c, row0,
-                                     p.out_kind == BI_OUT_PARTIALS ? s : 0,
-                                     live && n0 + c < p.N);
-                    }
-                }
+                store_block<BN>(p, &tmO, stg,
+                                lane_addr + buf * T::ACC_COLS + h * BN, row0,
+                                nt, s, row0 < p.M);
             }
             tc_fence_before();
             __syncwarp();
@@ -329,6 +343,197 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------ CTA pairs --
+//
+// The same tile plan on pairs of SMs (a cluster of two CTAs): a unit is
+// (m-tile of 256 rows, pair n-tile of 2 BN columns, slice).  Per k-block
+// each CTA loads its own 128 rows of A and BN / 2 rows of each of the two
+// BN-column halves of the pair tile's W block; the even CTA issues, per
+// 16-column step, two tcgen05.mma.cta_group::2 (M = 256, N = BN), one per
+// half, and each CTA receives its 128 rows of D in its own tensor memory.
+// Against one CTA per 256 x BN tile, each SM loads (128 + BN) instead of
+// (256 + BN) rows per k-block for the same number of outputs.  The
+// reduction order of an output is the same chain of 16-column steps in
+// ascending k, so the result is a function of (N, K) and the inputs only.
+//
+// Barriers: the even CTA's full[st] counts both CTAs' bytes (the odd CTA's
+// loads complete on it through its shared::cluster address); empty[st] and
+// acc_full[] are signalled in both CTAs by the pair commit; acc_empty[] of
+// the even CTA collects the 8 epilogue warps of the pair.
+template <int BN, bool ONE>
+struct PairTile {
+    static constexpr int A_CTA = HALF * BK * 2;             // 16 KB
+    static constexpr int B_CTA = BN * BK * 2;               // 2 x BN/2 rows
+    static constexpr int B_HALF = (BN / 2) * BK * 2;
+    static constexpr int STAGE_BYTES = A_CTA + B_CTA;
+    static constexpr int EPI_OWN = ONE ? 0 : EPI_BYTES;
+    static constexpr int FIT =
+        (SMEM_LIMIT - EPI_OWN - 1024 - 256) / STAGE_BYTES;
+    static constexpr int STAGES = FIT < 8 ? FIT : 8;
+    static constexpr int ACC_COLS = 2 * BN;
+    static constexpr int NACC = TMEM_COLS / ACC_COLS;
+    static constexpr uint32_t IDESC = make_idesc_bf16(2 * HALF, BN);
+    static constexpr size_t SMEM =
+        1024 + (size_t)STAGES * STAGE_BYTES + EPI_OWN + 256;
+    static_assert(STAGES >= 2 && NACC >= 1, "pair tile does not fit");
+    static_assert(ONE ? STAGES * A_CTA >= EPI_BYTES : true,
+                  "staging in the A stages");
+};
+
+template <int BN, bool ONE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmO, GemmArgs p) {
+    using T = PairTile<BN, ONE>;
+    constexpr int STAGES = T::STAGES, NACC = T::NACC;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = smem;
+    uint8_t *sB = smem + STAGES * T::A_CTA;
+    uint8_t *sE = ONE ? sA : sB + STAGES * T::B_CTA;
+    uint64_t *full =
+        reinterpret_cast<uint64_t *>(sB + STAGES * T::B_CTA + T::EPI_OWN);
+    uint64_t *empty = full + STAGES;
+    uint64_t *acc_full = empty + STAGES;
+    uint64_t *acc_empty = acc_full + NACC;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(acc_empty + NACC);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < NACC; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 8);
+        }
+        mbar_fence_init();
+    }
+    cluster_sync_all();  // both CTAs' barriers exist before either signals
+    if (warp == 1) tmem_alloc_pair(tslot, TMEM_COLS);
+    tc_fence_before();
+    cluster_sync_all();  // both CTAs hold the tensor memory
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------------------------------------------- producer --
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        const uint32_t lead_full = mapa_rank(full, 0);
+        int it = 0;
+        bool ok = true;
+        for (int u = cid; u < p.units && ok; u += ncl) {
+            int m0, np, s;
+            unit_coords(p, u, m0, np, s);
+            const int kb1 = slice_lo(p, s + 1);
+            for (int kb = slice_lo(p, s); kb < kb1; ++kb, ++it) {
+                const int st = it % STAGES;
+                const uint32_t round = it / STAGES;
+                if (round > 0 &&
+                    !mbar_wait(&empty[st], (round - 1) & 1, p.status)) {
+                    ok = false;
+                    break;
+                }
+                if (rank == 0)
+                    mbar_arrive_expect_tx(&full[st], 2 * T::STAGE_BYTES);
+                const uint32_t bar = lead_full + st * 8;
+                tma_load_2d_pair(sA + st * T::A_CTA, &tmA, kb * BK,
+                                 m0 + (int)rank * HALF, bar);
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    tma_load_2d_pair(sB + st * T::B_CTA + j * T::B_HALF, &tmB,
+                                     kb * BK,
+                                     np * 2 * BN + j * BN + (int)rank * (BN / 2),
+                                     bar);
+            }
+        }
+        // The pair commits of the last stages have reached this CTA's
+        // empty barriers before it may leave.
+        for (int j = it > STAGES ? it - STAGES : 0; j < it; ++j)
+            mbar_wait(&empty[j % STAGES], (j / STAGES) & 1, p.status);
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+        // ---------------------------------------------------- pair MMA --
+        int it = 0, acc = 0;
+        bool ok = true;
+        for (int u = cid; u < p.units && ok; u += ncl, ++acc) {
+            int m0, np, s;
+            unit_coords(p, u, m0, np, s);
+            const int buf = acc % NACC;
+            if (acc >= NACC &&
+                !mbar_wait(&acc_empty[buf], ((acc / NACC) - 1) & 1,
+                           p.status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d = tmem + buf * T::ACC_COLS;
+            const int kb0 = slice_lo(p, s), kb1 = slice_lo(p, s + 1);
+            for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                const int st = it % STAGES;
+                if (!mbar_wait(&full[st], (it / STAGES) & 1, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a = smem_u32(sA + st * T::A_CTA);
+                const uint32_t b = smem_u32(sB + st * T::B_CTA);
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k) {
+                    const uint64_t ad = make_sw128_desc(a + 32 * k);
+                    const uint32_t accumulate = (kb > kb0 || k > 0) ? 1u : 0u;
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+                        tc_mma_pair_bf16(
+                            d + j * BN, ad,
+                            make_sw128_desc(b + j * T::B_HALF + 32 * k),
+                            T::IDESC, accumulate);
+                }
+                tc_commit_pair(&empty[st]);
+            }
+            if (ok) tc_commit_pair(&acc_full[buf]);
+        }
+    } else if (warp >= 2) {
+        // ---------------------------------------------------- epilogue --
+        const int q = warp & 3;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+        const uint32_t lead_acc_empty = mapa_rank(acc_empty, 0);
+        Stager stg{sE + (warp - 2) * 2 * STORE_BYTES, 0};
+        int acc = 0;
+        for (int u = cid; u < p.units; u += ncl, ++acc) {
+            int m0, np, s;
+            unit_coords(p, u, m0, np, s);
+            const int buf = acc % NACC;
+            if (!mbar_wait(&acc_full[buf], (acc / NACC) & 1, p.status)) break;
+            tc_fence_after();
+            const int row0 = m0 + (int)rank * HALF + q * 32;
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                store_block<BN>(p, &tmO, stg,
+                                lane_addr + buf * T::ACC_COLS + j * BN, row0,
+                                2 * np + j, s, row0 < p.M);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(lead_acc_empty + buf * 8);
+        }
+        if (lane == 0) bulk_wait<0>();  // stores done before the CTA exits
+    }
+
+    tc_fence_before();
+    __syncwarp();
+    cluster_sync_all();  // epilogues of both CTAs are done with the TMEM
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, TMEM_COLS);
     }
 }
 
@@ -397,34 +602,59 @@ bi_status set_smem_attr() {
     return bi_cuda_check(err, "gemm smem attribute");
 }
 
+template <int BN, bool ONE>
+bi_status set_pair_smem_attr() {
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute(gemm_pair_kernel<BN, ONE>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)PairTile<BN, ONE>::SMEM);
+    });
+    return bi_cuda_check(err, "gemm pair smem attribute");
+}
+
 struct Plan {
     int bn, s;
+    bool pair;  // CTA pairs (2 BN columns per unit) instead of single CTAs
 };
 
-// (BN, S) for a weight of shape [N][K], from a time model of a 256-row
-// batch on a 152-SM GPU: the busiest SM loads waves * (256 + BN) * 128 *
-// ceil(KB / S) bytes at ~85 GB/s (waves = ceil(tiles * S / 152)), and for
-// S > 1 the S fp32 partial planes are written once and read once at
-// ~6 TB/s.  BN in {128, 192, 256}, S in 1 .. min(8, KB / 4); ties go to the
-// smaller S, then the smaller BN.  The model only ranks plans: any plan
-// gives M-invariant results, and the plan depends on (N, K) alone.
+// (BN, S, pair) for a weight of shape [N][K], from a time model of a
+// 256-row batch on 152 SMs calibrated on GB300 with a sweep of every plan
+// for the 8B projection shapes.  Per 64-column k-block an SM spends the
+// longer of its loads, R rows x 128 B at 112 GB/s (R = 256 + BN for a
+// single CTA, 128 + BN for a CTA of a pair), and its MMAs, 256 x BN x 64
+// multiply-adds at 12.5 TFLOP/s (so BN = 128 is load-bound alone and
+// MMA-bound in a pair, BN >= 192 MMA-bound either way).  The busiest SM
+// runs waves * ceil(KB / S) k-blocks (waves = ceil(CTAs / 152)); a pair
+// launch costs 6 us more (cluster set-up and teardown), and S > 1 adds
+// 0.44 us per MB of fp32 partial planes (written once, read once).
+// BN in {128, 192, 256}, S in 1 .. min(8, KB / 4); ties go to the smaller
+// S, the smaller BN, then single CTAs.  Any plan gives M-invariant
+// results, and the plan depends on (N, K) alone.
 Plan gemm_plan(int N, int K) {
     const int KB = (K + BK - 1) / BK;
     const int smax = std::max(1, std::min(MAX_SPLITS, KB / 4));
-    Plan best{128, 1};
+    Plan best{128, 1, false};
     double best_us = -1.0;
     for (int s = 1; s <= smax; ++s) {
         for (int bn : {128, 192, 256}) {
-            const int64_t units = (int64_t)((N + bn - 1) / bn) * s;
-            const int64_t waves = (units + PLAN_SMS - 1) / PLAN_SMS;
-            const double load_us = (double)waves * (256 + bn) * 128.0 *
-                                   ((KB + s - 1) / s) / 85e3;
-            const double part_us =
-                s > 1 ? 2.0 * s * 256.0 * N * 4.0 / 6e6 : 0.0;
-            const double us = load_us + part_us;
-            if (best_us < 0 || us < best_us) {
-                best_us = us;
-                best = {bn, s};
+            for (int pair = 0; pair < 2; ++pair) {
+                const int64_t cols = pair ? 2 * bn : bn;
+                const int64_t units = (int64_t)((N + cols - 1) / cols) * s;
+                const int64_t ctas = pair ? 2 * units : units;
+                const int64_t waves = (ctas + PLAN_SMS - 1) / PLAN_SMS;
+                const double rows = pair ? HALF + bn : BM + bn;
+                const double t_kb = std::max(rows * 128.0 / 112e3,
+                                             256.0 * bn * 64 * 2 / 12.5e6);
+                const double us =
+                    (double)waves * ((KB + s - 1) / s) * t_kb +
+                    (pair ? 6.0 : 0.0) +
+                    (s > 1 ? 0.44 * s * 256.0 * N * 4.0 / 1e6 : 0.0);
+                if (best_us < 0 || us < best_us) {
+                    best_us = us;
+                    best = {bn, s, pair != 0};
+                }
             }
         }
     }
@@ -448,6 +678,28 @@ bi_status launch(const CUtensorMap &ta, const CUtensorMap &tb,
             <<<grid, THREADS, Tile<BN, false>::SMEM, stream>>>(ta, tb, to, a);
     }
     BI_LAUNCH_CHECK("gemm launch");
+    return BI_OK;
+}
+
+template <int BN>
+bi_status launch_pair(const CUtensorMap &ta, const CUtensorMap &tb,
+                      const CUtensorMap &to, const GemmArgs &a,
+                      cudaStream_t stream) {
+    const int pairs = std::min(a.units, bi_sm_count() / 2);
+    if (a.units <= pairs) {  // one unit per pair
+        bi_status st = set_pair_smem_attr<BN, true>();
+        if (st != BI_OK) return st;
+        gemm_pair_kernel<BN, true>
+            <<<2 * pairs, THREADS, PairTile<BN, true>::SMEM, stream>>>(
+                ta, tb, to, a);
+    } else {
+        bi_status st = set_pair_smem_attr<BN, false>();
+        if (st != BI_OK) return st;
+        gemm_pair_kernel<BN, false>
+            <<<2 * pairs, THREADS, PairTile<BN, false>::SMEM, stream>>>(
+                ta, tb, to, a);
+    }
+    BI_LAUNCH_CHECK("gemm pair launch");
     return BI_OK;
 }
 
@@ -491,13 +743,18 @@ extern "C" bi_status bi_gemm(const bi_bf16 *x, int M, int K, const bi_bf16 *W,
     const Plan plan = gemm_plan(N, K);
     const int S = plan.s, BN = plan.bn;
     const int KB = (K + BK - 1) / BK;
-    const int mt = (M + BM - 1) / BM, nt = (N + BN - 1) / BN;
+    // n-tiles: BN columns, or 2 BN per CTA pair
+    const int cols = plan.pair ? 2 * BN : BN;
+    const int mt = (M + BM - 1) / BM, nt = (N + cols - 1) / cols;
 
+    // A boxes: 256 rows per CTA, or 128 per CTA of a pair; W boxes: BN
+    // rows, or BN / 2 per CTA of a pair and half of the pair tile
     CUtensorMap ta, tb, to;
-    bi_status st = bi_make_tmap_2d_bf16(&ta, x, K, M, (uint64_t)K * 2, BK, BM,
-                                        true);
+    bi_status st = bi_make_tmap_2d_bf16(&ta, x, K, M, (uint64_t)K * 2, BK,
+                                        plan.pair ? HALF : BM, true);
     if (st != BI_OK) return st;
-    st = bi_make_tmap_2d_bf16(&tb, W, K, N, (uint64_t)K * 2, BK, BN, true);
+    st = bi_make_tmap_2d_bf16(&tb, W, K, N, (uint64_t)K * 2, BK,
+                              plan.pair ? BN / 2 : BN, true);
     if (st != BI_OK) return st;
 
     GemmArgs a;
@@ -538,12 +795,21 @@ extern "C" bi_status bi_gemm(const bi_bf16 *x, int M, int K, const bi_bf16 *W,
         st = bi_make_tmap_3d(&to, dst, false, N / 2, M, 1, 32, 32, false);
     if (st != BI_OK) return st;
 
-    if (BN == 128)
-        st = launch<128>(ta, tb, to, a, stream);
-    else if (BN == 192)
-        st = launch<192>(ta, tb, to, a, stream);
-    else
-        st = launch<256>(ta, tb, to, a, stream);
+    if (plan.pair) {
+        if (BN == 128)
+            st = launch_pair<128>(ta, tb, to, a, stream);
+        else if (BN == 192)
+            st = launch_pair<192>(ta, tb, to, a, stream);
+        else
+            st = launch_pair<256>(ta, tb, to, a, stream);
+    } else {
+        if (BN == 128)
+            st = launch<128>(ta, tb, to, a, stream);
+        else if (BN == 192)
+            st = launch<192>(ta, tb, to, a, stream);
+        else
+            st = launch<256>(ta, tb, to, a, stream);
+    }
     if (st != BI_OK) return st;
     if (need_reduce) {
         if (out_kind == BI_OUT_SWIGLU) {

@@ -87,7 +87,9 @@ bi_status bi_device_status(int32_t *h_status, void *stream);
  *   BI_OUT_BF16      bf16 [M][N]: as F32, rounded to nearest even.
  *   BI_OUT_SWIGLU    bf16 [M][N/2]: W holds gate and up rows interleaved
  *                    as bi_pack_gate_up writes them; out = silu(g) * u with
- *                    silu(g) = g / (1 + e^-g) in fp32 on the slice sums.
+ *                    silu(g) = g / (1 + e^-g) in fp32 on the slice sums
+ *                    (fast exponential and division: within one bf16 ulp
+ *                    of bi_swiglu on the same sums).
  *                    N must be a multiple of 64; needs the workspace if
  *                    S > 1.
  */

@@ -46,11 +46,14 @@ def randn_bf16(shape, seed, std=1.0):
 
 @pytest.mark.parametrize("M,N,K", [(1, 128, 64), (5, 384, 512),
                                    (130, 256, 1024), (300, 200, 136),
-                                   (257, 1000, 264)])
+                                   (257, 1000, 264), (300, 40000, 64),
+                                   (3, 14336, 4096)])
 def test_exact_on_small_integers(bi, M, N, K):
     """Integer data keeps every partial sum exact, so any correct summation
     order gives exactly the integer product (catches a transposed operand,
-    a wrong tile offset or a dropped k-block)."""
+    a wrong tile offset or a dropped k-block).  (300, 40000, 64) runs
+    several units per CTA over two m-tiles; (3, 14336, 4096) takes CTA
+    pairs."""
     g = torch.Generator().manual_seed(M * 7 + N + K)
     xi = torch.randint(-4, 5, (M, K), generator=g)
     wi = torch.randint(-4, 5, (N, K), generator=g)
@@ -166,13 +169,15 @@ def _swiglu_via_f32(bi, orc, x, wgu, F):
     return orc.bf16_bits(orc.swiglu(g, u)).astype(np.int32)
 
 
-@pytest.mark.parametrize("F,K,M", [(14336, 4096, 5), (256, 4096, 70)])
+@pytest.mark.parametrize("F,K,M", [(14336, 4096, 5), (256, 4096, 70),
+                                   (20480, 128, 300)])
 def test_swiglu_tile_interleave(bi, orc, F, K, M):
     """The 8B gate/up shape (192-column tiles: 96 features per tile and a
-    last tile of 32) and a shape with 8 K slices (partials reduced by the
-    second-stage kernel): bi_pack_gate_up's interleave and the SwiGLU
-    epilogue agree with the de-interleaved F32 GEMM to one bf16 ulp (the
-    last bit of expf)."""
+    last tile of 32), a shape with 8 K slices (partials reduced by the
+    second-stage kernel) and a wide, shallow one with several units per CTA
+    over two m-tiles: bi_pack_gate_up's interleave and the SwiGLU epilogue
+    agree with the de-interleaved F32 GEMM to one bf16 ulp (the last bit of
+    the fast exponential and division)."""
     x = randn_bf16((M, K), 61)
     wg = randn_bf16((F, K), 62, 0.02)
     wu = randn_bf16((F, K), 63, 0.02)
