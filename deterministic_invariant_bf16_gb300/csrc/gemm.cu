@@ -16,13 +16,15 @@
 //   - slices are summed in fp32 in slice order ((p0 + p1) + p2) + ... by
 //     the consumer (bi_rmsnorm, bi_rope, or the reduce kernels here).
 //
-// Why 256-row tiles: on GB300 one SM ingests TMA loads at about 41 bytes
-// per clock whatever the box shape or the number of stages in flight
-// (measured with a load-only ring), so the projection GEMMs of a decode
-// batch are bound by the bytes each SM loads, (256 + BN) * 128 per k-block
-// here against 256 * 128 for 128 x 128 tiles: 1.3-1.75x fewer bytes per
-// multiply-add.  The plan picks BN and S to fill the 152 SMs with as few
-// bytes per SM as it can, counting the traffic of the fp32 partials.
+// Why 256-row tiles: a decode batch (M <= 256) is one m-tile, so every W
+// tile is loaded once for all rows, and per k-block an SM loads (256 + BN)
+// rows of 128 B for 256 x BN x 64 multiply-adds.  Measured on GB300 an SM
+// ingests about 112 GB/s and multiplies at about 12.5 TFLOP/s, so BN = 128
+// is load-bound and BN >= 192 tensor-bound in steady state; the rest of a
+// decode GEMM is fixed cost per launch (prologue, pipeline fill, epilogue:
+// eight epilogue warps instead of four measured no faster).  gemm_plan
+// ranks (BN, S, CTA pairs) by a time model calibrated on a sweep of every
+// plan for the 8B projection shapes.
 //
 // Persistent CTAs (one per SM, 192 threads) loop over work units (m-tile,
 // n-tile, slice), the m-tile fastest: warp 0 lane 0 issues TMA loads into a
