@@ -56,6 +56,10 @@ def parse():
     ap.add_argument("--no-comparator", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--report", action="store_true",
+                    help="instead of the step benchmark: decode tok/s over "
+                         "batch sizes 1..256 and invariant prefill tok/s on "
+                         "a sample of long prompts (one JSON line)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the decode iterations one call at a time "
                          "instead of replaying them as one CUDA graph")
@@ -190,7 +194,7 @@ def aggregate(ms_local, tokens_per_step_per_rank, world, dist=None,
 # --------------------------------------------------------------- our arm ----
 
 class Bench:
-    def __init__(self, args, device):
+    def __init__(self, args, device, weights=None):
         import torch
         from deterministic_invariant_bf16_gb300 import binding as bi
         from deterministic_invariant_bf16_gb300 import engine, synth
@@ -204,8 +208,8 @@ class Bench:
         ctx = wl["ctx"]
         max_kv = int(ctx.max()) + wl["headroom"]
         need = int(sum(-(-(int(c) + wl["headroom"]) // 16) for c in ctx))
-        self.weights = synth.make_weights(self.shape, 4, device,
-                                          n_layers=args.layers)
+        self.weights = weights if weights is not None else \
+            synth.make_weights(self.shape, 4, device, n_layers=args.layers)
         self.eng = engine.Engine(self.shape, self.weights, max_tokens=256,
                                  max_kv_len=max_kv, n_slots=B,
                                  n_pages=need + 64, page_seed=5)
@@ -362,6 +366,96 @@ def gemm_flops(b, cls):
         return None
     N, K = dims[cls]
     return 2.0 * B * N * K
+
+
+def verify_stats(b, ms):
+    """The step's grouped verification: windows, rollbacks (windows cut
+    before their end), candidates recomputed (those after the first
+    mismatch) and the committed output rate of the step (decoded tokens of
+    the unverified rows plus the committed tokens of the verified ones)."""
+    wl = b.wl
+    w = wl["window"]
+    commit = [int(x) for x in b.commits[-1][1]]
+    committed = sum(commit)
+    recomputed = sum(w - j for j in commit)
+    out_tokens = (wl["batch"] - wl["n_ver"]) * wl["iters"] + committed
+    return {"windows": len(commit), "window": w,
+            "rollbacks": sum(1 for j in commit if j < w),
+            "committed": committed, "recomputed": recomputed,
+            "recompute_fraction": recomputed / float(len(commit) * w),
+            "committed_tok_s": out_tokens / (ms / 1000.0)}
+
+
+def run_report(args):
+    """Decode tok/s over batch sizes (the same step workload at each B,
+    decode iterations replayed as a CUDA graph, no verify) and invariant
+    prefill tok/s on long prompts (8 requests, prompts U[4096, 8192], each
+    prefilled in 2048-token pieces).  Synthetic inputs, random weights."""
+    import copy
+    import torch
+    from deterministic_invariant_bf16_gb300 import binding as bi
+    from deterministic_invariant_bf16_gb300 import build, engine, synth
+    build.build()
+    bi.lib()
+    dev = "cuda:0"
+    torch.cuda.set_device(0)
+    shape = synth.LLAMA8B
+    W = synth.make_weights(shape, 4, dev, n_layers=args.layers)
+    rep = {"decode_tok_s": {}, "layers": args.layers}
+    for B in (1, 8, 32, 64, 128, 256):
+        a = copy.copy(args)
+        a.batch = B
+        b = Bench(a, dev, weights=W)
+        b.capture()
+        for _ in range(3):
+            b.graph.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            b.graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        rep["decode_tok_s"][str(B)] = B * b.wl["iters"] / (ms / 1000.0)
+        del b
+        torch.cuda.empty_cache()
+    # prefill
+    rng = np.random.default_rng(1005)
+    R, piece = 8, 2048
+    prompts = rng.integers(4096, 8193, size=R)
+    max_kv = int(prompts.max()) + 16
+    need = int(sum(-(-int(p) // 16) for p in prompts)) + 64
+    eng = engine.Engine(shape, W, max_tokens=piece, max_kv_len=max_kv,
+                        n_slots=R, n_pages=need, page_seed=7)
+    for r in range(R):
+        eng.reserve(r, int(prompts[r]))
+    toks = [synth.token_ids(int(p), shape.vocab, rng) for p in prompts]
+    logits = torch.empty(piece, shape.vocab, dtype=torch.float32, device=dev)
+
+    def prefill_all():
+        for r in range(R):
+            for p0 in range(0, int(prompts[r]), piece):
+                t = toks[r][p0:p0 + piece]
+                eng.prefill([(r, t, p0)], logits=logits[:len(t)])
+
+    prefill_all()  # warm-up
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    prefill_all()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    rep["prefill"] = {"tok_s": float(prompts.sum()) / (ms / 1000.0),
+                      "requests": R, "tokens": int(prompts.sum()),
+                      "piece": piece, "ms": ms}
+    rep["device_status"] = bi.bi_device_status()
+    print(json.dumps({"report": rep, "workload": WORKLOAD,
+                      "data": "synthetic (random-init weights, random KV)"}),
+          flush=True)
 
 
 def run_ours(args):
@@ -529,6 +623,7 @@ def run_ours(args):
         "clocks": clk,
         "device_status": status,
         "verify_commits": [int(x) for x in b.commits[-1][1]],
+        "verify": verify_stats(b, ms),
     }
     if rank == 0 and not args.no_comparator:
         line["comparator"] = run_comparator(b, args)
@@ -746,6 +841,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.report:
+        run_report(args)
     else:
         run_ours(args)
 
