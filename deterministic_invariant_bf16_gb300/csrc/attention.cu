@@ -1047,7 +1047,9 @@ __device__ __forceinline__ int v_load(int n) { return 2 * n + 1; }
 //               (two P tiles, two O buffers);
 //   warp 9      producer: page ids -> TMA boxes (K only for visible pages,
 //               V for all 16 pages, missing ones as zero-filled boxes);
-//   warp 10     asks L2 for the K/V pages of the next items.
+//   warp 10     asks L2 for the K/V pages of the item after the one the
+//               producer loads next (one item ahead: 1% faster than two,
+//               9% faster than four or none).
 __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap,
@@ -1118,9 +1120,9 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
         for (int n = 0; n < n_items; ++n) {
             const int i = blockIdx.x + n * gridDim.x;
             bool go = true;
-            if (lane == 0 && *progress + 2 < n) {
+            if (lane == 0 && *progress + 1 < n) {
                 const uint64_t t0 = bi_globaltimer();
-                while (*progress + 2 < n) {
+                while (*progress + 1 < n) {
                     __nanosleep(256);
                     if (bi_globaltimer() - t0 > BI_WAIT_LIMIT_NS) {
                         go = false;
