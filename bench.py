@@ -322,13 +322,10 @@ def algorithmic_bytes(b, cls, launches_per_step):
     ctx = wl["ctx"]
     bi = b.bi
     if cls == "attn":
-        # decode chunk kernel: K and V of every visible position, the
-        # queries, and one (m, l, o) partial per (row, head, chunk)
+        # decode attention (chunks merged in registers): K and V of every
+        # visible position, the queries in and the outputs out
         kv = sum(float((ctx + i + 1).sum()) for i in range(it)) / it
-        chunks = sum(float(np.ceil((ctx + i + 1) / 256).sum())
-                     for i in range(it)) / it
-        return (kv * Hkv * D * 2 * 2 + B * Hq * D * 2 +
-                chunks * Hq * (D + 4) * 4)
+        return kv * Hkv * D * 2 * 2 + 2 * B * Hq * D * 2
     if cls == "attn_merge":
         chunks = sum(float(np.ceil((ctx + i + 1) / 256).sum())
                      for i in range(it)) / it

@@ -1036,39 +1036,150 @@ __device__ __forceinline__ int v_load(int n) { return 2 * n + 1; }
 
 }  // namespace tca
 
-// Persistent decode chunk kernel on the tensor cores (head_dim 128).  CTA k
-// takes items k, k + grid, ...; item i is KV head i % Hkv of list entry
-// i / Hkv.  The ring loads K0 V0 K1 V1 ..., load j in slot j mod RING
-// (k_load / v_load below).
-//   warps 0-7   softmax and epilogue (thread t <-> key t of the chunk);
-//   warp 8      owns the tensor memory; lane 0 issues the MMAs: S^T of item
-//               n + 2 is issued as soon as item n's softmax has read S^T
-//               (two S buffers), O^T of item n once its P tile is written
+// Work list of the tensor-core decode kernel: the valid rows (row_req >= 0,
+// 0 < kv_len <= Cmax * 256) as (row, kv_len), most chunks first (ties by
+// row), then the other rows as (row, 0); prefix[B] = number of valid rows.
+// One block; every thread ranks its rows against all rows (keys compared in
+// shared-memory tiles), an exact and order-free computation.
+__global__ void build_rows_kernel(const int32_t *__restrict__ kv_len,
+                                  const int32_t *__restrict__ row_req, int B,
+                                  int Cmax, int32_t *__restrict__ prefix,
+                                  int2 *__restrict__ rows) {
+    constexpr int TILE = 2048;
+    __shared__ int skey[TILE];
+    __shared__ int nvalid;
+    const int tid = threadIdx.x;
+    auto key_of = [&](int b) {
+        const int L = kv_len[b];
+        return row_req[b] >= 0 && L > 0 && L <= Cmax * CHUNK
+                   ? (L + CHUNK - 1) / CHUNK
+                   : 0;
+    };
+    if (tid == 0) nvalid = 0;
+    for (int b0 = 0; b0 < B; b0 += blockDim.x) {
+        const int b = b0 + tid;
+        const int kb = b < B ? key_of(b) : -1;
+        int rank = 0;
+        for (int t0 = 0; t0 < B; t0 += TILE) {
+            const int n = min(TILE, B - t0);
+            __syncthreads();
+            for (int i = tid; i < n; i += blockDim.x) skey[i] = key_of(t0 + i);
+            __syncthreads();
+            if (b < B)
+                for (int i = 0; i < n; ++i) {
+                    const int k = skey[i];
+                    rank += k > kb || (k == kb && t0 + i < b);
+                }
+        }
+        if (b < B) {
+            rows[rank] = make_int2(b, kb > 0 ? kv_len[b] : 0);
+            if (kb > 0) atomicAdd(&nvalid, 1);
+        }
+    }
+    __syncthreads();
+    if (tid == 0) prefix[B] = nvalid;
+}
+
+namespace tca {
+
+__device__ __forceinline__ int warp_sum_int(int v) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Item n (0, 1, ...) of CTA k out of `grid`: the item list is walked in
+// rounds of `grid` items, the CTA order reversed every other round, so the
+// long rows at the front spread evenly over the CTAs.
+__device__ __forceinline__ int item_of(int n, int k, int grid) {
+    return n * grid + ((n & 1) ? grid - 1 - k : k);
+}
+
+// The units (chunks) of this CTA in order: item r of the CTA is KV head
+// j % Hkv of sorted row j / Hkv (j = item_of(r)); its units are chunks
+// 0 .. C - 1, C = ceil(kv_len / 256).  Every role walks the same sequence;
+// the next item's entry is loaded one item ahead.
+struct UnitWalk {
+    const int2 *rows;
+    int total, Hkv;
+    int r, c, C, b, L, g;  // current unit
+    int nb, nL, ng;        // next item
+    bool nok;
+
+    __device__ bool load(int rr, int &b_, int &L_, int &g_) const {
+        const int j = item_of(rr, blockIdx.x, gridDim.x);
+        if (j >= total) return false;
+        const int2 e = rows[j / Hkv];
+        b_ = e.x;
+        L_ = e.y;
+        g_ = j % Hkv;
+        return true;
+    }
+    __device__ bool begin() {
+        r = c = 0;
+        if (!load(0, b, L, g)) return false;
+        C = (L + CHUNK - 1) / CHUNK;
+        nok = load(1, nb, nL, ng);
+        return true;
+    }
+    __device__ bool next() {
+        if (++c < C) return true;
+        if (!nok) return false;
+        ++r;
+        c = 0;
+        b = nb;
+        L = nL;
+        g = ng;
+        C = (L + CHUNK - 1) / CHUNK;
+        nok = load(r + 1, nb, nL, ng);
+        return true;
+    }
+    __device__ int vl() const { return min(CHUNK, L - c * CHUNK); }
+};
+
+}  // namespace tca
+
+// Persistent decode kernel on the tensor cores (head_dim 128).  CTA k takes
+// whole (row, KV head) items (UnitWalk) and streams their 256-position
+// chunks through the pipeline in order; the chunk partials are merged in
+// registers in chunk order with the merge functions of the two-stage path,
+// as the prefill kernel does, and the last chunk of an item writes the
+// item's G output rows.  The ring loads K0 V0 K1 V1 ... over the units,
+// load j in slot j mod RING (k_load / v_load).
+//   warps 0-7   softmax (thread t <-> key t of the chunk); warps 0-3 also
+//               keep the running (m, l, o) of the item's rows for their dim
+//               and write the output;
+//   warp 8      owns the tensor memory; lane 0 issues the MMAs: S^T of unit
+//               n + 2 is issued as soon as unit n's softmax has read S^T
+//               (two S buffers), O^T of unit n once its P tile is written
 //               (two P tiles, two O buffers);
 //   warp 9      producer: page ids -> TMA boxes (K only for visible pages,
 //               V for all 16 pages, missing ones as zero-filled boxes);
-//   warp 10     asks L2 for the K/V pages of the item after the one the
-//               producer loads next (one item ahead: 1% faster than two,
-//               9% faster than four or none).
+//   warp 10     asks L2 for the K/V pages of the unit after the one the
+//               producer loads next (one ahead: 1% faster than two, 9%
+//               faster than four or none).
+// Rows outside the work list (no request, or a context out of range) get
+// zero outputs.
 __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap,
                      const __grid_constant__ CUtensorMap qmap,
                      const int32_t *__restrict__ page_table, int max_pages,
                      int n_pages, const int32_t *__restrict__ row_req,
-                     const int32_t *__restrict__ kv_len, int Hq, int Hkv,
-                     int G, float scale, float *__restrict__ ws, int Cmax,
+                     int Hq, int Hkv, int G, float scale,
                      const int32_t *__restrict__ prefix, int B,
-                     const int2 *__restrict__ items,
+                     const int2 *__restrict__ rows,
                      const bi_bf16 *__restrict__ k_pool,
-                     const bi_bf16 *__restrict__ v_pool, int32_t *status) {
+                     const bi_bf16 *__restrict__ v_pool,
+                     uint16_t *__restrict__ out, int32_t *status) {
     using namespace tca;
     constexpr int D = 128;
     constexpr int PAGE_BYTES = 16 * 64 * 2;   // one box: 16 rows x 64 dims
     constexpr int HALF_TILE = CHUNK * 128;
     constexpr int HALF_Q = 16 * 128;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ int s_progress;  // items the producer has issued
+    __shared__ int s_progress;  // units the producer has issued
+    __shared__ int s_units;     // units of this CTA
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t base = smem_u32(smem);
@@ -1081,10 +1192,8 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
     uint64_t *o_empty = o_full + 2;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(o_empty + 2);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int total = prefix[B] * Hkv;
-    int n_items = 0;  // items of this CTA
-    if ((int)blockIdx.x < total)
-        n_items = (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1;
+    const int n_valid = prefix[B];
+    const int total = n_valid * Hkv;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < RING; ++i) {
@@ -1107,44 +1216,57 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
             reinterpret_cast<uint4 *>(smem + DecL::P)[i] = make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
     }
+    if (warp == SW + 2) {
+        // units of this CTA: the chunk counts of its items, one round per
+        // lane (round r's item index is at least r * grid)
+        int sum = 0;
+        for (int r0 = 0; r0 * (int)gridDim.x < total; r0 += 32) {
+            const int j = item_of(r0 + lane, blockIdx.x, gridDim.x);
+            const int C = j < total ? (rows[j / Hkv].y + CHUNK - 1) / CHUNK : 0;
+            sum += warp_sum_int(C);
+        }
+        if (lane == 0) s_units = sum;
+    }
     if (warp == SW) tmem_alloc(tslot, 128);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
     volatile int *progress = &s_progress;
+    const int n_units = s_units;
 
     if (warp == SW + 2) {
         // ------------------------------------------------------ prefetch --
         constexpr uint32_t PAGE_KV = 16 * D * 2;
-        for (int n = 0; n < n_items; ++n) {
-            const int i = blockIdx.x + n * gridDim.x;
-            bool go = true;
-            if (lane == 0 && *progress + 1 < n) {
-                const uint64_t t0 = bi_globaltimer();
-                while (*progress + 1 < n) {
-                    __nanosleep(256);
-                    if (bi_globaltimer() - t0 > BI_WAIT_LIMIT_NS) {
-                        go = false;
-                        break;
+        UnitWalk w{rows, total, Hkv};
+        if (w.begin()) {
+            int req = row_req[w.b];
+            for (int n = 0;; ++n) {
+                bool go = true;
+                if (lane == 0 && *progress + 1 < n) {
+                    const uint64_t t0 = bi_globaltimer();
+                    while (*progress + 1 < n) {
+                        __nanosleep(256);
+                        if (bi_globaltimer() - t0 > BI_WAIT_LIMIT_NS) {
+                            go = false;
+                            break;
+                        }
                     }
                 }
-            }
-            if (!__shfl_sync(0xffffffffu, go ? 1 : 0, 0)) break;
-            const int g = i % Hkv;
-            const int2 bc = items[i / Hkv];
-            const int vl = min(CHUNK, kv_len[bc.x] - bc.y * CHUNK);
-            if (lane < ((vl + 15) >> 4)) {
-                const int pi = bc.y * 16 + lane;
-                const int pg = pi < max_pages
-                                   ? page_table[(int64_t)row_req[bc.x] *
-                                                    max_pages + pi]
-                                   : -1;
-                if (pg >= 0 && pg < n_pages) {
-                    const int64_t off = ((int64_t)pg * Hkv + g) * 16 * D;
-                    prefetch_l2_bulk(k_pool + off, PAGE_KV);
-                    prefetch_l2_bulk(v_pool + off, PAGE_KV);
+                if (!__shfl_sync(0xffffffffu, go ? 1 : 0, 0)) break;
+                if (lane < ((w.vl() + 15) >> 4)) {
+                    const int pi = w.c * 16 + lane;
+                    const int pg = pi < max_pages
+                                       ? page_table[(int64_t)req * max_pages + pi]
+                                       : -1;
+                    if (pg >= 0 && pg < n_pages) {
+                        const int64_t off = ((int64_t)pg * Hkv + w.g) * 16 * D;
+                        prefetch_l2_bulk(k_pool + off, PAGE_KV);
+                        prefetch_l2_bulk(v_pool + off, PAGE_KV);
+                    }
                 }
+                if (!w.next()) break;
+                if (w.c == 0) req = row_req[w.b];
             }
         }
         return;
@@ -1158,56 +1280,66 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
             tma_prefetch_desc(&qmap);
         }
         bool ok = true;
-        // load t of the sequence: the K (t even) or V (t odd) of item t / 2
-        for (int t = 0; t < 2 * n_items && ok; ++t) {
-            const bool is_k = (t & 1) == 0;
-            const int n = t >> 1;
-            const int i = blockIdx.x + n * gridDim.x;
-            const int g = i % Hkv;
-            const int2 bc = items[i / Hkv];
-            const int b = bc.x, c = bc.y;
-            const int vl = min(CHUNK, kv_len[b] - c * CHUNK);
-            const int npg = (vl + 15) >> 4;
-            const int32_t *pt_row = page_table + (int64_t)row_req[b] * max_pages;
-            int pg = -1;
-            if (lane < npg) {
-                const int pi = c * 16 + lane;
-                pg = pi < max_pages ? pt_row[pi] : -1;
-                if (pg < 0 || pg >= n_pages) {
-                    if (is_k) bi_record_error(status, BI_ERR_BOUNDS);
-                    pg = -1;
+        UnitWalk w{rows, total, Hkv};
+        if (w.begin()) {
+            // page-table rows of the current and the next item
+            int req = row_req[w.b];
+            int nreq = w.nok ? row_req[w.nb] : 0;
+            for (int n = 0; ok; ++n) {
+                const int b = w.b, c = w.c, g = w.g;
+                const int npg = (w.vl() + 15) >> 4;
+                const int32_t *pt_row = page_table + (int64_t)req * max_pages;
+                int pg = -1;
+                if (lane < npg) {
+                    const int pi = c * 16 + lane;
+                    pg = pi < max_pages ? pt_row[pi] : -1;
+                    if (pg < 0 || pg >= n_pages) {
+                        bi_record_error(status, BI_ERR_BOUNDS);
+                        pg = -1;
+                    }
                 }
-            }
-            const int nvalid = __popc(__ballot_sync(0xffffffffu, pg >= 0));
-            const int slot = t % RING;
-            const int use = t / RING;
-            bool w_ok = true;
-            if (lane == 0 && use > 0)
-                w_ok = mbar_wait(&empty[slot], (use - 1) & 1, status);
-            ok = __shfl_sync(0xffffffffu, w_ok ? 1 : 0, 0) != 0;
-            if (!ok) break;
-            // K: the visible pages (+ Q).  V: all 16 pages, the ones
-            // without data as boxes wholly above row 0 (zero-filled).
-            if (lane == 0)
-                mbar_arrive_expect_tx(&full[slot],
-                                      is_k ? nvalid * 2 * PAGE_BYTES + 2 * HALF_Q
-                                           : 16 * 2 * PAGE_BYTES);
-            __syncwarp();
-            uint8_t *tile = smem + DecL::SLOT + slot * DecL::TB;
-            if (lane < 16 && (!is_k || pg >= 0)) {
-                const int row = pg >= 0 ? (pg * Hkv + g) * 16 : -16;
-                const CUtensorMap *map = is_k ? &kmap : &vmap;
+                const int nvalid = __popc(__ballot_sync(0xffffffffu, pg >= 0));
+                // K (+ Q): the visible pages.  V: all 16 pages, the ones
+                // without data as boxes wholly above row 0 (zero-filled).
+                for (int kv = 0; kv < 2 && ok; ++kv) {
+                    const int t = 2 * n + kv;
+                    const int slot = t % RING;
+                    const int use = t / RING;
+                    bool w_ok = true;
+                    if (lane == 0 && use > 0)
+                        w_ok = mbar_wait(&empty[slot], (use - 1) & 1, status);
+                    ok = __shfl_sync(0xffffffffu, w_ok ? 1 : 0, 0) != 0;
+                    if (!ok) break;
+                    if (lane == 0)
+                        mbar_arrive_expect_tx(&full[slot],
+                                              kv == 0 ? nvalid * 2 * PAGE_BYTES +
+                                                            2 * HALF_Q
+                                                      : 16 * 2 * PAGE_BYTES);
+                    __syncwarp();
+                    uint8_t *tile = smem + DecL::SLOT + slot * DecL::TB;
+                    if (lane < 16 && (kv == 1 || pg >= 0)) {
+                        const int row = pg >= 0 ? (pg * Hkv + g) * 16 : -16;
+                        const CUtensorMap *map = kv == 0 ? &kmap : &vmap;
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
-                    tma_load_2d(tile + h * HALF_TILE + lane * PAGE_BYTES, map,
-                                h * 64, row, &full[slot]);
-            }
-            if (is_k && lane == 0) {
+                        for (int h = 0; h < 2; ++h)
+                            tma_load_2d(tile + h * HALF_TILE + lane * PAGE_BYTES,
+                                        map, h * 64, row, &full[slot]);
+                    }
+                    if (kv == 0 && lane == 0) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
-                    tma_load_2d(smem + DecL::QSLOT + slot * DecL::QB + h * HALF_Q,
-                                &qmap, h * 64, b * Hq + g * G, &full[slot]);
-                *progress = n + 1;
+                        for (int h = 0; h < 2; ++h)
+                            tma_load_2d(smem + DecL::QSLOT + slot * DecL::QB +
+                                            h * HALF_Q,
+                                        &qmap, h * 64, b * Hq + g * G,
+                                        &full[slot]);
+                        *progress = n + 1;
+                    }
+                }
+                if (!ok || !w.next()) break;
+                if (w.c == 0) {
+                    req = nreq;
+                    nreq = w.nok ? row_req[w.nb] : 0;
+                }
             }
         }
         if (lane == 0) *progress = 0x3fffffff;  // release the prefetch warp
@@ -1216,17 +1348,17 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
 
     if (warp == SW) {
         // ----------------------------------------------------------- MMA --
-        // Event loop: the S^T MMAs of item nq (once its K tile has landed
-        // and S^T buffer nq % 2 is free, i.e. the PV MMAs of item nq - 2 are
-        // issued) and the PV MMAs of item np (once its P tile is written and
+        // Event loop: the S^T MMAs of unit nq (once its K tile has landed
+        // and S^T buffer nq % 2 is free, i.e. the PV MMAs of unit nq - 2 are
+        // issued) and the PV MMAs of unit np (once its P tile is written and
         // O^T buffer np % 2 has been read), whichever is ready first, each
-        // in item order.  Gives up after a stall of the wait limit.
+        // in unit order.  Gives up after a stall of the wait limit.
         if (lane == 0) {
             int nq = 0, np = 0;
             uint64_t t0 = bi_globaltimer();
-            while (np < n_items) {
+            while (np < n_units) {
                 bool did = false;
-                if (nq < n_items && nq < np + 2) {
+                if (nq < n_units && nq < np + 2) {
                     const int jk = k_load(nq), sk = jk % RING;
                     if (mbar_try_wait(&full[sk], (jk / RING) & 1)) {
                         tc_fence_after();
@@ -1275,33 +1407,26 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
 
     // ------------------------------------------------ softmax + epilogue --
     const int tid = threadIdx.x;  // 0 .. 255
-    float m[16], m_prev[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) m_prev[r] = 0.f;
-    int pb = 0, pc = 0, pg_ = 0;  // previous item: row, chunk, KV head
-    // (row, chunk, visible length) of the next item, loaded one item ahead
-    int nb = 0, nc = 0, nvl = 0;
-    if (n_items > 0) {
-        const int2 bc = items[blockIdx.x / Hkv];
-        nb = bc.x;
-        nc = bc.y;
-        nvl = min(CHUNK, kv_len[nb] - nc * CHUNK);
+    // rows outside the work list: zero outputs
+    for (int i = blockIdx.x; i < B - n_valid; i += gridDim.x) {
+        uint4 *dst = reinterpret_cast<uint4 *>(
+            out + (int64_t)rows[n_valid + i].x * Hq * D);
+        for (int k = tid; k < Hq * D / 8; k += STHREADS)
+            dst[k] = make_uint4(0, 0, 0, 0);
     }
-    // epilogue of item e (buffer e & 1): records of rows < G
+    float m[16], m_prev[16];
+    // running (max, sum, output) of the item's rows for this thread's dim
+    // (warps 0-3), merged chunk by chunk in order
+    float Mr[16], Lr[16], Or[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) m_prev[r] = Mr[r] = Lr[r] = Or[r] = 0.f;
+    int pb = 0, pc = 0, pg_ = 0, pC = 1;  // previous unit: row, chunk, head
+    // epilogue of unit e (buffer e & 1): merge its partial into the running
+    // state; the item's last chunk writes the outputs
     auto epilogue = [&](int e) -> bool {
         const int bf = e & 1;
         const float *red = reinterpret_cast<const float *>(
             smem + DecL::RED + bf * RED_FLOATS * 4);
-        if (warp == 4 && lane < G) {
-            float *rec = ws + (((int64_t)pb * Hq + pg_ * G + lane) * Cmax +
-                               pc) * rec_floats<D>();
-            float mm = m_prev[0];
-#pragma unroll
-            for (int r = 1; r < 16; ++r)
-                if (r == lane) mm = m_prev[r];
-            rec[0] = mm;
-            rec[1] = row_sum(red, lane);
-        }
         if (warp < 4) {
             if (!mbar_wait(&o_full[bf], (e >> 1) & 1, status)) return false;
             tc_fence_after();
@@ -1312,8 +1437,19 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
                 if (r >= G) break;
-                ws[(((int64_t)pb * Hq + pg_ * G + r) * Cmax + pc) *
-                       rec_floats<D>() + 4 + dim] = o[r];
+                const float l = row_sum(red, r);
+                if (pc == 0) {
+                    Mr[r] = m_prev[r];
+                    Lr[r] = l;
+                    Or[r] = o[r];
+                } else {
+                    float a, bb;
+                    merge_scalars(Mr[r], Lr[r], m_prev[r], l, a, bb);
+                    Or[r] = merge_value(Or[r], o[r], a, bb);
+                }
+                if (pc == pC - 1)
+                    out[((int64_t)pb * Hq + pg_ * G + r) * D + dim] =
+                        f32_to_bf16(__fdiv_rn(Or[r], Lr[r]));
             }
             tc_fence_before();
             __syncwarp();
@@ -1322,56 +1458,55 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
         return true;
     };
     bool ok = true;
-    for (int n = 0; n < n_items && ok; ++n) {
-        const int i = blockIdx.x + n * gridDim.x;
-        const int g = i % Hkv;
-        const int b = nb, c = nc, vl = nvl;
-        if (n + 1 < n_items) {
-            const int2 bc = items[(i + gridDim.x) / Hkv];
-            nb = bc.x;
-            nc = bc.y;
-            nvl = min(CHUNK, kv_len[nb] - nc * CHUNK);
-        }
-        const int bf = n & 1;
-        float *red = reinterpret_cast<float *>(smem + DecL::RED +
-                                               bf * RED_FLOATS * 4);
-        const uint32_t ptile = base + DecL::P + bf * P_TILE;
-        if (!mbar_wait(&s_full[bf], (n >> 1) & 1, status) ||
-            (n >= 2 && !mbar_wait(&p_empty[bf], ((n - 2) >> 1) & 1, status))) {
-            ok = false;
-            break;
-        }
-        tc_fence_after();
-        int len[16];
+    int n = 0;
+    UnitWalk w{rows, total, Hkv};
+    if (w.begin()) {
+        do {
+            const int vl = w.vl();
+            const int bf = n & 1;
+            float *red = reinterpret_cast<float *>(smem + DecL::RED +
+                                                   bf * RED_FLOATS * 4);
+            const uint32_t ptile = base + DecL::P + bf * P_TILE;
+            if (!mbar_wait(&s_full[bf], (n >> 1) & 1, status) ||
+                (n >= 2 &&
+                 !mbar_wait(&p_empty[bf], ((n - 2) >> 1) & 1, status))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            int len[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) len[r] = r < G ? vl : 0;
-        if (G <= 4)
-            softmax<4>(tmem + bf * 32, scale, len, ptile, red, m);
-        else
-            softmax<16>(tmem + bf * 32, scale, len, ptile, red, m);
-        // V rows past the context inside the last visible page
-        const int jv = v_load(n), sv = jv % RING;
-        if (!mbar_wait(&full[sv], (jv / RING) & 1, status)) {
-            ok = false;
-            break;
-        }
-        if (vl & 15)
-            zero_v_rows(smem + DecL::SLOT + sv * DecL::TB, vl, (vl + 15) & ~15,
-                        tid, STHREADS);
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&p_full[bf]);
-        if (n > 0) ok = epilogue(n - 1);
+            for (int r = 0; r < 16; ++r) len[r] = r < G ? vl : 0;
+            if (G <= 4)
+                softmax<4>(tmem + bf * 32, scale, len, ptile, red, m);
+            else
+                softmax<16>(tmem + bf * 32, scale, len, ptile, red, m);
+            // V rows past the context inside the last visible page
+            const int jv = v_load(n), sv = jv % RING;
+            if (!mbar_wait(&full[sv], (jv / RING) & 1, status)) {
+                ok = false;
+                break;
+            }
+            if (vl & 15)
+                zero_v_rows(smem + DecL::SLOT + sv * DecL::TB, vl,
+                            (vl + 15) & ~15, tid, STHREADS);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[bf]);
+            if (n > 0) ok = epilogue(n - 1);
 #pragma unroll
-        for (int r = 0; r < 16; ++r) m_prev[r] = m[r];
-        pb = b;
-        pc = c;
-        pg_ = g;
+            for (int r = 0; r < 16; ++r) m_prev[r] = m[r];
+            pb = w.b;
+            pc = w.c;
+            pg_ = w.g;
+            pC = w.C;
+            ++n;
+        } while (ok && w.next());
     }
-    if (ok && n_items > 0) {
-        sync_softmax();  // every warp's row sums of the last item are in
-        epilogue(n_items - 1);
+    if (ok && n > 0) {
+        sync_softmax();  // every warp's row sums of the last unit are in
+        epilogue(n - 1);
     }
 }
 
@@ -1640,8 +1775,8 @@ bi_status launch_decode_chunks(const CUtensorMap &km, const CUtensorMap &vm,
                                float scale, float *rec, int Cmax,
                                const int32_t *prefix, int B,
                                const int2 *items, const bi_bf16 *k_pool,
-                               const bi_bf16 *v_pool, int32_t *status,
-                               cudaStream_t s) {
+                               const bi_bf16 *v_pool, bi_bf16 *out,
+                               int32_t *status, cudaStream_t s) {
     static std::once_flag f;
     static bi_status fs;
     if constexpr (D == 128) {
@@ -1651,8 +1786,9 @@ bi_status launch_decode_chunks(const CUtensorMap &km, const CUtensorMap &vm,
         if (fs != BI_OK) return fs;
         decode_tc_kernel<<<bi_sm_count(), tca::DEC_THREADS, tca::DecL::ALLOC,
                            s>>>(km, vm, qm, page_table, max_pages, n_pages,
-                                row_req, kv_len, Hq, Hkv, G, scale, rec, Cmax,
-                                prefix, B, items, k_pool, v_pool, status);
+                                row_req, Hq, Hkv, G, scale, prefix, B, items,
+                                k_pool, v_pool,
+                                reinterpret_cast<uint16_t *>(out), status);
     } else {
         std::call_once(f, [] {
             fs = set_attr(decode_chunks_kernel<D>, DecSmem<D>::ALLOC);
@@ -1682,7 +1818,9 @@ extern "C" size_t bi_decode_attn_workspace_size(int B, int Hq, int D,
 // Decode attention with the pool size known (page ids are range-checked
 // against it).  stages: bit 0 runs the chunk kernels (after building the
 // work list, unless bit 2 says the list in `ws` is already built for these
-// kv_len and row_req), bit 1 the merge.
+// kv_len and row_req), bit 1 the merge.  For head_dim 128 the chunk kernel
+// merges in registers and writes `out` itself (bit 1 does nothing); its work
+// list is the sorted row list of build_rows_kernel.
 bi_status bi_decode_attn_pool(const bi_bf16 *q, const bi_bf16 *k_pool,
                               const bi_bf16 *v_pool, const int32_t *page_table,
                               int max_pages, int n_pages,
@@ -1738,23 +1876,28 @@ bi_status bi_decode_attn_pool(const bi_bf16 *q, const bi_bf16 *k_pool,
                                        16, D == 128)) != BI_OK)
             return st;
         if (!(stages & 4)) {
-            build_items_kernel<<<1, 1024, 0, s>>>(kv_len, row_req, B, Cmax,
-                                                  prefix, items);
+            if (D == 128)
+                build_rows_kernel<<<1, 1024, 0, s>>>(kv_len, row_req, B, Cmax,
+                                                     prefix, items);
+            else
+                build_items_kernel<<<1, 1024, 0, s>>>(kv_len, row_req, B,
+                                                      Cmax, prefix, items);
             BI_LAUNCH_CHECK("decode item list launch");
         }
         if (D == 128)
             st = launch_decode_chunks<128>(km, vm, qm, page_table, max_pages,
                                            n_pages, row_req, kv_len, Hq, Hkv,
                                            G, scale, rec, Cmax, prefix, B,
-                                           items, k_pool, v_pool, status, s);
+                                           items, k_pool, v_pool, out, status,
+                                           s);
         else
             st = launch_decode_chunks<32>(km, vm, qm, page_table, max_pages,
                                           n_pages, row_req, kv_len, Hq, Hkv, G,
                                           scale, rec, Cmax, prefix, B, items,
-                                          k_pool, v_pool, status, s);
+                                          k_pool, v_pool, out, status, s);
         if (st != BI_OK) return st;
     }
-    if (stages & 2) {
+    if ((stages & 2) && D != 128) {
         const int warps = B * Hq;
         const int blocks = (warps * 32 + 255) / 256;
         if (D == 128)
