@@ -77,6 +77,9 @@ SIGNATURES = {
                                       V, V], I),
     "bi_prefill_attn": ([V, V, V, I, I, V, I, I, V, V, V, I, I, I, I, F, V,
                          V], I),
+    "bi_prefill_attn_workspace_size": ([I, I, I, I], Z),
+    "bi_prefill_attn_ws": ([V, V, V, I, I, V, I, I, V, V, V, I, I, I, I, F, V,
+                            V, Z, V], I),
     "bi_argmax_logits": ([V, I, I, V, V], I),
     "philox_sample": ([V, I, I, V, V, F, V, V], I),
     "bi_model_workspace_size": ([ctypes.POINTER(ModelCfg)], Z),
@@ -236,6 +239,22 @@ def bi_prefill_attn(q, cu_q, seg_req, pos, max_q, max_kv_len, k_pool, v_pool,
         _p(q), _p(cu_q), _p(seg_req), R, T, _p(pos), max_q, max_kv_len,
         _p(k_pool), _p(v_pool), _p(page_table), page_table.shape[1], Hq, Hkv,
         D_, scale, _p(out), _stream(stream)))
+
+
+def bi_prefill_attn_workspace_size(T, R, Hq, Hkv):
+    return lib().bi_prefill_attn_workspace_size(T, R, Hq, Hkv)
+
+
+def bi_prefill_attn_ws(q, cu_q, seg_req, pos, max_q, max_kv_len, k_pool,
+                       v_pool, page_table, scale, out, ws, stream=None):
+    T, Hq, D_ = q.shape
+    R = seg_req.numel()
+    Hkv = k_pool.shape[1]
+    _check(lib().bi_prefill_attn_ws(
+        _p(q), _p(cu_q), _p(seg_req), R, T, _p(pos), max_q, max_kv_len,
+        _p(k_pool), _p(v_pool), _p(page_table), page_table.shape[1], Hq, Hkv,
+        D_, scale, _p(out), _p(ws), ws.numel() * ws.element_size(),
+        _stream(stream)))
 
 
 def bi_argmax_logits(logits, ids, stream=None):

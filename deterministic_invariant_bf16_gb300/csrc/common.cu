@@ -106,14 +106,15 @@ static encode_tiled_fn get_encode() {
 
 bi_status bi_make_tmap_3d(CUtensorMap *map, const void *base, bool f32,
                           uint64_t d0, uint64_t d1, uint64_t d2,
-                          uint32_t box0, uint32_t box1, bool swizzle128) {
+                          uint32_t box0, uint32_t box1, bool swizzle128,
+                          uint32_t box2) {
     encode_tiled_fn enc = get_encode();
     if (!enc)
         return bi_fail(BI_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
     const uint64_t es = f32 ? 4 : 2;
     cuuint64_t dims[3] = {d0, d1, d2};
     cuuint64_t strides[2] = {d0 * es, d0 * d1 * es};
-    cuuint32_t box[3] = {box0, box1, 1};
+    cuuint32_t box[3] = {box0, box1, box2};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map,
                      f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32

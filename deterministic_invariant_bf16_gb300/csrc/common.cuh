@@ -149,6 +149,17 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *m,
         : "memory");
 }
 
+// 3-D form of tma_load_2d (box coordinates x, y, z).
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *m,
+                                            int32_t x, int32_t y, int32_t z,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx"
+        "::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+        "l"(m), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Hint to bring `bytes` (a multiple of 16, 16-byte aligned) at `src` into
 // L2: no shared memory, no completion to wait for.
 __device__ __forceinline__ void prefetch_l2_bulk(const void *src,

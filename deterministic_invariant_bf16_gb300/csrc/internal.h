@@ -22,11 +22,12 @@ bi_status bi_make_tmap_2d_bf16(CUtensorMap *map, const void *base,
                                uint32_t box_outer, bool swizzle128);
 
 // 3-D tensor map over a row-major [d2][d1][d0] array of fp32 (f32) or bf16,
-// box {box0, box1, 1}; with swizzle128 the 128-byte swizzle (box0 * element
-// size must then be 128), else no swizzle.
+// box {box0, box1, box2}; with swizzle128 the 128-byte swizzle (box0 *
+// element size must then be 128), else no swizzle.
 bi_status bi_make_tmap_3d(CUtensorMap *map, const void *base, bool f32,
                           uint64_t d0, uint64_t d1, uint64_t d2,
-                          uint32_t box0, uint32_t box1, bool swizzle128);
+                          uint32_t box0, uint32_t box1, bool swizzle128,
+                          uint32_t box2 = 1);
 
 
 
@@ -46,7 +47,12 @@ bi_status bi_prefill_attn_pool(const bi_bf16 *q, const int32_t *cu_q,
                                const bi_bf16 *k_pool, const bi_bf16 *v_pool,
                                const int32_t *page_table, int max_pages,
                                int n_pages, int Hq, int Hkv, int D,
-                               float scale, bi_bf16 *out, cudaStream_t stream);
+                               float scale, bi_bf16 *out, void *ws,
+                               size_t ws_bytes, cudaStream_t stream);
+
+// Workspace with which bi_prefill_attn_pool runs the persistent tensor-core
+// path (head_dim 128; without it, one CTA per query tile): its tile lists.
+size_t bi_prefill_attn_ws_bytes(int T, int R, int Hq, int Hkv);
 
 // RoPE in two parts for the model driver: the (cos, sin) table of the rows'
 // positions ([T][D/2] float2), computed once per forward, and the rotation

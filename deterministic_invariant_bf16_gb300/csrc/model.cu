@@ -392,7 +392,7 @@ extern "C" bi_status bi_model_forward(bi_model *m, int T, const int32_t *tokens,
                                           max_kv_len, m->kpool[l],
                                           m->vpool[l], page_table, c.max_pages,
                                           c.n_pages, Hq, Hkv, D, scale, attn,
-                                          s));
+                                          att_ws, att_ws_bytes, s));
         }
         BI_TIMED(BI_PROF_GEMM_O,
                  gemm_slices(attn, T, QD, m->wo[l], H, o, &s_o, s));

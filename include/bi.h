@@ -257,6 +257,25 @@ bi_status bi_prefill_attn(const bi_bf16 *q, const int32_t *cu_q,
                           int Hkv, int D, float scale, bi_bf16 *out,
                           void *stream);
 
+/* Workspace bytes with which bi_prefill_attn_ws runs its persistent path:
+ * the query-tile lists of T rows in R segments (0 if the shape has none). */
+size_t bi_prefill_attn_workspace_size(int T, int R, int Hq, int Hkv);
+
+/* bi_prefill_attn with a workspace (device, caller-owned, no initial
+ * contents).  For head_dim 128, T <= 512 rows (verify-sized batches),
+ * R <= 4096 and ws_bytes >= bi_prefill_attn_workspace_size: one persistent
+ * kernel per SM over (16 / G-token query tile, KV head) items sorted by
+ * chunk count, with the decode kernel's pipeline and merge, instead of one
+ * CTA per (tile, KV head).  Otherwise exactly bi_prefill_attn.  The bits of
+ * `out` are the same either way. */
+bi_status bi_prefill_attn_ws(const bi_bf16 *q, const int32_t *cu_q,
+                             const int32_t *seg_req, int R, int T,
+                             const int32_t *pos, int max_q, int max_kv_len,
+                             const bi_bf16 *k_pool, const bi_bf16 *v_pool,
+                             const int32_t *page_table, int max_pages, int Hq,
+                             int Hkv, int D, float scale, bi_bf16 *out,
+                             void *ws, size_t ws_bytes, void *stream);
+
 /* ------------------------------------------------------- token selection --
  * Greedy: ids[t] = first index of the maximum of logits[t] (fp32 [T][V]).
  * NaN counts as maximal and the first NaN wins; -0 equals +0.  Exact, so the

@@ -169,19 +169,28 @@ def decode(bi, q, kv, rows, kv_len):
     return out
 
 
-def prefill(bi, q, kv, segs):
-    """segs: list of (request, first position, n rows); q rows in order."""
+def prefill(bi, q, kv, segs, ws=False):
+    """segs: list of (request, first position, n rows); q rows in order.
+    ws: run bi_prefill_attn_ws with a workspace (the persistent path)."""
     cu, sr, pos = [0], [], []
     for r, p0, n in segs:
         cu.append(cu[-1] + n)
         sr.append(r)
         pos += list(range(p0, p0 + n))
     out = torch.empty_like(q)
-    bi.bi_prefill_attn(q, torch.tensor(cu, dtype=torch.int32).cuda(),
-                       torch.tensor(sr, dtype=torch.int32).cuda(),
-                       torch.tensor(pos, dtype=torch.int32).cuda(),
-                       max(n for _, _, n in segs), max(pos) + 1, kv.kp, kv.vp,
-                       kv.table, 1 / math.sqrt(q.shape[2]), out)
+    args = (q, torch.tensor(cu, dtype=torch.int32).cuda(),
+            torch.tensor(sr, dtype=torch.int32).cuda(),
+            torch.tensor(pos, dtype=torch.int32).cuda(),
+            max(n for _, _, n in segs), max(pos) + 1, kv.kp, kv.vp, kv.table,
+            1 / math.sqrt(q.shape[2]), out)
+    if ws:
+        T, Hq = q.shape[0], q.shape[1]
+        nb = bi.bi_prefill_attn_workspace_size(T, len(segs), Hq,
+                                               kv.kp.shape[1])
+        w = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda")
+        bi.bi_prefill_attn_ws(*args, w)
+    else:
+        bi.bi_prefill_attn(*args)
     return out, pos
 
 
@@ -282,6 +291,18 @@ def test_prefill_matches_decode_bitwise(bi, orc, Hq, Hkv, D):
     out2, pos2 = prefill(bi, q, kv, segs2)
     sync_ok(bi)
     assert pos2 == pos and np.array_equal(bits(out2), bits(out))
+    # the persistent path (with a workspace), on both segmentations and with
+    # a pad segment: same bits
+    for sg in (segs, segs2):
+        out3, pos3 = prefill(bi, q, kv, sg, ws=True)
+        sync_ok(bi)
+        assert pos3 == pos and np.array_equal(bits(out3), bits(out))
+    pad = torch.zeros((T + 9, Hq, D), dtype=torch.bfloat16, device="cuda")
+    pad[:T] = q
+    out4, _ = prefill(bi, pad, kv, segs + [(-1, 0, 9)], ws=True)
+    sync_ok(bi)
+    assert np.array_equal(bits(out4)[:T], bits(out))
+    assert not bits(out4)[T:].any()
 
 
 # -------------------------------------------------------------- argmax --
