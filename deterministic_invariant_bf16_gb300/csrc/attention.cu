@@ -1687,6 +1687,351 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
     }
 }
 
+// Per-chunk form of the tensor-core decode kernel, for small batches (too
+// few (row, KV head) items to fill the SMs): CTA k takes chunk items k,
+// k + grid, ...; item i is KV head i % Hkv of list entry i / Hkv (a (row,
+// chunk) of build_items_kernel), and writes the chunk's (m, l, o) record;
+// decode_merge_kernel merges the records in chunk order with the same
+// functions, so the bits equal the whole-row kernel's.  The ring loads K0
+// V0 K1 V1 ..., load j in slot j mod RING (k_load / v_load below).
+//   warps 0-7   softmax and epilogue (thread t <-> key t of the chunk);
+//   warp 8      owns the tensor memory; lane 0 issues the MMAs: S^T of item
+//               n + 2 is issued as soon as item n's softmax has read S^T
+//               (two S buffers), O^T of item n once its P tile is written
+//               (two P tiles, two O buffers);
+//   warp 9      producer: page ids -> TMA boxes (K only for visible pages,
+//               V for all 16 pages, missing ones as zero-filled boxes);
+//   warp 10     asks L2 for the K/V pages of the item after the one the
+//               producer loads next (one item ahead: 1% faster than two,
+//               9% faster than four or none).
+__global__ void __launch_bounds__(tca::DEC_THREADS, 1)
+    decode_tc_chunks_kernel(const __grid_constant__ CUtensorMap kmap,
+                            const __grid_constant__ CUtensorMap vmap,
+                            const __grid_constant__ CUtensorMap qmap,
+                            const int32_t *__restrict__ page_table,
+                            int max_pages, int n_pages,
+                            const int32_t *__restrict__ row_req,
+                            const int32_t *__restrict__ kv_len, int Hq,
+                            int Hkv, int G, float scale,
+                            float *__restrict__ ws, int Cmax,
+                            const int32_t *__restrict__ prefix, int B,
+                            const int2 *__restrict__ items,
+                            const bi_bf16 *__restrict__ k_pool,
+                            const bi_bf16 *__restrict__ v_pool,
+                            int32_t *status) {
+    using namespace tca;
+    constexpr int D = 128;
+    constexpr int PAGE_BYTES = 16 * 64 * 2;   // one box: 16 rows x 64 dims
+    constexpr int HALF_TILE = CHUNK * 128;
+    constexpr int HALF_Q = 16 * 128;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ int s_progress;  // items the producer has issued
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t base = smem_u32(smem);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + DecL::BAR);
+    uint64_t *empty = full + RING;
+    uint64_t *s_full = empty + RING;
+    uint64_t *p_full = s_full + 2;
+    uint64_t *p_empty = p_full + 2;
+    uint64_t *o_full = p_empty + 2;
+    uint64_t *o_empty = o_full + 2;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(o_empty + 2);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int total = prefix[B] * Hkv;
+    int n_items = 0;  // items of this CTA
+    if ((int)blockIdx.x < total)
+        n_items = (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < RING; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], SW);
+            mbar_init(&p_empty[i], 1);
+            mbar_init(&o_full[i], 1);
+            mbar_init(&o_empty[i], 4);
+        }
+        mbar_fence_init();
+        s_progress = 0;
+    }
+    if (warp < SW) {
+        // both P tiles start at zero: rows >= G are never written again
+        for (int i = threadIdx.x; i < 2 * P_TILE / 16; i += STHREADS)
+            reinterpret_cast<uint4 *>(smem + DecL::P)[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+    }
+    if (warp == SW) tmem_alloc(tslot, 128);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    volatile int *progress = &s_progress;
+
+    if (warp == SW + 2) {
+        // ------------------------------------------------------ prefetch --
+        constexpr uint32_t PAGE_KV = 16 * D * 2;
+        for (int n = 0; n < n_items; ++n) {
+            const int i = blockIdx.x + n * gridDim.x;
+            bool go = true;
+            if (lane == 0 && *progress + 1 < n) {
+                const uint64_t t0 = bi_globaltimer();
+                while (*progress + 1 < n) {
+                    __nanosleep(256);
+                    if (bi_globaltimer() - t0 > BI_WAIT_LIMIT_NS) {
+                        go = false;
+                        break;
+                    }
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, go ? 1 : 0, 0)) break;
+            const int g = i % Hkv;
+            const int2 bc = items[i / Hkv];
+            const int vl = min(CHUNK, kv_len[bc.x] - bc.y * CHUNK);
+            if (lane < ((vl + 15) >> 4)) {
+                const int pi = bc.y * 16 + lane;
+                const int pg = pi < max_pages
+                                   ? page_table[(int64_t)row_req[bc.x] *
+                                                    max_pages + pi]
+                                   : -1;
+                if (pg >= 0 && pg < n_pages) {
+                    const int64_t off = ((int64_t)pg * Hkv + g) * 16 * D;
+                    prefetch_l2_bulk(k_pool + off, PAGE_KV);
+                    prefetch_l2_bulk(v_pool + off, PAGE_KV);
+                }
+            }
+        }
+        return;
+    }
+
+    if (warp == SW + 1) {
+        // ------------------------------------------------------ producer --
+        if (lane == 0) {
+            tma_prefetch_desc(&kmap);
+            tma_prefetch_desc(&vmap);
+            tma_prefetch_desc(&qmap);
+        }
+        bool ok = true;
+        // load t of the sequence: the K (t even) or V (t odd) of item t / 2
+        for (int t = 0; t < 2 * n_items && ok; ++t) {
+            const bool is_k = (t & 1) == 0;
+            const int n = t >> 1;
+            const int i = blockIdx.x + n * gridDim.x;
+            const int g = i % Hkv;
+            const int2 bc = items[i / Hkv];
+            const int b = bc.x, c = bc.y;
+            const int vl = min(CHUNK, kv_len[b] - c * CHUNK);
+            const int npg = (vl + 15) >> 4;
+            const int32_t *pt_row = page_table + (int64_t)row_req[b] * max_pages;
+            int pg = -1;
+            if (lane < npg) {
+                const int pi = c * 16 + lane;
+                pg = pi < max_pages ? pt_row[pi] : -1;
+                if (pg < 0 || pg >= n_pages) {
+                    if (is_k) bi_record_error(status, BI_ERR_BOUNDS);
+                    pg = -1;
+                }
+            }
+            const int nvalid = __popc(__ballot_sync(0xffffffffu, pg >= 0));
+            const int slot = t % RING;
+            const int use = t / RING;
+            bool w_ok = true;
+            if (lane == 0 && use > 0)
+                w_ok = mbar_wait(&empty[slot], (use - 1) & 1, status);
+            ok = __shfl_sync(0xffffffffu, w_ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
+            // K: the visible pages (+ Q).  V: all 16 pages, the ones
+            // without data as boxes wholly above row 0 (zero-filled).
+            if (lane == 0)
+                mbar_arrive_expect_tx(&full[slot],
+                                      is_k ? nvalid * 2 * PAGE_BYTES + 2 * HALF_Q
+                                           : 16 * 2 * PAGE_BYTES);
+            __syncwarp();
+            uint8_t *tile = smem + DecL::SLOT + slot * DecL::TB;
+            if (lane < 16 && (!is_k || pg >= 0)) {
+                const int row = pg >= 0 ? (pg * Hkv + g) * 16 : -16;
+                const CUtensorMap *map = is_k ? &kmap : &vmap;
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    tma_load_2d(tile + h * HALF_TILE + lane * PAGE_BYTES, map,
+                                h * 64, row, &full[slot]);
+            }
+            if (is_k && lane == 0) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    tma_load_2d(smem + DecL::QSLOT + slot * DecL::QB + h * HALF_Q,
+                                &qmap, h * 64, b * Hq + g * G, &full[slot]);
+                *progress = n + 1;
+            }
+        }
+        if (lane == 0) *progress = 0x3fffffff;  // release the prefetch warp
+        return;
+    }
+
+    if (warp == SW) {
+        // ----------------------------------------------------------- MMA --
+        // Event loop: the S^T MMAs of item nq (once its K tile has landed
+        // and S^T buffer nq % 2 is free, i.e. the PV MMAs of item nq - 2 are
+        // issued) and the PV MMAs of item np (once its P tile is written and
+        // O^T buffer np % 2 has been read), whichever is ready first, each
+        // in item order.  Gives up after a stall of the wait limit.
+        if (lane == 0) {
+            int nq = 0, np = 0;
+            uint64_t t0 = bi_globaltimer();
+            while (np < n_items) {
+                bool did = false;
+                if (nq < n_items && nq < np + 2) {
+                    const int jk = k_load(nq), sk = jk % RING;
+                    if (mbar_try_wait(&full[sk], (jk / RING) & 1)) {
+                        tc_fence_after();
+                        issue_qk(tmem + (nq & 1) * 32,
+                                 base + DecL::SLOT + sk * DecL::TB,
+                                 base + DecL::QSLOT + sk * DecL::QB);
+                        tc_commit(&s_full[nq & 1]);
+                        tc_commit(&empty[sk]);
+                        ++nq;
+                        did = true;
+                    }
+                }
+                if (np < nq) {
+                    const int bf = np & 1;
+                    if (mbar_try_wait(&p_full[bf], (np >> 1) & 1) &&
+                        (np < 2 ||
+                         mbar_try_wait(&o_empty[bf], ((np - 2) >> 1) & 1))) {
+                        const int sv = v_load(np) % RING;
+                        tc_fence_after();
+                        issue_pv(tmem + 64 + bf * 16,
+                                 base + DecL::SLOT + sv * DecL::TB,
+                                 base + DecL::P + bf * P_TILE);
+                        tc_commit(&o_full[bf]);
+                        tc_commit(&p_empty[bf]);
+                        tc_commit(&empty[sv]);
+                        ++np;
+                        did = true;
+                    }
+                }
+                if (did) {
+                    t0 = bi_globaltimer();
+                } else if (bi_globaltimer() - t0 > BI_WAIT_LIMIT_NS) {
+                    bi_record_error(status, BI_ERR_TIMEOUT);
+                    break;
+                }
+            }
+            // the last epilogues have read O^T before the memory is freed
+            for (int n = max(0, np - 2); n < np; ++n)
+                mbar_wait(&o_empty[n & 1], (n >> 1) & 1, status);
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 128);
+        return;
+    }
+
+    // ------------------------------------------------ softmax + epilogue --
+    const int tid = threadIdx.x;  // 0 .. 255
+    float m[16], m_prev[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) m_prev[r] = 0.f;
+    int pb = 0, pc = 0, pg_ = 0;  // previous item: row, chunk, KV head
+    // (row, chunk, visible length) of the next item, loaded one item ahead
+    int nb = 0, nc = 0, nvl = 0;
+    if (n_items > 0) {
+        const int2 bc = items[blockIdx.x / Hkv];
+        nb = bc.x;
+        nc = bc.y;
+        nvl = min(CHUNK, kv_len[nb] - nc * CHUNK);
+    }
+    // epilogue of item e (buffer e & 1): records of rows < G
+    auto epilogue = [&](int e) -> bool {
+        const int bf = e & 1;
+        const float *red = reinterpret_cast<const float *>(
+            smem + DecL::RED + bf * RED_FLOATS * 4);
+        if (warp == 4 && lane < G) {
+            float *rec = ws + (((int64_t)pb * Hq + pg_ * G + lane) * Cmax +
+                               pc) * rec_floats<D>();
+            float mm = m_prev[0];
+#pragma unroll
+            for (int r = 1; r < 16; ++r)
+                if (r == lane) mm = m_prev[r];
+            rec[0] = mm;
+            rec[1] = row_sum(red, lane);
+        }
+        if (warp < 4) {
+            if (!mbar_wait(&o_full[bf], (e >> 1) & 1, status)) return false;
+            tc_fence_after();
+            float o[16];
+            tmem_ld_16cols(tmem + 64 + bf * 16 + ((uint32_t)(warp * 32) << 16),
+                           o);
+            const int dim = warp * 32 + lane;
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                if (r >= G) break;
+                ws[(((int64_t)pb * Hq + pg_ * G + r) * Cmax + pc) *
+                       rec_floats<D>() + 4 + dim] = o[r];
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_empty[bf]);
+        }
+        return true;
+    };
+    bool ok = true;
+    for (int n = 0; n < n_items && ok; ++n) {
+        const int i = blockIdx.x + n * gridDim.x;
+        const int g = i % Hkv;
+        const int b = nb, c = nc, vl = nvl;
+        if (n + 1 < n_items) {
+            const int2 bc = items[(i + gridDim.x) / Hkv];
+            nb = bc.x;
+            nc = bc.y;
+            nvl = min(CHUNK, kv_len[nb] - nc * CHUNK);
+        }
+        const int bf = n & 1;
+        float *red = reinterpret_cast<float *>(smem + DecL::RED +
+                                               bf * RED_FLOATS * 4);
+        const uint32_t ptile = base + DecL::P + bf * P_TILE;
+        if (!mbar_wait(&s_full[bf], (n >> 1) & 1, status) ||
+            (n >= 2 && !mbar_wait(&p_empty[bf], ((n - 2) >> 1) & 1, status))) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        int len[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) len[r] = r < G ? vl : 0;
+        if (G <= 4)
+            softmax<4>(tmem + bf * 32, scale, len, ptile, red, m);
+        else
+            softmax<16>(tmem + bf * 32, scale, len, ptile, red, m);
+        // V rows past the context inside the last visible page
+        const int jv = v_load(n), sv = jv % RING;
+        if (!mbar_wait(&full[sv], (jv / RING) & 1, status)) {
+            ok = false;
+            break;
+        }
+        if (vl & 15)
+            zero_v_rows(smem + DecL::SLOT + sv * DecL::TB, vl, (vl + 15) & ~15,
+                        tid, STHREADS);
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[bf]);
+        if (n > 0) ok = epilogue(n - 1);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) m_prev[r] = m[r];
+        pb = b;
+        pc = c;
+        pg_ = g;
+    }
+    if (ok && n_items > 0) {
+        sync_softmax();  // every warp's row sums of the last item are in
+        epilogue(n_items - 1);
+    }
+}
+
 // Prefill / verify on the tensor cores (head_dim 128): CTA = (16-row tile of
 // one segment, KV head g); loops over the chunks with the functions above and
 // merges the chunk partials in registers in chunk order, as the decode merge
@@ -1943,8 +2288,21 @@ size_t records_bytes(int B, int Hq, int D, int max_kv_len) {
     return up256((size_t)B * Hq * C * (D + 4) * sizeof(float));
 }
 
+}  // namespace
+
+// Whole (row, KV head) items when there are at least 8 per SM; below that
+// the per-chunk kernel spreads a row's chunks over the SMs.  Measured at 8
+// KV heads: batches of 8-128 rows 2-6% faster per chunk, 256 rows 4.6%
+// faster as whole rows.  Both forms give the same bits.
+bool bi_decode_whole_rows(int B, int Hkv, int D) {
+    return D == 128 && (int64_t)B * Hkv >= 8 * (int64_t)bi_sm_count();
+}
+
+namespace {
+
 template <int D>
-bi_status launch_decode_chunks(const CUtensorMap &km, const CUtensorMap &vm,
+bi_status launch_decode_chunks(bool whole_rows, const CUtensorMap &km,
+                               const CUtensorMap &vm,
                                const CUtensorMap &qm,
                                const int32_t *page_table, int max_pages,
                                int n_pages, const int32_t *row_req,
@@ -1954,9 +2312,19 @@ bi_status launch_decode_chunks(const CUtensorMap &km, const CUtensorMap &vm,
                                const int2 *items, const bi_bf16 *k_pool,
                                const bi_bf16 *v_pool, bi_bf16 *out,
                                int32_t *status, cudaStream_t s) {
-    static std::once_flag f;
-    static bi_status fs;
-    if constexpr (D == 128) {
+    static std::once_flag f, f2;
+    static bi_status fs, fs2;
+    if (D == 128 && !whole_rows) {
+        std::call_once(f2, [] {
+            fs2 = set_attr(decode_tc_chunks_kernel, tca::DecL::ALLOC);
+        });
+        if (fs2 != BI_OK) return fs2;
+        decode_tc_chunks_kernel<<<bi_sm_count(), tca::DEC_THREADS,
+                                  tca::DecL::ALLOC, s>>>(
+            km, vm, qm, page_table, max_pages, n_pages, row_req, kv_len, Hq,
+            Hkv, G, scale, rec, Cmax, prefix, B, items, k_pool, v_pool,
+            status);
+    } else if constexpr (D == 128) {
         std::call_once(f, [] {
             fs = set_attr(attn_tc_kernel<false>, tca::DecL::ALLOC);
         });
@@ -1995,9 +2363,11 @@ extern "C" size_t bi_decode_attn_workspace_size(int B, int Hq, int D,
 // Decode attention with the pool size known (page ids are range-checked
 // against it).  stages: bit 0 runs the chunk kernels (after building the
 // work list, unless bit 2 says the list in `ws` is already built for these
-// kv_len and row_req), bit 1 the merge.  For head_dim 128 the chunk kernel
-// merges in registers and writes `out` itself (bit 1 does nothing); its work
-// list is the sorted row list of build_rows_kernel.
+// kv_len and row_req), bit 1 the merge.  With whole-row items (head_dim 128,
+// bi_decode_whole_rows) the kernel merges in registers and writes `out`
+// itself (bit 1 does nothing); its work list is the sorted row list of
+// build_rows_kernel.  Otherwise the work list holds (row, chunk) items and
+// bit 1 merges the chunk records.
 bi_status bi_decode_attn_pool(const bi_bf16 *q, const bi_bf16 *k_pool,
                               const bi_bf16 *v_pool, const int32_t *page_table,
                               int max_pages, int n_pages,
@@ -2052,8 +2422,9 @@ bi_status bi_decode_attn_pool(const bi_bf16 *q, const bi_bf16 *k_pool,
         if ((st = bi_make_tmap_2d_bf16(&qm, q, D, (uint64_t)B * Hq, D * 2, bw,
                                        16, D == 128)) != BI_OK)
             return st;
+        const bool rows = bi_decode_whole_rows(B, Hkv, D);
         if (!(stages & 4)) {
-            if (D == 128)
+            if (rows)
                 build_rows_kernel<<<1, 1024, 0, s>>>(kv_len, row_req, B, Cmax,
                                                      prefix, items);
             else
@@ -2062,19 +2433,21 @@ bi_status bi_decode_attn_pool(const bi_bf16 *q, const bi_bf16 *k_pool,
             BI_LAUNCH_CHECK("decode item list launch");
         }
         if (D == 128)
-            st = launch_decode_chunks<128>(km, vm, qm, page_table, max_pages,
+            st = launch_decode_chunks<128>(rows, km, vm, qm, page_table,
+                                           max_pages,
                                            n_pages, row_req, kv_len, Hq, Hkv,
                                            G, scale, rec, Cmax, prefix, B,
                                            items, k_pool, v_pool, out, status,
                                            s);
         else
-            st = launch_decode_chunks<32>(km, vm, qm, page_table, max_pages,
+            st = launch_decode_chunks<32>(false, km, vm, qm, page_table,
+                                          max_pages,
                                           n_pages, row_req, kv_len, Hq, Hkv, G,
                                           scale, rec, Cmax, prefix, B, items,
                                           k_pool, v_pool, out, status, s);
         if (st != BI_OK) return st;
     }
-    if ((stages & 2) && D != 128) {
+    if ((stages & 2) && !bi_decode_whole_rows(B, Hkv, D)) {
         const int warps = B * Hq;
         const int blocks = (warps * 32 + 255) / 256;
         if (D == 128)

@@ -33,7 +33,9 @@ bi_status bi_make_tmap_3d(CUtensorMap *map, const void *base, bool f32,
 
 // Attention with the KV pool size known, for the model driver.  Decode
 // stages: bit 0 chunk kernels (bit 2: reuse the work list already in ws),
-// bit 1 merge.
+// bit 1 merge (nothing to do when bi_decode_whole_rows holds: the kernel
+// then merges in registers and writes `out` itself).
+bool bi_decode_whole_rows(int B, int Hkv, int D);
 bi_status bi_decode_attn_pool(const bi_bf16 *q, const bi_bf16 *k_pool,
                               const bi_bf16 *v_pool, const int32_t *page_table,
                               int max_pages, int n_pages,

@@ -376,8 +376,8 @@ extern "C" bi_status bi_model_forward(bi_model *m, int T, const int32_t *tokens,
                                          row_req, kvlen, T, max_kv_len, Hq,
                                          Hkv, D, scale, attn, att_ws,
                                          att_ws_bytes, l == 0 ? 1 : 1 | 4, s));
-            // head_dim 128: the chunk kernel merges and writes attn itself
-            if (D != 128) {
+            // whole-row items: the kernel merges and writes attn itself
+            if (!bi_decode_whole_rows(T, Hkv, D)) {
                 BI_TIMED(BI_PROF_ATTN_MERGE,
                          bi_decode_attn_pool(q, m->kpool[l], m->vpool[l],
                                              page_table, c.max_pages,

@@ -267,6 +267,30 @@ def test_decode_work_list_over_many_rows(bi, orc, D):
     assert np.array_equal(bits(shuf), full[perm])
 
 
+def test_decode_whole_rows_match_chunk_items(bi, orc):
+    """Batches with at least 8 (row, KV head) items per SM run whole-row
+    items merged in registers; smaller ones run (row, chunk) items and a
+    separate merge.  Both must give the same bits for a row: a batch of 200
+    rows (1600 items) against 40-row sub-batches of it (320 items)."""
+    rng = np.random.default_rng(17)
+    lens = rng.integers(1, 520, 200)
+    lens[::13] = 256
+    lens[3::17] = 512
+    kv = PagedKV(lens, 8, 128, seed=19)
+    q = randn_bf16((200, 32, 128), 20)
+    full = bits(decode(bi, q, kv, list(range(200)), lens))
+    sync_ok(bi)
+    for lo in range(0, 200, 40):
+        part = decode(bi, q[lo:lo + 40].contiguous(), kv,
+                      list(range(lo, lo + 40)), lens[lo:lo + 40])
+        sync_ok(bi)
+        assert np.array_equal(bits(part), full[lo:lo + 40])
+    pick = np.sort(rng.choice(200, 6, replace=False))
+    ref = attn_ref(orc, q[torch.from_numpy(pick).cuda()], kv, pick,
+                   lens[pick] - 1)
+    check_close(full[pick], ref, orc)
+
+
 @pytest.mark.parametrize("Hq,Hkv,D", [(32, 8, 128), (4, 4, 32)])
 def test_prefill_matches_decode_bitwise(bi, orc, Hq, Hkv, D):
     """Query-length invariance (Vosti): a position computed inside a window
