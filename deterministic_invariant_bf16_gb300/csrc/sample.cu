@@ -70,16 +70,31 @@ __global__ void __launch_bounds__(SEL_THREADS)
     float bv = -INFINITY;
     int bi = 0x7fffffff;
     if ((V & 3) == 0) {
+        // UNROLL float4 loads in flight per thread: a row is read by one
+        // block, so its time is the loads' latency unless they overlap.
+        constexpr int UNROLL = 4;
         const float4 *r4 = reinterpret_cast<const float4 *>(row);
-        for (int k = threadIdx.x; k < V / 4; k += SEL_THREADS) {
-            const float4 x = r4[k];
-            const float xs[4] = {x.x, x.y, x.z, x.w};
+        const int n4 = V / 4;
+        for (int k0 = threadIdx.x; k0 < n4; k0 += UNROLL * SEL_THREADS) {
+            float4 x[UNROLL];
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (better(xs[e], 4 * k + e, bv, bi)) {
-                    bv = xs[e];
-                    bi = 4 * k + e;
-                }
+            for (int u = 0; u < UNROLL; ++u) {
+                const int k = k0 + u * SEL_THREADS;
+                x[u] = k < n4 ? __ldg(r4 + k)
+                              : make_float4(-INFINITY, -INFINITY, -INFINITY,
+                                            -INFINITY);
+            }
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                const int k = k0 + u * SEL_THREADS;
+                const float xs[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (k < n4 && better(xs[e], 4 * k + e, bv, bi)) {
+                        bv = xs[e];
+                        bi = 4 * k + e;
+                    }
+            }
         }
     } else {
         for (int k = threadIdx.x; k < V; k += SEL_THREADS)
@@ -167,9 +182,31 @@ __global__ void __launch_bounds__(SEL_THREADS)
                   int32_t *__restrict__ ids) {
     const int t = blockIdx.x;
     const float *row = logits + (int64_t)t * V;
-    // 1. maximum (exact; NaN ignored)
+    // 1. maximum (exact and order-free; NaN ignored), several loads in
+    // flight per thread
     float mx = -INFINITY;
-    for (int k = threadIdx.x; k < V; k += SEL_THREADS) mx = fmaxf(mx, row[k]);
+    if ((V & 3) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0) {
+        constexpr int UNROLL = 4;
+        const float4 *r4 = reinterpret_cast<const float4 *>(row);
+        const int n4 = V / 4;
+        for (int k0 = threadIdx.x; k0 < n4; k0 += UNROLL * SEL_THREADS) {
+            float4 x[UNROLL];
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                const int k = k0 + u * SEL_THREADS;
+                x[u] = k < n4 ? __ldg(r4 + k)
+                              : make_float4(-INFINITY, -INFINITY, -INFINITY,
+                                            -INFINITY);
+            }
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u)
+                mx = fmaxf(fmaxf(mx, fmaxf(x[u].x, x[u].y)),
+                           fmaxf(x[u].z, x[u].w));
+        }
+    } else {
+        for (int k = threadIdx.x; k < V; k += SEL_THREADS)
+            mx = fmaxf(mx, row[k]);
+    }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1)
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -178,12 +215,44 @@ __global__ void __launch_bounds__(SEL_THREADS)
     __syncthreads();
     mx = smx[0];
     for (int i = 1; i < SEL_THREADS / 32; ++i) mx = fmaxf(mx, smx[i]);
-    // 2. contiguous slice sums in index order
+    // 2. contiguous slice sums in index order.  A warp's 32 slices are one
+    // contiguous range; it is read 8 columns of every slice at a time, with
+    // lane -> (slice 4 i + lane / 8, column lane % 8) so that each load
+    // covers four 32-byte runs, and each lane then sums its own slice's 8
+    // values from shared memory in index order.
     const int per = (V + SEL_THREADS - 1) / SEL_THREADS;
     const int lo = min(V, threadIdx.x * per), hi = min(V, lo + per);
+    __shared__ float cols[SEL_THREADS / 32][32][9];
+    float(*cw)[9] = cols[threadIdx.x >> 5];
+    const int lane = threadIdx.x & 31;
+    const int64_t wbase = (int64_t)(threadIdx.x & ~31) * per;
     float part = 0.f;
-    for (int k = lo; k < hi; ++k)
-        part = __fadd_rn(part, expf(__fdiv_rn(__fsub_rn(row[k], mx), tau)));
+    // the next column block is loaded into registers while the current
+    // one is summed
+    float nxt[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = 4 * i + (lane >> 3), c = lane & 7;
+        const int64_t e = wbase + (int64_t)r * per + c;
+        nxt[i] = c < per && e < V ? __ldg(row + e) : 0.f;
+    }
+    for (int c0 = 0; c0 < per; c0 += 8) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cw[4 * i + (lane >> 3)][lane & 7] = nxt[i];
+        __syncwarp();
+        const int c = c0 + 8 + (lane & 7);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = 4 * i + (lane >> 3);
+            const int64_t e = wbase + (int64_t)r * per + c;
+            nxt[i] = c < per && e < V ? __ldg(row + e) : 0.f;
+        }
+        const int n = min(8, hi - lo - c0);
+        for (int j = 0; j < n; ++j)
+            part = __fadd_rn(part,
+                             expf(__fdiv_rn(__fsub_rn(cw[lane][j], mx), tau)));
+        __syncwarp();
+    }
     float total;
     const float prefix = block_exclusive_scan(part, &total);
     // 3. first index whose running sum exceeds u * total.  A slice whose
