@@ -288,20 +288,9 @@ class Bench:
 
     def capture(self):
         """Capture one step's decode iterations (the library's calls, same
-        buffers and arguments) as a CUDA graph; the verify part syncs with
-        the host and stays eager."""
-        torch = self.torch
-        torch.cuda.synchronize()
-        side = torch.cuda.Stream()
-        side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            self.decode_iters()
-        torch.cuda.current_stream().wait_stream(side)
-        torch.cuda.synchronize()
-        self.graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(self.graph):
-            self.decode_iters()
-        torch.cuda.synchronize()
+        buffers and arguments) as a CUDA graph through Engine.capture; the
+        verify part syncs with the host and stays eager."""
+        self.graph = self.eng.capture(self.decode_iters)
 
     def step(self, graph=False):
         if graph and getattr(self, "graph", None) is not None:
@@ -521,7 +510,9 @@ def run_ours(args):
                           dist if world > 1 else None, dev)
 
     # ---- end to end through the public API with host buffers: every step
-    # uploads its inputs from pinned host memory and reads back the tokens.
+    # uploads its inputs from pinned host memory into the buffers the
+    # decode graph (Engine.capture) reads, replays it, runs the verify
+    # group, and reads back the tokens.
     h_in_tok = b.tok0.cpu().pin_memory()
     h_in_pos = b.pos.cpu().pin_memory()
     h_in_step = b.stepv.cpu().pin_memory()
@@ -538,7 +529,7 @@ def run_ours(args):
         b.tok0.copy_(h_in_tok, non_blocking=True)
         b.pos.copy_(h_in_pos, non_blocking=True)
         b.stepv.copy_(h_in_step, non_blocking=True)
-        b.step()
+        b.step(graph=use_graph)
         h_out.copy_(b.ids, non_blocking=True)
         stream.synchronize()
     e3.record(stream)
@@ -611,7 +602,7 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (weights + KV >> 129 MB)",
                    "parallelism": "replicas" if world > 1 else "single",
                    "decode_launch": "cuda_graph" if use_graph else "eager",
-                   "e2e_launch": "eager"},
+                   "e2e_launch": "cuda_graph" if use_graph else "eager"},
         "e2e": e2e,
         "gpu_launches": int(round(launches * args.steps)),
         "roofline": roof,

@@ -240,11 +240,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         mbar_fence_init();
     }
-    if (warp == 1) tmem_alloc(tslot, TMEM_COLS);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tslot;
+    __syncthreads();  // the barriers exist
+    // The producer needs no tensor memory: its loads start while warp 1
+    // allocates it; warps 1-5 meet on named barrier 1 once it is held.
+    uint32_t tmem = 0;
+    if (warp >= 1) {
+        if (warp == 1) tmem_alloc(tslot, TMEM_COLS);
+        tc_fence_before();
+        asm volatile("bar.sync 1, %0;" ::"n"(THREADS - 32) : "memory");
+        tc_fence_after();
+        tmem = *tslot;
+    }
 
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------- producer --

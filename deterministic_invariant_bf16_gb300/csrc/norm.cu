@@ -31,15 +31,6 @@ __global__ void __launch_bounds__(NORM_THREADS)
     const int64_t row = (int64_t)t * H;
     const int64_t TH = (int64_t)T * H;
     float v[NORM_MAX_VEC][8];
-    // The weights do not depend on the row: their loads are issued first so
-    // that they are not a second memory round trip after the reduction.
-    uint4 wv[NORM_MAX_VEC];
-#pragma unroll
-    for (int k = 0; k < NORM_MAX_VEC; ++k) {
-        const int vi = tid + k * NORM_THREADS;
-        if (vi >= nvec) break;
-        wv[k] = __ldg(reinterpret_cast<const uint4 *>(w + (int64_t)vi * 8));
-    }
     float ss = 0.0f;
 #pragma unroll
     for (int k = 0; k < NORM_MAX_VEC; ++k) {
@@ -119,7 +110,8 @@ __global__ void __launch_bounds__(NORM_THREADS)
         const int vi = tid + k * NORM_THREADS;
         if (vi >= nvec) break;
         const int64_t off = row + (int64_t)vi * 8;
-        const uint32_t ww[4] = {wv[k].x, wv[k].y, wv[k].z, wv[k].w};
+        uint4 wv = *reinterpret_cast<const uint4 *>(w + (int64_t)vi * 8);
+        const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
         uint32_t o[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j)

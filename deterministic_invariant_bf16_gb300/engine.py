@@ -162,6 +162,30 @@ class Engine:
                             max_kv_len, self.page_table, logits, ids, stream)
         return logits
 
+    def capture(self, fn):
+        """Record the library calls that `fn()` makes as one CUDA graph
+        and return it (`torch.cuda.CUDAGraph`; `.replay()` issues them
+        again).  fn runs once first on a side stream, then once under
+        capture.  Every tensor fn passes must stay alive and be refilled in
+        place between replays (tokens, positions, ids ...); fn must not
+        read results on the host, so verify_commit_rollback, which does,
+        stays outside.  A decode iteration captured this way launches the
+        same kernels with the same arguments, so its results are those of
+        the eager calls bit for bit."""
+        dev = torch.device(self.device)
+        torch.cuda.synchronize(dev)
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize(dev)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn()
+        torch.cuda.synchronize(dev)
+        return graph
+
     def prefill(self, segments, logits=None, ids=None, stream=None):
         """segments: list of (slot, tokens, first_position).  Rows of a
         segment take consecutive positions."""

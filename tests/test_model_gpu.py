@@ -158,6 +158,46 @@ def test_repeated_runs_identical(tiny):
         assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
 
 
+def test_captured_decode_replays_bitwise(tiny, lib):
+    """Engine.capture: decode iterations recorded as a CUDA graph and
+    replayed with new inputs copied into the same buffers give the logits
+    and ids of the eager calls, bit for bit."""
+    shape = tiny[0]
+    prompts = prompts8(shape)
+    slots = list(range(8))
+    eng = new_engine(tiny, page_seed=12)
+    for r in slots:
+        eng.reserve(r, 16 + 4)
+    eng.prefill([(r, prompts[r], 0) for r in slots])
+    dev = "cuda"
+    tok = torch.zeros(8, dtype=torch.int32, device=dev)
+    pos = torch.zeros(8, dtype=torch.int32, device=dev)
+    rr = torch.tensor(slots, dtype=torch.int32, device=dev)
+    ids = torch.empty(8, dtype=torch.int32, device=dev)
+    lg = torch.empty(8, shape.vocab, dtype=torch.float32, device=dev)
+
+    def one():
+        eng.decode(tok, pos, rr, logits=lg, ids=ids, max_kv_len=20)
+
+    tok.copy_(torch.tensor([int(p[-1]) for p in prompts], dtype=torch.int32))
+    pos.fill_(16)
+    g = eng.capture(one)
+    rng = np.random.default_rng(5)
+    for step in range(3):
+        t = rng.integers(0, shape.vocab, 8).astype(np.int32)
+        p = np.full(8, 16 + step, np.int32)
+        tok.copy_(torch.from_numpy(t))
+        pos.copy_(torch.from_numpy(p))
+        g.replay()
+        torch.cuda.synchronize()
+        got_l, got_i = lg.clone(), ids.clone()
+        one()  # eager, same inputs: rewrites the same KV slots
+        torch.cuda.synchronize()
+        assert torch.equal(got_l.view(torch.int32), lg.view(torch.int32))
+        assert torch.equal(got_i, ids)
+    assert lib.bi_device_status() == 0
+
+
 # ---------------------------------------------------------------- verify --
 
 def _decode_reference(tiny, prompts, n_new):
