@@ -438,10 +438,68 @@ def run_report(args):
     rep["prefill"] = {"tok_s": float(prompts.sum()) / (ms / 1000.0),
                       "requests": R, "tokens": int(prompts.sum()),
                       "piece": piece, "ms": ms}
+    del eng, logits
+    torch.cuda.empty_cache()
+    rep["prefix_sharing"] = prefix_report(torch, bi, engine, synth, shape, W,
+                                          dev, piece)
     rep["device_status"] = bi.bi_device_status()
     print(json.dumps({"report": rep, "workload": WORKLOAD,
                       "data": "synthetic (random-init weights, random KV)"}),
           flush=True)
+
+
+def prefix_report(torch, bi, engine, synth, shape, W, dev, piece):
+    """8 prompts = one common 4096-token prefix + 256 tokens of their own,
+    prefilled (a) each from scratch and (b) with the prefix computed once
+    and its 256 pages shared (Engine.share_prefix); the last-row logits of
+    every prompt must be bitwise equal between (a) and (b)."""
+    rng = np.random.default_rng(1006)
+    R, P, U = 8, 4096, 256
+    common = synth.token_ids(P, shape.vocab, rng)
+    toks = [np.concatenate([common, synth.token_ids(U, shape.vocab, rng)])
+            for _ in range(R)]
+    per = (P + U) // 16
+    eng = engine.Engine(shape, W, max_tokens=piece, max_kv_len=P + U + 16,
+                        n_slots=2 * R, n_pages=R * per + per +
+                        (R - 1) * (U // 16) + 32, page_seed=9)
+    logits = torch.empty(piece, shape.vocab, dtype=torch.float32, device=dev)
+    last = torch.empty(2, R, shape.vocab, dtype=torch.float32, device=dev)
+    for r in range(R + 1):
+        eng.reserve(r, P + U)
+
+    def fill(slot, t, p0, out):
+        for q in range(p0, P + U, piece):
+            c = t[q:q + piece]
+            eng.prefill([(slot, c, q)], logits=logits[:len(c)])
+        out.copy_(logits[len(c) - 1])
+
+    def scratch():
+        for r in range(R):
+            fill(r, toks[r], 0, last[0, r])
+
+    def shared():
+        fill(R, toks[0], 0, last[1, 0])
+        for r in range(1, R):
+            start = eng.share_prefix(R, R + r, P)
+            eng.reserve(R + r, P + U)
+            fill(R + r, toks[r], start, last[1, r])
+
+    scratch()  # warm-up
+    out = {"requests": R, "prefix": P, "own": U, "piece": piece}
+    for name, fn in (("scratch", scratch), ("shared", shared)):
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        out[name + "_ms"] = ms
+        out[name + "_prompt_tok_s"] = R * (P + U) / (ms / 1000.0)
+    out["bitwise_equal"] = bool(torch.equal(last[0].view(torch.int32),
+                                            last[1].view(torch.int32)))
+    return out
 
 
 def run_ours(args):

@@ -19,20 +19,87 @@ from .synth import PAGE_SIZE, ModelShape
 
 
 class PageAllocator:
-    """Free list of physical page ids, drawn in a seeded random order."""
+    """Free list of physical page ids, drawn in a seeded random order, with
+    a reference count per page in use: a page shared by several requests'
+    page tables (a common prefix) returns to the free list when the last
+    of them gives it back."""
 
     def __init__(self, n_pages: int, seed: int = 0):
         self.free = list(np.random.default_rng(seed).permutation(n_pages))
+        self.refs = {}
 
     def take(self, n: int):
         if n > len(self.free):
             raise RuntimeError("KV pool exhausted (%d pages asked, %d free)"
                                % (n, len(self.free)))
         out, self.free = self.free[:n], self.free[n:]
-        return [int(p) for p in out]
+        out = [int(p) for p in out]
+        for p in out:
+            self.refs[p] = 1
+        return out
+
+    def share(self, pages):
+        for p in pages:
+            p = int(p)
+            if p not in self.refs:
+                raise RuntimeError("page %d is not in use" % p)
+            self.refs[p] += 1
 
     def give_back(self, pages):
-        self.free.extend(int(p) for p in pages)
+        for p in pages:
+            p = int(p)
+            n = self.refs.get(p, 0)
+            if n <= 0:
+                raise RuntimeError("page %d given back but not in use" % p)
+            if n == 1:
+                del self.refs[p]
+                self.free.append(p)
+            else:
+                self.refs[p] = n - 1
+
+
+class PrefixIndex:
+    """Token-keyed index of cached KV prefixes in whole pages.
+
+    KV is bound to its logical prefix: with batch- and query-length-
+    invariant kernels the K and V of positions [0, 16 k) depend only on the
+    tokens there, not on the request, batch or step that computed them
+    (Vosti abstract: cached KV tied to its logical token prefix, a paged
+    prefix-sharing KV cache).  So a new request whose first 16 k tokens
+    equal a cached request's may point its page table at that request's
+    first k pages.  Only full pages are shared; the position after a shared
+    prefix always starts a page of the new request's own."""
+
+    def __init__(self):
+        self.by_prefix = {}   # tokens of a whole-page prefix -> [slots]
+
+    def add(self, slot: int, tokens):
+        """Record the whole-page prefixes of `tokens` (the slot's committed
+        KV) as available from `slot`."""
+        t = tuple(int(x) for x in tokens)
+        for k in range(1, len(t) // PAGE_SIZE + 1):
+            owners = self.by_prefix.setdefault(t[:k * PAGE_SIZE], [])
+            if slot not in owners:
+                owners.append(slot)
+
+    def drop(self, slot: int):
+        """Forget `slot` (before its pages are released)."""
+        for key in list(self.by_prefix):
+            owners = self.by_prefix[key]
+            if slot in owners:
+                owners.remove(slot)
+                if not owners:
+                    del self.by_prefix[key]
+
+    def lookup(self, tokens):
+        """(slot, n_positions) of the longest cached whole-page prefix of
+        `tokens` (its earliest recorded owner), or (None, 0)."""
+        t = tuple(int(x) for x in tokens)
+        for k in range(len(t) // PAGE_SIZE, 0, -1):
+            owners = self.by_prefix.get(t[:k * PAGE_SIZE])
+            if owners:
+                return owners[0], k * PAGE_SIZE
+        return None, 0
 
 
 class Engine:
@@ -127,6 +194,26 @@ class Engine:
         self.host_table[slot, :len(pages)] = pages
         self.page_table[slot] = torch.from_numpy(self.host_table[slot].copy()
                                                  ).to(self.device)
+
+    def share_prefix(self, src: int, dst: int, n_positions: int) -> int:
+        """Point the first n_positions // 16 page-table entries of the empty
+        slot `dst` at the pages holding positions [0, 16 k) of slot `src`
+        (whose KV there must be committed and computed from the same
+        tokens).  Returns 16 k, the first position `dst` must compute
+        itself; its later pages are its own (reserve)."""
+        k = n_positions // PAGE_SIZE
+        src_row, dst_row = self.host_table[src], self.host_table[dst]
+        if (dst_row >= 0).any():
+            raise RuntimeError("slot %d is not empty" % dst)
+        pages = src_row[:k]
+        if (pages < 0).any():
+            raise RuntimeError("slot %d has no pages for positions [0, %d)"
+                               % (src, k * PAGE_SIZE))
+        self.alloc.share(pages)
+        dst_row[:k] = pages
+        self.page_table[dst, :k] = torch.from_numpy(pages.copy()).to(
+            self.device)
+        return k * PAGE_SIZE
 
     def release(self, slot: int):
         row = self.host_table[slot]

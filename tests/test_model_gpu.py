@@ -198,6 +198,60 @@ def test_captured_decode_replays_bitwise(tiny, lib):
     assert lib.bi_device_status() == 0
 
 
+def test_prefix_sharing_bitwise(tiny, lib):
+    """Prefix caching (Vosti abstract: KV tied to its logical token prefix,
+    a paged prefix-sharing KV cache).  Request B's first 37 tokens equal
+    request A's; B takes A's first two whole KV pages (PrefixIndex lookup,
+    Engine.share_prefix) and computes only positions 32 onwards.  B's
+    logits equal those of B computed from scratch in another engine, bit
+    for bit, also after A is released and a third request has taken the
+    pages A gave back (the shared ones must not be among them)."""
+    from deterministic_invariant_bf16_gb300 import binding as bi
+    from deterministic_invariant_bf16_gb300 import synth
+    from deterministic_invariant_bf16_gb300.engine import PrefixIndex
+    shape = tiny[0]
+    rng = np.random.default_rng(77)
+    pa = list(synth.token_ids(40, shape.vocab, rng))
+    pb = pa[:37] + list(synth.token_ids(9, shape.vocab, rng))
+    n_new = 6
+    ref_l, ref_t = greedy_run(new_engine(tiny, page_seed=31), [pb], n_new,
+                              [[0]])
+
+    eng = new_engine(tiny, page_seed=32, n_pages=12)
+    eng.reserve(0, len(pa))
+    eng.prefill([(0, pa, 0)])
+    ix = PrefixIndex()
+    ix.add(0, pa)
+    src, n = ix.lookup(pb)
+    assert (src, n) == (0, 32)
+    start = eng.share_prefix(0, 1, n)
+    assert start == 32
+    eng.reserve(1, len(pb) + n_new)
+    shared = set(eng.host_table[0][:2])
+    assert set(eng.host_table[1][:2]) == shared
+    ids = torch.empty(1, dtype=torch.int32, device="cuda")
+    lg = eng.prefill([(1, pb[start:], start)])
+    bi.bi_argmax_logits(lg[-1:].contiguous(), ids)
+    rows, toks = [lg[-1].cpu().numpy()], [int(ids.item())]
+    # A leaves; C takes every free page and overwrites it
+    ix.drop(0)
+    eng.release(0)
+    assert not shared & set(eng.alloc.free)
+    free_now = len(eng.alloc.free)
+    pc = list(synth.token_ids(free_now * 16, shape.vocab, rng))
+    eng.reserve(2, len(pc))
+    eng.prefill([(2, pc, 0)])
+    for step in range(1, n_new):
+        lg = eng.decode([toks[-1]], [len(pb) + step - 1], [1], ids=ids)
+        rows.append(lg[0].cpu().numpy())
+        toks.append(int(ids.item()))
+    torch.cuda.synchronize()
+    assert toks == ref_t[0]
+    assert np.array_equal(np.stack(rows).view(np.uint32),
+                          ref_l[0].view(np.uint32))
+    assert lib.bi_device_status() == 0
+
+
 # ---------------------------------------------------------------- verify --
 
 def _decode_reference(tiny, prompts, n_new):
