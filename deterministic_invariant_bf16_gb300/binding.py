@@ -82,6 +82,7 @@ SIGNATURES = {
                             V, Z, V], I),
     "bi_argmax_logits": ([V, I, I, V, V], I),
     "philox_sample": ([V, I, I, V, V, F, V, V], I),
+    "philox_sample_top": ([V, I, I, V, V, F, I, F, V, V], I),
     "bi_model_workspace_size": ([ctypes.POINTER(ModelCfg)], Z),
     "bi_model_create": ([ctypes.POINTER(ModelCfg),
                          ctypes.POINTER(ModelWeights), V, Z,
@@ -267,6 +268,14 @@ def philox_sample(logits, request_id, step, temperature, ids, stream=None):
     T, V_ = logits.shape
     _check(lib().philox_sample(_p(logits), T, V_, _p(request_id), _p(step),
                                temperature, _p(ids), _stream(stream)))
+
+
+def philox_sample_top(logits, request_id, step, temperature, top_k, top_p,
+                      ids, stream=None):
+    T, V_ = logits.shape
+    _check(lib().philox_sample_top(_p(logits), T, V_, _p(request_id),
+                                   _p(step), temperature, top_k, top_p,
+                                   _p(ids), _stream(stream)))
 
 
 # -------------------------------------------------------------- model --

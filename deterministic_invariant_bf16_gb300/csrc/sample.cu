@@ -17,6 +17,8 @@
 // on nothing but the row.
 #include <float.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -302,6 +304,243 @@ __global__ void __launch_bounds__(SEL_THREADS)
     if (threadIdx.x == 0) ids[t] = max(s_last, 0);
 }
 
+
+// ------------------------------------------------------ top-k / top-p --
+//
+// Token order: larger logit first, equal logits by lower index; NaN ranks
+// as -inf, -0 as +0.  rank_key maps a logit to a uint32 whose unsigned
+// order is that order of values (ties are then broken by index).
+constexpr int TOPK_MAX = 1024;
+
+__device__ __forceinline__ uint32_t rank_key(float v) {
+    if (isnan(v)) v = -INFINITY;
+    if (v == 0.0f) v = 0.0f;
+    const uint32_t u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Calls f(i, x) for every logit of the row (float4 loads when aligned).
+template <class F>
+__device__ __forceinline__ void for_each_logit(const float *row, int V,
+                                               bool vec, F f) {
+    if (vec) {
+        const float4 *r4 = reinterpret_cast<const float4 *>(row);
+        for (int k = threadIdx.x; k < V / 4; k += SEL_THREADS) {
+            const float4 x = __ldg(r4 + k);
+            f(4 * k, x.x);
+            f(4 * k + 1, x.y);
+            f(4 * k + 2, x.z);
+            f(4 * k + 3, x.w);
+        }
+    } else {
+        for (int k = threadIdx.x; k < V; k += SEL_THREADS) f(k, row[k]);
+    }
+}
+
+// Exclusive prefix of one int per thread over the block (warp shuffles,
+// then the warp totals); *total gets the block sum.  Integer: exact.
+__device__ __forceinline__ int block_excl_scan_i32(int v, int *total) {
+    __shared__ int wt[SEL_THREADS / 32];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += n;
+    }
+    if (lane == 31) wt[w] = inc;
+    __syncthreads();
+    if (w == 0) {
+        int x = wt[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += n;
+        }
+        wt[lane] = x;
+    }
+    __syncthreads();
+    *total = wt[SEL_THREADS / 32 - 1];
+    const int r = (w > 0 ? wt[w - 1] : 0) + inc - v;
+    __syncthreads();
+    return r;
+}
+
+__global__ void __launch_bounds__(SEL_THREADS)
+    sample_top_kernel(const float *__restrict__ logits, int V,
+                      const uint64_t *__restrict__ request_id,
+                      const uint64_t *__restrict__ step, float tau, int K,
+                      float top_p, int32_t *__restrict__ ids) {
+    __shared__ uint32_t hist[256];
+    __shared__ unsigned long long cand[TOPK_MAX];
+    __shared__ float pw[TOPK_MAX], cs[TOPK_MAX];
+    __shared__ int s_bin, s_above, s_eq, n_cand;
+    const int t = blockIdx.x;
+    const float *row = logits + (int64_t)t * V;
+    const bool vec =
+        (V & 3) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    // 1. the key theta of the K-th ranked token: radix select, 8 bits a
+    // pass from the top; `rank` counts within the keys matching `prefix`.
+    uint32_t prefix = 0, mask = 0;
+    int rank = K, above = 0, n_eq = 0;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        if (threadIdx.x < 256) hist[threadIdx.x] = 0;
+        __syncthreads();
+        for_each_logit(row, V, vec, [&](int, float x) {
+            const uint32_t k = rank_key(x);
+            if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
+        });
+        __syncthreads();
+        if (warp == 0) {
+            // lane l holds bins 8l .. 8l+7; suffix sums over the lanes
+            uint32_t sl = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) sl += hist[8 * lane + j];
+            uint32_t suf = sl;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t n = __shfl_down_sync(0xffffffffu, suf, o);
+                if (lane + o < 32) suf += n;
+            }
+            const unsigned top =
+                __ballot_sync(0xffffffffu, suf >= (uint32_t)rank);
+            const int L = 31 - __clz((int)top);
+            if (lane == L) {
+                uint32_t acc = suf - sl;
+                int b = 8 * L + 7;
+                for (; b > 8 * L; --b) {
+                    if (acc + hist[b] >= (uint32_t)rank) break;
+                    acc += hist[b];
+                }
+                s_bin = b;
+                s_above = (int)acc;
+                s_eq = (int)hist[b];
+            }
+        }
+        __syncthreads();
+        prefix |= (uint32_t)s_bin << shift;
+        mask |= 0xffu << shift;
+        rank -= s_above;
+        above += s_above;
+        n_eq = s_eq;
+        __syncthreads();
+    }
+    const uint32_t theta = prefix;
+    const int need = K - above;  // tokens of key theta kept, 1 .. n_eq
+
+    // 2. the K kept tokens as (key << 32 | ~index): keys above theta, and
+    // the first `need` tokens of key theta in index order
+    if (threadIdx.x == 0) n_cand = 0;
+    for (int j = threadIdx.x; j < TOPK_MAX; j += SEL_THREADS) cand[j] = 0ull;
+    __syncthreads();
+    auto put = [&](int i, uint32_t k) {
+        const int at = atomicAdd(&n_cand, 1);
+        if (at < TOPK_MAX)
+            cand[at] = ((unsigned long long)k << 32) | (0xffffffffu - (uint32_t)i);
+    };
+    if (need == n_eq) {
+        for_each_logit(row, V, vec, [&](int i, float x) {
+            const uint32_t k = rank_key(x);
+            if (k >= theta) put(i, k);
+        });
+    } else {
+        // thread-ordered pieces of 4 consecutive tokens, so that a block
+        // scan of the per-thread counts ranks the ties in index order
+        int base = 0;
+        for (int c0 = 0; c0 < V; c0 += 4 * SEL_THREADS) {
+            const int i0 = c0 + 4 * threadIdx.x;
+            uint32_t k4[4];
+            int eq = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                k4[e] = i0 + e < V ? rank_key(row[i0 + e]) : 0u;
+                eq += (i0 + e < V && k4[e] == theta) ? 1 : 0;
+            }
+            int tot;
+            int r = base + block_excl_scan_i32(eq, &tot);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                if (i0 + e >= V) continue;
+                if (k4[e] > theta) {
+                    put(i0 + e, k4[e]);
+                } else if (k4[e] == theta) {
+                    if (r < need) put(i0 + e, k4[e]);
+                    ++r;
+                }
+            }
+            base += tot;
+        }
+    }
+    __syncthreads();
+
+    // 3. rank order: bitonic sort of the 1024 entries, descending (empty
+    // entries are 0 and sort last)
+    for (int size = 2; size <= TOPK_MAX; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = threadIdx.x; i < TOPK_MAX; i += SEL_THREADS) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const unsigned long long a = cand[i], b = cand[j];
+                    const bool desc = (i & size) == 0;
+                    if (desc ? a < b : a > b) {
+                        cand[i] = b;
+                        cand[j] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+
+    // 4. weights, sequential running sums, nucleus, inverse CDF
+    const float l0 = key_value((uint32_t)(cand[0] >> 32));
+    for (int j = threadIdx.x; j < K; j += SEL_THREADS)
+        pw[j] = expf(__fdiv_rn(
+            __fsub_rn(key_value((uint32_t)(cand[j] >> 32)), l0), tau));
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        auto index_of = [&](int j) {
+            return (int32_t)(0xffffffffu - (uint32_t)(cand[j] & 0xffffffffull));
+        };
+        if (n_cand != K || l0 == -INFINITY) {
+            ids[t] = index_of(0);
+            return;
+        }
+        int last_pos = 0;
+        float c = 0.0f;
+        for (int j = 0; j < K; ++j) {
+            c = __fadd_rn(c, pw[j]);
+            cs[j] = c;
+        }
+        int n = K - 1;
+        if (top_p < 1.0f) {
+            const float cut = __fmul_rn(top_p, cs[K - 1]);
+            for (int j = 0; j < K; ++j)
+                if (cs[j] >= cut) {
+                    n = j;
+                    break;
+                }
+        }
+        const float target =
+            __fmul_rn(sample_uniform(request_id[t], step[t]), cs[n]);
+        int chosen = -1;
+        for (int j = 0; j <= n; ++j) {
+            if (pw[j] > 0.0f) last_pos = j;
+            if (cs[j] > target) {
+                chosen = j;
+                break;
+            }
+        }
+        ids[t] = index_of(chosen >= 0 ? chosen : last_pos);
+    }
+}
+
 }  // namespace
 
 extern "C" bi_status bi_argmax_logits(const float *logits, int T, int V,
@@ -312,6 +551,31 @@ extern "C" bi_status bi_argmax_logits(const float *logits, int T, int V,
     BI_REQUIRE(bi_aligned16(logits), "bi_argmax_logits: logits alignment");
     argmax_kernel<<<T, SEL_THREADS, 0, bi_stream(stream)>>>(logits, V, ids);
     BI_LAUNCH_CHECK("argmax launch");
+    return BI_OK;
+}
+
+extern "C" bi_status philox_sample_top(const float *logits, int T, int V,
+                                       const uint64_t *request_id,
+                                       const uint64_t *step,
+                                       float temperature, int top_k,
+                                       float top_p, int32_t *ids,
+                                       void *stream) {
+    BI_REQUIRE(T >= 0 && V > 0, "philox_sample_top: T=%d V=%d", T, V);
+    BI_REQUIRE(temperature >= 0.f, "philox_sample_top: temperature < 0");
+    BI_REQUIRE(top_k >= 1, "philox_sample_top: top_k=%d", top_k);
+    BI_REQUIRE(top_p > 0.f && top_p <= 1.f, "philox_sample_top: top_p=%g",
+               (double)top_p);
+    if (top_k > TOPK_MAX)
+        return bi_fail(BI_ERR_UNSUPPORTED, "philox_sample_top: top_k=%d > %d",
+                       top_k, TOPK_MAX);
+    if (T == 0) return BI_OK;
+    BI_REQUIRE(logits && ids, "philox_sample_top: null pointer");
+    if (temperature == 0.f) return bi_argmax_logits(logits, T, V, ids, stream);
+    BI_REQUIRE(request_id && step, "philox_sample_top: null request_id/step");
+    sample_top_kernel<<<T, SEL_THREADS, 0, bi_stream(stream)>>>(
+        logits, V, request_id, step, temperature, std::min(top_k, V), top_p,
+        ids);
+    BI_LAUNCH_CHECK("sample top launch");
     return BI_OK;
 }
 

@@ -293,6 +293,23 @@ bi_status philox_sample(const float *logits, int T, int V,
                         const uint64_t *request_id, const uint64_t *step,
                         float temperature, int32_t *ids, void *stream);
 
+/* philox_sample restricted to the top_k most likely tokens and, within
+ * them, to the nucleus of mass top_p (the LLM-42 page's sampling
+ * hyperparameters, fixed per request).  Tokens are ranked by logit, larger
+ * first, equal logits by lower index, NaN as -inf; K = min(top_k, V).  In
+ * rank order p_j = exp((l_j - l_0) / temperature) and c_j are the
+ * sequential fp32 running sums; the kept tokens are the first n + 1, n the
+ * first j < K with c_j >= top_p * c_{K-1} (all K when top_p = 1); the token
+ * is the first kept j with c_j > u * c_n (u as in philox_sample), or, when
+ * rounding leaves none, the last kept j with p_j > 0.  temperature 0 means
+ * greedy.  1 <= top_k (above 1024: BI_ERR_UNSUPPORTED), 0 < top_p <= 1
+ * (else BI_ERR_INVALID_ARG).  One block per row; the result is a function
+ * of the row, request_id and step only. */
+bi_status philox_sample_top(const float *logits, int T, int V,
+                            const uint64_t *request_id, const uint64_t *step,
+                            float temperature, int top_k, float top_p,
+                            int32_t *ids, void *stream);
+
 /* ------------------------------------------------------------ the model --
  * Pre-norm Llama decoder: embed, n_layers x (RMSNorm, QKV GEMM, RoPE + KV
  * append, attention, O GEMM + residual, RMSNorm, gate/up GEMM with SwiGLU,

@@ -67,6 +67,8 @@ def _lib():
             "orc_sample_seed": [ctypes.c_uint64, ctypes.c_uint64],
             "orc_sample_uniform": [ctypes.c_uint64],
             "orc_philox_sample": [f32p, I, I, u64p, u64p, F, f32p, i32p],
+            "orc_philox_sample_top": [f32p, I, I, u64p, u64p, F, I, F, i32p,
+                                      f32p, i32p],
         }
         for name, args in sig.items():
             fn = getattr(lib, name)
@@ -229,6 +231,24 @@ def philox_sample(logits, request_id, step, tau) -> np.ndarray:
     if T:
         _lib().orc_philox_sample(logits, T, V, rid, st, float(tau), scratch,
                                  ids)
+    return ids
+
+
+def philox_sample_top(logits, request_id, step, tau, top_k, top_p):
+    """Temperature sampling within the top_k highest-ranked tokens (larger
+    logit first, ties to the lower index, NaN as -inf) and their nucleus of
+    mass top_p, inverse CDF in rank order with the request's Philox
+    uniform."""
+    logits = _f32(logits)
+    T, V = logits.shape
+    rid = np.ascontiguousarray(request_id, dtype=np.uint64)
+    st = np.ascontiguousarray(step, dtype=np.uint64)
+    ids = np.empty(T, np.int32)
+    if T:
+        _lib().orc_philox_sample_top(logits, T, V, rid, st, float(tau),
+                                     int(top_k), float(top_p),
+                                     np.empty(V, np.int32),
+                                     np.empty(V, np.float32), ids)
     return ids
 
 

@@ -19,6 +19,7 @@
  * bf16 values travel as uint16 bit patterns; fp32 everywhere else.
  */
 #include <math.h>
+#include <stdlib.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -317,5 +318,90 @@ void orc_philox_sample(const float *logits, int T, int V,
                 chosen = i;
         }
         ids[t] = chosen >= 0 ? chosen : last_pos;
+    }
+}
+
+/* ------------------------------------------------------ top-k / top-p -- */
+
+/* Order of tokens for top-k / top-p: larger logit first, equal logits by
+ * lower index; NaN ranks as -inf and -0 as +0. */
+static float rank_value(float v)
+{
+    if (isnan(v))
+        return -INFINITY;
+    return v == 0.0f ? 0.0f : v;
+}
+
+static const float *g_sort_row; /* row being sorted (one thread per call) */
+
+static int by_rank(const void *a, const void *b)
+{
+    const int32_t i = *(const int32_t *)a, j = *(const int32_t *)b;
+    const float x = rank_value(g_sort_row[i]), y = rank_value(g_sort_row[j]);
+    if (x != y)
+        return x > y ? -1 : 1;
+    return i < j ? -1 : (i > j ? 1 : 0);
+}
+
+/* Temperature sampling over the K = min(top_k, V) highest-ranked tokens
+ * and, within them, the nucleus of mass top_p: with the tokens in rank
+ * order and p_j = exp((l_j - l_0) / tau) (l_0 the largest logit), c_j the
+ * sequential fp32 running sums, the kept tokens are the first n + 1 where
+ * n is the first j < K with c_j >= top_p * c_{K-1} (all K when top_p = 1);
+ * the token is the first kept j (in rank order) with c_j > u * c_{n},
+ * u the request's Philox uniform.  Rounding that leaves no such j takes the
+ * last kept j with p_j > 0; a row whose largest logit is -inf (or NaN)
+ * takes the first-ranked token.  tau == 0 is greedy (orc_argmax).
+ * Sequential per row (the qsort order is a total order, so the result does
+ * not depend on the sort algorithm). */
+void orc_philox_sample_top(const float *logits, int T, int V,
+                           const uint64_t *request_id, const uint64_t *step,
+                           float tau, int top_k, float top_p,
+                           int32_t *order_scratch /* [V] */,
+                           float *c_scratch /* [V] */, int32_t *ids)
+{
+    if (tau == 0.0f) {
+        orc_argmax(logits, T, V, ids);
+        return;
+    }
+    const int K = top_k < V ? top_k : V;
+    for (int t = 0; t < T; ++t) {
+        const float *row = logits + (int64_t)t * V;
+        for (int i = 0; i < V; ++i)
+            order_scratch[i] = i;
+        g_sort_row = row;
+        qsort(order_scratch, (size_t)V, sizeof(int32_t), by_rank);
+        const float l0 = rank_value(row[order_scratch[0]]);
+        if (l0 == -INFINITY) {
+            ids[t] = order_scratch[0];
+            continue;
+        }
+        float c = 0.0f;
+        for (int j = 0; j < K; ++j) {
+            const float p = expf((rank_value(row[order_scratch[j]]) - l0) / tau);
+            c += p;
+            c_scratch[j] = c;
+        }
+        int n = K - 1;
+        if (top_p < 1.0f) {
+            const float cut = top_p * c_scratch[K - 1];
+            for (int j = 0; j < K; ++j)
+                if (c_scratch[j] >= cut) {
+                    n = j;
+                    break;
+                }
+        }
+        const float u = orc_sample_uniform(orc_sample_seed(request_id[t],
+                                                           step[t]));
+        const float target = u * c_scratch[n];
+        int chosen = -1, last_pos = 0;
+        for (int j = 0; j <= n; ++j) {
+            const float p = expf((rank_value(row[order_scratch[j]]) - l0) / tau);
+            if (p > 0.0f)
+                last_pos = j;
+            if (chosen < 0 && c_scratch[j] > target)
+                chosen = j;
+        }
+        ids[t] = order_scratch[chosen >= 0 ? chosen : last_pos];
     }
 }

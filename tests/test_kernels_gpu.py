@@ -360,6 +360,76 @@ def test_argmax_exact(bi, orc):
 
 # -------------------------------------------------------------- Philox --
 
+def _top_boundary_ok(x, rid, st, tau, k, top_p, a, b):
+    """Two draws of the same row may differ only where fp32 rounding (of
+    exp or the running sums) moves u * Z or the nucleus cut across a
+    boundary of the rank-order CDF."""
+    import oracle
+    v = np.where(np.isnan(x), -np.inf, x.astype(np.float64))
+    order = np.argsort(-v, kind="stable")[:k]
+    pv = np.exp((v[order] - v[order[0]]) / tau)
+    c = np.cumsum(pv)
+    cut = top_p * c[-1]
+    u = oracle.sample_uniform(oracle.sample_seed(int(rid), int(st)))
+    ja = int(np.nonzero(order == a)[0][0])
+    jb = int(np.nonzero(order == b)[0][0])
+    lo, hi = min(ja, jb), max(ja, jb)
+    tol = 1e-4 * c[-1]
+    n = int(np.nonzero(c >= cut * (1 - 1e-6))[0][0])
+    near_cut = top_p < 1 and abs(c[min(hi, len(c) - 1)] - cut) < tol or \
+        abs(c[lo] - cut) < tol
+    return near_cut or abs(c[lo] - u * c[n]) < tol
+
+
+def test_philox_sample_top_against_oracle(bi, orc):
+    """Top-k / top-p sampling against the oracle: ids equal except on CDF or
+    nucleus boundaries within fp32 rounding (at most 1% of rows); top_k = 1
+    is argmax; heavy ties at the cut (the index-ordered path); V not a
+    multiple of 4; K > V; the full 128256-token vocabulary; rows do not
+    depend on the batch."""
+    cases = [(1500, 1000, 50, 0.9, False), (1500, 1000, 1024, 0.95, False),
+             (1500, 1000, 7, 1.0, False), (800, 1001, 64, 0.8, False),
+             (600, 300, 1024, 1.0, False), (800, 512, 40, 0.9, True),
+             (16, 128256, 1024, 0.9, False)]
+    for ci, (T, V, k, top_p, ties) in enumerate(cases):
+        g = torch.Generator(device="cuda").manual_seed(70 + ci)
+        if ties:
+            x = torch.randint(0, 6, (T, V), generator=g, device="cuda").float()
+        else:
+            x = torch.randn(T, V, generator=g, device="cuda") * 2
+        rid = torch.arange(T, dtype=torch.int64, device="cuda") * 131 + ci
+        st = torch.arange(T, dtype=torch.int64, device="cuda") % 29
+        ids = torch.empty(T, dtype=torch.int32, device="cuda")
+        tau = 0.8
+        bi.philox_sample_top(x, rid, st, tau, k, top_p, ids)
+        sync_ok(bi)
+        got = ids.cpu().numpy()
+        xl = x.cpu().numpy()
+        rl, sl = rid.cpu().numpy().astype(np.uint64), st.cpu().numpy().astype(np.uint64)
+        ref = orc.philox_sample_top(xl, rl, sl, tau, k, top_p)
+        mism = np.nonzero(got != ref)[0]
+        assert len(mism) <= max(1, T // 100), (ci, len(mism))
+        for t in mism:
+            assert _top_boundary_ok(xl[t], rl[t], sl[t], tau, min(k, V),
+                                    top_p, got[t], ref[t]), (ci, t)
+        if ci == 0:
+            one = torch.empty(1, dtype=torch.int32, device="cuda")
+            bi.philox_sample_top(x[9:10].contiguous(), rid[9:10].contiguous(),
+                                 st[9:10].contiguous(), tau, k, top_p, one)
+            sync_ok(bi)
+            assert one.item() == got[9]
+            bi.philox_sample_top(x, rid, st, tau, 1, 1.0, ids)
+            sync_ok(bi)
+            assert np.array_equal(ids.cpu().numpy(), orc.argmax(xl))
+    x = torch.zeros(2, 64, device="cuda")
+    ids = torch.empty(2, dtype=torch.int32, device="cuda")
+    r = torch.zeros(2, dtype=torch.int64, device="cuda")
+    with pytest.raises(bi.BiError, match="UNSUPPORTED"):
+        bi.philox_sample_top(x, r, r, 1.0, 1025, 1.0, ids)
+    with pytest.raises(bi.BiError, match="INVALID"):
+        bi.philox_sample_top(x, r, r, 1.0, 8, 0.0, ids)
+
+
 def test_philox_sample_against_oracle(bi, orc):
     import oracle
     T, V, tau = 3000, 512, 0.8

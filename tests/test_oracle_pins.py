@@ -471,3 +471,96 @@ def test_pack_fifo():
     assert n == 16 and starts[-1] == 240
     n, starts = oracle.pack_fifo([40, 50, 60, 70, 80])
     assert n == 4 and sum([40, 50, 60, 70]) <= 256
+
+
+# ------------------------------------------------- top-k / top-p sampling --
+
+def _rank_order(row):
+    """Rank order of a row: larger value first, ties to the lower index,
+    NaN as -inf (numpy's stable sort on the negated values)."""
+    v = np.where(np.isnan(row), -np.inf, row.astype(np.float64))
+    return np.argsort(-v, kind="stable")
+
+
+def test_sample_top_reductions(orc):
+    """top_k = 1 and a nucleus smaller than the largest token's mass are
+    greedy; temperature 0 is argmax; K > V keeps every token."""
+    rng = np.random.default_rng(31)
+    x = rng.normal(size=(40, 300)).astype(np.float32)
+    rid = np.arange(40, dtype=np.uint64) * 11
+    st = np.arange(40, dtype=np.uint64)
+    am = np.argmax(x, 1)
+    assert np.array_equal(orc.philox_sample_top(x, rid, st, 0.9, 1, 1.0), am)
+    assert np.array_equal(orc.philox_sample_top(x, rid, st, 0.9, 50, 1e-6), am)
+    assert np.array_equal(orc.philox_sample_top(x, rid, st, 0.0, 50, 0.5), am)
+    # K >= V with top_p = 1: the token's rank-order CDF interval holds u*Z
+    ids = orc.philox_sample_top(x[:, :20], rid, st, 1.0, 1000, 1.0)
+    assert ids.min() >= 0 and ids.max() < 20
+
+
+def test_sample_top_ties_and_nan(orc):
+    """Equal logits at the cut keep the lower indices; NaN ranks last and
+    is never drawn."""
+    n = 2000
+    row = np.array([1.0, 3.0, 3.0, 3.0, 0.0, np.nan], np.float32)
+    lg = np.tile(row, (n, 1))
+    rid = np.full(n, 5, np.uint64)
+    st = np.arange(n, dtype=np.uint64)
+    ids = orc.philox_sample_top(lg, rid, st, 1.0, 2, 1.0)
+    assert set(np.unique(ids)) == {1, 2}
+    ids = orc.philox_sample_top(lg, rid, st, 1.0, 3, 1.0)
+    assert set(np.unique(ids)) == {1, 2, 3}
+    ids = orc.philox_sample_top(lg, rid, st, 1.0, 6, 1.0)
+    assert 5 not in set(np.unique(ids)) and {0, 4} <= set(np.unique(ids))
+
+
+def test_sample_top_frequencies(orc):
+    """Over many steps the draws follow the kept tokens' renormalised
+    probabilities (chi^2 at the 99.9% quantile)."""
+    p = np.array([0.05, 0.1, 0.15, 0.2, 0.2, 0.3])
+    row = np.log(p).astype(np.float32)
+    n = 6000
+    lg = np.tile(row, (n, 1))
+    rid = np.full(n, 9, np.uint64)
+    st = np.arange(n, dtype=np.uint64)
+    for k, top_p, kept, q99 in [(4, 1.0, [5, 3, 4, 2], 16.27),
+                                (6, 0.6, [5, 3, 4], 13.82)]:
+        ids = orc.philox_sample_top(lg, rid, st, 1.0, k, top_p)
+        assert set(np.unique(ids)) <= set(kept)
+        counts = np.bincount(ids, minlength=6)[kept]
+        exp = p[kept] / p[kept].sum() * n
+        assert ((counts - exp) ** 2 / exp).sum() < q99
+
+
+def test_sample_top_within_error_bound(orc):
+    """Against float64: the drawn token lies in the top-k set, inside the
+    nucleus, and its rank-order CDF interval holds u * Z up to fp32
+    rounding of the sums."""
+    import oracle
+    rng = np.random.default_rng(32)
+    T, V, tau = 300, 400, 0.7
+    x = (rng.normal(size=(T, V)) * 2).astype(np.float32)
+    rid = np.arange(T, dtype=np.uint64) * 7 + 1
+    st = np.arange(T, dtype=np.uint64) % 13
+    for k, top_p in [(100, 0.8), (400, 0.95), (17, 1.0)]:
+        ids = orc.philox_sample_top(x, rid, st, tau, k, top_p)
+        near = 0
+        for t in range(T):
+            order = _rank_order(x[t])[:k]
+            j = int(np.nonzero(order == ids[t])[0][0])
+            pv = np.exp((x[t][order].astype(np.float64) - x[t][order[0]]) / tau)
+            c = np.cumsum(pv)
+            n = int(np.nonzero(c >= top_p * c[-1] * (1 - 1e-6))[0][0])
+            assert j <= n + 1
+            u = oracle.sample_uniform(oracle.sample_seed(int(rid[t]),
+                                                          int(st[t])))
+            target = u * c[n]
+            lo = c[j - 1] if j > 0 else 0.0
+            tol = 1e-5 * c[-1]
+            assert lo <= target + tol and c[j] >= target - tol, (t, j)
+            cut_near = top_p < 1 and (
+                abs(c[n] - top_p * c[-1]) < tol or
+                (n > 0 and abs(c[n - 1] - top_p * c[-1]) < tol))
+            if j > n or abs(lo - target) < tol or cut_near:
+                near += 1
+        assert near <= T // 50
