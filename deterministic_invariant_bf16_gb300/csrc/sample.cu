@@ -311,6 +311,7 @@ __global__ void __launch_bounds__(SEL_THREADS)
 // as -inf, -0 as +0.  rank_key maps a logit to a uint32 whose unsigned
 // order is that order of values (ties are then broken by index).
 constexpr int TOPK_MAX = 1024;
+constexpr int TOPK_CAND = 2048;  // candidate buffer (>= TOPK_MAX)
 
 __device__ __forceinline__ uint32_t rank_key(float v) {
     if (isnan(v)) v = -INFINITY;
@@ -323,21 +324,41 @@ __device__ __forceinline__ float key_value(uint32_t k) {
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-// Calls f(i, x) for every logit of the row (float4 loads when aligned).
+// Calls f(i, x, live) for every logit of the row, 4 float4 loads in flight
+// per thread when aligned.  Every lane of a warp makes the same calls (the
+// ones past the row with live = false), so f may use warp collectives.
 template <class F>
 __device__ __forceinline__ void for_each_logit(const float *row, int V,
                                                bool vec, F f) {
     if (vec) {
+        constexpr int UNROLL = 4;
         const float4 *r4 = reinterpret_cast<const float4 *>(row);
-        for (int k = threadIdx.x; k < V / 4; k += SEL_THREADS) {
-            const float4 x = __ldg(r4 + k);
-            f(4 * k, x.x);
-            f(4 * k + 1, x.y);
-            f(4 * k + 2, x.z);
-            f(4 * k + 3, x.w);
+        const int n4 = V / 4;
+        const int span = UNROLL * SEL_THREADS;
+        for (int k0 = threadIdx.x & ~31; k0 < n4; k0 += span) {
+            const int base = k0 + (threadIdx.x & 31);
+            float4 x[UNROLL];
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                const int k = base + u * SEL_THREADS;
+                x[u] = k < n4 ? __ldg(r4 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                const int k = base + u * SEL_THREADS;
+                const bool live = k < n4;
+                f(4 * k, x[u].x, live);
+                f(4 * k + 1, x[u].y, live);
+                f(4 * k + 2, x[u].z, live);
+                f(4 * k + 3, x[u].w, live);
+            }
         }
     } else {
-        for (int k = threadIdx.x; k < V; k += SEL_THREADS) f(k, row[k]);
+        for (int k0 = threadIdx.x & ~31; k0 < V; k0 += SEL_THREADS) {
+            const int k = k0 + (threadIdx.x & 31);
+            const bool live = k < V;
+            f(k, live ? row[k] : 0.f, live);
+        }
     }
 }
 
@@ -376,25 +397,31 @@ __global__ void __launch_bounds__(SEL_THREADS)
                       const uint64_t *__restrict__ step, float tau, int K,
                       float top_p, int32_t *__restrict__ ids) {
     __shared__ uint32_t hist[256];
-    __shared__ unsigned long long cand[TOPK_MAX];
+    __shared__ unsigned long long cand[TOPK_CAND];
     __shared__ float pw[TOPK_MAX], cs[TOPK_MAX];
-    __shared__ int s_bin, s_above, s_eq, n_cand;
+    __shared__ int s_bin, s_above, s_eq, n_cand, s_n, s_first, s_last;
     const int t = blockIdx.x;
     const float *row = logits + (int64_t)t * V;
     const bool vec =
         (V & 3) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    // 1. the key theta of the K-th ranked token: radix select, 8 bits a
-    // pass from the top; `rank` counts within the keys matching `prefix`.
+    // 1. radix select, 8 bits a pass from the top: after each pass the
+    // K-th ranked key matches `prefix` under `mask`, `above` keys rank above
+    // the prefix and `rank` counts within it.  As soon as the keys at or
+    // above the prefix fit the candidate buffer, one more pass collects
+    // them all (the top K are among them, ranked above every other key);
+    // otherwise the select runs to the full key theta.
     uint32_t prefix = 0, mask = 0;
     int rank = K, above = 0, n_eq = 0;
+    bool early = false;
     for (int shift = 24; shift >= 0; shift -= 8) {
         if (threadIdx.x < 256) hist[threadIdx.x] = 0;
         __syncthreads();
-        for_each_logit(row, V, vec, [&](int, float x) {
+        for_each_logit(row, V, vec, [&](int, float x, bool live) {
             const uint32_t k = rank_key(x);
-            if ((k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
+            if (live && (k & mask) == prefix)
+                atomicAdd(&hist[(k >> shift) & 255u], 1u);
         });
         __syncthreads();
         if (warp == 0) {
@@ -430,28 +457,33 @@ __global__ void __launch_bounds__(SEL_THREADS)
         above += s_above;
         n_eq = s_eq;
         __syncthreads();
+        if (shift > 0 && above + n_eq <= TOPK_CAND) {
+            early = true;
+            break;
+        }
     }
-    const uint32_t theta = prefix;
-    const int need = K - above;  // tokens of key theta kept, 1 .. n_eq
 
-    // 2. the K kept tokens as (key << 32 | ~index): keys above theta, and
-    // the first `need` tokens of key theta in index order
+    // 2. candidates as (key << 32 | ~index), at most TOPK_CAND of them
     if (threadIdx.x == 0) n_cand = 0;
-    for (int j = threadIdx.x; j < TOPK_MAX; j += SEL_THREADS) cand[j] = 0ull;
+    for (int j = threadIdx.x; j < TOPK_CAND; j += SEL_THREADS) cand[j] = 0ull;
     __syncthreads();
     auto put = [&](int i, uint32_t k) {
         const int at = atomicAdd(&n_cand, 1);
-        if (at < TOPK_MAX)
+        if (at < TOPK_CAND)
             cand[at] = ((unsigned long long)k << 32) | (0xffffffffu - (uint32_t)i);
     };
-    if (need == n_eq) {
-        for_each_logit(row, V, vec, [&](int i, float x) {
+    const int need = K - above;  // (full select) tokens of key theta kept
+    if (early || need == n_eq) {
+        // every key at or above the prefix (early), or every key >= theta
+        for_each_logit(row, V, vec, [&](int i, float x, bool live) {
             const uint32_t k = rank_key(x);
-            if (k >= theta) put(i, k);
+            if (live && (k & mask) >= prefix) put(i, k);
         });
     } else {
-        // thread-ordered pieces of 4 consecutive tokens, so that a block
-        // scan of the per-thread counts ranks the ties in index order
+        // full key theta with ties at the cut: keys above theta, and the
+        // first `need` tokens of key theta in index order (thread-ordered
+        // pieces of 4 tokens, ranked by a block scan)
+        const uint32_t theta = prefix;
         int base = 0;
         for (int c0 = 0; c0 < V; c0 += 4 * SEL_THREADS) {
             const int i0 = c0 + 4 * threadIdx.x;
@@ -479,11 +511,11 @@ __global__ void __launch_bounds__(SEL_THREADS)
     }
     __syncthreads();
 
-    // 3. rank order: bitonic sort of the 1024 entries, descending (empty
-    // entries are 0 and sort last)
-    for (int size = 2; size <= TOPK_MAX; size <<= 1) {
+    // 3. rank order: bitonic sort, descending (empty entries are 0 and sort
+    // last); the first K entries are the kept tokens
+    for (int size = 2; size <= TOPK_CAND; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = threadIdx.x; i < TOPK_MAX; i += SEL_THREADS) {
+            for (int i = threadIdx.x; i < TOPK_CAND; i += SEL_THREADS) {
                 const int j = i ^ stride;
                 if (j > i) {
                     const unsigned long long a = cand[i], b = cand[j];
@@ -498,47 +530,59 @@ __global__ void __launch_bounds__(SEL_THREADS)
         }
     }
 
-    // 4. weights, sequential running sums, nucleus, inverse CDF
+    // 4. weights, sequential running sums (one thread: the order is part of
+    // the result), then the nucleus cut and the draw as block-wide searches
     const float l0 = key_value((uint32_t)(cand[0] >> 32));
     for (int j = threadIdx.x; j < K; j += SEL_THREADS)
         pw[j] = expf(__fdiv_rn(
             __fsub_rn(key_value((uint32_t)(cand[j] >> 32)), l0), tau));
-    __syncthreads();
     if (threadIdx.x == 0) {
-        auto index_of = [&](int j) {
-            return (int32_t)(0xffffffffu - (uint32_t)(cand[j] & 0xffffffffull));
-        };
-        if (n_cand != K || l0 == -INFINITY) {
-            ids[t] = index_of(0);
-            return;
-        }
-        int last_pos = 0;
+        s_n = K - 1;
+        s_first = 0x7fffffff;
+        s_last = 0;
+    }
+    __syncthreads();
+    auto index_of = [&](int j) {
+        return (int32_t)(0xffffffffu - (uint32_t)(cand[j] & 0xffffffffull));
+    };
+    if (n_cand < K || l0 == -INFINITY) {
+        if (threadIdx.x == 0) ids[t] = index_of(0);
+        return;
+    }
+    if (threadIdx.x == 0) {
         float c = 0.0f;
+#pragma unroll 8
         for (int j = 0; j < K; ++j) {
             c = __fadd_rn(c, pw[j]);
             cs[j] = c;
         }
-        int n = K - 1;
-        if (top_p < 1.0f) {
-            const float cut = __fmul_rn(top_p, cs[K - 1]);
-            for (int j = 0; j < K; ++j)
-                if (cs[j] >= cut) {
-                    n = j;
-                    break;
-                }
-        }
-        const float target =
-            __fmul_rn(sample_uniform(request_id[t], step[t]), cs[n]);
-        int chosen = -1;
-        for (int j = 0; j <= n; ++j) {
-            if (pw[j] > 0.0f) last_pos = j;
-            if (cs[j] > target) {
-                chosen = j;
-                break;
-            }
-        }
-        ids[t] = index_of(chosen >= 0 ? chosen : last_pos);
     }
+    __syncthreads();
+    // (K <= TOPK_MAX = SEL_THREADS: one j per thread; a warp reduction
+    // before each shared atomic)
+    static_assert(TOPK_MAX == SEL_THREADS, "one rank position per thread");
+    const int j = threadIdx.x;
+    if (top_p < 1.0f) {
+        const float cut = __fmul_rn(top_p, cs[K - 1]);
+        const int c = __reduce_min_sync(
+            0xffffffffu, j < K && cs[j] >= cut ? j : 0x7fffffff);
+        if (lane == 0) atomicMin(&s_n, c);
+        __syncthreads();
+    }
+    const int n = s_n;
+    const float target =
+        __fmul_rn(sample_uniform(request_id[t], step[t]), cs[n]);
+    const int f = __reduce_min_sync(
+        0xffffffffu, j <= n && cs[j] > target ? j : 0x7fffffff);
+    const int l = __reduce_max_sync(0xffffffffu,
+                                    j <= n && pw[j] > 0.0f ? j : 0);
+    if (lane == 0) {
+        atomicMin(&s_first, f);
+        atomicMax(&s_last, l);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        ids[t] = index_of(s_first != 0x7fffffff ? s_first : s_last);
 }
 
 }  // namespace
