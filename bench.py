@@ -407,6 +407,13 @@ def run_report(args):
         rep["decode_tok_s"][str(B)] = B * b.wl["iters"] / (ms / 1000.0)
         del b
         torch.cuda.empty_cache()
+    # LLM-42 with the cuBLAS path as the fast path (B = 256)
+    a = copy.copy(args)
+    a.batch = 256
+    b = Bench(a, dev, weights=W)
+    rep["llm42_fast_path"] = fast_path_report(b)
+    del b
+    torch.cuda.empty_cache()
     # prefill
     rng = np.random.default_rng(1005)
     R, piece = 8, 2048
@@ -683,17 +690,16 @@ def run_ours(args):
 
 # ------------------------------------------------------------- comparator --
 
-def run_comparator(b, args):
-    """The same decode iterations with every GEMM through torch.matmul
-    (cuBLAS default heuristics), the library's norm / RoPE / attention /
-    argmax around them, against the invariant path's decode iterations alone.
-    Run with the default bf16 reduced-precision setting and with it off
-    (ybb.press section 5)."""
+def cublas_forward(b):
+    """Decode forward of the bench's requests with every GEMM through
+    torch.matmul (cuBLAS heuristics: not batch-invariant), the library's
+    norm / RoPE / attention around them; returns fwd(tok, pos, maxkv) ->
+    fp32 logits [B, V]."""
     import torch
     bi = b.bi
     eng = b.eng
     S = b.shape
-    B, it = b.wl["batch"], b.wl["iters"]
+    B = b.wl["batch"]
     H, F, D, Hq, Hkv = S.hidden, S.ffn, S.head_dim, S.n_heads, S.n_kv_heads
     dev = b.dev
     x = torch.empty(B, H, dtype=torch.bfloat16, device=dev)
@@ -730,6 +736,20 @@ def run_comparator(b, args):
         bi.bi_rmsnorm(d, 1, None, h, W["final_norm"], B, H, S.eps, x)
         return torch.matmul(x, W["lm_head"].T).float()
 
+    return fwd
+
+
+def run_comparator(b, args):
+    """The same decode iterations with every GEMM through torch.matmul
+    (cuBLAS default heuristics), the library's norm / RoPE / attention /
+    argmax around them, against the invariant path's decode iterations alone.
+    Run with the default bf16 reduced-precision setting and with it off
+    (ybb.press section 5)."""
+    import torch
+    bi = b.bi
+    B, it = b.wl["batch"], b.wl["iters"]
+    fwd = cublas_forward(b)
+
     def run_cmp():
         cur = b.tok0.clone()
         for i in range(it):
@@ -763,6 +783,89 @@ def run_comparator(b, args):
     torch.backends.cuda.matmul.allow_bf16_reduced_precision_reduction = flag
     out["invariant_over_default"] = (out["invariant_decode_tok_s"] /
                                      out["cublas_default_tok_s"])
+    return out
+
+
+def fast_path_report(b, fractions=(0.02, 0.10, 0.50, 1.0)):
+    """LLM-42 with a real non-deterministic fast path (LLM-42 page, core
+    method: decode everything on the fast path, verify the deterministic
+    requests' windows with the invariant path, commit up to the first
+    mismatch).  Per deterministic fraction d, one round: 32 greedy decode
+    iterations of all B requests on the cuBLAS path, then the first
+    round(d * B) requests' 32-token windows verified in groups of 8 (256
+    rows) by verify_commit_rollback.  Committed tokens: 32 per unverified
+    request, commit length (+1 for the verifier's own token after a
+    mismatch) per verified one.  Against: 32 invariant decode iterations of
+    all B requests."""
+    import torch
+    eng, wl = b.eng, b.wl
+    B, w = wl["batch"], 32
+    ctx = wl["ctx"]
+    dev = b.dev
+    fwd = cublas_forward(b)
+    pos = [torch.from_numpy(ctx + i).to(dev).int() for i in range(w)]
+    maxkv = [int(ctx.max()) + i + 1 for i in range(w)]
+    ids = torch.empty(w, B, dtype=torch.int32, device=dev)
+    logits = torch.empty(B, b.shape.vocab, dtype=torch.float32, device=dev)
+
+    def fast():
+        cur = b.tok0
+        for i in range(w):
+            lg = fwd(cur, pos[i], maxkv[i])
+            b.bi.bi_argmax_logits(lg, ids[i])
+            cur = ids[i]
+
+    def invariant():
+        cur = b.tok0
+        for i in range(w):
+            eng.decode(cur, pos[i], b.slots, logits=logits, ids=ids[i],
+                       max_kv_len=maxkv[i])
+            cur = ids[i]
+
+    def rearm(slots):
+        for r in slots:
+            eng.reserve(r, int(ctx[r]) + wl["headroom"])
+
+    def timed(fn):
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        out = fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1), out
+
+    fast()
+    invariant()
+    inv_ms, _ = timed(invariant)
+    out = {"window": w, "batch": B,
+           "invariant_only_tok_s": B * w / (inv_ms / 1e3), "fractions": {}}
+    last = b.tok0.cpu().numpy()
+    for d in fractions:
+        n_f = max(1, int(round(d * B)))
+
+        def llm42():
+            fast()
+            cand = ids[:, :n_f].T.cpu().numpy()
+            res = []
+            for g in range(0, n_f, 8):
+                sl = list(range(g, min(n_f, g + 8)))
+                res.append(eng.verify(sl, ctx[sl], last[sl],
+                                      [list(map(int, cand[r])) for r in sl]))
+            return res
+
+        ms, res = timed(llm42)
+        commit = np.concatenate([r[1] for r in res])
+        rolled = int((commit < w).sum())
+        committed = (B - n_f) * w + int(commit.sum()) + rolled
+        out["fractions"][str(d)] = {
+            "verified": n_f, "ms": ms,
+            "committed_tok_s": committed / (ms / 1e3),
+            "windows_rolled_back": rolled,
+            "mean_commit": float(commit.mean()),
+            "recomputed": int((w - commit - 1)[commit < w].sum())}
+        rearm(range(n_f))
     return out
 
 
