@@ -380,18 +380,20 @@ def test_verify_grouping_invariance(tiny):
 
 # ------------------------------------------------------ one 8B layer --
 
-def test_one_8b_layer_decode_against_oracle(lib, orc):
+@pytest.mark.parametrize("B", [64, 256])
+def test_one_8b_layer_decode_against_oracle(lib, orc, B):
     """Config: Llama-3.1-8B layer (hidden 4096, 32/8 heads of 128, FFN
-    14336, theta 5e5), decode batch of 64 with lognormal contexts (median
-    512, sigma 1, clipped 16..4096), page size 16 in random order.  The layer
-    runs through the C ABI ops in model order; sampled rows are compared
-    with the oracle layer fed the same input and the same cache."""
+    14336, theta 5e5), decode batch of 64 (per-chunk attention items) and of
+    256 (the benchmark's batch: whole-row attention items, M = 256 GEMMs)
+    with lognormal contexts (median 512, sigma 1, clipped 16..4096), page
+    size 16 in random order.  The layer runs through the C ABI ops in model
+    order; sampled rows (and the longest context) are compared with the
+    oracle layer fed the same input and the same cache."""
     from deterministic_invariant_bf16_gb300 import synth
     bi = lib
     S = synth.LLAMA8B
     H, Hq, Hkv, D, F = S.hidden, S.n_heads, S.n_kv_heads, S.head_dim, S.ffn
-    B = 64
-    rng = np.random.default_rng(1003)
+    rng = np.random.default_rng(1003 + B)
     lens = synth.lognormal_lengths(B, 512, 1.0, 16, 4096, rng)
     w = synth.make_weights(S, 3, "cuda", n_layers=1)["layers"][0]
     table, n_pages = synth.paged_layout(lens, 16, rng, extra_pages=3)
@@ -441,7 +443,7 @@ def test_one_8b_layer_decode_against_oracle(lib, orc):
                      head_dim=D, ffn=F, vocab=16, eps=S.eps, theta=S.theta)
     lw = {k: np16(v) for k, v in w.items()}
     kb, vb = bits(kp), bits(vp)
-    for b in (0, 17, 63):
+    for b in sorted({0, 17, B - 1, int(np.argmax(lens))}):
         L = int(lens[b])
         kc = np.zeros((1, L, Hkv, D), np.float32)
         vc = np.zeros_like(kc)
