@@ -449,7 +449,10 @@ def run_report(args):
     torch.cuda.empty_cache()
     rep["prefix_sharing"] = prefix_report(torch, bi, engine, synth, shape, W,
                                           dev, piece)
+    rep["gemm_sweep"] = gemm_sweep(torch, bi, dev)
     rep["device_status"] = bi.bi_device_status()
+    # the oracle's own timings (CPU baseline) beside the GPU numbers
+    rep["cpu_baseline_configs"] = oracle_configs()
     print(json.dumps({"report": rep, "workload": WORKLOAD,
                       "data": "synthetic (random-init weights, random KV)"}),
           flush=True)
@@ -506,6 +509,115 @@ def prefix_report(torch, bi, engine, synth, shape, W, dev, piece):
         out[name + "_prompt_tok_s"] = R * (P + U) / (ms / 1000.0)
     out["bitwise_equal"] = bool(torch.equal(last[0].view(torch.int32),
                                             last[1].view(torch.int32)))
+    return out
+
+
+def gemm_sweep(torch, bi, dev):
+    """bi_gemm at the GEMM sweep's shapes: M = 1 .. 256 against a 4096 x 4096
+    weight, and at M = 256 the literal 14336 x 14336, the FFN shapes and the
+    LM head.  Split partials out (as the model uses it), weights cycled over
+    copies larger than L2, 20 launches per CUDA graph."""
+    import math
+    x = (torch.randn(256, 14336, device=dev) * 0.5).bfloat16()
+    out = torch.empty(8 * 256 * 128256, dtype=torch.float32, device=dev)
+    res = {}
+    cases = [(m, 4096, 4096) for m in (1, 2, 4, 8, 16, 32, 64, 128, 256)] + \
+        [(256, 14336, 14336), (256, 14336, 4096), (256, 4096, 14336),
+         (256, 128256, 4096)]
+    Ws, key = None, None
+    for M, N, K in cases:
+        if key != (N, K):
+            Ws = None
+            torch.cuda.empty_cache()
+            n = max(2, math.ceil(400e6 / (N * K * 2)))
+            Ws = [(torch.randn(N, K, device=dev) * 0.02).bfloat16()
+                  for _ in range(n)]
+            key = (N, K)
+        xm = x[:M, :K].contiguous()
+
+        def run():
+            for i in range(20):
+                bi.bi_gemm(xm, Ws[i % len(Ws)], out, bi.OUT_PARTIALS)
+
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            run()
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            run()
+        g.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(3):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / 60 * 1e3
+        wbytes = 2.0 * N * K + 2.0 * M * K + 4.0 * M * N
+        res["%dx%dx%d" % (M, N, K)] = {
+            "us": us, "GBps": wbytes / us / 1e3,
+            "TFLOPs": 2.0 * M * N * K / us / 1e6,
+            "splits": bi.bi_gemm_splits(N, K)}
+    del Ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def oracle_configs():
+    """The oracle as it stands on the host cores, beside the GPU numbers:
+    the 4096 x 4096 GEMM at M = 1, 8, 256; one 8B-shape decoder layer for
+    B = 1, 8, 32 decode rows (contexts from the step workload's
+    distribution); the tiny decoder's greedy run (8 requests, 16-token
+    prompts, 16 new tokens)."""
+    import oracle
+    from deterministic_invariant_bf16_gb300 import synth
+    rng = np.random.default_rng(11)
+    cores = len(os.sched_getaffinity(0))
+    out = {"cores": cores, "kind": "oracle", "gemm_4096": {}, "layer_8b": {}}
+    w = oracle.bf16_bits(rng.normal(0, 0.02, (4096, 4096)).astype(np.float32))
+    for M in (1, 8, 256):
+        x = oracle.bf16_bits(rng.normal(0, 1, (M, 4096)).astype(np.float32))
+        t0 = time.perf_counter()
+        oracle.gemm(x, w)
+        t = time.perf_counter() - t0
+        out["gemm_4096"][str(M)] = {"s": t, "GFLOPs": 2 * M * 4096 * 4096 / t / 1e9}
+    S = synth.LLAMA8B
+    cfg = oracle.Cfg(n_layers=1, hidden=S.hidden, n_heads=S.n_heads,
+                     n_kv_heads=S.n_kv_heads, head_dim=S.head_dim, ffn=S.ffn,
+                     vocab=256, eps=S.eps, theta=S.theta)
+    lw = oracle_weights()["layer"]
+    for B in (1, 8, 32):
+        L = synth.lognormal_lengths(B, 512, 1.0, 16, 4096, rng)
+        Lm = int(L.max())
+        kc = oracle.bf16r(rng.standard_normal((B, Lm, S.n_kv_heads, S.head_dim),
+                                              np.float32))
+        vc = oracle.bf16r(rng.standard_normal(kc.shape, np.float32))
+        h = oracle.bf16r(rng.standard_normal((B, S.hidden), np.float32))
+        t0 = time.perf_counter()
+        oracle.decoder_layer(h, np.arange(B, dtype=np.int32),
+                             (L - 1).astype(np.int32), lw, kc, vc, cfg)
+        t = time.perf_counter() - t0
+        out["layer_8b"][str(B)] = {"s": t, "rows_per_s": B / t}
+    tiny = synth.TINY
+    import torch
+    tw = synth.make_weights(tiny, 0, "cpu")
+
+    def u16(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    ow = dict(embed=u16(tw["embed"]), final_norm=u16(tw["final_norm"]),
+              lm_head=u16(tw["lm_head"]),
+              layers=[{k: u16(v) for k, v in lw_.items()}
+                      for lw_ in tw["layers"]])
+    prompts = [synth.token_ids(16, tiny.vocab, rng) for _ in range(8)]
+    t0 = time.perf_counter()
+    oracle.greedy_decode(prompts, 16, ow, oracle.Cfg())
+    t = time.perf_counter() - t0
+    out["tiny_greedy"] = {"s": t, "tok_s": 8 * 16 / t}
     return out
 
 
