@@ -152,10 +152,11 @@ def test_query_length_invariance_at_model_level(tiny):
 def test_repeated_runs_identical(tiny):
     shape = tiny[0]
     prompts = prompts8(shape)[:3]
-    a, _ = greedy_run(new_engine(tiny, 7), prompts, 4, [[0, 1, 2]])
-    b, _ = greedy_run(new_engine(tiny, 7), prompts, 4, [[0, 1, 2]])
-    for x, y in zip(a, b):
-        assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
+    runs = [greedy_run(new_engine(tiny, 7), prompts, 4, [[0, 1, 2]])[0]
+            for _ in range(3)]
+    for other in runs[1:]:
+        for x, y in zip(runs[0], other):
+            assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
 
 
 def test_captured_decode_replays_bitwise(tiny, lib):
