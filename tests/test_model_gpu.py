@@ -416,28 +416,41 @@ def test_one_8b_layer_decode_against_oracle(lib, orc, B):
         bi.bi_gemm(x, W, out, bi.OUT_PARTIALS)
         return out, s
 
-    h = h_in.clone()
-    x = torch.empty(B, H, dtype=torch.bfloat16, device="cuda")
-    bi.bi_rmsnorm(None, 0, None, h, w["attn_norm"], B, H, S.eps, x)
-    qkv, s1 = gemm_slices(x, w["wqkv"])
-    q = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
-    bi.bi_rope(qkv, s1, pos, rows, Hq, Hkv, D, S.theta, q, kp, vp, pt)
-    max_kv = int(lens.max())
-    ws = torch.empty(bi.bi_decode_attn_workspace_size(B, Hq, D, max_kv) // 4,
-                     dtype=torch.float32, device="cuda")
-    a = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
-    bi.bi_paged_decode_attn(q, kp, vp, pt, rows, kvl, max_kv,
-                            1 / math.sqrt(D), a, ws)
-    o, s2 = gemm_slices(a.view(B, Hq * D), w["wo"])
-    bi.bi_rmsnorm(o, s2, None, h, w["ffn_norm"], B, H, S.eps, x)
-    f = torch.empty(B, F, dtype=torch.bfloat16, device="cuda")
-    bi.bi_gemm(x, wgu, f, bi.OUT_SWIGLU)
-    d, s3 = gemm_slices(f, w["wd"])
-    y = torch.empty(B, H, dtype=torch.bfloat16, device="cuda")
-    bi.bi_rmsnorm(d, s3, None, h, w["attn_norm"], B, H, S.eps, y)
-    torch.cuda.synchronize()
-    assert bi.bi_device_status() == 0
-    h_out = orc.bf16_value(bits(h))
+    def layer(sel):
+        """The layer on the decode rows `sel` (a batch of len(sel))."""
+        n = len(sel)
+        idx = torch.as_tensor(sel, dtype=torch.long, device="cuda")
+        h = h_in[idx].contiguous()
+        x = torch.empty(n, H, dtype=torch.bfloat16, device="cuda")
+        bi.bi_rmsnorm(None, 0, None, h, w["attn_norm"], n, H, S.eps, x)
+        qkv, s1 = gemm_slices(x, w["wqkv"])
+        q = torch.empty(n, Hq, D, dtype=torch.bfloat16, device="cuda")
+        bi.bi_rope(qkv, s1, pos[idx].contiguous(), rows[idx].contiguous(),
+                   Hq, Hkv, D, S.theta, q, kp, vp, pt)
+        max_kv = int(lens[np.asarray(sel)].max())
+        ws = torch.empty(bi.bi_decode_attn_workspace_size(n, Hq, D, max_kv)
+                         // 4, dtype=torch.float32, device="cuda")
+        a = torch.empty(n, Hq, D, dtype=torch.bfloat16, device="cuda")
+        bi.bi_paged_decode_attn(q, kp, vp, pt, rows[idx].contiguous(),
+                                kvl[idx].contiguous(), max_kv,
+                                1 / math.sqrt(D), a, ws)
+        o, s2 = gemm_slices(a.view(n, Hq * D), w["wo"])
+        bi.bi_rmsnorm(o, s2, None, h, w["ffn_norm"], n, H, S.eps, x)
+        f = torch.empty(n, F, dtype=torch.bfloat16, device="cuda")
+        bi.bi_gemm(x, wgu, f, bi.OUT_SWIGLU)
+        d, s3 = gemm_slices(f, w["wd"])
+        y = torch.empty(n, H, dtype=torch.bfloat16, device="cuda")
+        bi.bi_rmsnorm(d, s3, None, h, w["attn_norm"], n, H, S.eps, y)
+        torch.cuda.synchronize()
+        assert bi.bi_device_status() == 0
+        return bits(h)
+
+    h_bits = layer(list(range(B)))
+    h_out = orc.bf16_value(h_bits)
+    # the longest-context row alone gives the same bits as inside the batch
+    # (K/V of its own position are rewritten with the same values)
+    far = int(np.argmax(lens))
+    assert np.array_equal(layer([far])[0], h_bits[far])
 
     import oracle
     cfg = oracle.Cfg(n_layers=1, hidden=H, n_heads=Hq, n_kv_heads=Hkv,
