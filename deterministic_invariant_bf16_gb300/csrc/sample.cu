@@ -15,6 +15,15 @@
 // prefix sums: thread k sums its contiguous slice in index order, the
 // slice totals are scanned by a fixed shuffle pattern, so the result depends
 // on nothing but the row.
+//
+// philox_sample_top: the same draw restricted to the top_k highest-ranked
+// tokens (larger logit first, ties to the lower index) and, within them, the
+// nucleus of mass top_p, the LLM-42 page's fixed sampling hyperparameters.
+// One block per row finds the K-th ranked key by an 8-bit radix select,
+// collects the keys at or above it (as soon as they fit a 2048-entry
+// buffer), sorts them into rank order, and one thread runs the fp32 running
+// sums in rank order; the cut and the draw are block-wide index searches.
+// Everything depends on the row, request_id and step only.
 #include <float.h>
 
 #include <algorithm>
