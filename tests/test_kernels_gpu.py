@@ -385,12 +385,14 @@ def test_philox_sample_top_against_oracle(bi, orc):
     """Top-k / top-p sampling against the oracle: ids equal except on CDF or
     nucleus boundaries within fp32 rounding (at most 1% of rows); top_k = 1
     is argmax; heavy ties at the cut (the index-ordered path); V not a
-    multiple of 4; K > V; the full 128256-token vocabulary; rows do not
-    depend on the batch."""
+    multiple of 4; K > V; the full 128256-token vocabulary at K = 1024 and
+    50, and a long row of only six distinct values (ties at the cut on the
+    index-ordered path); rows do not depend on the batch."""
     cases = [(1500, 1000, 50, 0.9, False), (1500, 1000, 1024, 0.95, False),
              (1500, 1000, 7, 1.0, False), (800, 1001, 64, 0.8, False),
              (600, 300, 1024, 1.0, False), (800, 512, 40, 0.9, True),
-             (16, 128256, 1024, 0.9, False)]
+             (16, 128256, 1024, 0.9, False), (16, 128256, 50, 1.0, False),
+             (6, 131072, 64, 0.9, True)]
     for ci, (T, V, k, top_p, ties) in enumerate(cases):
         g = torch.Generator(device="cuda").manual_seed(70 + ci)
         if ties:
