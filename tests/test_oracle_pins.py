@@ -409,6 +409,202 @@ def test_causality_and_incremental_decode(orc):
         assert np.array_equal(step[0], full[p])
 
 
+# ------------------------------------- decoder composition, float64 --
+#
+# The pre-norm Llama block (RMSNorm -> QKV -> RoPE -> causal GQA attention ->
+# O projection + residual -> RMSNorm of the post-attention residual -> SwiGLU
+# FFN + residual) and the model head (untied embedding gather, final RMSNorm,
+# LM head) are the reading the oracle takes of the operators the pages name
+# (LLM-42 summary, 核心方法: GEMM, attention and normalisation kernels;
+# ybb.press section 1: residual and normalisation).  Below they are written a
+# second time, independently of ``oracle/``, in float64 numpy with bf16
+# rounding (torch's CPU conversion) at the same storage points, plus a closed
+# form whose FFN branch is a known function of its normed input.
+
+
+def _bf(x):
+    """float64 -> bf16 -> float64 through torch's CPU conversions."""
+    t = torch.from_numpy(np.ascontiguousarray(x, np.float64)).to(torch.float32)
+    return t.to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def _w64(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
+        torch.bfloat16).to(torch.float64).numpy()
+
+
+def _f64_norm(x, w, eps):
+    return x / np.sqrt((x * x).mean(axis=1, keepdims=True) + eps) * w
+
+
+def _f64_block(h, pos, lw, cfg):
+    """One block for the rows of ONE request at positions ``pos`` (its
+    cache empty before the call), float64 arithmetic."""
+    W = {k: _w64(v) for k, v in lw.items()}
+    T = h.shape[0]
+    Hq, Hkv, D = cfg.n_heads, cfg.n_kv_heads, cfg.head_dim
+    x = _bf(_f64_norm(h, W["attn_norm"], cfg.eps))
+    qkv = _bf(x @ W["wqkv"].T)
+    q = qkv[:, :Hq * D].reshape(T, Hq, D)
+    k = qkv[:, Hq * D:(Hq + Hkv) * D].reshape(T, Hkv, D)
+    v = qkv[:, (Hq + Hkv) * D:].reshape(T, Hkv, D)
+    half = D // 2
+    ang = np.asarray(pos, np.float64)[:, None] * cfg.theta ** (
+        -2.0 * np.arange(half) / D)[None, :]
+    rot = np.exp(1j * ang)[:, None, :]
+
+    def rope(t):
+        z = (t[..., :half] + 1j * t[..., half:]) * rot
+        return np.concatenate([z.real, z.imag], axis=-1)
+
+    q, k = _bf(rope(q)), _bf(rope(k))
+    out = np.zeros((T, Hq, D))
+    for t in range(T):
+        vis = np.asarray(pos) <= pos[t]
+        for hh in range(Hq):
+            g = hh // (Hq // Hkv)
+            s = k[vis, g] @ q[t, hh] / math.sqrt(D)
+            p = np.exp(s - s.max())
+            out[t, hh] = (p / p.sum()) @ v[vis, g]
+    h = _bf(h + _bf(out.reshape(T, Hq * D)) @ W["wo"].T)
+    x2 = _bf(_f64_norm(h, W["ffn_norm"], cfg.eps))
+    g, u = x2 @ W["wg"].T, x2 @ W["wu"].T
+    f = _bf(g / (1.0 + np.exp(-g)) * u)
+    return _bf(h + f @ W["wd"].T)
+
+
+def _relerr(a, b):
+    return float(np.linalg.norm(np.asarray(a, np.float64) - b)
+                 / np.linalg.norm(b))
+
+
+def test_decoder_layer_float64_brute_force(orc):
+    """The oracle's block against the float64 restatement: the whole output
+    and the residual branch alone (output minus input) agree norm-wise to
+    well within what one bf16 rounding step per storage point allows.  A
+    block that normalises the layer input instead of the post-attention
+    residual for the FFN misses the branch by tens of percent."""
+    w, cfg = _tiny_weights()
+    rng = np.random.default_rng(31)
+    T = 12
+    h = orc.bf16r(rng.normal(0, 0.5, size=(T, cfg.hidden)).astype(np.float32))
+    pos = np.arange(T, dtype=np.int32)
+    for lw in w["layers"]:
+        kc, vc = orc.new_caches(cfg, 1, 16)[0]
+        got = orc.decoder_layer(h, np.zeros(T, np.int32), pos, lw, kc, vc,
+                                cfg)
+        ref = _f64_block(h.astype(np.float64), pos, lw, cfg)
+        assert _relerr(got, ref) < 2e-3
+        assert _relerr(got - h, ref - h) < 1e-2
+
+
+def test_model_forward_float64_brute_force(orc):
+    """Embedding gather, two blocks, final RMSNorm and LM head against the
+    float64 restatement: logits within 1e-2 norm-wise, the per-layer hidden
+    states within 2e-3.  Dropping the final norm scales the logits by the
+    reciprocal RMS of the last hidden state (about 4x here)."""
+    w, cfg = _tiny_weights()
+    rng = np.random.default_rng(32)
+    T = 10
+    ids = rng.integers(0, cfg.vocab, size=T)
+    pos = np.arange(T, dtype=np.int32)
+    hidden = []
+    got = orc.model_forward(ids, np.zeros(T, np.int32), pos, w,
+                            orc.new_caches(cfg, 1, 16), cfg,
+                            hidden_out=hidden)
+    h = _w64(w["embed"])[ids]
+    assert np.array_equal(hidden[0].astype(np.float64), h)
+    for li, lw in enumerate(w["layers"]):
+        h = _f64_block(h, pos, lw, cfg)
+        assert _relerr(hidden[li + 1], h) < 2e-3
+    x = _bf(_f64_norm(h, _w64(w["final_norm"]), cfg.eps))
+    ref = x @ _w64(w["lm_head"]).T
+    assert _relerr(got, ref) < 1e-2
+
+
+def test_decoder_layer_ffn_closed_form(orc):
+    """A block whose weights make every step a known function, one row at
+    position 0 (attention over one key returns that key's value exactly):
+      * V rows of wqkv = a permutation P, wo = identity, so the
+        post-attention residual is h2 = bf16(h + P n(h)), n = RMSNorm;
+      * gate rows (x, -x), up rows (x/4, x/4) and wd = [I I], so the FFN
+        returns, per feature, silu(x) x/4 + silu(-x) x/4 = x^2 tanh(x/2) / 4
+        of its normed input x = n(h2).
+    The block output is therefore bf16(h2 + n(h2)^2 tanh(n(h2)/2) / 4).  The
+    FFN reading n(h) instead of n(h2), swapped gate and up (x^2 tanh(x/8)/4),
+    V taken from the K rows, or a dropped residual each miss it by far more
+    than the bf16 rounding of the intermediate values."""
+    cfg = orc.Cfg(n_layers=1)
+    H, F = cfg.hidden, cfg.ffn
+    assert F == 2 * H and cfg.q_dim == H and cfg.kv_dim == H
+
+    def bits(a):
+        t = torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16)
+        return t.view(torch.int16).numpy().view(np.uint16)
+
+    rng = np.random.default_rng(33)
+    perm = rng.permutation(H)
+    P = np.eye(H)[perm]
+    eye = np.eye(H)
+    wqkv = np.concatenate([rng.normal(0, 0.02, size=(2 * H, H)), P])
+    lw = dict(attn_norm=bits(np.ones(H)), wqkv=bits(wqkv), wo=bits(eye),
+              ffn_norm=bits(np.ones(H)), wg=bits(np.concatenate([eye, -eye])),
+              wu=bits(np.concatenate([eye, eye]) / 4),
+              wd=bits(np.concatenate([eye, eye], axis=1)))
+    h = orc.bf16r(rng.normal(0, 1.0, size=(1, H)).astype(np.float32))
+    kc, vc = orc.new_caches(cfg, 1, 4)[0]
+    got = orc.decoder_layer(h, np.zeros(1, np.int32), np.zeros(1, np.int32),
+                            lw, kc, vc, cfg).astype(np.float64)
+
+    def n(x):
+        return x / np.sqrt((x * x).mean() + cfg.eps)
+
+    h64 = h.astype(np.float64)
+    h2 = _bf(h64 + _bf(n(h64))[:, perm])
+    x = n(h2)
+    want = h2 + x * x * np.tanh(x / 2) / 4
+    # every intermediate is rounded to bf16 once or twice: a few bf16 ulps
+    # of the output's magnitude
+    tol = 8 * 2.0 ** -8 * np.abs(want).max()
+    assert np.abs(got - want).max() < tol
+    xn = n(h64)
+    for wrong in (h2 + xn * xn * np.tanh(xn / 2) / 4,
+                  h2 + x * x * np.tanh(x / 8) / 4,
+                  x * x * np.tanh(x / 2) / 4):
+        assert np.abs(wrong - want).max() > 4 * tol
+
+
+def test_model_head_closed_form(orc):
+    """A model with no blocks: logits = LM head . bf16(RMSNorm(E[id])).  With
+    LM-head row v the unit vector e_(v mod H) times 2^(v // H), logit v is
+    2^(v // H) times feature v mod H of the normed embedding row, exactly
+    (one nonzero product per sum)."""
+    cfg = orc.Cfg(n_layers=0)
+    H, V = cfg.hidden, cfg.vocab
+    rng = np.random.default_rng(34)
+    embed = rand_bf16_bits(rng, (V, H), std=0.02)
+    head = np.zeros((V, H), np.float32)
+    head[np.arange(V), np.arange(V) % H] = 2.0 ** (np.arange(V) // H)
+    t = torch.from_numpy(head).to(torch.bfloat16)
+    w = dict(embed=embed, layers=[], final_norm=_bits_ones(H),
+             lm_head=t.view(torch.int16).numpy().view(np.uint16))
+    ids = rng.integers(0, V, size=6)
+    got = orc.model_forward(ids, np.zeros(6, np.int32),
+                            np.arange(6, dtype=np.int32), w, [], cfg)
+    e = _w64(embed)[ids]
+    x = _bf(e / np.sqrt((e * e).mean(axis=1, keepdims=True) + cfg.eps))
+    want = x[:, np.arange(V) % H] * 2.0 ** (np.arange(V) // H)
+    # x is bf16 on both sides; the normalisation itself differs by at most
+    # one bf16 rounding step
+    assert np.abs(got - want).max() <= 2.0 ** -7 * np.abs(want).max()
+    assert np.array_equal(np.sign(got), np.sign(want))
+
+
+def _bits_ones(n):
+    t = torch.ones(n, dtype=torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
 def test_greedy_tokens_identical_at_batch_1_and_32(orc):
     """ybb.press section 8, item 1: batch=1 and batch=32 outputs must be
     token-identical."""
