@@ -12,11 +12,16 @@ processed tokens is N(0, 1) bf16 in randomly ordered 16-token pages.
 
 One step = 10 invariant decode iterations of all 256 requests (greedy for
 flagged requests, Philox temperature sampling keyed by (request, step) for
-the rest) followed by one fixed 256-row grouped verification of 8 flagged
-requests' 32-token candidate windows with commit and rollback.  Ten
-iterations per verify is the ratio 10% deterministic traffic implies
-(26 flagged requests x 10 tokens ~ one 256-row verify batch).  The metric
-counts decoded tokens: 10 x 256 per step.
+the rest) followed by one fixed 256-row grouped verification with commit and
+rollback: 4, 8 or 16 flagged requests' windows of 64, 32 or 16 candidates
+(the group size cycling from step to step, the requests rotating through
+the 26 flagged ones), each candidate perturbed with probability 0.003 to
+force mismatches.  Ten iterations per verify is the ratio 10% deterministic
+traffic implies (26 flagged requests x 10 tokens ~ one 256-row verify
+batch).  The page table, the decode iterations and the verification of a
+step are one CUDA graph; the step's verify plan is copied into its device
+buffers before the replay.  The metric counts decoded tokens: 10 x 256 per
+step.
 
 Run with no flags for one GPU.  Under torchrun (N > 1) every rank runs an
 independent replica (the path has no exchange step) and the line reports the
@@ -76,11 +81,12 @@ def make_workload(batch, iters, seed=1003):
     progress = rng.uniform(0.0, 1.0, size=batch)
     ctx = (prompts + np.floor(progress * outputs)).astype(np.int64)
     n_flag = max(1, int(round(0.10 * batch)))
-    n_ver = min(8, n_flag)
-    window = 256 // n_ver
+    # verify groups of g requests with windows of 256 / g candidates
+    groups = [g for g in (4, 8, 16) if g <= n_flag] or [n_flag]
+    max_window = 256 // min(groups)
     return dict(batch=batch, iters=iters, ctx=ctx, prompts=prompts,
-                outputs=outputs, n_flag=n_flag, n_ver=n_ver, window=window,
-                headroom=iters + window + 2,
+                outputs=outputs, n_flag=n_flag, groups=groups,
+                max_window=max_window, headroom=max(iters, max_window) + 2,
                 first_tokens=synth.token_ids(batch, synth.LLAMA8B.vocab, rng),
                 rng=rng)
 
@@ -178,6 +184,33 @@ def recorded_traffic(kernel_class):
     return rec.get("bytes_per_launch")
 
 
+def versions():
+    """What produced the numbers (ybb.press section 6 item 4 and section 8:
+    record the engine, library, driver and flag versions): the library's
+    source hash and compiler flags, CUDA, torch, the driver and the GPU."""
+    import torch
+    from deterministic_invariant_bf16_gb300 import build
+    out = {"libbi_source_sha256": build.source_hash()[:16],
+           "nvcc_flags": " ".join(build.ARCH + build.NVCC_FLAGS[:-2]),
+           "torch": torch.__version__, "cuda_runtime": torch.version.cuda}
+    try:
+        q = subprocess.run(["nvidia-smi", "--query-gpu=driver_version,name",
+                            "--format=csv,noheader"], capture_output=True,
+                           text=True, timeout=20).stdout.strip().splitlines()
+        if q:
+            drv, name = [x.strip() for x in q[0].split(",", 1)]
+            out.update(driver=drv, gpu=name)
+    except (OSError, subprocess.TimeoutExpired, ValueError):
+        pass
+    try:
+        nv = subprocess.run([build.nvcc(), "--version"], capture_output=True,
+                            text=True, timeout=20).stdout.strip().splitlines()
+        out["nvcc"] = nv[-1] if nv else None
+    except (OSError, RuntimeError, subprocess.TimeoutExpired):
+        pass
+    return out
+
+
 def aggregate(ms_local, tokens_per_step_per_rank, world, dist=None,
               device="cpu"):
     """Replicas: every rank decodes its own requests; the step time is the
@@ -192,6 +225,43 @@ def aggregate(ms_local, tokens_per_step_per_rank, world, dist=None,
 
 
 # --------------------------------------------------------------- our arm ----
+
+def verify_plans(wl, greedy, V, n_plans=None, seed=2024):
+    """The verify plans the steps cycle through.  Plan k takes g =
+    groups[k mod len(groups)] flagged requests (the g after plan k-1's,
+    modulo the flagged count) with windows of 256 / g candidates starting at
+    their current context: row 0 feeds the request's last token, the
+    candidates are its greedy continuation (greedy[r]), each perturbed with
+    probability 0.003 to (t + 1 + U[0, V-1)) mod V.  The expected commit of
+    a window is its first perturbed index (its length if none).  Returns
+    (plans as int32 arrays in the device plan layout, expected commits per
+    plan, plan metadata)."""
+    from deterministic_invariant_bf16_gb300 import binding as bi
+    rng = np.random.default_rng(seed)
+    groups = wl["groups"]
+    n_plans = n_plans or 3 * wl["n_flag"]
+    plans, expect, meta = [], [], []
+    at = 0
+    for k in range(n_plans):
+        g = groups[k % len(groups)]
+        w = 256 // g
+        reqs = [(at + i) % wl["n_flag"] for i in range(g)]
+        at = (at + g) % wl["n_flag"]
+        wins, exp = [], []
+        for r in reqs:
+            c = np.array(greedy[r][:w], np.int64)
+            flip = rng.uniform(size=w) < 0.003
+            c[flip] = (c[flip] + 1 + rng.integers(0, V - 1,
+                                                  size=flip.sum())) % V
+            wins.append([int(x) for x in c])
+            exp.append(int(np.argmax(flip)) if flip.any() else w)
+        kv = [int(wl["ctx"][r]) for r in reqs]
+        last = [int(wl["first_tokens"][r]) for r in reqs]
+        plans.append(bi.VerifyBuffers.host_plan(reqs, kv, last, wins))
+        expect.append(exp)
+        meta.append(dict(g=g, w=w, reqs=reqs, kv=kv, windows=wins))
+    return plans, expect, meta
+
 
 class Bench:
     def __init__(self, args, device, weights=None):
@@ -236,6 +306,8 @@ class Bench:
         self.tau = 0.7
         self.n_flag = wl["n_flag"]
         self._make_candidates()
+        self.table0 = self.eng.page_table.clone()
+        self._make_plans()
 
     def decode_iters(self, n=None):
         bi, eng = self.bi, self.eng
@@ -251,11 +323,10 @@ class Bench:
                              ids[F:])
 
     def _make_candidates(self):
-        """Candidate windows of the verified requests: their own invariant
-        greedy continuation (32 decode iterations run once here), with each
-        candidate perturbed with probability 0.003 to force mismatches."""
+        """Candidates of the flagged requests: their own invariant greedy
+        continuation (max_window decode iterations run once here)."""
         wl = self.wl
-        nv, w = wl["n_ver"], wl["window"]
+        w = wl["max_window"]
         ctx = wl["ctx"]
         keep_pos, keep_maxkv = self.pos, self.maxkv
         self.pos = self.torch.stack([self.torch.from_numpy(ctx + i).to(
@@ -265,39 +336,76 @@ class Bench:
         self.ids = self.torch.empty(w, wl["batch"], dtype=self.torch.int32,
                                     device=self.dev)
         self.decode_iters(w)
-        cand = self.ids[:, :nv].T.cpu().numpy().copy()
+        self.greedy = self.ids[:, :self.n_flag].T.cpu().numpy().copy()
         self.pos, self.maxkv, self.ids = keep_pos, keep_maxkv, keep_ids
-        rng = wl["rng"]
-        flip = rng.uniform(size=cand.shape) < 0.003
-        V = self.shape.vocab
-        cand[flip] = (cand[flip] + 1 + rng.integers(0, V - 1, size=flip.sum())) % V
-        self.cand = [list(map(int, c)) for c in cand]
-        self.v_slots = list(range(nv))
-        self.v_kv = [int(c) for c in ctx[:nv]]
-        self.v_last = [int(t) for t in wl["first_tokens"][:nv]]
-        self.commits = []
 
-    def verify(self):
-        wl = self.wl
-        taken, commit, fix, freed = self.eng.verify(
-            self.v_slots, self.v_kv, self.v_last, self.cand,
-            logits=self.vlogits)
-        self.commits.append((taken, commit.copy(), fix.copy()))
-        for r in self.v_slots:  # pages for the next step's positions
-            self.eng.reserve(r, int(wl["ctx"][r]) + wl["headroom"])
+    def _make_plans(self, n_plans=None):
+        from deterministic_invariant_bf16_gb300 import binding as bi
+        plans, expect, meta = verify_plans(self.wl, self.greedy,
+                                           self.shape.vocab, n_plans)
+        self.plans_host = self.torch.from_numpy(np.stack(plans)).pin_memory()
+        self.plans_dev = self.plans_host.to(self.dev)
+        self.plan_expect = expect
+        self.plan_meta = meta
+        self.vbufs = self.eng.verify_buffers()
+        n = bi.VERIFY_ROWS
+        self.out_len = 8 + 2 * n
+        self.records = self.torch.zeros(len(plans), self.out_len,
+                                        dtype=self.torch.int32,
+                                        device=self.dev)
+        self.step_no = 0
+
+    def step_ops(self):
+        """The device work of one step (what the graph holds): the page
+        table back to its reserved rows (the previous verify cut the rows
+        of rolled-back requests; the pages are this bench's to re-reserve),
+        the decode iterations, the grouped verification."""
+        self.eng.page_table.copy_(self.table0)
+        self.decode_iters()
+        self.eng.verify_device(self.vbufs, self.vlogits)
+
+    def verify_ops(self):
+        self.eng.page_table.copy_(self.table0)
+        self.eng.verify_device(self.vbufs, self.vlogits)
 
     def capture(self):
-        """Capture one step's decode iterations (the library's calls, same
-        buffers and arguments) as a CUDA graph through Engine.capture; the
-        verify part syncs with the host and stays eager."""
-        self.graph = self.eng.capture(self.decode_iters)
+        """One step as a CUDA graph (Engine.capture).  The capture's first
+        run executes the ops once; the page table is restored by every
+        replay."""
+        self.vbufs.plan.copy_(self.plans_dev[0])
+        self.graph = self.eng.capture(self.step_ops)
+        self.vgraph = self.eng.capture(self.verify_ops)
+
+    def load_plan(self, k, host=False):
+        src = self.plans_host[k] if host else self.plans_dev[k]
+        self.vbufs.plan.copy_(src, non_blocking=True)
 
     def step(self, graph=False):
+        k = self.step_no % len(self.plan_expect)
+        self.load_plan(k)
         if graph and getattr(self, "graph", None) is not None:
             self.graph.replay()
         else:
-            self.decode_iters()
-        self.verify()
+            self.step_ops()
+        self.records[k].copy_(self.vbufs.out[:self.out_len])
+        self.step_no += 1
+
+    def check_commits(self):
+        """Commits of every plan run so far against the forced
+        perturbations: (windows checked, mismatches, per-plan commits)."""
+        rec = self.records.cpu().numpy()
+        n = self.bi.VERIFY_ROWS
+        checked = bad = 0
+        for k, exp in enumerate(self.plan_expect):
+            if rec[k, 0] == 0:
+                continue   # plan not run
+            taken = int(rec[k, 0])
+            got = rec[k, 8:8 + taken]
+            checked += len(exp)
+            bad += int(taken != len(exp)) * len(exp)
+            if taken == len(exp):
+                bad += int((got != np.array(exp)).sum())
+        return checked, bad, rec
 
 
 def algorithmic_bytes(b, cls, launches_per_step):
@@ -354,22 +462,89 @@ def gemm_flops(b, cls):
     return 2.0 * B * N * K
 
 
-def verify_stats(b, ms):
-    """The step's grouped verification: windows, rollbacks (windows cut
-    before their end), candidates recomputed (those after the first
-    mismatch) and the committed output rate of the step (decoded tokens of
-    the unverified rows plus the committed tokens of the verified ones)."""
+def verify_stats(b, ms, rec):
+    """The grouped verification over the plans the steps ran: windows,
+    rollbacks (windows cut before their end), candidates recomputed (those
+    after a window's first mismatch), the recompute fraction (recomputed /
+    committed candidates, the LLM-42 summary's "extra recomputed tokens",
+    section 5.1, Table 2), the commits checked against the forced
+    perturbations, and the committed output rate (tokens decoded for the
+    requests not in the step's verify group plus the verified candidates
+    committed, over the step's device time)."""
     wl = b.wl
-    w = wl["window"]
-    commit = [int(x) for x in b.commits[-1][1]]
-    committed = sum(commit)
-    recomputed = sum(w - j for j in commit)
-    out_tokens = (wl["batch"] - wl["n_ver"]) * wl["iters"] + committed
-    return {"windows": len(commit), "window": w,
-            "rollbacks": sum(1 for j in commit if j < w),
-            "committed": committed, "recomputed": recomputed,
-            "recompute_fraction": recomputed / float(len(commit) * w),
-            "committed_tok_s": out_tokens / (ms / 1000.0)}
+    n = b.bi.VERIFY_ROWS
+    ran = [k for k in range(len(b.plan_expect)) if rec[k, 0] > 0]
+    windows = rollbacks = committed = recomputed = out_tokens = 0
+    for k in ran:
+        taken = int(rec[k, 0])
+        w = b.plan_meta[k]["w"]
+        commit = rec[k, 8:8 + taken]
+        windows += taken
+        rollbacks += int((commit < w).sum())
+        committed += int(commit.sum())
+        recomputed += int((w - commit).sum())
+        out_tokens += (wl["batch"] - taken) * wl["iters"] + int(commit.sum())
+    checked, bad, _ = b.check_commits()
+    per = max(1, len(ran))
+    return {"plans_run": len(ran), "groups": wl["groups"],
+            "windows_per_step": windows / per,
+            "rollbacks_per_step": rollbacks / per,
+            "committed_per_step": committed / per,
+            "recomputed_per_step": recomputed / per,
+            "recompute_fraction": recomputed / max(1, committed),
+            "commits_checked": checked, "commit_mismatches": bad,
+            "committed_tok_s": out_tokens / per / (ms / 1000.0)}
+
+
+def verify_bytes(b, k):
+    """Algorithmic bytes of verify plan k: every layer's weights and the LM
+    head once, the gathered embedding rows, each window's K and V over its
+    whole context (kv_len + w positions) read once and its own w positions
+    written, and the fp32 logits written."""
+    S = b.shape
+    L = b.args.layers
+    H, F, V = S.hidden, S.ffn, S.vocab
+    n = b.bi.VERIFY_ROWS
+    kv_pos = S.n_kv_heads * S.head_dim * 2 * 2   # K and V bytes/position
+    layer_w = 2.0 * (S.qkv_dim * H + H * S.q_dim + 2 * F * H + H * F)
+    m = b.plan_meta[k]
+    ctx = sum(kv + m["w"] for kv in m["kv"])
+    rows = m["w"] * len(m["reqs"])
+    return (L * layer_w + 2.0 * V * H + n * H * 2.0 +
+            L * kv_pos * (ctx + rows) + n * V * 4.0)
+
+
+def verify_attn_bytes(b, k):
+    """Algorithmic bytes of one verify attention launch (one layer): each
+    window's K and V over kv_len + w positions, the 256 rows' queries in and
+    outputs out."""
+    S = b.shape
+    m = b.plan_meta[k]
+    kv_pos = S.n_kv_heads * S.head_dim * 2 * 2
+    qo = b.bi.VERIFY_ROWS * S.n_heads * S.head_dim * 2 * 2
+    return kv_pos * sum(kv + m["w"] for kv in m["kv"]) + qo
+
+
+def time_verify(b, reps):
+    """The step's verification alone, replayed as its own CUDA graph (page
+    table restore + device-side verify) over the plans in turn."""
+    torch = b.torch
+    P = len(b.plan_expect)
+    for k in range(3):
+        b.load_plan(k % P)
+        b.vgraph.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for r in range(reps):
+        b.load_plan(r % P)
+        b.vgraph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    byt = sum(verify_bytes(b, r % P) for r in range(reps)) / reps
+    return ms, byt
 
 
 def run_report(args):
@@ -392,15 +567,15 @@ def run_report(args):
         a = copy.copy(args)
         a.batch = B
         b = Bench(a, dev, weights=W)
-        b.capture()
+        dgraph = b.eng.capture(b.decode_iters)
         for _ in range(3):
-            b.graph.replay()
+            dgraph.replay()
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record()
         for _ in range(args.steps):
-            b.graph.replay()
+            dgraph.replay()
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1) / args.steps
@@ -643,14 +818,12 @@ def run_ours(args):
         if world > 1:
             dist.barrier()
 
-    for _ in range(args.warmup):
-        b.step()
-    torch.cuda.synchronize()
     use_graph = not args.no_graph
     if use_graph:
         b.capture()
-        b.step(graph=True)
-        torch.cuda.synchronize()
+    for _ in range(args.warmup):
+        b.step(graph=use_graph)
+    torch.cuda.synchronize()
     # ---- device-resident timed region (inputs are in HBM: weights 16 GB,
     # KV ~20 GB, far beyond the 129 MB L2, so no flush is needed)
     barrier()
@@ -668,12 +841,17 @@ def run_ours(args):
     barrier()
     clk = clocks.stop()
     ms = e0.elapsed_time(e1) / args.steps
+    rec = b.check_commits()[2]
+    # ---- the grouped verification alone (its own graph)
+    v_ms, v_bytes = time_verify(b, 3 * len(b.plan_expect)) if use_graph \
+        else (None, None)
     # ---- the same steps again with every kernel launch of the forward
     # bracketed by CUDA events on its stream (per-kernel time for the
     # roofline); kept out of the headline region above.
     bi.bi_model_profile(b.eng.handle, True)
     ep0 = torch.cuda.Event(enable_timing=True)
     ep1 = torch.cuda.Event(enable_timing=True)
+    first_prof = b.step_no
     ep0.record(stream)
     for _ in range(args.steps):
         b.step()
@@ -682,32 +860,42 @@ def run_ours(args):
     ms_profiled = ep0.elapsed_time(ep1) / args.steps
     prof = bi.bi_model_profile_read(b.eng.handle)
     bi.bi_model_profile(b.eng.handle, False)
+    prof_plans = [(first_prof + i) % len(b.plan_expect)
+                  for i in range(args.steps)]
     status = bi.bi_device_status()
     ms, value = aggregate(ms, tokens_per_step, world,
                           dist if world > 1 else None, dev)
 
     # ---- end to end through the public API with host buffers: every step
-    # uploads its inputs from pinned host memory into the buffers the
-    # decode graph (Engine.capture) reads, replays it, runs the verify
-    # group, and reads back the tokens.
+    # uploads its inputs (tokens, positions, sampling steps, verify plan)
+    # from pinned host memory into the buffers the step's graph reads,
+    # replays it, and reads back every decoded token and the verify results.
     h_in_tok = b.tok0.cpu().pin_memory()
     h_in_pos = b.pos.cpu().pin_memory()
     h_in_step = b.stepv.cpu().pin_memory()
     h_out = torch.empty(it, B, dtype=torch.int32).pin_memory()
+    h_vout = torch.empty(b.out_len, dtype=torch.int32).pin_memory()
     bytes_in = (h_in_tok.numel() * 4 + h_in_pos.numel() * 4 +
-                h_in_step.numel() * 8)
-    bytes_out = h_out.numel() * 4
+                h_in_step.numel() * 8 + b.plans_host[0].numel() * 4)
+    bytes_out = h_out.numel() * 4 + h_vout.numel() * 4
     barrier()
     torch.cuda.synchronize()
     e2 = torch.cuda.Event(enable_timing=True)
     e3 = torch.cuda.Event(enable_timing=True)
     e2.record(stream)
     for _ in range(args.steps):
+        k = b.step_no % len(b.plan_expect)
         b.tok0.copy_(h_in_tok, non_blocking=True)
         b.pos.copy_(h_in_pos, non_blocking=True)
         b.stepv.copy_(h_in_step, non_blocking=True)
-        b.step(graph=use_graph)
+        b.load_plan(k, host=True)
+        if use_graph:
+            b.graph.replay()
+        else:
+            b.step_ops()
+        b.step_no += 1
         h_out.copy_(b.ids, non_blocking=True)
+        h_vout.copy_(b.vbufs.out[:b.out_len], non_blocking=True)
         stream.synchronize()
     e3.record(stream)
     torch.cuda.synchronize()
@@ -716,7 +904,7 @@ def run_ours(args):
                               dist if world > 1 else None, dev)
     e2e = {"value": v_e2e, "unit": UNIT,
            "h2d_bytes_per_step": bytes_in,
-           "d2h_bytes_per_step": bytes_out + 3 * 4 * b.wl["n_ver"]}
+           "d2h_bytes_per_step": bytes_out}
 
     # ---- roofline of the dominant kernel (largest share of device time)
     pk = peaks()
@@ -761,8 +949,26 @@ def run_ours(args):
     launches = sum(v[1] for v in prof.values()) / args.steps
     # kernels the profile does not bracket: per decode iteration the
     # kv-length setup, the greedy argmax and the Philox sampler; per verify
-    # the commit kernel.  Every bracketed class is one kernel per launch.
-    launches += 3 * it + 1
+    # the packing and commit kernels.  Every bracketed class is one kernel
+    # per launch.
+    launches += 3 * it + 2
+    pk_hbm = pk["hbm"]
+    verify = verify_stats(b, ms, rec)
+    if v_ms:
+        verify.update({"verify_ms": v_ms,
+                       "verify_algorithmic_bytes": v_bytes,
+                       "verify_GBps": v_bytes / (v_ms / 1e3) / 1e9,
+                       "verify_hbm_frac": v_bytes / (v_ms / 1e3) / 1e9 /
+                       pk_hbm,
+                       "verify_timing": "own CUDA graph (page-table restore "
+                                        "+ pack + 256-row forward + commit),"
+                                        " plans in turn"})
+    if "attn_prefill" in kernels:
+        ab = sum(verify_attn_bytes(b, k) for k in prof_plans) / len(prof_plans)
+        per = prof["attn_prefill"][0] / prof["attn_prefill"][1]
+        kernels["attn_prefill"]["GBps"] = ab / (per / 1e3) / 1e9
+        kernels["attn_prefill"]["hbm_frac"] = \
+            kernels["attn_prefill"]["GBps"] / pk_hbm
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -772,13 +978,13 @@ def run_ours(args):
                    "layers": args.layers, "batch": B,
                    "decode_iters_per_step": it,
                    "verify_rows_per_step": 256,
-                   "verify_windows": "%d x %d" % (b.wl["n_ver"],
-                                                  b.wl["window"]),
+                   "verify_windows": "g x 256/g, g cycling over %s" %
+                                     (b.wl["groups"],),
                    "deterministic_fraction": b.wl["n_flag"] / B,
                    "mean_context": float(b.wl["ctx"].mean()),
                    "l2": "inputs larger than L2 (weights + KV >> 129 MB)",
                    "parallelism": "replicas" if world > 1 else "single",
-                   "decode_launch": "cuda_graph" if use_graph else "eager",
+                   "step_launch": "cuda_graph" if use_graph else "eager",
                    "e2e_launch": "cuda_graph" if use_graph else "eager"},
         "e2e": e2e,
         "gpu_launches": int(round(launches * args.steps)),
@@ -787,8 +993,8 @@ def run_ours(args):
         "profiled_ms_per_step": ms_profiled,
         "clocks": clk,
         "device_status": status,
-        "verify_commits": [int(x) for x in b.commits[-1][1]],
-        "verify": verify_stats(b, ms),
+        "verify": verify,
+        "versions": versions(),
     }
     if rank == 0 and not args.no_comparator:
         line["comparator"] = run_comparator(b, args)

@@ -94,6 +94,9 @@ SIGNATURES = {
                                ctypes.POINTER(ctypes.c_int64)], I),
     "verify_commit_rollback": ([V, I, I32P, I32P, I32P, I32P, I32P, V, V,
                                 I32P, I32P, I32P, I, I32P, I32P, V, V], I),
+    "verify_commit_rollback_device": ([V, V, V, V, V, V, V, V, V, V, V, V,
+                                       I, V, V, V, V], I),
+    "bi_model_hidden": ([V, ctypes.POINTER(V)], I),
 }
 
 
@@ -346,3 +349,100 @@ def verify_commit_rollback(handle, req, kv_len_host, last_token, win_len,
         ctypes.byref(taken), _p(logits), _stream(stream)))
     n = taken.value
     return n, commit[:n], fix[:n], freed[:n_freed.value]
+
+
+class VerifyBuffers:
+    """Device buffers of one verify_commit_rollback_device call: the plan
+    (window count, per-window request / KV length / last token / length,
+    candidates) and the results (commit length, fix token, freed pages and
+    their count, windows taken).  ``load`` fills the plan from host lists
+    (a caller that captures the call refills these buffers between
+    replays); ``read`` returns the results as numpy arrays."""
+
+    def __init__(self, freed_cap, device="cuda"):
+        import torch
+        n = VERIFY_ROWS
+        i32 = dict(dtype=torch.int32, device=device)
+        # plan: [0] = R, then req, kv_len, last token, window length (n
+        # each) and n candidates
+        self.plan = torch.zeros(8 + 5 * n, **i32)
+        self.n_windows = self.plan[0:1]
+        self.req = self.plan[8:8 + n]
+        self.win_kv_len = self.plan[8 + n:8 + 2 * n]
+        self.last_token = self.plan[8 + 2 * n:8 + 3 * n]
+        self.win_len = self.plan[8 + 3 * n:8 + 4 * n]
+        self.candidates = self.plan[8 + 4 * n:8 + 5 * n]
+        # results: [0] = taken, [1] = n_freed, commit, fix, freed pages
+        self.freed_cap = int(freed_cap)
+        self.out = torch.zeros(8 + 2 * n + max(self.freed_cap, 1), **i32)
+        self.taken = self.out[0:1]
+        self.n_freed = self.out[1:2]
+        self.commit_len = self.out[8:8 + n]
+        self.fix_token = self.out[8 + n:8 + 2 * n]
+        self.freed = self.out[8 + 2 * n:]
+
+    @staticmethod
+    def host_plan(req, kv_len, last_token, windows):
+        """The plan as one int32 array in the layout of ``plan`` (windows
+        past the fixed batch's capacity are dropped from the candidates,
+        as the packing never reads them)."""
+        n = VERIFY_ROWS
+        a = np.zeros(8 + 5 * n, np.int32)
+        R = len(req)
+        if not 1 <= R < n:
+            raise ValueError("1 <= number of windows < %d" % n)
+        a[0] = R
+        a[8:8 + R] = req
+        a[8 + n:8 + n + R] = kv_len
+        a[8 + 2 * n:8 + 2 * n + R] = last_token
+        a[8 + 3 * n:8 + 3 * n + R] = [len(w) for w in windows]
+        cands = np.concatenate([np.asarray(w, np.int32) for w in windows])
+        cands = cands[:n]
+        a[8 + 4 * n:8 + 4 * n + len(cands)] = cands
+        return a
+
+    def load(self, req, kv_len, last_token, windows):
+        import torch
+        self.plan.copy_(torch.from_numpy(
+            self.host_plan(req, kv_len, last_token, windows)))
+
+    def read(self):
+        """(taken, commit_len, fix_token, freed_pages) as numpy arrays."""
+        o = self.out.cpu().numpy()
+        n, nf = int(o[0]), int(o[1])
+        m = VERIFY_ROWS
+        return (n, o[8:8 + n].copy(), o[8 + m:8 + m + n].copy(),
+                o[8 + 2 * m:8 + 2 * m + min(nf, self.freed_cap)].copy())
+
+
+def verify_commit_rollback_device(handle, bufs: VerifyBuffers, page_table,
+                                  kv_len, logits, stream=None):
+    """Enqueues the device-side verification on ``bufs`` (no host sync)."""
+    b = bufs
+    _check(lib().verify_commit_rollback_device(
+        handle, _p(b.n_windows), _p(b.req), _p(b.win_kv_len),
+        _p(b.last_token), _p(b.win_len), _p(b.candidates), _p(page_table),
+        _p(kv_len), _p(b.commit_len), _p(b.fix_token), _p(b.freed),
+        b.freed_cap, _p(b.n_freed), _p(b.taken), _p(logits),
+        _stream(stream)))
+
+
+def bi_model_hidden(handle, T, hidden):
+    """The residual stream of the last forward of T rows (a bf16 [T][hidden]
+    tensor viewing the model's workspace)."""
+    import torch
+    ptr = ctypes.c_void_p()
+    _check(lib().bi_model_hidden(handle, ctypes.byref(ptr)))
+    return _view_bf16(ptr.value, T, hidden)
+
+
+def _view_bf16(addr, rows, cols):
+    """A torch bf16 [rows][cols] tensor over device memory at ``addr`` (not
+    owned; valid while the memory is)."""
+    import torch
+
+    class _Mem:
+        __cuda_array_interface__ = {
+            "shape": (rows, cols), "typestr": "<i2", "version": 3,
+            "data": (addr, False), "strides": None}
+    return torch.as_tensor(_Mem(), device="cuda").view(torch.bfloat16)

@@ -10,6 +10,7 @@ from __future__ import annotations
 
 import concurrent.futures as cf
 import glob
+import hashlib
 import os
 import shutil
 import subprocess
@@ -43,17 +44,35 @@ def _deps():
             glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def source_hash(extra_flags=None) -> str:
+    """sha256 over every source and header the library is built from and the
+    compiler flags: the key that decides whether libbi.so is current (file
+    times say nothing once a tree has been copied to another machine)."""
+    h = hashlib.sha256()
+    for path in sorted(_deps()):
+        h.update(os.path.relpath(path, HERE).encode())
+        with open(path, "rb") as f:
+            h.update(f.read())
+    h.update(" ".join(ARCH + NVCC_FLAGS[:-2] + list(extra_flags or []))
+             .encode())
+    return h.hexdigest()
+
+
+STAMP = LIB + ".sha256"
+
+
+def _stale(extra_flags=None) -> bool:
+    if not os.path.exists(LIB) or not os.path.exists(STAMP):
         return True
-    t = os.path.getmtime(LIB)
-    return any(os.path.getmtime(p) > t for p in _deps())
+    with open(STAMP) as f:
+        return f.read().strip() != source_hash(extra_flags)
 
 
 def build(force: bool = False, verbose: bool = False,
           extra_flags=None) -> str:
-    if not force and not _stale():
+    if not force and not _stale(extra_flags):
         return LIB
+    key = source_hash(extra_flags)
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
     flags = ARCH + NVCC_FLAGS + list(extra_flags or [])
@@ -78,6 +97,8 @@ def build(force: bool = False, verbose: bool = False,
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(key + "\n")
     return LIB
 
 

@@ -62,16 +62,26 @@ struct Layout {
     int S_qkv, S_o, S_d;
 };
 
-// Integer scratch of one verify call (device side), in int32 units.
+// Integer scratch of one verify call (device side), in int32 units: the
+// packed rows and segments of the fixed batch, the argmax ids, the plan of
+// the host entry point (uploaded there) and its outputs (downloaded there).
 struct VerifyIdx {
     static constexpr int T = BI_VERIFY_ROWS;
+    // segments of the forward: the taken windows, one pad segment, then
+    // empty segments up to this fixed count, so that the forward's launch
+    // configuration never depends on the plan
+    static constexpr int NSEG = T + 1;
     static constexpr int TOK = 0, POS = T, ROWREQ = 2 * T, CAND = 3 * T,
                          CUQ = 4 * T, SEGREQ = 5 * T + 8, SEGSTART = 6 * T + 16,
                          SEGW = 7 * T + 16, SEGKV = 8 * T + 16,
-                         IDS = 9 * T + 16, PACKED = 9 * T + 16,
-                         OUT_COMMIT = 10 * T + 16, OUT_FIX = 11 * T + 16,
-                         OUT_NFREED = 12 * T + 16, OUT_FREED = 12 * T + 32,
-                         COUNT = 12 * T + 32;
+                         IDS = 9 * T + 16, TAKEN = 10 * T + 16,
+                         PLAN = 10 * T + 24, PLAN_R = PLAN,
+                         PLAN_REQ = PLAN + 8, PLAN_KV = PLAN_REQ + T,
+                         PLAN_LAST = PLAN_KV + T, PLAN_WIN = PLAN_LAST + T,
+                         PLAN_CAND = PLAN_WIN + T, OUT = PLAN_CAND + T,
+                         OUT_TAKEN = OUT, OUT_NFREED = OUT + 1,
+                         OUT_COMMIT = OUT + 8, OUT_FIX = OUT_COMMIT + T,
+                         OUT_FREED = OUT_FIX + T, COUNT = OUT_FREED;
 };
 
 Layout layout(const bi_model_cfg &c, int max_pages_total) {
@@ -114,15 +124,131 @@ __global__ void kvlen_kernel(const int32_t *pos, int T, int32_t *kvlen) {
     if (t < T) kvlen[t] = pos[t] + 1;
 }
 
-// One thread per packed request: first mismatch, commit, rollback.  The
+// Packs a verify plan into the fixed batch (LLM-42 section 4.3: windows
+// taken first-in first-out while their rows fit).  One block of
+// BI_VERIFY_ROWS threads.  The windows' fields are staged in shared memory
+// and thread 0 walks them in order, with exactly the checks of the host
+// entry point: every window up to the first that does not fit must have
+// w >= 1, kv_len >= 0 and req >= 0; every taken window must end within
+// max_kv_len and name a request no earlier taken window names.  A plan that
+// fails a check (or has R outside [1, BI_VERIFY_ROWS)) takes no window and
+// records BI_ERR_BOUNDS; the batch is then all pad rows.  Then thread i
+// fills row i: window row k of request r sits at position kv_len_r + k with
+// input token last_r (k = 0) or candidate k - 1, compared with candidate k;
+// rows after the taken windows are pad rows (token 0, no request).
+__global__ void pack_kernel(const int32_t *__restrict__ n_windows,
+                            const int32_t *__restrict__ req,
+                            const int32_t *__restrict__ kvl,
+                            const int32_t *__restrict__ last,
+                            const int32_t *__restrict__ win,
+                            const int32_t *__restrict__ cand, int max_kv_len,
+                            int32_t *__restrict__ vb, int32_t *status) {
+    constexpr int T = BI_VERIFY_ROWS;
+    __shared__ int s_req[T], s_kv[T], s_w[T], s_start[T];
+    __shared__ int s_taken, s_used;
+    const int t = threadIdx.x;
+    const int R = *n_windows;
+    const bool r_ok = R >= 1 && R < T;
+    if (r_ok && t < R) {
+        s_req[t] = req[t];
+        s_kv[t] = kvl[t];
+        s_w[t] = win[t];
+    }
+    __syncthreads();
+    if (t == 0) {
+        int used = 0, taken = 0;
+        bool bad = !r_ok;
+        for (int r = 0; !bad && r < R; ++r) {
+            const int w = s_w[r];
+            if (w < 1 || s_kv[r] < 0 || s_req[r] < 0) {
+                bad = true;
+                break;
+            }
+            if (used + w > T) break;
+            if (s_kv[r] + w > max_kv_len) {
+                bad = true;
+                break;
+            }
+            s_start[r] = used;
+            used += w;
+            ++taken;
+        }
+        if (taken == 0) bad = true;
+        s_taken = bad ? 0 : taken;
+        s_used = bad ? 0 : used;
+        if (bad) bi_record_error(status, BI_ERR_BOUNDS);
+    }
+    __syncthreads();
+    int taken = s_taken;
+    // a request named by two taken windows would have both write its KV
+    // and both commit kernels cut its page-table row: refuse the plan
+    bool dup = false;
+    if (t < taken)
+        for (int i = 0; i < t; ++i) dup |= s_req[i] == s_req[t];
+    if (__syncthreads_or(dup)) {
+        taken = 0;
+        if (t == 0) bi_record_error(status, BI_ERR_BOUNDS);
+    }
+    const int used = taken > 0 ? s_used : 0;
+    // row t
+    if (t < used) {
+        int lo = 0, hi = taken - 1;  // the last window starting at or before t
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_start[mid] <= t)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        const int k = t - s_start[lo];
+        vb[VerifyIdx::TOK + t] = k == 0 ? last[lo] : cand[t - 1];
+        vb[VerifyIdx::POS + t] = s_kv[lo] + k;
+        vb[VerifyIdx::ROWREQ + t] = s_req[lo];
+        vb[VerifyIdx::CAND + t] = cand[t];
+    } else {
+        vb[VerifyIdx::TOK + t] = 0;
+        vb[VerifyIdx::POS + t] = t - used;
+        vb[VerifyIdx::ROWREQ + t] = -1;
+        vb[VerifyIdx::CAND + t] = -1;
+    }
+    // segments: taken windows, the pad segment, then empty segments
+    for (int i = t; i <= VerifyIdx::NSEG; i += T) {
+        int cu, sr;
+        if (i < taken) {
+            cu = s_start[i];
+            sr = s_req[i];
+        } else if (i == taken) {
+            cu = used;
+            sr = -1;
+        } else {
+            cu = T;
+            sr = -1;
+        }
+        vb[VerifyIdx::CUQ + i] = cu;
+        if (i < VerifyIdx::NSEG) vb[VerifyIdx::SEGREQ + i] = sr;
+    }
+    if (t < taken) {
+        vb[VerifyIdx::SEGSTART + t] = s_start[t];
+        vb[VerifyIdx::SEGW + t] = s_w[t];
+        vb[VerifyIdx::SEGKV + t] = s_kv[t];
+    }
+    if (t == 0) vb[VerifyIdx::TAKEN] = taken;
+}
+
+// One thread per taken window: first mismatch, commit, rollback.  The
 // freed-page list is laid out request after request, pages in ascending
 // table index, by a sequential prefix over the requests (thread 0), so its
-// order is fixed.
-__global__ void commit_kernel(int R, int max_pages, int32_t *vb,
-                              const int32_t *ids, int32_t *page_table,
-                              int32_t *kv_len, int freed_cap) {
+// order is fixed.  Pages past freed_cap are cut from the table but not
+// listed; *n_freed counts them all.
+__global__ void commit_kernel(int max_pages, const int32_t *__restrict__ vb,
+                              const int32_t *__restrict__ ids,
+                              int32_t *page_table, int32_t *kv_len,
+                              int32_t *commit_len, int32_t *fix_token,
+                              int32_t *freed, int freed_cap, int32_t *n_freed,
+                              int32_t *taken_out) {
     __shared__ int counts[BI_VERIFY_ROWS], offs[BI_VERIFY_ROWS];
     const int r = threadIdx.x;
+    const int R = vb[VerifyIdx::TAKEN];
     int j = 0, w = 0, newlen = 0, req = -1, keep = 0;
     if (r < R) {
         const int start = vb[VerifyIdx::SEGSTART + r];
@@ -135,8 +261,8 @@ __global__ void commit_kernel(int R, int max_pages, int32_t *vb,
                 break;
             }
         newlen = vb[VerifyIdx::SEGKV + r] + j;
-        vb[VerifyIdx::OUT_COMMIT + r] = j;
-        vb[VerifyIdx::OUT_FIX + r] = j < w ? ids[start + j] : -1;
+        commit_len[r] = j;
+        fix_token[r] = j < w ? ids[start + j] : -1;
         keep = (newlen + 15) / 16;
         int cnt = 0;
         for (int p = keep; p < max_pages; ++p)
@@ -150,7 +276,8 @@ __global__ void commit_kernel(int R, int max_pages, int32_t *vb,
             offs[i] = acc;
             acc += counts[i];
         }
-        vb[VerifyIdx::OUT_NFREED] = acc;
+        *n_freed = acc;
+        *taken_out = R;
     }
     __syncthreads();
     if (r < R) {
@@ -158,7 +285,7 @@ __global__ void commit_kernel(int R, int max_pages, int32_t *vb,
         for (int p = keep; p < max_pages; ++p) {
             int32_t *e = page_table + (int64_t)req * max_pages + p;
             if (*e >= 0) {
-                if (at < freed_cap) vb[VerifyIdx::OUT_FREED + at] = *e;
+                if (at < freed_cap) freed[at] = *e;
                 ++at;
                 *e = -1;
             }
@@ -417,6 +544,50 @@ extern "C" bi_status bi_model_forward(bi_model *m, int T, const int32_t *tokens,
     return BI_OK;
 }
 
+extern "C" bi_status bi_model_hidden(bi_model *m, void **out) {
+    BI_REQUIRE(m && out, "bi_model_hidden: null pointer");
+    *out = m->ws + m->L.h;
+    return BI_OK;
+}
+
+extern "C" bi_status verify_commit_rollback_device(
+    bi_model *m, const int32_t *n_windows, const int32_t *req,
+    const int32_t *win_kv_len, const int32_t *last_token,
+    const int32_t *win_len, const int32_t *candidates, int32_t *page_table,
+    int32_t *kv_len, int32_t *commit_len, int32_t *fix_token, int32_t *freed,
+    int freed_cap, int32_t *n_freed, int32_t *taken, float *logits,
+    void *stream) {
+    BI_REQUIRE(m, "verify_commit_rollback: null model");
+    const bi_model_cfg &c = m->cfg;
+    BI_REQUIRE(c.max_tokens >= BI_VERIFY_ROWS,
+               "verify_commit_rollback: model built for %d rows < %d",
+               c.max_tokens, BI_VERIFY_ROWS);
+    BI_REQUIRE(n_windows && req && win_kv_len && last_token && win_len &&
+                   candidates && page_table && kv_len && commit_len &&
+                   fix_token && n_freed && taken && logits &&
+                   (freed || freed_cap == 0) && freed_cap >= 0,
+               "verify_commit_rollback: null pointer");
+    const int T = BI_VERIFY_ROWS;
+    cudaStream_t s = bi_stream(stream);
+    int32_t *dvb = reinterpret_cast<int32_t *>(m->ws + m->L.vbuf);
+    pack_kernel<<<1, T, 0, s>>>(n_windows, req, win_kv_len, last_token,
+                                win_len, candidates, c.max_kv_len, dvb,
+                                bi_status_ptr());
+    BI_LAUNCH_CHECK("verify pack launch");
+    int32_t *ids = dvb + VerifyIdx::IDS;
+    bi_status st = bi_model_forward(
+        m, T, dvb + VerifyIdx::TOK, dvb + VerifyIdx::POS,
+        dvb + VerifyIdx::ROWREQ, VerifyIdx::NSEG, dvb + VerifyIdx::CUQ,
+        dvb + VerifyIdx::SEGREQ, T, c.max_kv_len, page_table, logits, ids,
+        stream);
+    if (st != BI_OK) return st;
+    commit_kernel<<<1, T, 0, s>>>(c.max_pages, dvb, ids, page_table, kv_len,
+                                  commit_len, fix_token, freed, freed_cap,
+                                  n_freed, taken);
+    BI_LAUNCH_CHECK("verify commit launch");
+    return BI_OK;
+}
+
 extern "C" bi_status verify_commit_rollback(
     bi_model *m, int R, const int32_t *h_req, const int32_t *h_kv_len,
     const int32_t *h_last_token, const int32_t *h_win_len,
@@ -432,12 +603,13 @@ extern "C" bi_status verify_commit_rollback(
                c.max_tokens, BI_VERIFY_ROWS);
     BI_REQUIRE(h_req && h_kv_len && h_last_token && h_win_len && h_candidates &&
                    page_table && kv_len && h_commit_len && h_fix_token &&
-                   h_n_freed && h_taken && logits && (h_freed || freed_cap == 0),
+                   h_n_freed && h_taken && logits &&
+                   (h_freed || freed_cap == 0) && freed_cap >= 0,
                "verify_commit_rollback: null pointer");
     const int T = BI_VERIFY_ROWS;
-    // ---- FIFO packing into the fixed-shape batch (host).
-    std::vector<int32_t> vb(VerifyIdx::PACKED, 0);
-    int used = 0, taken = 0, cand_at = 0, max_w = 1, max_kv = 1;
+    // The checks of the device-side packing, made here first so that a bad
+    // plan is refused before anything is launched.
+    int used = 0, taken = 0;
     for (int r = 0; r < R; ++r) {
         const int w = h_win_len[r];
         BI_REQUIRE(w >= 1, "verify_commit_rollback: window %d has length %d", r,
@@ -448,85 +620,77 @@ extern "C" bi_status verify_commit_rollback(
         BI_REQUIRE(h_kv_len[r] + w <= c.max_kv_len,
                    "verify_commit_rollback: window %d reaches %d > max_kv_len",
                    r, h_kv_len[r] + w);
-        for (int i = 0; i < w; ++i) {
-            const int row = used + i;
-            vb[VerifyIdx::TOK + row] =
-                i == 0 ? h_last_token[r] : h_candidates[cand_at + i - 1];
-            vb[VerifyIdx::POS + row] = h_kv_len[r] + i;
-            vb[VerifyIdx::ROWREQ + row] = h_req[r];
-            vb[VerifyIdx::CAND + row] = h_candidates[cand_at + i];
-        }
-        vb[VerifyIdx::CUQ + taken] = used;
-        vb[VerifyIdx::SEGREQ + taken] = h_req[r];
-        vb[VerifyIdx::SEGSTART + taken] = used;
-        vb[VerifyIdx::SEGW + taken] = w;
-        vb[VerifyIdx::SEGKV + taken] = h_kv_len[r];
-        max_w = std::max(max_w, w);
-        max_kv = std::max(max_kv, h_kv_len[r] + w);
+        for (int i = 0; i < taken; ++i)
+            BI_REQUIRE(h_req[i] != h_req[r],
+                       "verify_commit_rollback: windows %d and %d both name "
+                       "request %d",
+                       i, r, h_req[r]);
         used += w;
-        cand_at += w;
         ++taken;
     }
     BI_REQUIRE(taken >= 1, "verify_commit_rollback: first window longer than "
                            "%d rows",
                T);
-    // Pad rows form one extra segment with no request.
-    int nseg = taken;
-    for (int row = used; row < T; ++row) {
-        vb[VerifyIdx::TOK + row] = 0;
-        vb[VerifyIdx::POS + row] = row - used;
-        vb[VerifyIdx::ROWREQ + row] = -1;
-        vb[VerifyIdx::CAND + row] = -1;
+    // Plan upload: the windows (the device packs only the taken ones, whose
+    // candidates are the first `used` entries).
+    std::vector<int32_t> plan(VerifyIdx::OUT - VerifyIdx::PLAN, 0);
+    plan[VerifyIdx::PLAN_R - VerifyIdx::PLAN] = R;
+    for (int r = 0; r < R; ++r) {
+        plan[VerifyIdx::PLAN_REQ - VerifyIdx::PLAN + r] = h_req[r];
+        plan[VerifyIdx::PLAN_KV - VerifyIdx::PLAN + r] = h_kv_len[r];
+        plan[VerifyIdx::PLAN_LAST - VerifyIdx::PLAN + r] = h_last_token[r];
+        plan[VerifyIdx::PLAN_WIN - VerifyIdx::PLAN + r] = h_win_len[r];
     }
-    if (used < T) {
-        vb[VerifyIdx::CUQ + nseg] = used;
-        vb[VerifyIdx::SEGREQ + nseg] = -1;
-        ++nseg;
-        max_w = std::max(max_w, T - used);
-        max_kv = std::max(max_kv, T - used);
-    }
-    vb[VerifyIdx::CUQ + nseg] = T;
-
+    for (int i = 0; i < used; ++i)
+        plan[VerifyIdx::PLAN_CAND - VerifyIdx::PLAN + i] = h_candidates[i];
     cudaStream_t s = bi_stream(stream);
     int32_t *dvb = reinterpret_cast<int32_t *>(m->ws + m->L.vbuf);
     bi_status st = bi_cuda_check(
-        cudaMemcpyAsync(dvb, vb.data(), vb.size() * sizeof(int32_t),
-                        cudaMemcpyHostToDevice, s),
-        "verify: pack upload");
+        cudaMemcpyAsync(dvb + VerifyIdx::PLAN, plan.data(),
+                        plan.size() * sizeof(int32_t), cudaMemcpyHostToDevice,
+                        s),
+        "verify: plan upload");
     if (st != BI_OK) return st;
-    int32_t *ids = dvb + VerifyIdx::IDS;
-    st = bi_model_forward(m, T, dvb + VerifyIdx::TOK, dvb + VerifyIdx::POS,
-                          dvb + VerifyIdx::ROWREQ, nseg, dvb + VerifyIdx::CUQ,
-                          dvb + VerifyIdx::SEGREQ, max_w,
-                          std::min(max_kv, c.max_kv_len), page_table, logits,
-                          ids, stream);
+    const int cap = c.max_pages * BI_VERIFY_ROWS;
+    st = verify_commit_rollback_device(
+        m, dvb + VerifyIdx::PLAN_R, dvb + VerifyIdx::PLAN_REQ,
+        dvb + VerifyIdx::PLAN_KV, dvb + VerifyIdx::PLAN_LAST,
+        dvb + VerifyIdx::PLAN_WIN, dvb + VerifyIdx::PLAN_CAND, page_table,
+        kv_len, dvb + VerifyIdx::OUT_COMMIT, dvb + VerifyIdx::OUT_FIX,
+        dvb + VerifyIdx::OUT_FREED, cap, dvb + VerifyIdx::OUT_NFREED,
+        dvb + VerifyIdx::OUT_TAKEN, logits, stream);
     if (st != BI_OK) return st;
-    commit_kernel<<<1, BI_VERIFY_ROWS, 0, s>>>(
-        taken, c.max_pages, dvb, ids, page_table, kv_len,
-        c.max_pages * BI_VERIFY_ROWS);
-    BI_LAUNCH_CHECK("verify commit launch");
-    std::vector<int32_t> outv(VerifyIdx::OUT_FREED - VerifyIdx::OUT_COMMIT);
+    std::vector<int32_t> outv(VerifyIdx::OUT_FREED - VerifyIdx::OUT);
     st = bi_cuda_check(
-        cudaMemcpyAsync(outv.data(), dvb + VerifyIdx::OUT_COMMIT,
+        cudaMemcpyAsync(outv.data(), dvb + VerifyIdx::OUT,
                         outv.size() * sizeof(int32_t), cudaMemcpyDeviceToHost,
                         s),
         "verify: result download");
     if (st != BI_OK) return st;
     st = bi_cuda_check(cudaStreamSynchronize(s), "verify: sync");
     if (st != BI_OK) return st;
-    const int nfreed = outv[VerifyIdx::OUT_NFREED - VerifyIdx::OUT_COMMIT];
+    const int nfreed = outv[VerifyIdx::OUT_NFREED - VerifyIdx::OUT];
+    const int got = outv[VerifyIdx::OUT_TAKEN - VerifyIdx::OUT];
+    if (got != taken)
+        return bi_fail(BI_ERR_CUDA,
+                       "verify_commit_rollback: device packed %d windows, "
+                       "host %d",
+                       got, taken);
     for (int r = 0; r < taken; ++r) {
-        h_commit_len[r] = outv[r];
-        h_fix_token[r] = outv[VerifyIdx::OUT_FIX - VerifyIdx::OUT_COMMIT + r];
+        h_commit_len[r] = outv[VerifyIdx::OUT_COMMIT - VerifyIdx::OUT + r];
+        h_fix_token[r] = outv[VerifyIdx::OUT_FIX - VerifyIdx::OUT + r];
     }
     *h_n_freed = nfreed;
     *h_taken = taken;
-    if (nfreed > 0 && freed_cap > 0) {
+    const int listed = std::min(std::min(nfreed, freed_cap), cap);
+    if (listed > 0) {
         st = bi_cuda_check(
-            cudaMemcpy(h_freed, dvb + VerifyIdx::OUT_FREED,
-                       (size_t)std::min(nfreed, freed_cap) * sizeof(int32_t),
-                       cudaMemcpyDeviceToHost),
+            cudaMemcpyAsync(h_freed, dvb + VerifyIdx::OUT_FREED,
+                            (size_t)listed * sizeof(int32_t),
+                            cudaMemcpyDeviceToHost, s),
             "verify: freed pages download");
+        if (st != BI_OK) return st;
+        st = bi_cuda_check(cudaStreamSynchronize(s), "verify: sync");
         if (st != BI_OK) return st;
     }
     if (nfreed > freed_cap)

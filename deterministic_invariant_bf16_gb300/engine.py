@@ -311,14 +311,37 @@ class Engine:
             self.handle, slots, kv_lens, last_tokens,
             [len(w) for w in windows], cands, self.page_table, self.kv_len,
             logits, freed_cap=self.max_pages * bi.VERIFY_ROWS, stream=stream)
-        # mirror the device-side page-table cut in the host bookkeeping
+        self.mirror_cut(slots, kv_lens, taken, commit)
+        return taken, commit, fix, freed
+
+    def verify_buffers(self):
+        """Device plan and result buffers for verify_device."""
+        return bi.VerifyBuffers(self.max_pages * bi.VERIFY_ROWS, self.device)
+
+    def verify_device(self, bufs, logits, stream=None):
+        """verify_commit_rollback_device on a plan already in ``bufs``: no
+        host synchronisation, so a caller may capture it (Engine.capture).
+        The page table and kv_len are cut on the device; once the results
+        are read (``bufs.read()``), ``mirror_cut`` brings the host page
+        bookkeeping in line."""
+        bi.verify_commit_rollback_device(self.handle, bufs, self.page_table,
+                                         self.kv_len, logits, stream)
+
+    def mirror_cut(self, slots, kv_lens, taken, commit):
+        """Mirror a verify's page-table cut in the host bookkeeping: pages
+        at or past ceil((kv_len + commit) / 16) go back to the allocator."""
         for r in range(taken):
             keep = -(-(int(kv_lens[r]) + int(commit[r])) // PAGE_SIZE)
             row = self.host_table[slots[r]]
             gone = row[keep:][row[keep:] >= 0]
             row[keep:] = -1
             self.alloc.give_back(gone)
-        return taken, commit, fix, freed
+
+    def hidden(self, T):
+        """The residual stream after the last forward of T rows: bf16
+        [T][hidden], the last layer's output before the final RMSNorm
+        (a view of the workspace, valid until the next forward)."""
+        return bi.bi_model_hidden(self.handle, T, self.shape.hidden)
 
 
 def to_device(weights: dict, device="cuda") -> dict:

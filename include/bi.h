@@ -350,6 +350,12 @@ bi_status bi_model_create(const bi_model_cfg *cfg, const bi_model_weights *w,
 
 void bi_model_destroy(bi_model *m);
 
+/* Device address of the model's residual stream in its workspace: bf16
+ * [T][hidden] after a bi_model_forward of T rows holds the last layer's
+ * output (the hidden state before the final RMSNorm), valid until the next
+ * forward.  For inspection; the library never frees it. */
+bi_status bi_model_hidden(bi_model *m, void **out);
+
 /* One forward pass over T rows.
  *   tokens, pos, row_req: device int32 [T] (row_req = page-table row,
  *   < 0 for a pad row).
@@ -412,7 +418,8 @@ bi_status bi_model_profile_read(bi_model *m, double *h_ms,
  * cache must hold the request's committed tokens except the last one, and
  * pages for every window position must already be in the page table.
  * Windows that do not fit after the first ones are not taken: *h_taken says
- * how many were.
+ * how many were.  Two taken windows may not name the same request
+ * (BI_ERR_INVALID_ARG).
  *   h_req, h_kv_len, h_last_token, h_win_len: host int32 [R]
  *   h_candidates: host int32 [sum w], windows concatenated
  *   page_table: device int32 [slots][max_pages], updated in place
@@ -433,6 +440,39 @@ bi_status verify_commit_rollback(bi_model *m, int R, const int32_t *h_req,
                                  int32_t *h_freed, int freed_cap,
                                  int32_t *h_n_freed, int32_t *h_taken,
                                  float *logits, void *stream);
+
+/* verify_commit_rollback with its plan and results in device memory: no
+ * host synchronisation and no host-dependent launch configuration, so the
+ * call can sit in a captured CUDA graph beside the decode iterations (the
+ * host reads the results after the replay).  The windows are packed on the
+ * device, first-in first-out as above: the forward always runs the same
+ * kernels over BI_VERIFY_ROWS rows in BI_VERIFY_ROWS + 1 segments (the
+ * taken windows, one pad segment, empty segments).
+ *   n_windows: device int32 scalar R, 1 <= R < BI_VERIFY_ROWS
+ *   req, win_kv_len, last_token, win_len: device int32 [R] (as h_req,
+ *     h_kv_len, h_last_token, h_win_len above)
+ *   candidates: device int32, windows concatenated; only the taken
+ *     windows' entries (at most BI_VERIFY_ROWS) are read
+ *   page_table, kv_len: as above, updated in place
+ *   commit_len, fix_token: device int32 [BI_VERIFY_ROWS] (entries of the
+ *     taken windows written)
+ *   freed: device int32 [freed_cap]; *n_freed (device) receives the count
+ *     of pages cut (also those past freed_cap, which are cut but unlisted)
+ *   taken: device int32 scalar, windows taken
+ *   logits: device fp32 [BI_VERIFY_ROWS][V] scratch.
+ * The plan is checked on the device with the rules above, and also
+ * against two windows naming one request: a plan that fails takes no
+ * window (*taken = 0, nothing committed or cut) and records BI_ERR_BOUNDS
+ * in the device status word (bi_device_status).  Requests must be valid
+ * page-table rows.  Returns an error before launching only for null
+ * pointers or a model built for fewer than BI_VERIFY_ROWS rows. */
+bi_status verify_commit_rollback_device(
+    bi_model *m, const int32_t *n_windows, const int32_t *req,
+    const int32_t *win_kv_len, const int32_t *last_token,
+    const int32_t *win_len, const int32_t *candidates, int32_t *page_table,
+    int32_t *kv_len, int32_t *commit_len, int32_t *fix_token, int32_t *freed,
+    int freed_cap, int32_t *n_freed, int32_t *taken, float *logits,
+    void *stream);
 
 #ifdef __cplusplus
 }

@@ -90,3 +90,51 @@ def test_decode_workspace_formula(bi):
         up(3 * 32 * 2 * 132 * 4) + up(4 * 4) + up(3 * 2 * 8)
     assert bi.bi_decode_attn_workspace_size(1, 4, 32, 16) == \
         up(1 * 4 * 1 * 36 * 4) + up(2 * 4) + up(1 * 1 * 8)
+
+
+def test_verify_refuses_bad_plans_before_launch(bi):
+    """The host entry point checks the FIFO plan before it uploads anything:
+    two taken windows naming one request (both would write that request's
+    KV and cut its page-table row), an empty window, a window past the
+    model's longest context.  No GPU is touched: the model handle holds
+    placeholder addresses that nothing dereferences."""
+    lib = bi.lib()
+    cfg = bi.ModelCfg(n_layers=1, hidden=128, n_heads=4, n_kv_heads=4,
+                      head_dim=32, ffn=256, vocab=512, eps=1e-5, theta=1e4,
+                      max_tokens=256, max_kv_len=64, max_pages=4, n_pages=8)
+    nbytes = bi.bi_model_workspace_size(cfg)
+    assert nbytes > 0
+    fake = ctypes.c_void_p(1 << 20)
+    arr = (ctypes.c_void_p * 1)(1 << 20)
+    pp = ctypes.cast(arr, bi.PP)
+    w = bi.ModelWeights(embed=1 << 20, final_norm=1 << 20, lm_head=1 << 20,
+                        attn_norm=pp, wqkv=pp, wo=pp, ffn_norm=pp, wgu=pp,
+                        wd=pp, k_pool=pp, v_pool=pp)
+    handle = ctypes.c_void_p()
+    assert lib.bi_model_create(ctypes.byref(cfg), ctypes.byref(w), fake,
+                               nbytes, ctypes.byref(handle)) == 0
+    try:
+        I32 = ctypes.c_int32
+
+        def call(req, kv, last, wl, cands):
+            R = len(req)
+            a = [(I32 * max(1, len(x)))(*x) for x in (req, kv, last, wl,
+                                                      cands)]
+            out = [(I32 * 8)() for _ in range(2)]
+            freed = (I32 * 8)()
+            nf, tk = I32(0), I32(0)
+            return lib.verify_commit_rollback(
+                handle, R, *a, fake, fake, out[0], out[1], freed, 8,
+                ctypes.byref(nf), ctypes.byref(tk), fake, None)
+
+        st = call([3, 3], [10, 12], [1, 2], [4, 4], [0] * 8)
+        assert st == 1 and b"both name request 3" in lib.bi_last_error()
+        st = call([3, 4], [10, 12], [1, 2], [4, 0], [0] * 4)
+        assert st == 1 and b"length 0" in lib.bi_last_error()
+        st = call([3], [62], [1], [4], [0] * 4)
+        assert st == 1 and b"max_kv_len" in lib.bi_last_error()
+        # the device variant needs every pointer
+        assert lib.verify_commit_rollback_device(
+            handle, *([None] * 11), 0, None, None, None, None) == 1
+    finally:
+        lib.bi_model_destroy(handle)

@@ -49,8 +49,45 @@ def test_single_rank_aggregation():
 def test_workload_shapes():
     import bench
     wl = bench.make_workload(256, 10)
-    assert wl["n_flag"] == 26 and wl["n_ver"] * wl["window"] == 256
+    assert wl["n_flag"] == 26 and wl["groups"] == [4, 8, 16]
+    assert wl["max_window"] == 64 and wl["headroom"] >= 64
     assert wl["ctx"].min() >= 4 and wl["ctx"].max() <= 2048 + 1024
     # same seed, same workload
     wl2 = bench.make_workload(256, 10)
     assert np.array_equal(wl["ctx"], wl2["ctx"])
+
+
+def test_verify_plans_layout_and_expected_commits():
+    """The bench's verify plans: group sizes cycle over 4 / 8 / 16 with
+    windows of 64 / 32 / 16 candidates (256 rows each), the requests of a
+    plan are distinct flagged requests, the plan array holds the windows in
+    the device layout (count, requests, contexts, last tokens, lengths,
+    candidates), and the expected commit is the first perturbed index."""
+    import bench
+    from deterministic_invariant_bf16_gb300 import binding as bi
+    wl = bench.make_workload(256, 10)
+    V = 128256
+    rng = np.random.default_rng(0)
+    greedy = rng.integers(0, V, size=(wl["n_flag"], wl["max_window"]))
+    plans, expect, meta = bench.verify_plans(wl, greedy, V, n_plans=12)
+    n = bi.VERIFY_ROWS
+    flips = 0
+    for k, (a, exp, m) in enumerate(zip(plans, expect, meta)):
+        g = [4, 8, 16][k % 3]
+        assert m["g"] == g and m["w"] * g == 256
+        assert len(set(m["reqs"])) == g
+        assert all(0 <= r < wl["n_flag"] for r in m["reqs"])
+        assert a[0] == g
+        assert list(a[8:8 + g]) == m["reqs"]
+        assert list(a[8 + n:8 + n + g]) == [int(wl["ctx"][r])
+                                            for r in m["reqs"]]
+        assert list(a[8 + 2 * n:8 + 2 * n + g]) == [
+            int(wl["first_tokens"][r]) for r in m["reqs"]]
+        assert all(a[8 + 3 * n:8 + 3 * n + g] == m["w"])
+        cands = a[8 + 4 * n:8 + 5 * n]
+        for i, (r, win, j) in enumerate(zip(m["reqs"], m["windows"], exp)):
+            assert list(cands[i * m["w"]:(i + 1) * m["w"]]) == win
+            diff = np.nonzero(np.array(win) != greedy[r][:m["w"]])[0]
+            assert j == (diff[0] if len(diff) else m["w"])
+            flips += len(diff)
+    assert flips > 0   # some windows roll back

@@ -251,6 +251,19 @@ def test_prefix_sharing_bitwise(tiny, lib):
     assert np.array_equal(np.stack(rows).view(np.uint32),
                           ref_l[0].view(np.uint32))
     assert lib.bi_device_status() == 0
+    # and against the oracle: B's whole sequence computed from scratch on
+    # the CPU; the shared-prefix logits within 2e-2 norm-wise, the greedy
+    # ids equal to the oracle's argmax of the GPU's logits
+    import oracle
+    cfg = oracle.Cfg()
+    seq = list(pb) + toks[:-1]
+    caches = oracle.new_caches(cfg, 1, len(seq) + 1)
+    ref = oracle.model_forward(seq, np.zeros(len(seq), np.int32),
+                               np.arange(len(seq), dtype=np.int32),
+                               oracle_weights(tiny[1]), caches, cfg)
+    got = np.stack(rows)
+    assert norm_rel_err(got, ref[len(pb) - 1:]) < 2e-2
+    assert list(oracle.argmax(got)) == toks
 
 
 # ---------------------------------------------------------------- verify --
@@ -377,6 +390,254 @@ def test_verify_grouping_invariance(tiny):
     b = run(list(rng.permutation(n_req)), 2, 22)
     assert a == b
     assert all(a[r][0] == (5 * r) % w for r in range(n_req))
+
+
+def test_verify_device_matches_host_and_replays(tiny, lib):
+    """verify_commit_rollback_device (plan and results in device memory,
+    packing on the device) gives the host entry point's commits, fix
+    tokens, freed pages, page-table cut and logits bit for bit: called
+    eagerly, and captured once in a CUDA graph and replayed with two
+    different plans refilled in place (the page table restored between
+    replays).  A plan whose windows name one request twice takes nothing,
+    leaves the table alone and records BI_ERR_BOUNDS."""
+    shape = tiny[0]
+    from deterministic_invariant_bf16_gb300 import synth
+    rng = np.random.default_rng(3100)
+    n_req, w = 8, 24
+    prompts = [synth.token_ids(int(n), shape.vocab, rng)
+               for n in rng.integers(4, 12, size=n_req)]
+    _, ref_toks = _decode_reference(tiny, prompts, w + 4)
+    slots = list(range(n_req))
+    kv = [len(p) for p in prompts]
+    last = [ref_toks[r][0] for r in range(n_req)]
+
+    def windows(shift):
+        out = []
+        for r in range(n_req):
+            c = list(ref_toks[r][1:1 + w])
+            if (r + shift) % 4 != 3:
+                i = (5 * r + shift) % w
+                c[i] = (c[i] + 3) % shape.vocab
+            out.append(c)
+        return out
+
+    def fresh():
+        eng = new_engine(tiny, page_seed=40)
+        for r in range(n_req):
+            eng.reserve(r, len(prompts[r]) + w + 4)
+            eng.prefill([(r, list(prompts[r]), 0)])
+        return eng
+
+    def logits_buf():
+        return torch.empty(256, shape.vocab, dtype=torch.float32,
+                           device="cuda")
+
+    ref = []
+    for shift in (0, 7):
+        e = fresh()
+        lg = logits_buf()
+        res = e.verify(slots, kv, last, windows(shift), lg)
+        torch.cuda.synchronize()
+        ref.append((res, e.page_table.clone(), e.kv_len.clone(), lg.clone()))
+
+    def same(got, want, e, lg):
+        (taken, commit, fix, freed), pt, kvl, rlg = want
+        assert got[0] == taken == n_req
+        assert np.array_equal(got[1], commit) and np.array_equal(got[2], fix)
+        assert np.array_equal(got[3], freed)
+        assert torch.equal(e.page_table, pt) and torch.equal(e.kv_len, kvl)
+        assert torch.equal(lg.view(torch.int32), rlg.view(torch.int32))
+
+    e = fresh()
+    bufs = e.verify_buffers()
+    lg = logits_buf()
+    bufs.load(slots, kv, last, windows(0))
+    e.verify_device(bufs, lg)
+    torch.cuda.synchronize()
+    same(bufs.read(), ref[0], e, lg)
+
+    e = fresh()
+    bufs = e.verify_buffers()
+    lg = logits_buf()
+    table0, kv0 = e.page_table.clone(), e.kv_len.clone()
+    bufs.load(slots, kv, last, windows(0))
+    g = e.capture(lambda: e.verify_device(bufs, lg))
+    for shift, want in zip((0, 7), ref):
+        e.page_table.copy_(table0)
+        e.kv_len.copy_(kv0)
+        bufs.out.zero_()
+        bufs.load(slots, kv, last, windows(shift))
+        g.replay()
+        torch.cuda.synchronize()
+        same(bufs.read(), want, e, lg)
+    assert lib.bi_device_status() == 0
+
+    e.page_table.copy_(table0)
+    bufs.load([0, 1, 0], kv[:3], last[:3], windows(0)[:3])
+    g.replay()
+    torch.cuda.synchronize()
+    taken, commit, _, freed = bufs.read()
+    assert taken == 0 and len(freed) == 0
+    assert torch.equal(e.page_table, table0)
+    assert lib.bi_device_status() == 5   # BI_ERR_BOUNDS, read and cleared
+    assert lib.bi_device_status() == 0
+
+
+# ------------------------------------------ 2-layer 8B-shape model --
+
+def test_8b_shape_two_layer_model_decode_and_verify(lib, orc):
+    """Llama-3.1-8B shape (hidden 4096, 32/8 heads of 128, FFN 14336, full
+    128256-token vocabulary, theta 5e5) with two layers, through
+    bi_model_forward and verify_commit_rollback (Engine): the model driver's
+    8B workspace layout, the fused RoPE over three QKV slices, the
+    tensor-core decode attention (whole-row items at 256 rows, per-chunk
+    items for one row) and verify attention, and the CTA-pair LM head.
+      * Decode of 256 requests (contexts lognormal, median 512, sigma 1,
+        clipped 16..2048, random KV in shuffled pages): on sampled rows each
+        layer's output against the oracle layer fed the GPU's input and
+        cache (teacher forcing) within 1e-2 norm-wise, the logits against
+        the oracle's final norm and LM head within 2e-2, greedy ids equal
+        to the oracle's argmax of the GPU's logits; the longest-context
+        row alone gives its row's logits bit for bit.
+      * Grouped verification (LLM-42, section 核心方法, Fig. 8) of 8
+        windows of 32 greedy candidates with forced perturbations: commits
+        equal the first perturbed index (or 32), fix tokens the unperturbed
+        tokens, the oracle commit rule on the GPU's verified ids agrees bit
+        for bit, verify rows equal the decode rows bit for bit up to the
+        perturbation, and the verify's hidden state against the oracle's
+        head within 2e-2."""
+    from deterministic_invariant_bf16_gb300 import engine, synth
+    import dataclasses
+    import oracle
+    S = synth.LLAMA8B
+    H, Hq, Hkv, D, F, V = (S.hidden, S.n_heads, S.n_kv_heads, S.head_dim,
+                           S.ffn, S.vocab)
+    B, W, NV = 256, 32, 8
+    rng = np.random.default_rng(4242)
+    ctx = synth.lognormal_lengths(B, 512, 1.0, 16, 2048, rng)
+    w = synth.make_weights(S, 5, "cuda", n_layers=2)
+    w1 = dict(w, layers=w["layers"][:1])
+    max_kv = int(ctx.max()) + W + 8
+    need = int(sum(-(-(int(c) + W + 8) // 16) for c in ctx))
+
+    def build(weights):
+        e = engine.Engine(dataclasses.replace(S, n_layers=len(
+            weights["layers"])), weights, max_tokens=256, max_kv_len=max_kv,
+            n_slots=B, n_pages=need + 8, page_seed=9)
+        for r in range(B):
+            e.reserve(r, int(ctx[r]) + W + 8)
+        for li, (kp, vp) in enumerate(zip(e.k_pool, e.v_pool)):
+            g = torch.Generator(device="cuda").manual_seed(600 + li)
+            kp.normal_(generator=g)
+            vp.normal_(generator=g)
+        return e
+
+    e2, e1 = build(w), build(w1)
+    assert np.array_equal(e2.host_table, e1.host_table)
+    tok = synth.token_ids(B, V, rng)
+    slots = list(range(B))
+    ids2 = torch.empty(B, dtype=torch.int32, device="cuda")
+    lg2 = e2.decode(list(tok), list(ctx), slots, ids=ids2).clone()
+    h2 = bits(e2.hidden(B))
+    e1.decode(list(tok), list(ctx), slots)
+    h1 = bits(e1.hidden(B))
+    torch.cuda.synchronize()
+    assert lib.bi_device_status() == 0
+    far = int(np.argmax(ctx))
+    one = e2.decode([int(tok[far])], [int(ctx[far])], [far]).clone()
+    assert torch.equal(one[0].view(torch.int32), lg2[far].view(torch.int32))
+
+    cfg = oracle.Cfg(n_layers=2, hidden=H, n_heads=Hq, n_kv_heads=Hkv,
+                     head_dim=D, ffn=F, vocab=V, eps=S.eps, theta=S.theta)
+    lws = [{k: np16(v) for k, v in lw.items()} for lw in w["layers"]]
+    rows = sorted({0, 17, B - 1, far, int(np.argmin(ctx))})
+    Lmax = int(ctx[rows].max()) + 1
+
+    def caches(layer, rows_):
+        """Logical [row, position, head, dim] caches of the sampled rows,
+        gathered from the pool pages (positions before each row's own)."""
+        kc = np.zeros((len(rows_), Lmax, Hkv, D), np.float32)
+        vc = np.zeros_like(kc)
+        for pool, out in ((e2.k_pool[layer], kc), (e2.v_pool[layer], vc)):
+            for i, b in enumerate(rows_):
+                n = int(ctx[b])
+                pages = torch.as_tensor(e2.host_table[b, :-(-n // 16)]).long()
+                blk = pool[pages.cuda()].permute(0, 2, 1, 3).reshape(
+                    -1, Hkv, D)[:n]
+                out[i, :n] = orc.bf16_value(bits(blk))
+        return kc, vc
+
+    req = np.arange(len(rows), dtype=np.int32)
+    pos = ctx[rows].astype(np.int32)
+    emb = orc.bf16_value(np16(w["embed"][torch.as_tensor(tok[rows]).long()
+                                         .cuda()]))
+    hin = [emb, orc.bf16_value(h1[rows])]
+    hout = [orc.bf16_value(h1[rows]), orc.bf16_value(h2[rows])]
+    for layer in range(2):
+        kc, vc = caches(layer, rows)
+        ref = orc.decoder_layer(hin[layer], req, pos, lws[layer], kc, vc,
+                                cfg)
+        for i in range(len(rows)):
+            assert norm_rel_err(hout[layer][i], ref[i]) < 1e-2, (layer, i)
+            assert norm_rel_err(hout[layer][i] - hin[layer][i],
+                                ref[i] - hin[layer][i]) < 3e-2, (layer, i)
+    fn, head = np16(w["final_norm"]), np16(w["lm_head"])
+
+    def oracle_head(hrows):
+        return orc.gemm(orc.bf16_bits(orc.rmsnorm(hrows, fn, S.eps)), head)
+
+    got = lg2[torch.as_tensor(rows).cuda()].cpu().numpy()
+    ref = oracle_head(orc.bf16_value(h2[rows]))
+    for i in range(len(rows)):
+        assert norm_rel_err(got[i], ref[i]) < 2e-2, i
+    assert np.array_equal(orc.argmax(got), ids2.cpu().numpy()[rows])
+
+    # --- grouped verification of 8 windows of 32 greedy candidates
+    first = ids2.cpu().numpy()[:NV]
+    cand, dec_rows = [], []
+    cur = list(first)
+    ids8 = torch.empty(NV, dtype=torch.int32, device="cuda")
+    for i in range(W):
+        lg = e2.decode(cur, list(ctx[:NV] + 1 + i), list(range(NV)),
+                       ids=ids8)
+        dec_rows.append(lg.cpu().numpy())
+        cur = list(ids8.cpu().numpy())
+        cand.append(cur)
+    cand = np.array(cand).T            # [NV, W]
+    dec_rows = np.stack(dec_rows, 1)   # [NV, W, V]
+    pert = [int(rng.integers(0, W)) if r % 4 != 3 else -1 for r in range(NV)]
+    wins = []
+    for r in range(NV):
+        c = list(map(int, cand[r]))
+        if pert[r] >= 0:
+            c[pert[r]] = (c[pert[r]] + 1 + r) % V
+        wins.append(c)
+    kv = [int(ctx[r]) + 1 for r in range(NV)]
+    vl = torch.empty(256, V, dtype=torch.float32, device="cuda")
+    taken, commit, fix, _ = e2.verify(list(range(NV)), kv, list(map(int, first)),
+                                      wins, vl)
+    hv = bits(e2.hidden(256))
+    torch.cuda.synchronize()
+    assert lib.bi_device_status() == 0
+    assert taken == NV
+    lv = vl.cpu().numpy()
+    ver = orc.argmax(lv)
+    for r in range(NV):
+        want = pert[r] if pert[r] >= 0 else W
+        assert commit[r] == want
+        if want < W:
+            assert fix[r] == cand[r, want]
+        j, _, fx, _ = orc.commit_rule(kv[r], wins[r], ver[r * W:(r + 1) * W])
+        assert (j, fx) == (commit[r], fix[r])
+        for i in range(W if pert[r] < 0 else pert[r] + 1):
+            assert np.array_equal(lv[r * W + i].view(np.uint32),
+                                  dec_rows[r, i].view(np.uint32)), (r, i)
+    vrows = [0, 5, W + 3, 7 * W + 31]
+    ref = oracle_head(orc.bf16_value(hv[vrows]))
+    for i, t in enumerate(vrows):
+        assert norm_rel_err(lv[t], ref[i]) < 2e-2
+    e1.close()
+    e2.close()
 
 
 # ------------------------------------------------------ one 8B layer --
