@@ -883,7 +883,7 @@ __global__ void __launch_bounds__(cthreads<D>())
 //     and 128-255; M = 128 keys, N = 16 rows), each over the dims in
 //     ascending 16-steps, fp32 in tensor memory;
 //   s = S^T * scale, -inf past the row's visible length; m = block maximum;
-//   p = exp(s - m) (0 when masked); l = per-warp xor-tree sums over 32 keys
+//   p = exp_s(s - m) (0 when masked); l = per-warp xor-tree sums over 32 keys
 //   (16, 8, 4, 2, 1), then (((w0 + w1) + w2) .. + w7) over the 8 warps;
 //   O^T[dim][row] = sum_key V[key][dim] bf16(p)[row][key]: one MMA chain
 //   (M = 128 dims, N = 16 rows) over the keys in ascending 16-steps, with V
@@ -891,6 +891,14 @@ __global__ void __launch_bounds__(cthreads<D>())
 // V rows past a chunk's visible part are zero when the PV MMAs read them
 // (0 * NaN would poison the sum); K rows there are never used (masked).
 namespace tca {
+
+// exp of a chunk score minus the chunk maximum (argument <= 0): the
+// hardware exponential (__expf: one multiply and one ex2, a few fp32 ulp,
+// far below the bf16 rounding P gets next).  Every head_dim-128 path
+// (decode, prefill, verify) takes p from this one function, so they agree
+// bit for bit; the full-accuracy expf cost about a third of the softmax's
+// instructions.
+__device__ __forceinline__ float exp_s(float x) { return __expf(x); }
 
 constexpr int SW = 8;                         // softmax warps, thread = key
 constexpr int STHREADS = SW * 32;
@@ -979,7 +987,7 @@ __device__ __forceinline__ void softmax(uint32_t s_tmem, float scale,
         for (int k = 1; k < SW; ++k) mm = fmaxf(mm, red[k * 16 + r]);
         m[r] = mm;
         const float mu = mm == -INFINITY ? 0.f : mm;
-        const float p = key < len[r] ? expf(__fsub_rn(v[r], mu)) : 0.f;
+        const float p = key < len[r] ? exp_s(__fsub_rn(v[r], mu)) : 0.f;
         v[r] = p;
         x[r] = p;
         asm volatile("st.shared.b16 [%0], %1;" ::"r"(ptile + poff(r, key)),
@@ -2266,6 +2274,483 @@ __global__ void __launch_bounds__(tca::PRE_THREADS, 1)
     }
 }
 
+// Prefill / verify on the tensor cores (head_dim 128) with one K and V chunk
+// shared by a group of query tiles.  An item is (group, KV head g): a group
+// is up to GT consecutive 16-row tiles of one segment (16 / G tokens x G
+// heads each), i.e. up to 16 GT / G consecutive tokens, as build_tiles_kernel
+// lists them (QPT = 16 GT / G tokens per entry).  Per chunk the CTA loads K
+// and V once and runs, for each tile whose context reaches the chunk, the
+// per-tile computation of the other kernels: issue_qk (N = 16 rows),
+// softmax<16>, issue_pv, then the merge into the tile's running (m, l, o) in
+// chunk order with merge_scalars / merge_value.  So every row gets the bits
+// of decode and of the per-tile prefill kernel, while a chunk's K and V are
+// read once per group instead of once per tile.
+//   warps 0-7  softmax (thread t <-> key t), one tile after the other (P and
+//              the reduction slots double-buffered); warps 0-3 then merge
+//              the previous tile's O (thread = dim) into its running O in
+//              tensor memory, or write the tile's output after its last
+//              chunk;
+//   warp 8     lanes 0-15 issue the TMA page boxes of a chunk (K and V as
+//              the other kernels load them); lane 0 issues the MMAs: the
+//              scores of tile n + 1 before the PV products of tile n, K of
+//              chunk c + 1 once the chunk's last scores have read K, V once
+//              its last PV products have read V.
+// Tensor memory (256 columns): S^T of two tiles (32 columns each), the PV
+// products of two tiles (16 each), the running O of each tile of the group
+// (16 each).  The persistent CTAs walk items in list order (most chunks
+// first); entries the builder marked invalid (no request, or a context out
+// of range) get zero outputs.  Waits are bounded; after one runs out every
+// later wait of the CTA returns at once and the CTA finishes its walk
+// without waiting (garbage out, BI_ERR_TIMEOUT recorded), so no barrier is
+// left unmatched.
+namespace tca {
+constexpr int GT_MAX = 8;
+struct GrpL {
+    static constexpr int TB = CHUNK * 128 * 2;            // K or V tile
+    static constexpr int QB = 16 * 128 * 2;               // one query tile
+    static constexpr int SB = 16 * CHUNK * 4;             // scores, fp32
+    static constexpr int K = 0, V = TB, Q = 2 * TB;
+    static constexpr int P = Q + GT_MAX * QB;             // 2 P tiles
+    static constexpr int S = P + 2 * P_TILE;              // 2 score buffers
+    static constexpr int ML = S + 2 * SB;                 // [GT_MAX][16] (M, L)
+    static constexpr int AB = ML + GT_MAX * 16 * 2 * 4;   // [2][16] float4
+    static constexpr int PROW = AB + 2 * 16 * 16;         // [GT_MAX][16]
+    static constexpr int CI = PROW + GT_MAX * 16 * 4;     // [GT_MAX]
+    static constexpr int BAR = CI + GT_MAX * 4 + 32;
+    // k_full, v_full, s_full[2], s_empty[2], p_full[2], o_full[2],
+    // o_empty[2], then the TMEM address and the failure flag
+    static constexpr int BYTES = BAR + 12 * 8 + 16;
+    static constexpr int ALLOC = BYTES + 1024;
+};
+constexpr int GRP_THREADS = STHREADS + 32;
+constexpr uint32_t GRP_TMEM = 256;
+constexpr uint32_t T_S = 0, T_OC = 64, T_ORUN = 128;
+
+// Word of (row, key) in a score buffer [16][256] fp32: within each 32-key
+// group g the 16-byte units are permuted by (g & 1) | (g & 2) << 1, so that
+// the float4 reads of softmax16_t's row phase hit eight distinct bank
+// groups in every quarter-warp.
+__device__ __forceinline__ int sbw(int r, int key) {
+    const int g = key >> 5;
+    return r * CHUNK + (((key >> 2) ^ ((g & 1) | ((g & 2) << 1))) << 2) +
+           (key & 3);
+}
+
+// The softmax of softmax<16> for one chunk of a 16-row tile, bit for bit,
+// with fewer instructions: the same scaled and masked scores, the same
+// exact row maximum (fmaxf), p = exp_s(s - m) with the same masking, the
+// same bf16(p) in the P tile, and the row sum in the same order (the
+// xor-tree of lane 0 over each 32-key group, then the groups in order).
+//   Phase A, thread t <-> key t: scores from S^T in TMEM, scaled and
+//   masked, to the score buffer.
+//   Phase B, thread <-> (row r = 2 w + lane / 16, group g = lane / 2 % 8,
+//   half h = lane % 2): keys 32 g + 8 h + [0, 8) and 32 g + 16 + 8 h +
+//   [0, 8).  The maximum is a 16-lane xor reduction (exact, any order);
+//   the group sum's first tree level (keys i, i + 16) is thread-local, the
+//   second (i, i + 8) pairs the two halves (one shuffle), the rest is
+//   thread-local again; the groups are then added in order.  P leaves as
+//   two 16-byte units per thread.
+// Every thread of row r returns its m and l.  len(r) = visible keys of row
+// r in chunk c: min(256, prow[r] + 1 - 256 c), at least 0.
+__device__ __forceinline__ void softmax16_t(uint32_t s_tmem, float scale,
+                                            const int *prow, int c, float *sb,
+                                            uint32_t ptile, float &m_out,
+                                            float &l_out, uint64_t *s_empty) {
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    {
+        const int key = 32 * w + lane;
+        float v[16];
+        tmem_ld_16cols(
+            s_tmem + ((uint32_t)((w & 3) * 32) << 16) + (w >> 2) * 16, v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_empty);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const int len = prow[r] + 1 - c * CHUNK;
+            const float s = __fmul_rn(v[r], scale);
+            sb[sbw(r, key)] = key < len ? s : -INFINITY;
+        }
+    }
+    sync_softmax();
+    const int r = 2 * w + (lane >> 4), g = (lane >> 1) & 7, h = lane & 1;
+    const int klo = 32 * g + 8 * h;
+    float x[16];
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const float4 f = *reinterpret_cast<const float4 *>(
+                sb + sbw(r, klo + 16 * q + 4 * e));
+            x[8 * q + 4 * e + 0] = f.x;
+            x[8 * q + 4 * e + 1] = f.y;
+            x[8 * q + 4 * e + 2] = f.z;
+            x[8 * q + 4 * e + 3] = f.w;
+        }
+    float mx = x[0];
+#pragma unroll
+    for (int j = 1; j < 16; ++j) mx = fmaxf(mx, x[j]);
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float mu = mx == -INFINITY ? 0.f : mx;
+    const int len = prow[r] + 1 - c * CHUNK;
+    float pv[16];
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int key = klo + 16 * q + j;
+            pv[8 * q + j] =
+                key < len ? exp_s(__fsub_rn(x[8 * q + j], mu)) : 0.f;
+        }
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                         ptile + poff(r, klo + 16 * q)),
+                     "r"(pack_bf16x2(pv[8 * q + 0], pv[8 * q + 1])),
+                     "r"(pack_bf16x2(pv[8 * q + 2], pv[8 * q + 3])),
+                     "r"(pack_bf16x2(pv[8 * q + 4], pv[8 * q + 5])),
+                     "r"(pack_bf16x2(pv[8 * q + 6], pv[8 * q + 7]))
+                     : "memory");
+    // lane 0's xor tree over group g: level 16 pairs keys (i, i + 16),
+    // level 8 (i, i + 8) across the halves, then levels 4, 2, 1
+    float b[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float a = __fadd_rn(pv[j], pv[8 + j]);
+        b[j] = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 1));
+    }
+    const float c0 = __fadd_rn(b[0], b[4]), c1 = __fadd_rn(b[1], b[5]);
+    const float c2 = __fadd_rn(b[2], b[6]), c3 = __fadd_rn(b[3], b[7]);
+    const float W = __fadd_rn(__fadd_rn(c0, c2), __fadd_rn(c1, c3));
+    const int rb = lane & 16;
+    float l = __shfl_sync(0xffffffffu, W, rb);
+#pragma unroll
+    for (int k = 1; k < SW; ++k)
+        l = __fadd_rn(l, __shfl_sync(0xffffffffu, W, rb + 2 * k));
+    m_out = mx;
+    l_out = l;
+}
+}  // namespace tca
+
+__global__ void __launch_bounds__(tca::GRP_THREADS, 1)
+    attn_group_kernel(const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap,
+                      const uint16_t *__restrict__ q,
+                      const int4 *__restrict__ list,
+                      const int32_t *__restrict__ cnt,
+                      const int32_t *__restrict__ pos,
+                      const int32_t *__restrict__ page_table, int max_pages,
+                      int n_pages, int Hq, int Hkv, int G, int GT,
+                      float scale, uint16_t *__restrict__ out,
+                      int32_t *status) {
+    using namespace tca;
+    constexpr int D = 128;
+    constexpr int NCH = D / 8;
+    constexpr int PAGE_BYTES = 16 * 64 * 2;   // one box: 16 rows x 64 dims
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t base = smem_u32(smem);
+    const uint32_t ktile = base + GrpL::K, vtile = base + GrpL::V;
+    const uint32_t qtile = base + GrpL::Q, ptile = base + GrpL::P;
+    float *sbuf = reinterpret_cast<float *>(smem + GrpL::S);
+    float *mls = reinterpret_cast<float *>(smem + GrpL::ML);
+    float4 *abs_ = reinterpret_cast<float4 *>(smem + GrpL::AB);
+    int *s_prow = reinterpret_cast<int *>(smem + GrpL::PROW);
+    int *s_ci = reinterpret_cast<int *>(smem + GrpL::CI);
+    uint64_t *k_full = reinterpret_cast<uint64_t *>(smem + GrpL::BAR);
+    uint64_t *v_full = k_full + 1;
+    uint64_t *s_full = k_full + 2, *s_empty = k_full + 4;
+    uint64_t *p_full = k_full + 6, *o_full = k_full + 8;
+    uint64_t *o_empty = k_full + 10;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(k_full + 12);
+    volatile int *fail = reinterpret_cast<volatile int *>(k_full + 12) + 1;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int QPT = 16 / G;
+    const int n_valid = cnt[0], n_all = cnt[1];
+    const int items = n_valid * Hkv;
+
+    // Bounded wait; once any wait of the CTA has run out, returns at once.
+    auto gw = [&](uint64_t *bar, uint32_t parity) {
+        if (*fail) return;
+        if (mbar_try_wait(bar, parity)) return;
+        const uint64_t t0 = bi_globaltimer();
+        uint32_t n = 0;
+        while (!mbar_try_wait(bar, parity)) {
+            if ((++n & 1023u) == 0) {
+                if (*fail) return;
+                if (bi_globaltimer() - t0 > BI_WAIT_LIMIT_NS) {
+                    bi_record_error(status, BI_ERR_TIMEOUT);
+                    *fail = 1;
+                    return;
+                }
+            }
+        }
+    };
+
+    if (threadIdx.x == 0) {
+        mbar_init(k_full, 1);
+        mbar_init(v_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], SW);
+            mbar_init(&p_full[i], SW);
+            mbar_init(&o_full[i], 1);
+            mbar_init(&o_empty[i], 4);
+        }
+        mbar_fence_init();
+        *fail = 0;
+    }
+    if (warp == SW) tmem_alloc(tslot, GRP_TMEM);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    if (warp == SW && lane == 0) {
+        tma_prefetch_desc(&kmap);
+        tma_prefetch_desc(&vmap);
+    }
+
+    int nu = 0, nc = 0;  // units and chunks of the items done so far
+    for (int it = blockIdx.x; it < items; it += gridDim.x) {
+        const int4 e = list[it / Hkv];
+        const int g = it % Hkv;
+        const int t0 = e.x, L = e.y, ntok = e.z, req = e.w;
+        const int nt = min(GT, (ntok + QPT - 1) / QPT);
+        const int C = (L + CHUNK - 1) / CHUNK;
+        __syncthreads();  // the previous item is finished by every role
+        for (int idx = threadIdx.x; idx < nt * 16; idx += GRP_THREADS) {
+            const int tk = (idx >> 4) * QPT + (idx & 15) / G;
+            s_prow[idx] = tk < ntok ? pos[t0 + tk] : -1;
+        }
+        // query tiles: row r of tile i = (token i * QPT + r / G, head r % G)
+        for (int idx = threadIdx.x; idx < nt * 16 * NCH; idx += GRP_THREADS) {
+            const int i = idx / (16 * NCH), r = (idx / NCH) % 16,
+                      ch = idx % NCH;
+            const int tk = i * QPT + r / G, hh = r % G;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (tk < ntok)
+                v = *reinterpret_cast<const uint4 *>(
+                    q + ((int64_t)(t0 + tk) * Hq + g * G + hh) * D + ch * 8);
+            *reinterpret_cast<uint4 *>(smem + GrpL::Q + i * GrpL::QB +
+                                       toff<D, 16>(r, ch)) = v;
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (threadIdx.x < nt) {
+            int last = -1;
+            for (int r = 0; r < 16; ++r)
+                last = max(last, s_prow[threadIdx.x * 16 + r]);
+            s_ci[threadIdx.x] = (last + 1 + CHUNK - 1) / CHUNK;
+        }
+        __syncthreads();
+        // first tile whose context reaches chunk c (tile contexts grow with
+        // the tile index: a segment's positions are consecutive)
+        auto first_tile = [&](int c) {
+            int i = 0;
+            while (i < nt - 1 && s_ci[i] <= c) ++i;
+            return i;
+        };
+        const int32_t *pt_row = page_table + (int64_t)req * max_pages;
+
+        if (warp == SW) {
+            // ------------------------------------------- loads and MMAs --
+            auto load = [&](int c, bool is_k) {
+                int pg = -1;
+                if (lane < 16) {
+                    const int pi = c * 16 + lane;
+                    if (c * CHUNK + lane * 16 < L && pi < max_pages) {
+                        pg = pt_row[pi];
+                        if (pg < 0 || pg >= n_pages) {
+                            if (is_k) bi_record_error(status, BI_ERR_BOUNDS);
+                            pg = -1;
+                        }
+                    }
+                }
+                uint64_t *bar = is_k ? k_full : v_full;
+                if (lane == 0) mbar_arrive_expect_tx(bar, 16 * 2 * PAGE_BYTES);
+                __syncwarp();
+                if (lane < 16) {
+                    const int row = pg >= 0 ? (pg * Hkv + g) * 16 : -16;
+                    uint8_t *tile = smem + (is_k ? GrpL::K : GrpL::V);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_2d(tile + h * (CHUNK * 128) + lane * PAGE_BYTES,
+                                    is_k ? &kmap : &vmap, h * 64, row, bar);
+                }
+            };
+            // PV products of unit u (tile of chunk cu); V of chunk cu + 1
+            // once the chunk's last products have read V
+            auto pv = [&](int u, int cu, bool first_c, bool last_c) {
+                const int j = u & 1;
+                if (lane == 0) {
+                    if (first_c) gw(v_full, (nc + cu) & 1);
+                    gw(&p_full[j], (u >> 1) & 1);
+                    if (u >= 2) gw(&o_empty[j], ((u >> 1) - 1) & 1);
+                    tc_fence_after();
+                    issue_pv(tmem + T_OC + 16 * j, vtile, ptile + j * P_TILE);
+                    tc_commit(&o_full[j]);
+                    if (last_c && cu + 1 < C) gw(&o_full[j], (u >> 1) & 1);
+                }
+                __syncwarp();
+                if (last_c && cu + 1 < C) load(cu + 1, false);
+            };
+            load(0, true);
+            load(0, false);
+            int u = nu;
+            int pu = -1, pcu = 0;
+            bool pfirst = false, plast = false;
+            for (int c = 0; c < C; ++c) {
+                const int i0 = first_tile(c);
+                for (int i = i0; i < nt; ++i, ++u) {
+                    const int j = u & 1;
+                    if (lane == 0) {
+                        if (i == i0) gw(k_full, (nc + c) & 1);
+                        if (u >= 2) gw(&s_empty[j], ((u >> 1) - 1) & 1);
+                        tc_fence_after();
+                        issue_qk(tmem + T_S + 32 * j, ktile,
+                                 qtile + i * GrpL::QB);
+                        tc_commit(&s_full[j]);
+                    }
+                    __syncwarp();
+                    if (pu >= 0) pv(pu, pcu, pfirst, plast);
+                    if (i == nt - 1 && c + 1 < C) {
+                        // the chunk's last scores have read K
+                        if (lane == 0) gw(&s_full[j], (u >> 1) & 1);
+                        __syncwarp();
+                        load(c + 1, true);
+                    }
+                    pu = u;
+                    pcu = c;
+                    pfirst = i == i0;
+                    plast = i == nt - 1;
+                }
+            }
+            if (pu >= 0) pv(pu, pcu, pfirst, plast);
+        } else {
+            // --------------------------------------- softmax and merge --
+            int pu = -1, pi_ = 0, pc = 0;
+            // merge of unit u (tile i, chunk c) by warps 0-3, thread = dim:
+            // per row, keep O (chunk not visible), take the chunk's o (the
+            // tile's first chunk) or O a + o b, with (a, b) and the row's L
+            // from the row owner's merge_scalars
+            auto merge = [&](int u, int i, int c) {
+                const int j = u & 1;
+                const uint32_t lq = (uint32_t)(warp * 32) << 16;
+                gw(&o_full[j], (u >> 1) & 1);
+                tc_fence_after();
+                float o[16], O[16];
+                tmem_ld_16cols(tmem + T_OC + 16 * j + lq, o);
+                if (c > 0)
+                    tmem_ld_16cols(tmem + T_ORUN + 16 * i + lq, O);
+                else
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) O[r] = 0.f;
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&o_empty[j]);
+                float Lr[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    const float4 ab = abs_[j * 16 + r];
+                    const int flag = __float_as_int(ab.z);
+                    if (flag == 1)
+                        O[r] = o[r];
+                    else if (flag == 2)
+                        O[r] = merge_value(O[r], o[r], ab.x, ab.y);
+                    Lr[r] = ab.w;
+                }
+                if (c == s_ci[i] - 1) {
+                    const int dim = warp * 32 + lane;
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) {
+                        const int tk = i * QPT + r / G, hh = r % G;
+                        if (tk >= ntok) continue;
+                        out[((int64_t)(t0 + tk) * Hq + g * G + hh) * D + dim] =
+                            f32_to_bf16(__fdiv_rn(O[r], Lr[r]));
+                    }
+                } else {
+                    tmem_st_16cols(tmem + T_ORUN + 16 * i + lq, O);
+                    tc_fence_before();
+                }
+            };
+            int u = nu;
+            for (int c = 0; c < C; ++c) {
+                const int i0 = first_tile(c);
+                for (int i = i0; i < nt; ++i, ++u) {
+                    const int j = u & 1;
+                    gw(&s_full[j], (u >> 1) & 1);
+                    tc_fence_after();
+                    float m, l;
+                    softmax16_t(tmem + T_S + 32 * j, scale, s_prow + i * 16, c,
+                                sbuf + j * (GrpL::SB / 4), ptile + j * P_TILE,
+                                m, l, &s_empty[j]);
+                    if ((lane & 15) == 0) {
+                        // the row's running (M, L) and this chunk's factors
+                        const int r = 2 * warp + (lane >> 4);
+                        float *ml = mls + (i * 16 + r) * 2;
+                        float a = 0.f, bb = 0.f;
+                        int flag = 0;
+                        if (s_prow[i * 16 + r] + 1 - c * CHUNK > 0) {
+                            if (c == 0) {
+                                ml[0] = m;
+                                ml[1] = l;
+                                flag = 1;
+                            } else {
+                                float M = ml[0], L = ml[1];
+                                merge_scalars(M, L, m, l, a, bb);
+                                ml[0] = M;
+                                ml[1] = L;
+                                flag = 2;
+                            }
+                        }
+                        abs_[j * 16 + r] =
+                            make_float4(a, bb, __int_as_float(flag), ml[1]);
+                    }
+                    if (i == i0) {
+                        // V rows past the group's last visible position in
+                        // the chunk's last page: zero (0 * NaN would poison
+                        // the PV sums)
+                        gw(v_full, (nc + c) & 1);
+                        const int vl = min(CHUNK, L - c * CHUNK);
+                        if (vl & 15)
+                            zero_v_rows(smem + GrpL::V, vl, (vl + 15) & ~15,
+                                        threadIdx.x, STHREADS);
+                    }
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&p_full[j]);
+                    if (warp < 4 && pu >= 0) merge(pu, pi_, pc);
+                    pu = u;
+                    pi_ = i;
+                    pc = c;
+                }
+            }
+            sync_softmax();  // the last unit's row factors are in
+            if (warp < 4 && pu >= 0) merge(pu, pi_, pc);
+        }
+        // the same walk in every role: advance the unit and chunk counters
+        for (int c = 0; c < C; ++c) nu += nt - first_tile(c);
+        nc += C;
+    }
+    // entries with no valid context: zero outputs
+    for (int j = n_valid + blockIdx.x; j < n_all; j += gridDim.x) {
+        const int4 e = list[j];
+        const int64_t n = (int64_t)e.z * Hq * D;
+        for (int64_t idx = threadIdx.x; idx < n; idx += GRP_THREADS)
+            out[(int64_t)e.x * Hq * D + idx] = 0;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == SW) {
+        tc_fence_after();
+        tmem_dealloc(tmem, GRP_TMEM);
+    }
+}
+
 // ------------------------------------------------------------------- host --
 
 template <typename K>
@@ -2573,11 +3058,14 @@ bi_status bi_prefill_attn_pool(const bi_bf16 *q, const int32_t *cu_q,
     const int tiles = (T + QPT - 1) / QPT + R;
     int32_t *status = bi_status_ptr();
     dim3 grid(tiles, Hkv);
-    // The persistent path (a sorted tile list, then the decode kernel's
-    // pipeline over (tile, KV head) items) for verify-sized batches: 87 us
-    // against 101 us for 8 windows of 32 rows; for long prompt pieces (2048
-    // rows at contexts of 4-8k) one CTA per tile measured 9% faster.  Both
-    // give the same bits.
+    // With a workspace, head_dim 128: verify-sized batches (T <= 512) on
+    // the persistent decode kernel over (16 / G-token tile, KV head) items
+    // (8 windows of 32 rows: 75 us against 110 us for the group kernel),
+    // longer prompt pieces on the group kernel over a sorted list of
+    // 8-tile groups (one K / V chunk load per group instead of per tile:
+    // 2048 rows at contexts of 2-4k, 1.05 ms against 1.97 ms one CTA per
+    // tile).  Without a workspace, one CTA per 16-row tile.  All three give
+    // the same bits.
     if (D == 128 && ws && R <= MAX_SEGS && T <= 512 &&
         ws_bytes >= bi_prefill_attn_ws_bytes(T, R, Hq, Hkv)) {
         static std::once_flag f;
@@ -2611,6 +3099,40 @@ bi_status bi_prefill_attn_pool(const bi_bf16 *q, const int32_t *cu_q,
                 km, vm, qm, page_table, max_pages, n_pages, nullptr, Hq, Hkv,
                 G, scale, cnt, 0, list, k_pool, v_pool,
                 reinterpret_cast<uint16_t *>(out), status);
+    } else if (D == 128 && ws && R <= MAX_SEGS &&
+               ws_bytes >= bi_prefill_attn_ws_bytes(T, R, Hq, Hkv)) {
+        const int GT = tca::GT_MAX;
+        const int QPG = GT * QPT;
+        static std::once_flag f;
+        static bi_status fs;
+        std::call_once(f, [] {
+            fs = set_attr(attn_group_kernel, tca::GrpL::ALLOC);
+        });
+        if (fs != BI_OK) return fs;
+        const uint64_t pool_rows = (uint64_t)n_pages * Hkv * 16;
+        CUtensorMap km, vm;
+        bi_status st;
+        if ((st = bi_make_tmap_2d_bf16(&km, k_pool, D, pool_rows, D * 2, 64, 16,
+                                       true)) != BI_OK)
+            return st;
+        if ((st = bi_make_tmap_2d_bf16(&vm, v_pool, D, pool_rows, D * 2, 64, 16,
+                                       true)) != BI_OK)
+            return st;
+        const int groups = (T + QPG - 1) / QPG + R;
+        int4 *tmp = static_cast<int4 *>(ws);
+        int4 *list = tmp + groups;
+        int32_t *cnt = reinterpret_cast<int32_t *>(list + groups);
+        build_tiles_kernel<<<1, 1024, 0, stream>>>(cu_q, seg_req, pos, R, QPG,
+                                                   max_kv_len, tmp, list, cnt,
+                                                   status);
+        BI_LAUNCH_CHECK("prefill group list launch");
+        const int grid =
+            (int)std::min<int64_t>((int64_t)groups * Hkv, bi_sm_count());
+        attn_group_kernel<<<grid, tca::GRP_THREADS, tca::GrpL::ALLOC,
+                            stream>>>(
+            km, vm, reinterpret_cast<const uint16_t *>(q), list, cnt, pos,
+            page_table, max_pages, n_pages, Hq, Hkv, G, GT, scale,
+            reinterpret_cast<uint16_t *>(out), status);
     } else if (D == 128) {
         static std::once_flag f;
         static bi_status fs;

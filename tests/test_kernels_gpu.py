@@ -329,6 +329,39 @@ def test_prefill_matches_decode_bitwise(bi, orc, Hq, Hkv, D):
     assert not bits(out4)[T:].any()
 
 
+def test_prefill_group_path_bitwise(bi, orc):
+    """Prompt pieces longer than a verify batch (here 1358 rows) take the
+    group kernel, which loads each K / V chunk once for up to 8 query tiles
+    (32 tokens x 4 heads) of a segment: its outputs equal, bit for bit, the
+    one-CTA-per-tile prefill and decode of each row alone, over segments
+    whose lengths are not multiples of the group (partial groups), two
+    pieces of one request, a pad segment (zero outputs) and NaN-filled
+    stale pages; sampled rows agree with the oracle."""
+    Hq, Hkv, D = 32, 8, 128
+    lens = [2100, 700, 1600]
+    kv = PagedKV(lens, Hkv, D, seed=51)
+    segs = [(0, 1300, 700), (1, 100, 533), (2, 1490, 10), (2, 1500, 100),
+            (-1, 0, 15)]
+    T = sum(n for _, _, n in segs)
+    q = randn_bf16((T, Hq, D), 52)
+    grp, pos = prefill(bi, q, kv, segs, ws=True)
+    sync_ok(bi)
+    real = T - 15
+    assert not bits(grp)[real:].any()
+    one, _ = prefill(bi, q[:real].contiguous(), kv, segs[:-1])
+    sync_ok(bi)
+    assert np.array_equal(bits(grp)[:real], bits(one))
+    rows = sum([[r] * n for r, _, n in segs[:-1]], [])
+    dec = decode(bi, q[:real].contiguous(), kv, rows,
+                 [p + 1 for p in pos[:real]])
+    sync_ok(bi)
+    assert np.array_equal(bits(dec), bits(one))
+    pick = [0, 31, 32, 699, 700, 1232, 1233, 1242, real - 1]
+    ref = attn_ref(orc, q[pick].contiguous(), kv, [rows[i] for i in pick],
+                   [pos[i] for i in pick])
+    check_close(bits(grp)[pick], ref, orc)
+
+
 # -------------------------------------------------------------- argmax --
 
 def test_argmax_exact(bi, orc):
