@@ -919,10 +919,12 @@ __device__ __forceinline__ uint32_t poff(int row, int key) {
 // [256][128 B] layout the TMA writes; Q tile: 2 halves of [16][128 B].
 __device__ __forceinline__ void issue_qk(uint32_t d, uint32_t ktile,
                                          uint32_t qtile) {
+    // the two chains' steps alternate, so each step's MMA has the other
+    // chain's to overlap with (each chain's own k order is unchanged)
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
+    for (int kk = 0; kk < 8; ++kk)
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int h = 0; h < 2; ++h) {
             const uint32_t a = ktile + (kk >> 2) * (CHUNK * 128) +
                                h * (128 * 128) + (kk & 3) * 32;
             const uint32_t b = qtile + (kk >> 2) * (16 * 128) + (kk & 3) * 32;
@@ -2280,26 +2282,34 @@ __global__ void __launch_bounds__(tca::PRE_THREADS, 1)
 // heads each), i.e. up to 16 GT / G consecutive tokens, as build_tiles_kernel
 // lists them (QPT = 16 GT / G tokens per entry).  Per chunk the CTA loads K
 // and V once and runs, for each tile whose context reaches the chunk, the
-// per-tile computation of the other kernels: issue_qk (N = 16 rows),
-// softmax<16>, issue_pv, then the merge into the tile's running (m, l, o) in
-// chunk order with merge_scalars / merge_value.  So every row gets the bits
-// of decode and of the per-tile prefill kernel, while a chunk's K and V are
-// read once per group instead of once per tile.
-//   warps 0-7  softmax (thread t <-> key t), one tile after the other (P and
-//              the reduction slots double-buffered); warps 0-3 then merge
-//              the previous tile's O (thread = dim) into its running O in
-//              tensor memory, or write the tile's output after its last
-//              chunk;
+// per-tile computation of the other kernels: issue_qk (N = 16 rows), the
+// softmax of softmax<16>, issue_pv, then the merge into the tile's running
+// (m, l, o) in chunk order with merge_scalars / merge_value.  So every row
+// gets the bits of decode and of the per-tile prefill kernel, while a
+// chunk's K and V are read once per group instead of once per tile.
+//   warps 0-3, 4-7  two teams; team q takes the tiles i with i % 2 = q,
+//              one (tile, chunk) unit after the other, so two units are in
+//              flight and every tile's chunks are merged in order by one
+//              team.  A team issues its own MMAs (lane 0 of its first warp),
+//              so no unit waits on another warp: per unit, the scores to a
+//              shared-memory buffer (softmax_team, thread = key), then the
+//              next unit's QK MMAs into the team's S, the previous unit's
+//              PV products merged into the tile's running O in tensor
+//              memory (thread = dim) or written out after the tile's last
+//              chunk, the softmax (softmax_team_b, thread = (row, 32-key
+//              group)), the row factors by one thread per row
+//              (merge_scalars), then this unit's PV MMAs;
 //   warp 8     lanes 0-15 issue the TMA page boxes of a chunk (K and V as
-//              the other kernels load them); lane 0 issues the MMAs: the
-//              scores of tile n + 1 before the PV products of tile n, K of
-//              chunk c + 1 once the chunk's last scores have read K, V once
-//              its last PV products have read V.
-// Tensor memory (256 columns): S^T of two tiles (32 columns each), the PV
-// products of two tiles (16 each), the running O of each tile of the group
-// (16 each).  The persistent CTAs walk items in list order (most chunks
-// first); entries the builder marked invalid (no request, or a context out
-// of range) get zero outputs.  Waits are bounded; after one runs out every
+//              the other kernels load them): K of chunk c + 1 once each team
+//              with tiles in chunk c has committed its last QK MMAs of it
+//              (k_free), V once their last PV MMAs are committed (v_free),
+//              then zeroes the V rows past the group's last visible
+//              position (v_ready).
+// Tensor memory (256 columns): S^T of each team's unit (32 columns), each
+// team's PV products (16), the running O of each tile of the group (16).
+// The persistent CTAs walk items in list order (most chunks first);
+// entries the builder marked invalid (no request, or a context out of
+// range) get zero outputs.  Waits are bounded; after one runs out every
 // later wait of the CTA returns at once and the CTA finishes its walk
 // without waiting (garbage out, BI_ERR_TIMEOUT recorded), so no barrier is
 // left unmatched.
@@ -2310,15 +2320,15 @@ struct GrpL {
     static constexpr int QB = 16 * 128 * 2;               // one query tile
     static constexpr int SB = 16 * CHUNK * 4;             // scores, fp32
     static constexpr int K = 0, V = TB, Q = 2 * TB;
-    static constexpr int P = Q + GT_MAX * QB;             // 2 P tiles
-    static constexpr int S = P + 2 * P_TILE;              // 2 score buffers
+    static constexpr int P = Q + GT_MAX * QB;             // a P tile per team
+    static constexpr int S = P + 2 * P_TILE;              // a score buffer each
     static constexpr int ML = S + 2 * SB;                 // [GT_MAX][16] (M, L)
     static constexpr int AB = ML + GT_MAX * 16 * 2 * 4;   // [2][16] float4
     static constexpr int PROW = AB + 2 * 16 * 16;         // [GT_MAX][16]
     static constexpr int CI = PROW + GT_MAX * 16 * 4;     // [GT_MAX]
     static constexpr int BAR = CI + GT_MAX * 4 + 32;
-    // k_full, v_full, s_full[2], s_empty[2], p_full[2], o_full[2],
-    // o_empty[2], then the TMEM address and the failure flag
+    // k_full, v_full, v_ready, then per team s_full, o_full, k_free,
+    // v_free, then the TMEM address and the failure flag
     static constexpr int BYTES = BAR + 12 * 8 + 16;
     static constexpr int ALLOC = BYTES + 1024;
 };
@@ -2326,109 +2336,116 @@ constexpr int GRP_THREADS = STHREADS + 32;
 constexpr uint32_t GRP_TMEM = 256;
 constexpr uint32_t T_S = 0, T_OC = 64, T_ORUN = 128;
 
-// Word of (row, key) in a score buffer [16][256] fp32: within each 32-key
-// group g the 16-byte units are permuted by (g & 1) | (g & 2) << 1, so that
-// the float4 reads of softmax16_t's row phase hit eight distinct bank
-// groups in every quarter-warp.
+// Word of (row, key) in a score buffer [16][256] fp32: the eight 16-byte
+// units of each 32-key group g in the order u ^ g, so that the float4 reads
+// of softmax_team (eight groups of one row per quarter-warp) hit eight
+// distinct bank groups.
 __device__ __forceinline__ int sbw(int r, int key) {
-    const int g = key >> 5;
-    return r * CHUNK + (((key >> 2) ^ ((g & 1) | ((g & 2) << 1))) << 2) +
-           (key & 3);
+    const int u = key >> 2;
+    return r * CHUNK + ((u ^ ((u >> 3) & 7)) << 2) + (key & 3);
 }
 
-// The softmax of softmax<16> for one chunk of a 16-row tile, bit for bit,
-// with fewer instructions: the same scaled and masked scores, the same
-// exact row maximum (fmaxf), p = exp_s(s - m) with the same masking, the
-// same bf16(p) in the P tile, and the row sum in the same order (the
-// xor-tree of lane 0 over each 32-key group, then the groups in order).
-//   Phase A, thread t <-> key t: scores from S^T in TMEM, scaled and
-//   masked, to the score buffer.
-//   Phase B, thread <-> (row r = 2 w + lane / 16, group g = lane / 2 % 8,
-//   half h = lane % 2): keys 32 g + 8 h + [0, 8) and 32 g + 16 + 8 h +
-//   [0, 8).  The maximum is a 16-lane xor reduction (exact, any order);
-//   the group sum's first tree level (keys i, i + 16) is thread-local, the
-//   second (i, i + 8) pairs the two halves (one shuffle), the rest is
-//   thread-local again; the groups are then added in order.  P leaves as
-//   two 16-byte units per thread.
-// Every thread of row r returns its m and l.  len(r) = visible keys of row
-// r in chunk c: min(256, prow[r] + 1 - 256 c), at least 0.
-__device__ __forceinline__ void softmax16_t(uint32_t s_tmem, float scale,
-                                            const int *prow, int c, float *sb,
-                                            uint32_t ptile, float &m_out,
-                                            float &l_out, uint64_t *s_empty) {
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    {
-        const int key = 32 * w + lane;
-        float v[16];
-        tmem_ld_16cols(
-            s_tmem + ((uint32_t)((w & 3) * 32) << 16) + (w >> 2) * 16, v);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(s_empty);
+// Team barrier (named barrier 2 + team, 128 threads).
+__device__ __forceinline__ void sync_team(int team) {
+    asm volatile("bar.sync %0, 128;" ::"r"(2 + team) : "memory");
+}
+
+// The softmax of softmax<16> for one chunk of a 16-row tile, bit for bit, by
+// one team of four warps (thread t of the team, warp wq = t / 32): the same
+// scaled and masked scores, the same exact row maximum (fmaxf), p =
+// exp_s(s - m) with the same masking, the same bf16(p) in the P tile and the
+// row sum in the same order (lane 0's xor tree over each 32-key group, then
+// the eight groups in order).
+//   softmax_team (phase A), thread <-> keys 32 wq + lane and 128 + 32 wq +
+//   lane: scores from S^T in TMEM (lane quarter wq), scaled and masked, to
+//   the buffer; ends with the team barrier (S fully read, buffer written).
+//   softmax_team_b (phase B), thread <-> (row r = 4 wq + lane / 8, group
+//   g = lane % 8): keys 32 g .. 32 g + 31 of row r.  The maximum is exact
+//   (any order); the group's xor tree is thread-local; the groups are added
+//   in order over the row's 8 lanes.  P leaves as four 16-byte units per
+//   thread.  Every thread of row r returns its m and l.
+// prow[r] + 1 - 256 c = keys of chunk c visible to row r.
+__device__ __forceinline__ void softmax_team(uint32_t s_tmem, float scale,
+                                             const int *prow, int c, float *sb,
+                                             uint32_t ptile, int team) {
+    const int wq = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
+    float v[32];
+    tmem_ld_32cols(s_tmem + ((uint32_t)(wq * 32) << 16), v);
+    const int k0 = 32 * wq + lane, k1 = k0 + 128;
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const int len = prow[r] + 1 - c * CHUNK;
-            const float s = __fmul_rn(v[r], scale);
-            sb[sbw(r, key)] = key < len ? s : -INFINITY;
-        }
+    for (int r = 0; r < 16; ++r) {
+        const int len = prow[r] + 1 - c * CHUNK;
+        const float s0 = __fmul_rn(v[r], scale);
+        const float s1 = __fmul_rn(v[16 + r], scale);
+        sb[sbw(r, k0)] = k0 < len ? s0 : -INFINITY;
+        sb[sbw(r, k1)] = k1 < len ? s1 : -INFINITY;
     }
-    sync_softmax();
-    const int r = 2 * w + (lane >> 4), g = (lane >> 1) & 7, h = lane & 1;
-    const int klo = 32 * g + 8 * h;
-    float x[16];
+    tc_fence_before();
+    sync_team(team);
+}
+
+__device__ __forceinline__ void softmax_team_b(float scale, const int *prow,
+                                               int c, const float *sb,
+                                               uint32_t ptile, float &m_out,
+                                               float &l_out) {
+    const int wq = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
+    const int r = 4 * wq + (lane >> 3), g = lane & 7;
+    const int k0 = 32 * g;
+    float x[32];
 #pragma unroll
-    for (int q = 0; q < 2; ++q)
+    for (int e = 0; e < 8; ++e) {
+        const float4 f =
+            *reinterpret_cast<const float4 *>(sb + sbw(r, k0 + 4 * e));
+        x[4 * e + 0] = f.x;
+        x[4 * e + 1] = f.y;
+        x[4 * e + 2] = f.z;
+        x[4 * e + 3] = f.w;
+    }
+    // exact maximum: a tree over the 32 values, then 8 lanes
+    float mm[16];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const float4 f = *reinterpret_cast<const float4 *>(
-                sb + sbw(r, klo + 16 * q + 4 * e));
-            x[8 * q + 4 * e + 0] = f.x;
-            x[8 * q + 4 * e + 1] = f.y;
-            x[8 * q + 4 * e + 2] = f.z;
-            x[8 * q + 4 * e + 3] = f.w;
-        }
-    float mx = x[0];
+    for (int j = 0; j < 16; ++j) mm[j] = fmaxf(x[j], x[j + 16]);
 #pragma unroll
-    for (int j = 1; j < 16; ++j) mx = fmaxf(mx, x[j]);
+    for (int j = 0; j < 8; ++j) mm[j] = fmaxf(mm[j], mm[j + 8]);
 #pragma unroll
-    for (int o = 8; o >= 1; o >>= 1)
+    for (int j = 0; j < 4; ++j) mm[j] = fmaxf(mm[j], mm[j + 4]);
+    float mx = fmaxf(fmaxf(mm[0], mm[2]), fmaxf(mm[1], mm[3]));
+#pragma unroll
+    for (int o = 4; o >= 1; o >>= 1)
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     const float mu = mx == -INFINITY ? 0.f : mx;
     const int len = prow[r] + 1 - c * CHUNK;
-    float pv[16];
 #pragma unroll
-    for (int q = 0; q < 2; ++q)
+    for (int j = 0; j < 32; ++j)
+        x[j] = k0 + j < len ? exp_s(__fsub_rn(x[j], mu)) : 0.f;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int key = klo + 16 * q + j;
-            pv[8 * q + j] =
-                key < len ? exp_s(__fsub_rn(x[8 * q + j], mu)) : 0.f;
-        }
-#pragma unroll
-    for (int q = 0; q < 2; ++q)
+    for (int e = 0; e < 4; ++e)
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                         ptile + poff(r, klo + 16 * q)),
-                     "r"(pack_bf16x2(pv[8 * q + 0], pv[8 * q + 1])),
-                     "r"(pack_bf16x2(pv[8 * q + 2], pv[8 * q + 3])),
-                     "r"(pack_bf16x2(pv[8 * q + 4], pv[8 * q + 5])),
-                     "r"(pack_bf16x2(pv[8 * q + 6], pv[8 * q + 7]))
+                         ptile + poff(r, k0 + 8 * e)),
+                     "r"(pack_bf16x2(x[8 * e + 0], x[8 * e + 1])),
+                     "r"(pack_bf16x2(x[8 * e + 2], x[8 * e + 3])),
+                     "r"(pack_bf16x2(x[8 * e + 4], x[8 * e + 5])),
+                     "r"(pack_bf16x2(x[8 * e + 6], x[8 * e + 7]))
                      : "memory");
-    // lane 0's xor tree over group g: level 16 pairs keys (i, i + 16),
-    // level 8 (i, i + 8) across the halves, then levels 4, 2, 1
-    float b[8];
+    // lane 0's xor tree over the group's keys i = 0..31: levels 16, 8, 4,
+    // 2, 1 pair i with i + 16, i + 8, ...
+    float a[16];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const float a = __fadd_rn(pv[j], pv[8 + j]);
-        b[j] = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, 1));
-    }
-    const float c0 = __fadd_rn(b[0], b[4]), c1 = __fadd_rn(b[1], b[5]);
-    const float c2 = __fadd_rn(b[2], b[6]), c3 = __fadd_rn(b[3], b[7]);
-    const float W = __fadd_rn(__fadd_rn(c0, c2), __fadd_rn(c1, c3));
-    const int rb = lane & 16;
-    float l = __shfl_sync(0xffffffffu, W, rb);
+    for (int i = 0; i < 16; ++i) a[i] = __fadd_rn(x[i], x[i + 16]);
 #pragma unroll
-    for (int k = 1; k < SW; ++k)
-        l = __fadd_rn(l, __shfl_sync(0xffffffffu, W, rb + 2 * k));
+    for (int i = 0; i < 8; ++i) a[i] = __fadd_rn(a[i], a[i + 8]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = __fadd_rn(a[i], a[i + 4]);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) a[i] = __fadd_rn(a[i], a[i + 2]);
+    const float W = __fadd_rn(a[0], a[1]);
+    const int rb = lane & 24;
+    float w8[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w8[k] = __shfl_sync(0xffffffffu, W, rb + k);
+    float l = w8[0];
+#pragma unroll
+    for (int k = 1; k < 8; ++k) l = __fadd_rn(l, w8[k]);
     m_out = mx;
     l_out = l;
 }
@@ -2461,12 +2478,11 @@ __global__ void __launch_bounds__(tca::GRP_THREADS, 1)
     int *s_prow = reinterpret_cast<int *>(smem + GrpL::PROW);
     int *s_ci = reinterpret_cast<int *>(smem + GrpL::CI);
     uint64_t *k_full = reinterpret_cast<uint64_t *>(smem + GrpL::BAR);
-    uint64_t *v_full = k_full + 1;
-    uint64_t *s_full = k_full + 2, *s_empty = k_full + 4;
-    uint64_t *p_full = k_full + 6, *o_full = k_full + 8;
-    uint64_t *o_empty = k_full + 10;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(k_full + 12);
-    volatile int *fail = reinterpret_cast<volatile int *>(k_full + 12) + 1;
+    uint64_t *v_full = k_full + 1, *v_ready = k_full + 2;
+    uint64_t *s_full = k_full + 3, *o_full = k_full + 5;
+    uint64_t *k_free = k_full + 7, *v_free = k_full + 9;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(k_full + 11);
+    volatile int *fail = reinterpret_cast<volatile int *>(k_full + 11) + 1;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int QPT = 16 / G;
     const int n_valid = cnt[0], n_all = cnt[1];
@@ -2493,12 +2509,12 @@ __global__ void __launch_bounds__(tca::GRP_THREADS, 1)
     if (threadIdx.x == 0) {
         mbar_init(k_full, 1);
         mbar_init(v_full, 1);
+        mbar_init(v_ready, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&s_empty[i], SW);
-            mbar_init(&p_full[i], SW);
             mbar_init(&o_full[i], 1);
-            mbar_init(&o_empty[i], 4);
+            mbar_init(&k_free[i], 1);
+            mbar_init(&v_free[i], 1);
         }
         mbar_fence_init();
         *fail = 0;
@@ -2513,7 +2529,9 @@ __global__ void __launch_bounds__(tca::GRP_THREADS, 1)
         tma_prefetch_desc(&vmap);
     }
 
-    int nu = 0, nc = 0;  // units and chunks of the items done so far
+    // over all items so far: units done by each team, chunks done, and the
+    // chunks in which each team had units (the phases of k_free / v_free)
+    int nq[2] = {0, 0}, nc = 0, fq[2] = {0, 0};
     for (int it = blockIdx.x; it < items; it += gridDim.x) {
         const int4 e = list[it / Hkv];
         const int g = it % Hkv;
@@ -2547,16 +2565,27 @@ __global__ void __launch_bounds__(tca::GRP_THREADS, 1)
         }
         __syncthreads();
         // first tile whose context reaches chunk c (tile contexts grow with
-        // the tile index: a segment's positions are consecutive)
+        // the tile index: a segment's positions are consecutive); team t's
+        // tiles in chunk c are first_t(c, t), + 2, ... < nt, so a team's
+        // chunks form a prefix 0 .. C_t - 1
         auto first_tile = [&](int c) {
             int i = 0;
             while (i < nt - 1 && s_ci[i] <= c) ++i;
             return i;
         };
+        auto first_t = [&](int c, int t) {
+            const int i0 = first_tile(c);
+            return i0 + ((i0 & 1) != t);
+        };
         const int32_t *pt_row = page_table + (int64_t)req * max_pages;
 
         if (warp == SW) {
-            // ------------------------------------------- loads and MMAs --
+            // ---------------------------------------------------- loads --
+            // K of chunk c + 1 once every team with tiles in chunk c has
+            // committed its last scores of it (k_free), V likewise after the
+            // last PV products (v_free); V rows past the group's last
+            // visible position in a chunk's last page are then zeroed
+            // (0 * NaN would poison the PV sums) before v_ready.
             auto load = [&](int c, bool is_k) {
                 int pg = -1;
                 if (lane < 16) {
@@ -2581,89 +2610,91 @@ __global__ void __launch_bounds__(tca::GRP_THREADS, 1)
                                     is_k ? &kmap : &vmap, h * 64, row, bar);
                 }
             };
-            // PV products of unit u (tile of chunk cu); V of chunk cu + 1
-            // once the chunk's last products have read V
-            auto pv = [&](int u, int cu, bool first_c, bool last_c) {
-                const int j = u & 1;
-                if (lane == 0) {
-                    if (first_c) gw(v_full, (nc + cu) & 1);
-                    gw(&p_full[j], (u >> 1) & 1);
-                    if (u >= 2) gw(&o_empty[j], ((u >> 1) - 1) & 1);
-                    tc_fence_after();
-                    issue_pv(tmem + T_OC + 16 * j, vtile, ptile + j * P_TILE);
-                    tc_commit(&o_full[j]);
-                    if (last_c && cu + 1 < C) gw(&o_full[j], (u >> 1) & 1);
-                }
+            auto v_in = [&](int c) {
+                gw(v_full, (nc + c) & 1);
+                const int vl = min(CHUNK, L - c * CHUNK);
+                if (vl & 15)
+                    zero_v_rows(smem + GrpL::V, vl, (vl + 15) & ~15, lane, 32);
+                fence_proxy_async_smem();
                 __syncwarp();
-                if (last_c && cu + 1 < C) load(cu + 1, false);
+                if (lane == 0) mbar_arrive(v_ready);
             };
+            int f2[2] = {fq[0], fq[1]};
             load(0, true);
             load(0, false);
-            int u = nu;
-            int pu = -1, pcu = 0;
-            bool pfirst = false, plast = false;
-            for (int c = 0; c < C; ++c) {
-                const int i0 = first_tile(c);
-                for (int i = i0; i < nt; ++i, ++u) {
-                    const int j = u & 1;
-                    if (lane == 0) {
-                        if (i == i0) gw(k_full, (nc + c) & 1);
-                        if (u >= 2) gw(&s_empty[j], ((u >> 1) - 1) & 1);
-                        tc_fence_after();
-                        issue_qk(tmem + T_S + 32 * j, ktile,
-                                 qtile + i * GrpL::QB);
-                        tc_commit(&s_full[j]);
-                    }
-                    __syncwarp();
-                    if (pu >= 0) pv(pu, pcu, pfirst, plast);
-                    if (i == nt - 1 && c + 1 < C) {
-                        // the chunk's last scores have read K
-                        if (lane == 0) gw(&s_full[j], (u >> 1) & 1);
-                        __syncwarp();
-                        load(c + 1, true);
-                    }
-                    pu = u;
-                    pcu = c;
-                    pfirst = i == i0;
-                    plast = i == nt - 1;
-                }
+            v_in(0);
+            for (int c = 1; c < C; ++c) {
+                bool act[2];
+                for (int t = 0; t < 2; ++t) act[t] = first_t(c - 1, t) < nt;
+                if (lane == 0)
+                    for (int t = 0; t < 2; ++t)
+                        if (act[t]) gw(&k_free[t], f2[t] & 1);
+                __syncwarp();
+                load(c, true);
+                if (lane == 0)
+                    for (int t = 0; t < 2; ++t)
+                        if (act[t]) gw(&v_free[t], f2[t] & 1);
+                __syncwarp();
+                load(c, false);
+                v_in(c);
+                for (int t = 0; t < 2; ++t) f2[t] += act[t];
             }
-            if (pu >= 0) pv(pu, pcu, pfirst, plast);
         } else {
-            // --------------------------------------- softmax and merge --
-            int pu = -1, pi_ = 0, pc = 0;
-            // merge of unit u (tile i, chunk c) by warps 0-3, thread = dim:
-            // per row, keep O (chunk not visible), take the chunk's o (the
-            // tile's first chunk) or O a + o b, with (a, b) and the row's L
-            // from the row owner's merge_scalars
-            auto merge = [&](int u, int i, int c) {
-                const int j = u & 1;
-                const uint32_t lq = (uint32_t)(warp * 32) << 16;
-                gw(&o_full[j], (u >> 1) & 1);
+            // ------------------------------- softmax teams (and MMAs) --
+            const int team = warp >> 2, wq = warp & 3;
+            const bool issuer = wq == 0 && lane == 0;
+            const uint32_t lq = (uint32_t)(wq * 32) << 16;
+            float *sb = sbuf + team * (GrpL::SB / 4);
+            float4 *ab = abs_ + team * 16;
+            const uint32_t s_t = tmem + T_S + 32 * team;
+            const uint32_t oc_t = tmem + T_OC + 16 * team;
+            const uint32_t p_t = ptile + team * P_TILE;
+            // the team's units: chunk c, tiles first_t(c, team), + 2, ..;
+            // cc == C once the team has none left
+            int cc = 0, ii = first_t(0, team);
+            if (ii >= nt) cc = C;
+            auto next = [&](int &c, int &i) {
+                i += 2;
+                if (i >= nt) {
+                    ++c;
+                    i = c < C ? first_t(c, team) : nt;
+                    if (i >= nt) c = C;
+                }
+            };
+            auto qk = [&](int c, int i) {   // issuer only
+                if (i == first_t(c, team)) gw(k_full, (nc + c) & 1);
+                tc_fence_after();
+                issue_qk(s_t, ktile, qtile + i * GrpL::QB);
+                tc_commit(&s_full[team]);
+                if (i + 2 >= nt) tc_commit(&k_free[team]);
+            };
+            // merge of the team's unit n (tile i, chunk c), thread = dim:
+            // per row keep O (chunk not visible), take the chunk's o (the
+            // tile's first chunk) or O a + o b, with (a, b) and L from the
+            // row owner's merge_scalars
+            auto merge = [&](int n, int i, int c) {
+                gw(&o_full[team], n & 1);
                 tc_fence_after();
                 float o[16], O[16];
-                tmem_ld_16cols(tmem + T_OC + 16 * j + lq, o);
+                tmem_ld_16cols(oc_t + lq, o);
                 if (c > 0)
                     tmem_ld_16cols(tmem + T_ORUN + 16 * i + lq, O);
                 else
 #pragma unroll
                     for (int r = 0; r < 16; ++r) O[r] = 0.f;
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&o_empty[j]);
                 float Lr[16];
 #pragma unroll
                 for (int r = 0; r < 16; ++r) {
-                    const float4 ab = abs_[j * 16 + r];
-                    const int flag = __float_as_int(ab.z);
+                    const float4 f = ab[r];
+                    const int flag = __float_as_int(f.z);
                     if (flag == 1)
                         O[r] = o[r];
                     else if (flag == 2)
-                        O[r] = merge_value(O[r], o[r], ab.x, ab.y);
-                    Lr[r] = ab.w;
+                        O[r] = merge_value(O[r], o[r], f.x, f.y);
+                    Lr[r] = f.w;
                 }
                 if (c == s_ci[i] - 1) {
-                    const int dim = warp * 32 + lane;
+                    const int dim = wq * 32 + lane;
 #pragma unroll
                     for (int r = 0; r < 16; ++r) {
                         const int tk = i * QPT + r / G, hh = r % G;
@@ -2673,67 +2704,85 @@ __global__ void __launch_bounds__(tca::GRP_THREADS, 1)
                     }
                 } else {
                     tmem_st_16cols(tmem + T_ORUN + 16 * i + lq, O);
-                    tc_fence_before();
                 }
+                tc_fence_before();
             };
-            int u = nu;
-            for (int c = 0; c < C; ++c) {
-                const int i0 = first_tile(c);
-                for (int i = i0; i < nt; ++i, ++u) {
-                    const int j = u & 1;
-                    gw(&s_full[j], (u >> 1) & 1);
-                    tc_fence_after();
-                    float m, l;
-                    softmax16_t(tmem + T_S + 32 * j, scale, s_prow + i * 16, c,
-                                sbuf + j * (GrpL::SB / 4), ptile + j * P_TILE,
-                                m, l, &s_empty[j]);
-                    if ((lane & 15) == 0) {
-                        // the row's running (M, L) and this chunk's factors
-                        const int r = 2 * warp + (lane >> 4);
-                        float *ml = mls + (i * 16 + r) * 2;
-                        float a = 0.f, bb = 0.f;
-                        int flag = 0;
-                        if (s_prow[i * 16 + r] + 1 - c * CHUNK > 0) {
-                            if (c == 0) {
-                                ml[0] = m;
-                                ml[1] = l;
-                                flag = 1;
-                            } else {
-                                float M = ml[0], L = ml[1];
-                                merge_scalars(M, L, m, l, a, bb);
-                                ml[0] = M;
-                                ml[1] = L;
-                                flag = 2;
-                            }
+            if (issuer && cc < C) qk(cc, ii);
+            int n = nq[team];
+            int pn = -1, pi_ = 0, pc = 0;
+            while (cc < C) {
+                const int c = cc, i = ii;
+                int nc2 = cc, ni = ii;
+                next(nc2, ni);
+                gw(&s_full[team], n & 1);
+                tc_fence_after();
+                softmax_team(s_t, scale, s_prow + i * 16, c, sb, p_t, team);
+                // phase A done by the whole team (S read): the next unit's
+                // scores may overwrite S
+                if (issuer && nc2 < C) qk(nc2, ni);
+                if (pn >= 0) merge(pn, pi_, pc);
+                sync_team(team);  // the previous unit's P and factors used
+                float m, l;
+                softmax_team_b(scale, s_prow + i * 16, c, sb, p_t, m, l);
+                if ((lane & 7) == 0) {
+                    // the row's running (M, L) and this chunk's factors
+                    const int r = 4 * wq + (lane >> 3);
+                    float *ml = mls + (i * 16 + r) * 2;
+                    float a = 0.f, bb = 0.f;
+                    int flag = 0;
+                    if (s_prow[i * 16 + r] + 1 - c * CHUNK > 0) {
+                        if (c == 0) {
+                            ml[0] = m;
+                            ml[1] = l;
+                            flag = 1;
+                        } else {
+                            float M = ml[0], Lr = ml[1];
+                            merge_scalars(M, Lr, m, l, a, bb);
+                            ml[0] = M;
+                            ml[1] = Lr;
+                            flag = 2;
                         }
-                        abs_[j * 16 + r] =
-                            make_float4(a, bb, __int_as_float(flag), ml[1]);
                     }
-                    if (i == i0) {
-                        // V rows past the group's last visible position in
-                        // the chunk's last page: zero (0 * NaN would poison
-                        // the PV sums)
-                        gw(v_full, (nc + c) & 1);
-                        const int vl = min(CHUNK, L - c * CHUNK);
-                        if (vl & 15)
-                            zero_v_rows(smem + GrpL::V, vl, (vl + 15) & ~15,
-                                        threadIdx.x, STHREADS);
-                    }
-                    fence_proxy_async_smem();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&p_full[j]);
-                    if (warp < 4 && pu >= 0) merge(pu, pi_, pc);
-                    pu = u;
-                    pi_ = i;
-                    pc = c;
+                    ab[r] = make_float4(a, bb, __int_as_float(flag), ml[1]);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                sync_team(team);  // P and the factors are written
+                if (issuer) {
+                    if (i == first_t(c, team)) gw(v_ready, (nc + c) & 1);
+                    tc_fence_after();
+                    issue_pv(oc_t, vtile, p_t);
+                    tc_commit(&o_full[team]);
+                    if (i + 2 >= nt) tc_commit(&v_free[team]);
+                }
+                pn = n;
+                pi_ = i;
+                pc = c;
+                ++n;
+                cc = nc2;
+                ii = ni;
+            }
+            if (pn >= 0) merge(pn, pi_, pc);
+            if (issuer) {
+                // the commits of the item's last chunk have landed before
+                // the next item waits on these barriers again
+                int ch = 0;
+                for (int c = 0; c < C; ++c) ch += first_t(c, team) < nt;
+                if (ch > 0) {
+                    gw(&k_free[team], (fq[team] + ch - 1) & 1);
+                    gw(&v_free[team], (fq[team] + ch - 1) & 1);
                 }
             }
-            sync_softmax();  // the last unit's row factors are in
-            if (warp < 4 && pu >= 0) merge(pu, pi_, pc);
         }
-        // the same walk in every role: advance the unit and chunk counters
-        for (int c = 0; c < C; ++c) nu += nt - first_tile(c);
+        // the same walk in every role: advance the counters
+        for (int c = 0; c < C; ++c)
+            for (int t = 0; t < 2; ++t) {
+                const int i0 = first_t(c, t);
+                if (i0 < nt) {
+                    nq[t] += (nt - i0 + 1) / 2;
+                    ++fq[t];
+                }
+            }
         nc += C;
     }
     // entries with no valid context: zero outputs
