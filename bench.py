@@ -310,7 +310,17 @@ class Bench:
         self.n_flag = wl["n_flag"]
         self._make_candidates()
         self.table0 = self.eng.page_table.clone()
+        self.host0 = self.eng.host_table.copy()
+        self.alloc0 = (list(self.eng.alloc.free), dict(self.eng.alloc.refs))
         self._make_plans()
+
+    def restore_pages(self):
+        """Page table, host page bookkeeping and free list back to the
+        reservation made at start-up (verifications cut rows)."""
+        self.eng.page_table.copy_(self.table0)
+        self.eng.host_table[:] = self.host0
+        self.eng.alloc.free = list(self.alloc0[0])
+        self.eng.alloc.refs = dict(self.alloc0[1])
 
     def decode_iters(self, n=None):
         bi, eng = self.bi, self.eng
@@ -589,7 +599,7 @@ def run_report(args):
     a = copy.copy(args)
     a.batch = 256
     b = Bench(a, dev, weights=W)
-    rep["llm42_fast_path"] = fast_path_report(b)
+    rep["llm42_fast_path"] = llm42_mixed(b)
     del b
     torch.cuda.empty_cache()
     # prefill
@@ -1234,6 +1244,7 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_extras:
         # the other reported numbers, each on the same box in the same run
         line["decode_batch_sweep"] = decode_batch_sweep(b)
+        line["llm42_mixed_traffic"] = llm42_mixed(b)
         line["long_prompt"] = long_prompt_stress(b)
         line["gemm_sweep"] = gemm_sweep(torch, bi, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -1246,73 +1257,23 @@ def run_ours(args):
 
 # ------------------------------------------------------------- comparator --
 
-def cublas_forward(b):
-    """Decode forward of the bench's requests with every GEMM through
-    torch.matmul (cuBLAS heuristics: not batch-invariant), the library's
-    norm / RoPE / attention around them; returns fwd(tok, pos, maxkv) ->
-    fp32 logits [B, V]."""
-    import torch
-    bi = b.bi
-    eng = b.eng
-    S = b.shape
-    B = b.wl["batch"]
-    H, F, D, Hq, Hkv = S.hidden, S.ffn, S.head_dim, S.n_heads, S.n_kv_heads
-    dev = b.dev
-    x = torch.empty(B, H, dtype=torch.bfloat16, device=dev)
-    h = torch.empty(B, H, dtype=torch.bfloat16, device=dev)
-    q = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev)
-    a = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev)
-    kvl = torch.empty(B, dtype=torch.int32, device=dev)
-    ws = torch.empty(bi.bi_decode_attn_workspace_size(
-        B, Hq, D, eng.max_kv_len) // 4, dtype=torch.float32, device=dev)
-    W = b.weights
-    scale = 1.0 / math.sqrt(D)
-
-    def fwd(tok, pos, maxkv):
-        torch.index_select(W["embed"], 0, tok, out=h)
-        kvl.copy_(pos + 1)
-        d = None
-        for l, lw in enumerate(W["layers"]):
-            if d is None:
-                bi.bi_rmsnorm(None, 0, None, h, lw["attn_norm"], B, H, S.eps, x)
-            else:
-                bi.bi_rmsnorm(d, 1, None, h, lw["attn_norm"], B, H, S.eps, x)
-            qkv = torch.matmul(x, lw["wqkv"].T).float()
-            bi.bi_rope(qkv, 1, pos, b.slots, Hq, Hkv, D, S.theta, q,
-                       eng.k_pool[l], eng.v_pool[l], eng.page_table)
-            bi.bi_paged_decode_attn(q, eng.k_pool[l], eng.v_pool[l],
-                                    eng.page_table, b.slots, kvl, maxkv, scale,
-                                    a, ws)
-            o = torch.matmul(a.view(B, Hq * D), lw["wo"].T).float()
-            bi.bi_rmsnorm(o, 1, None, h, lw["ffn_norm"], B, H, S.eps, x)
-            g = torch.matmul(x, lw["wg"].T)
-            u = torch.matmul(x, lw["wu"].T)
-            f = torch.nn.functional.silu(g) * u
-            d = torch.matmul(f, lw["wd"].T).float()
-        bi.bi_rmsnorm(d, 1, None, h, W["final_norm"], B, H, S.eps, x)
-        return torch.matmul(x, W["lm_head"].T).float()
-
-    return fwd
-
-
 def run_comparator(b, args):
-    """The same decode iterations with every GEMM through torch.matmul
-    (cuBLAS default heuristics), the library's norm / RoPE / attention /
-    argmax around them, against the invariant path's decode iterations alone.
-    Run with the default bf16 reduced-precision setting and with it off
-    (ybb.press section 5)."""
+    """The same decode iterations on the non-invariant fast path (FastPath:
+    every GEMM through cuBLAS via torch.mm, default heuristics, gate and up
+    as one GEMM, fp32 output straight from cuBLAS; the library's norm /
+    RoPE / attention / argmax around them), against the invariant path's
+    decode iterations alone.  Run with the default bf16 reduced-precision
+    setting and with it off (ybb.press section 5)."""
     import torch
-    bi = b.bi
+    from deterministic_invariant_bf16_gb300 import fastpath
     B, it = b.wl["batch"], b.wl["iters"]
-    fwd = cublas_forward(b)
+    fast = fastpath.FastPath(b.eng, B)
 
     def run_cmp():
-        cur = b.tok0.clone()
+        cur = b.tok0
         for i in range(it):
-            lg = fwd(cur, b.pos[i], b.maxkv[i])
-            ids = b.ids[i]
-            bi.bi_argmax_logits(lg, ids)
-            cur = ids
+            fast.decode(cur, b.pos[i], b.slots, b.ids[i], b.maxkv[i])
+            cur = b.ids[i]
 
     def timed(fn, reps):
         for _ in range(2):
@@ -1329,7 +1290,9 @@ def run_comparator(b, args):
 
     reps = max(2, min(args.steps, 4))
     ours_ms = timed(b.decode_iters, reps)
-    out = {"what": "same decode iterations, GEMMs via torch.matmul (cuBLAS)",
+    out = {"what": "same decode iterations, GEMMs via torch.mm (cuBLAS), "
+                   "gate/up as one GEMM, fp32 output %s" %
+                   ("from cuBLAS" if fast.f32 else "by a cast"),
            "invariant_decode_tok_s": B * it / (ours_ms / 1e3)}
     flag = torch.backends.cuda.matmul.allow_bf16_reduced_precision_reduction
     for name, val in (("cublas_default", flag), ("cublas_no_reduced_bf16", False)):
@@ -1339,89 +1302,74 @@ def run_comparator(b, args):
     torch.backends.cuda.matmul.allow_bf16_reduced_precision_reduction = flag
     out["invariant_over_default"] = (out["invariant_decode_tok_s"] /
                                      out["cublas_default_tok_s"])
+    b.restore_pages()
     return out
 
 
-def fast_path_report(b, fractions=(0.02, 0.10, 0.50, 1.0)):
-    """LLM-42 with a real non-deterministic fast path (LLM-42 page, core
-    method: decode everything on the fast path, verify the deterministic
-    requests' windows with the invariant path, commit up to the first
-    mismatch).  Per deterministic fraction d, one round: 32 greedy decode
-    iterations of all B requests on the cuBLAS path, then the first
-    round(d * B) requests' 32-token windows verified in groups of 8 (256
-    rows) by verify_commit_rollback.  Committed tokens: 32 per unverified
-    request, commit length (+1 for the verifier's own token after a
-    mismatch) per verified one.  Against: 32 invariant decode iterations of
-    all B requests."""
+def llm42_mixed(b, fractions=(0.0, 0.02, 0.10, 0.50, 1.0), max_new=48,
+                window=32):
+    """LLM-42 with a real non-invariant fast path and selective determinism
+    (LLM-42 summary, 核心方法 and section 5.1: +33% over the deterministic
+    mode at 10% deterministic traffic): the step workload's 256 requests
+    produce max_new tokens each through SelectiveScheduler: every request
+    decodes on FastPath (cuBLAS), the first round(d * 256) are flagged and
+    their tokens verified in 32-token windows packed into 256-row verify
+    batches.  Against: the same 256 x max_new tokens decoded greedily on
+    the invariant path alone, with the same one-call-per-iteration host
+    loop.  Rates are committed output tokens over wall time (the scheduler
+    reads every iteration's tokens on the host)."""
     import torch
-    eng, wl = b.eng, b.wl
-    B, w = wl["batch"], 32
+    from deterministic_invariant_bf16_gb300 import fastpath, scheduler
+    wl, eng = b.wl, b.eng
+    B = wl["batch"]
     ctx = wl["ctx"]
+    first = wl["first_tokens"]
+    fast = fastpath.FastPath(eng, B)
+    out = {"requests": B, "max_new": max_new, "window": window}
+
+    def hist(r):
+        return [0] * int(ctx[r]) + [int(first[r])]
+
+    # invariant only
+    b.restore_pages()
     dev = b.dev
-    fwd = cublas_forward(b)
-    pos = [torch.from_numpy(ctx + i).to(dev).int() for i in range(w)]
-    maxkv = [int(ctx.max()) + i + 1 for i in range(w)]
-    ids = torch.empty(w, B, dtype=torch.int32, device=dev)
-    logits = torch.empty(B, b.shape.vocab, dtype=torch.float32, device=dev)
-
-    def fast():
-        cur = b.tok0
-        for i in range(w):
-            lg = fwd(cur, pos[i], maxkv[i])
-            b.bi.bi_argmax_logits(lg, ids[i])
-            cur = ids[i]
-
-    def invariant():
-        cur = b.tok0
-        for i in range(w):
-            eng.decode(cur, pos[i], b.slots, logits=logits, ids=ids[i],
-                       max_kv_len=maxkv[i])
-            cur = ids[i]
-
-    def rearm(slots):
-        for r in slots:
-            eng.reserve(r, int(ctx[r]) + wl["headroom"])
-
-    def timed(fn):
-        torch.cuda.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record()
-        out = fn()
-        e1.record()
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1), out
-
-    fast()
-    invariant()
-    inv_ms, _ = timed(invariant)
-    out = {"window": w, "batch": B,
-           "invariant_only_tok_s": B * w / (inv_ms / 1e3), "fractions": {}}
-    last = b.tok0.cpu().numpy()
+    slots = b.slots
+    ids = torch.empty(B, dtype=torch.int32, device=dev)
+    lg = torch.empty(B, b.shape.vocab, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    cur = torch.from_numpy(first.astype(np.int32)).to(dev)
+    for i in range(max_new):
+        pos = torch.from_numpy((ctx + i).astype(np.int32)).to(dev)
+        eng.decode(cur, pos, slots, logits=lg, ids=ids,
+                   max_kv_len=int(ctx.max()) + i + 1)
+        cur = torch.from_numpy(ids.cpu().numpy()).to(dev)
+    torch.cuda.synchronize()
+    t_inv = time.perf_counter() - t0
+    out["invariant_only_tok_s"] = B * max_new / t_inv
+    out["fractions"] = {}
     for d in fractions:
-        n_f = max(1, int(round(d * B)))
-
-        def llm42():
-            fast()
-            cand = ids[:, :n_f].T.cpu().numpy()
-            res = []
-            for g in range(0, n_f, 8):
-                sl = list(range(g, min(n_f, g + 8)))
-                res.append(eng.verify(sl, ctx[sl], last[sl],
-                                      [list(map(int, cand[r])) for r in sl]))
-            return res
-
-        ms, res = timed(llm42)
-        commit = np.concatenate([r[1] for r in res])
-        rolled = int((commit < w).sum())
-        committed = (B - n_f) * w + int(commit.sum()) + rolled
+        b.restore_pages()
+        nf = int(round(d * B))
+        sch = scheduler.SelectiveScheduler(eng, fast, window=window)
+        for r in range(B):
+            sch.adopt(r, hist(r), r < nf, max_new)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        sch.run()
+        torch.cuda.synchronize()
+        t = time.perf_counter() - t0
+        st = sch.stats
         out["fractions"][str(d)] = {
-            "verified": n_f, "ms": ms,
-            "committed_tok_s": committed / (ms / 1e3),
-            "windows_rolled_back": rolled,
-            "mean_commit": float(commit.mean()),
-            "recomputed": int((w - commit - 1)[commit < w].sum())}
-        rearm(range(n_f))
+            "deterministic_requests": nf,
+            "tok_s": B * max_new / t,
+            "over_invariant_only": (B * max_new / t) /
+            out["invariant_only_tok_s"],
+            "fast_steps": st["fast_steps"], "verify_calls":
+            st["verify_calls"], "windows": st["windows"],
+            "rollbacks": st["rollbacks"],
+            "recompute_fraction": st["recomputed"] / max(1, st["committed"])}
+    b.restore_pages()
     return out
 
 

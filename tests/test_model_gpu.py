@@ -483,6 +483,55 @@ def test_verify_device_matches_host_and_replays(tiny, lib):
     assert lib.bi_device_status() == 0
 
 
+def test_llm42_selective_determinism(tiny, lib, orc):
+    """LLM-42 with a real non-invariant fast path (SelectiveScheduler over
+    FastPath: every GEMM through cuBLAS), half of the requests flagged
+    deterministic, their fast-path tokens perturbed now and then to force
+    rollbacks.  Every flagged request's output equals the invariant greedy
+    output token for token (all its tokens are verified; after a rollback
+    the verifier's token continues it); every verification's commits and
+    fix tokens equal the oracle's commit rule on the GPU's verified ids;
+    unflagged requests produce their full budget."""
+    from deterministic_invariant_bf16_gb300 import fastpath, scheduler, synth
+    shape = tiny[0]
+    rng = np.random.default_rng(4200)
+    R, max_new = 12, 40
+    prompts = [synth.token_ids(int(n), shape.vocab, rng)
+               for n in rng.integers(5, 20, size=R)]
+    flagged = [r % 2 == 0 for r in range(R)]
+    _, ref_toks = greedy_run(new_engine(tiny, page_seed=50), prompts,
+                             max_new, [list(range(R))])
+    eng = new_engine(tiny, page_seed=51, n_pages=220)
+    fast = fastpath.FastPath(eng, max_batch=R)
+    prng = np.random.default_rng(7)
+
+    def perturb(req, t):
+        return (t + 1 + req.slot) % shape.vocab if prng.uniform() < 0.06 \
+            else t
+
+    sch = scheduler.SelectiveScheduler(eng, fast, window=8, perturb=perturb)
+    sch.keep_logits = True
+    for r in range(R):
+        sch.add(r, prompts[r], flagged[r], max_new)
+    sch.run()
+    outs = sch.outputs()
+    for r in range(R):
+        assert len(outs[r]) == max_new
+        if flagged[r]:
+            assert outs[r] == ref_toks[r], r
+    st = sch.stats
+    assert st["rollbacks"] > 0 and st["verify_calls"] > 1
+    for slots, kv, last, wins, commit, fix, lg in sch.verify_log:
+        ver = orc.argmax(lg)
+        row = 0
+        for k_, w_, j_, f_ in zip(kv, wins, commit, fix):
+            j, _, fx, _ = orc.commit_rule(k_, w_, ver[row:row + len(w_)])
+            assert (j, fx) == (int(j_), int(f_))
+            row += len(w_)
+    assert lib.bi_device_status() == 0
+    eng.close()
+
+
 # ------------------------------------------ 2-layer 8B-shape model --
 
 def test_8b_shape_two_layer_model_decode_and_verify(lib, orc):
