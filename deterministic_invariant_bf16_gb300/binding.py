@@ -97,6 +97,7 @@ SIGNATURES = {
     "verify_commit_rollback_device": ([V, V, V, V, V, V, V, V, V, V, V, V,
                                        I, V, V, V, V], I),
     "bi_model_hidden": ([V, ctypes.POINTER(V)], I),
+    "bi_test_wait_timeout": ([L, V, V], I),
 }
 
 
@@ -446,3 +447,8 @@ def _view_bf16(addr, rows, cols):
             "shape": (rows, cols), "typestr": "<i2", "version": 3,
             "data": (addr, False), "strides": None}
     return torch.as_tensor(_Mem(), device="cuda").view(torch.bfloat16)
+
+
+def bi_test_wait_timeout(limit_ns, done, stream=None):
+    _check(lib().bi_test_wait_timeout(int(limit_ns), _p(done),
+                                      _stream(stream)))

@@ -3021,9 +3021,12 @@ extern "C" bi_status bi_paged_decode_attn(
 static __device__ __align__(256) uint8_t
     g_decode_noalloc_scratch[BI_DECODE_ATTN_NOALLOC_SCRATCH_BYTES];
 
-// Device address of the scratch array on the current device, looked up with
-// cudaGetSymbolAddress the first time the variant runs on that device.
-static bi_status noalloc_scratch(void **out) {
+// Device address of the scratch array on the current device.  Every call
+// made outside a stream capture looks it up again (cudaGetSymbolAddress, a
+// host-side lookup), so a device reset that reloads the module, and may move
+// the array, is followed; a call being captured reuses the address of the
+// device's last uncaptured call (and looks it up only if there was none).
+static bi_status noalloc_scratch(cudaStream_t s, void **out) {
     static std::mutex mu;
     static void *ptrs[64] = {nullptr};
     int dev = 0;
@@ -3031,8 +3034,12 @@ static bi_status noalloc_scratch(void **out) {
     if (st != BI_OK) return st;
     if (dev < 0 || dev >= 64)
         return bi_fail(BI_ERR_UNSUPPORTED, "noalloc: device %d", dev);
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    st = bi_cuda_check(cudaStreamIsCapturing(s, &cs),
+                       "noalloc: cudaStreamIsCapturing");
+    if (st != BI_OK) return st;
     std::lock_guard<std::mutex> lock(mu);
-    if (!ptrs[dev]) {
+    if (cs == cudaStreamCaptureStatusNone || !ptrs[dev]) {
         void *p = nullptr;
         st = bi_cuda_check(cudaGetSymbolAddress(&p, g_decode_noalloc_scratch),
                            "noalloc: cudaGetSymbolAddress");
@@ -3059,7 +3066,7 @@ extern "C" bi_status bi_paged_decode_attn_noalloc(
                        (int)BI_DECODE_ATTN_NOALLOC_SCRATCH_BYTES);
     BI_REQUIRE(Hkv > 0, "bi_paged_decode_attn_noalloc: Hkv=%d", Hkv);
     void *ws = nullptr;
-    bi_status st = noalloc_scratch(&ws);
+    bi_status st = noalloc_scratch(bi_stream(stream), &ws);
     if (st != BI_OK) return st;
     // The chunk kernel writes every partial the merge kernel reads, and the
     // item list is rebuilt by every call, so nothing left in the array by an

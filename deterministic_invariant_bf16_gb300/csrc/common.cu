@@ -161,3 +161,34 @@ bi_status bi_make_tmap_2d_bf16(CUtensorMap *map, const void *base,
                        (unsigned long long)row_stride_bytes);
     return BI_OK;
 }
+
+// Test aid for the bounded waits: one thread initialises an mbarrier that
+// expects one arrival, which never comes, and waits for its phase with
+// the library's bounded wait (mbar_wait_for, the loop mbar_wait runs with
+// the 2 s limit) and the given limit.  Nothing else touches the barrier, so
+// the wait runs out, BI_ERR_TIMEOUT goes to the status word and the kernel
+// returns: no copy, MMA or tensor memory is involved.
+__global__ void wait_probe_kernel(uint64_t limit_ns, int32_t *status,
+                                  int32_t *done) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_fence_init();
+        const bool ok = mbar_wait_for(&bar, 0, status, limit_ns);
+        *done = ok ? 1 : 2;
+    }
+}
+
+extern "C" bi_status bi_test_wait_timeout(int64_t limit_ns, int32_t *done,
+                                          void *stream) {
+    BI_REQUIRE(limit_ns >= 1000 && limit_ns <= 100000000,
+               "bi_test_wait_timeout: limit %lld ns outside [1 us, 100 ms]",
+               (long long)limit_ns);
+    BI_REQUIRE(done, "bi_test_wait_timeout: null pointer");
+    int32_t *st = bi_status_ptr();
+    if (!st) return bi_fail(BI_ERR_CUDA, "bi_test_wait_timeout: no status");
+    wait_probe_kernel<<<1, 32, 0, bi_stream(stream)>>>((uint64_t)limit_ns, st,
+                                                      done);
+    BI_LAUNCH_CHECK("wait probe launch");
+    return BI_OK;
+}

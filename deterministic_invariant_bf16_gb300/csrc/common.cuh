@@ -115,19 +115,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete.  Returns
-// false (and records BI_ERR_TIMEOUT) if it did not within the limit.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          int32_t *status) {
+// false (and records BI_ERR_TIMEOUT) if it did not within limit_ns.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity,
+                                              int32_t *status,
+                                              uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = bi_globaltimer();
     uint32_t n = 0;
     while (!mbar_try_wait(bar, parity)) {
-        if ((++n & 1023u) == 0 && bi_globaltimer() - t0 > BI_WAIT_LIMIT_NS) {
+        if ((++n & 1023u) == 0 && bi_globaltimer() - t0 > limit_ns) {
             bi_record_error(status, BI_ERR_TIMEOUT);
             return false;
         }
     }
     return true;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          int32_t *status) {
+    return mbar_wait_for(bar, parity, status, BI_WAIT_LIMIT_NS);
 }
 
 // -------------------------------------------------------------------- TMA --

@@ -65,6 +65,16 @@ const char *bi_last_error(void);
  * first error recorded since the previous call. */
 bi_status bi_device_status(int32_t *h_status, void *stream);
 
+/* Test aid for the bounded device waits (every mbarrier wait in the
+ * library gives up after 2 s, records BI_ERR_TIMEOUT and lets its kernel
+ * finish instead of hanging).  Launches one block whose thread waits, with
+ * the library's bounded wait and a limit of limit_ns (1 us .. 100 ms, else
+ * BI_ERR_INVALID_ARG), on a barrier nothing arrives at: the wait runs out,
+ * BI_ERR_TIMEOUT is recorded in the status word and the kernel returns.
+ * done: device int32, set to 2 when the wait ran out (1 if it completed).
+ * Touches no other state; later calls run normally. */
+bi_status bi_test_wait_timeout(int64_t limit_ns, int32_t *done, void *stream);
+
 /* ------------------------------------------------------------------ GEMM --
  * y = x W^T.  ybb.press section 2.2 (GEMM heuristics switch tile shape and
  * split-K with (M, N, K); split-K with atomicAdd is run-to-run
@@ -222,9 +232,11 @@ bi_status bi_paged_decode_attn(const bi_bf16 *q, const bi_bf16 *k_pool,
  *     the scratch size return BI_ERR_WORKSPACE_TOO_SMALL without launching
  *     (with D = 128 and Hq = 32: B * ceil(max_kv_len / 256) <= 992, e.g.
  *     62 rows of up to 4096 positions or 248 rows of up to 1024).
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress); make that first call before any stream
- *     capture.  No call allocates or frees device memory.
+ *   - Every call made outside a stream capture looks up the array's
+ *     device address (cudaGetSymbolAddress), so the variant keeps working
+ *     after a cudaDeviceReset; a captured call reuses the address of the
+ *     device's last uncaptured call, so make one call before capturing.
+ *     No call allocates or frees device memory.
  *   - Every call uses the same array.  Nothing in it needs to start at zero
  *     (each call writes every partial it reads), but calls whose kernels
  *     overlap on the GPU (different streams, no ordering between them) race

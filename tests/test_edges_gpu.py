@@ -132,3 +132,32 @@ def test_bad_token_id_is_recorded(bi):
     assert bi.bi_device_status() == 5
     assert torch.count_nonzero(h[1]) == 0
     assert torch.equal(h[0], E[3]) and torch.equal(h[2], E[7])
+
+
+def test_bounded_wait_runs_out_and_the_library_recovers(bi):
+    """A device wait that nothing completes gives up after its limit (here
+    5 ms, the same wait loop the kernels run with 2 s), records
+    BI_ERR_TIMEOUT in the status word and lets its kernel return; the
+    context stays usable and the next ordinary call gives the same bits as
+    before."""
+    g = torch.Generator(device="cuda").manual_seed(5)
+    x = torch.randn(64, 512, generator=g, device="cuda").to(torch.bfloat16)
+    w = torch.randn(384, 512, generator=g, device="cuda").to(torch.bfloat16)
+    S = bi.bi_gemm_splits(384, 512)
+    before = torch.empty(S, 64, 384, dtype=torch.float32, device="cuda")
+    bi.bi_gemm(x, w, before, bi.OUT_PARTIALS)
+    torch.cuda.synchronize()
+    assert bi.bi_device_status() == 0
+    done = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bi.bi_test_wait_timeout(5_000_000, done)
+    torch.cuda.synchronize()
+    assert done.item() == 2
+    assert bi.bi_device_status() == 6      # BI_ERR_TIMEOUT, read and cleared
+    assert bi.bi_device_status() == 0
+    after = torch.empty_like(before)
+    bi.bi_gemm(x, w, after, bi.OUT_PARTIALS)
+    torch.cuda.synchronize()
+    assert bi.bi_device_status() == 0
+    assert torch.equal(before.view(torch.int32), after.view(torch.int32))
+    with pytest.raises(bi.BiError, match="INVALID"):
+        bi.bi_test_wait_timeout(10**9, done)

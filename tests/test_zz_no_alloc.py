@@ -82,6 +82,32 @@ def test_noalloc_matches_workspace_variant_on_two_calls(bi):
         assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), i
 
 
+def test_noalloc_whole_row_items_match_workspace_variant(bi):
+    """At 8 or more (row, KV head) items per SM the decode kernel takes
+    whole rows and merges their chunks in registers (the form 8B-shape
+    batches of 160 rows and more use); with contexts of at most 1024
+    positions such a batch fits the fixed scratch.  Same bits as with a
+    caller workspace, on two calls in a row."""
+    Hq, Hkv, D = 32, 8, 128
+    B = 8 * torch.cuda.get_device_properties(0).multi_processor_count // Hkv
+    B = max(B, 160)
+    for i in range(2):
+        rng = np.random.default_rng(300 + i)
+        lens = [int(x) for x in rng.integers(1, 1025, size=B)]
+        q, kp, vp, pt, rows, kvl = _paged_case(lens, Hq, Hkv, D, 200 + i)
+        max_kv = max(lens)
+        assert bi.bi_decode_attn_workspace_size(B, Hq, D, max_kv) <= \
+            bi.NOALLOC_SCRATCH_BYTES
+        scale = 1.0 / math.sqrt(D)
+        ref = _with_workspace(bi, q, kp, vp, pt, rows, kvl, max_kv, scale)
+        out = torch.empty_like(q)
+        bi.bi_paged_decode_attn_noalloc(q, kp, vp, pt, rows, kvl, max_kv,
+                                        scale, out)
+        torch.cuda.synchronize()
+        assert bi.bi_device_status() == 0
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), i
+
+
 def test_noalloc_rejects_oversized_calls(bi):
     lib = bi.lib()
     # 64 rows of 4096 positions need 64 * 32 * 16 * 528 bytes > 16 MiB
