@@ -68,6 +68,13 @@ def parse():
                     help="instead of the step benchmark: decode tok/s over "
                          "batch sizes 1..256 and invariant prefill tok/s on "
                          "a sample of long prompts (one JSON line)")
+    ap.add_argument("--attn-probe", action="store_true",
+                    help="instead of the step benchmark: the attention "
+                         "entry points alone on synthetic pages (a 256-row "
+                         "decode batch, one 2048-row prompt piece at "
+                         "positions 2048..4095, a verify-like batch of 8 "
+                         "windows of 32), each timed with CUDA events; one "
+                         "launch of each is what an ncu capture targets")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the decode iterations one call at a time "
                          "instead of replaying them as one CUDA graph")
@@ -1039,6 +1046,96 @@ def long_prompt_stress(b, fractions=(0.02, 0.10, 0.50, 1.0), piece=2048):
     return res
 
 
+def attn_probe(args):
+    """The attention entry points alone, through the C ABI, on synthetic
+    pages in random physical order (K, V ~ N(0, 1) bf16): decode at the
+    step workload's batch (256 rows, lognormal contexts median 512), one
+    prompt piece (2048 tokens at positions 2048..4095 of one request) with
+    a workspace (the group kernel) and without (one CTA per tile), a
+    verify-like batch (8 windows of 32 at lognormal contexts) with and
+    without a workspace.  Prints one JSON line of per-call microseconds."""
+    import torch
+    from deterministic_invariant_bf16_gb300 import binding as bi
+    from deterministic_invariant_bf16_gb300 import build, synth
+    build.build()
+    bi.lib()
+    dev = "cuda"
+    Hq, Hkv, D = 32, 8, 128
+    scale = 1 / math.sqrt(D)
+    rng = np.random.default_rng(5)
+
+    def pools(lens):
+        table, n_pages = synth.paged_layout(lens, 16, rng)
+        g = torch.Generator(device=dev).manual_seed(1)
+        kp = torch.randn(n_pages, Hkv, 16, D, generator=g,
+                         device=dev).to(torch.bfloat16)
+        vp = torch.randn(n_pages, Hkv, 16, D, generator=g,
+                         device=dev).to(torch.bfloat16)
+        return kp, vp, torch.from_numpy(table).to(dev)
+
+    def timeit(fn, reps):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps * 1e3
+
+    def ws(nbytes):
+        return torch.empty(nbytes // 4 + 64, dtype=torch.float32, device=dev)
+
+    res = {}
+    B = 256
+    lens = synth.lognormal_lengths(B, 512, 1.0, 16, 4096, rng)
+    kd, vd, td = pools(lens)
+    qd = torch.randn(B, Hq, D, device=dev).to(torch.bfloat16)
+    rows = torch.arange(B, dtype=torch.int32, device=dev)
+    kvl = torch.from_numpy(lens.astype(np.int32)).to(dev)
+    mkv = int(lens.max())
+    wd = ws(bi.bi_decode_attn_workspace_size(B, Hq, D, mkv))
+    od = torch.empty_like(qd)
+    res["decode_us"] = timeit(lambda: bi.bi_paged_decode_attn(
+        qd, kd, vd, td, rows, kvl, mkv, scale, od, wd), 10)
+    Tq, p0 = 2048, 2048
+    kp, vp, tp = pools(np.array([p0 + Tq]))
+    qp = torch.randn(Tq, Hq, D, device=dev).to(torch.bfloat16)
+    cu = torch.tensor([0, Tq], dtype=torch.int32, device=dev)
+    sr = torch.zeros(1, dtype=torch.int32, device=dev)
+    pos = torch.arange(p0, p0 + Tq, dtype=torch.int32, device=dev)
+    wp = ws(bi.bi_prefill_attn_workspace_size(Tq, 1, Hq, Hkv))
+    op = torch.empty_like(qp)
+    res["prefill_piece_ws_us"] = timeit(lambda: bi.bi_prefill_attn_ws(
+        qp, cu, sr, pos, Tq, p0 + Tq, kp, vp, tp, scale, op, wp), 3)
+    res["prefill_piece_no_ws_us"] = timeit(lambda: bi.bi_prefill_attn(
+        qp, cu, sr, pos, Tq, p0 + Tq, kp, vp, tp, scale, op), 3)
+    fl = sum(p0 + i + 1 for i in range(Tq)) * Hq * D * 4
+    res["prefill_piece_ws_TFLOPs"] = fl / (res["prefill_piece_ws_us"] *
+                                           1e-6) / 1e12
+    W = 32
+    vl = synth.lognormal_lengths(8, 512, 1.0, 16, 2048, rng)
+    kv, vv, tv = pools(vl + W)
+    qv = torch.randn(256, Hq, D, device=dev).to(torch.bfloat16)
+    cuv = torch.tensor([0] + list(np.cumsum([W] * 8)), dtype=torch.int32,
+                       device=dev)
+    srv = torch.arange(8, dtype=torch.int32, device=dev)
+    posv = torch.from_numpy(np.concatenate(
+        [np.arange(v, v + W) for v in vl]).astype(np.int32)).to(dev)
+    wv = ws(bi.bi_prefill_attn_workspace_size(256, 8, Hq, Hkv))
+    ov = torch.empty_like(qv)
+    res["verify_ws_us"] = timeit(lambda: bi.bi_prefill_attn_ws(
+        qv, cuv, srv, posv, W, int(vl.max()) + W, kv, vv, tv, scale, ov, wv),
+        10)
+    res["verify_no_ws_us"] = timeit(lambda: bi.bi_prefill_attn(
+        qv, cuv, srv, posv, W, int(vl.max()) + W, kv, vv, tv, scale, ov), 10)
+    res["device_status"] = bi.bi_device_status()
+    print(json.dumps({"attn_probe": res}), flush=True)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -1496,6 +1593,8 @@ def main():
         run_reference(args)
     elif args.report:
         run_report(args)
+    elif args.attn_probe:
+        attn_probe(args)
     else:
         run_ours(args)
 
