@@ -883,7 +883,8 @@ __global__ void __launch_bounds__(cthreads<D>())
 //     and 128-255; M = 128 keys, N = 16 rows), each over the dims in
 //     ascending 16-steps, fp32 in tensor memory;
 //   s = S^T * scale, -inf past the row's visible length; m = block maximum;
-//   p = exp_s(s - m) (0 when masked); l = per-warp xor-tree sums over 32 keys
+//   p = p_of(raw score, rn(scale log2 e), rn(m log2 e)) = 2^(s log2 e -
+//   m log2 e) (0 when masked); l = per-warp xor-tree sums over 32 keys
 //   (16, 8, 4, 2, 1), then (((w0 + w1) + w2) .. + w7) over the 8 warps;
 //   O^T[dim][row] = sum_key V[key][dim] bf16(p)[row][key]: one MMA chain
 //   (M = 128 dims, N = 16 rows) over the keys in ascending 16-steps, with V
@@ -892,13 +893,24 @@ __global__ void __launch_bounds__(cthreads<D>())
 // (0 * NaN would poison the sum); K rows there are never used (masked).
 namespace tca {
 
-// exp of a chunk score minus the chunk maximum (argument <= 0): the
-// hardware exponential (__expf: one multiply and one ex2, a few fp32 ulp,
-// far below the bf16 rounding P gets next).  Every head_dim-128 path
-// (decode, prefill, verify) takes p from this one function, so they agree
-// bit for bit; the full-accuracy expf cost about a third of the softmax's
-// instructions.
-__device__ __forceinline__ float exp_s(float x) { return __expf(x); }
+// p = e^(s scale - mu) for a raw score s (QK product) of a chunk whose
+// scaled maximum is mu, by the change of base e^x = 2^(x log2 e):
+// 2^(s c1 - mu2) with c1 = rn(scale log2 e) and mu2 = rn(mu log2 e), the
+// argument from one fma, then the PTX base-2 exponential ex2.approx.ftz
+// (relative error about 2^-22; results below 2^-126 flush to zero).  The
+// argument's error is a few fp32 ulp of |s scale|, far below the bf16
+// rounding P gets next.  Every head_dim-128 path (decode, prefill, verify)
+// takes p from this one function, so they agree bit for bit; it is two
+// instructions per score.
+constexpr float LOG2E = 1.4426950408889634f;
+__device__ __forceinline__ float exp2_approx(float y) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
+    return r;
+}
+__device__ __forceinline__ float p_of(float s, float c1, float mu2) {
+    return exp2_approx(__fmaf_rn(s, c1, -mu2));
+}
 
 constexpr int SW = 8;                         // softmax warps, thread = key
 constexpr int STHREADS = SW * 32;
@@ -963,15 +975,14 @@ __device__ __forceinline__ void softmax(uint32_t s_tmem, float scale,
                                         float *red, float (&m)[16]) {
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int key = (w >> 2) * 128 + (w & 3) * 32 + lane;
-    float v[16], x[NR];
+    const float c1 = __fmul_rn(scale, LOG2E);
+    float v[16], x[NR];   // v: raw scores
     tmem_ld_16cols(s_tmem + ((uint32_t)((w & 3) * 32) << 16) + (w >> 2) * 16,
                    v);
 #pragma unroll
     for (int r = 0; r < NR; ++r) {
-        float s = __fmul_rn(v[r], scale);
-        s = key < len[r] ? s : -INFINITY;
-        v[r] = s;
-        x[r] = s;
+        const float s = __fmul_rn(v[r], scale);
+        x[r] = key < len[r] ? s : -INFINITY;
     }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1)
@@ -989,7 +1000,8 @@ __device__ __forceinline__ void softmax(uint32_t s_tmem, float scale,
         for (int k = 1; k < SW; ++k) mm = fmaxf(mm, red[k * 16 + r]);
         m[r] = mm;
         const float mu = mm == -INFINITY ? 0.f : mm;
-        const float p = key < len[r] ? exp_s(__fsub_rn(v[r], mu)) : 0.f;
+        const float p =
+            key < len[r] ? p_of(v[r], c1, __fmul_rn(mu, LOG2E)) : 0.f;
         v[r] = p;
         x[r] = p;
         asm volatile("st.shared.b16 [%0], %1;" ::"r"(ptile + poff(r, key)),
@@ -2276,159 +2288,102 @@ __global__ void __launch_bounds__(tca::PRE_THREADS, 1)
     }
 }
 
-// Prefill / verify on the tensor cores (head_dim 128) with one K and V chunk
-// shared by a group of query tiles.  An item is (group, KV head g): a group
-// is up to GT consecutive 16-row tiles of one segment (16 / G tokens x G
-// heads each), i.e. up to 16 GT / G consecutive tokens, as build_tiles_kernel
-// lists them (QPT = 16 GT / G tokens per entry).  Per chunk the CTA loads K
-// and V once and runs, for each tile whose context reaches the chunk, the
-// per-tile computation of the other kernels: issue_qk (N = 16 rows), the
-// softmax of softmax<16>, issue_pv, then the merge into the tile's running
-// (m, l, o) in chunk order with merge_scalars / merge_value.  So every row
-// gets the bits of decode and of the per-tile prefill kernel, while a
-// chunk's K and V are read once per group instead of once per tile.
-//   warps 0-3, 4-7  two teams; team q takes the tiles i with i % 2 = q,
-//              one (tile, chunk) unit after the other, so two units are in
-//              flight and every tile's chunks are merged in order by one
-//              team.  A team issues its own MMAs (lane 0 of its first warp),
-//              so no unit waits on another warp: per unit, the scores to a
-//              shared-memory buffer (softmax_team, thread = key), then the
-//              next unit's QK MMAs into the team's S, the previous unit's
-//              PV products merged into the tile's running O in tensor
-//              memory (thread = dim) or written out after the tile's last
-//              chunk, the softmax (softmax_team_b, thread = (row, 32-key
-//              group)), the row factors by one thread per row
-//              (merge_scalars), then this unit's PV MMAs;
-//   warp 8     lanes 0-15 issue the TMA page boxes of a chunk (K and V as
-//              the other kernels load them): K of chunk c + 1 once each team
-//              with tiles in chunk c has committed its last QK MMAs of it
-//              (k_free), V once their last PV MMAs are committed (v_free),
-//              then zeroes the V rows past the group's last visible
-//              position (v_ready).
-// Tensor memory (256 columns): S^T of each team's unit (32 columns), each
-// team's PV products (16), the running O of each tile of the group (16).
-// The persistent CTAs walk items in list order (most chunks first);
-// entries the builder marked invalid (no request, or a context out of
-// range) get zero outputs.  Waits are bounded; after one runs out every
-// later wait of the CTA returns at once and the CTA finishes its walk
-// without waiting (garbage out, BI_ERR_TIMEOUT recorded), so no barrier is
-// left unmatched.
+// ------------------------------------------------- prefill, row per thread --
+// Attention of query tiles of 128 rows (128 / G consecutive tokens x the G
+// query heads of KV head g; row r = token r / G, head r % G) with one thread
+// per row.  The tensor core computes the chunk's scores untransposed,
+// S[row][key] = Q K^T (M = 128 rows, N = 256 keys, K = 128 dims in 8 steps
+// of 16), and the chunk's values O[row][dim] = P V (M = 128 rows, N = 128
+// dims, K = 256 keys in 16 steps).  The other kernels compute the same
+// elements as S^T = K Q^T and O^T = V^T P^T over 16-row tiles; the tensor
+// core's result for an element does not depend on N nor on which operand
+// holds the row (checked bit for bit on GB300 for both products over
+// N = 16 .. 256), so each element keeps its bits.  Thread r then runs the
+// decode softmax of its row alone: the exact maximum of the scaled, masked
+// scores (for scale > 0 taken on the raw scores and scaled once: rounding is
+// monotone, so the maximum is the same number), p = p_of(s, c1, mu2),
+// bf16(p) into the P tile, the row sum as the xor tree over each 32-key
+// group (16, 8, 4, 2, 1) and the eight groups in order, then merge_scalars /
+// merge_value against the row's running (M, L, O) in chunk order and
+// bf16(O / L) at the end.  No value crosses threads, so no shuffle, shared
+// score buffer or barrier sits between a row's operations.
+//   warps 0-3   rows 32 w + lane (TMEM lane quarter w); per chunk n: the
+//               maximum (pass 1), the merge of chunk n - 1 into the running
+//               O held in registers (its values arrive while pass 1 runs),
+//               the exponentials, P and the row sum (pass 2);
+//   warp 4      one lane issues the MMAs: S of chunk n + 1 into the other
+//               tensor-memory slot once the merge of chunk n - 1 has read
+//               it (so it runs under pass 2 of chunk n), then the values of
+//               chunk n into the first 128 columns of chunk n's own slot
+//               (its scores are consumed) once P and V are in;
+//   warp 5      the query tile (once per item) and K of each chunk by TMA;
+//   warp 6      V of each chunk by TMA, then zeroes the rows past the last
+//               visible position in the chunk's last page (0 * NaN would
+//               poison the sums).
+// Tensor memory (512 columns): two slots of 256, chunk n in slot n % 2 (S,
+// then its values).  Items (tile, KV head) are walked by persistent CTAs in
+// list order (most chunks first); chunks are counted over the CTA's walk.
+// Waits are bounded as in the other kernels, and each role waits (bounded)
+// for its own copies and products in flight before the CTA leaves.
 namespace tca {
-constexpr int GT_MAX = 8;
-struct GrpL {
-    static constexpr int TB = CHUNK * 128 * 2;            // K or V tile
-    static constexpr int QB = 16 * 128 * 2;               // one query tile
-    static constexpr int SB = 16 * CHUNK * 4;             // scores, fp32
-    static constexpr int K = 0, V = TB, Q = 2 * TB;
-    static constexpr int P = Q + GT_MAX * QB;             // a P tile per team
-    static constexpr int S = P + 2 * P_TILE;              // a score buffer each
-    static constexpr int ML = S + 2 * SB;                 // [GT_MAX][16] (M, L)
-    static constexpr int AB = ML + GT_MAX * 16 * 2 * 4;   // [2][16] float4
-    static constexpr int PROW = AB + 2 * 16 * 16;         // [GT_MAX][16]
-    static constexpr int CI = PROW + GT_MAX * 16 * 4;     // [GT_MAX]
-    static constexpr int BAR = CI + GT_MAX * 4 + 32;
-    // k_full, v_full, v_ready, then per team s_full, o_full, k_free,
-    // v_free, then the TMEM address and the failure flag
-    static constexpr int BYTES = BAR + 12 * 8 + 16;
+struct RowL {
+    static constexpr int TB = CHUNK * 128 * 2;   // K or V tile, 64 KB
+    static constexpr int QH = 128 * 128;         // a 64-dim half of Q, 16 KB
+    static constexpr int PG = 128 * 128;         // a 64-key group of P, 16 KB
+    static constexpr int Q = 0, K = 2 * QH, V = K + TB, P = V + TB;
+    static constexpr int BAR = P + 4 * PG;
+    // k_full, k_free, v_full, v_ready, v_free, p_full, o_full, done,
+    // s_full[2], slot_free[2]; then the TMEM address and the failure flag
+    static constexpr int NBAR = 12;
+    static constexpr int BYTES = BAR + NBAR * 8 + 8;
     static constexpr int ALLOC = BYTES + 1024;
 };
-constexpr int GRP_THREADS = STHREADS + 32;
-constexpr uint32_t GRP_TMEM = 256;
-constexpr uint32_t T_S = 0, T_OC = 64, T_ORUN = 128;
+constexpr int ROW_THREADS = 128 + 3 * 32;
+constexpr uint32_t ROW_TMEM = 512;
+constexpr uint32_t IDESC_S = make_idesc_bf16(128, 256);
+constexpr uint32_t IDESC_O = make_idesc_bf16(128, 128) | (1u << 16);
 
-// Word of (row, key) in a score buffer [16][256] fp32: the eight 16-byte
-// units of each 32-key group g in the order u ^ g, so that the float4 reads
-// of softmax_team (eight groups of one row per quarter-warp) hit eight
-// distinct bank groups.
-__device__ __forceinline__ int sbw(int r, int key) {
-    const int u = key >> 2;
-    return r * CHUNK + ((u ^ ((u >> 3) & 7)) << 2) + (key & 3);
-}
-
-// Team barrier (named barrier 2 + team, 128 threads).
-__device__ __forceinline__ void sync_team(int team) {
-    asm volatile("bar.sync %0, 128;" ::"r"(2 + team) : "memory");
-}
-
-// The softmax of softmax<16> for one chunk of a 16-row tile, bit for bit, by
-// one team of four warps (thread t of the team, warp wq = t / 32): the same
-// scaled and masked scores, the same exact row maximum (fmaxf), p =
-// exp_s(s - m) with the same masking, the same bf16(p) in the P tile and the
-// row sum in the same order (lane 0's xor tree over each 32-key group, then
-// the eight groups in order).
-//   softmax_team (phase A), thread <-> keys 32 wq + lane and 128 + 32 wq +
-//   lane: scores from S^T in TMEM (lane quarter wq), scaled and masked, to
-//   the buffer; ends with the team barrier (S fully read, buffer written).
-//   softmax_team_b (phase B), thread <-> (row r = 4 wq + lane / 8, group
-//   g = lane % 8): keys 32 g .. 32 g + 31 of row r.  The maximum is exact
-//   (any order); the group's xor tree is thread-local; the groups are added
-//   in order over the row's 8 lanes.  P leaves as four 16-byte units per
-//   thread.  Every thread of row r returns its m and l.
-// prow[r] + 1 - 256 c = keys of chunk c visible to row r.
-__device__ __forceinline__ void softmax_team(uint32_t s_tmem, float scale,
-                                             const int *prow, int c, float *sb,
-                                             uint32_t ptile, int team) {
-    const int wq = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
-    float v[32];
-    tmem_ld_32cols(s_tmem + ((uint32_t)(wq * 32) << 16), v);
-    const int k0 = 32 * wq + lane, k1 = k0 + 128;
+// S = Q K^T of one chunk into TMEM columns d .. d + 255 (lane = row).
+__device__ __forceinline__ void issue_rows_s(uint32_t d, uint32_t qt,
+                                             uint32_t kt) {
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-        const int len = prow[r] + 1 - c * CHUNK;
-        const float s0 = __fmul_rn(v[r], scale);
-        const float s1 = __fmul_rn(v[16 + r], scale);
-        sb[sbw(r, k0)] = k0 < len ? s0 : -INFINITY;
-        sb[sbw(r, k1)] = k1 < len ? s1 : -INFINITY;
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t a = qt + (kk >> 2) * RowL::QH + (kk & 3) * 32;
+        const uint32_t b = kt + (kk >> 2) * (CHUNK * 128) + (kk & 3) * 32;
+        tc_mma_bf16(d, make_sw128_desc(a), make_sw128_desc(b), IDESC_S,
+                    kk > 0 ? 1u : 0u);
     }
-    tc_fence_before();
-    sync_team(team);
 }
 
-__device__ __forceinline__ void softmax_team_b(float scale, const int *prow,
-                                               int c, const float *sb,
-                                               uint32_t ptile, float &m_out,
-                                               float &l_out) {
-    const int wq = (threadIdx.x >> 5) & 3, lane = threadIdx.x & 31;
-    const int r = 4 * wq + (lane >> 3), g = lane & 7;
-    const int k0 = 32 * g;
-    float x[32];
+// O = P V of one chunk into TMEM columns d .. d + 127 (lane = row); V read
+// in place as the MN-major operand (its two 64-dim halves are the atoms).
+__device__ __forceinline__ void issue_rows_o(uint32_t d, uint32_t pt,
+                                             uint32_t vt) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const float4 f =
-            *reinterpret_cast<const float4 *>(sb + sbw(r, k0 + 4 * e));
-        x[4 * e + 0] = f.x;
-        x[4 * e + 1] = f.y;
-        x[4 * e + 2] = f.z;
-        x[4 * e + 3] = f.w;
+    for (int kk = 0; kk < CHUNK / 16; ++kk) {
+        const uint32_t a = pt + (kk >> 2) * RowL::PG + (kk & 3) * 32;
+        const uint32_t b = vt + kk * 2048;
+        tc_mma_bf16(d, make_sw128_desc(a),
+                    make_sw128_desc_mn(b, CHUNK * 128, 1024), IDESC_O,
+                    kk > 0 ? 1u : 0u);
     }
-    // exact maximum: a tree over the 32 values, then 8 lanes
-    float mm[16];
+}
+
+// Exact maximum of 32 values (any order gives the same number).
+__device__ __forceinline__ float max32(const float *v) {
+    float m[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) mm[j] = fmaxf(x[j], x[j + 16]);
+    for (int j = 0; j < 16; ++j) m[j] = fmaxf(v[j], v[j + 16]);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) mm[j] = fmaxf(mm[j], mm[j + 8]);
+    for (int j = 0; j < 8; ++j) m[j] = fmaxf(m[j], m[j + 8]);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) mm[j] = fmaxf(mm[j], mm[j + 4]);
-    float mx = fmaxf(fmaxf(mm[0], mm[2]), fmaxf(mm[1], mm[3]));
-#pragma unroll
-    for (int o = 4; o >= 1; o >>= 1)
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    const float mu = mx == -INFINITY ? 0.f : mx;
-    const int len = prow[r] + 1 - c * CHUNK;
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-        x[j] = k0 + j < len ? exp_s(__fsub_rn(x[j], mu)) : 0.f;
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                         ptile + poff(r, k0 + 8 * e)),
-                     "r"(pack_bf16x2(x[8 * e + 0], x[8 * e + 1])),
-                     "r"(pack_bf16x2(x[8 * e + 2], x[8 * e + 3])),
-                     "r"(pack_bf16x2(x[8 * e + 4], x[8 * e + 5])),
-                     "r"(pack_bf16x2(x[8 * e + 6], x[8 * e + 7]))
-                     : "memory");
-    // lane 0's xor tree over the group's keys i = 0..31: levels 16, 8, 4,
-    // 2, 1 pair i with i + 16, i + 8, ...
+    for (int j = 0; j < 4; ++j) m[j] = fmaxf(m[j], m[j + 4]);
+    return fmaxf(fmaxf(m[0], m[2]), fmaxf(m[1], m[3]));
+}
+
+// The decode path's sum of one 32-key group: lane 0's xor tree, levels 16,
+// 8, 4, 2, 1 pairing key i with i + 16, i + 8, ...
+__device__ __forceinline__ float xor_tree32(const float *x) {
     float a[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) a[i] = __fadd_rn(x[i], x[i + 16]);
@@ -2438,53 +2393,34 @@ __device__ __forceinline__ void softmax_team_b(float scale, const int *prow,
     for (int i = 0; i < 4; ++i) a[i] = __fadd_rn(a[i], a[i + 4]);
 #pragma unroll
     for (int i = 0; i < 2; ++i) a[i] = __fadd_rn(a[i], a[i + 2]);
-    const float W = __fadd_rn(a[0], a[1]);
-    const int rb = lane & 24;
-    float w8[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) w8[k] = __shfl_sync(0xffffffffu, W, rb + k);
-    float l = w8[0];
-#pragma unroll
-    for (int k = 1; k < 8; ++k) l = __fadd_rn(l, w8[k]);
-    m_out = mx;
-    l_out = l;
+    return __fadd_rn(a[0], a[1]);
 }
 }  // namespace tca
 
-__global__ void __launch_bounds__(tca::GRP_THREADS, 1)
-    attn_group_kernel(const __grid_constant__ CUtensorMap kmap,
-                      const __grid_constant__ CUtensorMap vmap,
-                      const uint16_t *__restrict__ q,
-                      const int4 *__restrict__ list,
-                      const int32_t *__restrict__ cnt,
-                      const int32_t *__restrict__ pos,
-                      const int32_t *__restrict__ page_table, int max_pages,
-                      int n_pages, int Hq, int Hkv, int G, int GT,
-                      float scale, uint16_t *__restrict__ out,
-                      int32_t *status) {
+__global__ void __launch_bounds__(tca::ROW_THREADS, 1)
+    attn_rows_kernel(const __grid_constant__ CUtensorMap kmap,
+                     const __grid_constant__ CUtensorMap vmap,
+                     const __grid_constant__ CUtensorMap qmap,
+                     const int4 *__restrict__ list,
+                     const int32_t *__restrict__ cnt,
+                     const int32_t *__restrict__ page_table, int max_pages,
+                     int n_pages, int Hq, int Hkv, int G, float scale,
+                     uint16_t *__restrict__ out, int32_t *status) {
     using namespace tca;
     constexpr int D = 128;
-    constexpr int NCH = D / 8;
     constexpr int PAGE_BYTES = 16 * 64 * 2;   // one box: 16 rows x 64 dims
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t base = smem_u32(smem);
-    const uint32_t ktile = base + GrpL::K, vtile = base + GrpL::V;
-    const uint32_t qtile = base + GrpL::Q, ptile = base + GrpL::P;
-    float *sbuf = reinterpret_cast<float *>(smem + GrpL::S);
-    float *mls = reinterpret_cast<float *>(smem + GrpL::ML);
-    float4 *abs_ = reinterpret_cast<float4 *>(smem + GrpL::AB);
-    int *s_prow = reinterpret_cast<int *>(smem + GrpL::PROW);
-    int *s_ci = reinterpret_cast<int *>(smem + GrpL::CI);
-    uint64_t *k_full = reinterpret_cast<uint64_t *>(smem + GrpL::BAR);
-    uint64_t *v_full = k_full + 1, *v_ready = k_full + 2;
-    uint64_t *s_full = k_full + 3, *o_full = k_full + 5;
-    uint64_t *k_free = k_full + 7, *v_free = k_full + 9;
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(k_full + 11);
-    volatile int *fail = reinterpret_cast<volatile int *>(k_full + 11) + 1;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + RowL::BAR);
+    uint64_t *k_full = bars, *k_free = bars + 1, *v_full = bars + 2,
+             *v_ready = bars + 3, *v_free = bars + 4, *p_full = bars + 5,
+             *o_full = bars + 6, *done = bars + 7, *s_full = bars + 8,
+             *slot_free = bars + 10;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(bars + RowL::NBAR);
+    volatile int *fail = reinterpret_cast<volatile int *>(tslot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int QPT = 16 / G;
     const int n_valid = cnt[0], n_all = cnt[1];
     const int items = n_valid * Hkv;
 
@@ -2508,85 +2444,49 @@ __global__ void __launch_bounds__(tca::GRP_THREADS, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(k_full, 1);
+        mbar_init(k_free, 1);
         mbar_init(v_full, 1);
         mbar_init(v_ready, 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&o_full[i], 1);
-            mbar_init(&k_free[i], 1);
-            mbar_init(&v_free[i], 1);
+        mbar_init(v_free, 1);
+        mbar_init(p_full, 4);
+        mbar_init(o_full, 1);
+        mbar_init(done, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&s_full[b], 1);
+            mbar_init(&slot_free[b], 4);
         }
         mbar_fence_init();
         *fail = 0;
     }
-    if (warp == SW) tmem_alloc(tslot, GRP_TMEM);
+    if (warp == 4) tmem_alloc(tslot, ROW_TMEM);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    if (warp == SW && lane == 0) {
-        tma_prefetch_desc(&kmap);
-        tma_prefetch_desc(&vmap);
-    }
 
-    // over all items so far: units done by each team, chunks done, and the
-    // chunks in which each team had units (the phases of k_free / v_free)
-    int nq[2] = {0, 0}, nc = 0, fq[2] = {0, 0};
-    for (int it = blockIdx.x; it < items; it += gridDim.x) {
-        const int4 e = list[it / Hkv];
-        const int g = it % Hkv;
-        const int t0 = e.x, L = e.y, ntok = e.z, req = e.w;
-        const int nt = min(GT, (ntok + QPT - 1) / QPT);
-        const int C = (L + CHUNK - 1) / CHUNK;
-        __syncthreads();  // the previous item is finished by every role
-        for (int idx = threadIdx.x; idx < nt * 16; idx += GRP_THREADS) {
-            const int tk = (idx >> 4) * QPT + (idx & 15) / G;
-            s_prow[idx] = tk < ntok ? pos[t0 + tk] : -1;
+    if (warp >= 5) {
+        // ------------------------------------------------ K and V loads --
+        const bool is_k = warp == 5;
+        if (lane == 0) {
+            tma_prefetch_desc(is_k ? &kmap : &vmap);
+            if (is_k) tma_prefetch_desc(&qmap);
         }
-        // query tiles: row r of tile i = (token i * QPT + r / G, head r % G)
-        for (int idx = threadIdx.x; idx < nt * 16 * NCH; idx += GRP_THREADS) {
-            const int i = idx / (16 * NCH), r = (idx / NCH) % 16,
-                      ch = idx % NCH;
-            const int tk = i * QPT + r / G, hh = r % G;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (tk < ntok)
-                v = *reinterpret_cast<const uint4 *>(
-                    q + ((int64_t)(t0 + tk) * Hq + g * G + hh) * D + ch * 8);
-            *reinterpret_cast<uint4 *>(smem + GrpL::Q + i * GrpL::QB +
-                                       toff<D, 16>(r, ch)) = v;
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (threadIdx.x < nt) {
-            int last = -1;
-            for (int r = 0; r < 16; ++r)
-                last = max(last, s_prow[threadIdx.x * 16 + r]);
-            s_ci[threadIdx.x] = (last + 1 + CHUNK - 1) / CHUNK;
-        }
-        __syncthreads();
-        // first tile whose context reaches chunk c (tile contexts grow with
-        // the tile index: a segment's positions are consecutive); team t's
-        // tiles in chunk c are first_t(c, t), + 2, ... < nt, so a team's
-        // chunks form a prefix 0 .. C_t - 1
-        auto first_tile = [&](int c) {
-            int i = 0;
-            while (i < nt - 1 && s_ci[i] <= c) ++i;
-            return i;
-        };
-        auto first_t = [&](int c, int t) {
-            const int i0 = first_tile(c);
-            return i0 + ((i0 & 1) != t);
-        };
-        const int32_t *pt_row = page_table + (int64_t)req * max_pages;
-
-        if (warp == SW) {
-            // ---------------------------------------------------- loads --
-            // K of chunk c + 1 once every team with tiles in chunk c has
-            // committed its last scores of it (k_free), V likewise after the
-            // last PV products (v_free); V rows past the group's last
-            // visible position in a chunk's last page are then zeroed
-            // (0 * NaN would poison the PV sums) before v_ready.
-            auto load = [&](int c, bool is_k) {
+        uint64_t *full = is_k ? k_full : v_full;
+        uint64_t *freed = is_k ? k_free : v_free;
+        const CUtensorMap *map = is_k ? &kmap : &vmap;
+        uint8_t *tile = smem + (is_k ? RowL::K : RowL::V);
+        uint32_t n = 0;   // loads so far
+        for (int it = blockIdx.x; it < items; it += gridDim.x) {
+            const int4 e = list[it / Hkv];
+            const int g = it % Hkv;
+            const int L = e.y, req = e.w;
+            const int C = (L + CHUNK - 1) / CHUNK;
+            const int32_t *pt_row = page_table + (int64_t)req * max_pages;
+            for (int c = 0; c < C; ++c, ++n) {
+                // the buffer is free once the previous chunk's products
+                // that read it have completed
+                if (lane == 0 && n > 0) gw(freed, (n - 1) & 1);
+                __syncwarp();
                 int pg = -1;
                 if (lane < 16) {
                     const int pi = c * 16 + lane;
@@ -2598,205 +2498,243 @@ __global__ void __launch_bounds__(tca::GRP_THREADS, 1)
                         }
                     }
                 }
-                uint64_t *bar = is_k ? k_full : v_full;
-                if (lane == 0) mbar_arrive_expect_tx(bar, 16 * 2 * PAGE_BYTES);
+                if (lane == 0)
+                    mbar_arrive_expect_tx(
+                        full, 16 * 2 * PAGE_BYTES +
+                                  (is_k && c == 0 ? 2 * RowL::QH : 0));
                 __syncwarp();
                 if (lane < 16) {
                     const int row = pg >= 0 ? (pg * Hkv + g) * 16 : -16;
-                    uint8_t *tile = smem + (is_k ? GrpL::K : GrpL::V);
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
                         tma_load_2d(tile + h * (CHUNK * 128) + lane * PAGE_BYTES,
-                                    is_k ? &kmap : &vmap, h * 64, row, bar);
+                                    map, h * 64, row, full);
                 }
-            };
-            auto v_in = [&](int c) {
-                gw(v_full, (nc + c) & 1);
-                const int vl = min(CHUNK, L - c * CHUNK);
-                if (vl & 15)
-                    zero_v_rows(smem + GrpL::V, vl, (vl + 15) & ~15, lane, 32);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(v_ready);
-            };
-            int f2[2] = {fq[0], fq[1]};
-            load(0, true);
-            load(0, false);
-            v_in(0);
-            for (int c = 1; c < C; ++c) {
-                bool act[2];
-                for (int t = 0; t < 2; ++t) act[t] = first_t(c - 1, t) < nt;
-                if (lane == 0)
-                    for (int t = 0; t < 2; ++t)
-                        if (act[t]) gw(&k_free[t], f2[t] & 1);
-                __syncwarp();
-                load(c, true);
-                if (lane == 0)
-                    for (int t = 0; t < 2; ++t)
-                        if (act[t]) gw(&v_free[t], f2[t] & 1);
-                __syncwarp();
-                load(c, false);
-                v_in(c);
-                for (int t = 0; t < 2; ++t) f2[t] += act[t];
-            }
-        } else {
-            // ------------------------------- softmax teams (and MMAs) --
-            const int team = warp >> 2, wq = warp & 3;
-            const bool issuer = wq == 0 && lane == 0;
-            const uint32_t lq = (uint32_t)(wq * 32) << 16;
-            float *sb = sbuf + team * (GrpL::SB / 4);
-            float4 *ab = abs_ + team * 16;
-            const uint32_t s_t = tmem + T_S + 32 * team;
-            const uint32_t oc_t = tmem + T_OC + 16 * team;
-            const uint32_t p_t = ptile + team * P_TILE;
-            // the team's units: chunk c, tiles first_t(c, team), + 2, ..;
-            // cc == C once the team has none left
-            int cc = 0, ii = first_t(0, team);
-            if (ii >= nt) cc = C;
-            auto next = [&](int &c, int &i) {
-                i += 2;
-                if (i >= nt) {
-                    ++c;
-                    i = c < C ? first_t(c, team) : nt;
-                    if (i >= nt) c = C;
-                }
-            };
-            auto qk = [&](int c, int i) {   // issuer only
-                if (i == first_t(c, team)) gw(k_full, (nc + c) & 1);
-                tc_fence_after();
-                issue_qk(s_t, ktile, qtile + i * GrpL::QB);
-                tc_commit(&s_full[team]);
-                if (i + 2 >= nt) tc_commit(&k_free[team]);
-            };
-            // merge of the team's unit n (tile i, chunk c), thread = dim:
-            // per row keep O (chunk not visible), take the chunk's o (the
-            // tile's first chunk) or O a + o b, with (a, b) and L from the
-            // row owner's merge_scalars
-            auto merge = [&](int n, int i, int c) {
-                gw(&o_full[team], n & 1);
-                tc_fence_after();
-                float o[16], O[16];
-                tmem_ld_16cols(oc_t + lq, o);
-                if (c > 0)
-                    tmem_ld_16cols(tmem + T_ORUN + 16 * i + lq, O);
-                else
+                if (is_k && c == 0 && lane == 0) {
+                    // rows = 128 / G tokens from e.x x the G heads of g
 #pragma unroll
-                    for (int r = 0; r < 16; ++r) O[r] = 0.f;
-                float Lr[16];
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    const float4 f = ab[r];
-                    const int flag = __float_as_int(f.z);
-                    if (flag == 1)
-                        O[r] = o[r];
-                    else if (flag == 2)
-                        O[r] = merge_value(O[r], o[r], f.x, f.y);
-                    Lr[r] = f.w;
+                    for (int h = 0; h < 2; ++h)
+                        tma_load_3d(smem + RowL::Q + h * RowL::QH, &qmap,
+                                    h * 64, g * G, e.x, full);
                 }
-                if (c == s_ci[i] - 1) {
-                    const int dim = wq * 32 + lane;
-#pragma unroll
-                    for (int r = 0; r < 16; ++r) {
-                        const int tk = i * QPT + r / G, hh = r % G;
-                        if (tk >= ntok) continue;
-                        out[((int64_t)(t0 + tk) * Hq + g * G + hh) * D + dim] =
-                            f32_to_bf16(__fdiv_rn(O[r], Lr[r]));
-                    }
-                } else {
-                    tmem_st_16cols(tmem + T_ORUN + 16 * i + lq, O);
-                }
-                tc_fence_before();
-            };
-            if (issuer && cc < C) qk(cc, ii);
-            int n = nq[team];
-            int pn = -1, pi_ = 0, pc = 0;
-            while (cc < C) {
-                const int c = cc, i = ii;
-                int nc2 = cc, ni = ii;
-                next(nc2, ni);
-                gw(&s_full[team], n & 1);
-                tc_fence_after();
-                softmax_team(s_t, scale, s_prow + i * 16, c, sb, p_t, team);
-                // phase A done by the whole team (S read): the next unit's
-                // scores may overwrite S
-                if (issuer && nc2 < C) qk(nc2, ni);
-                if (pn >= 0) merge(pn, pi_, pc);
-                sync_team(team);  // the previous unit's P and factors used
-                float m, l;
-                softmax_team_b(scale, s_prow + i * 16, c, sb, p_t, m, l);
-                if ((lane & 7) == 0) {
-                    // the row's running (M, L) and this chunk's factors
-                    const int r = 4 * wq + (lane >> 3);
-                    float *ml = mls + (i * 16 + r) * 2;
-                    float a = 0.f, bb = 0.f;
-                    int flag = 0;
-                    if (s_prow[i * 16 + r] + 1 - c * CHUNK > 0) {
-                        if (c == 0) {
-                            ml[0] = m;
-                            ml[1] = l;
-                            flag = 1;
-                        } else {
-                            float M = ml[0], Lr = ml[1];
-                            merge_scalars(M, Lr, m, l, a, bb);
-                            ml[0] = M;
-                            ml[1] = Lr;
-                            flag = 2;
-                        }
-                    }
-                    ab[r] = make_float4(a, bb, __int_as_float(flag), ml[1]);
-                }
-                fence_proxy_async_smem();
-                tc_fence_before();
-                sync_team(team);  // P and the factors are written
-                if (issuer) {
-                    if (i == first_t(c, team)) gw(v_ready, (nc + c) & 1);
-                    tc_fence_after();
-                    issue_pv(oc_t, vtile, p_t);
-                    tc_commit(&o_full[team]);
-                    if (i + 2 >= nt) tc_commit(&v_free[team]);
-                }
-                pn = n;
-                pi_ = i;
-                pc = c;
-                ++n;
-                cc = nc2;
-                ii = ni;
-            }
-            if (pn >= 0) merge(pn, pi_, pc);
-            if (issuer) {
-                // the commits of the item's last chunk have landed before
-                // the next item waits on these barriers again
-                int ch = 0;
-                for (int c = 0; c < C; ++c) ch += first_t(c, team) < nt;
-                if (ch > 0) {
-                    gw(&k_free[team], (fq[team] + ch - 1) & 1);
-                    gw(&v_free[team], (fq[team] + ch - 1) & 1);
+                if (!is_k) {
+                    gw(v_full, n & 1);
+                    const int vl = min(CHUNK, L - c * CHUNK);
+                    if (vl & 15)
+                        zero_v_rows(tile, vl, (vl + 15) & ~15, lane, 32);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(v_ready);
                 }
             }
         }
-        // the same walk in every role: advance the counters
-        for (int c = 0; c < C; ++c)
-            for (int t = 0; t < 2; ++t) {
-                const int i0 = first_t(c, t);
-                if (i0 < nt) {
-                    nq[t] += (nt - i0 + 1) / 2;
-                    ++fq[t];
+        // own copies in flight have landed before the CTA leaves (after a
+        // wait gave up, the last load may not have been waited on)
+        if (lane == 0 && n > 0)
+            mbar_wait_for(full, (n - 1) & 1, status, BI_WAIT_LIMIT_NS);
+    } else if (warp == 4) {
+        // ---------------------------------------------------------- MMAs --
+        if (lane == 0) {
+            const uint32_t qt = base + RowL::Q, kt = base + RowL::K,
+                           vt = base + RowL::V, pt = base + RowL::P;
+            // S of chunk n into slot n % 2: the slot's previous chunk
+            // (n - 2) has been merged, K of chunk n is in
+            auto qk = [&](uint32_t n) {
+                const uint32_t b = n & 1;
+                if (n >= 2) gw(&slot_free[b], ((n - 2) >> 1) & 1);
+                gw(k_full, n & 1);
+                tc_fence_after();
+                issue_rows_s(tmem + 256 * b, qt, kt);
+                tc_commit(&s_full[b]);
+                tc_commit(k_free);
+            };
+            uint32_t n = 0;
+            const int it0 = blockIdx.x;
+            if (it0 < items) qk(0);
+            for (int it = it0; it < items; it += gridDim.x) {
+                const int L = list[it / Hkv].y;
+                const int C = (L + CHUNK - 1) / CHUNK;
+                for (int c = 0; c < C; ++c, ++n) {
+                    // the next chunk (of this item or the next one) first
+                    if (c + 1 < C || it + (int)gridDim.x < items) qk(n + 1);
+                    gw(p_full, n & 1);   // pass 2 of chunk n wrote P
+                    gw(v_ready, n & 1);
+                    tc_fence_after();
+                    issue_rows_o(tmem + 256 * (n & 1), pt, vt);
+                    tc_commit(o_full);
+                    tc_commit(v_free);
                 }
             }
-        nc += C;
+            // the products in flight have completed before the CTA leaves
+            tc_commit(done);
+            mbar_wait_for(done, 0, status, BI_WAIT_LIMIT_NS);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------- rows: softmax and merges --
+        const int r = threadIdx.x;   // 0..127
+        const uint32_t lq = (uint32_t)(warp * 32) << 16;
+        const uint32_t prow_smem = base + RowL::P + r * 128;
+        const bool pos_scale = scale > 0.f;
+        const float c1 = __fmul_rn(scale, LOG2E);
+        uint32_t n = 0;
+        for (int it = blockIdx.x; it < items; it += gridDim.x) {
+            const int4 e = list[it / Hkv];
+            const int g = it % Hkv;
+            const int t0 = e.x, L = e.y, ntok = e.z;
+            const int C = (L + CHUNK - 1) / CHUNK;
+            const int tk = r / G, hh = r % G;
+            // position of the row's token (tokens of a tile are consecutive
+            // positions ending at L - 1), -1 past the tile's tokens
+            const int prow = tk < ntok ? L - ntok + tk : -1;
+            float O[D];                      // running values
+            float M = -INFINITY, Ls = 0.f;   // running max and sum
+            float pm = 0.f, pl = 0.f;        // chunk n - 1
+            int plen = 0;
+            // merge of the previous chunk (index np, first of the item if
+            // first): its values from its slot into O, then the slot is free
+            auto merge = [&](uint32_t np, bool first) {
+                gw(o_full, np & 1);
+                tc_fence_after();
+                const uint32_t o_t = tmem + 256 * (np & 1) + lq;
+                const bool part = plen > 0;
+                if (first) {
+                    if (part) {
+                        M = pm;
+                        Ls = pl;
+                    }
+#pragma unroll
+                    for (int blk = 0; blk < 4; ++blk)
+                        tmem_ld_32cols(o_t + 32 * blk, O + 32 * blk);
+                } else {
+                    float a = 0.f, b = 0.f;
+                    if (part) merge_scalars(M, Ls, pm, pl, a, b);
+                    if (__any_sync(0xffffffffu, part)) {
+#pragma unroll
+                        for (int blk = 0; blk < 4; ++blk) {
+                            float o[32];
+                            tmem_ld_32cols(o_t + 32 * blk, o);
+                            if (part)
+#pragma unroll
+                                for (int i = 0; i < 32; ++i)
+                                    O[32 * blk + i] = merge_value(
+                                        O[32 * blk + i], o[i], a, b);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&slot_free[np & 1]);
+            };
+            for (int c = 0; c < C; ++c, ++n) {
+                const uint32_t s_t = tmem + 256 * (n & 1) + lq;
+                gw(&s_full[n & 1], (n >> 1) & 1);
+                tc_fence_after();
+                const int len = prow + 1 - c * CHUNK;   // visible keys
+                const bool any = __any_sync(0xffffffffu, len > 0);
+                // pass 1: the exact maximum of the row's visible scores
+                float m = -INFINITY;
+                if (any) {
+#pragma unroll 1
+                    for (int gq = 0; gq < 8; ++gq) {
+                        float v[32];
+                        tmem_ld_32cols(s_t + 32 * gq, v);
+                        if (!pos_scale)
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                v[j] = __fmul_rn(v[j], scale);
+                        if (len < CHUNK)
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (32 * gq + j >= len) v[j] = -INFINITY;
+                        m = fmaxf(m, max32(v));
+                    }
+                    if (pos_scale) m = __fmul_rn(m, scale);
+                }
+                const float mu2 =
+                    __fmul_rn(m == -INFINITY ? 0.f : m, LOG2E);
+                // the previous chunk's values (its products also finished
+                // reading P)
+                if (c > 0) merge(n - 1, c == 1);
+                // pass 2: p, bf16(p) into P, the row sum in the decode order
+                float l = 0.f;
+#pragma unroll 1
+                for (int gq = 0; gq < 8; ++gq) {
+                    float x[32];
+                    if (any) {
+                        tmem_ld_32cols(s_t + 32 * gq, x);
+                        if (len >= CHUNK) {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                x[j] = p_of(x[j], c1, mu2);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                x[j] = 32 * gq + j < len ? p_of(x[j], c1, mu2)
+                                                         : 0.f;
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) x[j] = 0.f;
+                    }
+                    const uint32_t pg_base =
+                        prow_smem + (gq >> 1) * RowL::PG;
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        const int u = ((gq & 1) * 4 + q4) ^ (r & 7);
+                        asm volatile(
+                            "st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                pg_base + (u << 4)),
+                            "r"(pack_bf16x2(x[8 * q4 + 0], x[8 * q4 + 1])),
+                            "r"(pack_bf16x2(x[8 * q4 + 2], x[8 * q4 + 3])),
+                            "r"(pack_bf16x2(x[8 * q4 + 4], x[8 * q4 + 5])),
+                            "r"(pack_bf16x2(x[8 * q4 + 6], x[8 * q4 + 7]))
+                            : "memory");
+                    }
+                    const float W = xor_tree32(x);
+                    l = gq == 0 ? W : __fadd_rn(l, W);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(p_full);
+                pm = m;
+                pl = l;
+                plen = len;
+            }
+            // the last chunk's values, then the rows out
+            merge(n - 1, C == 1);
+            if (prow >= 0) {
+                uint16_t *dst =
+                    out + ((int64_t)(t0 + tk) * Hq + g * G + hh) * D;
+#pragma unroll
+                for (int q8 = 0; q8 < D / 8; ++q8) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__fdiv_rn(O[8 * q8 + 0], Ls),
+                                      __fdiv_rn(O[8 * q8 + 1], Ls));
+                    w.y = pack_bf16x2(__fdiv_rn(O[8 * q8 + 2], Ls),
+                                      __fdiv_rn(O[8 * q8 + 3], Ls));
+                    w.z = pack_bf16x2(__fdiv_rn(O[8 * q8 + 4], Ls),
+                                      __fdiv_rn(O[8 * q8 + 5], Ls));
+                    w.w = pack_bf16x2(__fdiv_rn(O[8 * q8 + 6], Ls),
+                                      __fdiv_rn(O[8 * q8 + 7], Ls));
+                    *reinterpret_cast<uint4 *>(dst + 8 * q8) = w;
+                }
+            }
+        }
     }
     // entries with no valid context: zero outputs
     for (int j = n_valid + blockIdx.x; j < n_all; j += gridDim.x) {
         const int4 e = list[j];
         const int64_t n = (int64_t)e.z * Hq * D;
-        for (int64_t idx = threadIdx.x; idx < n; idx += GRP_THREADS)
+        for (int64_t idx = threadIdx.x; idx < n; idx += ROW_THREADS)
             out[(int64_t)e.x * Hq * D + idx] = 0;
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == SW) {
+    if (warp == 4) {
         tc_fence_after();
-        tmem_dealloc(tmem, GRP_TMEM);
+        tmem_dealloc(tmem, ROW_TMEM);
     }
 }
 
@@ -3114,20 +3052,17 @@ bi_status bi_prefill_attn_pool(const bi_bf16 *q, const int32_t *cu_q,
     const int tiles = (T + QPT - 1) / QPT + R;
     int32_t *status = bi_status_ptr();
     dim3 grid(tiles, Hkv);
-    // With a workspace, head_dim 128: verify-sized batches (T <= 512) on
-    // the persistent decode kernel over (16 / G-token tile, KV head) items
-    // (8 windows of 32 rows: 75 us against 110 us for the group kernel),
-    // longer prompt pieces on the group kernel over a sorted list of
-    // 8-tile groups (one K / V chunk load per group instead of per tile:
-    // 2048 rows at contexts of 2-4k, 1.05 ms against 1.97 ms one CTA per
-    // tile).  Without a workspace, one CTA per 16-row tile.  All three give
-    // the same bits.
-    if (D == 128 && ws && R <= MAX_SEGS && T <= 512 &&
-        ws_bytes >= bi_prefill_attn_ws_bytes(T, R, Hq, Hkv)) {
+    // With a workspace, head_dim 128: the row-per-thread kernel over a
+    // sorted list of 128-row tiles (one K / V chunk load per tile of
+    // 128 / G tokens).  Without a workspace, one CTA per 16-row tile.  Both
+    // give the bits of decode.
+    if (D == 128 && ws && R <= MAX_SEGS &&
+               ws_bytes >= bi_prefill_attn_ws_bytes(T, R, Hq, Hkv)) {
+        const int QPR = 128 / G;   // tokens per 128-row tile
         static std::once_flag f;
         static bi_status fs;
         std::call_once(f, [] {
-            fs = set_attr(attn_tc_kernel<true>, tca::DecL::ALLOC);
+            fs = set_attr(attn_rows_kernel, tca::RowL::ALLOC);
         });
         if (fs != BI_OK) return fs;
         const uint64_t pool_rows = (uint64_t)n_pages * Hkv * 16;
@@ -3139,56 +3074,25 @@ bi_status bi_prefill_attn_pool(const bi_bf16 *q, const int32_t *cu_q,
         if ((st = bi_make_tmap_2d_bf16(&vm, v_pool, D, pool_rows, D * 2, 64, 16,
                                        true)) != BI_OK)
             return st;
-        // queries as [T][Hq][D]: boxes of 64 dims x G heads x QPT tokens
+        // queries as [T][Hq][D]: boxes of 64 dims x G heads x QPR tokens
         if ((st = bi_make_tmap_3d(&qm, q, false, D, Hq, T, 64, G, true,
-                                  QPT)) != BI_OK)
+                                  QPR)) != BI_OK)
             return st;
+        const int tiles128 = (T + QPR - 1) / QPR + R;
         int4 *tmp = static_cast<int4 *>(ws);
-        int4 *list = tmp + tiles;
-        int32_t *cnt = reinterpret_cast<int32_t *>(list + tiles);
-        build_tiles_kernel<<<1, 1024, 0, stream>>>(cu_q, seg_req, pos, R, QPT,
+        int4 *list = tmp + tiles128;
+        int32_t *cnt = reinterpret_cast<int32_t *>(list + tiles128);
+        build_tiles_kernel<<<1, 1024, 0, stream>>>(cu_q, seg_req, pos, R, QPR,
                                                    max_kv_len, tmp, list, cnt,
                                                    status);
-        BI_LAUNCH_CHECK("prefill tile list launch");
-        attn_tc_kernel<true>
-            <<<bi_sm_count(), tca::DEC_THREADS, tca::DecL::ALLOC, stream>>>(
-                km, vm, qm, page_table, max_pages, n_pages, nullptr, Hq, Hkv,
-                G, scale, cnt, 0, list, k_pool, v_pool,
-                reinterpret_cast<uint16_t *>(out), status);
-    } else if (D == 128 && ws && R <= MAX_SEGS &&
-               ws_bytes >= bi_prefill_attn_ws_bytes(T, R, Hq, Hkv)) {
-        const int GT = tca::GT_MAX;
-        const int QPG = GT * QPT;
-        static std::once_flag f;
-        static bi_status fs;
-        std::call_once(f, [] {
-            fs = set_attr(attn_group_kernel, tca::GrpL::ALLOC);
-        });
-        if (fs != BI_OK) return fs;
-        const uint64_t pool_rows = (uint64_t)n_pages * Hkv * 16;
-        CUtensorMap km, vm;
-        bi_status st;
-        if ((st = bi_make_tmap_2d_bf16(&km, k_pool, D, pool_rows, D * 2, 64, 16,
-                                       true)) != BI_OK)
-            return st;
-        if ((st = bi_make_tmap_2d_bf16(&vm, v_pool, D, pool_rows, D * 2, 64, 16,
-                                       true)) != BI_OK)
-            return st;
-        const int groups = (T + QPG - 1) / QPG + R;
-        int4 *tmp = static_cast<int4 *>(ws);
-        int4 *list = tmp + groups;
-        int32_t *cnt = reinterpret_cast<int32_t *>(list + groups);
-        build_tiles_kernel<<<1, 1024, 0, stream>>>(cu_q, seg_req, pos, R, QPG,
-                                                   max_kv_len, tmp, list, cnt,
-                                                   status);
-        BI_LAUNCH_CHECK("prefill group list launch");
+        BI_LAUNCH_CHECK("prefill row-tile list launch");
         const int grid =
-            (int)std::min<int64_t>((int64_t)groups * Hkv, bi_sm_count());
-        attn_group_kernel<<<grid, tca::GRP_THREADS, tca::GrpL::ALLOC,
-                            stream>>>(
-            km, vm, reinterpret_cast<const uint16_t *>(q), list, cnt, pos,
-            page_table, max_pages, n_pages, Hq, Hkv, G, GT, scale,
-            reinterpret_cast<uint16_t *>(out), status);
+            (int)std::min<int64_t>((int64_t)tiles128 * Hkv, bi_sm_count());
+        attn_rows_kernel<<<grid, tca::ROW_THREADS, tca::RowL::ALLOC,
+                           stream>>>(km, vm, qm, list, cnt, page_table,
+                                     max_pages, n_pages, Hq, Hkv, G, scale,
+                                     reinterpret_cast<uint16_t *>(out),
+                                     status);
     } else if (D == 128) {
         static std::once_flag f;
         static bi_status fs;

@@ -169,7 +169,7 @@ def decode(bi, q, kv, rows, kv_len):
     return out
 
 
-def prefill(bi, q, kv, segs, ws=False):
+def prefill(bi, q, kv, segs, ws=False, scale=None):
     """segs: list of (request, first position, n rows); q rows in order.
     ws: run bi_prefill_attn_ws with a workspace (the persistent path)."""
     cu, sr, pos = [0], [], []
@@ -182,7 +182,7 @@ def prefill(bi, q, kv, segs, ws=False):
             torch.tensor(sr, dtype=torch.int32).cuda(),
             torch.tensor(pos, dtype=torch.int32).cuda(),
             max(n for _, _, n in segs), max(pos) + 1, kv.kp, kv.vp, kv.table,
-            1 / math.sqrt(q.shape[2]), out)
+            1 / math.sqrt(q.shape[2]) if scale is None else scale, out)
     if ws:
         T, Hq = q.shape[0], q.shape[1]
         nb = bi.bi_prefill_attn_workspace_size(T, len(segs), Hq,
@@ -331,12 +331,12 @@ def test_prefill_matches_decode_bitwise(bi, orc, Hq, Hkv, D):
 
 def test_prefill_group_path_bitwise(bi, orc):
     """Prompt pieces longer than a verify batch (here 1358 rows) take the
-    group kernel, which loads each K / V chunk once for up to 8 query tiles
-    (32 tokens x 4 heads) of a segment: its outputs equal, bit for bit, the
-    one-CTA-per-tile prefill and decode of each row alone, over segments
-    whose lengths are not multiples of the group (partial groups), two
-    pieces of one request, a pad segment (zero outputs) and NaN-filled
-    stale pages; sampled rows agree with the oracle."""
+    row-per-thread kernel over 128-row tiles (32 tokens x 4 heads) of a
+    segment: its outputs equal, bit for bit, the one-CTA-per-16-row-tile
+    prefill and decode of each row alone, over segments whose lengths are
+    not multiples of the tile (partial tiles), two pieces of one request, a
+    pad segment (zero outputs) and NaN-filled stale pages; sampled rows
+    agree with the oracle."""
     Hq, Hkv, D = 32, 8, 128
     lens = [2100, 700, 1600]
     kv = PagedKV(lens, Hkv, D, seed=51)
@@ -360,6 +360,29 @@ def test_prefill_group_path_bitwise(bi, orc):
     ref = attn_ref(orc, q[pick].contiguous(), kv, [rows[i] for i in pick],
                    [pos[i] for i in pick])
     check_close(bits(grp)[pick], ref, orc)
+
+
+@pytest.mark.parametrize("Hq,Hkv,scale", [(16, 2, None), (8, 8, None),
+                                          (32, 2, None), (16, 8, None),
+                                          (8, 2, -0.06)])
+def test_prefill_row_tiles_other_groupings(bi, Hq, Hkv, scale):
+    """The 128-row tiles hold 128 / G tokens (G = Hq / Hkv query heads per
+    KV head: 16, 128, 8 and 64 tokens here); each grouping, and a negative
+    scale (the maximum is then taken on the scaled scores), gives the bits
+    of the one-CTA-per-16-row-tile kernel."""
+    D = 128
+    lens = [1100, 900]
+    kv = PagedKV(lens, Hkv, D, seed=61)
+    segs = [(0, 300, 800), (1, 0, 900)]
+    T = sum(n for _, _, n in segs)
+    q = randn_bf16((T, Hq, D), 62)
+    rows_, _ = prefill(bi, q, kv, segs, ws=True, scale=scale)
+    sync_ok(bi)
+    one, _ = prefill(bi, q, kv, segs, scale=scale)
+    sync_ok(bi)
+    assert np.array_equal(bits(rows_), bits(one))
+    b = bits(rows_)
+    assert not (((b & 0x7f80) == 0x7f80) & ((b & 0x7f) != 0)).any()
 
 
 # -------------------------------------------------------------- argmax --
