@@ -323,12 +323,25 @@ __device__ __forceinline__ void chunk_phase2(uint32_t vtile, uint32_t ptile,
                                  __fadd_rn(oc[2][nt][e], oc[3][nt][e]));
 }
 
-// One step of the fixed-order chunk merge.
+// 2^y by the PTX base-2 exponential ex2.approx.ftz (relative error about
+// 2^-22; results below 2^-126 flush to zero).  e^x is taken as
+// 2^rn(x log2 e) (change of base) by the merge below and, with the
+// argument from one fma, for the softmax's p (p_of).
+constexpr float LOG2E = 1.4426950408889634f;
+__device__ __forceinline__ float exp2_approx(float y) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
+    return r;
+}
+
+// One step of the fixed-order chunk merge: the new maximum, the factors
+// a = e^(M - M'), b = e^(m - M') (each 2^rn(rn(x - M') log2 e)), and the
+// running sum.  Every path's merge goes through this one function.
 __device__ __forceinline__ void merge_scalars(float &M, float &L, float m,
                                               float l, float &a, float &b) {
     const float Mn = fmaxf(M, m);
-    a = expf(__fsub_rn(M, Mn));
-    b = expf(__fsub_rn(m, Mn));
+    a = exp2_approx(__fmul_rn(__fsub_rn(M, Mn), LOG2E));
+    b = exp2_approx(__fmul_rn(__fsub_rn(m, Mn), LOG2E));
     L = __fadd_rn(__fmul_rn(L, a), __fmul_rn(l, b));
     M = Mn;
 }
@@ -896,18 +909,11 @@ namespace tca {
 // p = e^(s scale - mu) for a raw score s (QK product) of a chunk whose
 // scaled maximum is mu, by the change of base e^x = 2^(x log2 e):
 // 2^(s c1 - mu2) with c1 = rn(scale log2 e) and mu2 = rn(mu log2 e), the
-// argument from one fma, then the PTX base-2 exponential ex2.approx.ftz
-// (relative error about 2^-22; results below 2^-126 flush to zero).  The
+// argument from one fma, then exp2_approx.  The
 // argument's error is a few fp32 ulp of |s scale|, far below the bf16
 // rounding P gets next.  Every head_dim-128 path (decode, prefill, verify)
 // takes p from this one function, so they agree bit for bit; it is two
 // instructions per score.
-constexpr float LOG2E = 1.4426950408889634f;
-__device__ __forceinline__ float exp2_approx(float y) {
-    float r;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
-    return r;
-}
 __device__ __forceinline__ float p_of(float s, float c1, float mu2) {
     return exp2_approx(__fmaf_rn(s, c1, -mu2));
 }
@@ -969,10 +975,11 @@ __device__ __forceinline__ void sync_softmax() {
 // reductions of the NR rows run stage by stage across the rows (independent
 // shuffle chains side by side); each row's own operations and their order
 // do not depend on NR.
-template <int NR>
+template <int NR, int NA>
 __device__ __forceinline__ void softmax(uint32_t s_tmem, float scale,
-                                        const int (&len)[16], uint32_t ptile,
-                                        float *red, float (&m)[16]) {
+                                        const int (&len)[NA], uint32_t ptile,
+                                        float *red, float (&m)[NA]) {
+    static_assert(NR <= NA, "rows");
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int key = (w >> 2) * 128 + (w & 3) * 32 + lane;
     const float c1 = __fmul_rn(scale, LOG2E);
@@ -1051,7 +1058,9 @@ struct DecL {
     static constexpr int BYTES = BAR + (2 * RING + 10) * 8 + 16;
     static constexpr int ALLOC = BYTES + 1024;
 };
-constexpr int DEC_THREADS = (SW + 3) * 32;  // softmax, MMA, producer, prefetch
+constexpr int DEC_THREADS = (SW + 4) * 32;  // softmax, MMA, K, prefetch, V
+// the whole-row decode kernel: two K and two V producer warps
+constexpr int DEC_ROW_THREADS = (SW + 6) * 32;
 
 // Position of the K and V loads of item n in the ring's load sequence.
 __device__ __forceinline__ int k_load(int n) { return 2 * n; }
@@ -1309,8 +1318,8 @@ struct UnitWalk {
 //               n + 2 is issued as soon as unit n's softmax has read S^T
 //               (two S buffers), O^T of unit n once its P tile is written
 //               (two P tiles, two O buffers);
-//   warp 9      producer: page ids -> TMA boxes (K only for visible pages,
-//               V for all 16 pages, missing ones as zero-filled boxes);
+//   warp 9      producer: page ids -> TMA boxes (K and V of the visible pages;
+//               the V rows past them are zeroed by the softmax warps);
 //   warp 10     asks L2 for the K/V pages of the unit after the one the
 //               producer loads next (one ahead: 1% faster than two, 9%
 //               faster than four or none).
@@ -1323,8 +1332,8 @@ struct UnitWalk {
 // its own position, all 16 rows merged and written.  The chunk partials and
 // their merge are the same computation as decode's, so a (request,
 // position) gets the same bits either way.
-template <bool PRE>
-__global__ void __launch_bounds__(tca::DEC_THREADS, 1)
+template <bool PRE, int NR>
+__global__ void __launch_bounds__(tca::DEC_ROW_THREADS, 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap,
                    const __grid_constant__ CUtensorMap qmap,
@@ -1345,7 +1354,10 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
     constexpr int HALF_TILE = CHUNK * 128;
     constexpr int HALF_Q = 16 * 128;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ int s_progress;  // units the producer has issued
+    // units whose K (s_progress, s_kprog2) / V (s_vprog[2]) each of the
+    // producer warps has issued
+    __shared__ int s_progress, s_kprog2;
+    __shared__ int s_vprog[2];
     __shared__ int s_units;     // units of this CTA
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1365,7 +1377,7 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < RING; ++i) {
-            mbar_init(&full[i], 1);
+            mbar_init(&full[i], 2);  // the two producer warps of the load
             mbar_init(&empty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -1377,6 +1389,8 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
         }
         mbar_fence_init();
         s_progress = 0;
+        s_kprog2 = 0;
+        s_vprog[0] = s_vprog[1] = 0;
     }
     if (warp < SW) {
         // both P tiles start at zero: rows >= G are never written again
@@ -1440,12 +1454,33 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
         return;
     }
 
-    if (warp == SW + 1) {
-        // ------------------------------------------------------ producer --
-        if (lane == 0) {
-            tma_prefetch_desc(&kmap);
-            tma_prefetch_desc(&vmap);
-            tma_prefetch_desc(&qmap);
+    if (warp == SW + 1 || warp >= SW + 3) {
+        // ----------------------------------------------------- producers --
+        // Warps SW + 1 and SW + 3 issue K (+ Q), warps SW + 4 and SW + 5
+        // issue V, each for half of a unit's 16 pages (lanes 0-7: pages
+        // 8 hf + lane): a TMA box costs its issuing warp about 70 cycles,
+        // so a tile's boxes go out from two warps at once.  Load t = 2n + kv
+        // goes to slot t % RING after the consumer of load t - RING has
+        // released it; t - RING is always the other pair's, so before load t
+        // a warp also waits until both warps of the other pair have issued
+        // t - RING (their progress counters): every slot's loads are then
+        // issued in order and each empty-barrier wait names an unambiguous
+        // phase.  full[] takes one arrival (with its bytes) from each warp
+        // of the pair.
+        const int kv = warp == SW + 1 || warp == SW + 3 ? 0 : 1;
+        const int hf = warp == SW + 1 || warp == SW + 4 ? 0 : 1;
+        volatile int *kp[2] = {progress, (volatile int *)&s_kprog2};
+        volatile int *vp[2] = {(volatile int *)&s_vprog[0],
+                               (volatile int *)&s_vprog[1]};
+        volatile int *mine = kv == 0 ? kp[hf] : vp[hf];
+        volatile int *const *other = kv == 0 ? vp : kp;
+        if (lane == 0 && hf == 0) {
+            if (kv == 0) {
+                tma_prefetch_desc(&kmap);
+                tma_prefetch_desc(&qmap);
+            } else {
+                tma_prefetch_desc(&vmap);
+            }
         }
         bool ok = true;
         Walk w{rows, total, Hkv};
@@ -1457,9 +1492,10 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
                 const int b = w.b, c = w.c, g = w.g;
                 const int npg = (w.vl() + 15) >> 4;
                 const int32_t *pt_row = page_table + (int64_t)req * max_pages;
+                const int pl = 8 * hf + lane;   // this lane's page of the chunk
                 int pg = -1;
-                if (lane < npg) {
-                    const int pi = c * 16 + lane;
+                if (lane < 8 && pl < npg) {
+                    const int pi = c * 16 + pl;
                     pg = pi < max_pages ? pt_row[pi] : -1;
                     if (pg < 0 || pg >= n_pages) {
                         bi_record_error(status, BI_ERR_BOUNDS);
@@ -1467,33 +1503,52 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
                     }
                 }
                 const int nvalid = __popc(__ballot_sync(0xffffffffu, pg >= 0));
-                // K (+ Q): the visible pages.  V: all 16 pages, the ones
-                // without data as boxes wholly above row 0 (zero-filled).
-                for (int kv = 0; kv < 2 && ok; ++kv) {
+                // K (+ Q) and V: the visible pages only; the V rows past
+                // them are zeroed in shared memory by the softmax warps
+                // (a TMA box each would cost the producer as much as a
+                // page of data).
+                {
                     const int t = 2 * n + kv;
                     const int slot = t % RING;
                     const int use = t / RING;
                     bool w_ok = true;
-                    if (lane == 0 && use > 0)
-                        w_ok = mbar_wait(&empty[slot], (use - 1) & 1, status);
+                    if (lane == 0 && use > 0) {
+                        // load t - RING = 2 m + (1 - kv) issued by both
+                        // warps of the other pair: their counts passed m
+                        const int need = (t - RING - (1 - kv)) / 2 + 1;
+                        if (*other[0] < need || *other[1] < need) {
+                            const uint64_t t0 = bi_globaltimer();
+                            while (*other[0] < need || *other[1] < need) {
+                                __nanosleep(64);
+                                if (bi_globaltimer() - t0 > BI_WAIT_LIMIT_NS) {
+                                    bi_record_error(status, BI_ERR_TIMEOUT);
+                                    w_ok = false;
+                                    break;
+                                }
+                            }
+                        }
+                        if (w_ok)
+                            w_ok = mbar_wait(&empty[slot], (use - 1) & 1,
+                                             status);
+                    }
                     ok = __shfl_sync(0xffffffffu, w_ok ? 1 : 0, 0) != 0;
                     if (!ok) break;
                     if (lane == 0)
-                        mbar_arrive_expect_tx(&full[slot],
-                                              kv == 0 ? nvalid * 2 * PAGE_BYTES +
-                                                            2 * HALF_Q
-                                                      : 16 * 2 * PAGE_BYTES);
+                        mbar_arrive_expect_tx(
+                            &full[slot],
+                            nvalid * 2 * PAGE_BYTES +
+                                (kv == 0 && hf == 0 ? 2 * HALF_Q : 0));
                     __syncwarp();
                     uint8_t *tile = smem + DecL::SLOT + slot * DecL::TB;
-                    if (lane < 16 && (kv == 1 || pg >= 0)) {
-                        const int row = pg >= 0 ? (pg * Hkv + g) * 16 : -16;
+                    if (pg >= 0) {
+                        const int row = (pg * Hkv + g) * 16;
                         const CUtensorMap *map = kv == 0 ? &kmap : &vmap;
 #pragma unroll
                         for (int h = 0; h < 2; ++h)
-                            tma_load_2d(tile + h * HALF_TILE + lane * PAGE_BYTES,
+                            tma_load_2d(tile + h * HALF_TILE + pl * PAGE_BYTES,
                                         map, h * 64, row, &full[slot]);
                     }
-                    if (kv == 0 && lane == 0) {
+                    if (kv == 0 && hf == 0 && lane == 0) {
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             uint8_t *qdst = smem + DecL::QSLOT +
@@ -1505,7 +1560,11 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
                                 tma_load_2d(qdst, &qmap, h * 64, b * Hq + g * G,
                                             &full[slot]);
                         }
-                        *progress = n + 1;
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        __threadfence_block();
+                        *mine = n + 1;
                     }
                 }
                 if (!ok || !w.next()) break;
@@ -1519,7 +1578,11 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
                 }
             }
         }
-        if (lane == 0) *progress = 0x3fffffff;  // release the prefetch warp
+        // every load issued: release the prefetch warp and the other pair.
+        // After a failed wait the count stays where it is, so the other
+        // pair's wait for it runs out too and nothing is issued into a slot
+        // out of order.
+        if (lane == 0 && ok) *mine = 0x3fffffff;
         return;
     }
 
@@ -1593,12 +1656,12 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
         for (int k = tid; k < nt * Hq * D / 8; k += STHREADS)
             dst[k] = make_uint4(0, 0, 0, 0);
     }
-    float m[16], m_prev[16];
+    float m[NR], m_prev[NR];
     // running (max, sum, output) of the item's rows for this thread's dim
     // (warps 0-3), merged chunk by chunk in order
-    float Mr[16], Lr[16], Or[16];
+    float Mr[NR], Lr[NR], Or[NR];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) m_prev[r] = Mr[r] = Lr[r] = Or[r] = 0.f;
+    for (int r = 0; r < NR; ++r) m_prev[r] = Mr[r] = Lr[r] = Or[r] = 0.f;
     // previous unit: row (first token), chunk, head, chunks, tokens, and
     // the position of its first token relative to the chunk (PRE)
     int pb = 0, pc = 0, pg_ = 0, pC = 1, pnt = 1, pp0 = 0;
@@ -1616,7 +1679,7 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
                            o);
             const int dim = warp * 32 + lane;
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
+            for (int r = 0; r < NR; ++r) {
                 if (!PRE && r >= G) break;
                 const int qi = PRE ? r / G : 0;  // token of row r
                 if (qi >= pnt) continue;
@@ -1660,40 +1723,36 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
                 break;
             }
             tc_fence_after();
-            int len[16];
+            int len[NR];
             if constexpr (PRE) {
                 // row r: token r / G at position (L - ntok) + r / G
                 const int p0 = w.L - w.ntok - w.c * CHUNK;
 #pragma unroll
-                for (int r = 0; r < 16; ++r) {
+                for (int r = 0; r < NR; ++r) {
                     const int qi = r / G;
                     len[r] = qi < w.ntok ? max(0, min(CHUNK, p0 + qi + 1)) : 0;
                 }
-                softmax<16>(tmem + bf * 32, scale, len, ptile, red, m);
             } else {
 #pragma unroll
-                for (int r = 0; r < 16; ++r) len[r] = r < G ? vl : 0;
-                if (G <= 4)
-                    softmax<4>(tmem + bf * 32, scale, len, ptile, red, m);
-                else
-                    softmax<16>(tmem + bf * 32, scale, len, ptile, red, m);
+                for (int r = 0; r < NR; ++r) len[r] = r < G ? vl : 0;
             }
-            // V rows past the context inside the last visible page
+            softmax<NR>(tmem + bf * 32, scale, len, ptile, red, m);
+            // V rows past the context: the rest of the tile
             const int jv = v_load(n), sv = jv % RING;
             if (!mbar_wait(&full[sv], (jv / RING) & 1, status)) {
                 ok = false;
                 break;
             }
-            if (vl & 15)
-                zero_v_rows(smem + DecL::SLOT + sv * DecL::TB, vl,
-                            (vl + 15) & ~15, tid, STHREADS);
+            if (vl < CHUNK)
+                zero_v_rows(smem + DecL::SLOT + sv * DecL::TB, vl, CHUNK, tid,
+                            STHREADS);
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[bf]);
             if (n > 0) ok = epilogue(n - 1);
 #pragma unroll
-            for (int r = 0; r < 16; ++r) m_prev[r] = m[r];
+            for (int r = 0; r < NR; ++r) m_prev[r] = m[r];
             pp0 = w.L - w.ntok - w.c * CHUNK;
             pb = w.b;
             pc = w.c;
@@ -1721,8 +1780,8 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
 //               n + 2 is issued as soon as item n's softmax has read S^T
 //               (two S buffers), O^T of item n once its P tile is written
 //               (two P tiles, two O buffers);
-//   warp 9      producer: page ids -> TMA boxes (K only for visible pages,
-//               V for all 16 pages, missing ones as zero-filled boxes);
+//   warp 9      producer: page ids -> TMA boxes (K and V of the visible pages;
+//               the V rows past them are zeroed by the softmax warps);
 //   warp 10     asks L2 for the K/V pages of the item after the one the
 //               producer loads next (one item ahead: 1% faster than two,
 //               9% faster than four or none).
@@ -1791,6 +1850,7 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    if (warp > SW + 2) return;  // one producer here
     volatile int *progress = &s_progress;
 
     if (warp == SW + 2) {
@@ -1865,16 +1925,16 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
                 w_ok = mbar_wait(&empty[slot], (use - 1) & 1, status);
             ok = __shfl_sync(0xffffffffu, w_ok ? 1 : 0, 0) != 0;
             if (!ok) break;
-            // K: the visible pages (+ Q).  V: all 16 pages, the ones
-            // without data as boxes wholly above row 0 (zero-filled).
+            // K (+ Q) and V: the visible pages only; the V rows past them
+            // are zeroed in shared memory by the softmax warps.
             if (lane == 0)
                 mbar_arrive_expect_tx(&full[slot],
-                                      is_k ? nvalid * 2 * PAGE_BYTES + 2 * HALF_Q
-                                           : 16 * 2 * PAGE_BYTES);
+                                      nvalid * 2 * PAGE_BYTES +
+                                          (is_k ? 2 * HALF_Q : 0));
             __syncwarp();
             uint8_t *tile = smem + DecL::SLOT + slot * DecL::TB;
-            if (lane < 16 && (!is_k || pg >= 0)) {
-                const int row = pg >= 0 ? (pg * Hkv + g) * 16 : -16;
+            if (lane < 16 && pg >= 0) {
+                const int row = (pg * Hkv + g) * 16;
                 const CUtensorMap *map = is_k ? &kmap : &vmap;
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
@@ -2028,15 +2088,15 @@ __global__ void __launch_bounds__(tca::DEC_THREADS, 1)
             softmax<4>(tmem + bf * 32, scale, len, ptile, red, m);
         else
             softmax<16>(tmem + bf * 32, scale, len, ptile, red, m);
-        // V rows past the context inside the last visible page
+        // V rows past the context: the rest of the tile
         const int jv = v_load(n), sv = jv % RING;
         if (!mbar_wait(&full[sv], (jv / RING) & 1, status)) {
             ok = false;
             break;
         }
-        if (vl & 15)
-            zero_v_rows(smem + DecL::SLOT + sv * DecL::TB, vl, (vl + 15) & ~15,
-                        tid, STHREADS);
+        if (vl < CHUNK)
+            zero_v_rows(smem + DecL::SLOT + sv * DecL::TB, vl, CHUNK, tid,
+                        STHREADS);
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
@@ -2798,14 +2858,17 @@ bi_status launch_decode_chunks(bool whole_rows, const CUtensorMap &km,
             status);
     } else if constexpr (D == 128) {
         std::call_once(f, [] {
-            fs = set_attr(attn_tc_kernel<false>, tca::DecL::ALLOC);
+            fs = set_attr(attn_tc_kernel<false, 4>, tca::DecL::ALLOC);
+            if (fs == BI_OK)
+                fs = set_attr(attn_tc_kernel<false, 16>, tca::DecL::ALLOC);
         });
         if (fs != BI_OK) return fs;
-        attn_tc_kernel<false>
-            <<<bi_sm_count(), tca::DEC_THREADS, tca::DecL::ALLOC, s>>>(
-                km, vm, qm, page_table, max_pages, n_pages, row_req, Hq, Hkv,
-                G, scale, prefix + B, B, items, k_pool, v_pool,
-                reinterpret_cast<uint16_t *>(out), status);
+        // rows per item: G query heads (the arrays of the row state)
+        auto kern = G <= 4 ? attn_tc_kernel<false, 4> : attn_tc_kernel<false, 16>;
+        kern<<<bi_sm_count(), tca::DEC_ROW_THREADS, tca::DecL::ALLOC, s>>>(
+            km, vm, qm, page_table, max_pages, n_pages, row_req, Hq, Hkv, G,
+            scale, prefix + B, B, items, k_pool, v_pool,
+            reinterpret_cast<uint16_t *>(out), status);
     } else {
         std::call_once(f, [] {
             fs = set_attr(decode_chunks_kernel<D>, DecSmem<D>::ALLOC);
