@@ -147,6 +147,126 @@ __global__ void swiglu_kernel(const float *__restrict__ g,
 
 }  // namespace
 
+// The same computation for H <= VEC * 8 * NORM_THREADS with every load
+// (the slice partials, the residual or x, the weights) issued before the
+// first use: one round of memory latency instead of one per slice group
+// and another for the weights.  The arithmetic and its order are those of
+// rmsnorm_kernel, so the bits are the same.
+template <int S, int VEC>
+__global__ void __launch_bounds__(NORM_THREADS)
+    rmsnorm_fast_kernel(const float *__restrict__ partials,
+                        const uint16_t *__restrict__ x, uint16_t *residual,
+                        const uint16_t *__restrict__ w, int T, int H, float eps,
+                        uint16_t *__restrict__ y) {
+    const int t = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int nvec = H / 8;
+    const int64_t row = (int64_t)t * H;
+    const int64_t TH = (int64_t)T * H;
+    constexpr int SP = S > 0 ? S : 1;
+    float4 pa[VEC][SP][2];
+    uint4 rv[VEC], wv[VEC];
+    bool act[VEC];
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+        const int vi = tid + k * NORM_THREADS;
+        act[k] = vi < nvec;
+        rv[k] = make_uint4(0, 0, 0, 0);
+        if (!act[k]) continue;
+        const int64_t off = row + (int64_t)vi * 8;
+        if (S > 0) {
+#pragma unroll
+            for (int s = 0; s < S; ++s) {
+                const float4 *ps =
+                    reinterpret_cast<const float4 *>(partials + s * TH + off);
+                pa[k][s][0] = __ldcs(ps);
+                pa[k][s][1] = __ldcs(ps + 1);
+            }
+        }
+        const uint16_t *src = residual ? residual : x;
+        if (S == 0 || residual)
+            rv[k] = *reinterpret_cast<const uint4 *>(src + off);
+        wv[k] = *reinterpret_cast<const uint4 *>(w + (int64_t)vi * 8);
+    }
+    float v[VEC][8];
+    float ss = 0.0f;
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+        if (!act[k]) continue;
+        const int64_t off = row + (int64_t)(tid + k * NORM_THREADS) * 8;
+        const uint32_t rr[4] = {rv[k].x, rv[k].y, rv[k].z, rv[k].w};
+        if (S > 0) {
+            float acc[8] = {pa[k][0][0].x, pa[k][0][0].y, pa[k][0][0].z,
+                            pa[k][0][0].w, pa[k][0][1].x, pa[k][0][1].y,
+                            pa[k][0][1].z, pa[k][0][1].w};
+#pragma unroll
+            for (int s = 1; s < S; ++s) {
+                const float4 c = pa[k][s][0], d = pa[k][s][1];
+                acc[0] = __fadd_rn(acc[0], c.x);
+                acc[1] = __fadd_rn(acc[1], c.y);
+                acc[2] = __fadd_rn(acc[2], c.z);
+                acc[3] = __fadd_rn(acc[3], c.w);
+                acc[4] = __fadd_rn(acc[4], d.x);
+                acc[5] = __fadd_rn(acc[5], d.y);
+                acc[6] = __fadd_rn(acc[6], d.z);
+                acc[7] = __fadd_rn(acc[7], d.w);
+            }
+            if (residual) {
+                uint32_t o[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float lo = bf16_to_f32(f32_to_bf16(
+                        __fadd_rn(bf16_lo(rr[j]), acc[2 * j])));
+                    const float hi = bf16_to_f32(f32_to_bf16(
+                        __fadd_rn(bf16_hi(rr[j]), acc[2 * j + 1])));
+                    v[k][2 * j] = lo;
+                    v[k][2 * j + 1] = hi;
+                    o[j] = pack_bf16x2(lo, hi);
+                }
+                *reinterpret_cast<uint4 *>(residual + off) =
+                    make_uint4(o[0], o[1], o[2], o[3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    v[k][j] = bf16_to_f32(f32_to_bf16(acc[j]));
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                v[k][2 * j] = bf16_lo(rr[j]);
+                v[k][2 * j + 1] = bf16_hi(rr[j]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            ss = __fadd_rn(ss, __fmul_rn(v[k][j], v[k][j]));
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1)
+        ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
+    __shared__ float warp_ss[NORM_THREADS / 32];
+    if ((tid & 31) == 0) warp_ss[tid >> 5] = ss;
+    __syncthreads();
+    float tot = warp_ss[0];
+#pragma unroll
+    for (int i = 1; i < NORM_THREADS / 32; ++i) tot = __fadd_rn(tot, warp_ss[i]);
+    const float r = __fdiv_rn(
+        1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(tot, (float)H), eps)));
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+        if (!act[k]) continue;
+        const int64_t off = row + (int64_t)(tid + k * NORM_THREADS) * 8;
+        const uint32_t ww[4] = {wv[k].x, wv[k].y, wv[k].z, wv[k].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            o[j] = pack_bf16x2(
+                __fmul_rn(__fmul_rn(v[k][2 * j], r), bf16_lo(ww[j])),
+                __fmul_rn(__fmul_rn(v[k][2 * j + 1], r), bf16_hi(ww[j])));
+        *reinterpret_cast<uint4 *>(y + off) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
 extern "C" bi_status bi_rmsnorm(const float *partials, int S,
                                 const bi_bf16 *x, bi_bf16 *residual,
                                 const bi_bf16 *w, int T, int H, float eps,
@@ -166,11 +286,21 @@ extern "C" bi_status bi_rmsnorm(const float *partials, int S,
                    bi_aligned16(y),
                "bi_rmsnorm: pointers must be 16-byte aligned");
     cudaStream_t s = bi_stream(stream);
+    // up to two 8-element slices per thread (H <= 4096): all loads first
+    const int vec = (H / 8 + NORM_THREADS - 1) / NORM_THREADS;
     switch (partials ? S : 0) {
 #define BI_NORM_CASE(n)                                                      \
     case n:                                                                  \
-        rmsnorm_kernel<n><<<T, NORM_THREADS, 0, s>>>(partials, x, residual,  \
-                                                     w, T, H, eps, y);       \
+        if (vec == 1)                                                        \
+            rmsnorm_fast_kernel<n, 1><<<T, NORM_THREADS, 0, s>>>(            \
+                partials, x, residual, w, T, H, eps, y);                     \
+        else if (vec == 2)                                                   \
+            rmsnorm_fast_kernel<n, 2><<<T, NORM_THREADS, 0, s>>>(            \
+                partials, x, residual, w, T, H, eps, y);                     \
+        else                                                                 \
+            rmsnorm_kernel<n><<<T, NORM_THREADS, 0, s>>>(partials, x,        \
+                                                         residual, w, T, H,  \
+                                                         eps, y);            \
         break;
         BI_NORM_CASE(0) BI_NORM_CASE(1) BI_NORM_CASE(2) BI_NORM_CASE(3)
         BI_NORM_CASE(4) BI_NORM_CASE(5) BI_NORM_CASE(6) BI_NORM_CASE(7)
