@@ -1051,7 +1051,8 @@ def attn_probe(args):
     pages in random physical order (K, V ~ N(0, 1) bf16): decode at the
     step workload's batch (256 rows, lognormal contexts median 512), one
     prompt piece (2048 tokens at positions 2048..4095 of one request) with
-    a workspace (the group kernel) and without (one CTA per tile), a
+    a workspace (the row-per-thread kernel) and without (one CTA per
+    16-row tile), a
     verify-like batch (8 windows of 32 at lognormal contexts) with and
     without a workspace.  Prints one JSON line of per-call microseconds."""
     import torch
