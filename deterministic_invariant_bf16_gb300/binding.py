@@ -78,6 +78,7 @@ SIGNATURES = {
     "bi_prefill_attn": ([V, V, V, I, I, V, I, I, V, V, V, I, I, I, I, F, V,
                          V], I),
     "bi_prefill_attn_workspace_size": ([I, I, I, I], Z),
+    "bi_prefill_attn_split_workspace_size": ([I, I, I, I, I], Z),
     "bi_prefill_attn_ws": ([V, V, V, I, I, V, I, I, V, V, V, I, I, I, I, F, V,
                             V, Z, V], I),
     "bi_argmax_logits": ([V, I, I, V, V], I),
@@ -248,6 +249,11 @@ def bi_prefill_attn(q, cu_q, seg_req, pos, max_q, max_kv_len, k_pool, v_pool,
 
 def bi_prefill_attn_workspace_size(T, R, Hq, Hkv):
     return lib().bi_prefill_attn_workspace_size(T, R, Hq, Hkv)
+
+
+def bi_prefill_attn_split_workspace_size(T, R, Hq, Hkv, max_kv_len):
+    return lib().bi_prefill_attn_split_workspace_size(T, R, Hq, Hkv,
+                                                      max_kv_len)
 
 
 def bi_prefill_attn_ws(q, cu_q, seg_req, pos, max_q, max_kv_len, k_pool,

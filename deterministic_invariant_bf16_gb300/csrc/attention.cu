@@ -1114,7 +1114,10 @@ __global__ void build_tiles_kernel(const int32_t *__restrict__ cu_q,
                                    int4 *__restrict__ tmp,
                                    int4 *__restrict__ tiles,
                                    int32_t *__restrict__ cnt,
-                                   int32_t *status) {
+                                   int32_t *status, int T = 0,
+                                   int2 *__restrict__ sitems = nullptr,
+                                   int32_t *__restrict__ kvl_tok = nullptr,
+                                   int32_t *__restrict__ req_tok = nullptr) {
     constexpr int TILE = 2048;
     __shared__ int soff[MAX_SEGS + 1];  // first tile of each segment
     __shared__ int skey[TILE];
@@ -1184,6 +1187,37 @@ __global__ void build_tiles_kernel(const int32_t *__restrict__ cu_q,
     if (tid == 0) {
         cnt[0] = nvalid;
         cnt[1] = ntiles;
+    }
+    if (sitems) {
+        // split form: one item per (valid entry, chunk), the entries in list
+        // order, cnt[2] items; every token's context and request (no
+        // request for tokens of invalid entries or of no entry)
+        const int nv = nvalid;
+        int carry2 = 0;
+        for (int j0 = 0; j0 < nv; j0 += blockDim.x) {
+            const int j = j0 + tid;
+            const int Cj = j < nv ? (tiles[j].y + CHUNK - 1) / CHUNK : 0;
+            int tot;
+            __syncthreads();
+            const int before = block_excl_scan_int(Cj, wsum, &tot);
+            for (int c = 0; c < Cj; ++c)
+                sitems[carry2 + before + c] = make_int2(j, c);
+            carry2 += tot;
+        }
+        for (int t = tid; t < T; t += blockDim.x) {
+            kvl_tok[t] = 0;
+            req_tok[t] = -1;
+        }
+        __syncthreads();
+        for (int j = tid; j < ntiles; j += blockDim.x) {
+            const int4 e = tiles[j];
+            const bool valid = j < nv;
+            for (int i = 0; i < e.z; ++i) {
+                kvl_tok[e.x + i] = valid ? e.y - e.z + i + 1 : 0;
+                req_tok[e.x + i] = valid ? e.w : -1;
+            }
+        }
+        if (tid == 0) cnt[2] = carry2;
     }
 }
 
@@ -2457,6 +2491,7 @@ __device__ __forceinline__ float xor_tree32(const float *x) {
 }
 }  // namespace tca
 
+template <bool SPLIT>
 __global__ void __launch_bounds__(tca::ROW_THREADS, 1)
     attn_rows_kernel(const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap,
@@ -2465,7 +2500,9 @@ __global__ void __launch_bounds__(tca::ROW_THREADS, 1)
                      const int32_t *__restrict__ cnt,
                      const int32_t *__restrict__ page_table, int max_pages,
                      int n_pages, int Hq, int Hkv, int G, float scale,
-                     uint16_t *__restrict__ out, int32_t *status) {
+                     uint16_t *__restrict__ out, int32_t *status,
+                     const int2 *__restrict__ sitems, float *__restrict__ rec,
+                     int Cmax) {
     using namespace tca;
     constexpr int D = 128;
     constexpr int PAGE_BYTES = 16 * 64 * 2;   // one box: 16 rows x 64 dims
@@ -2482,7 +2519,22 @@ __global__ void __launch_bounds__(tca::ROW_THREADS, 1)
     volatile int *fail = reinterpret_cast<volatile int *>(tslot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_valid = cnt[0], n_all = cnt[1];
-    const int items = n_valid * Hkv;
+    // item it: KV head it % Hkv of list entry it / Hkv, chunks 0 .. C - 1;
+    // split form: of split item it / Hkv = (entry, chunk c0), that chunk
+    const int items = (SPLIT ? cnt[2] : n_valid) * Hkv;
+    auto item = [&](int it, int4 &e, int &g, int &c0, int &Cn) {
+        g = it % Hkv;
+        if constexpr (SPLIT) {
+            const int2 si = sitems[it / Hkv];
+            e = list[si.x];
+            c0 = si.y;
+            Cn = 1;
+        } else {
+            e = list[it / Hkv];
+            c0 = 0;
+            Cn = (e.y + CHUNK - 1) / CHUNK;
+        }
+    };
 
     // Bounded wait; once any wait of the CTA has run out, returns at once.
     auto gw = [&](uint64_t *bar, uint32_t parity) {
@@ -2537,12 +2589,13 @@ __global__ void __launch_bounds__(tca::ROW_THREADS, 1)
         uint8_t *tile = smem + (is_k ? RowL::K : RowL::V);
         uint32_t n = 0;   // loads so far
         for (int it = blockIdx.x; it < items; it += gridDim.x) {
-            const int4 e = list[it / Hkv];
-            const int g = it % Hkv;
+            int4 e;
+            int g, c0, C;
+            item(it, e, g, c0, C);
             const int L = e.y, req = e.w;
-            const int C = (L + CHUNK - 1) / CHUNK;
             const int32_t *pt_row = page_table + (int64_t)req * max_pages;
-            for (int c = 0; c < C; ++c, ++n) {
+            for (int cl = 0; cl < C; ++cl, ++n) {
+                const int c = c0 + cl;   // the chunk
                 // the buffer is free once the previous chunk's products
                 // that read it have completed
                 if (lane == 0 && n > 0) gw(freed, (n - 1) & 1);
@@ -2561,7 +2614,7 @@ __global__ void __launch_bounds__(tca::ROW_THREADS, 1)
                 if (lane == 0)
                     mbar_arrive_expect_tx(
                         full, 16 * 2 * PAGE_BYTES +
-                                  (is_k && c == 0 ? 2 * RowL::QH : 0));
+                                  (is_k && cl == 0 ? 2 * RowL::QH : 0));
                 __syncwarp();
                 if (lane < 16) {
                     const int row = pg >= 0 ? (pg * Hkv + g) * 16 : -16;
@@ -2570,7 +2623,7 @@ __global__ void __launch_bounds__(tca::ROW_THREADS, 1)
                         tma_load_2d(tile + h * (CHUNK * 128) + lane * PAGE_BYTES,
                                     map, h * 64, row, full);
                 }
-                if (is_k && c == 0 && lane == 0) {
+                if (is_k && cl == 0 && lane == 0) {
                     // rows = 128 / G tokens from e.x x the G heads of g
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
@@ -2612,8 +2665,9 @@ __global__ void __launch_bounds__(tca::ROW_THREADS, 1)
             const int it0 = blockIdx.x;
             if (it0 < items) qk(0);
             for (int it = it0; it < items; it += gridDim.x) {
-                const int L = list[it / Hkv].y;
-                const int C = (L + CHUNK - 1) / CHUNK;
+                int4 e;
+                int g, c0, C;
+                item(it, e, g, c0, C);
                 for (int c = 0; c < C; ++c, ++n) {
                     // the next chunk (of this item or the next one) first
                     if (c + 1 < C || it + (int)gridDim.x < items) qk(n + 1);
@@ -2639,10 +2693,10 @@ __global__ void __launch_bounds__(tca::ROW_THREADS, 1)
         const float c1 = __fmul_rn(scale, LOG2E);
         uint32_t n = 0;
         for (int it = blockIdx.x; it < items; it += gridDim.x) {
-            const int4 e = list[it / Hkv];
-            const int g = it % Hkv;
+            int4 e;
+            int g, c0, C;
+            item(it, e, g, c0, C);
             const int t0 = e.x, L = e.y, ntok = e.z;
-            const int C = (L + CHUNK - 1) / CHUNK;
             const int tk = r / G, hh = r % G;
             // position of the row's token (tokens of a tile are consecutive
             // positions ending at L - 1), -1 past the tile's tokens
@@ -2690,7 +2744,7 @@ __global__ void __launch_bounds__(tca::ROW_THREADS, 1)
                 const uint32_t s_t = tmem + 256 * (n & 1) + lq;
                 gw(&s_full[n & 1], (n >> 1) & 1);
                 tc_fence_after();
-                const int len = prow + 1 - c * CHUNK;   // visible keys
+                const int len = prow + 1 - (c0 + c) * CHUNK;   // visible keys
                 const bool any = __any_sync(0xffffffffu, len > 0);
                 // pass 1: the exact maximum of the row's visible scores
                 float m = -INFINITY;
@@ -2764,7 +2818,20 @@ __global__ void __launch_bounds__(tca::ROW_THREADS, 1)
             }
             // the last chunk's values, then the rows out
             merge(n - 1, C == 1);
-            if (prow >= 0) {
+            if constexpr (SPLIT) {
+                // the chunk's record (m, l, 2 pad, o[D]) of the decode
+                // path's two-stage form, for rows that see the chunk
+                if (prow >= 0 && plen > 0) {
+                    float4 *dst = reinterpret_cast<float4 *>(
+                        rec + (((int64_t)(t0 + tk) * Hq + g * G + hh) * Cmax +
+                               c0) * rec_floats<D>());
+                    dst[0] = make_float4(M, Ls, 0.f, 0.f);
+#pragma unroll
+                    for (int i = 0; i < D / 4; ++i)
+                        dst[1 + i] = make_float4(O[4 * i], O[4 * i + 1],
+                                                 O[4 * i + 2], O[4 * i + 3]);
+                }
+            } else if (prow >= 0) {
                 uint16_t *dst =
                     out + ((int64_t)(t0 + tk) * Hq + g * G + hh) * D;
 #pragma unroll
@@ -2783,8 +2850,9 @@ __global__ void __launch_bounds__(tca::ROW_THREADS, 1)
             }
         }
     }
-    // entries with no valid context: zero outputs
-    for (int j = n_valid + blockIdx.x; j < n_all; j += gridDim.x) {
+    // entries with no valid context: zero outputs (split form: the merge
+    // writes every row)
+    for (int j = n_valid + blockIdx.x; !SPLIT && j < n_all; j += gridDim.x) {
         const int4 e = list[j];
         const int64_t n = (int64_t)e.z * Hq * D;
         for (int64_t idx = threadIdx.x; idx < n; idx += ROW_THREADS)
@@ -3086,6 +3154,24 @@ size_t bi_prefill_attn_ws_bytes(int T, int R, int Hq, int Hkv) {
     return up256(2 * tiles * sizeof(int4) + 2 * sizeof(int32_t));
 }
 
+// Split form (head_dim 128, T <= SPLIT_MAX_T): the tile list and counts,
+// the (entry, chunk) items, every token's context and request, and the
+// chunk records [T][Hq][Cmax] of the decode path's two-stage form.
+constexpr int SPLIT_MAX_T = 512;
+size_t bi_prefill_attn_split_ws_bytes(int T, int R, int Hq, int Hkv,
+                                      int max_kv_len) {
+    if (T <= 0 || T > SPLIT_MAX_T || R <= 0 || Hkv <= 0 || Hq % Hkv ||
+        !group_ok(Hq, Hkv) || max_kv_len <= 0)
+        return 0;
+    const int QPT = 16 / (Hq / Hkv);
+    const size_t tiles = (size_t)(T + QPT - 1) / QPT + R;
+    const size_t Cmax = (size_t)(max_kv_len + CHUNK - 1) / CHUNK;
+    return up256(2 * tiles * sizeof(int4) + 4 * sizeof(int32_t)) +
+           up256(tiles * Cmax * sizeof(int2)) +
+           up256(2 * (size_t)T * sizeof(int32_t)) +
+           up256((size_t)T * Hq * Cmax * rec_floats<128>() * sizeof(float));
+}
+
 bi_status bi_prefill_attn_pool(const bi_bf16 *q, const int32_t *cu_q,
                                const int32_t *seg_req, int R, int T,
                                const int32_t *pos, int max_q, int max_kv_len,
@@ -3093,7 +3179,8 @@ bi_status bi_prefill_attn_pool(const bi_bf16 *q, const int32_t *cu_q,
                                const int32_t *page_table, int max_pages,
                                int n_pages, int Hq, int Hkv, int D,
                                float scale, bi_bf16 *out, void *ws,
-                               size_t ws_bytes, cudaStream_t stream) {
+                               size_t ws_bytes, cudaStream_t stream,
+                               bool reuse_list) {
     BI_REQUIRE(R >= 0 && T >= 0 && max_q >= 0 && max_kv_len > 0 &&
                    max_kv_len <= 16 * max_pages,
                "bi_prefill_attn: R=%d T=%d max_q=%d max_kv_len=%d", R, T,
@@ -3119,13 +3206,68 @@ bi_status bi_prefill_attn_pool(const bi_bf16 *q, const int32_t *cu_q,
     // sorted list of 128-row tiles (one K / V chunk load per tile of
     // 128 / G tokens).  Without a workspace, one CTA per 16-row tile.  Both
     // give the bits of decode.
-    if (D == 128 && ws && R <= MAX_SEGS &&
+    const size_t split_need =
+        D == 128 ? bi_prefill_attn_split_ws_bytes(T, R, Hq, Hkv, max_kv_len)
+                 : 0;
+    if (D == 128 && ws && R <= MAX_SEGS && split_need &&
+        ws_bytes >= split_need) {
+        // verify-sized batches: every (tile, chunk) its own item, the
+        // records merged in chunk order by the decode merge
+        const int QPR = 128 / G;
+        static std::once_flag f;
+        static bi_status fs;
+        std::call_once(f, [] {
+            fs = set_attr(attn_rows_kernel<true>, tca::RowL::ALLOC);
+        });
+        if (fs != BI_OK) return fs;
+        const uint64_t pool_rows = (uint64_t)n_pages * Hkv * 16;
+        CUtensorMap km, vm, qm;
+        bi_status st;
+        if ((st = bi_make_tmap_2d_bf16(&km, k_pool, D, pool_rows, D * 2, 64, 16,
+                                       true)) != BI_OK)
+            return st;
+        if ((st = bi_make_tmap_2d_bf16(&vm, v_pool, D, pool_rows, D * 2, 64, 16,
+                                       true)) != BI_OK)
+            return st;
+        if ((st = bi_make_tmap_3d(&qm, q, false, D, Hq, T, 64, G, true,
+                                  QPR)) != BI_OK)
+            return st;
+        const int Cmax = (max_kv_len + CHUNK - 1) / CHUNK;
+        int4 *tmp = static_cast<int4 *>(ws);
+        int4 *list = tmp + tiles;
+        int32_t *cnt = reinterpret_cast<int32_t *>(list + tiles);
+        uint8_t *p = static_cast<uint8_t *>(ws) +
+                     up256(2 * (size_t)tiles * sizeof(int4) +
+                           4 * sizeof(int32_t));
+        int2 *sitems = reinterpret_cast<int2 *>(p);
+        p += up256((size_t)tiles * Cmax * sizeof(int2));
+        int32_t *kvl_tok = reinterpret_cast<int32_t *>(p);
+        int32_t *req_tok = kvl_tok + T;
+        p += up256(2 * (size_t)T * sizeof(int32_t));
+        float *rec = reinterpret_cast<float *>(p);
+        if (!reuse_list) {
+            build_tiles_kernel<<<1, 1024, 0, stream>>>(
+                cu_q, seg_req, pos, R, QPR, max_kv_len, tmp, list, cnt, status,
+                T, sitems, kvl_tok, req_tok);
+            BI_LAUNCH_CHECK("prefill split list launch");
+        }
+        attn_rows_kernel<true>
+            <<<bi_sm_count(), tca::ROW_THREADS, tca::RowL::ALLOC, stream>>>(
+                km, vm, qm, list, cnt, page_table, max_pages, n_pages, Hq, Hkv,
+                G, scale, reinterpret_cast<uint16_t *>(out), status, sitems,
+                rec, Cmax);
+        BI_LAUNCH_CHECK("prefill split attention launch");
+        const int warps = T * Hq;
+        decode_merge_kernel<128><<<(warps * 32 + 255) / 256, 256, 0, stream>>>(
+            rec, kvl_tok, req_tok, T, Hq, Cmax,
+            reinterpret_cast<uint16_t *>(out));
+    } else if (D == 128 && ws && R <= MAX_SEGS &&
                ws_bytes >= bi_prefill_attn_ws_bytes(T, R, Hq, Hkv)) {
         const int QPR = 128 / G;   // tokens per 128-row tile
         static std::once_flag f;
         static bi_status fs;
         std::call_once(f, [] {
-            fs = set_attr(attn_rows_kernel, tca::RowL::ALLOC);
+            fs = set_attr(attn_rows_kernel<false>, tca::RowL::ALLOC);
         });
         if (fs != BI_OK) return fs;
         const uint64_t pool_rows = (uint64_t)n_pages * Hkv * 16;
@@ -3145,17 +3287,19 @@ bi_status bi_prefill_attn_pool(const bi_bf16 *q, const int32_t *cu_q,
         int4 *tmp = static_cast<int4 *>(ws);
         int4 *list = tmp + tiles128;
         int32_t *cnt = reinterpret_cast<int32_t *>(list + tiles128);
-        build_tiles_kernel<<<1, 1024, 0, stream>>>(cu_q, seg_req, pos, R, QPR,
-                                                   max_kv_len, tmp, list, cnt,
-                                                   status);
-        BI_LAUNCH_CHECK("prefill row-tile list launch");
+        if (!reuse_list) {
+            build_tiles_kernel<<<1, 1024, 0, stream>>>(cu_q, seg_req, pos, R,
+                                                       QPR, max_kv_len, tmp,
+                                                       list, cnt, status);
+            BI_LAUNCH_CHECK("prefill row-tile list launch");
+        }
         const int grid =
             (int)std::min<int64_t>((int64_t)tiles128 * Hkv, bi_sm_count());
-        attn_rows_kernel<<<grid, tca::ROW_THREADS, tca::RowL::ALLOC,
-                           stream>>>(km, vm, qm, list, cnt, page_table,
-                                     max_pages, n_pages, Hq, Hkv, G, scale,
-                                     reinterpret_cast<uint16_t *>(out),
-                                     status);
+        attn_rows_kernel<false><<<grid, tca::ROW_THREADS, tca::RowL::ALLOC,
+                                  stream>>>(
+            km, vm, qm, list, cnt, page_table, max_pages, n_pages, Hq, Hkv, G,
+            scale, reinterpret_cast<uint16_t *>(out), status, nullptr, nullptr,
+            0);
     } else if (D == 128) {
         static std::once_flag f;
         static bi_status fs;
@@ -3201,12 +3345,19 @@ extern "C" bi_status bi_prefill_attn(
     return bi_prefill_attn_pool(q, cu_q, seg_req, R, T, pos, max_q, max_kv_len,
                                 k_pool, v_pool, page_table, max_pages,
                                 Hkv > 0 ? unbounded_pages(Hkv) : 1, Hq, Hkv, D,
-                                scale, out, nullptr, 0, bi_stream(stream));
+                                scale, out, nullptr, 0, bi_stream(stream),
+                                false);
 }
 
 extern "C" size_t bi_prefill_attn_workspace_size(int T, int R, int Hq,
                                                  int Hkv) {
     return bi_prefill_attn_ws_bytes(T, R, Hq, Hkv);
+}
+
+extern "C" size_t bi_prefill_attn_split_workspace_size(int T, int R, int Hq,
+                                                       int Hkv,
+                                                       int max_kv_len) {
+    return bi_prefill_attn_split_ws_bytes(T, R, Hq, Hkv, max_kv_len);
 }
 
 extern "C" bi_status bi_prefill_attn_ws(
@@ -3219,5 +3370,6 @@ extern "C" bi_status bi_prefill_attn_ws(
     return bi_prefill_attn_pool(q, cu_q, seg_req, R, T, pos, max_q, max_kv_len,
                                 k_pool, v_pool, page_table, max_pages,
                                 Hkv > 0 ? unbounded_pages(Hkv) : 1, Hq, Hkv, D,
-                                scale, out, ws, ws_bytes, bi_stream(stream));
+                                scale, out, ws, ws_bytes, bi_stream(stream),
+                                false);
 }

@@ -50,11 +50,17 @@ bi_status bi_prefill_attn_pool(const bi_bf16 *q, const int32_t *cu_q,
                                const int32_t *page_table, int max_pages,
                                int n_pages, int Hq, int Hkv, int D,
                                float scale, bi_bf16 *out, void *ws,
-                               size_t ws_bytes, cudaStream_t stream);
+                               size_t ws_bytes, cudaStream_t stream,
+                               bool reuse_list = false);
+// reuse_list: ws already holds the tile list (and the split form's items)
+// an earlier call with the same segments, positions and shapes built — the
+// layers of one forward; the list depends on nothing else.
 
 // Workspace with which bi_prefill_attn_pool runs the persistent tensor-core
 // path (head_dim 128; without it, one CTA per query tile): its tile lists.
 size_t bi_prefill_attn_ws_bytes(int T, int R, int Hq, int Hkv);
+size_t bi_prefill_attn_split_ws_bytes(int T, int R, int Hq, int Hkv,
+                                      int max_kv_len);
 
 // RoPE in two parts for the model driver: the (cos, sin) table of the rows'
 // positions ([T][D/2] float2), computed once per forward, and the rotation

@@ -110,8 +110,13 @@ Layout layout(const bi_model_cfg &c, int max_pages_total) {
     // shapes with more than one K slice)
     L.gemm_ws = take(std::max(bi_gemm_workspace_size(T, 2 * F, H),
                               bi_gemm_workspace_size(T, c.vocab, H)));
-    L.att_ws = take(bi_decode_attn_workspace_size(T, c.n_heads, c.head_dim,
-                                                  c.max_kv_len));
+    // decode records of T rows, or the split form of a verify-sized batch
+    // (its segments: the taken windows, a pad segment, empty ones)
+    L.att_ws = take(std::max(
+        bi_decode_attn_workspace_size(T, c.n_heads, c.head_dim, c.max_kv_len),
+        bi_prefill_attn_split_ws_bytes(std::min(T, BI_VERIFY_ROWS),
+                                       BI_VERIFY_ROWS + 1, c.n_heads,
+                                       c.n_kv_heads, c.max_kv_len)));
     L.kvlen = take((size_t)T * 4);
     L.rope = take((size_t)T * (c.head_dim / 2) * 8);
     L.vbuf = take((size_t)(VerifyIdx::COUNT + max_pages_total) * 4);
@@ -519,7 +524,8 @@ extern "C" bi_status bi_model_forward(bi_model *m, int T, const int32_t *tokens,
                                           max_kv_len, m->kpool[l],
                                           m->vpool[l], page_table, c.max_pages,
                                           c.n_pages, Hq, Hkv, D, scale, attn,
-                                          att_ws, att_ws_bytes, s));
+                                          att_ws, att_ws_bytes, s,
+                                          /* list of layer 0 */ l > 0));
         }
         BI_TIMED(BI_PROF_GEMM_O,
                  gemm_slices(attn, T, QD, m->wo[l], H, o, &s_o, s));

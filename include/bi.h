@@ -273,6 +273,17 @@ bi_status bi_prefill_attn(const bi_bf16 *q, const int32_t *cu_q,
  * the query-tile lists of T rows in R segments (0 if the shape has none). */
 size_t bi_prefill_attn_workspace_size(int T, int R, int Hq, int Hkv);
 
+/* Workspace bytes with which bi_prefill_attn_ws (head_dim 128, T <= 512:
+ * verify-sized batches, LLM-42 section 4.3) spreads every query tile's
+ * chunks over the SMs: one work item per (128-row tile, 256-position chunk,
+ * KV head) writes the chunk's record (m, l, o) of the decode path's
+ * two-stage form, and the decode merge folds the records in chunk order,
+ * so the bits are those of decode.  Covers the tile list, the items, every
+ * row's context and request and the records [T][Hq][ceil(max_kv_len/256)].
+ * 0 when the form does not apply. */
+size_t bi_prefill_attn_split_workspace_size(int T, int R, int Hq, int Hkv,
+                                            int max_kv_len);
+
 /* bi_prefill_attn with a workspace (device, caller-owned, no initial
  * contents).  For head_dim 128, T <= 512 rows (verify-sized batches),
  * R <= 4096 and ws_bytes >= bi_prefill_attn_workspace_size: one persistent

@@ -169,9 +169,10 @@ def decode(bi, q, kv, rows, kv_len):
     return out
 
 
-def prefill(bi, q, kv, segs, ws=False, scale=None):
+def prefill(bi, q, kv, segs, ws=False, scale=None, split=False):
     """segs: list of (request, first position, n rows); q rows in order.
-    ws: run bi_prefill_attn_ws with a workspace (the persistent path)."""
+    ws: run bi_prefill_attn_ws with a workspace (the persistent path);
+    split: with the workspace of the split form (verify-sized batches)."""
     cu, sr, pos = [0], [], []
     for r, p0, n in segs:
         cu.append(cu[-1] + n)
@@ -187,6 +188,10 @@ def prefill(bi, q, kv, segs, ws=False, scale=None):
         T, Hq = q.shape[0], q.shape[1]
         nb = bi.bi_prefill_attn_workspace_size(T, len(segs), Hq,
                                                kv.kp.shape[1])
+        if split:
+            nb = bi.bi_prefill_attn_split_workspace_size(
+                T, len(segs), Hq, kv.kp.shape[1], max(pos) + 1)
+            assert nb > 0
         w = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda")
         bi.bi_prefill_attn_ws(*args, w)
     else:
@@ -383,6 +388,42 @@ def test_prefill_row_tiles_other_groupings(bi, Hq, Hkv, scale):
     assert np.array_equal(bits(rows_), bits(one))
     b = bits(rows_)
     assert not (((b & 0x7f80) == 0x7f80) & ((b & 0x7f) != 0)).any()
+
+
+def test_prefill_split_form_bitwise(bi, orc):
+    """A verify-sized batch (windows of 64, 32 and 16 tokens at contexts
+    spanning one to nine 256-position chunks, a pad segment) with the
+    workspace of the split form — one work item per (128-row tile, chunk,
+    KV head), the chunk records merged in order by the decode merge — gives
+    the bits of the in-kernel form, of one CTA per 16-row tile and of each
+    row's decode, over NaN-filled stale pages; sampled rows agree with the
+    oracle."""
+    Hq, Hkv, D = 32, 8, 128
+    lens = [2200, 300, 64, 900, 1500]
+    kv = PagedKV(lens, Hkv, D, seed=71)
+    segs = [(0, 2136, 64), (1, 268, 32), (2, 48, 16), (3, 836, 64),
+            (4, 1468, 32), (-1, 0, 16)]
+    T = sum(n for _, _, n in segs)
+    q = randn_bf16((T, Hq, D), 72)
+    spl, pos = prefill(bi, q, kv, segs, ws=True, split=True)
+    sync_ok(bi)
+    real = T - 16
+    assert not bits(spl)[real:].any()
+    ink, _ = prefill(bi, q, kv, segs, ws=True)
+    sync_ok(bi)
+    assert np.array_equal(bits(spl), bits(ink))
+    one, _ = prefill(bi, q[:real].contiguous(), kv, segs[:-1])
+    sync_ok(bi)
+    assert np.array_equal(bits(spl)[:real], bits(one))
+    rows = sum([[r] * n for r, _, n in segs[:-1]], [])
+    dec = decode(bi, q[:real].contiguous(), kv, rows,
+                 [p + 1 for p in pos[:real]])
+    sync_ok(bi)
+    assert np.array_equal(bits(dec), bits(spl)[:real])
+    pick = [0, 63, 64, 95, 96, 111, 112, 175, real - 1]
+    ref = attn_ref(orc, q[pick].contiguous(), kv, [rows[i] for i in pick],
+                   [pos[i] for i in pick])
+    check_close(bits(spl)[pick], ref, orc)
 
 
 # -------------------------------------------------------------- argmax --
