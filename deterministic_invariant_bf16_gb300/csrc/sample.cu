@@ -14,7 +14,9 @@
 // CDF over p_i = exp((logit_i - max) / temperature) with fixed-order blocked
 // prefix sums: thread k sums its contiguous slice in index order, the
 // slice totals are scanned by a fixed shuffle pattern, so the result depends
-// on nothing but the row.
+// on nothing but the row.  p_i is taken as 2^((logit_i - max) * c) with
+// c = rn(log2(e) / temperature) and the PTX base-2 exponential (relative
+// error about 2^-22, well inside the rounding of the running sums).
 //
 // philox_sample_top: the same draw restricted to the top_k highest-ranked
 // tokens (larger logit first, ties to the lower index) and, within them, the
@@ -186,13 +188,30 @@ __device__ __forceinline__ float block_exclusive_scan(float v, float *total) {
     return lane == 0 ? before_warp : __fadd_rn(before_warp, prev);
 }
 
-__global__ void __launch_bounds__(SEL_THREADS)
+// One p of the sampling distribution: 2^((x - mx) * c), c = log2(e) / tau
+// rounded once.  x == mx gives exactly 1 (also when c overflows for a
+// subnormal tau); x = -inf gives 0.  ex2.approx.f32 without .ftz keeps
+// subnormal results, as the definition's exp does.
+__device__ __forceinline__ float sample_p(float x, float mx, float c) {
+    const float d = __fsub_rn(x, mx);
+    const float y = d == 0.f ? 0.f : __fmul_rn(d, c);
+    float r;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(r) : "f"(y));
+    return r;
+}
+
+// Two blocks per SM (32 registers a thread), so that a batch of up to
+// 2 x 152 rows is one wave.
+__global__ void __launch_bounds__(SEL_THREADS, 2)
     sample_kernel(const float *__restrict__ logits, int V,
                   const uint64_t *__restrict__ request_id,
                   const uint64_t *__restrict__ step, float tau,
                   int32_t *__restrict__ ids) {
     const int t = blockIdx.x;
     const float *row = logits + (int64_t)t * V;
+    // The request's uniform, drawn by one thread before the row is read.
+    __shared__ float s_u;
+    if (threadIdx.x == 0) s_u = sample_uniform(request_id[t], step[t]);
     // 1. maximum (exact and order-free; NaN ignored), several loads in
     // flight per thread
     float mx = -INFINITY;
@@ -231,12 +250,13 @@ __global__ void __launch_bounds__(SEL_THREADS)
     // lane -> (slice 4 i + lane / 8, column lane % 8) so that each load
     // covers four 32-byte runs, and each lane then sums its own slice's 8
     // values from shared memory in index order.
+    const float l2t = __fdiv_rn(1.4426950408889634f, tau);  // log2(e) / tau
     const int per = (V + SEL_THREADS - 1) / SEL_THREADS;
     const int lo = min(V, threadIdx.x * per), hi = min(V, lo + per);
     __shared__ float cols[SEL_THREADS / 32][32][9];
     float(*cw)[9] = cols[threadIdx.x >> 5];
     const int lane = threadIdx.x & 31;
-    const int64_t wbase = (int64_t)(threadIdx.x & ~31) * per;
+    const int wbase = (threadIdx.x & ~31) * per;
     float part = 0.f;
     // the next column block is loaded into registers while the current
     // one is summed
@@ -244,7 +264,7 @@ __global__ void __launch_bounds__(SEL_THREADS)
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int r = 4 * i + (lane >> 3), c = lane & 7;
-        const int64_t e = wbase + (int64_t)r * per + c;
+        const int e = wbase + r * per + c;
         nxt[i] = c < per && e < V ? __ldg(row + e) : 0.f;
     }
     for (int c0 = 0; c0 < per; c0 += 8) {
@@ -255,13 +275,12 @@ __global__ void __launch_bounds__(SEL_THREADS)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int r = 4 * i + (lane >> 3);
-            const int64_t e = wbase + (int64_t)r * per + c;
+            const int e = wbase + r * per + c;
             nxt[i] = c < per && e < V ? __ldg(row + e) : 0.f;
         }
         const int n = min(8, hi - lo - c0);
         for (int j = 0; j < n; ++j)
-            part = __fadd_rn(part,
-                             expf(__fdiv_rn(__fsub_rn(cw[lane][j], mx), tau)));
+            part = __fadd_rn(part, sample_p(cw[lane][j], mx, l2t));
         __syncwarp();
     }
     float total;
@@ -273,17 +292,26 @@ __global__ void __launch_bounds__(SEL_THREADS)
     // grows by at most 1 + u) and sum p <= part / (1 - u)^(n - 1); both
     // factors are below f = 1 + 2 (n + 1) u while n u < 1/2, so with the
     // bound in double the skip never changes the result of the full scan.
-    const float target = __fmul_rn(sample_uniform(request_id[t], step[t]), total);
+    const float target = __fmul_rn(s_u, total);
     int first = 0x7fffffff;
     const double f = 1.0 + 2.0 * (double)(hi - lo + 1) * 0x1p-24;
     const double bound = ((double)prefix + (double)part * f) * f;
+    // The slice is read 8 values at a time, all loads in flight before the
+    // running sums use them.
     if (bound > (double)target) {
+        constexpr int CH = 8;
         float cdf = prefix;
-        for (int k = lo; k < hi; ++k) {
-            cdf = __fadd_rn(cdf, expf(__fdiv_rn(__fsub_rn(row[k], mx), tau)));
-            if (cdf > target) {
-                first = k;
-                break;
+        for (int k0 = lo; k0 < hi && first == 0x7fffffff; k0 += CH) {
+            float x[CH];
+#pragma unroll
+            for (int i = 0; i < CH; ++i)
+                x[i] = k0 + i < hi ? __ldg(row + k0 + i) : 0.f;
+#pragma unroll
+            for (int i = 0; i < CH; ++i) {
+                if (k0 + i < hi && first == 0x7fffffff) {
+                    cdf = __fadd_rn(cdf, sample_p(x[i], mx, l2t));
+                    if (cdf > target) first = k0 + i;
+                }
             }
         }
     }
@@ -304,7 +332,7 @@ __global__ void __launch_bounds__(SEL_THREADS)
     // p > 0.
     int lp = -1;
     for (int k = hi - 1; k >= lo; --k)
-        if (expf(__fdiv_rn(__fsub_rn(row[k], mx), tau)) > 0.f) {
+        if (sample_p(row[k], mx, l2t) > 0.f) {
             lp = k;
             break;
         }
@@ -636,7 +664,9 @@ extern "C" bi_status philox_sample(const float *logits, int T, int V,
                                    const uint64_t *request_id,
                                    const uint64_t *step, float temperature,
                                    int32_t *ids, void *stream) {
-    BI_REQUIRE(T >= 0 && V > 0, "philox_sample: T=%d V=%d", T, V);
+    // (V < 2^30 keeps the kernel's in-row element offsets in 32 bits)
+    BI_REQUIRE(T >= 0 && V > 0 && V < (1 << 30), "philox_sample: T=%d V=%d",
+               T, V);
     BI_REQUIRE(temperature >= 0.f, "philox_sample: temperature < 0");
     if (T == 0) return BI_OK;
     BI_REQUIRE(logits && ids, "philox_sample: null pointer");
