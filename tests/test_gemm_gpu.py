@@ -121,6 +121,24 @@ def test_batch_invariance_8b_shapes(bi, orc, N, K):
     _check_rows(bi, orc, x, W, [1, 64, 128], [0, 5, 128, 255], n_cols=24)
 
 
+@pytest.mark.parametrize("M", [1, 70, 256, 300])
+def test_kernels_agree_across_plans(bi, M):
+    """An output depends on its rows of x and W, on K and on the K slices
+    only.  At K = 2048 with one slice, N = 8192 runs the 128-column plan of
+    single CTAs, N = 20480 the 192-column plan and N = 90112 the 128-column
+    CTA pairs (cta_group::2, M = 256 across two SMs); the columns they
+    share agree bit for bit."""
+    K = 2048
+    Ns = (8192, 20480, 90112)
+    assert [bi.bi_gemm_splits(n, K) for n in Ns] == [1, 1, 1]
+    assert [bi.bi_gemm_tile_n(n, K) for n in Ns] == [128, 192, 128]
+    W = randn_bf16((Ns[-1], K), 71)
+    x = randn_bf16((M, K), 72 + M)
+    outs = [f32bits(gemm(bi, x, W[:n].contiguous()))[:, :Ns[0]] for n in Ns]
+    assert np.array_equal(outs[0], outs[1])
+    assert np.array_equal(outs[0], outs[2])
+
+
 def test_rows_agree_at_prefill_size(bi):
     """M=2048 (eight m-tiles) against the same rows computed at M=64."""
     W = randn_bf16((4096, 4096), 31)
