@@ -116,6 +116,19 @@ __global__ void __launch_bounds__(ROPE_THREADS)
         __syncthreads();
     }
     if (head >= Hq + 2 * Hkv) return;
+    // The slice partials and the (cos, sin) pairs are read before the
+    // page lookup, so that their loads and the page-table load are in
+    // flight together.
+    const int64_t c0 = rowoff + (int64_t)head * D + i;
+    float x0[PAIRS], x1[PAIRS];
+    qkv_values<S, PAIRS>(qkv, TQ, c0, x0);
+    qkv_values<S, PAIRS>(qkv, TQ, c0 + half, x1);
+    float2 cs[PAIRS];
+    if (head < Hq + Hkv) {
+#pragma unroll
+        for (int k = 0; k < PAIRS; ++k)
+            cs[k] = table ? table[(int64_t)t * half + i + k] : cs_s[i + k];
+    }
     int64_t page = -1;
     if (req >= 0 && head >= Hq) {
         const int pi = p / 16;
@@ -131,17 +144,11 @@ __global__ void __launch_bounds__(ROPE_THREADS)
         }
     }
     const int slot = p & 15;
-    const int64_t c0 = rowoff + (int64_t)head * D + i;
-    float x0[PAIRS], x1[PAIRS];
-    qkv_values<S, PAIRS>(qkv, TQ, c0, x0);
-    qkv_values<S, PAIRS>(qkv, TQ, c0 + half, x1);
     if (head < Hq + Hkv) {
         float y0[PAIRS], y1[PAIRS];
 #pragma unroll
         for (int k = 0; k < PAIRS; ++k) {
-            const float2 cs = table ? table[(int64_t)t * half + i + k]
-                                    : cs_s[i + k];
-            const float c = cs.x, s = cs.y;
+            const float c = cs[k].x, s = cs[k].y;
             y0[k] = __fsub_rn(__fmul_rn(x0[k], c), __fmul_rn(x1[k], s));
             y1[k] = __fadd_rn(__fmul_rn(x1[k], c), __fmul_rn(x0[k], s));
         }
@@ -169,9 +176,11 @@ __global__ void __launch_bounds__(ROPE_THREADS)
 bi_status bi_rope_table(const int32_t *pos, int T, int D, double theta,
                         float2 *table, cudaStream_t s) {
     if (T == 0) return BI_OK;
+    // 64-thread blocks: the double-precision power, cosine and sine of a
+    // 256-row table then run on every SM instead of a quarter of them
     const int64_t n = (int64_t)T * (D / 2);
-    const int blocks = (int)((n + 255) / 256);
-    rope_table_kernel<<<blocks, 256, 0, s>>>(pos, T, D, theta, table);
+    const int blocks = (int)((n + 63) / 64);
+    rope_table_kernel<<<blocks, 64, 0, s>>>(pos, T, D, theta, table);
     BI_LAUNCH_CHECK("rope table launch");
     return BI_OK;
 }

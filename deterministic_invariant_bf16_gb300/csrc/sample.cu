@@ -4,7 +4,8 @@
 // the argmax of the logits.  The comparison here is a total order
 // (NaN above everything with the lower index winning among NaNs, then the
 // larger value, then the lower index; -0 == +0), so the result is unique
-// whatever order the block visits the elements in.
+// whatever order and split the elements are visited in: a row is split over
+// a cluster of eight CTAs, whose bests are combined by the first.
 //
 // philox_sample: ybb.press section 6 item 3, one counter-based generator per
 // request derived from (request_id, step): seed = request_id * 1000003 + step
@@ -76,48 +77,89 @@ __device__ __forceinline__ void block_best(float &v, int &i) {
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(SEL_THREADS)
+// Argmax of one row by a cluster of AM_CLUSTER CTAs: CTA r of the cluster
+// takes the r-th contiguous part of the row, and rank 0 combines the
+// parts' bests read from the other CTAs' shared memory.  `better` is a
+// strict total order, so the result is the same for any split.
+constexpr int AM_CLUSTER = 8;
+constexpr int AM_THREADS = 256;
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(const void *p,
+                                                   uint32_t rank) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];"
+                 : "=r"(v)
+                 : "r"(mapa_rank(p, rank))
+                 : "memory");
+    return v;
+}
+
+__global__ void __cluster_dims__(AM_CLUSTER, 1, 1)
+    __launch_bounds__(AM_THREADS)
     argmax_kernel(const float *__restrict__ logits, int V,
                   int32_t *__restrict__ ids) {
-    const float *row = logits + (int64_t)blockIdx.x * V;
+    const int t = blockIdx.x / AM_CLUSTER;
+    const uint32_t part = cluster_rank();
+    const float *row = logits + (int64_t)t * V;
     float bv = -INFINITY;
     int bi = 0x7fffffff;
     if ((V & 3) == 0) {
-        // UNROLL float4 loads in flight per thread: a row is read by one
-        // block, so its time is the loads' latency unless they overlap.
+        // UNROLL float4 loads in flight per thread over this CTA's part
         constexpr int UNROLL = 4;
         const float4 *r4 = reinterpret_cast<const float4 *>(row);
         const int n4 = V / 4;
-        for (int k0 = threadIdx.x; k0 < n4; k0 += UNROLL * SEL_THREADS) {
+        const int per = (n4 + AM_CLUSTER - 1) / AM_CLUSTER;
+        const int lo = min(n4, (int)part * per), hi = min(n4, lo + per);
+        for (int k0 = lo + threadIdx.x; k0 < hi; k0 += UNROLL * AM_THREADS) {
             float4 x[UNROLL];
 #pragma unroll
             for (int u = 0; u < UNROLL; ++u) {
-                const int k = k0 + u * SEL_THREADS;
-                x[u] = k < n4 ? __ldg(r4 + k)
+                const int k = k0 + u * AM_THREADS;
+                x[u] = k < hi ? __ldg(r4 + k)
                               : make_float4(-INFINITY, -INFINITY, -INFINITY,
                                             -INFINITY);
             }
 #pragma unroll
             for (int u = 0; u < UNROLL; ++u) {
-                const int k = k0 + u * SEL_THREADS;
+                const int k = k0 + u * AM_THREADS;
                 const float xs[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                    if (k < n4 && better(xs[e], 4 * k + e, bv, bi)) {
+                    if (k < hi && better(xs[e], 4 * k + e, bv, bi)) {
                         bv = xs[e];
                         bi = 4 * k + e;
                     }
             }
         }
     } else {
-        for (int k = threadIdx.x; k < V; k += SEL_THREADS)
+        const int per = (V + AM_CLUSTER - 1) / AM_CLUSTER;
+        const int lo = min(V, (int)part * per), hi = min(V, lo + per);
+        for (int k = lo + threadIdx.x; k < hi; k += AM_THREADS)
             if (better(row[k], k, bv, bi)) {
                 bv = row[k];
                 bi = k;
             }
     }
     block_best(bv, bi);
-    if (threadIdx.x == 0) ids[blockIdx.x] = bi;
+    __shared__ float s_v;
+    __shared__ int s_i;
+    if (threadIdx.x == 0) {
+        s_v = bv;
+        s_i = bi;
+    }
+    cluster_sync_all();  // every part's best is in its CTA's shared memory
+    if (part == 0 && threadIdx.x == 0) {
+        for (uint32_t r = 1; r < AM_CLUSTER; ++r) {
+            const float v = __uint_as_float(ld_cluster_u32(&s_v, r));
+            const int i = (int)ld_cluster_u32(&s_i, r);
+            if (better(v, i, bv, bi)) {
+                bv = v;
+                bi = i;
+            }
+        }
+        ids[t] = bi;
+    }
+    cluster_sync_all();  // rank 0 has read the others before they exit
 }
 
 // ---------------------------------------------------------------- Philox --
@@ -630,7 +672,8 @@ extern "C" bi_status bi_argmax_logits(const float *logits, int T, int V,
     if (T == 0) return BI_OK;
     BI_REQUIRE(logits && ids, "bi_argmax_logits: null pointer");
     BI_REQUIRE(bi_aligned16(logits), "bi_argmax_logits: logits alignment");
-    argmax_kernel<<<T, SEL_THREADS, 0, bi_stream(stream)>>>(logits, V, ids);
+    argmax_kernel<<<T * AM_CLUSTER, AM_THREADS, 0, bi_stream(stream)>>>(
+        logits, V, ids);
     BI_LAUNCH_CHECK("argmax launch");
     return BI_OK;
 }
