@@ -26,26 +26,42 @@
 namespace {
 
 // Per-kernel-class event timing (bi_model_profile).  Events come from a pool
-// that grows on first use and is reused by later measurement windows.
+// that grows on first use and is reused by later measurement windows.  On
+// a stream that is being captured the events become event-record nodes of
+// the graph (cudaEventRecordExternal), so a replay of that graph times
+// every launch without host launch latency inside the brackets; the pool
+// does not grow during a capture (such launches go untimed).
 struct Profiler {
     bool on = false;
     std::vector<cudaEvent_t> ev;
     size_t next = 0;
     std::vector<std::pair<int, size_t>> marks;  // (class, start index)
 
+    static bool capturing(cudaStream_t s) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        return cudaStreamIsCapturing(s, &cs) == cudaSuccess &&
+               cs == cudaStreamCaptureStatusActive;
+    }
+    static void record(cudaEvent_t e, cudaStream_t s) {
+        if (capturing(s))
+            cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+        else
+            cudaEventRecord(e, s);
+    }
     int begin(cudaStream_t s) {
         if (!on) return -1;
         while (ev.size() < next + 2) {
+            if (capturing(s)) return -1;
             cudaEvent_t e;
             if (cudaEventCreate(&e) != cudaSuccess) return -1;
             ev.push_back(e);
         }
-        cudaEventRecord(ev[next], s);
+        record(ev[next], s);
         return (int)next;
     }
     void end(int cls, int start, cudaStream_t s) {
         if (start < 0) return;
-        cudaEventRecord(ev[start + 1], s);
+        record(ev[start + 1], s);
         marks.emplace_back(cls, (size_t)start);
         next = start + 2;
     }

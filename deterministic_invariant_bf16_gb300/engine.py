@@ -249,10 +249,11 @@ class Engine:
                             max_kv_len, self.page_table, logits, ids, stream)
         return logits
 
-    def capture(self, fn):
+    def capture(self, fn, warm=True):
         """Record the library calls that `fn()` makes as one CUDA graph
         and return it (`torch.cuda.CUDAGraph`; `.replay()` issues them
-        again).  fn runs once first on a side stream, then once under
+        again).  fn runs once first on a side stream (unless warm is
+        False: everything fn touches already exists), then once under
         capture.  Every tensor fn passes must stay alive and be refilled in
         place between replays (tokens, positions, ids ...); fn must not
         read results on the host, so verify_commit_rollback, which does,
@@ -261,12 +262,13 @@ class Engine:
         the eager calls bit for bit."""
         dev = torch.device(self.device)
         torch.cuda.synchronize(dev)
-        side = torch.cuda.Stream(device=dev)
-        side.wait_stream(torch.cuda.current_stream(dev))
-        with torch.cuda.stream(side):
-            fn()
-        torch.cuda.current_stream(dev).wait_stream(side)
-        torch.cuda.synchronize(dev)
+        if warm:
+            side = torch.cuda.Stream(device=dev)
+            side.wait_stream(torch.cuda.current_stream(dev))
+            with torch.cuda.stream(side):
+                fn()
+            torch.cuda.current_stream(dev).wait_stream(side)
+            torch.cuda.synchronize(dev)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             fn()
