@@ -7,31 +7,37 @@
 // depends only on its query vector, its position and the logical KV prefix:
 //
 //   chunk c covers absolute positions [256c, 256c + 256).  For each chunk a
-//   partial (m, l, o) is computed FROM SCRATCH by chunk_phase1/chunk_phase2
-//   with NW compute warps (a compile-time constant per head dimension):
-//     s_j = (q . k_j) * scale   mma.sync m16n8k16, dims in ascending 16-steps
+//   partial (m, l, o) is computed FROM SCRATCH:
+//     s_j = (q . k_j) * scale   MMA over the head dims in ascending 16-steps
 //     s_j = -inf past the row's context
 //     m   = max_j s_j
-//     p_j = exp(s_j - m)
-//     l   = sum_j p_j           fixed order: per thread its values in key
-//                               order, quad xor-tree (1, 2), warps in order
-//     o   = sum_j bf16(p_j) v_j mma.sync, keys in ascending 16-steps
+//     p_j = exp(s_j - m)        head_dim 128: p_of, 2^(s c1 - m log2 e)
+//     l   = sum_j p_j           fixed order: each 32-key group by an xor
+//                               tree, the eight groups in order
+//     o   = sum_j bf16(p_j) v_j MMA over the keys in ascending 16-steps
 //   chunks are merged in ascending c by merge_scalars/merge_value:
 //     m' = max(m, m_c); a = exp(m - m'); b = exp(m_c - m')
 //     l  = l a + l_c b;  o = o a + o_c b;   out = bf16(o / l)
 //
-// Decode computes every (row, chunk, KV head) item in a persistent,
-// warp-specialised kernel: a producer warp looks up the pages and issues TMA
-// loads into a ring of shared-memory slots, the compute warps run the two
-// phases; a second kernel merges the stored partials.  Prefill loops over
-// the chunks of a 16-row query tile inside one CTA (cp.async loads) and
-// merges in registers.  Both run the same phase and merge functions with the
-// same warp and lane mapping on the same shared-memory tile layout, and every
+// Kernels.  Head_dim 128 runs on tcgen05 with TMA page boxes:
+//   attn_tc_kernel       decode, persistent over whole (row, KV head) items
+//                        (S^T = K Q^T and O^T = V^T P^T, N = 16 query rows),
+//                        chunks merged in registers;
+//   decode_tc_chunks_kernel  the same over (row, chunk) items for small
+//                        batches, writing fp32 records that
+//                        decode_merge_kernel merges in chunk order;
+//   attn_rows_kernel     prefill and verify, 128-row query tiles with one
+//                        thread per query row (S = Q K^T, O = P V, N = 256
+//                        keys / 128 dims); in-kernel over a tile's chunks, or
+//                        in split form, one item per (tile, chunk, KV head)
+//                        writing the same records for decode_merge_kernel;
+//   prefill_tc_kernel    prefill without a workspace, 16-row tiles.
+// Head_dim 32 runs the mma.sync forms (decode_chunks_kernel + merge,
+// prefill_kernel).  All forms share the phase and merge functions, every
 // floating-point operation outside the MMAs is an explicit round-to-nearest
-// intrinsic, so no contraction can differ.  A row sits in a 16-row MMA tile
-// (decode: the G query heads of one KV head; prefill: 16/G queries x G
-// heads); the tensor core treats rows independently, so the other rows of
-// the tile do not matter.
+// intrinsic, and the tensor core's per-element results do not depend on N
+// or on which operand holds the row, so a row's bits are the same in every
+// kernel and batch.
 //
 // Positions past a row's context never contribute: their scores are
 // replaced by -inf (a select, so stale or NaN keys cannot leak) and their
