@@ -455,6 +455,38 @@ def test_argmax_exact(bi, orc):
     assert np.array_equal(ids2.cpu().numpy(), orc.argmax(x2.cpu().numpy()))
 
 
+def test_argmax_short_rows_and_cross_part_ties(bi, orc):
+    """A row is split into eight contiguous parts, one per CTA of a
+    cluster: rows shorter than the cluster (some parts empty), lengths
+    around multiples of 4 and 8, ties and NaNs in different parts, and an
+    all -inf row all give the oracle's index."""
+    g = torch.Generator(device="cuda").manual_seed(53)
+    for V in (1, 2, 3, 4, 5, 7, 8, 9, 31, 32, 33, 4100):
+        x = torch.randn(12, V, generator=g, device="cuda")
+        x[1] = float("-inf")
+        if V >= 2:
+            x[2, [0, V - 1]] = 9.0                 # tie: first and last part
+            x[3, V - 1] = float("nan")             # a NaN beats any value
+            x[4, [V // 2, V - 1]] = float("nan")   # first NaN wins
+            x[5] = 1.0                             # all equal: index 0
+            x[6, V - 1] = float("inf")
+            x[7, 0] = -0.0
+            x[7, 1:] = 0.0                         # -0 == +0: index 0
+        ids = torch.empty(12, dtype=torch.int32, device="cuda")
+        bi.bi_argmax_logits(x, ids)
+        sync_ok(bi)
+        assert np.array_equal(ids.cpu().numpy(), orc.argmax(x.cpu().numpy())), V
+    x = torch.randn(3, 128256, generator=g, device="cuda")
+    x[0, [16031, 16032]] = 40.0      # tie across the first part boundary
+    x[1, [5000, 120000]] = float("nan")
+    x[2, [127000, 130]] = 40.0
+    ids = torch.empty(3, dtype=torch.int32, device="cuda")
+    bi.bi_argmax_logits(x, ids)
+    sync_ok(bi)
+    assert ids.cpu().tolist() == [16031, 5000, 130]
+    assert np.array_equal(ids.cpu().numpy(), orc.argmax(x.cpu().numpy()))
+
+
 # -------------------------------------------------------------- Philox --
 
 def _top_boundary_ok(x, rid, st, tau, k, top_p, a, b):
