@@ -302,16 +302,23 @@ bi_status bi_prefill_attn_ws(const bi_bf16 *q, const int32_t *cu_q,
 /* ------------------------------------------------------- token selection --
  * Greedy: ids[t] = first index of the maximum of logits[t] (fp32 [T][V]).
  * NaN counts as maximal and the first NaN wins; -0 equals +0.  Exact, so the
- * result is unique (ybb.press section 1: a tiny perturbation flips argmax). */
+ * result is unique (ybb.press section 1: a tiny perturbation flips argmax);
+ * a row is searched by a cluster of eight CTAs, whose bests are combined in
+ * this total order.  logits 16-byte aligned. */
 bi_status bi_argmax_logits(const float *logits, int T, int V, int32_t *ids,
                            void *stream);
 
 /* Temperature sampling with a counter-based generator per request (ybb.press
  * section 6, item 3): seed = (request_id * 1000003 + step) mod 2^64,
  * u = (Philox4x64-10(counter 0, key (seed, 0)) word 0 >> 40) * 2^-24,
- * p_i = exp((logits_i - max) / temperature), token = first i whose running
- * sum exceeds u * sum(p) (fixed-order blocked prefix sums).  temperature 0
- * means greedy.  request_id, step: device uint64 [T]. */
+ * p_i = exp((logits_i - max) / temperature), evaluated as
+ * 2^((logits_i - max) * rn(log2(e) / temperature)) with the base-2
+ * exponential (relative error about 2^-22), token = first i whose running
+ * sum exceeds u * sum(p) (fixed-order blocked prefix sums over 1024
+ * contiguous slices of the row; when rounding leaves none, the last i with
+ * p_i > 0).  temperature 0 means greedy, temperature < 0 is refused, and
+ * V must be below 2^30.  request_id, step: device uint64 [T].  The result
+ * is a function of the row, request_id and step only. */
 bi_status philox_sample(const float *logits, int T, int V,
                         const uint64_t *request_id, const uint64_t *step,
                         float temperature, int32_t *ids, void *stream);
@@ -400,7 +407,11 @@ bi_status bi_model_forward(bi_model *m, int T, const int32_t *tokens,
 /* Per-kernel-class timing of bi_model_forward for roofline accounting:
  * while enabled, every launch of a class is bracketed by CUDA events recorded
  * on the forward's stream (events are created by the library on first use
- * and reused; no device memory is allocated).  bi_model_profile(m, 1) opens
+ * and reused; no device memory is allocated).  On a stream being captured
+ * the events are recorded as event-record nodes of the graph
+ * (cudaEventRecordExternal), so replays of that graph time each launch;
+ * the pool does not grow during a capture, so run the forward once with
+ * profiling enabled before capturing.  bi_model_profile(m, 1) opens
  * a new measurement window, bi_model_profile(m, 0) stops recording.
  * bi_model_profile_read waits for the recorded events and writes, per class,
  * the summed device milliseconds and the launch count into host arrays of

@@ -68,6 +68,15 @@ def test_bad_arguments_fail_before_launch(bi):
         ctypes.c_void_p(16), 4, ctypes.c_void_p(16), ctypes.c_void_p(16),
         1, 16, 4, 4, 64, 0.1, ctypes.c_void_p(16), ctypes.c_void_p(16),
         1 << 20, None) == 2
+    # sampling: a row of 2^30 logits, a negative temperature, top_k > 1024
+    f = ctypes.c_void_p(16)
+    assert lib.philox_sample(f, 1, 1 << 30, f, f, ctypes.c_float(1.0), f,
+                             None) == 1
+    assert lib.philox_sample(f, 1, 64, f, f, ctypes.c_float(-1.0), f,
+                             None) == 1
+    assert b"temperature" in lib.bi_last_error()
+    assert lib.philox_sample_top(f, 1, 64, f, f, ctypes.c_float(1.0), 1025,
+                                 ctypes.c_float(0.9), f, None) == 2
     # verify needs a model
     assert lib.verify_commit_rollback(None, 1, *([None] * 5), None, None,
                                       None, None, None, 0, None, None, None,
