@@ -75,6 +75,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<const uint32_t *>(&v);
 }
 
+// Drop the 128-byte L2 line at p (128-byte aligned) without writing it
+// back; later reads of it return undefined data until it is written again.
+// For scratch that has had its last read.
+__device__ __forceinline__ void discard_l2_line(const void *p) {
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // --------------------------------------------------------------- mbarrier --
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

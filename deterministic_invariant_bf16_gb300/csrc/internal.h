@@ -65,7 +65,9 @@ size_t bi_prefill_attn_split_ws_bytes(int T, int R, int Hq, int Hkv,
 // RoPE in two parts for the model driver: the (cos, sin) table of the rows'
 // positions ([T][D/2] float2), computed once per forward, and the rotation
 // + KV append reading it (table == nullptr computes the same values
-// in-kernel).
+// in-kernel).  discard_partials: the qkv slice partials are scratch read
+// here for the last time, so their L2 lines are dropped without a write-back
+// (their contents are undefined afterwards).
 bi_status bi_rope_table(const int32_t *pos, int T, int D, double theta,
                         float2 *table, cudaStream_t s);
 bi_status bi_rope_apply(const float *qkv, int S, const float2 *table,
@@ -73,4 +75,10 @@ bi_status bi_rope_apply(const float *qkv, int S, const float2 *table,
                         int Hq, int Hkv, int D, double theta,
                         bi_bf16 *q_out, bi_bf16 *k_pool, bi_bf16 *v_pool,
                         const int32_t *page_table, int max_pages, int n_pages,
-                        cudaStream_t st);
+                        cudaStream_t st, bool discard_partials = false);
+
+// bi_rmsnorm on a stream, with the same option for its slice partials.
+bi_status bi_rmsnorm_apply(const float *partials, int S, const bi_bf16 *x,
+                           bi_bf16 *residual, const bi_bf16 *w, int T, int H,
+                           float eps, bi_bf16 *y, bool discard_partials,
+                           cudaStream_t s);

@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(NORM_THREADS)
     rmsnorm_fast_kernel(const float *__restrict__ partials,
                         const uint16_t *__restrict__ x, uint16_t *residual,
                         const uint16_t *__restrict__ w, int T, int H, float eps,
-                        uint16_t *__restrict__ y) {
+                        uint16_t *__restrict__ y, int discard) {
     const int t = blockIdx.x;
     const int tid = threadIdx.x;
     const int nvec = H / 8;
@@ -241,6 +241,20 @@ __global__ void __launch_bounds__(NORM_THREADS)
         for (int j = 0; j < 8; ++j)
             ss = __fadd_rn(ss, __fmul_rn(v[k][j], v[k][j]));
     }
+    if (S > 0 && discard) {
+        // The partial planes have had their only read: drop their lines from
+        // L2 without writing them back.  A 128-byte line holds the 8-element
+        // slices of four consecutive threads of one warp, all read by now.
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < VEC; ++k) {
+            const int vi = tid + k * NORM_THREADS;
+            if (!act[k] || (vi & 3)) continue;
+#pragma unroll
+            for (int s = 0; s < SP; ++s)
+                discard_l2_line(partials + s * TH + row + (int64_t)vi * 8);
+        }
+    }
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1)
         ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, o));
@@ -267,10 +281,10 @@ __global__ void __launch_bounds__(NORM_THREADS)
     }
 }
 
-extern "C" bi_status bi_rmsnorm(const float *partials, int S,
-                                const bi_bf16 *x, bi_bf16 *residual,
-                                const bi_bf16 *w, int T, int H, float eps,
-                                bi_bf16 *y, void *stream) {
+bi_status bi_rmsnorm_apply(const float *partials, int S, const bi_bf16 *x,
+                           bi_bf16 *residual, const bi_bf16 *w, int T, int H,
+                           float eps, bi_bf16 *y, bool discard_partials,
+                           cudaStream_t s) {
     BI_REQUIRE(T >= 0 && H > 0 && H % 8 == 0 &&
                    H <= NORM_MAX_VEC * 8 * NORM_THREADS,
                "bi_rmsnorm: H=%d must be a positive multiple of 8, <= 16384",
@@ -285,7 +299,7 @@ extern "C" bi_status bi_rmsnorm(const float *partials, int S,
                    (!residual || bi_aligned16(residual)) && bi_aligned16(w) &&
                    bi_aligned16(y),
                "bi_rmsnorm: pointers must be 16-byte aligned");
-    cudaStream_t s = bi_stream(stream);
+    const int dis = discard_partials ? 1 : 0;
     // up to two 8-element slices per thread (H <= 4096): all loads first
     const int vec = (H / 8 + NORM_THREADS - 1) / NORM_THREADS;
     switch (partials ? S : 0) {
@@ -293,10 +307,10 @@ extern "C" bi_status bi_rmsnorm(const float *partials, int S,
     case n:                                                                  \
         if (vec == 1)                                                        \
             rmsnorm_fast_kernel<n, 1><<<T, NORM_THREADS, 0, s>>>(            \
-                partials, x, residual, w, T, H, eps, y);                     \
+                partials, x, residual, w, T, H, eps, y, dis);                \
         else if (vec == 2)                                                   \
             rmsnorm_fast_kernel<n, 2><<<T, NORM_THREADS, 0, s>>>(            \
-                partials, x, residual, w, T, H, eps, y);                     \
+                partials, x, residual, w, T, H, eps, y, dis);                \
         else                                                                 \
             rmsnorm_kernel<n><<<T, NORM_THREADS, 0, s>>>(partials, x,        \
                                                          residual, w, T, H,  \
@@ -309,6 +323,14 @@ extern "C" bi_status bi_rmsnorm(const float *partials, int S,
     }
     BI_LAUNCH_CHECK("rmsnorm launch");
     return BI_OK;
+}
+
+extern "C" bi_status bi_rmsnorm(const float *partials, int S,
+                                const bi_bf16 *x, bi_bf16 *residual,
+                                const bi_bf16 *w, int T, int H, float eps,
+                                bi_bf16 *y, void *stream) {
+    return bi_rmsnorm_apply(partials, S, x, residual, w, T, H, eps, y, false,
+                            bi_stream(stream));
 }
 
 extern "C" bi_status bi_embed(const int32_t *tokens, int T, const bi_bf16 *E,

@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(ROPE_THREADS)
                 int D, double theta, uint16_t *__restrict__ q_out,
                 uint16_t *__restrict__ k_pool, uint16_t *__restrict__ v_pool,
                 const int32_t *__restrict__ page_table, int max_pages,
-                int n_pages, int32_t *status) {
+                int n_pages, int32_t *status, int discard) {
     __shared__ float2 cs_s[64];
     const int t = blockIdx.x;
     const int half = D / 2;
@@ -123,6 +123,19 @@ __global__ void __launch_bounds__(ROPE_THREADS)
     float x0[PAIRS], x1[PAIRS];
     qkv_values<S, PAIRS>(qkv, TQ, c0, x0);
     qkv_values<S, PAIRS>(qkv, TQ, c0 + half, x1);
+    if (PAIRS == 4 && discard) {
+        // The slice partials have had their only read: drop their lines from
+        // L2 without writing them back.  A 128-byte line holds the pairs of
+        // eight consecutive threads of one warp (i = 0 .. 28 or 32 .. 60).
+        __syncwarp(__activemask());
+        if ((i & 31) == 0) {
+#pragma unroll
+            for (int s = 0; s < S; ++s) {
+                discard_l2_line(qkv + s * TQ + c0);
+                discard_l2_line(qkv + s * TQ + c0 + half);
+            }
+        }
+    }
     float2 cs[PAIRS];
     if (head < Hq + Hkv) {
 #pragma unroll
@@ -190,7 +203,7 @@ bi_status bi_rope_apply(const float *qkv, int S, const float2 *table,
                         int Hq, int Hkv, int D, double theta,
                         bi_bf16 *q_out, bi_bf16 *k_pool, bi_bf16 *v_pool,
                         const int32_t *page_table, int max_pages, int n_pages,
-                        cudaStream_t st) {
+                        cudaStream_t st, bool discard_partials) {
     BI_REQUIRE(T >= 0 && S >= 1 && S <= 8 && Hq > 0 && Hkv > 0 &&
                    Hq % Hkv == 0,
                "bi_rope: bad shape T=%d S=%d Hq=%d Hkv=%d", T, S, Hq, Hkv);
@@ -209,17 +222,19 @@ bi_status bi_rope_apply(const float *qkv, int S, const float2 *table,
     const int tph = vec ? D / 8 : D / 2;
     const int hpb = ROPE_THREADS / tph;
     dim3 grid(T, (Hq + 2 * Hkv + hpb - 1) / hpb);
+    // the discard needs whole 128-byte lines per head: D = 128, 16-byte loads
+    const int dis = discard_partials && vec && D == 128 ? 1 : 0;
     switch (S) {
 #define BI_ROPE_CASE(n)                                                       \
     case n:                                                                   \
         if (vec)                                                              \
             rope_kernel<n, 4><<<grid, ROPE_THREADS, 0, st>>>(                 \
                 qkv, table, pos, row_req, T, Hq, Hkv, D, theta, q_out,        \
-                k_pool, v_pool, page_table, max_pages, n_pages, status);      \
+                k_pool, v_pool, page_table, max_pages, n_pages, status, dis); \
         else                                                                  \
             rope_kernel<n, 1><<<grid, ROPE_THREADS, 0, st>>>(                 \
                 qkv, table, pos, row_req, T, Hq, Hkv, D, theta, q_out,        \
-                k_pool, v_pool, page_table, max_pages, n_pages, status);      \
+                k_pool, v_pool, page_table, max_pages, n_pages, status, 0);   \
         break;
         BI_ROPE_CASE(1) BI_ROPE_CASE(2) BI_ROPE_CASE(3) BI_ROPE_CASE(4)
         BI_ROPE_CASE(5) BI_ROPE_CASE(6) BI_ROPE_CASE(7) BI_ROPE_CASE(8)
@@ -237,5 +252,5 @@ extern "C" bi_status bi_rope(const float *qkv, int S, const int32_t *pos,
                              int n_pages, void *stream) {
     return bi_rope_apply(qkv, S, nullptr, pos, row_req, T, Hq, Hkv, D, theta,
                          q_out, k_pool, v_pool, page_table, max_pages, n_pages,
-                         bi_stream(stream));
+                         bi_stream(stream), false);
 }
