@@ -67,7 +67,9 @@ size_t bi_prefill_attn_split_ws_bytes(int T, int R, int Hq, int Hkv,
 // + KV append reading it (table == nullptr computes the same values
 // in-kernel).  discard_partials: the qkv slice partials are scratch read
 // here for the last time, so their L2 lines are dropped without a write-back
-// (their contents are undefined afterwards).
+// (their contents are undefined afterwards); dead / dead_bytes: another
+// scratch region (128-byte aligned) whose contents are dead by the time
+// this runs, dropped the same way.
 bi_status bi_rope_table(const int32_t *pos, int T, int D, double theta,
                         float2 *table, cudaStream_t s);
 bi_status bi_rope_apply(const float *qkv, int S, const float2 *table,
@@ -75,10 +77,14 @@ bi_status bi_rope_apply(const float *qkv, int S, const float2 *table,
                         int Hq, int Hkv, int D, double theta,
                         bi_bf16 *q_out, bi_bf16 *k_pool, bi_bf16 *v_pool,
                         const int32_t *page_table, int max_pages, int n_pages,
-                        cudaStream_t st, bool discard_partials = false);
+                        cudaStream_t st, bool discard_partials = false,
+                        const void *dead = nullptr, size_t dead_bytes = 0);
 
-// bi_rmsnorm on a stream, with the same option for its slice partials.
+// bi_rmsnorm on a stream, with the same options for its slice partials and
+// up to two dead scratch regions (H <= 4096; other widths drop nothing).
 bi_status bi_rmsnorm_apply(const float *partials, int S, const bi_bf16 *x,
                            bi_bf16 *residual, const bi_bf16 *w, int T, int H,
                            float eps, bi_bf16 *y, bool discard_partials,
-                           cudaStream_t s);
+                           cudaStream_t s, const void *dead0 = nullptr,
+                           size_t dead0_bytes = 0, const void *dead1 = nullptr,
+                           size_t dead1_bytes = 0);

@@ -507,16 +507,19 @@ extern "C" bi_status bi_model_forward(bi_model *m, int T, const int32_t *tokens,
                      bi_rmsnorm(nullptr, 0, nullptr, h, m->attn_norm[l], T, H,
                                 c.eps, x, s));
         else
+            // (the previous layer's SwiGLU output has had its last read)
             BI_TIMED(BI_PROF_NORM,
                      bi_rmsnorm_apply(d, s_d, nullptr, h, m->attn_norm[l], T,
-                                      H, c.eps, x, true, s));
+                                      H, c.eps, x, true, s, f,
+                                      (size_t)T * F * 2));
         int s_qkv = 0, s_o = 0;
         BI_TIMED(BI_PROF_GEMM_QKV,
                  gemm_slices(x, T, H, m->wqkv[l], QKV, qkv, &s_qkv, s));
         BI_TIMED(BI_PROF_ROPE,
                  bi_rope_apply(qkv, s_qkv, rope_tab, pos, row_req, T, Hq, Hkv,
                                D, c.theta, q, m->kpool[l], m->vpool[l],
-                               page_table, c.max_pages, c.n_pages, s, true));
+                               page_table, c.max_pages, c.n_pages, s, true,
+                               x, (size_t)T * H * 2));  // x: QKV's input
         if (R == 0) {
             BI_TIMED(BI_PROF_ATTN,
                      bi_decode_attn_pool(q, m->kpool[l], m->vpool[l],
@@ -545,9 +548,11 @@ extern "C" bi_status bi_model_forward(bi_model *m, int T, const int32_t *tokens,
         }
         BI_TIMED(BI_PROF_GEMM_O,
                  gemm_slices(attn, T, QD, m->wo[l], H, o, &s_o, s));
+        // (the queries and the attention output have had their last reads)
         BI_TIMED(BI_PROF_NORM,
                  bi_rmsnorm_apply(o, s_o, nullptr, h, m->ffn_norm[l], T, H,
-                                  c.eps, x, true, s));
+                                  c.eps, x, true, s, attn,
+                                  (size_t)T * QD * 2, q, (size_t)T * QD * 2));
         BI_TIMED(BI_PROF_GEMM_GATE_UP,
                  bi_gemm(x, T, H, m->wgu[l], 2 * F, f, BI_OUT_SWIGLU,
                          gemm_ws, gemm_ws_bytes, s));
@@ -556,7 +561,7 @@ extern "C" bi_status bi_model_forward(bi_model *m, int T, const int32_t *tokens,
     }
     BI_TIMED(BI_PROF_NORM,
              bi_rmsnorm_apply(d, s_d, nullptr, h, m->final_norm, T, H, c.eps,
-                              x, true, s));
+                              x, true, s, f, (size_t)T * F * 2));
     BI_TIMED(BI_PROF_LM_HEAD,
              bi_gemm(x, T, H, m->lm_head, c.vocab, logits, BI_OUT_F32,
                      gemm_ws, gemm_ws_bytes, s));

@@ -157,7 +157,10 @@ __global__ void __launch_bounds__(NORM_THREADS)
     rmsnorm_fast_kernel(const float *__restrict__ partials,
                         const uint16_t *__restrict__ x, uint16_t *residual,
                         const uint16_t *__restrict__ w, int T, int H, float eps,
-                        uint16_t *__restrict__ y, int discard) {
+                        uint16_t *__restrict__ y, int discard,
+                        DeadRegion dead0, DeadRegion dead1) {
+    discard_region(dead0);
+    discard_region(dead1);
     const int t = blockIdx.x;
     const int tid = threadIdx.x;
     const int nvec = H / 8;
@@ -284,7 +287,9 @@ __global__ void __launch_bounds__(NORM_THREADS)
 bi_status bi_rmsnorm_apply(const float *partials, int S, const bi_bf16 *x,
                            bi_bf16 *residual, const bi_bf16 *w, int T, int H,
                            float eps, bi_bf16 *y, bool discard_partials,
-                           cudaStream_t s) {
+                           cudaStream_t s, const void *dead0,
+                           size_t dead0_bytes, const void *dead1,
+                           size_t dead1_bytes) {
     BI_REQUIRE(T >= 0 && H > 0 && H % 8 == 0 &&
                    H <= NORM_MAX_VEC * 8 * NORM_THREADS,
                "bi_rmsnorm: H=%d must be a positive multiple of 8, <= 16384",
@@ -300,6 +305,7 @@ bi_status bi_rmsnorm_apply(const float *partials, int S, const bi_bf16 *x,
                    bi_aligned16(y),
                "bi_rmsnorm: pointers must be 16-byte aligned");
     const int dis = discard_partials ? 1 : 0;
+    const DeadRegion d0{dead0, dead0_bytes}, d1{dead1, dead1_bytes};
     // up to two 8-element slices per thread (H <= 4096): all loads first
     const int vec = (H / 8 + NORM_THREADS - 1) / NORM_THREADS;
     switch (partials ? S : 0) {
@@ -307,10 +313,10 @@ bi_status bi_rmsnorm_apply(const float *partials, int S, const bi_bf16 *x,
     case n:                                                                  \
         if (vec == 1)                                                        \
             rmsnorm_fast_kernel<n, 1><<<T, NORM_THREADS, 0, s>>>(            \
-                partials, x, residual, w, T, H, eps, y, dis);                \
+                partials, x, residual, w, T, H, eps, y, dis, d0, d1);        \
         else if (vec == 2)                                                   \
             rmsnorm_fast_kernel<n, 2><<<T, NORM_THREADS, 0, s>>>(            \
-                partials, x, residual, w, T, H, eps, y, dis);                \
+                partials, x, residual, w, T, H, eps, y, dis, d0, d1);        \
         else                                                                 \
             rmsnorm_kernel<n><<<T, NORM_THREADS, 0, s>>>(partials, x,        \
                                                          residual, w, T, H,  \
@@ -330,7 +336,7 @@ extern "C" bi_status bi_rmsnorm(const float *partials, int S,
                                 const bi_bf16 *w, int T, int H, float eps,
                                 bi_bf16 *y, void *stream) {
     return bi_rmsnorm_apply(partials, S, x, residual, w, T, H, eps, y, false,
-                            bi_stream(stream));
+                            bi_stream(stream), nullptr, 0, nullptr, 0);
 }
 
 extern "C" bi_status bi_embed(const int32_t *tokens, int T, const bi_bf16 *E,

@@ -97,7 +97,8 @@ __global__ void __launch_bounds__(ROPE_THREADS)
                 int D, double theta, uint16_t *__restrict__ q_out,
                 uint16_t *__restrict__ k_pool, uint16_t *__restrict__ v_pool,
                 const int32_t *__restrict__ page_table, int max_pages,
-                int n_pages, int32_t *status, int discard) {
+                int n_pages, int32_t *status, int discard, DeadRegion dead) {
+    discard_region(dead);
     __shared__ float2 cs_s[64];
     const int t = blockIdx.x;
     const int half = D / 2;
@@ -203,7 +204,8 @@ bi_status bi_rope_apply(const float *qkv, int S, const float2 *table,
                         int Hq, int Hkv, int D, double theta,
                         bi_bf16 *q_out, bi_bf16 *k_pool, bi_bf16 *v_pool,
                         const int32_t *page_table, int max_pages, int n_pages,
-                        cudaStream_t st, bool discard_partials) {
+                        cudaStream_t st, bool discard_partials,
+                        const void *dead, size_t dead_bytes) {
     BI_REQUIRE(T >= 0 && S >= 1 && S <= 8 && Hq > 0 && Hkv > 0 &&
                    Hq % Hkv == 0,
                "bi_rope: bad shape T=%d S=%d Hq=%d Hkv=%d", T, S, Hq, Hkv);
@@ -224,17 +226,20 @@ bi_status bi_rope_apply(const float *qkv, int S, const float2 *table,
     dim3 grid(T, (Hq + 2 * Hkv + hpb - 1) / hpb);
     // the discard needs whole 128-byte lines per head: D = 128, 16-byte loads
     const int dis = discard_partials && vec && D == 128 ? 1 : 0;
+    const DeadRegion dr{dead, dead_bytes};
     switch (S) {
 #define BI_ROPE_CASE(n)                                                       \
     case n:                                                                   \
         if (vec)                                                              \
             rope_kernel<n, 4><<<grid, ROPE_THREADS, 0, st>>>(                 \
                 qkv, table, pos, row_req, T, Hq, Hkv, D, theta, q_out,        \
-                k_pool, v_pool, page_table, max_pages, n_pages, status, dis); \
+                k_pool, v_pool, page_table, max_pages, n_pages, status, dis,  \
+                dr);                                                          \
         else                                                                  \
             rope_kernel<n, 1><<<grid, ROPE_THREADS, 0, st>>>(                 \
                 qkv, table, pos, row_req, T, Hq, Hkv, D, theta, q_out,        \
-                k_pool, v_pool, page_table, max_pages, n_pages, status, 0);   \
+                k_pool, v_pool, page_table, max_pages, n_pages, status, 0,    \
+                dr);                                                          \
         break;
         BI_ROPE_CASE(1) BI_ROPE_CASE(2) BI_ROPE_CASE(3) BI_ROPE_CASE(4)
         BI_ROPE_CASE(5) BI_ROPE_CASE(6) BI_ROPE_CASE(7) BI_ROPE_CASE(8)
@@ -252,5 +257,5 @@ extern "C" bi_status bi_rope(const float *qkv, int S, const int32_t *pos,
                              int n_pages, void *stream) {
     return bi_rope_apply(qkv, S, nullptr, pos, row_req, T, Hq, Hkv, D, theta,
                          q_out, k_pool, v_pool, page_table, max_pages, n_pages,
-                         bi_stream(stream), false);
+                         bi_stream(stream), false, nullptr, 0);
 }
