@@ -180,6 +180,29 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *m,
         : "memory");
 }
 
+// L2 policy for data read once and streamed through: evict it first, so
+// that the small data read again soon (activations, partial planes) stays.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;"
+                 : "=l"(p));
+    return p;
+}
+
+// tma_load_2d with an L2 cache policy (l2_evict_first_policy).
+__device__ __forceinline__ void tma_load_2d_hint(void *dst,
+                                                 const CUtensorMap *m,
+                                                 int32_t x, int32_t y,
+                                                 uint64_t *bar,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx"
+        "::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(
+            smem_u32(dst)),
+        "l"(m), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
 // 3-D form of tma_load_2d (box coordinates x, y, z).
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *m,
                                             int32_t x, int32_t y, int32_t z,

@@ -257,6 +257,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ---------------------------------------------------- producer --
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        // With one m-tile every W tile is read once: evict it from L2
+        // first, so that x and the partial planes stay.
+        const uint64_t pol = l2_evict_first_policy();
         int it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
@@ -274,8 +277,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mbar_arrive_expect_tx(&full[st],
                                       p.abox * BK * 2 + T::B_BYTES);
                 tma_load_2d(sA + st * A_BYTES, &tmA, kb * BK, m0, &full[st]);
-                tma_load_2d(sB + st * T::B_BYTES, &tmB, kb * BK, nt * BN,
-                            &full[st]);
+                if (p.MT == 1)
+                    tma_load_2d_hint(sB + st * T::B_BYTES, &tmB, kb * BK,
+                                     nt * BN, &full[st], pol);
+                else
+                    tma_load_2d(sB + st * T::B_BYTES, &tmB, kb * BK, nt * BN,
+                                &full[st]);
             }
         }
         if (!ok) {
