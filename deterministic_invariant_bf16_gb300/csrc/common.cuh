@@ -379,6 +379,20 @@ __device__ __forceinline__ void tma_load_2d_pair(void *dst,
         : "memory");
 }
 
+// tma_load_2d_pair with an L2 cache policy (l2_evict_first_policy).
+__device__ __forceinline__ void tma_load_2d_pair_hint(void *dst,
+                                                      const CUtensorMap *m,
+                                                      int x, int y,
+                                                      uint32_t bar,
+                                                      uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::"
+        "complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(
+            smem_u32(dst)),
+        "l"(m), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // Tensor memory of both CTAs of the pair: one warp of each CTA calls these
 // with the same arguments; both receive the same address.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t *slot, uint32_t ncols) {

@@ -449,6 +449,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
         const uint32_t lead_full = mapa_rank(full, 0);
+        // with one m-tile every W tile is read once (see gemm_kernel)
+        const uint64_t pol = l2_evict_first_policy();
         int it = 0;
         bool ok = true;
         for (int u = cid; u < p.units && ok; u += ncl) {
@@ -469,11 +471,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
                 tma_load_2d_pair(sA + st * T::A_CTA, &tmA, kb * BK,
                                  m0 + (int)rank * HALF, bar);
 #pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    tma_load_2d_pair(sB + st * T::B_CTA + j * T::B_HALF, &tmB,
-                                     kb * BK,
-                                     np * 2 * BN + j * BN + (int)rank * (BN / 2),
-                                     bar);
+                for (int j = 0; j < 2; ++j) {
+                    const int wy = np * 2 * BN + j * BN + (int)rank * (BN / 2);
+                    if (p.MT == 1)
+                        tma_load_2d_pair_hint(sB + st * T::B_CTA + j * T::B_HALF,
+                                              &tmB, kb * BK, wy, bar, pol);
+                    else
+                        tma_load_2d_pair(sB + st * T::B_CTA + j * T::B_HALF,
+                                         &tmB, kb * BK, wy, bar);
+                }
             }
         }
         // The pair commits of the last stages have reached this CTA's
