@@ -82,21 +82,25 @@ __device__ __forceinline__ void discard_l2_line(const void *p) {
     asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
 }
 
-// A scratch region whose contents are dead: its whole 128-byte lines are
-// dropped from L2 by every thread of a grid, grid-stride.  p must be
-// 128-byte aligned; a tail shorter than a line is left alone.
+// A region whose contents are dead: the 128-byte lines lying wholly inside
+// it are dropped from L2 by every thread of a grid, grid-stride (a line the
+// region shares with other data is left alone).
 struct DeadRegion {
     const void *p;
     size_t bytes;
 };
 __device__ __forceinline__ void discard_region(DeadRegion r) {
     if (!r.p) return;
-    const size_t lines = r.bytes >> 7;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(r.p);
+    const uintptr_t lo = (a + 127) & ~uintptr_t(127);
+    const uintptr_t hi = (a + r.bytes) & ~uintptr_t(127);
+    if (hi <= lo) return;
+    const size_t lines = (hi - lo) >> 7;
     const size_t n = (size_t)gridDim.x * gridDim.y * blockDim.x;
     for (size_t i = ((size_t)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x +
                     threadIdx.x;
          i < lines; i += n)
-        discard_l2_line(static_cast<const char *>(r.p) + i * 128);
+        discard_l2_line(reinterpret_cast<const void *>(lo + i * 128));
 }
 
 // --------------------------------------------------------------- mbarrier --

@@ -304,7 +304,13 @@ bi_status bi_rmsnorm_apply(const float *partials, int S, const bi_bf16 *x,
                    (!residual || bi_aligned16(residual)) && bi_aligned16(w) &&
                    bi_aligned16(y),
                "bi_rmsnorm: pointers must be 16-byte aligned");
-    const int dis = discard_partials ? 1 : 0;
+    // the partials' lines are dropped only where each 128-byte line holds
+    // four slices of one row (rows of a multiple of 32 elements, planes on
+    // 128-byte boundaries)
+    const int dis = discard_partials && partials && H % 32 == 0 &&
+                            (reinterpret_cast<uintptr_t>(partials) & 127) == 0
+                        ? 1
+                        : 0;
     const DeadRegion d0{dead0, dead0_bytes}, d1{dead1, dead1_bytes};
     // up to two 8-element slices per thread (H <= 4096): all loads first
     const int vec = (H / 8 + NORM_THREADS - 1) / NORM_THREADS;

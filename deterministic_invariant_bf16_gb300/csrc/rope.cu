@@ -224,8 +224,12 @@ bi_status bi_rope_apply(const float *qkv, int S, const float2 *table,
     const int tph = vec ? D / 8 : D / 2;
     const int hpb = ROPE_THREADS / tph;
     dim3 grid(T, (Hq + 2 * Hkv + hpb - 1) / hpb);
-    // the discard needs whole 128-byte lines per head: D = 128, 16-byte loads
-    const int dis = discard_partials && vec && D == 128 ? 1 : 0;
+    // the discard needs whole 128-byte lines per head: D = 128, 16-byte
+    // loads, the planes on 128-byte boundaries
+    const int dis = discard_partials && vec && D == 128 &&
+                            (reinterpret_cast<uintptr_t>(qkv) & 127) == 0
+                        ? 1
+                        : 0;
     const DeadRegion dr{dead, dead_bytes};
     switch (S) {
 #define BI_ROPE_CASE(n)                                                       \
