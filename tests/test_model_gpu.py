@@ -199,6 +199,50 @@ def test_captured_decode_replays_bitwise(tiny, lib):
     assert lib.bi_device_status() == 0
 
 
+def test_profile_of_a_captured_forward(tiny, lib):
+    """bi_model_profile inside a stream capture: the brackets become
+    event-record nodes of the graph, so each replay times every bracketed
+    launch (one per layer and class), and the profiled graph still gives
+    the eager logits bit for bit."""
+    shape = tiny[0]
+    prompts = prompts8(shape)
+    slots = list(range(8))
+    eng = new_engine(tiny, page_seed=14)
+    for r in slots:
+        eng.reserve(r, 16 + 4)
+    eng.prefill([(r, prompts[r], 0) for r in slots])
+    dev = "cuda"
+    tok = torch.tensor([int(p[-1]) for p in prompts], dtype=torch.int32,
+                       device=dev)
+    pos = torch.full((8,), 16, dtype=torch.int32, device=dev)
+    rr = torch.tensor(slots, dtype=torch.int32, device=dev)
+    ids = torch.empty(8, dtype=torch.int32, device=dev)
+    lg = torch.empty(8, shape.vocab, dtype=torch.float32, device=dev)
+
+    def one():
+        eng.decode(tok, pos, rr, logits=lg, ids=ids, max_kv_len=20)
+
+    # an eager profiled forward grows the event pool the capture draws on
+    lib.bi_model_profile(eng.handle, True)
+    one()
+    torch.cuda.synchronize()
+    eager = lib.bi_model_profile_read(eng.handle)
+    ref = lg.clone()
+    lib.bi_model_profile(eng.handle, True)
+    g = eng.capture(one, warm=False)
+    for _ in range(2):
+        g.replay()
+        torch.cuda.synchronize()
+        prof = lib.bi_model_profile_read(eng.handle)
+        for name, (ms, n) in prof.items():
+            assert n == eager[name][1], name
+            assert n == 0 or ms > 0.0, name
+        assert prof["norm"][1] == shape.n_layers * 2 + 1
+        assert torch.equal(lg.view(torch.int32), ref.view(torch.int32))
+    lib.bi_model_profile(eng.handle, False)
+    assert lib.bi_device_status() == 0
+
+
 def test_prefix_sharing_bitwise(tiny, lib):
     """Prefix caching (Vosti abstract: KV tied to its logical token prefix,
     a paged prefix-sharing KV cache).  Request B's first 37 tokens equal
