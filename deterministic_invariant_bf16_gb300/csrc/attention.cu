@@ -1457,42 +1457,11 @@ __global__ void __launch_bounds__(tca::DEC_ROW_THREADS, 1)
     volatile int *progress = &s_progress;
     const int n_units = s_units;
 
-    if (warp == SW + 2) {
-        // ------------------------------------------------------ prefetch --
-        constexpr uint32_t PAGE_KV = 16 * D * 2;
-        Walk w{rows, total, Hkv};
-        if (w.begin()) {
-            int req = PRE ? w.req : row_req[w.b];
-            for (int n = 0;; ++n) {
-                bool go = true;
-                if (lane == 0 && *progress + 1 < n) {
-                    const uint64_t t0 = bi_globaltimer();
-                    while (*progress + 1 < n) {
-                        __nanosleep(256);
-                        if (bi_globaltimer() - t0 > BI_WAIT_LIMIT_NS) {
-                            go = false;
-                            break;
-                        }
-                    }
-                }
-                if (!__shfl_sync(0xffffffffu, go ? 1 : 0, 0)) break;
-                if (lane < ((w.vl() + 15) >> 4)) {
-                    const int pi = w.c * 16 + lane;
-                    const int pg = pi < max_pages
-                                       ? page_table[(int64_t)req * max_pages + pi]
-                                       : -1;
-                    if (pg >= 0 && pg < n_pages) {
-                        const int64_t off = ((int64_t)pg * Hkv + w.g) * 16 * D;
-                        prefetch_l2_bulk(k_pool + off, PAGE_KV);
-                        prefetch_l2_bulk(v_pool + off, PAGE_KV);
-                    }
-                }
-                if (!w.next()) break;
-                if (w.c == 0) req = PRE ? w.req : row_req[w.b];
-            }
-        }
-        return;
-    }
+    // Warp SW + 2 counted the CTA's units above and has no further role:
+    // the K and V pages are streamed with the L2 evict-first policy and not
+    // prefetched (an L2 prefetch of the next unit's pages made the
+    // evict-first reads slower, and without the policy it gained nothing).
+    if (warp == SW + 2) return;
 
     if (warp == SW + 1 || warp >= SW + 3) {
         // ----------------------------------------------------- producers --
@@ -1509,6 +1478,9 @@ __global__ void __launch_bounds__(tca::DEC_ROW_THREADS, 1)
         // of the pair.
         const int kv = warp == SW + 1 || warp == SW + 3 ? 0 : 1;
         const int hf = warp == SW + 1 || warp == SW + 4 ? 0 : 1;
+        // each page is read once per forward: evict it from L2 first, so
+        // that the next kernels' inputs stay
+        const uint64_t pol = l2_evict_first_policy();
         volatile int *kp[2] = {progress, (volatile int *)&s_kprog2};
         volatile int *vp[2] = {(volatile int *)&s_vprog[0],
                                (volatile int *)&s_vprog[1]};
@@ -1585,8 +1557,10 @@ __global__ void __launch_bounds__(tca::DEC_ROW_THREADS, 1)
                         const CUtensorMap *map = kv == 0 ? &kmap : &vmap;
 #pragma unroll
                         for (int h = 0; h < 2; ++h)
-                            tma_load_2d(tile + h * HALF_TILE + pl * PAGE_BYTES,
-                                        map, h * 64, row, &full[slot]);
+                            tma_load_2d_hint(tile + h * HALF_TILE +
+                                                 pl * PAGE_BYTES,
+                                             map, h * 64, row, &full[slot],
+                                             pol);
                     }
                     if (kv == 0 && hf == 0 && lane == 0) {
 #pragma unroll
@@ -1618,7 +1592,7 @@ __global__ void __launch_bounds__(tca::DEC_ROW_THREADS, 1)
                 }
             }
         }
-        // every load issued: release the prefetch warp and the other pair.
+        // every load issued: release the other pair.
         // After a failed wait the count stays where it is, so the other
         // pair's wait for it runs out too and nothing is issued into a slot
         // out of order.
