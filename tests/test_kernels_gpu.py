@@ -296,6 +296,51 @@ def test_decode_whole_rows_match_chunk_items(bi, orc):
     check_close(full[pick], ref, orc)
 
 
+def test_decode_long_contexts_both_forms(bi, orc):
+    """Contexts of the long-prompt stress (4100 to 8600 positions: 17 to 34
+    chunks merged in order).  A batch of 160 rows (whole-row items, chunks
+    merged in registers) holding four long rows among short ones, and each
+    long row alone (per-chunk items and the record merge kernel), give the
+    same bits; the long rows are within tolerance of the oracle."""
+    import types
+    long_lens = np.array([4100, 6000, 8192, 8600])
+    rng = np.random.default_rng(23)
+    short_lens = rng.integers(1, 64, 156)
+    A = PagedKV(long_lens, 8, 128, seed=29)
+    B = PagedKV(short_lens, 8, 128, seed=31)
+    long_rows = [3, 50, 101, 157]
+    R = 160
+    lens = np.empty(R, np.int64)
+    table = np.full((R, A.max_pages), -1, np.int32)
+    ta, tb = A.table.cpu().numpy(), B.table.cpu().numpy()
+    si = 0
+    for r in range(R):
+        if r in long_rows:
+            j = long_rows.index(r)
+            lens[r] = long_lens[j]
+            table[r] = ta[j]
+        else:
+            lens[r] = short_lens[si]
+            row = tb[si]
+            table[r, :row.shape[0]] = np.where(row >= 0, row + A.n_pages, -1)
+            si += 1
+    kv = types.SimpleNamespace(kp=torch.cat([A.kp, B.kp]),
+                               vp=torch.cat([A.vp, B.vp]),
+                               table=torch.from_numpy(table).cuda())
+    q = randn_bf16((R, 32, 128), 33)
+    full = bits(decode(bi, q, kv, list(range(R)), lens))
+    sync_ok(bi)
+    # 160 rows x 8 KV heads reach the whole-row form's 8 items per SM
+    assert R * 8 >= 8 * torch.cuda.get_device_properties(0).multi_processor_count
+    for r in long_rows:
+        one = decode(bi, q[r:r + 1].contiguous(), kv, [r], [int(lens[r])])
+        sync_ok(bi)
+        assert np.array_equal(bits(one)[0], full[r]), r
+    ql = q[torch.tensor(long_rows).cuda()].contiguous()
+    ref = attn_ref(orc, ql, A, [0, 1, 2, 3], long_lens - 1)
+    check_close(full[long_rows], ref, orc)
+
+
 @pytest.mark.parametrize("Hq,Hkv,D", [(32, 8, 128), (4, 4, 32)])
 def test_prefill_matches_decode_bitwise(bi, orc, Hq, Hkv, D):
     """Query-length invariance (Vosti): a position computed inside a window
