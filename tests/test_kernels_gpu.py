@@ -412,6 +412,27 @@ def test_prefill_group_path_bitwise(bi, orc):
     check_close(bits(grp)[pick], ref, orc)
 
 
+def test_prefill_long_prompt_piece(bi, orc):
+    """A 2048-row piece of a long prompt at positions 4096..6143 (the
+    long-prompt stress's pieces: up to 24 chunks per row) on the row
+    kernel equals decode of each row alone bit for bit on sampled rows, and
+    those rows are within tolerance of the oracle."""
+    Hq, Hkv, D = 32, 8, 128
+    kv = PagedKV([6144], Hkv, D, seed=57)
+    segs = [(0, 4096, 2048)]
+    q = randn_bf16((2048, Hq, D), 58)
+    grp, pos = prefill(bi, q, kv, segs, ws=True)
+    sync_ok(bi)
+    pick = [0, 1, 31, 32, 127, 128, 1000, 1023, 1024, 2046, 2047]
+    dec = decode(bi, q[pick].contiguous(), kv, [0] * len(pick),
+                 [pos[i] + 1 for i in pick])
+    sync_ok(bi)
+    assert np.array_equal(bits(dec), bits(grp)[pick])
+    ref = attn_ref(orc, q[pick].contiguous(), kv, [0] * len(pick),
+                   [pos[i] for i in pick])
+    check_close(bits(grp)[pick], ref, orc)
+
+
 @pytest.mark.parametrize("Hq,Hkv,scale", [(16, 2, None), (8, 8, None),
                                           (32, 2, None), (16, 8, None),
                                           (8, 2, -0.06)])
