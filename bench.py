@@ -1431,17 +1431,32 @@ def run_comparator(b, args):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / reps
 
+    def graphed(fn):
+        # Both sides replay CUDA graphs, so neither pays host launch
+        # overhead (the fast path issues one Python call per operation).
+        # cuBLAS picks its kernels at capture time, under the flag then set.
+        try:
+            return b.eng.capture(fn).replay, "cuda_graph"
+        except Exception:  # capture refused: time the eager calls instead
+            torch.cuda.synchronize()
+            return fn, "eager"
+
     reps = max(2, min(args.steps, 4))
-    ours_ms = timed(b.decode_iters, reps)
+    ours_fn, ours_launch = graphed(b.decode_iters)
+    ours_ms = timed(ours_fn, reps)
     out = {"what": "same decode iterations, GEMMs via torch.mm (cuBLAS), "
                    "gate/up as one GEMM, fp32 output %s" %
                    ("from cuBLAS" if fast.f32 else "by a cast"),
-           "invariant_decode_tok_s": B * it / (ours_ms / 1e3)}
+           "invariant_decode_tok_s": B * it / (ours_ms / 1e3),
+           "launch": {"invariant": ours_launch}}
     flag = torch.backends.cuda.matmul.allow_bf16_reduced_precision_reduction
     for name, val in (("cublas_default", flag), ("cublas_no_reduced_bf16", False)):
         torch.backends.cuda.matmul.allow_bf16_reduced_precision_reduction = val
-        cms = timed(run_cmp, reps)
+        cmp_fn, launch = graphed(run_cmp)
+        cms = timed(cmp_fn, reps)
         out[name + "_tok_s"] = B * it / (cms / 1e3)
+        out["launch"][name] = launch
+        del cmp_fn
     torch.backends.cuda.matmul.allow_bf16_reduced_precision_reduction = flag
     out["invariant_over_default"] = (out["invariant_decode_tok_s"] /
                                      out["cublas_default_tok_s"])
